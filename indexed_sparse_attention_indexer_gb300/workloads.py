@@ -1,0 +1,309 @@
+"""Seeded synthetic workloads for the indexed sparse attention layer.
+
+This module only draws random numbers and lays them out in the buffers the
+library reads.  None of the scoring, selection or attention arithmetic lives
+here: the CUDA path (through the binding) and the CPU oracle (in the tests and
+the bench's CPU leg) both take their inputs from these functions, and nothing
+else is shared between them.
+
+Value recipe (shapes and distributions of the five workloads the layer is
+measured on):
+
+* index queries ``q_idx`` and index keys ``k_idx``: integers drawn uniformly
+  from {-3..3}, stored in bf16 (keys may instead be FP8 E4M3, which holds these
+  integers exactly, with one positive power-of-two scale 2^e, e in {-4..0}, per
+  token).  Every dot product of two such vectors is an exact small integer, so
+  fp32 scores are exact in any summation order.
+* head weights ``w``: uniform [0,1) rounded down to a multiple of 2^-7, so that
+  every partial sum of ``w_h * relu(u_h)`` is a multiple of 2^-7 below 2^24
+  and hence exact in fp32 whatever the order.
+* latent cache rows (512 latent + 64 rope dims): bf16 N(0,1).
+* attention queries ``q``: bf16 N(0,1)/sqrt(576); softmax scale 1/sqrt(576).
+* varlen decode: lengths floor(exp(U(ln 1024, ln 131072))), 64-token pages,
+  physical page ids a random permutation.
+
+Draw order for one generator: q_idx, k_idx, (k_scale), w, q, latent, then the
+page permutation.  A varlen workload draws its lengths first, from the same
+generator, because they size every other buffer.  A chunked prefill draws the
+sequence's cache (k_idx, latent) from ``seed`` and each query chunk from its
+own stream ``seed + 1_000_003 * (chunk + 1)``.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence
+
+import torch
+
+D_LATENT = 512          # value / latent width of one cache row
+D_ROPE = 64             # rope part of one cache row
+D_QK = D_LATENT + D_ROPE  # key width of one cache row (576)
+
+WEIGHT_GRID = 128       # head weights are multiples of 1/WEIGHT_GRID
+
+
+@dataclass
+class Workload:
+    """One batch of inputs for the layer.
+
+    Cache layout: contiguous caches are ``[B, S_max, ...]`` (``block_table`` is
+    None); paged caches are pools ``[P, page_size, ...]`` addressed through
+    ``block_table[B, max_pages]`` (unused entries are -1).  Decode rows are one
+    query token per sequence (T == B) and row b sees positions
+    ``0 .. seq_lens[b]-1``.  Prefill is one sequence (B == 1); query token t
+    sits at position ``q_offset + t`` and sees positions ``0 .. q_offset+t``.
+    """
+
+    name: str
+    mode: str                      # "decode" or "prefill"
+    H_i: int
+    d: int
+    K: int
+    H: int
+    scale: float
+    q_idx: torch.Tensor            # [T, H_i, d] bf16
+    w: torch.Tensor                # [T, H_i] fp32
+    q: torch.Tensor                # [T, H, 576] bf16
+    k_idx: torch.Tensor            # [B, S_max, d] or [P, page, d]; bf16 / fp8 e4m3
+    k_scale: Optional[torch.Tensor]  # same leading shape as k_idx minus d, fp32, or None
+    latent: torch.Tensor           # [B, S_max, 576] or [P, page, 576] bf16
+    seq_lens: torch.Tensor         # [B] int32
+    block_table: Optional[torch.Tensor] = None  # [B, max_pages] int32
+    page_size: int = 0
+    q_offset: int = 0
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def T(self) -> int:
+        return int(self.q_idx.shape[0])
+
+    @property
+    def B(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def paged(self) -> bool:
+        return self.block_table is not None
+
+    @property
+    def s_max(self) -> int:
+        """Rows per sequence in a contiguous cache; max_pages*page for a paged one."""
+        if self.paged:
+            return int(self.block_table.shape[1]) * self.page_size
+        return int(self.k_idx.shape[1])
+
+    def to(self, device) -> "Workload":
+        def mv(x):
+            return None if x is None else x.to(device)
+        return Workload(self.name, self.mode, self.H_i, self.d, self.K, self.H, self.scale,
+                        mv(self.q_idx), mv(self.w), mv(self.q), mv(self.k_idx), mv(self.k_scale),
+                        mv(self.latent), mv(self.seq_lens), mv(self.block_table),
+                        self.page_size, self.q_offset, dict(self.meta))
+
+    def input_bytes(self) -> int:
+        n = 0
+        for x in (self.q_idx, self.w, self.q, self.k_idx, self.k_scale, self.latent,
+                  self.seq_lens, self.block_table):
+            if x is not None:
+                n += x.numel() * x.element_size()
+        return n
+
+
+# ----------------------------------------------------------------------------
+# elementary draws
+# ----------------------------------------------------------------------------
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+_CHUNK = 1 << 24  # elements per draw, to bound temporary fp32 memory
+
+
+def _int_values(shape, g, device, dtype=torch.bfloat16) -> torch.Tensor:
+    out = torch.empty(shape, dtype=dtype, device=device)
+    flat = out.view(-1) if dtype != torch.float8_e4m3fn else None
+    n = out.numel()
+    if dtype == torch.float8_e4m3fn:
+        tmp = torch.empty(n, dtype=torch.float8_e4m3fn, device=device)
+        for s in range(0, n, _CHUNK):
+            e = min(n, s + _CHUNK)
+            tmp[s:e] = torch.randint(-3, 4, (e - s,), generator=g, device=device).to(torch.float32).to(dtype)
+        return tmp.view(shape)
+    for s in range(0, n, _CHUNK):
+        e = min(n, s + _CHUNK)
+        flat[s:e] = torch.randint(-3, 4, (e - s,), generator=g, device=device).to(dtype)
+    return out
+
+
+def _normal_bf16(shape, g, device, std: float = 1.0) -> torch.Tensor:
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    flat = out.view(-1)
+    n = out.numel()
+    for s in range(0, n, _CHUNK):
+        e = min(n, s + _CHUNK)
+        x = torch.randn(e - s, generator=g, device=device, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        flat[s:e] = x.to(torch.bfloat16)
+    return out
+
+
+def _weights(shape, g, device) -> torch.Tensor:
+    u = torch.rand(shape, generator=g, device=device, dtype=torch.float32)
+    return torch.floor(u * WEIGHT_GRID) / WEIGHT_GRID
+
+
+def _pow2_scales(shape, g, device) -> torch.Tensor:
+    e = torch.randint(0, 5, shape, generator=g, device=device)
+    return torch.pow(torch.tensor(2.0, device=device), -e.to(torch.float32))
+
+
+def loguniform_lengths(B: int, lo: int, hi: int, g, device) -> torch.Tensor:
+    u = torch.rand(B, generator=g, device=device, dtype=torch.float64)
+    L = torch.floor(torch.exp(math.log(lo) + u * (math.log(hi) - math.log(lo))))
+    return L.clamp(lo, hi).to(torch.int32)
+
+
+# ----------------------------------------------------------------------------
+# workloads
+# ----------------------------------------------------------------------------
+
+def make_decode(B: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
+                device="cpu", lengths: Optional[Sequence[int]] = None,
+                loguniform: Optional[tuple] = None, page_size: int = 0,
+                k_fp8: bool = False, scale: Optional[float] = None,
+                q_std: Optional[float] = None, name: str = "decode") -> Workload:
+    """Decode batch: one query token per sequence.
+
+    ``S`` is the history length of every sequence unless ``lengths`` gives them
+    or ``loguniform=(lo, hi)`` draws them.  ``page_size > 0`` stores the caches
+    as page pools behind a randomly permuted block table.
+    """
+    g = _gen(seed, device)
+    if loguniform is not None:
+        L = loguniform_lengths(B, loguniform[0], loguniform[1], g, device).cpu()
+    elif lengths is not None:
+        L = torch.tensor(list(lengths), dtype=torch.int32)
+        assert L.numel() == B
+    else:
+        L = torch.full((B,), S, dtype=torch.int32)
+    if page_size > 0:
+        pages_per = [(int(l) + page_size - 1) // page_size for l in L]
+        n_pages = max(1, sum(pages_per))
+        rows_shape = (n_pages, page_size)
+    else:
+        s_max = max(1, int(L.max()) if L.numel() else 1)
+        rows_shape = (B, s_max)
+    kdt = torch.float8_e4m3fn if k_fp8 else torch.bfloat16
+    q_idx = _int_values((B, H_i, d), g, device)
+    k_idx = _int_values(rows_shape + (d,), g, device, kdt)
+    k_scale = _pow2_scales(rows_shape, g, device) if k_fp8 else None
+    w = _weights((B, H_i), g, device)
+    std = (1.0 / math.sqrt(D_QK)) if q_std is None else q_std
+    q = _normal_bf16((B, H, D_QK), g, device, std)
+    latent = _normal_bf16(rows_shape + (D_QK,), g, device)
+    block_table = None
+    if page_size > 0:
+        perm = torch.randperm(n_pages, generator=g, device=device).to(torch.int32).cpu()
+        max_pages = max(1, max(pages_per) if pages_per else 1)
+        block_table = torch.full((B, max_pages), -1, dtype=torch.int32)
+        c = 0
+        for b, npg in enumerate(pages_per):
+            block_table[b, :npg] = perm[c:c + npg]
+            c += npg
+        block_table = block_table.to(device)
+    return Workload(name=name, mode="decode", H_i=H_i, d=d, K=K, H=H,
+                    scale=(1.0 / math.sqrt(D_QK)) if scale is None else scale,
+                    q_idx=q_idx, w=w, q=q, k_idx=k_idx, k_scale=k_scale, latent=latent,
+                    seq_lens=L.to(device), block_table=block_table, page_size=page_size)
+
+
+def make_prefill(T: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
+                 device="cpu", q_offset: int = 0, scale: Optional[float] = None,
+                 q_std: Optional[float] = None, name: str = "prefill") -> Workload:
+    """Causal prefill of one sequence: query tokens q_offset .. q_offset+T-1
+    against a cache of S >= q_offset+T rows, all from one generator."""
+    assert S >= q_offset + T
+    g = _gen(seed, device)
+    q_idx = _int_values((T, H_i, d), g, device)
+    k_idx = _int_values((1, S, d), g, device)
+    w = _weights((T, H_i), g, device)
+    std = (1.0 / math.sqrt(D_QK)) if q_std is None else q_std
+    q = _normal_bf16((T, H, D_QK), g, device, std)
+    latent = _normal_bf16((1, S, D_QK), g, device)
+    return Workload(name=name, mode="prefill", H_i=H_i, d=d, K=K, H=H,
+                    scale=(1.0 / math.sqrt(D_QK)) if scale is None else scale,
+                    q_idx=q_idx, w=w, q=q, k_idx=k_idx, k_scale=None, latent=latent,
+                    seq_lens=torch.tensor([S], dtype=torch.int32, device=device),
+                    q_offset=q_offset)
+
+
+CHUNK_STREAM = 1_000_003
+
+
+def make_long_cache(S: int, d: int, seed: int = 0, device="cpu"):
+    """Cache of one long sequence for chunked prefill: (k_idx [1,S,d], latent [1,S,576])."""
+    g = _gen(seed, device)
+    k_idx = _int_values((1, S, d), g, device)
+    latent = _normal_bf16((1, S, D_QK), g, device)
+    return k_idx, latent
+
+
+def make_chunk(k_idx: torch.Tensor, latent: torch.Tensor, chunk: int, T: int,
+               H_i: int, K: int, H: int, seed: int = 0,
+               name: str = "chunked-prefill") -> Workload:
+    """Query chunk ``chunk`` (tokens chunk*T .. chunk*T+T-1) of a long sequence."""
+    device = k_idx.device
+    d = int(k_idx.shape[-1])
+    S = int(k_idx.shape[1])
+    g = _gen(seed + CHUNK_STREAM * (chunk + 1), device)
+    q_idx = _int_values((T, H_i, d), g, device)
+    w = _weights((T, H_i), g, device)
+    q = _normal_bf16((T, H, D_QK), g, device, 1.0 / math.sqrt(D_QK))
+    return Workload(name=name, mode="prefill", H_i=H_i, d=d, K=K, H=H,
+                    scale=1.0 / math.sqrt(D_QK), q_idx=q_idx, w=w, q=q,
+                    k_idx=k_idx, k_scale=None, latent=latent,
+                    seq_lens=torch.tensor([S], dtype=torch.int32, device=device),
+                    q_offset=chunk * T, meta={"chunk": chunk})
+
+
+# ----------------------------------------------------------------------------
+# the five measured workloads
+# ----------------------------------------------------------------------------
+
+CONFIGS = {
+    1: dict(name="decode-s2048-hi4x64-k128-h16", mode="decode", B=1, S=2048, H_i=4, d=64,
+            K=128, H=16, seed=0),
+    2: dict(name="decode-b64-s32768-hi64x128-k2048-h128", mode="decode", B=64, S=32768,
+            H_i=64, d=128, K=2048, H=128, seed=0),
+    3: dict(name="prefill-t8192-hi64x128-k2048-h128", mode="prefill", T=8192, S=8192,
+            H_i=64, d=128, K=2048, H=128, seed=0),
+    4: dict(name="chunked-prefill-s131072-c4096-hi64x128-k2048-h128", mode="chunked",
+            S=131072, T=4096, H_i=64, d=128, K=2048, H=128, seed=0),
+    5: dict(name="paged-decode-b128-loguniform-fp8keys-k2048-h128", mode="decode", B=128,
+            S=131072, lo=1024, hi=131072, H_i=64, d=128, K=2048, H=128, page_size=64,
+            seed=7),
+}
+
+
+def make_config(cfg: int, device="cpu", chunk: int = 0) -> Workload:
+    c = CONFIGS[cfg]
+    if cfg in (1, 2):
+        return make_decode(c["B"], c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
+                           device=device, name=c["name"])
+    if cfg == 3:
+        return make_prefill(c["T"], c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
+                            device=device, name=c["name"])
+    if cfg == 4:
+        k_idx, latent = make_long_cache(c["S"], c["d"], c["seed"], device)
+        return make_chunk(k_idx, latent, chunk, c["T"], c["H_i"], c["K"], c["H"], c["seed"],
+                          name=c["name"])
+    if cfg == 5:
+        return make_decode(c["B"], 0, c["H_i"], c["d"], c["K"], c["H"], c["seed"],
+                           device=device, loguniform=(c["lo"], c["hi"]),
+                           page_size=c["page_size"], k_fp8=True, name=c["name"])
+    raise ValueError(cfg)

@@ -1,0 +1,10 @@
+"""CPU oracle of the indexed sparse attention layer — test infrastructure only.
+
+Imported by the tests, ``__graft_entry__.smoke()`` and the bench's CPU-baseline
+leg; never by the library.
+"""
+from .dsi_oracle import (index_scores, topk_select, sparse_mla, dense_mla, history_rows,
+                         layer_row, decode_row, prefill_row, row_scores, layer)
+
+__all__ = ["index_scores", "topk_select", "sparse_mla", "dense_mla", "history_rows",
+           "layer_row", "decode_row", "prefill_row", "row_scores", "layer"]

@@ -1,0 +1,216 @@
+"""Oracle for the indexed sparse attention layer — TEST INFRASTRUCTURE ONLY.
+
+A plain, slow CPU restatement in fp64 of what the layer computes.  Only the
+tests, the package's ``smoke()`` check and the bench's CPU-baseline leg may
+import it; the library never does, and it shares no code, tables or helpers
+with the CUDA path (inputs come from the seeded generators in the package's
+``workloads`` module, which hold none of the arithmetic).
+
+Sources (page titles, sections):
+* "Day 0 Inference Support for New LLM Architectures: Optimization Practices"
+  — "Index-Based Sparse Attention": an indexer scores history positions,
+  applies head-weight weighting and keeps the Top-K; the attention core reads
+  the KV entries at those indices.  "Internal Fusion of the Indexer": the three
+  steps are scoring, weighted sum over heads, top-k, read from a paged K cache.
+* "Day 0 Inference Acceleration for New LLM Architectures..." §2–§3: relevance
+  scoring, head weight summation, Top-K selection; only the index sequence is
+  passed to the attention kernel, which reads the key-values at those indices.
+* "Day 0 Inference Adaptation and Performance Optimization for New Models" §1:
+  index selection sits on top of Multi-head Latent Attention (MLA).
+
+Readings where the pages are silent (each also listed in the design notes):
+* gate = ReLU; one index key per position shared by all indexer heads; the
+  head weights are per query token.
+* Top-K: the K largest scores, equal scores go to the lower position; rows
+  with at most K candidates keep all of them; the selected positions are
+  reported in ascending order, padded with -1.
+* FP8 index keys carry one scale per token; the oracle dequantises each
+  element (key * scale) before the dot product.
+* Attention core = absorbed MLA: the key of a position is its whole 576-wide
+  latent row (512 latent + 64 rope), the value is the first 512 dims; logits
+  are ``scale * q . c``, softmax over the selected positions, ``lse`` is the
+  natural-log log-sum-exp of the scaled logits.
+* Decode row b sees positions 0..seq_lens[b]-1 (the new token's key is already
+  in the cache); prefill token t at position q_offset+t sees 0..q_offset+t.
+
+Every function is pinned by the CPU tests to closed forms, brute force and
+textbook routines (exact rational arithmetic, a rank-count definition of the
+selection, torch's scaled_dot_product_attention in fp64).  The pages print no
+worked example, so nothing is pinned to values printed on the pages.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+D_V = 512
+
+
+def _f64(x) -> np.ndarray:
+    """Any array-like (numpy or a CPU torch tensor of any float type) -> fp64."""
+    if hasattr(x, "detach"):
+        x = x.detach().cpu()
+        if x.dtype.is_floating_point and x.dtype != __import__("torch").float64:
+            x = x.float()
+        x = x.numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------
+# step 1-2: indexer score (dot product per indexer head, ReLU gate, weighted
+# sum over heads)
+# ----------------------------------------------------------------------------
+
+def index_scores(q_idx, w, k_rows, k_scale=None) -> np.ndarray:
+    """Indexer score of each given history row for one query token.
+
+    q_idx [H_i, d], w [H_i], k_rows [n, d], k_scale [n] or None -> I [n] fp64:
+        I[s] = sum_h w[h] * max(0, sum_j q_idx[h, j] * k[s, j]),
+    with k = k_rows * k_scale[s] when the keys are quantised (dequantise first).
+    """
+    q = _f64(q_idx)
+    k = _f64(k_rows)
+    if k_scale is not None:
+        k = k * _f64(k_scale)[:, None]
+    u = k @ q.T                       # relevance of row s for indexer head h: [n, H_i]
+    gated = np.maximum(u, 0.0)        # ReLU gate
+    return gated @ _f64(w)            # head-weight weighted sum over heads
+
+
+# ----------------------------------------------------------------------------
+# step 3: Top-K selection
+# ----------------------------------------------------------------------------
+
+def topk_select(scores, K: int):
+    """Top-K positions of one score row.
+
+    Returns (idx [K] int64 ascending, -1 padded; count).  Ordering: larger score
+    first, equal scores by lower position; the first min(K, n) of that order
+    are kept.
+    """
+    I = _f64(scores)
+    n = I.shape[0]
+    pos = np.arange(n)
+    order = np.lexsort((pos, -I))     # primary: score descending, secondary: position
+    keep = np.sort(order[:min(K, n)])
+    out = np.full(K, -1, dtype=np.int64)
+    out[:keep.shape[0]] = keep
+    return out, int(keep.shape[0])
+
+
+# ----------------------------------------------------------------------------
+# steps 4-5: gather + attention over the selected latent rows
+# ----------------------------------------------------------------------------
+
+def sparse_mla(q, rows, scale: float, d_v: int = D_V):
+    """Multi-head attention of one query token over the given latent rows.
+
+    q [H, D], rows [n, D] -> (o [H, d_v], lse [H]):
+        l[h, s] = scale * q[h] . rows[s]      (keys: the whole row)
+        p = softmax_s(l),  o[h] = sum_s p[h, s] * rows[s, :d_v]  (values)
+        lse[h] = log sum_s exp(l[h, s]).
+    An empty row set gives o = 0 and lse = -inf.
+    """
+    qq = _f64(q)
+    c = _f64(rows)
+    H = qq.shape[0]
+    if c.shape[0] == 0:
+        return np.zeros((H, d_v)), np.full(H, -np.inf)
+    logits = scale * (qq @ c.T)                   # [H, n]
+    m = logits.max(axis=1, keepdims=True)
+    e = np.exp(logits - m)
+    z = e.sum(axis=1, keepdims=True)
+    o = (e @ c[:, :d_v]) / z
+    lse = m[:, 0] + np.log(z[:, 0])
+    return o, lse
+
+
+def dense_mla(q, rows, scale: float, d_v: int = D_V):
+    """Attention over every given row (the K >= history special case)."""
+    return sparse_mla(q, rows, scale, d_v)
+
+
+# ----------------------------------------------------------------------------
+# cache addressing (contiguous or paged through a block table)
+# ----------------------------------------------------------------------------
+
+def history_rows(cache, b: int, positions, block_table=None, page_size: int = 0):
+    """Rows of sequence b at the given logical positions.
+
+    Contiguous cache: cache[b, pos].  Paged cache (a pool [P, page, ...]):
+    cache[block_table[b, pos // page], pos % page].
+    """
+    pos = np.asarray(positions, dtype=np.int64)
+    if block_table is None:
+        return cache[b][pos] if len(pos) else cache[b][:0]
+    bt = block_table[b]
+    if hasattr(bt, "numpy"):
+        bt = bt.cpu().numpy()
+    pages = np.asarray(bt, dtype=np.int64)[pos // page_size]
+    slots = pos % page_size
+    return cache[pages, slots]
+
+
+# ----------------------------------------------------------------------------
+# one row of the whole layer
+# ----------------------------------------------------------------------------
+
+def layer_row(q_idx_t, w_t, q_t, k_hist, k_scale_hist, latent_of, n_hist: int, K: int,
+              scale: float):
+    """Indexer -> Top-K -> sparse MLA for one query token with n_hist visible rows.
+
+    ``k_hist`` [n_hist, d] (and ``k_scale_hist``) are the visible index keys;
+    ``latent_of(positions)`` returns the latent rows at those positions.
+    Returns a dict with scores (fp64 and fp32-rounded), idx, count, out, lse.
+    """
+    I = index_scores(q_idx_t, w_t, k_hist, k_scale_hist)
+    idx, count = topk_select(I, K)
+    rows = latent_of(idx[:count])
+    o, lse = sparse_mla(q_t, rows, scale)
+    return {"scores": I, "scores_fp32": I.astype(np.float32), "idx": idx, "count": count,
+            "out": o, "lse": lse}
+
+
+def decode_row(ws, b: int):
+    """Row b of a decode batch (attributes as laid out by the seeded generators)."""
+    L = int(ws.seq_lens[b])
+    pos = np.arange(L)
+    bt = ws.block_table.cpu() if ws.block_table is not None else None
+    k_hist = history_rows(ws.k_idx.cpu(), b, pos, bt, ws.page_size)
+    ks = None
+    if ws.k_scale is not None:
+        ks = history_rows(ws.k_scale.cpu(), b, pos, bt, ws.page_size)
+    lat = ws.latent.cpu()
+    return layer_row(ws.q_idx[b].cpu(), ws.w[b].cpu(), ws.q[b].cpu(), k_hist, ks,
+                     lambda p: history_rows(lat, b, p, bt, ws.page_size), L, ws.K, ws.scale)
+
+
+def prefill_row(ws, t: int):
+    """Query token t (position q_offset+t) of a causal prefill of one sequence."""
+    n = ws.q_offset + t + 1
+    k_hist = ws.k_idx[0, :n].cpu()
+    lat = ws.latent[0].cpu()
+    return layer_row(ws.q_idx[t].cpu(), ws.w[t].cpu(), ws.q[t].cpu(), k_hist, None,
+                     lambda p: lat[np.asarray(p, dtype=np.int64)] if len(p) else lat[:0],
+                     n, ws.K, ws.scale)
+
+
+def row_scores(ws, r: int) -> np.ndarray:
+    """Indexer scores only, for row r (decode sequence or prefill token)."""
+    if ws.mode == "decode":
+        L = int(ws.seq_lens[r])
+        pos = np.arange(L)
+        bt = ws.block_table.cpu() if ws.block_table is not None else None
+        k_hist = history_rows(ws.k_idx.cpu(), r, pos, bt, ws.page_size)
+        ks = None if ws.k_scale is None else history_rows(ws.k_scale.cpu(), r, pos, bt,
+                                                           ws.page_size)
+        return index_scores(ws.q_idx[r].cpu(), ws.w[r].cpu(), k_hist, ks)
+    n = ws.q_offset + r + 1
+    return index_scores(ws.q_idx[r].cpu(), ws.w[r].cpu(), ws.k_idx[0, :n].cpu(), None)
+
+
+def layer(ws, rows=None):
+    """The whole layer for the given rows (all rows by default)."""
+    R = ws.q_idx.shape[0]
+    rows = range(R) if rows is None else rows
+    f = decode_row if ws.mode == "decode" else prefill_row
+    return {r: f(ws, r) for r in rows}

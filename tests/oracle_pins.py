@@ -1,0 +1,350 @@
+"""Pins of the CPU oracle against what the mathematics fixes.
+
+Each ``check_*`` takes an oracle namespace (the real one, or a deliberately
+broken copy in the mutation tests) and raises AssertionError when the oracle
+disagrees with an independent statement of the same quantity: exact rational
+arithmetic, a rank-count definition of the selection, closed forms, textbook
+library routines, invariants.  None of them re-types the oracle's own formula.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ----------------------------------------------------------------------------
+# small deterministic inputs (numpy only; the oracle sees plain arrays here)
+# ----------------------------------------------------------------------------
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _int_mat(rng, shape, lo=-3, hi=3):
+    return rng.integers(lo, hi + 1, size=shape).astype(np.float64)
+
+
+def _grid_w(rng, n):
+    return np.floor(rng.random(n) * 128) / 128
+
+
+# ----------------------------------------------------------------------------
+# scores
+# ----------------------------------------------------------------------------
+
+def check_scores_bruteforce(o):
+    """Exact rational evaluation of the score definition on tiny inputs."""
+    for seed in range(6):
+        rng = _rng(seed)
+        Hi, d, n = 3, 5, 17
+        q = _int_mat(rng, (Hi, d)); k = _int_mat(rng, (n, d)); w = _grid_w(rng, Hi)
+        got = o.index_scores(q, w, k)
+        for s in range(n):
+            tot = Fraction(0)
+            for h in range(Hi):
+                dot = sum(Fraction(int(q[h, j])) * Fraction(int(k[s, j])) for j in range(d))
+                if dot > 0:
+                    tot += Fraction(w[h]) * dot
+            assert Fraction(got[s]) == tot, (seed, s, got[s], tot)
+
+
+def check_scores_one_hot(o):
+    """One-hot query/key per head: score = w_h * max(0, a*b) for the matching head only."""
+    Hi, d = 4, 6
+    for h, j, a, b in [(0, 0, 2, 3), (1, 5, -2, 3), (3, 2, -1, -3), (2, 4, 3, 0)]:
+        q = np.zeros((Hi, d)); q[h, j] = a
+        k = np.zeros((2, d)); k[0, j] = b; k[1, (j + 1) % d] = 1
+        w = np.array([0.25, 0.5, 0.75, 0.125])
+        got = o.index_scores(q, w, k)
+        assert got[0] == w[h] * max(0, a * b), (h, j, a, b, got)
+        assert got[1] == 0.0
+
+
+def check_scores_relu_gate(o):
+    """A head whose dot product is negative contributes nothing (gate), a positive one fully."""
+    k = np.array([[1.0, 2.0, -1.0]])
+    q = np.array([[-1.0, -2.0, 1.0], [1.0, 2.0, -1.0]])   # dots: -6 and +6
+    got = o.index_scores(q, np.array([0.5, 0.25]), k)
+    assert got[0] == 0.25 * 6.0, got
+
+
+def check_scores_zero_weight(o):
+    """Zeroing a head weight equals removing that head."""
+    rng = _rng(11)
+    Hi, d, n = 5, 8, 40
+    q = _int_mat(rng, (Hi, d)); k = _int_mat(rng, (n, d)); w = _grid_w(rng, Hi) + 1 / 128
+    for h in range(Hi):
+        w0 = w.copy(); w0[h] = 0.0
+        keep = [i for i in range(Hi) if i != h]
+        a = o.index_scores(q, w0, k)
+        b = o.index_scores(q[keep], w[keep], k)
+        assert np.array_equal(a, b), h
+        full = o.index_scores(q, w, k)
+        assert not np.array_equal(full, a) or np.all(q[h] @ k.T <= 0)
+
+
+def check_scores_head_permutation(o):
+    rng = _rng(12)
+    Hi, d, n = 6, 7, 30
+    q = _int_mat(rng, (Hi, d)); k = _int_mat(rng, (n, d)); w = _grid_w(rng, Hi)
+    perm = rng.permutation(Hi)
+    assert np.array_equal(o.index_scores(q, w, k), o.index_scores(q[perm], w[perm], k))
+
+
+def check_scores_fp8_scale(o):
+    """Doubling one token's key scale doubles that token's score only."""
+    rng = _rng(13)
+    Hi, d, n = 4, 8, 20
+    q = _int_mat(rng, (Hi, d)); k = _int_mat(rng, (n, d)); w = _grid_w(rng, Hi)
+    sc = 2.0 ** -rng.integers(0, 5, size=n)
+    base = o.index_scores(q, w, k, sc)
+    for s in (0, 7, n - 1):
+        sc2 = sc.copy(); sc2[s] *= 2
+        got = o.index_scores(q, w, k, sc2)
+        exp = base.copy(); exp[s] *= 2
+        assert np.array_equal(got, exp), s
+    # unit scales reduce to the unquantised score
+    assert np.array_equal(o.index_scores(q, w, k, np.ones(n)), o.index_scores(q, w, k))
+
+
+def _load_golden_indexer():
+    cases = []
+    path = os.path.join(GOLDEN, "indexer_tiny.txt")
+    cur = {}
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        key, val = line.split("=", 1)
+        key = key.strip()
+        if key == "case":
+            if cur:
+                cases.append(cur)
+            cur = {"name": val.strip()}
+            continue
+        cur[key] = val.strip()
+    if cur:
+        cases.append(cur)
+    out = []
+    for c in cases:
+        q = np.array([[float(x) for x in r.split()] for r in c["q_idx"].split(";")])
+        k = np.array([[float(x) for x in r.split()] for r in c["k"].split(";")])
+        w = np.array([float(Fraction(x)) for x in c["w"].split()])
+        sc = None
+        if "k_scale" in c:
+            sc = np.array([float(Fraction(x)) for x in c["k_scale"].split()])
+        scores = np.array([float(Fraction(x)) for x in c["scores"].split()])
+        topk = {}
+        for key, val in c.items():
+            if key.startswith("topk"):
+                K = int(key[4:])
+                topk[K] = [int(x) for x in val.split()]
+        out.append((c["name"], q, w, k, sc, scores, topk))
+    return out
+
+
+def check_scores_golden(o):
+    """Hand-worked tiny examples (tests/golden/indexer_tiny.txt)."""
+    for name, q, w, k, sc, scores, topk in _load_golden_indexer():
+        got = o.index_scores(q, w, k, sc)
+        assert np.array_equal(got, scores), (name, got, scores)
+        for K, exp in topk.items():
+            idx, cnt = o.topk_select(got, K)
+            assert list(idx) == exp, (name, K, list(idx), exp)
+
+
+# ----------------------------------------------------------------------------
+# Top-K
+# ----------------------------------------------------------------------------
+
+def _rank_count_select(I, K):
+    """Position p is kept iff fewer than K positions beat it, where q beats p when
+    I[q] > I[p], or I[q] == I[p] and q < p.  Pure-Python O(n^2)."""
+    n = len(I)
+    keep = []
+    for p in range(n):
+        better = 0
+        for q in range(n):
+            if I[q] > I[p] or (I[q] == I[p] and q < p):
+                better += 1
+        if better < K:
+            keep.append(p)
+    return keep
+
+
+def check_topk_rank_count(o):
+    for seed in range(20):
+        rng = _rng(100 + seed)
+        n = int(rng.integers(1, 60))
+        I = rng.integers(0, 6, size=n) / 4.0          # heavy ties
+        for K in (1, 3, 8, n, n + 5):
+            idx, cnt = o.topk_select(I, K)
+            exp = _rank_count_select(list(I), K)
+            assert cnt == len(exp), (seed, K)
+            assert list(idx[:cnt]) == exp, (seed, K, list(idx[:cnt]), exp)
+            assert all(x == -1 for x in idx[cnt:])
+
+
+def check_topk_special(o):
+    # all equal -> the first K positions
+    idx, cnt = o.topk_select(np.zeros(50), 7)
+    assert list(idx) == list(range(7)) and cnt == 7
+    # K >= n -> every position, -1 padded
+    idx, cnt = o.topk_select(np.array([3.0, 1.0, 2.0]), 5)
+    assert list(idx) == [0, 1, 2, -1, -1] and cnt == 3
+    # strictly decreasing -> the first K; strictly increasing -> the last K
+    idx, _ = o.topk_select(np.arange(20, 0, -1, dtype=float), 4)
+    assert list(idx) == [0, 1, 2, 3]
+    idx, _ = o.topk_select(np.arange(20, dtype=float), 4)
+    assert list(idx) == [16, 17, 18, 19]
+    # -inf and negative scores are ranked like any other value
+    idx, _ = o.topk_select(np.array([-1.0, -np.inf, -0.5, -2.0]), 2)
+    assert list(idx) == [0, 2]
+    # equals a full stable sort (library routine) of the scores
+    rng = _rng(7)
+    I = rng.integers(0, 30, size=500) / 8.0
+    full = np.argsort(-I, kind="stable")
+    idx, _ = o.topk_select(I, 64)
+    assert list(idx) == sorted(full[:64].tolist())
+
+
+# ----------------------------------------------------------------------------
+# attention core
+# ----------------------------------------------------------------------------
+
+def _load_golden_mla():
+    cases, cur = [], {}
+    for line in open(os.path.join(GOLDEN, "mla_tiny.txt")):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        key, val = [x.strip() for x in line.split("=", 1)]
+        if key == "case":
+            if cur:
+                cases.append(cur)
+            cur = {"name": val}
+            continue
+        cur[key] = val
+
+    if cur:
+        cases.append(cur)
+
+    def num(x):
+        x = x.strip()
+        if "+" in x:
+            return sum(num(t) for t in x.split("+"))
+        if "*" in x:
+            a, b = x.split("*", 1)
+            return num(a) * num(b)
+        if x.startswith("ln"):
+            return math.log(float(Fraction(x[2:])))
+        return float(Fraction(x))
+
+    def mat(v):
+        return np.array([[num(x) for x in r.split()] for r in v.split(";")])
+    return [(c["name"], mat(c["q"]), mat(c["rows"]), num(c["scale"]), int(c["d_v"]),
+             mat(c["out"]), mat(c["lse"])[0]) for c in cases]
+
+
+def check_mla_golden(o):
+    """Hand-worked tiny attention examples (tests/golden/mla_tiny.txt)."""
+    for name, q, rows, scale, d_v, out_exp, lse_exp in _load_golden_mla():
+        out, lse = o.sparse_mla(q, rows, scale, d_v=d_v)
+        assert np.allclose(out, out_exp, rtol=1e-14, atol=1e-14), (name, out, out_exp)
+        assert np.allclose(lse, lse_exp, rtol=1e-14, atol=1e-14), (name, lse, lse_exp)
+
+
+def check_mla_k1(o):
+    """A single selected row: the output is that row's value part, lse its logit."""
+    rng = _rng(21)
+    q = rng.standard_normal((4, 576)); c = rng.standard_normal((1, 576))
+    out, lse = o.sparse_mla(q, c, 0.125)
+    assert np.allclose(out, np.repeat(c[:, :512], 4, axis=0), rtol=1e-14, atol=1e-14)
+    assert np.allclose(lse, 0.125 * (q @ c[0]), rtol=1e-14, atol=1e-14)
+
+
+def check_mla_identical_rows(o):
+    rng = _rng(22)
+    q = rng.standard_normal((3, 576)); c = np.repeat(rng.standard_normal((1, 576)), 9, axis=0)
+    out, lse = o.sparse_mla(q, c, 0.3)
+    assert np.allclose(out, np.repeat(c[:1, :512], 3, axis=0), rtol=1e-13, atol=1e-13)
+    assert np.allclose(lse, 0.3 * (q @ c[0]) + math.log(9.0), rtol=1e-13, atol=1e-13)
+
+
+def check_mla_permutation(o):
+    rng = _rng(23)
+    q = rng.standard_normal((5, 576)); c = rng.standard_normal((33, 576))
+    perm = rng.permutation(33)
+    a = o.sparse_mla(q, c, 0.1); b = o.sparse_mla(q, c[perm], 0.1)
+    assert np.allclose(a[0], b[0], rtol=1e-12, atol=1e-14)
+    assert np.allclose(a[1], b[1], rtol=1e-12, atol=1e-14)
+
+
+def check_mla_vs_sdpa(o):
+    """Dense attention equals torch's scaled_dot_product_attention in fp64 (CPU)."""
+    import torch
+    rng = _rng(24)
+    for H, n, scale in [(16, 37, 1 / 24), (4, 300, 1.0), (2, 1, 0.5)]:
+        q = rng.standard_normal((H, 576)); c = rng.standard_normal((n, 576))
+        out, lse = o.dense_mla(q, c, scale)
+        tq = torch.tensor(q).view(H, 1, 576)
+        tk = torch.tensor(c).view(1, n, 576).expand(H, n, 576)
+        tv = torch.tensor(c[:, :512]).view(1, n, 512).expand(H, n, 512)
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale)
+        assert np.allclose(out, ref.view(H, 512).numpy(), rtol=1e-12, atol=1e-13), (H, n)
+        ref_lse = torch.logsumexp(scale * (tq @ tk.transpose(1, 2)).view(H, n), dim=1)
+        assert np.allclose(lse, ref_lse.numpy(), rtol=1e-13, atol=1e-13)
+
+
+def check_mla_softmax_stress(o):
+    """Large logits (scale 1, N(0,1) queries): still a proper convex combination."""
+    rng = _rng(25)
+    q = rng.standard_normal((8, 576)); c = rng.standard_normal((64, 576))
+    out, lse = o.sparse_mla(q, c, 1.0)
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    lo = c[:, :512].min(axis=0); hi = c[:, :512].max(axis=0)
+    assert np.all(out >= lo - 1e-9) and np.all(out <= hi + 1e-9)
+    # the dominant row wins: compare against explicit log-domain weights
+    logits = q @ c.T
+    w = np.exp(logits - logits.max(axis=1, keepdims=True))
+    w /= w.sum(axis=1, keepdims=True)
+    assert np.allclose(out, w @ c[:, :512], rtol=1e-10, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# the whole row: causality, K >= history, paging
+# ----------------------------------------------------------------------------
+
+def check_layer_k_ge_history_is_dense(o):
+    """With K >= visible history every position is kept and the output is dense attention."""
+    rng = _rng(31)
+    Hi, d, H, n = 4, 16, 6, 50
+    q_idx = _int_mat(rng, (Hi, d)); w = _grid_w(rng, Hi)
+    k = _int_mat(rng, (n, d)); lat = rng.standard_normal((n, 576)); q = rng.standard_normal((H, 576))
+    r = o.layer_row(q_idx, w, q, k, None, lambda p: lat[np.asarray(p, dtype=np.int64)], n, 64, 0.05)
+    assert r["count"] == n and list(r["idx"][:n]) == list(range(n))
+    out, lse = o.dense_mla(q, lat, 0.05)
+    assert np.allclose(r["out"], out, rtol=1e-13, atol=1e-14)
+
+
+def check_layer_selection_is_topk_of_scores(o):
+    """The attention reads exactly the rows of the top-K scored positions."""
+    rng = _rng(32)
+    Hi, d, H, n, K = 3, 8, 2, 90, 10
+    q_idx = _int_mat(rng, (Hi, d)); w = _grid_w(rng, Hi)
+    k = _int_mat(rng, (n, d)); lat = rng.standard_normal((n, 576)); q = rng.standard_normal((H, 576))
+    r = o.layer_row(q_idx, w, q, k, None, lambda p: lat[np.asarray(p, dtype=np.int64)], n, K, 0.07)
+    exp_idx = _rank_count_select(list(o.index_scores(q_idx, w, k)), K)
+    assert list(r["idx"][:K]) == exp_idx
+    out, _ = o.sparse_mla(q, lat[exp_idx], 0.07)
+    assert np.allclose(r["out"], out, rtol=1e-13, atol=1e-14)
+
+
+def all_checks():
+    return [v for k, v in sorted(globals().items()) if k.startswith("check_") and callable(v)]

@@ -1,0 +1,85 @@
+"""The oracle's per-row drivers on seeded workloads, and the workload recipes (CPU)."""
+import numpy as np
+import torch
+
+import oracle
+from indexed_sparse_attention_indexer_gb300 import workloads as W
+
+
+def test_recipe_values():
+    ws = W.make_decode(3, 100, 4, 16, 8, 2, seed=1, k_fp8=True, page_size=16,
+                       lengths=[100, 1, 37])
+    qi = ws.q_idx.float()
+    assert qi.min() >= -3 and qi.max() <= 3 and torch.equal(qi, qi.round())
+    ki = ws.k_idx.float()
+    assert ki.min() >= -3 and ki.max() <= 3 and torch.equal(ki, ki.round())
+    assert torch.equal(ws.w * 128, torch.floor(ws.w * 128)) and ws.w.min() >= 0 and ws.w.max() < 1
+    e = torch.log2(ws.k_scale)
+    assert torch.equal(e, e.round()) and e.min() >= -4 and e.max() <= 0
+    # block table: every used page id distinct, unused entries -1
+    used = [int(x) for b in range(3) for x in ws.block_table[b] if x >= 0]
+    assert len(used) == len(set(used)) == (100 + 15) // 16 + 1 + (37 + 15) // 16
+    L = W.loguniform_lengths(4096, 1024, 131072, torch.Generator().manual_seed(7), "cpu")
+    assert L.min() >= 1024 and L.max() <= 131072
+    # log-uniform: the median sits near the geometric mean (~11585)
+    assert 9000 < float(L.float().median()) < 14500
+
+
+def _as_paged(ws, page):
+    """Re-lay a contiguous decode workload into a shuffled page pool (test helper)."""
+    B, S = ws.k_idx.shape[:2]
+    npg = (S + page - 1) // page
+    P = B * npg
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(5))
+    kp = torch.zeros((P, page) + ws.k_idx.shape[2:], dtype=ws.k_idx.dtype)
+    lp = torch.zeros((P, page) + ws.latent.shape[2:], dtype=ws.latent.dtype)
+    bt = torch.full((B, npg), -1, dtype=torch.int32)
+    for b in range(B):
+        for j in range(npg):
+            p = int(perm[b * npg + j])
+            n = min(page, S - j * page)
+            kp[p, :n] = ws.k_idx[b, j * page:j * page + n]
+            lp[p, :n] = ws.latent[b, j * page:j * page + n]
+            bt[b, j] = p
+    out = ws.to("cpu")
+    out.k_idx, out.latent, out.block_table, out.page_size = kp, lp, bt, page
+    return out
+
+
+def test_paged_equals_contiguous():
+    ws = W.make_decode(3, 150, 4, 16, 20, 4, seed=3, lengths=[150, 61, 64])
+    pg = _as_paged(ws, 16)
+    for b in range(3):
+        a = oracle.decode_row(ws, b)
+        c = oracle.decode_row(pg, b)
+        assert np.array_equal(a["idx"], c["idx"]) and a["count"] == c["count"]
+        assert np.array_equal(a["out"], c["out"])
+
+
+def test_prefill_causality_and_chunk_invariance():
+    T, S = 24, 40
+    ws = W.make_prefill(T, S, 4, 16, 6, 2, seed=4, q_offset=16)
+    res = oracle.layer(ws)
+    for t, r in res.items():
+        sel = r["idx"][:r["count"]]
+        assert sel.max() <= ws.q_offset + t
+        assert r["count"] == min(ws.K, ws.q_offset + t + 1)
+    full = W.make_prefill(4, 8, 4, 16, 6, 2, seed=4, q_offset=0)
+    r0 = oracle.prefill_row(full, 0)
+    assert r0["count"] == 1 and r0["idx"][0] == 0
+    # a row's result depends only on its own query and the visible prefix
+    sub = ws.to("cpu")
+    sub.q_idx, sub.w, sub.q = ws.q_idx[5:9], ws.w[5:9], ws.q[5:9]
+    sub.q_offset = ws.q_offset + 5
+    for t in range(4):
+        a = oracle.prefill_row(sub, t)
+        b = res[5 + t]
+        assert np.array_equal(a["idx"], b["idx"]) and np.array_equal(a["out"], b["out"])
+
+
+def test_decode_row_short_history_takes_all():
+    ws = W.make_decode(2, 0, 4, 16, 32, 2, seed=6, lengths=[5, 40])
+    r = oracle.decode_row(ws, 0)
+    assert r["count"] == 5 and list(r["idx"][:6]) == [0, 1, 2, 3, 4, -1]
+    r = oracle.decode_row(ws, 1)
+    assert r["count"] == 32
