@@ -1,0 +1,470 @@
+"""Benchmark: the whole indexed sparse attention layer (indexer -> Top-K ->
+sparse MLA) on the batched-decode workload, 64 sequences x 32768 history,
+64x128 indexer heads, K = 2048, 128 MLA heads over a 576-wide bf16 latent cache.
+
+One step = one dsi_indexed_attention call over the batch (one query token per
+sequence), inputs resident in HBM.  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--config C]
+
+--impl reference times the CPU oracle (fp64 numpy) on a bounded sample of the
+same workload; it is the baseline arm, not a GPU implementation.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# the oracle's numpy BLAS runs single-threaded unless told otherwise (its core
+# count is reported with the CPU baseline)
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from indexed_sparse_attention_indexer_gb300 import workloads as W  # noqa: E402
+
+METRIC = "fused indexer+TopK+sparse-MLA tokens/s; achieved HBM GB/s vs GB300 peak"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work per step (only what the method must move)
+# ----------------------------------------------------------------------------
+
+def algorithmic_bytes(ws) -> dict:
+    """Bytes the layer must move per step: every visible index key (+ scale),
+    the query tensors, the K selected latent rows, the outputs and indices.
+    The score row (4 B per position) is written and read back once by the
+    unfused scoring/select pair; it is listed separately."""
+    B = ws.T
+    lens = ws.seq_lens.to(torch.int64).cpu()
+    if ws.mode == "decode":
+        vis = lens
+    else:
+        vis = torch.arange(1, B + 1, dtype=torch.int64) + ws.q_offset
+    kel = ws.k_idx.element_size()
+    key = int(vis.sum()) * ws.d * kel
+    scale = int(vis.sum()) * 4 if ws.k_scale is not None else 0
+    sel = torch.clamp(vis, max=ws.K)
+    gather = int(sel.sum()) * W.D_QK * 2
+    q_bytes = ws.q_idx.numel() * 2 + ws.w.numel() * 4 + ws.q.numel() * 2
+    out = B * ws.H * W.D_LATENT * 2 + B * ws.H * 4
+    idx = B * ws.K * 4
+    scores = int(vis.sum()) * 4 * 2
+    return {"index_keys": key + scale, "gather": gather, "queries": q_bytes, "outputs": out,
+            "indices": idx, "score_rows": scores,
+            "total": key + scale + gather + q_bytes + out + idx}
+
+
+def scoring_kernel_bytes(ws) -> int:
+    """Algorithmic bytes of one scoring launch: index keys (+ scales), q_idx,
+    head weights, and the fp32 score row it writes."""
+    a = algorithmic_bytes(ws)
+    return a["index_keys"] + ws.q_idx.numel() * 2 + ws.w.numel() * 4 + a["score_rows"] // 2
+
+
+def algorithmic_flops(ws) -> dict:
+    lens = ws.seq_lens.to(torch.int64).cpu()
+    vis = lens if ws.mode == "decode" else torch.arange(1, ws.T + 1) + ws.q_offset
+    idx_fl = 2 * int(vis.sum()) * ws.H_i * ws.d
+    sel = torch.clamp(vis, max=ws.K)
+    mla_fl = 2 * int(sel.sum()) * ws.H * (W.D_QK + W.D_LATENT)
+    return {"indexer": idx_fl, "mla": mla_fl}
+
+
+# ----------------------------------------------------------------------------
+# measured peaks, clocks, profiles
+# ----------------------------------------------------------------------------
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed loop runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, on: bool):
+        if on:
+            self.t_on = time.time()
+        else:
+            self.t_off = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        inside = [s for t, s in self.samples if self.t_on and self.t_off and
+                  self.t_on - 0.06 <= t <= self.t_off + 0.06]
+        used = inside if inside else [s for _, s in self.samples]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in used:
+            parts = [x.strip() for x in s.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0])); mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm), "samples_in_timed_region": len(inside)}
+
+
+def kernel_source_sha() -> str:
+    """Hash of the scoring kernels' sources (traffic figures go stale when they change)."""
+    h = hashlib.sha256()
+    for f in ("index_score.cu", "index_score_tc.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "indexed_sparse_attention_indexer_gb300", "csrc", f),
+                      "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now (profiles/traffic.txt: kernel workload bytes sha)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    sha = kernel_source_sha()
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = line.split()
+        if len(f) == 4 and f[0] == kernel and f[1] == workload and f[3] == sha:
+            return float(f[2])
+    return None
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_gpu(args):
+    from indexed_sparse_attention_indexer_gb300 import binding
+
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = W.CONFIGS[args.config]
+    ws = W.make_config(args.config, device=dev)  # seeded per config; each rank its own replica
+    torch.cuda.synchronize()
+    binding.load()
+    stream = torch.cuda.current_stream()
+    cache = binding.Cache.of(ws)
+    decode = ws.mode == "decode"
+    span = cache.struct.s_max if decode else ws.q_offset + ws.T
+    wsp = binding.alloc_workspace(
+        binding.workspace_size(ws.T, ws.H_i, ws.H, ws.K, span, decode), dev)
+    out = torch.empty((ws.T, ws.H, W.D_LATENT), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((ws.T, ws.H), dtype=torch.float32, device=dev)
+    idx = torch.empty((ws.T, ws.K), dtype=torch.int32, device=dev)
+    cnt = torch.empty((ws.T,), dtype=torch.int32, device=dev)
+
+    def step():
+        binding.indexed_attention(ws.q_idx, ws.w, ws.q, cache, ws.K, ws.scale, decode,
+                                  ws.q_offset, out=out, lse=lse, idx=idx, count=cnt,
+                                  workspace=wsp, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    # keep the GPU busy while the sampler starts, then time exactly K steps
+    t_end = time.time() + 0.3
+    while time.time() < t_end:
+        step()
+        torch.cuda.synchronize()
+    l0 = binding.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark(True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    barrier(world)
+    launches = binding.launch_count() - l0
+    ms_local = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    ms = max_over_ranks(ms_local, world)
+    ms_step = ms / args.steps
+    tokens = ws.T * world
+    value = tokens * args.steps / (ms / 1e3)
+
+    # ---- dominant kernel: the indexer scoring launch, timed alone ----------
+    scores = torch.empty((ws.T, span), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        binding.index_score(ws.q_idx, ws.w, cache, decode, ws.q_offset, scores=scores, ld=span,
+                            stream=stream)
+    torch.cuda.synchronize()
+    nk = max(10, args.steps)
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
+    for _ in range(nk):
+        binding.index_score(ws.q_idx, ws.w, cache, decode, ws.q_offset, scores=scores, ld=span,
+                            stream=stream)
+    k1.record(stream)
+    torch.cuda.synchronize()
+    k_ms = k0.elapsed_time(k1) / nk
+    hbm, tfl, src = peaks()
+    kbytes = scoring_kernel_bytes(ws)
+    achieved = kbytes / (k_ms / 1e3) / 1e9
+    kname = "index_score"
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": src,
+                "traffic": recorded_traffic(kname, cfg["name"]),
+                "algorithmic_bytes": kbytes, "kernel_ms": round(k_ms, 5)}
+    ab = algorithmic_bytes(ws)
+    step_gbs = ab["total"] / (ms_step / 1e3) / 1e9
+
+    # ---- end to end through the public API with host buffers ---------------
+    e2e = run_e2e(ws, cache, wsp, decode, args, stream, dev)
+
+    result = None
+    if rank == 0:
+        fl = algorithmic_flops(ws)
+        result = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded generators; integer-valued indexer inputs, N(0,1) latent)",
+            "config": {"workload": cfg["name"], "batch": ws.T, "history": int(ws.s_max),
+                       "indexer": f"{ws.H_i}x{ws.d}", "topk": ws.K, "mla_heads": ws.H,
+                       "parallelism": f"replicas x{world} (batch shards, no collective)",
+                       "l2": "inputs larger than L2 (537 MB of index keys streamed per step)"},
+            "hbm_gbs_step": round(step_gbs, 1),
+            "hbm_frac_step": round(step_gbs / hbm, 4),
+            "algorithmic_bytes_per_step": ab, "algorithmic_flops_per_step": fl,
+            "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
+            "gpu_launches_per_step": launches / args.steps, "clocks": clk,
+        }
+        if world == 1 and not args.no_cpu:
+            result["cpu_baseline"] = cpu_baseline(ws, budget_s=args.cpu_seconds)
+    barrier(world)
+    return result
+
+
+def run_e2e(ws, cache, wsp, decode, args, stream, dev):
+    """Same metric through binding.indexed_attention with the per-step inputs
+    (q_idx, w, q) copied from pinned host memory and the output read back every
+    step; the caches stay resident as they would in serving."""
+    from indexed_sparse_attention_indexer_gb300 import binding
+    h_qidx = ws.q_idx.cpu().pin_memory()
+    h_w = ws.w.cpu().pin_memory()
+    h_q = ws.q.cpu().pin_memory()
+    h_out = torch.empty((ws.T, ws.H, W.D_LATENT), dtype=torch.bfloat16).pin_memory()
+    d_qidx, d_w, d_q = torch.empty_like(ws.q_idx), torch.empty_like(ws.w), torch.empty_like(ws.q)
+    out = torch.empty((ws.T, ws.H, W.D_LATENT), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        d_qidx.copy_(h_qidx, non_blocking=True)
+        d_w.copy_(h_w, non_blocking=True)
+        d_q.copy_(h_q, non_blocking=True)
+        binding.indexed_attention(d_qidx, d_w, d_q, cache, ws.K, ws.scale, decode, ws.q_offset,
+                                  out=out, workspace=wsp, want_lse=False, want_idx=False,
+                                  stream=stream)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    bi = h_qidx.numel() * 2 + h_w.numel() * 4 + h_q.numel() * 2
+    bo = h_out.numel() * 2
+    return {"value": round(ws.T * args.steps / (ms / 1e3), 1), "unit": UNIT,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "ms_per_step": round(ms / args.steps, 5),
+            "note": "caches resident; per-step queries in, attention output out"}
+
+
+# ----------------------------------------------------------------------------
+# the oracle (CPU baseline / reference arm)
+# ----------------------------------------------------------------------------
+
+def _cpu_rows(ws_dev, rows):
+    """CPU copy of the sampled decode rows (the oracle's inputs)."""
+    sub = ws_dev.to(ws_dev.q.device)
+    sub.q_idx, sub.w, sub.q = ws_dev.q_idx[rows], ws_dev.w[rows], ws_dev.q[rows]
+    sub.seq_lens = ws_dev.seq_lens[rows]
+    sub.k_idx, sub.latent = ws_dev.k_idx[rows], ws_dev.latent[rows]
+    sub.k_scale = None if ws_dev.k_scale is None else ws_dev.k_scale[rows]
+    return sub.to("cpu")
+
+
+def _oracle_rows(ws, budget_s: float, start: int = 0):
+    """Run the oracle row by row (starting at ``start``) until ``budget_s`` has
+    passed (at least one row).  Returns (rows done, seconds)."""
+    import oracle
+    rows_done = 0
+    cpu_ws = None if ws.mode == "decode" else ws.to("cpu")
+    t0 = time.perf_counter()
+    while True:
+        r = (start + rows_done) % ws.T
+        if cpu_ws is None:
+            oracle.decode_row(_cpu_rows(ws, [r]), 0)
+        else:
+            oracle.prefill_row(cpu_ws, r)
+        rows_done += 1
+        if time.perf_counter() - t0 >= budget_s or rows_done >= ws.T:
+            break
+    return rows_done, time.perf_counter() - t0
+
+
+def cpu_baseline(ws, budget_s: float = 10.0) -> dict:
+    rows, el = _oracle_rows(ws, budget_s)
+    return {"value": round(rows / el, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of {ws.T} query rows of the same workload (fp64 numpy oracle, "
+                      f"single-threaded BLAS, inputs copied to the host per row), {el:.1f} s"}
+
+
+def run_reference(args):
+    """The baseline arm: the CPU oracle on a bounded sample, same metric and config."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return None
+    cfg = W.CONFIGS[args.config]
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    ws = W.make_config(args.config, device=dev)
+    per_step = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
+    start = 0
+    for _ in range(args.warmup):
+        n, _ = _oracle_rows(ws, per_step, start)
+        start += n
+    tot_rows, tot_s = 0, 0.0
+    for _ in range(args.steps):
+        n, el = _oracle_rows(ws, per_step, start)
+        start += n
+        tot_rows += n
+        tot_s += el
+    value = tot_rows / tot_s
+    sample = (f"{tot_rows} query rows over {args.steps} timed steps (each a bounded sample of the "
+              f"{ws.T}-row batch, ~{per_step:.1f} s), fp64 numpy oracle, single-threaded BLAS")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * tot_s / max(1, args.steps), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (same seeded generators as the GPU arm)",
+            "config": {"workload": cfg["name"], "batch": ws.T, "history": int(ws.s_max),
+                       "indexer": f"{ws.H_i}x{ws.d}", "topk": ws.K, "mla_heads": ws.H},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", type=int, default=2, choices=sorted(W.CONFIGS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and args.impl != "reference":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+/*
+ * dsi.h — C ABI of libdsi: the index-based sparse attention layer on one GPU.
+ *
+ * The layer has two stages ("Day 0 Inference Support for New LLM
+ * Architectures: Optimization Practices", section "Index-Based Sparse
+ * Attention"): a lightweight indexer scores the history positions of every
+ * query token, weights the per-head scores with per-token head weights and
+ * keeps the Top-K positions; a sparse attention core then reads only the
+ * latent (MLA) cache rows at those positions and attends over them.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Memory: every pointer argument is caller-owned DEVICE memory unless its
+ *   comment says otherwise.  The library allocates nothing per call; scratch
+ *   space is a caller-provided workspace sized by dsi_workspace_size().
+ * - Execution: calls enqueue kernels on `stream` (a cudaStream_t passed as
+ *   void*, NULL = legacy default stream) and return after launch, without a
+ *   host synchronisation.  Errors detectable on the host (null pointers,
+ *   shapes, alignment, unsupported sizes) return before anything is launched
+ *   and leave every output untouched.  Errors found by kernels (an index out
+ *   of range when the library is built with DSI_CHECKED, a bounded wait that
+ *   ran out) set a device status word that dsi_get_device_status() reads.
+ * - No CPU fallback: a shape without a kernel returns DSI_ERR_UNSUPPORTED.
+ * - Numbers: bf16 = IEEE bfloat16 (2 bytes), fp8 = E4M3 ("e4m3fn", 1 byte),
+ *   scores fp32, indices int32.  Arrays are row-major, densely packed except
+ *   where a leading dimension is passed.
+ *
+ * Cache layout (struct dsi_cache)
+ * -------------------------------
+ * One index key of width d per history position, shared by all indexer heads
+ * (the pages read "the paged K cache"; "Internal Fusion of the Indexer"), and
+ * one latent row of DSI_D_QK = 576 bf16 per position (512 latent + 64 rope;
+ * "Day 0 Inference Adaptation and Performance Optimization for New Models" §1:
+ * index selection on top of Multi-head Latent Attention).
+ * - Contiguous (block_table == NULL): k_idx [batch, s_max, d],
+ *   k_scale [batch, s_max], latent [batch, s_max, 576].
+ * - Paged (block_table != NULL): pools k_idx [num_pages, page_size, d],
+ *   k_scale [num_pages, page_size], latent [num_pages, page_size, 576];
+ *   logical position p of sequence b lives in page block_table[b, p/page_size]
+ *   at slot p % page_size.
+ * Row semantics:
+ * - decode != 0: one query token per sequence; row b sees positions
+ *   0 .. seq_lens[b]-1 (the new token's own key is already in the cache).
+ * - decode == 0 (prefill): one sequence (batch == 1); query token t sits at
+ *   position q_offset + t and sees positions 0 .. q_offset + t.
+ */
+#ifndef DSI_H
+#define DSI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSI_D_LATENT 512
+#define DSI_D_ROPE 64
+#define DSI_D_QK 576
+#define DSI_MAX_K 4096          /* largest supported top-k */
+#define DSI_VERSION 1
+
+typedef enum {
+  DSI_OK = 0,
+  DSI_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shape */
+  DSI_ERR_UNSUPPORTED = 2,   /* valid, but no kernel for this shape / dtype */
+  DSI_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, attribute) */
+  DSI_ERR_TIMEOUT = 4,       /* a bounded device wait ran out (device status) */
+  DSI_ERR_BOUNDS = 5,        /* an index or page id out of range (device status) */
+  DSI_ERR_WORKSPACE = 6      /* workspace NULL or smaller than dsi_workspace_size() */
+} dsi_status;
+
+typedef enum { DSI_BF16 = 0, DSI_FP8_E4M3 = 1 } dsi_dtype;
+
+typedef struct dsi_cache {
+  const void*    k_idx;        /* index keys, k_dtype elements */
+  int32_t        k_dtype;      /* dsi_dtype of k_idx */
+  int32_t        d;            /* index key width (64 or 128; any multiple of 8 on the generic kernel) */
+  const float*   k_scale;      /* FP8 only: one fp32 scale per position; NULL for bf16 */
+  const void*    latent;       /* bf16 latent rows, 576 per position */
+  const int32_t* block_table;  /* [batch, max_pages] page ids, or NULL for contiguous */
+  int32_t        page_size;    /* positions per page (paged only; multiple of 8) */
+  int32_t        max_pages;    /* columns of block_table (paged only) */
+  const int32_t* seq_lens;     /* [batch] history length per sequence (decode); may be NULL for prefill */
+  int32_t        batch;        /* number of sequences */
+  int64_t        s_max;        /* contiguous: rows per sequence; paged: max_pages * page_size */
+  int64_t        num_pages;    /* paged: pages in the pools (bounds checks); contiguous: 0 */
+} dsi_cache;
+
+/*
+ * dsi_index_score — indexer scores of every visible position.
+ * ("Day 0 Inference Support for New LLM Architectures: Optimization
+ * Practices", "Internal Fusion of the Indexer": relevance scoring, then the
+ * weighted sum over heads; "Day 0 Inference Adaptation and Performance
+ * Optimization for New Models" §3, indexing stage.)
+ *
+ *   scores[r, s] = k_scale_s * sum_h w[r, h] * max(0, q_idx[r, h, :] . k[s, :])
+ *
+ * with k_scale_s = 1 for bf16 keys.  The ReLU gate is this library's stated
+ * choice (the pages leave the activation open).
+ *   q_idx   bf16 [rows, n_heads_idx, d]
+ *   w       fp32 [rows, n_heads_idx] head weights per query token
+ *   cache   see above; decode: rows == batch
+ *   scores  fp32 [rows, ld_scores]; entries s < visible length of row r are
+ *           written, the rest are left untouched.  ld_scores >= s_max
+ *           (decode) or >= q_offset + rows (prefill).
+ * Errors: DSI_ERR_INVALID_ARG (null, rows < 0, ld too small, prefill with
+ * batch != 1 or q_offset + rows > s_max), DSI_ERR_UNSUPPORTED (d not a
+ * multiple of 8, n_heads_idx outside 1..128, page_size not a multiple of 8).
+ */
+dsi_status dsi_index_score(const void* q_idx, const float* w, const dsi_cache* cache,
+                           int32_t rows, int32_t n_heads_idx, int32_t decode, int64_t q_offset,
+                           float* scores, int64_t ld_scores, void* stream);
+
+/*
+ * dsi_topk — per-row Top-K selection.
+ * ("Day 0 Inference Support for New LLM Architectures: Optimization
+ * Practices", "Internal Fusion of the Indexer": top-k over the weighted
+ * scores, indices fed to the attention core.)
+ *
+ * For each row r with n_r candidates scores[r, 0 .. n_r-1]: keeps the
+ * min(K, n_r) largest scores; equal scores are ranked by lower position.  The
+ * kept positions are written to idx[r, 0 .. count-1] in ascending order, the
+ * rest of the row is -1.  (Ascending order and -1 padding are this library's
+ * reading; the pages only say an index sequence is output.)
+ *   scores   fp32 [rows, ld_scores]; NaN is not allowed (undefined rank)
+ *   row_len  int32 [rows] candidate count per row, or NULL for the causal
+ *            prefill rule n_r = q_offset + r + 1
+ *   idx      int32 [rows, K]
+ *   count    int32 [rows] or NULL
+ * Errors: DSI_ERR_INVALID_ARG (null, K < 1, rows < 0), DSI_ERR_UNSUPPORTED
+ * (K > DSI_MAX_K).  A row length outside 0..ld_scores is clamped to that range.
+ */
+dsi_status dsi_topk(const float* scores, int64_t ld_scores, int32_t rows,
+                    const int32_t* row_len, int64_t q_offset, int32_t K,
+                    int32_t* idx, int32_t* count, void* stream);
+
+/*
+ * dsi_sparse_mla_decode — attention of one query token per sequence over the
+ * latent rows at the selected positions.
+ * ("Day 0 Inference Support for New LLM Architectures: Optimization
+ * Practices", "Index-Based Sparse Attention": the attention core reads the KV
+ * entries at the selected indices; "Day 0 Inference Adaptation and
+ * Performance Optimization for New Models" §3, sparse attention stage.)
+ *
+ * Absorbed-MLA reading (the pages give no formula): for head h,
+ *   l_s = scale * q[b, h, :] . c_s  (c_s = latent row of position s, 576 wide)
+ *   out[b, h, :] = sum_s softmax(l)_s * c_s[0:512];  lse[b, h] = ln sum_s exp(l_s)
+ * over the positions s = idx[b, j] >= 0.
+ *   q       bf16 [batch, n_heads, 576]
+ *   idx     int32 [batch, K] logical positions (< seq_lens[b]); entries < 0 skipped
+ *   out     bf16 [batch, n_heads, 512]
+ *   lse     fp32 [batch, n_heads] or NULL; a row with no valid index gives
+ *           out = 0 and lse = -inf
+ *   workspace / workspace_bytes: optional (NULL, 0 allowed); with room for
+ *           dsi_workspace_size(batch, 0, n_heads, K, 0, 1) bytes the kernel
+ *           splits each row's K positions over several blocks.
+ * Errors: DSI_ERR_INVALID_ARG, DSI_ERR_UNSUPPORTED (n_heads outside 1..128 or
+ * not a multiple of 16 when > 16), DSI_ERR_BOUNDS (device status, DSI_CHECKED
+ * builds) for an index >= seq_lens[b].
+ */
+dsi_status dsi_sparse_mla_decode(const void* q, const dsi_cache* cache, const int32_t* idx,
+                                 int32_t batch, int32_t n_heads, int32_t K, float scale,
+                                 void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/*
+ * dsi_sparse_mla_prefill — the same attention for T query tokens of one
+ * sequence (batch == 1); token t sits at position q_offset + t and its
+ * indices must be <= q_offset + t.
+ *   q    bf16 [T, n_heads, 576];  idx int32 [T, K];  out bf16 [T, n_heads, 512]
+ *   lse  fp32 [T, n_heads] or NULL.  workspace as for decode (may be NULL).
+ */
+dsi_status dsi_sparse_mla_prefill(const void* q, const dsi_cache* cache, const int32_t* idx,
+                                  int32_t T, int32_t n_heads, int32_t K, int64_t q_offset,
+                                  float scale, void* out, float* lse, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
+ * dsi_indexed_attention — the whole layer: indexer scores -> Top-K -> sparse
+ * MLA, enqueued back to back on one stream (the only dependency is "Top-K
+ * ready"; "Day 0 Inference Adaptation and Performance Optimization for New
+ * Models" §3).  Arguments as in the entry points above.
+ *   idx_out   int32 [rows, K] or NULL (then the indices live in the workspace)
+ *   count_out int32 [rows] or NULL
+ *   workspace at least dsi_workspace_size(rows, n_heads_idx, n_heads, K,
+ *             s_max or q_offset + rows, decode) bytes, 256-byte aligned.
+ * Errors: as for the parts; DSI_ERR_WORKSPACE when the workspace is too small.
+ */
+dsi_status dsi_indexed_attention(const void* q_idx, const float* w, const void* q,
+                                 const dsi_cache* cache, int32_t rows, int32_t n_heads_idx,
+                                 int32_t n_heads, int32_t K, int64_t q_offset, float scale,
+                                 int32_t decode, int32_t* idx_out, int32_t* count_out,
+                                 void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/* Bytes of workspace dsi_indexed_attention needs (and the larger, split-K
+ * sizing of the dsi_sparse_mla_* calls when n_heads_idx == 0 and s_max == 0). */
+size_t dsi_workspace_size(int32_t rows, int32_t n_heads_idx, int32_t n_heads, int32_t K,
+                          int64_t s_max, int32_t decode);
+
+/* Synchronises `stream`, returns and clears the device status word of the
+ * current device (DSI_OK, DSI_ERR_BOUNDS or DSI_ERR_TIMEOUT), or DSI_ERR_CUDA
+ * when the stream reports an asynchronous CUDA error. */
+dsi_status dsi_get_device_status(void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* dsi_status_string(dsi_status status);
+
+/* DSI_VERSION of the built library. */
+int32_t dsi_version(void);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all streams; counted on the host at launch).  For accounting in benchmarks. */
+uint64_t dsi_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSI_H */

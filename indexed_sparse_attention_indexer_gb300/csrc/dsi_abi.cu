@@ -1,0 +1,263 @@
+// libdsi C ABI: argument validation on the host, then kernel launches on the
+// caller's stream.  Nothing here computes; see include/dsi.h for the contract.
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "kernels.h"
+
+using namespace dsi;
+
+namespace {
+
+std::atomic<unsigned long long> g_launches{0};
+
+__device__ int g_status_word;  // device status (DSI_ERR_BOUNDS / DSI_ERR_TIMEOUT), 0 = ok
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];  // per-device address of g_status_word
+
+// Device address of the status word on the current device (looked up once).
+int* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+dsi_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return DSI_OK;
+  if (e == cudaErrorInvalidValue) return DSI_ERR_UNSUPPORTED;
+  return DSI_ERR_CUDA;
+}
+
+// Validate a cache description for rows of a decode batch or of a prefill.
+dsi_status check_cache(const dsi_cache* c, int rows, int decode, int64_t q_offset, bool need_keys,
+                       bool need_latent) {
+  if (!c) return DSI_ERR_INVALID_ARG;
+  if (c->batch < 0) return DSI_ERR_INVALID_ARG;
+  if (need_keys) {
+    if (!c->k_idx) return DSI_ERR_INVALID_ARG;
+    if (c->k_dtype != DSI_BF16 && c->k_dtype != DSI_FP8_E4M3) return DSI_ERR_UNSUPPORTED;
+    if (c->d <= 0) return DSI_ERR_INVALID_ARG;
+    const int chunk = c->k_dtype == DSI_FP8_E4M3 ? 16 : 8;  // elements per 16-byte load
+    if (c->d % chunk != 0 || c->d > 256) return DSI_ERR_UNSUPPORTED;
+    if (!aligned(c->k_idx, 16)) return DSI_ERR_INVALID_ARG;
+    if (c->k_dtype == DSI_FP8_E4M3 && !c->k_scale) return DSI_ERR_INVALID_ARG;
+  }
+  if (need_latent && (!c->latent || !aligned(c->latent, 16))) return DSI_ERR_INVALID_ARG;
+  if (c->block_table) {
+    if (c->page_size <= 0 || c->max_pages <= 0 || c->num_pages <= 0) return DSI_ERR_INVALID_ARG;
+    if (c->page_size % 8 != 0) return DSI_ERR_UNSUPPORTED;
+    if (c->s_max != (int64_t)c->max_pages * c->page_size) return DSI_ERR_INVALID_ARG;
+  } else if (c->s_max <= 0) {
+    return DSI_ERR_INVALID_ARG;
+  }
+  if (decode) {
+    if (rows != c->batch || !c->seq_lens) return DSI_ERR_INVALID_ARG;
+  } else {
+    if (c->batch != 1 || q_offset < 0 || q_offset + rows > c->s_max) return DSI_ERR_INVALID_ARG;
+  }
+  return DSI_OK;
+}
+
+CacheView view_of(const dsi_cache* c) {
+  CacheView v;
+  v.k_idx = c->k_idx;
+  v.k_scale = c->k_scale;
+  v.latent = reinterpret_cast<const bf16*>(c->latent);
+  v.block_table = c->block_table;
+  v.seq_lens = c->seq_lens;
+  v.s_max = c->s_max;
+  v.num_pages = c->num_pages;
+  v.page_size = c->page_size;
+  v.max_pages = c->max_pages;
+  v.d = c->d;
+  v.k_dtype = c->k_dtype;
+  v.batch = c->batch;
+  return v;
+}
+
+dsi_status check_mla_heads(int H) {
+  if (H <= 0 || H > 128) return DSI_ERR_UNSUPPORTED;
+  if (H > 16 && H % 16 != 0) return DSI_ERR_UNSUPPORTED;
+  return DSI_OK;
+}
+
+// Workspace carving (every piece 256-byte aligned).
+struct WsPlan {
+  size_t scores_off, idx_off, mla_off, total;
+  int64_t ld;
+  int splits;
+};
+
+WsPlan plan_workspace(int rows, int Hi, int H, int K, int64_t s_max, size_t mla_budget_hint,
+                      bool with_scores, bool with_idx) {
+  WsPlan p;
+  p.ld = (int64_t)round_up((size_t)(s_max > 0 ? s_max : 1), 64);
+  size_t off = 0;
+  p.scores_off = off;
+  if (with_scores) off += round_up((size_t)rows * p.ld * sizeof(float), 256);
+  p.idx_off = off;
+  if (with_idx) off += round_up((size_t)rows * K * sizeof(int32_t), 256);
+  p.mla_off = off;
+  p.splits = mla_pick_splits(rows, H, K, mla_budget_hint);
+  off += round_up(mla_partials_bytes(rows, H, p.splits), 256);
+  p.total = off;
+  (void)Hi;
+  return p;
+}
+
+}  // namespace
+
+void dsi::note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+extern "C" {
+
+uint64_t dsi_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+
+const char* dsi_status_string(dsi_status s) {
+  switch (s) {
+    case DSI_OK: return "ok";
+    case DSI_ERR_INVALID_ARG: return "invalid argument";
+    case DSI_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case DSI_ERR_CUDA: return "CUDA error";
+    case DSI_ERR_TIMEOUT: return "device wait timed out";
+    case DSI_ERR_BOUNDS: return "index or page out of range";
+    case DSI_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+int32_t dsi_version(void) { return DSI_VERSION; }
+
+dsi_status dsi_index_score(const void* q_idx, const float* w, const dsi_cache* cache, int32_t rows,
+                           int32_t n_heads_idx, int32_t decode, int64_t q_offset, float* scores,
+                           int64_t ld_scores, void* stream) {
+  if (!q_idx || !w || !scores || rows < 0) return DSI_ERR_INVALID_ARG;
+  if (n_heads_idx < 1 || n_heads_idx > 128) return DSI_ERR_UNSUPPORTED;
+  dsi_status s = check_cache(cache, rows, decode, q_offset, true, false);
+  if (s != DSI_OK) return s;
+  if (!aligned(q_idx, 16)) return DSI_ERR_INVALID_ARG;
+  if (ld_scores < (decode ? cache->s_max : q_offset + rows)) return DSI_ERR_INVALID_ARG;
+  if (rows == 0) return DSI_OK;
+  CacheView v = view_of(cache);
+  return from_cuda(launch_index_score(reinterpret_cast<const bf16*>(q_idx), w, v, rows,
+                                      n_heads_idx, decode, q_offset, scores, ld_scores,
+                                      status_ptr(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dsi_status dsi_topk(const float* scores, int64_t ld_scores, int32_t rows, const int32_t* row_len,
+                    int64_t q_offset, int32_t K, int32_t* idx, int32_t* count, void* stream) {
+  if (!scores || !idx || rows < 0 || K < 1 || ld_scores < 1 || q_offset < 0)
+    return DSI_ERR_INVALID_ARG;
+  if (K > DSI_MAX_K) return DSI_ERR_UNSUPPORTED;
+  if (rows == 0) return DSI_OK;
+  return from_cuda(launch_topk(scores, ld_scores, rows, row_len, q_offset, K, idx, count,
+                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static dsi_status mla_common(const void* q, const dsi_cache* cache, const int32_t* idx, int rows,
+                             int H, int K, int decode, int64_t q_offset, float scale, void* out,
+                             float* lse, void* ws, size_t ws_bytes, void* stream) {
+  if (!q || !idx || !out || rows < 0 || K < 1) return DSI_ERR_INVALID_ARG;
+  dsi_status s = check_mla_heads(H);
+  if (s != DSI_OK) return s;
+  s = check_cache(cache, rows, decode, q_offset, false, true);
+  if (s != DSI_OK) return s;
+  if (!aligned(q, 16) || !aligned(out, 16)) return DSI_ERR_INVALID_ARG;
+  if (ws && !aligned(ws, 256)) return DSI_ERR_INVALID_ARG;
+  if (!(scale == scale)) return DSI_ERR_INVALID_ARG;
+  if (rows == 0) return DSI_OK;
+  CacheView v = view_of(cache);
+  return from_cuda(launch_sparse_mla(reinterpret_cast<const bf16*>(q), v, idx, rows, H, K, decode,
+                                     q_offset, scale, reinterpret_cast<bf16*>(out), lse, ws,
+                                     ws ? ws_bytes : 0, status_ptr(),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dsi_status dsi_sparse_mla_decode(const void* q, const dsi_cache* cache, const int32_t* idx,
+                                 int32_t batch, int32_t n_heads, int32_t K, float scale, void* out,
+                                 float* lse, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  return mla_common(q, cache, idx, batch, n_heads, K, 1, 0, scale, out, lse, workspace,
+                    workspace_bytes, stream);
+}
+
+dsi_status dsi_sparse_mla_prefill(const void* q, const dsi_cache* cache, const int32_t* idx,
+                                  int32_t T, int32_t n_heads, int32_t K, int64_t q_offset,
+                                  float scale, void* out, float* lse, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return mla_common(q, cache, idx, T, n_heads, K, 0, q_offset, scale, out, lse, workspace,
+                    workspace_bytes, stream);
+}
+
+size_t dsi_workspace_size(int32_t rows, int32_t n_heads_idx, int32_t n_heads, int32_t K,
+                          int64_t s_max, int32_t decode) {
+  (void)decode;
+  if (rows <= 0 || K <= 0 || n_heads <= 0) return 256;
+  const bool layer = n_heads_idx > 0 || s_max > 0;
+  WsPlan p = plan_workspace(rows, n_heads_idx, n_heads, K, s_max, (size_t)-1, layer, layer);
+  return p.total > 0 ? p.total : 256;
+}
+
+dsi_status dsi_indexed_attention(const void* q_idx, const float* w, const void* q,
+                                 const dsi_cache* cache, int32_t rows, int32_t n_heads_idx,
+                                 int32_t n_heads, int32_t K, int64_t q_offset, float scale,
+                                 int32_t decode, int32_t* idx_out, int32_t* count_out, void* out,
+                                 float* lse, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if (!q_idx || !w || !q || !out || rows < 0 || K < 1) return DSI_ERR_INVALID_ARG;
+  if (n_heads_idx < 1 || n_heads_idx > 128 || K > DSI_MAX_K) return DSI_ERR_UNSUPPORTED;
+  dsi_status s = check_mla_heads(n_heads);
+  if (s != DSI_OK) return s;
+  s = check_cache(cache, rows, decode, q_offset, true, true);
+  if (s != DSI_OK) return s;
+  if (!aligned(q_idx, 16) || !aligned(q, 16) || !aligned(out, 16)) return DSI_ERR_INVALID_ARG;
+  if (!(scale == scale)) return DSI_ERR_INVALID_ARG;
+  if (rows == 0) return DSI_OK;
+  const int64_t span = decode ? cache->s_max : q_offset + rows;
+  WsPlan p = plan_workspace(rows, n_heads_idx, n_heads, K, span, (size_t)-1, true, true);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < p.total) return DSI_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  float* scores = reinterpret_cast<float*>(ws + p.scores_off);
+  int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + p.idx_off);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* err = status_ptr();
+  CacheView v = view_of(cache);
+  cudaError_t e = launch_index_score(reinterpret_cast<const bf16*>(q_idx), w, v, rows, n_heads_idx,
+                                     decode, q_offset, scores, p.ld, err, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = launch_topk(scores, p.ld, rows, decode ? cache->seq_lens : nullptr, q_offset, K, idx,
+                  count_out, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = launch_sparse_mla(reinterpret_cast<const bf16*>(q), v, idx, rows, n_heads, K, decode,
+                        q_offset, scale, reinterpret_cast<bf16*>(out), lse, ws + p.mla_off,
+                        p.total - p.mla_off, err, st);
+  return from_cuda(e);
+}
+
+dsi_status dsi_get_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return DSI_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return DSI_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return DSI_ERR_CUDA;
+  }
+  if (v == DSI_ERR_BOUNDS) return DSI_ERR_BOUNDS;
+  if (v == DSI_ERR_TIMEOUT) return DSI_ERR_TIMEOUT;
+  return v == 0 ? DSI_OK : DSI_ERR_CUDA;
+}
+
+}  // extern "C"

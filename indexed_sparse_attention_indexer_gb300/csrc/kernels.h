@@ -1,0 +1,40 @@
+// Internal launchers of the libdsi kernels (host side).  Each returns the
+// cudaError_t of its launch; argument validation happens in dsi_abi.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dsi {
+
+// Counts kernel launches made by the library (dsi_launch_count()).
+void note_launch(int n = 1);
+
+// ---- indexer scoring -------------------------------------------------------
+// scores[r, s] for s < visible_len(r); kernels: warp-shuffle streaming (few
+// heads), tcgen05 tensor-core tiles (64 heads x 128 dims), generic SIMT.
+cudaError_t launch_index_score(const bf16* q_idx, const float* w, const CacheView& c, int rows,
+                               int n_heads_idx, int decode, int64_t q_offset, float* scores,
+                               int64_t ld, int* err, cudaStream_t st);
+
+// Which scoring kernel a shape takes (for tests and the bench's accounting).
+enum ScoreKernel { kScoreStream = 0, kScoreSimt = 1, kScoreTc = 2 };
+ScoreKernel pick_score_kernel(const CacheView& c, int n_heads_idx);
+
+// ---- Top-K -------------------------------------------------------------------
+cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t* row_len,
+                        int64_t q_offset, int K, int32_t* idx, int32_t* count,
+                        cudaStream_t st);
+
+// ---- sparse MLA ----------------------------------------------------------------
+// part_o / part_ml: split-K partials (may be null when splits == 1).
+size_t mla_partials_bytes(int rows, int n_heads, int splits);
+int mla_pick_splits(int rows, int n_heads, int K, size_t ws_bytes);
+cudaError_t launch_sparse_mla(const bf16* q, const CacheView& c, const int32_t* idx, int rows,
+                              int n_heads, int K, int decode, int64_t q_offset, float scale,
+                              bf16* out, float* lse, void* ws, size_t ws_bytes, int* err,
+                              cudaStream_t st);
+
+}  // namespace dsi

@@ -1,0 +1,284 @@
+// Sparse MLA attention core on CUDA cores (any head count that is a multiple
+// of 16, or fewer than 16 heads).
+//
+// ("Day 0 Inference Support for New LLM Architectures: Optimization
+// Practices", "Index-Based Sparse Attention": read the KV entries at the
+// selected indices and run the attention over them; "Day 0 Inference
+// Adaptation and Performance Optimization for New Models" §7: fuse the index
+// reading with the computation.)  Absorbed-MLA reading: the key of a
+// position is its whole 576-wide latent row, the value its first 512 dims.
+//
+// One block = (query row, group of 16 heads, split of the K indices).  The
+// selected latent rows are gathered in tiles of 32 with cp.async into a
+// double-buffered shared-memory tile (row stride padded to 1168 bytes so that
+// 16-byte reads of different rows fall in different banks), logits are dot
+// products against the block's fp32 query rows, the softmax is online (running
+// max and sum per head) and P.V accumulates in registers.  With several
+// splits, each block writes an unnormalised partial (o, m, l) and a combine
+// kernel merges them with their log-sum-exp weights.
+#include <math.h>
+
+#include "kernels.h"
+
+namespace dsi {
+
+constexpr int kHB = 16;        // heads per block
+constexpr int kNT = 32;        // gathered rows per tile
+constexpr int kRS = 584;       // shared row stride (bf16), 1168 bytes
+constexpr int kMlaThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct MlaSmem {
+  float q[kHB][DSI_D_QK];          // 36864 B
+  bf16 c[2][kNT][kRS];             // 74752 B
+  float p[kHB][kNT];               // 2048 B
+  float m[kHB], l[kHB], alpha[kHB];
+  int valid[2][kNT];
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n"); }
+
+__global__ void __launch_bounds__(kMlaThreads)
+mla_simt(const bf16* __restrict__ q, CacheView c, const int32_t* __restrict__ idx, int H, int K,
+         int decode, int64_t q_offset, float scale, bf16* __restrict__ out, float* __restrict__ lse,
+         float* __restrict__ part_o, float2* __restrict__ part_ml, int splits, int* err) {
+  extern __shared__ float4 mla_smem_raw[];
+  MlaSmem& S = *reinterpret_cast<MlaSmem*>(mla_smem_raw);
+  const int g = blockIdx.x, r = blockIdx.y, sp = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = decode ? r : 0;
+  const int64_t n_vis = visible_len(c, r, decode, q_offset);
+  const int hcount = H - g * kHB < kHB ? H - g * kHB : kHB;  // heads of this block
+  const int per = (K + splits - 1) / splits;
+  const int j_begin = sp * per;
+  const int j_end = min(K, j_begin + per);
+  const int32_t* irow = idx + (int64_t)r * K;
+  const float sl2 = scale * kLog2e;  // logits in log2 units
+
+  for (int i = tid; i < kHB * DSI_D_QK; i += kMlaThreads) {
+    const int h = i / DSI_D_QK, e = i - h * DSI_D_QK;
+    S.q[h][e] = h < hcount ? __bfloat162float(q[((int64_t)r * H + g * kHB + h) * DSI_D_QK + e]) * sl2
+                           : 0.f;
+  }
+  if (tid < kHB) { S.m[tid] = -INFINITY; S.l[tid] = 0.f; }
+
+  auto gather = [&](int buf, int j0) {
+    // 32 rows x 72 chunks of 16 bytes
+    for (int i = tid; i < kNT * 72; i += kMlaThreads) {
+      const int rr = i / 72, ch = i - rr * 72;
+      const int j = j0 + rr;
+      int pos = (j < j_end) ? __ldg(irow + j) : -1;
+#ifdef DSI_CHECKED
+      if (pos >= n_vis) { report(err, kErrBounds); pos = -1; }
+#endif
+      (void)n_vis;
+      int64_t row = pos >= 0 ? phys_row(c, b, pos, err) : -1;
+      if (ch == 0) S.valid[buf][rr] = row >= 0;
+      if (row >= 0) cp_async16(&S.c[buf][rr][ch * 8], c.latent + row * DSI_D_QK + ch * 8);
+    }
+    cp_async_commit();
+  };
+
+  const int ntiles = (j_end - j_begin + kNT - 1) / kNT;
+  // PV ownership: 8 dims (dc) x 4 heads (hq) per thread
+  const int dc = tid & 63, hq = (tid >> 6) * 4;
+  float acc[4][8];
+#pragma unroll
+  for (int h = 0; h < 4; ++h)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
+
+  if (ntiles > 0) gather(0, j_begin);
+  for (int t = 0; t < ntiles; ++t) {
+    const int buf = t & 1;
+    cp_async_wait_all();
+    __syncthreads();
+    if (t + 1 < ntiles) gather(buf ^ 1, j_begin + (t + 1) * kNT);
+    // ---- logits: lane = row of the tile, 2 heads per thread ----------------
+    {
+      const int pr = lane, h0 = warp * 2;
+      float a0 = 0.f, a1 = 0.f;
+      if (S.valid[buf][pr]) {
+        const bf16* crow = &S.c[buf][pr][0];
+#pragma unroll 4
+        for (int ch = 0; ch < 72; ++ch) {
+          float cf[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(crow + ch * 8), cf);
+          const float4* q0 = reinterpret_cast<const float4*>(&S.q[h0][ch * 8]);
+          const float4* q1 = reinterpret_cast<const float4*>(&S.q[h0 + 1][ch * 8]);
+          float4 x0 = q0[0], x1 = q0[1], y0 = q1[0], y1 = q1[1];
+          a0 = fmaf(x0.x, cf[0], a0); a0 = fmaf(x0.y, cf[1], a0); a0 = fmaf(x0.z, cf[2], a0);
+          a0 = fmaf(x0.w, cf[3], a0); a0 = fmaf(x1.x, cf[4], a0); a0 = fmaf(x1.y, cf[5], a0);
+          a0 = fmaf(x1.z, cf[6], a0); a0 = fmaf(x1.w, cf[7], a0);
+          a1 = fmaf(y0.x, cf[0], a1); a1 = fmaf(y0.y, cf[1], a1); a1 = fmaf(y0.z, cf[2], a1);
+          a1 = fmaf(y0.w, cf[3], a1); a1 = fmaf(y1.x, cf[4], a1); a1 = fmaf(y1.y, cf[5], a1);
+          a1 = fmaf(y1.z, cf[6], a1); a1 = fmaf(y1.w, cf[7], a1);
+        }
+      } else {
+        a0 = -INFINITY; a1 = -INFINITY;
+      }
+      // ---- online softmax for heads h0, h0+1 (whole warp owns them) --------
+#pragma unroll
+      for (int k2 = 0; k2 < 2; ++k2) {
+        const int h = h0 + k2;
+        const float v = k2 ? a1 : a0;
+        float mx = v;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float m_old = S.m[h];
+        const float m_new = fmaxf(m_old, mx);
+        const float pv = (m_new == -INFINITY) ? 0.f : exp2f(v - m_new);
+        float sum = pv;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float al = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
+        S.p[h][pr] = pv;
+        __syncwarp();
+        if (lane == 0) {
+          S.alpha[h] = al;
+          S.l[h] = S.l[h] * al + sum;
+          S.m[h] = m_new;
+        }
+      }
+    }
+    __syncthreads();
+    // ---- P.V: o[h, dims] = o * alpha + sum_j p[h, j] * c[j, dims] -----------
+    {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float al = S.alpha[hq + h];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[h][e] *= al;
+      }
+      for (int j = 0; j < kNT; ++j) {
+        if (!S.valid[buf][j]) continue;
+        float cf[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(&S.c[buf][j][dc * 8]), cf);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float pj = S.p[hq + h][j];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(pj, cf[e], acc[h][e]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // ---- epilogue ---------------------------------------------------------------
+  if (splits == 1) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int hh = hq + h;
+      if (hh >= hcount) continue;
+      const float l = S.l[hh];
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __align__(16) bf16 o8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o8[e] = __float2bfloat16(acc[h][e] * inv);
+      *reinterpret_cast<uint4*>(out + ((int64_t)r * H + g * kHB + hh) * DSI_D_LATENT + dc * 8) =
+          *reinterpret_cast<const uint4*>(o8);
+      if (lse && dc == 0)
+        lse[(int64_t)r * H + g * kHB + hh] = l > 0.f ? (S.m[hh] + log2f(l)) / kLog2e : -INFINITY;
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int hh = hq + h;
+      if (hh >= hcount) continue;
+      const int64_t pr = (((int64_t)r * splits + sp) * H + g * kHB + hh);
+      float4* po = reinterpret_cast<float4*>(part_o + pr * DSI_D_LATENT + dc * 8);
+      po[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+      po[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+      if (dc == 0) part_ml[pr] = make_float2(S.m[hh], S.l[hh]);
+    }
+  }
+}
+
+// Merge split-K partials: o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+__global__ void __launch_bounds__(128)
+mla_combine(const float* __restrict__ part_o, const float2* __restrict__ part_ml, int H,
+            int splits, bf16* __restrict__ out, float* __restrict__ lse) {
+  const int r = blockIdx.y, h = blockIdx.x, tid = threadIdx.x;
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, part_ml[((int64_t)r * splits + s) * H + h].x);
+  float L = 0.f;
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < splits; ++s) {
+    const int64_t pr = ((int64_t)r * splits + s) * H + h;
+    const float2 ml = part_ml[pr];
+    if (ml.x == -INFINITY) continue;
+    const float f = exp2f(ml.x - M);
+    L += f * ml.y;
+    const float4 v = reinterpret_cast<const float4*>(part_o + pr * DSI_D_LATENT)[tid];
+    o[0] += f * v.x; o[1] += f * v.y; o[2] += f * v.z; o[3] += f * v.w;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __align__(8) bf16 o4[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) o4[e] = __float2bfloat16(o[e] * inv);
+  *reinterpret_cast<uint2*>(out + ((int64_t)r * H + h) * DSI_D_LATENT + tid * 4) =
+      *reinterpret_cast<const uint2*>(o4);
+  if (lse && tid == 0) lse[(int64_t)r * H + h] = L > 0.f ? (M + log2f(L)) / kLog2e : -INFINITY;
+}
+
+size_t mla_partials_bytes(int rows, int n_heads, int splits) {
+  if (splits <= 1) return 0;
+  const size_t n = (size_t)rows * splits * n_heads;
+  return n * DSI_D_LATENT * sizeof(float) + n * sizeof(float2) + 256;
+}
+
+int mla_pick_splits(int rows, int n_heads, int K, size_t ws_bytes) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int groups = (n_heads + kHB - 1) / kHB;
+  const long blocks = (long)rows * groups;
+  int splits = 1;
+  // aim for >= 2 blocks per SM, each split keeping >= 4 tiles of work
+  while (blocks * splits < 2L * sms && (K / (splits * 2)) >= 4 * kNT && splits < 16) splits *= 2;
+  while (splits > 1 && mla_partials_bytes(rows, n_heads, splits) > ws_bytes) splits /= 2;
+  return splits;
+}
+
+cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const int32_t* idx, int rows,
+                                 int n_heads, int K, int decode, int64_t q_offset, float scale,
+                                 bf16* out, float* lse, void* ws, size_t ws_bytes, int* err,
+                                 cudaStream_t st);
+bool tc_mla_supported(int n_heads);
+
+cudaError_t launch_sparse_mla(const bf16* q, const CacheView& c, const int32_t* idx, int rows,
+                              int H, int K, int decode, int64_t q_offset, float scale, bf16* out,
+                              float* lse, void* ws, size_t ws_bytes, int* err, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  if (tc_mla_supported(H))
+    return launch_sparse_mla_tc(q, c, idx, rows, H, K, decode, q_offset, scale, out, lse, ws,
+                                ws_bytes, err, st);
+  const int splits = mla_pick_splits(rows, H, K, ws ? ws_bytes : 0);
+  const size_t smem = sizeof(MlaSmem);
+  cudaError_t e = cudaFuncSetAttribute(mla_simt, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  float* part_o = nullptr;
+  float2* part_ml = nullptr;
+  if (splits > 1) {
+    const size_t n = (size_t)rows * splits * H;
+    part_o = reinterpret_cast<float*>(ws);
+    part_ml = reinterpret_cast<float2*>(reinterpret_cast<char*>(ws) + n * DSI_D_LATENT * sizeof(float));
+  }
+  dim3 grid((H + kHB - 1) / kHB, rows, splits);
+  mla_simt<<<grid, kMlaThreads, smem, st>>>(q, c, idx, H, K, decode, q_offset, scale, out, lse,
+                                            part_o, part_ml, splits, err);
+  note_launch();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || splits == 1) return e;
+  mla_combine<<<dim3(H, rows), 128, 0, st>>>(part_o, part_ml, H, splits, out, lse);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace dsi

@@ -140,6 +140,10 @@ def history_rows(cache, b: int, positions, block_table=None, page_size: int = 0)
     cache[block_table[b, pos // page], pos % page].
     """
     pos = np.asarray(positions, dtype=np.int64)
+    fp8 = getattr(cache, "dtype", None) is not None and "float8" in str(cache.dtype)
+    if fp8:   # index the raw bytes (not every torch build indexes float8 tensors)
+        return history_rows(cache.view(__import__("torch").uint8), b, pos, block_table,
+                            page_size).view(cache.dtype)
     if block_table is None:
         return cache[b][pos] if len(pos) else cache[b][:0]
     bt = block_table[b]

@@ -1,0 +1,156 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every symbol
+include/dsi.h declares, matches the header's struct layout, and rejects bad
+arguments on the host before launching anything."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+from indexed_sparse_attention_indexer_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsi.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsi_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module", params=[False, True], ids=["release", "checked"])
+def L(request):
+    path = binding.lib_path(request.param)
+    if not os.path.exists(path):
+        pytest.skip("library not built (run __graft_entry__.build())")
+    return binding.load(request.param)
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(binding.SIGNATURES), "binding and header disagree"
+
+
+def test_version_and_status_strings(L):
+    assert L.dsi_version() == 1
+    for code in range(7):
+        s = L.dsi_status_string(code)
+        assert s and s != b"unknown status"
+    assert L.dsi_status_string(99) == b"unknown status"
+
+
+def test_struct_layout_matches_header(tmp_path):
+    prog = tmp_path / "layout.c"
+    prog.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "dsi.h"\n'
+        "#define O(f) printf(\"%s %zu\\n\", #f, offsetof(dsi_cache, f));\n"
+        "int main(void){ printf(\"size %zu\\n\", sizeof(dsi_cache));"
+        + "".join(f"O({f})" for f, _ in binding.DsiCache._fields_) + "return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = dict(line.split() for line in out if line)
+    assert int(got["size"]) == ctypes.sizeof(binding.DsiCache)
+    for f, _ in binding.DsiCache._fields_:
+        assert int(got[f]) == getattr(binding.DsiCache, f).offset, f
+
+
+FAKE = 1 << 20  # an aligned, never dereferenced stand-in for a device pointer
+
+
+def _cache(**kw):
+    c = binding.DsiCache()
+    c.k_idx, c.k_dtype, c.d, c.k_scale = FAKE, 0, 128, None
+    c.latent, c.block_table, c.page_size, c.max_pages = FAKE, None, 0, 0
+    c.seq_lens, c.batch, c.s_max, c.num_pages = FAKE, 4, 1024, 0
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def _score(L, c, rows=4, heads=64, decode=1, q_offset=0, ld=1024, q=FAKE, w=FAKE, s=FAKE):
+    return L.dsi_index_score(q, w, ctypes.byref(c), rows, heads, decode, q_offset, s, ld, None)
+
+
+def test_index_score_validation(L):
+    E, U = binding.DSI_ERR_INVALID_ARG, binding.DSI_ERR_UNSUPPORTED
+    assert _score(L, _cache(), q=None) == E
+    assert _score(L, _cache(), w=None) == E
+    assert _score(L, _cache(), s=None) == E
+    assert _score(L, _cache(), rows=-1) == E
+    assert _score(L, _cache(), heads=0) == U
+    assert _score(L, _cache(), heads=129) == U
+    assert _score(L, _cache(k_idx=None)) == E
+    assert _score(L, _cache(d=12)) == U                       # not a multiple of 8
+    assert _score(L, _cache(k_dtype=1, d=24, k_scale=FAKE)) == U  # fp8 needs multiples of 16
+    assert _score(L, _cache(k_dtype=1)) == E                  # fp8 without scales
+    assert _score(L, _cache(k_dtype=7)) == U
+    assert _score(L, _cache(k_idx=FAKE + 2)) == E             # misaligned
+    assert _score(L, _cache(), rows=3) == E                   # decode rows != batch
+    assert _score(L, _cache(seq_lens=None)) == E
+    assert _score(L, _cache(), ld=1000) == E                  # ld < s_max
+    # prefill: one sequence, q_offset + rows <= s_max
+    assert _score(L, _cache(batch=1), decode=0, rows=8, q_offset=1020, ld=2048) == E
+    assert _score(L, _cache(batch=2), decode=0, rows=8, ld=2048) == E
+    # paged: s_max must be max_pages * page_size, page size a multiple of 8
+    assert _score(L, _cache(block_table=FAKE, page_size=64, max_pages=8, num_pages=10)) == E
+    assert _score(L, _cache(block_table=FAKE, page_size=60, max_pages=16, num_pages=10,
+                            s_max=960), ld=960) == U
+    # zero rows: nothing to launch, success
+    assert _score(L, _cache(batch=0), rows=0) == binding.DSI_OK
+
+
+def test_topk_validation(L):
+    E, U = binding.DSI_ERR_INVALID_ARG, binding.DSI_ERR_UNSUPPORTED
+    assert L.dsi_topk(None, 16, 2, None, 0, 4, FAKE, None, None) == E
+    assert L.dsi_topk(FAKE, 16, 2, None, 0, 0, FAKE, None, None) == E
+    assert L.dsi_topk(FAKE, 16, 2, None, 0, 4, None, None, None) == E
+    assert L.dsi_topk(FAKE, 16, 2, None, -1, 4, FAKE, None, None) == E
+    assert L.dsi_topk(FAKE, 16, 2, None, 0, 4097, FAKE, None, None) == U
+    assert L.dsi_topk(FAKE, 16, 0, None, 0, 4, FAKE, None, None) == binding.DSI_OK
+
+
+def test_mla_validation(L):
+    E, U = binding.DSI_ERR_INVALID_ARG, binding.DSI_ERR_UNSUPPORTED
+    c = _cache()
+    f = L.dsi_sparse_mla_decode
+    assert f(None, ctypes.byref(c), FAKE, 4, 128, 64, 0.1, FAKE, None, None, 0, None) == E
+    assert f(FAKE, ctypes.byref(c), FAKE, 4, 129, 64, 0.1, FAKE, None, None, 0, None) == U
+    assert f(FAKE, ctypes.byref(c), FAKE, 4, 40, 64, 0.1, FAKE, None, None, 0, None) == U
+    assert f(FAKE, ctypes.byref(c), FAKE, 4, 128, 0, 0.1, FAKE, None, None, 0, None) == E
+    assert f(FAKE, ctypes.byref(c), FAKE, 4, 128, 64, float("nan"), FAKE, None, None, 0, None) == E
+    assert f(FAKE, ctypes.byref(_cache(latent=None)), FAKE, 4, 128, 64, 0.1, FAKE, None, None, 0,
+             None) == E
+    assert f(FAKE, ctypes.byref(c), FAKE, 4, 128, 64, 0.1, FAKE, None, FAKE + 16, 1 << 20,
+             None) == E  # workspace not 256-byte aligned
+    g = L.dsi_sparse_mla_prefill
+    assert g(FAKE, ctypes.byref(_cache(batch=1)), FAKE, 8, 128, 64, 1020, 0.1, FAKE, None, None,
+             0, None) == E
+
+
+def test_fused_validation(L):
+    c = _cache()
+    f = L.dsi_indexed_attention
+    args = [FAKE, FAKE, FAKE, ctypes.byref(c), 4, 64, 128, 2048, 0, 0.04, 1, None, None, FAKE,
+            None]
+    assert f(*args, None, 0, None) == binding.DSI_ERR_WORKSPACE
+    assert f(*args, FAKE, 16, None) == binding.DSI_ERR_WORKSPACE
+    bad = list(args); bad[7] = 5000
+    assert f(*bad, None, 0, None) == binding.DSI_ERR_UNSUPPORTED
+    bad = list(args); bad[2] = None
+    assert f(*bad, None, 0, None) == binding.DSI_ERR_INVALID_ARG
+
+
+def test_workspace_size(L):
+    a = L.dsi_workspace_size(64, 64, 128, 2048, 32768, 1)
+    # at least the fp32 score rows and the index rows
+    assert a >= 64 * 32768 * 4 + 64 * 2048 * 4
+    assert L.dsi_workspace_size(64, 64, 128, 2048, 65536, 1) > a
+    assert L.dsi_workspace_size(0, 64, 128, 2048, 32768, 1) == 256

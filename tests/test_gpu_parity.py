@@ -1,0 +1,205 @@
+"""CUDA path (through the C ABI) against the CPU oracle on seeded inputs at
+sizes the oracle finishes in seconds: several tiles, ragged tails, paged and
+FP8 caches, prefill with offsets, and the degenerate cases."""
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from indexed_sparse_attention_indexer_gb300 import binding
+from indexed_sparse_attention_indexer_gb300 import workloads as W
+from tests.parity import assert_lse_close, assert_out_close
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+DECODE_CASES = {
+    # name: (B, lengths, H_i, d, K, H, page, fp8, extra)
+    "small_heads_d64": (3, [300, 77, 1], 4, 64, 32, 16, 0, False, {}),
+    "small_heads_d128": (2, [513, 1000], 2, 128, 100, 16, 0, False, {}),
+    "hi64_d128_h128": (4, [700, 129, 64, 1000], 64, 128, 64, 128, 0, False, {}),
+    "hi64_ragged_tiles": (3, [4097, 127, 2049], 64, 128, 256, 128, 0, False, {}),
+    "paged_bf16": (3, [650, 64, 1], 64, 128, 128, 128, 64, False, {}),
+    "paged_fp8": (4, [1100, 300, 65, 2], 64, 128, 128, 128, 64, True, {}),
+    "paged_fp8_small_heads": (2, [333, 90], 4, 64, 40, 16, 16, True, {}),
+    "k_ge_history": (2, [200, 31], 4, 64, 512, 16, 0, False, {}),
+    "heads_8": (2, [100, 257], 4, 64, 16, 8, 0, False, {}),
+    "heads_48_hi16": (2, [300, 90], 16, 64, 50, 48, 0, False, {}),
+    "softmax_stress": (2, [400, 150], 4, 64, 64, 16, 0, False, {"q_std": 1.0, "scale": 1.0}),
+}
+
+
+def _decode(name):
+    B, lens, Hi, d, K, H, page, fp8, extra = DECODE_CASES[name]
+    return W.make_decode(B, max(lens), Hi, d, K, H, seed=zlib.crc32(name.encode()) % 1000, lengths=lens,
+                         page_size=page, k_fp8=fp8, **extra)
+
+
+def _check_scores(ws, g, cache):
+    decode = ws.mode == "decode"
+    scores = binding.index_score(g.q_idx, g.w, cache, decode, ws.q_offset)
+    torch.cuda.synchronize()
+    sc = scores.cpu().numpy()
+    for r in range(ws.T):
+        ref = oracle.row_scores(ws, r).astype(np.float32)
+        n = ref.shape[0]
+        assert np.array_equal(sc[r, :n], ref), f"scores differ in row {r}"
+    return scores
+
+
+@pytest.mark.parametrize("name", sorted(DECODE_CASES))
+def test_decode_entry_points(name):
+    ws = _decode(name)
+    g = ws.to(DEV)
+    cache = binding.Cache.of(g)
+    scores = _check_scores(ws, g, cache)
+    idx, count = binding.topk(scores, ws.K, row_len=g.seq_lens)
+    ref = oracle.layer(ws)
+    idx_h, cnt_h = idx.cpu().numpy(), count.cpu().numpy()
+    for b in range(ws.B):
+        assert np.array_equal(idx_h[b], ref[b]["idx"]), f"indices differ, row {b}"
+        assert cnt_h[b] == ref[b]["count"]
+    # attention core on the oracle's own indices
+    ref_idx = torch.tensor(np.stack([ref[b]["idx"] for b in range(ws.B)]), dtype=torch.int32,
+                           device=DEV)
+    out, lse = binding.sparse_mla_decode(g.q, cache, ref_idx, ws.scale)
+    torch.cuda.synchronize()
+    assert_out_close(out.float().cpu().numpy(), np.stack([ref[b]["out"] for b in range(ws.B)]), name)
+    assert_lse_close(lse.cpu().numpy(), np.stack([ref[b]["lse"] for b in range(ws.B)]), name)
+    assert binding.device_status() == 0
+
+
+@pytest.mark.parametrize("name", sorted(DECODE_CASES))
+def test_decode_fused(name):
+    ws = _decode(name)
+    g = ws.to(DEV)
+    out, lse, idx, count = binding.layer(g)
+    torch.cuda.synchronize()
+    ref = oracle.layer(ws)
+    for b in range(ws.B):
+        assert np.array_equal(idx[b].cpu().numpy(), ref[b]["idx"]), f"row {b}"
+        assert int(count[b]) == ref[b]["count"]
+    assert_out_close(out.float().cpu().numpy(), np.stack([ref[b]["out"] for b in range(ws.B)]), name)
+    assert_lse_close(lse.cpu().numpy(), np.stack([ref[b]["lse"] for b in range(ws.B)]), name)
+    assert binding.device_status() == 0
+
+
+PREFILL_CASES = {
+    # name: (T, S, q_offset, H_i, d, K, H)
+    "from_start_small_heads": (130, 130, 0, 4, 64, 32, 16),
+    "offset_hi64": (200, 400, 150, 64, 128, 64, 128),
+    "from_start_hi64": (300, 300, 0, 64, 128, 128, 128),
+    "k_ge_history": (70, 100, 20, 4, 64, 128, 16),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_CASES))
+def test_prefill(name):
+    T, S, off, Hi, d, K, H = PREFILL_CASES[name]
+    ws = W.make_prefill(T, S, Hi, d, K, H, seed=5, q_offset=off)
+    g = ws.to(DEV)
+    cache = binding.Cache.of(g)
+    scores = _check_scores(ws, g, cache)
+    idx, count = binding.topk(scores, K, q_offset=off)
+    ref = oracle.layer(ws)
+    idx_h = idx.cpu().numpy()
+    for t in range(T):
+        assert np.array_equal(idx_h[t], ref[t]["idx"]), f"row {t}"
+        sel = idx_h[t][idx_h[t] >= 0]
+        assert sel.max() <= off + t          # causality
+    ref_idx = torch.tensor(np.stack([ref[t]["idx"] for t in range(T)]), dtype=torch.int32,
+                           device=DEV)
+    out, lse = binding.sparse_mla_prefill(g.q, cache, ref_idx, off, ws.scale)
+    ref_out = np.stack([ref[t]["out"] for t in range(T)])
+    assert_out_close(out.float().cpu().numpy(), ref_out, name)
+    out2, lse2, idx2, _ = binding.layer(g)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx2.cpu().numpy(), idx_h)
+    assert_out_close(out2.float().cpu().numpy(), ref_out, name + " fused")
+    assert_lse_close(lse2.cpu().numpy(), np.stack([ref[t]["lse"] for t in range(T)]), name)
+    assert binding.device_status() == 0
+
+
+def test_prefill_chunk_invariance():
+    """A prefill split into query chunks gives the same indices (and outputs) as one call."""
+    T, S, Hi, d, K, H = 256, 256, 64, 128, 64, 128
+    ws = W.make_prefill(T, S, Hi, d, K, H, seed=9)
+    g = ws.to(DEV)
+    out, _, idx, _ = binding.layer(g)
+    for c0 in (0, 96, 200):
+        c1 = min(T, c0 + 96)
+        sub = g.to(DEV)
+        sub.q_idx, sub.w, sub.q, sub.q_offset = g.q_idx[c0:c1], g.w[c0:c1], g.q[c0:c1], c0
+        o2, _, i2, _ = binding.layer(sub)
+        torch.cuda.synchronize()
+        assert torch.equal(i2, idx[c0:c1])
+        d = (o2.float() - out[c0:c1].float()).abs().max().item()
+        assert d <= 1e-2 * out.float().abs().max().item()
+
+
+TOPK_CASES = [
+    # rows, ld, K, value levels (ties), with -inf, staged in shared memory?
+    (5, 1000, 7, 4, False),
+    (3, 5000, 2048, 16, True),
+    (2, 50000, 2048, 1000, True),     # longer than the shared-memory stage
+    (4, 33000, 1, 3, False),
+    (3, 600, 600, 5, False),          # K == n
+    (2, 70000, 4096, 1 << 20, False),
+]
+
+
+@pytest.mark.parametrize("case", TOPK_CASES, ids=[str(c) for c in TOPK_CASES])
+def test_topk_ties_and_lengths(case):
+    rows, ld, K, levels, with_inf = case
+    gen = torch.Generator().manual_seed(rows * 1000 + K)
+    sc = torch.randint(0, levels, (rows, ld), generator=gen).float() / 8 - levels / 16
+    if with_inf:
+        sc[:, ::7] = -math.inf
+    lens = torch.randint(1, ld + 1, (rows,), generator=gen).to(torch.int32)
+    lens[0] = ld
+    g = sc.to(DEV)
+    idx, count = binding.topk(g, K, row_len=lens.to(DEV))
+    torch.cuda.synchronize()
+    for r in range(rows):
+        n = int(lens[r])
+        exp, cnt = oracle.topk_select(sc[r, :n].numpy(), K)
+        assert np.array_equal(idx[r].cpu().numpy(), exp), f"row {r}"
+        assert int(count[r]) == cnt
+
+
+def test_topk_negative_zero_ties_positive_zero():
+    sc = torch.zeros((1, 64))
+    sc[0, ::2] = -0.0
+    g = sc.to(DEV)
+    idx, _ = binding.topk(g, 5, row_len=torch.tensor([64], dtype=torch.int32, device=DEV))
+    assert idx[0].tolist() == [0, 1, 2, 3, 4]
+
+
+def test_zeroed_head_weight_matches_removed_head():
+    ws = _decode("hi64_d128_h128")
+    g = ws.to(DEV)
+    w0 = g.w.clone()
+    w0[:, 5] = 0
+    s0 = binding.index_score(g.q_idx, w0, binding.Cache.of(g), True)
+    keep = [h for h in range(64) if h != 5]
+    s1 = binding.index_score(g.q_idx[:, keep].contiguous(), g.w[:, keep].contiguous(),
+                             binding.Cache.of(g), True)
+    torch.cuda.synchronize()
+    for b in range(ws.B):
+        n = int(ws.seq_lens[b])
+        assert torch.equal(s0[b, :n], s1[b, :n])
+
+
+def test_checked_build_flags_out_of_range_index():
+    """With the bounds-checked library an index >= seq_len is skipped and reported."""
+    ws = _decode("small_heads_d64")
+    g = ws.to(DEV)
+    idx = torch.zeros((ws.B, 4), dtype=torch.int32, device=DEV)
+    idx[1, 2] = int(ws.seq_lens[1]) + 5     # beyond the history, inside the allocation
+    binding.sparse_mla_decode(g.q, binding.Cache.of(g), idx, ws.scale, checked=True)
+    assert binding.device_status(checked=True) == binding.DSI_ERR_BOUNDS
+    assert binding.device_status(checked=True) == 0   # read clears it
