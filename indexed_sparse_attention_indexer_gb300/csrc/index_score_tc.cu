@@ -1,13 +1,515 @@
-// Indexer scoring on tcgen05 tensor cores (placeholder until the kernel lands).
+// Indexer scoring on the tcgen05 tensor cores (64 indexer heads x 128 dims).
+//
+// ("Day 0 Inference Support for New LLM Architectures: Optimization
+// Practices", "Internal Fusion of the Indexer": relevance scoring then the
+// weighted sum over heads, reading the paged K cache directly.)
+//
+// One tile is a GEMM D[128 positions x N] = K_tile[128 x 128] . Q^T with
+// N = 64 heads x NT query tokens, accumulated in fp32 in TMEM:
+//  * A (index keys) streams through a ring of shared-memory stages filled by
+//    TMA (128-byte swizzle); paged caches are read page by page through the
+//    block table (64-position sub-tiles, so any page size that is a multiple
+//    of 64 works).
+//  * B (the index queries of the current group of NT tokens) stays resident
+//    in one of two shared-memory slots while its tiles stream by.
+//  * the epilogue warps read one TMEM lane (= one position) per thread,
+//    apply the ReLU gate and the per-token head weights, sum over heads and
+//    (FP8 keys) multiply by the token's key scale.  Every head sum is
+//    thread-local: no shuffles.
+// Roles: warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer, the rest =
+// epilogue.  Two TMEM accumulators let the epilogue of tile i overlap the MMA
+// of tile i+1.  Work = (group, tile) items in causal order, split into equal
+// contiguous ranges over one CTA per SM, so causal prefill rows balance
+// without a special order.  FP8 keys use kind::f8f6f4 with the queries
+// rounded to E4M3 (exact for the integer-valued index queries).
+#include <cudaTypedefs.h>
+
 #include "kernels.h"
+#include "tc_common.cuh"
 
 namespace dsi {
+using namespace tc;
 
-bool tc_score_supported(const CacheView&, int) { return false; }
+namespace {
 
-cudaError_t launch_index_score_tc(const bf16*, const float*, const CacheView&, int, int, int64_t,
-                                  float*, int64_t, int*, cudaStream_t) {
-  return cudaErrorInvalidValue;
+constexpr int kD = 128;          // index key width
+constexpr int kHeads = 64;       // indexer heads
+constexpr int kTileM = 128;      // positions per tile
+constexpr int kSub = 64;         // positions per TMA sub-tile
+constexpr int kMaxGroups = 2048;
+
+template <int NT, bool FP8>
+struct Cfg {
+  static constexpr int N = NT * kHeads;
+  static constexpr int EB = FP8 ? 1 : 2;                  // key/query element bytes
+  static constexpr int A_BYTES = kTileM * kD * EB;        // 16 or 32 KB
+  static constexpr int B_BYTES = N * kD * EB;
+  static constexpr int STAGES = FP8 ? 8 : (NT == 1 ? 4 : 2);
+  static constexpr int EPI_WARPS = NT == 1 ? 4 : 8;
+  static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr int THREADS = 64 + EPI_THREADS;
+  static constexpr int TMEM_COLS = 2 * N <= 128 ? 128 : (2 * N <= 256 ? 256 : 512);
+  static constexpr int KSTEPS = FP8 ? 4 : 8;              // 32 bytes of K per MMA
+  static constexpr uint32_t IDESC = idesc_f32(FP8 ? 0u : 1u, kTileM, N);
+  static constexpr int TOK_PER_THREAD = NT == 1 ? 1 : NT / 2;   // epilogue column split
+  // shared memory carve (offsets from a 1024-aligned base)
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_W = OFF_B + 2 * B_BYTES;                 // 2 x NT x 64 fp32
+  static constexpr int OFF_PREFIX = OFF_W + 2 * NT * kHeads * 4;    // kMaxGroups+1 int32
+  static constexpr int OFF_BAR = (OFF_PREFIX + (kMaxGroups + 1) * 4 + 7) & ~7;
+  static constexpr int NBARS = 2 * STAGES + 2 + 2 + 2 + 2 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8 + 8;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;                 // + alignment slack
+};
+
+struct ScoreArgs {
+  const bf16* q_idx;
+  const float* w;
+  float* scores;
+  int64_t ld;
+  int64_t q_offset;
+  int rows;      // query rows (decode: sequences)
+  int groups;
+  int decode;
+};
+
+// Tiles of group g (decode: sequence g; prefill: tokens g*NT .. g*NT+NT-1).
+template <int NT>
+__device__ __forceinline__ int group_tiles(const CacheView& c, const ScoreArgs& a, int g) {
+  int64_t n;
+  if (a.decode) {
+    n = visible_len(c, g, 1, 0);
+  } else {
+    const int last = min(a.rows, (g + 1) * NT) - 1;
+    n = a.q_offset + last + 1;
+  }
+  return (int)((n + kTileM - 1) / kTileM);
+}
+
+// Walks the CTA's contiguous range of (group, tile) items.
+struct ItemIter {
+  int g, j, left;
+  const int* prefix;
+  int groups;
+  __device__ void init(const int* pre, int G, int64_t begin, int64_t end) {
+    prefix = pre;
+    groups = G;
+    left = (int)(end - begin);
+    // largest g with prefix[g] <= begin
+    int lo = 0, hi = G;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= begin) lo = mid; else hi = mid;
+    }
+    g = lo;
+    j = (int)(begin - prefix[g]);
+    skip_empty();
+  }
+  __device__ void skip_empty() {
+    while (g < groups && prefix[g] + j >= prefix[g + 1]) { ++g; j = 0; }
+  }
+  __device__ bool valid() const { return left > 0; }
+  __device__ void next() {
+    --left;
+    ++j;
+    skip_empty();
+  }
+  // group of the item after the current one (or -1 when none)
+  __device__ int next_group() const {
+    if (left <= 1) return -1;
+    int gg = g, jj = j + 1;
+    while (gg < groups && prefix[gg] + jj >= prefix[gg + 1]) { ++gg; jj = 0; }
+    return gg;
+  }
+};
+
+__device__ __forceinline__ void bar_sync_named(int id, int count) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+
+template <int NT, bool FP8>
+__global__ void __launch_bounds__(Cfg<NT, FP8>::THREADS, 1)
+score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+         CacheView c, ScoreArgs a, int* err) {
+  using C = Cfg<NT, FP8>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  float* wbuf = reinterpret_cast<float*>(smem + C::OFF_W);
+  int* prefix = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* acc_full = bars + 2 * C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* q_full = acc_empty + 2;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* done_bar = q_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  __shared__ int scan_tmp[40];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- per-CTA set-up: tile prefix over groups, barriers, TMEM --------------
+  {
+    const int G = a.groups;
+    const int per = (G + C::THREADS - 1) / C::THREADS;
+    const int g0 = min(G, tid * per), g1 = min(G, g0 + per);
+    int mine = 0;
+    for (int g = g0; g < g1; ++g) mine += group_tiles<NT>(c, a, g);
+    int total;
+    int run = block_exclusive_scan(mine, scan_tmp, total);
+    for (int g = g0; g < g1; ++g) {
+      prefix[g] = run;
+      run += group_tiles<NT>(c, a, g);
+    }
+    if (tid == 0) prefix[G] = total;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], C::EPI_THREADS);
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int64_t total_items = prefix[a.groups];
+  const int64_t it_begin = total_items * blockIdx.x / gridDim.x;
+  const int64_t it_end = total_items * (blockIdx.x + 1) / gridDim.x;
+
+  if (warp == 0) {
+    // ======================= TMA producer ====================================
+    ItemIter it;
+    it.init(prefix, a.groups, it_begin, it_end);
+    int gprev = -1, qcount = 0, stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_phase[C::STAGES];
+    bool issued[C::STAGES];
+#pragma unroll
+    for (int s = 0; s < C::STAGES; ++s) { issued[s] = false; issued_phase[s] = 0; }
+    if (lane == 0) { prefetch_tmap(&kmap); if (!FP8) prefetch_tmap(&qmap); }
+    while (it.valid() && !*abort_flag) {
+      const int g = it.g, j = it.j;
+      if (g != gprev) {
+        const int slot = qcount & 1;
+        const uint32_t qph = (qcount >> 1) & 1;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&q_empty[slot], qph ^ 1, abort_flag, err);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        uint8_t* qs = smem + C::OFF_B + slot * C::B_BYTES;
+        if (FP8) {
+          // round the bf16 index queries to E4M3 into the swizzled B slot
+          for (int i = lane; i < C::N * 8; i += 32) {
+            const int n = i >> 3, u = i & 7;
+            const int t = n / kHeads, h = n % kHeads;
+            const int r = a.decode ? g : g * NT + t;
+            uint4 outv = make_uint4(0, 0, 0, 0);
+            if (r < a.rows) {
+              const bf16* src = a.q_idx + ((int64_t)r * kHeads + h) * kD + u * 16;
+              const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(src));
+              const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(src + 8));
+              float f[16];
+              bf16x8_to_f32(v0, f);
+              bf16x8_to_f32(v1, f + 8);
+              uint32_t wds[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const __nv_fp8x2_storage_t lo =
+                    __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k], f[4 * k + 1]), __NV_SATFINITE,
+                                             __NV_E4M3);
+                const __nv_fp8x2_storage_t hi =
+                    __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k + 2], f[4 * k + 3]),
+                                             __NV_SATFINITE, __NV_E4M3);
+                wds[k] = (uint32_t)lo | ((uint32_t)hi << 16);
+              }
+              outv = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+            }
+            *reinterpret_cast<uint4*>(qs + sw128_offset(n, u)) = outv;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&q_full[slot]);
+        } else if (lane == 0) {
+          mbar_arrive_expect_tx(&q_full[slot], C::B_BYTES);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const int r = a.decode ? g : g * NT + t;   // rows past the end read as zeros
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc)
+              tma_load_2d(qs + cc * (C::N * 128) + t * kHeads * 128, &qmap, cc * 64, r * kHeads,
+                          &q_full[slot]);
+          }
+        }
+        __syncwarp();
+        ++qcount;
+        gprev = g;
+      }
+      // ---- one key tile -----------------------------------------------------
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane == 0) {
+        const int b = a.decode ? g : 0;
+        int64_t nvis;
+        if (a.decode) nvis = visible_len(c, g, 1, 0);
+        else nvis = a.q_offset + min(a.rows, (g + 1) * NT);
+        const int64_t p0 = (int64_t)j * kTileM;
+        int64_t prow[2];
+        int nsub = 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int64_t p = p0 + i * kSub;
+          prow[i] = -1;
+          if (p < nvis) { prow[i] = phys_row(c, b, p, err); if (prow[i] >= 0) ++nsub; }
+        }
+        uint8_t* as = smem + C::OFF_A + stage * C::A_BYTES;
+        mbar_arrive_expect_tx(&full[stage], (uint32_t)(nsub * (C::A_BYTES / 2)));
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (prow[i] < 0) continue;
+          if (FP8) {
+            tma_load_2d(as + i * (kSub * 128), &kmap, 0, (int)prow[i], &full[stage]);
+          } else {
+            tma_load_2d(as + i * (kSub * 128), &kmap, 0, (int)prow[i], &full[stage]);
+            tma_load_2d(as + 16384 + i * (kSub * 128), &kmap, 64, (int)prow[i], &full[stage]);
+          }
+        }
+        issued[stage] = true;
+        issued_phase[stage] = phase;
+      }
+      if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+      it.next();
+    }
+    // never leave the CTA with a TMA copy still landing in shared memory
+    if (lane == 0 && *abort_flag) {
+      for (int s = 0; s < C::STAGES; ++s)
+        if (issued[s]) mbar_wait(&full[s], issued_phase[s], abort_flag, err, 100000000ull);
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================================
+    if (lane == 0) {
+      ItemIter it;
+      it.init(prefix, a.groups, it_begin, it_end);
+      int gprev = -1, qcount = 0, stage = 0, abuf = 0, slot = 0;
+      uint32_t phase = 0, aph = 0;
+      while (it.valid()) {
+        const int g = it.g;
+        if (g != gprev) {
+          slot = qcount & 1;
+          if (!mbar_wait(&q_full[slot], (qcount >> 1) & 1, abort_flag, err)) break;
+          ++qcount;
+          gprev = g;
+        }
+        if (!mbar_wait(&full[stage], phase, abort_flag, err)) break;
+        if (!mbar_wait(&acc_empty[abuf], aph ^ 1, abort_flag, err)) break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(smem + C::OFF_A + stage * C::A_BYTES);
+        const uint32_t b_base = smem_u32(smem + C::OFF_B + slot * C::B_BYTES);
+        const uint32_t d_tmem = tmem + abuf * C::N;
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS; ++k) {
+          uint32_t ao, bo;
+          if (FP8) { ao = k * 32; bo = k * 32; }
+          else { ao = (k >> 2) * 16384 + (k & 3) * 32; bo = (k >> 2) * (C::N * 128) + (k & 3) * 32; }
+          const uint64_t ad = desc_sw128(a_base + ao);
+          const uint64_t bd = desc_sw128(b_base + bo);
+          if (FP8) mma_fp8(d_tmem, ad, bd, C::IDESC, k > 0);
+          else mma_bf16(d_tmem, ad, bd, C::IDESC, k > 0);
+        }
+        mma_commit(&empty[stage]);
+        mma_commit(&acc_full[abuf]);
+        if (it.next_group() != g) mma_commit(&q_empty[slot]);
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        if (++abuf == 2) { abuf = 0; aph ^= 1; }
+        it.next();
+      }
+      // all MMAs of this CTA complete before TMEM is released
+      mma_commit(done_bar);
+      mbar_wait(done_bar, 0, abort_flag, err, 100000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ======================= epilogue =========================================
+    const int ew = warp - 2;                 // 0 .. EPI_WARPS-1
+    const int quarter = warp & 3;            // TMEM lane quarter this warp may read
+    const int half = ew / 4;                 // column half (8-warp epilogue)
+    const int et = tid - 64;
+    const int row = quarter * 32 + lane;     // position within the tile
+    ItemIter it;
+    it.init(prefix, a.groups, it_begin, it_end);
+    int gprev = -1, gcount = 0, abuf = 0;
+    uint32_t aph = 0;
+    const float* wg = wbuf;
+    while (it.valid()) {
+      const int g = it.g, j = it.j;
+      if (g != gprev) {
+        // head weights of the new group into the slot the previous group did not use
+        float* wn = wbuf + (gcount & 1) * NT * kHeads;
+        for (int i = et; i < NT * kHeads; i += C::EPI_THREADS) {
+          const int t = i / kHeads, h = i % kHeads;
+          const int r = a.decode ? g : g * NT + t;
+          wn[i] = r < a.rows ? __ldg(a.w + (int64_t)r * kHeads + h) : 0.f;
+        }
+        bar_sync_named(1, C::EPI_THREADS);
+        wg = wn;
+        ++gcount;
+        gprev = g;
+      }
+      if (!mbar_wait(&acc_full[abuf], aph, abort_flag, err)) break;
+      tc_fence_after();
+      constexpr int TPT = C::TOK_PER_THREAD;
+      float v[TPT][kHeads];
+#pragma unroll
+      for (int tt = 0; tt < TPT; ++tt) {
+        const int t = half * TPT + tt;
+        const uint32_t col = abuf * C::N + t * kHeads;
+        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + col;
+        tmem_ld32(taddr, v[tt]);
+        tmem_ld32(taddr + 32, v[tt] + 32);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&acc_empty[abuf]);
+      const int b = a.decode ? g : 0;
+      const int64_t p = (int64_t)j * kTileM + row;
+#pragma unroll
+      for (int tt = 0; tt < TPT; ++tt) {
+        const int t = half * TPT + tt;
+        const int r = a.decode ? g : g * NT + t;
+        if (r >= a.rows) continue;
+        const int64_t nvis = a.decode ? visible_len(c, g, 1, 0) : a.q_offset + r + 1;
+        if (p >= nvis) continue;
+        const float* wt = wg + t * kHeads;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < kHeads; h += 2) {
+          s0 = fmaf(wt[h], fmaxf(v[tt][h], 0.f), s0);
+          s1 = fmaf(wt[h + 1], fmaxf(v[tt][h + 1], 0.f), s1);
+        }
+        float s = s0 + s1;
+        if (FP8) {
+          const int64_t pr = phys_row(c, b, p, err);
+          if (pr >= 0) s *= __ldg(c.k_scale + pr);
+        }
+        a.scores[(int64_t)r * a.ld + p] = s;
+      }
+      if (++abuf == 2) { abuf = 0; aph ^= 1; }
+      it.next();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2D map over a row-major [rows, cols] array, box [box_rows, box_cols], 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t rows,
+              uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * (cuuint64_t)esize};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NT, bool FP8>
+cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, int decode,
+               int64_t q_offset, float* scores, int64_t ld, int* err, cudaStream_t st) {
+  using C = Cfg<NT, FP8>;
+  const uint64_t krows = c.block_table ? (uint64_t)c.num_pages * c.page_size
+                                       : (uint64_t)c.batch * c.s_max;
+  CUtensorMap kmap, qmap;
+  memset(&qmap, 0, sizeof(qmap));
+  if (FP8) {
+    if (!make_map(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, krows, kD, 128, kSub))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!make_map(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, krows, kD, 64, kSub))
+      return cudaErrorInvalidValue;
+    if (!make_map(&qmap, q_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)rows * kHeads, kD,
+                  64, kHeads))
+      return cudaErrorInvalidValue;
+  }
+  ScoreArgs a;
+  a.q_idx = q_idx;
+  a.w = w;
+  a.scores = scores;
+  a.ld = ld;
+  a.q_offset = q_offset;
+  a.rows = rows;
+  a.decode = decode;
+  a.groups = decode ? rows : (rows + NT - 1) / NT;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = cudaFuncSetAttribute(score_tc<NT, FP8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  score_tc<NT, FP8><<<sms, C::THREADS, C::SMEM, st>>>(kmap, qmap, c, a, err);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_score_supported(const CacheView& c, int H) {
+  if (H != kHeads || c.d != kD) return false;
+  if (c.block_table && c.page_size % kSub != 0) return false;
+  const uint64_t krows = c.block_table ? (uint64_t)c.num_pages * c.page_size
+                                       : (uint64_t)c.batch * c.s_max;
+  if (krows >= (1ull << 31)) return false;
+  if ((reinterpret_cast<uintptr_t>(c.k_idx) & 15) != 0) return false;
+  return get_encode() != nullptr;
+}
+
+bool tc_score_shape_ok(int rows, int decode) {
+  const int groups = decode ? rows : (rows + 3) / 4;
+  return groups <= kMaxGroups && (int64_t)rows * kHeads < (1ll << 31);
+}
+
+cudaError_t launch_index_score_tc(const bf16* q_idx, const float* w, const CacheView& c, int rows,
+                                  int decode, int64_t q_offset, float* scores, int64_t ld,
+                                  int* err, cudaStream_t st) {
+  const bool fp8 = c.k_dtype == DSI_FP8_E4M3;
+  if (decode) {
+    return fp8 ? go<1, true>(q_idx, w, c, rows, 1, 0, scores, ld, err, st)
+               : go<1, false>(q_idx, w, c, rows, 1, 0, scores, ld, err, st);
+  }
+  return fp8 ? go<4, true>(q_idx, w, c, rows, 0, q_offset, scores, ld, err, st)
+             : go<4, false>(q_idx, w, c, rows, 0, q_offset, scores, ld, err, st);
 }
 
 }  // namespace dsi

@@ -30,6 +30,11 @@ DECODE_CASES = {
     "heads_8": (2, [100, 257], 4, 64, 16, 8, 0, False, {}),
     "heads_48_hi16": (2, [300, 90], 16, 64, 50, 48, 0, False, {}),
     "softmax_stress": (2, [400, 150], 4, 64, 64, 16, 0, False, {"q_std": 1.0, "scale": 1.0}),
+    "hi64_fp8_contiguous": (3, [900, 129, 2], 64, 128, 100, 128, 0, True, {}),
+    "hi64_paged_page128": (3, [1000, 128, 300], 64, 128, 200, 128, 128, False, {}),
+    "hi64_paged_page16_generic": (2, [333, 40], 64, 128, 64, 128, 16, False, {}),
+    "zero_length_sequence": (3, [100, 0, 5], 64, 128, 16, 128, 0, False, {}),
+    "zero_length_paged_fp8": (3, [0, 70, 200], 64, 128, 16, 128, 64, True, {}),
 }
 
 
@@ -94,6 +99,8 @@ PREFILL_CASES = {
     "offset_hi64": (200, 400, 150, 64, 128, 64, 128),
     "from_start_hi64": (300, 300, 0, 64, 128, 128, 128),
     "k_ge_history": (70, 100, 20, 4, 64, 128, 16),
+    "ragged_groups_hi64": (130, 333, 203, 64, 128, 100, 128),   # T not a multiple of 4
+    "single_token_hi64": (1, 50, 49, 64, 128, 8, 128),
 }
 
 
