@@ -194,6 +194,31 @@ dsi_status dsi_indexed_attention(const void* q_idx, const float* w, const void* 
                                  void* out, float* lse, void* workspace, size_t workspace_bytes,
                                  void* stream);
 
+/*
+ * dsi_indexed_attention_static — dsi_indexed_attention for callers that
+ * cannot allocate device memory.  The pages have no counterpart: this entry
+ * exists for callers such as a plugin inside a runtime that owns every device
+ * allocation and offers its kernels no scratch, or a latency-critical path
+ * that cannot afford cudaMalloc's implicit device synchronisation.
+ *
+ * Same arguments and results as dsi_indexed_attention, minus the workspace:
+ * the scratch (score rows, indices, split-K partials) lives in one device
+ * array of DSI_STATIC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library keeps until the process exits.  The caller still owns
+ * inputs and outputs.  Returns DSI_ERR_WORKSPACE, before launching anything,
+ * when dsi_workspace_size() for the call exceeds DSI_STATIC_SCRATCH_BYTES.
+ * The first call on a device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * All calls share the array: calls whose kernels overlap on the GPU race.
+ * Nothing in the array needs to start at zero.  Allocates nothing.
+ */
+#define DSI_STATIC_SCRATCH_BYTES (16u << 20)
+dsi_status dsi_indexed_attention_static(const void* q_idx, const float* w, const void* q,
+                                        const dsi_cache* cache, int32_t rows, int32_t n_heads_idx,
+                                        int32_t n_heads, int32_t K, int64_t q_offset, float scale,
+                                        int32_t decode, int32_t* idx_out, int32_t* count_out,
+                                        void* out, float* lse, void* stream);
+
 /* Bytes of workspace dsi_indexed_attention needs (and the larger, split-K
  * sizing of the dsi_sparse_mla_* calls when n_heads_idx == 0 and s_max == 0). */
 size_t dsi_workspace_size(int32_t rows, int32_t n_heads_idx, int32_t n_heads, int32_t K,

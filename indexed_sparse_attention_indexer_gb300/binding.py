@@ -49,6 +49,10 @@ SIGNATURES = {
                                         c_int32, c_int32, c_int32, c_int32, c_int64, c_float,
                                         c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
                                         c_void_p, c_size_t, c_void_p]),
+    "dsi_indexed_attention_static": (c_int32, [c_void_p, c_void_p, c_void_p,
+                                               ctypes.POINTER(DsiCache), c_int32, c_int32,
+                                               c_int32, c_int32, c_int64, c_float, c_int32,
+                                               c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dsi_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int64, c_int32]),
     "dsi_get_device_status": (c_int32, [c_void_p]),
     "dsi_status_string": (ctypes.c_char_p, [c_int32]),
