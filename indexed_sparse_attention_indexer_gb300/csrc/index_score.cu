@@ -17,13 +17,18 @@
 namespace dsi {
 
 template <typename KT> struct KeyTraits;
+// kPerChunk: key elements per 16-byte load.  query(): the value an index
+// query element takes part in the dot product with (with FP8 keys the index
+// query is quantised to E4M3 as well).
 template <> struct KeyTraits<bf16> {
-  static constexpr int kPerChunk = 8;  // elements per 16-byte load
+  static constexpr int kPerChunk = 8;
   __device__ static void unpack(const uint4& v, float* f) { bf16x8_to_f32(v, f); }
+  __device__ static float query(float x) { return x; }
 };
 template <> struct KeyTraits<__nv_fp8_e4m3> {
   static constexpr int kPerChunk = 16;
   __device__ static void unpack(const uint4& v, float* f) { fp8x16_to_f32(v, f); }
+  __device__ static float query(float x) { return static_cast<float>(__nv_fp8_e4m3(x)); }
 };
 
 constexpr int kStreamWarps = 8;
@@ -52,6 +57,8 @@ score_stream(const bf16* __restrict__ q_idx, const float* __restrict__ w, CacheV
       uint4 v = *reinterpret_cast<const uint4*>(qp + e);
       bf16x8_to_f32(v, &qr[h][e]);
     }
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) qr[h][e] = KeyTraits<KT>::query(qr[h][e]);
     wr[h] = w[(int64_t)r * HI + h];
   }
   const KT* kbase = reinterpret_cast<const KT*>(c.k_idx);
@@ -106,7 +113,7 @@ score_simt(const bf16* __restrict__ q_idx, const float* __restrict__ w, CacheVie
   const int b = decode ? r : 0;
   const int64_t n = visible_len(c, r, decode, q_offset);
   for (int i = threadIdx.x; i < H * D; i += blockDim.x)
-    qs[i] = __bfloat162float(q_idx[(int64_t)r * H * D + i]);
+    qs[i] = KeyTraits<KT>::query(__bfloat162float(q_idx[(int64_t)r * H * D + i]));
   for (int i = threadIdx.x; i < H; i += blockDim.x) ws[i] = w[(int64_t)r * H + i];
   __syncthreads();
   constexpr int EPC = KeyTraits<KT>::kPerChunk;

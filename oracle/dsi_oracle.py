@@ -25,7 +25,9 @@ Readings where the pages are silent (each also listed in the design notes):
   with at most K candidates keep all of them; the selected positions are
   reported in ascending order, padded with -1.
 * FP8 index keys carry one scale per token; the oracle dequantises each
-  element (key * scale) before the dot product.
+  element (key * scale) before the dot product, and the index query takes
+  part rounded to E4M3 (the index path quantises both index Q and K, "Day 0
+  Inference Support...", "A Layered Strategy").
 * Attention core = absorbed MLA: the key of a position is its whole 576-wide
   latent row (512 latent + 64 rope), the value is the first 512 dims; logits
   are ``scale * q . c``, softmax over the selected positions, ``lse`` is the
@@ -60,16 +62,26 @@ def _f64(x) -> np.ndarray:
 # sum over heads)
 # ----------------------------------------------------------------------------
 
+def e4m3_round(x) -> np.ndarray:
+    """Round to the nearest FP8 E4M3 value (ties to even), saturating at +-448."""
+    import torch
+    t = torch.as_tensor(np.clip(_f64(x), -448.0, 448.0))
+    return t.to(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
 def index_scores(q_idx, w, k_rows, k_scale=None) -> np.ndarray:
     """Indexer score of each given history row for one query token.
 
     q_idx [H_i, d], w [H_i], k_rows [n, d], k_scale [n] or None -> I [n] fp64:
         I[s] = sum_h w[h] * max(0, sum_j q_idx[h, j] * k[s, j]),
     with k = k_rows * k_scale[s] when the keys are quantised (dequantise first).
+    With quantised (FP8) keys the index query takes part in E4M3 as well: the
+    index path quantises both index Q and K.
     """
     q = _f64(q_idx)
     k = _f64(k_rows)
     if k_scale is not None:
+        q = e4m3_round(q)
         k = k * _f64(k_scale)[:, None]
     u = k @ q.T                       # relevance of row s for indexer head h: [n, H_i]
     gated = np.maximum(u, 0.0)        # ReLU gate

@@ -113,6 +113,18 @@ def check_scores_fp8_scale(o):
     assert np.array_equal(o.index_scores(q, w, k, np.ones(n)), o.index_scores(q, w, k))
 
 
+def check_scores_fp8_query_rounding(o):
+    """With FP8 keys the query is rounded to E4M3: values from the format's definition
+    (3 mantissa bits; 0.1 -> 13/128; 0.3 -> 5/16; 449 -> 448 saturated)."""
+    k = np.array([[1.0]])
+    for qv, exp in [(0.1, 13 / 128), (0.3, 5 / 16), (3.0, 3.0), (449.0, 448.0), (-0.1, -13 / 128),
+                    (17.0, 16.0), (19.0, 20.0)]:
+        got = o.index_scores(np.array([[qv]]), np.array([1.0]), k, np.array([1.0]))
+        assert got[0] == max(exp, 0.0), (qv, got[0], exp)
+    # without quantised keys the query is used as given
+    assert o.index_scores(np.array([[0.1]]), np.array([1.0]), k)[0] == 0.1
+
+
 def _load_golden_indexer():
     cases = []
     path = os.path.join(GOLDEN, "indexer_tiny.txt")

@@ -186,6 +186,24 @@ def test_topk_negative_zero_ties_positive_zero():
     assert idx[0].tolist() == [0, 1, 2, 3, 4]
 
 
+@pytest.mark.parametrize("heads,d", [(64, 128), (4, 64)])
+def test_fp8_keys_round_queries_to_e4m3(heads, d):
+    """Non-integer index queries with FP8 keys: both sides score with E4M3 queries."""
+    ws = W.make_decode(2, 0, heads, d, 32, 16, seed=31, lengths=[500, 77], page_size=64,
+                       k_fp8=True)
+    gen = torch.Generator().manual_seed(3)
+    ws.q_idx = (torch.randn(ws.q_idx.shape, generator=gen) * 2).to(torch.bfloat16)
+    g = ws.to(DEV)
+    scores = binding.index_score(g.q_idx, g.w, binding.Cache.of(g), True)
+    torch.cuda.synchronize()
+    for b in range(ws.B):
+        n = int(ws.seq_lens[b])
+        ref = oracle.row_scores(ws, b)
+        got = scores[b, :n].cpu().numpy().astype(np.float64)
+        # products are no longer small integers: compare within fp32 summation noise
+        assert np.allclose(got, ref, rtol=1e-5, atol=1e-4 * np.abs(ref).max())
+
+
 def test_zeroed_head_weight_matches_removed_head():
     ws = _decode("hi64_d128_h128")
     g = ws.to(DEV)
