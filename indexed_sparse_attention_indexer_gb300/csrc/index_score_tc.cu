@@ -55,8 +55,8 @@ struct Cfg {
   // shared memory carve (offsets from a 1024-aligned base)
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_W = OFF_B + 2 * B_BYTES;                 // 2 x NT x 64 fp32
-  static constexpr int OFF_PREFIX = OFF_W + 2 * NT * kHeads * 4;    // kMaxGroups+1 int32
+  static constexpr int OFF_W = OFF_B + 2 * B_BYTES;                 // per epilogue warp: its tokens' weights
+  static constexpr int OFF_PREFIX = OFF_W + EPI_WARPS * TOK_PER_THREAD * kHeads * 4;
   static constexpr int OFF_BAR = (OFF_PREFIX + (kMaxGroups + 1) * 4 + 7) & ~7;
   static constexpr int NBARS = 2 * STAGES + 2 + 2 + 2 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8 + 8;
@@ -123,10 +123,6 @@ struct ItemIter {
     return gg;
   }
 };
-
-__device__ __forceinline__ void bar_sync_named(int id, int count) {
-  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
-}
 
 template <int NT, bool FP8>
 __global__ void __launch_bounds__(Cfg<NT, FP8>::THREADS, 1)
@@ -347,31 +343,29 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     const int ew = warp - 2;                 // 0 .. EPI_WARPS-1
     const int quarter = warp & 3;            // TMEM lane quarter this warp may read
     const int half = ew / 4;                 // column half (8-warp epilogue)
-    const int et = tid - 64;
     const int row = quarter * 32 + lane;     // position within the tile
     ItemIter it;
     it.init(prefix, a.groups, it_begin, it_end);
-    int gprev = -1, gcount = 0, abuf = 0;
+    int gprev = -1, abuf = 0;
     uint32_t aph = 0;
-    const float* wg = wbuf;
+    constexpr int TPT = C::TOK_PER_THREAD;
+    // this warp's private copy of the head weights of its tokens (no
+    // cross-warp barrier: a warp that leaves early can never block the others)
+    float* wg = wbuf + ew * TPT * kHeads;
     while (it.valid()) {
       const int g = it.g, j = it.j;
       if (g != gprev) {
-        // head weights of the new group into the slot the previous group did not use
-        float* wn = wbuf + (gcount & 1) * NT * kHeads;
-        for (int i = et; i < NT * kHeads; i += C::EPI_THREADS) {
-          const int t = i / kHeads, h = i % kHeads;
+        __syncwarp();
+        for (int i = lane; i < TPT * kHeads; i += 32) {
+          const int t = half * TPT + i / kHeads, h = i % kHeads;
           const int r = a.decode ? g : g * NT + t;
-          wn[i] = r < a.rows ? __ldg(a.w + (int64_t)r * kHeads + h) : 0.f;
+          wg[i] = r < a.rows ? __ldg(a.w + (int64_t)r * kHeads + h) : 0.f;
         }
-        bar_sync_named(1, C::EPI_THREADS);
-        wg = wn;
-        ++gcount;
+        __syncwarp();
         gprev = g;
       }
-      if (!mbar_wait(&acc_full[abuf], aph, abort_flag, err)) break;
+      if (!warp_wait(&acc_full[abuf], aph, abort_flag, err)) break;
       tc_fence_after();
-      constexpr int TPT = C::TOK_PER_THREAD;
       float v[TPT][kHeads];
 #pragma unroll
       for (int tt = 0; tt < TPT; ++tt) {
@@ -393,7 +387,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         if (r >= a.rows) continue;
         const int64_t nvis = a.decode ? visible_len(c, g, 1, 0) : a.q_offset + r + 1;
         if (p >= nvis) continue;
-        const float* wt = wg + t * kHeads;
+        const float* wt = wg + tt * kHeads;
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int h = 0; h < kHeads; h += 2) {

@@ -31,6 +31,9 @@ cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t
 // ---- sparse MLA ----------------------------------------------------------------
 // part_o / part_ml: split-K partials (may be null when splits == 1).
 size_t mla_partials_bytes(int rows, int n_heads, int splits);
+// Merges split-K partials (unnormalised o, running max m in log2 units, sum l).
+cudaError_t launch_mla_combine(const float* part_o, const float2* part_ml, int rows, int H,
+                               int splits, bf16* out, float* lse, cudaStream_t st);
 int mla_pick_splits(int rows, int n_heads, int K, size_t ws_bytes);
 cudaError_t launch_sparse_mla(const bf16* q, const CacheView& c, const int32_t* idx, int rows,
                               int n_heads, int K, int decode, int64_t q_offset, float scale,

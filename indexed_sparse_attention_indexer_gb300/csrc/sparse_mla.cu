@@ -226,6 +226,13 @@ mla_combine(const float* __restrict__ part_o, const float2* __restrict__ part_ml
   if (lse && tid == 0) lse[(int64_t)r * H + h] = L > 0.f ? (M + log2f(L)) / kLog2e : -INFINITY;
 }
 
+cudaError_t launch_mla_combine(const float* part_o, const float2* part_ml, int rows, int H,
+                               int splits, bf16* out, float* lse, cudaStream_t st) {
+  mla_combine<<<dim3(H, rows), 128, 0, st>>>(part_o, part_ml, H, splits, out, lse);
+  note_launch();
+  return cudaGetLastError();
+}
+
 size_t mla_partials_bytes(int rows, int n_heads, int splits) {
   if (splits <= 1) return 0;
   const size_t n = (size_t)rows * splits * n_heads;

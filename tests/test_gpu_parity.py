@@ -35,6 +35,10 @@ DECODE_CASES = {
     "hi64_paged_page16_generic": (2, [333, 40], 64, 128, 64, 128, 16, False, {}),
     "zero_length_sequence": (3, [100, 0, 5], 64, 128, 16, 128, 0, False, {}),
     "zero_length_paged_fp8": (3, [0, 70, 200], 64, 128, 16, 128, 64, True, {}),
+    "softmax_stress_h128": (2, [3000, 700], 4, 64, 2048, 128, 0, False,
+                            {"q_std": 1.0, "scale": 1.0}),
+    "k100_h128": (3, [900, 50, 101], 4, 64, 100, 128, 0, False, {}),
+    "single_seq_h128_splitk": (1, [5000], 64, 128, 2048, 128, 0, False, {}),
 }
 
 
