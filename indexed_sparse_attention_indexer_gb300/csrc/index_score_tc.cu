@@ -22,10 +22,9 @@
 // contiguous ranges over one CTA per SM, so causal prefill rows balance
 // without a special order.  FP8 keys use kind::f8f6f4 with the queries
 // rounded to E4M3 (exact for the integer-valued index queries).
-#include <cudaTypedefs.h>
-
 #include "kernels.h"
 #include "tc_common.cuh"
+#include "tma_host.h"
 
 namespace dsi {
 using namespace tc;
@@ -292,8 +291,9 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     }
     // never leave the CTA with a TMA copy still landing in shared memory
     if (lane == 0 && *abort_flag) {
+      volatile int no_abort = 0;   // the drain is bounded by time only
       for (int s = 0; s < C::STAGES; ++s)
-        if (issued[s]) mbar_wait(&full[s], issued_phase[s], abort_flag, err, 100000000ull);
+        if (issued[s]) mbar_wait(&full[s], issued_phase[s], &no_abort, err, 100000000ull);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================================
@@ -412,33 +412,6 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 2D map over a row-major [rows, cols] array, box [box_rows, box_cols], 128B swizzle.
-bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t rows,
-              uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * (cuuint64_t)esize};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int NT, bool FP8>
 cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, int decode,
                int64_t q_offset, float* scores, int64_t ld, int* err, cudaStream_t st) {
@@ -448,12 +421,12 @@ cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, 
   CUtensorMap kmap, qmap;
   memset(&qmap, 0, sizeof(qmap));
   if (FP8) {
-    if (!make_map(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, krows, kD, 128, kSub))
+    if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, krows, kD, 128, kSub))
       return cudaErrorInvalidValue;
   } else {
-    if (!make_map(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, krows, kD, 64, kSub))
+    if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, krows, kD, 64, kSub))
       return cudaErrorInvalidValue;
-    if (!make_map(&qmap, q_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)rows * kHeads, kD,
+    if (!tma_map_2d(&qmap, q_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)rows * kHeads, kD,
                   64, kHeads))
       return cudaErrorInvalidValue;
   }
@@ -486,7 +459,7 @@ bool tc_score_supported(const CacheView& c, int H) {
                                        : (uint64_t)c.batch * c.s_max;
   if (krows >= (1ull << 31)) return false;
   if ((reinterpret_cast<uintptr_t>(c.k_idx) & 15) != 0) return false;
-  return get_encode() != nullptr;
+  return tma_encode_fn() != nullptr;
 }
 
 bool tc_score_shape_ok(int rows, int decode) {

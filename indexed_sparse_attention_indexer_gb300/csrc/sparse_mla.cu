@@ -257,12 +257,13 @@ cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const int32_
                                  bf16* out, float* lse, void* ws, size_t ws_bytes, int* err,
                                  cudaStream_t st);
 bool tc_mla_supported(int n_heads);
+bool tc_mla_cache_ok(const CacheView& c);
 
 cudaError_t launch_sparse_mla(const bf16* q, const CacheView& c, const int32_t* idx, int rows,
                               int H, int K, int decode, int64_t q_offset, float scale, bf16* out,
                               float* lse, void* ws, size_t ws_bytes, int* err, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  if (tc_mla_supported(H))
+  if (tc_mla_supported(H) && tc_mla_cache_ok(c))
     return launch_sparse_mla_tc(q, c, idx, rows, H, K, decode, q_offset, scale, out, lse, ws,
                                 ws_bytes, err, st);
   const int splits = mla_pick_splits(rows, H, K, ws ? ws_bytes : 0);

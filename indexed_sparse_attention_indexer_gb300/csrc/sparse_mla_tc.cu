@@ -18,18 +18,21 @@
 // TMEM.  The two partial logit tiles (128 heads x 64 positions, fp32) are
 // swapped through distributed shared memory, so both CTAs hold the same
 // logits and take the same softmax decisions.  Per 64-position tile:
-//   producers (4 warps): cp.async gather of the tile's rows into a
-//     128-byte-swizzled stage (ring of 4), zero rows for skipped entries;
+//   producer (1 thread): TMA gather4 of the tile's rows (four rows per
+//     instruction) into a 128-byte-swizzled stage (ring of 3);
 //   MMA (1 thread):  S = Qslice . C^T  (A from TMEM, B K-major from the stage)
 //                    O += P . V        (A = P K-major, B = V MN-major, same stage)
 //   softmax (4 warps, one head per thread): read S from TMEM, exchange with
-//     the peer, online softmax in log2 units with a lazily moved reference max
-//     (the accumulator is rescaled only when the max grows by more than 2^8),
-//     P in bf16 to shared memory.
+//     the peer (software-pipelined: tile t+1 is sent before tile t is
+//     finished; a relay lane of the MMA warp turns local arrivals into one
+//     cluster-scope arrival per tile), online softmax in log2 units with a
+//     lazily moved reference max (the accumulator is rescaled only when the
+//     max grows by more than 2^8), P in bf16 to shared memory.
 // Every wait is bounded; the cluster syncs once after set-up and once before
 // exit so no CTA leaves while its peer may still write into it.
 #include "kernels.h"
 #include "tc_common.cuh"
+#include "tma_host.h"
 
 namespace dsi {
 using namespace tc;
@@ -39,19 +42,22 @@ namespace {
 constexpr int kH = 128;                        // heads (MMA M)
 constexpr int kNp = 64;                        // positions per tile (MMA N of the logits)
 constexpr int kChunks = 5;                     // 64-dim blocks each CTA gathers per row
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kChunkBytes = kNp * 128;         // one 64-dim block of a tile: 8 KB
 constexpr int kStageBytes = kChunks * kChunkBytes;
-constexpr int kProducerWarps = 4;
-constexpr int kMmaWarp = kProducerWarps;       // warp 4
-constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;   // 288
-constexpr int kProducers = kProducerWarps * 32;
+// 8 warps: two per SM sub-partition, so each thread may use up to 255 registers
+constexpr int kProducerWarps = 3;
+constexpr int kMmaWarp = kProducerWarps;       // warp 3: lane 0 issues MMAs, lane 1 relays
+constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;   // 256
+
+constexpr int kMaxEntries = DSI_MAX_K;         // index entries one split can hold
 
 constexpr int OFF_C = 0;
 constexpr int OFF_P = OFF_C + kStages * kStageBytes;      // P [128 x 64] bf16, 16 KB
-constexpr int OFF_X = OFF_P + kH * kNp * 2;               // peer logits [128 x 64] fp32, 32 KB
-constexpr int OFF_BAR = OFF_X + kH * kNp * 4;
-constexpr int NBARS = 2 * kStages + 8;
+constexpr int OFF_X = OFF_P + kH * kNp * 2;               // 2 x peer logits [128 x 64] fp32
+constexpr int OFF_ROWS = OFF_X + 2 * kH * kNp * 4;        // physical row of each entry (or -1)
+constexpr int OFF_BAR = OFF_ROWS + kMaxEntries * 4;
+constexpr int NBARS = 2 * kStages + 6 + 8;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM = OFF_MISC + 64 + 1024;
 
@@ -85,28 +91,39 @@ __device__ __forceinline__ bool pos_ok(int pos, int64_t n_vis) {
 #endif
 }
 
+__device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float* v) {
+  uint32_t r[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+  tmem_st32(taddr, r);
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-mla_tc(CacheView c, MlaArgs a, int* err) {
+mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* s_full = bars + 2 * kStages;
-  uint64_t* s_empty = s_full + 1;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* p_empty = s_full + 3;
-  uint64_t* q_ready = s_full + 4;
-  uint64_t* x_full = s_full + 5;
-  uint64_t* x_empty = s_full + 6;
-  uint64_t* o_done = s_full + 7;
+  uint64_t* full = bars;                       // [kStages] gather landed (TMA transactions)
+  uint64_t* empty = bars + kStages;            // [kStages] stage free (MMA commit)
+  uint64_t* s_full = bars + 2 * kStages;       // logits in TMEM (MMA commit)
+  uint64_t* s_empty = s_full + 1;              // logits read out (softmax threads)
+  uint64_t* p_full = s_full + 2;               // P written (softmax threads)
+  uint64_t* p_empty = s_full + 3;              // P.V done (MMA commit)
+  uint64_t* q_ready = s_full + 4;              // query slice in TMEM (softmax threads)
+  uint64_t* o_done = s_full + 5;               // last P.V done (MMA commit)
+  uint64_t* x_full = s_full + 6;               // [2] peer's partial logits arrived (peer relay)
+  uint64_t* x_empty = x_full + 2;              // [2] peer has read what we sent (peer relay)
+  uint64_t* sent = x_full + 4;                 // [2] our partial logits stored to the peer
+  uint64_t* consumed = x_full + 6;             // [2] we have read the peer's partial logits
+  int32_t* rows_s = reinterpret_cast<int32_t*>(smem + OFF_ROWS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   int* last_valid = reinterpret_cast<int*>(smem + OFF_MISC + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rho = cluster_ctarank();          // which half of the dims this CTA owns
+  const uint32_t peer = rho ^ 1u;
   const int pair = blockIdx.x >> 1;
   const int r = pair / a.splits, sp = pair % a.splits;
   const int b = a.decode ? r : 0;
@@ -115,114 +132,167 @@ mla_tc(CacheView c, MlaArgs a, int* err) {
   const int tiles_per = (tiles_all + a.splits - 1) / a.splits;
   const int j_begin = sp * tiles_per * kNp;
   const int j_end = min(a.K, j_begin + tiles_per * kNp);
+  const int span = tiles_per * kNp;                // entries this split owns (<= kMaxEntries)
   const int32_t* irow = a.idx + (int64_t)r * a.K;
   const int g0 = rho ? 4 : 0;                      // first gathered 64-dim block
   const int qk_first = rho ? 1 : 0;                // first stage block used by the logits
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], kProducers); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     mbar_init(s_full, 1);
     mbar_init(s_empty, 128);
     mbar_init(p_full, 128);
     mbar_init(p_empty, 1);
     mbar_init(q_ready, 128);
-    mbar_init(x_full, 128);
-    mbar_init(x_empty, 128);
     mbar_init(o_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&x_full[i], 1);
+      mbar_init(&x_empty[i], 1);
+      mbar_init(&sent[i], 128);
+      mbar_init(&consumed[i], 128);
+    }
     *abort_flag = 0;
     *last_valid = -1;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, TMEM_COLS);
   __syncthreads();
-  // last valid entry of this split (tiles past it are skipped)
-  for (int j = j_begin + tid; j < j_end; j += kThreads)
-    if (pos_ok(__ldg(irow + j), n_vis)) atomicMax(last_valid, j);
+  // the split's entries, translated once to physical cache rows (-1 = skipped)
+  for (int jj = tid; jj < span; jj += kThreads) {
+    const int j = j_begin + jj;
+    int pr = -1;
+    if (j < j_end) {
+      const int pos = __ldg(irow + j);
+#ifdef DSI_CHECKED
+      if (pos >= n_vis) report(err, kErrBounds);
+#endif
+      if (pos_ok(pos, n_vis)) {
+        const int64_t x = phys_row(c, b, pos, err);
+        if (x >= 0) { pr = (int)x; atomicMax(last_valid, jj); }
+      }
+    }
+    rows_s[jj] = pr;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   cluster_sync();   // the peer's barriers exist before anyone arrives on them
   const uint32_t tmem = *tmem_slot;
-  const int n_tiles = *last_valid < 0 ? 0 : (*last_valid - j_begin) / kNp + 1;
+  const int n_tiles = *last_valid < 0 ? 0 : *last_valid / kNp + 1;
 
   if (warp < kProducerWarps) {
-    // ======================= gather producers =================================
-    const int pt = tid;                 // 0..127
-    const int rr = pt >> 1;             // row of the tile
-    const int half = pt & 1;            // which 20 of the row's 40 16-byte pieces
-    int stage = 0, prev = -1;
-    uint32_t ph = 0;
-    for (int t = 0; t < n_tiles; ++t) {
-      if (!mbar_wait(&empty[stage], ph ^ 1, abort_flag, err)) break;
-      const int j = j_begin + t * kNp + rr;
-      int pos = j < j_end ? __ldg(irow + j) : -1;
-#ifdef DSI_CHECKED
-      if (pos >= n_vis) { report(err, kErrBounds); pos = -1; }
-#endif
-      const int64_t prow = pos >= 0 ? phys_row(c, b, pos, err) : -1;
-      uint8_t* st_base = smem + OFF_C + stage * kStageBytes;
-      const uint32_t st_addr = smem_u32(st_base);
-#pragma unroll 4
-      for (int i = 0; i < 20; ++i) {
-        const int pi = half * 20 + i;
-        const int ch = pi >> 3, u = pi & 7;
-        const uint32_t off = ch * kChunkBytes + sw128_offset(rr, u);
-        if (prow >= 0)
-          cp_async_16(st_addr + off, c.latent + prow * DSI_D_QK + (g0 + ch) * 64 + u * 8);
-        else
-          *reinterpret_cast<uint4*>(st_base + off) = make_uint4(0, 0, 0, 0);
-      }
-      cp_async_commit();
-      if (prev >= 0) {
-        cp_async_wait<1>();
-        fence_proxy_async_smem();
-        mbar_arrive(&full[prev]);
-      }
-      prev = stage;
-      if (++stage == kStages) { stage = 0; ph ^= 1; }
-    }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (prev >= 0) mbar_arrive(&full[prev]);
-  } else if (warp == kMmaWarp) {
-    // ======================= MMA issuer =======================================
-    if (lane == 0) {
-      bool ok = mbar_wait(q_ready, 0, abort_flag, err);
-      tc_fence_after();
-      int stage = 0, prev = -1;
+    // ======================= gather producer ==================================
+    // warp 0, 16 lanes: per tile, lane g gathers rows 4g..4g+3 of the tile, five
+    // 64-dim blocks, each a TMA gather of four 128-byte rows into the swizzled
+    // stage.  Lane 0 first arms the stage's barrier with the tile's byte count.
+    // Skipped entries fetch row 0 (their probability is zero).
+    if (warp == 0 && lane < kNp / 4) {
+      if (lane == 0) prefetch_tmap(&lmap);
+      int stage = 0;
       uint32_t ph = 0;
-      auto pv = [&](int tt, int st) -> bool {
-        if (!mbar_wait(p_full, tt & 1, abort_flag, err)) return false;
-        tc_fence_after();
-        const uint32_t pbase = smem_u32(smem + OFF_P);
-        const uint32_t vbase = smem_u32(smem + OFF_C + st * kStageBytes);
-#pragma unroll
-        for (int kk = 0; kk < kNp / 16; ++kk)
-          mma_bf16(tmem + TM_O, desc_sw128(pbase + kk * 32), desc_sw128_mn(vbase + kk * 2048, kChunkBytes),
-                   IDESC_O, (tt > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(p_empty);
-        mma_commit(&empty[st]);
-        return true;
-      };
-      for (int t = 0; ok && t < n_tiles; ++t) {
-        if (!mbar_wait(&full[stage], ph, abort_flag, err)) break;
-        if (!mbar_wait(s_empty, (t & 1) ^ 1, abort_flag, err)) break;
-        tc_fence_after();
-        const uint32_t cbase = smem_u32(smem + OFF_C + stage * kStageBytes);
-        int k = 0;
-        for (int kc = qk_first; kc < kChunks; ++kc) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks, ++k)
-            mma_bf16_tmem_a(tmem + TM_S, tmem + TM_Q + k * 8,
-                            desc_sw128(cbase + kc * kChunkBytes + ks * 32), IDESC_S, k > 0 ? 1u : 0u);
+      bool issued[kStages] = {false, false, false};
+      uint32_t issued_ph[kStages] = {0, 0, 0};
+      const unsigned gmask = 0x0000ffffu;
+      for (int t = 0; t < n_tiles; ++t) {
+        bool ok = true;
+        if (lane == 0) {
+          ok = mbar_wait(&empty[stage], ph ^ 1, abort_flag, err);
+          if (ok) mbar_arrive_expect_tx(&full[stage], kStageBytes);
         }
-        mma_commit(s_full);
-        if (prev >= 0 && !pv(t - 1, prev)) break;
-        prev = stage;
+        ok = __shfl_sync(gmask, ok, 0);
+        if (!ok) break;
+        issued[stage] = true;
+        issued_ph[stage] = ph;
+        uint8_t* st_base = smem + OFF_C + stage * kStageBytes;
+        const int r4 = lane * 4;
+        const int32_t* rw = rows_s + t * kNp + r4;
+        const int y0 = max(rw[0], 0), y1 = max(rw[1], 0), y2 = max(rw[2], 0), y3 = max(rw[3], 0);
+#pragma unroll
+        for (int ch = 0; ch < kChunks; ++ch)
+          tma_gather4(st_base + ch * kChunkBytes + r4 * 128, &lmap, (g0 + ch) * 64, y0, y1, y2, y3,
+                      &full[stage]);
         if (++stage == kStages) { stage = 0; ph ^= 1; }
       }
-      if (!*abort_flag && prev >= 0) pv(n_tiles - 1, prev);
+      // never leave the CTA with a gather still landing in shared memory
+      if (lane == 0 && *abort_flag) {
+        volatile int no_abort = 0;   // the drain is bounded by time only
+        for (int s2 = 0; s2 < kStages; ++s2)
+          if (issued[s2]) mbar_wait(&full[s2], issued_ph[s2], &no_abort, err, 100000000ull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      // ===================== MMA issuer =======================================
+      // Event-driven: a logit tile (QK) is issued when its gather has landed and
+      // the TMEM logit tile is free; a P.V tile when its P is ready -- whichever
+      // comes first, so a slow gather never delays the previous tile's P.V.
+      bool ok = mbar_wait(q_ready, 0, abort_flag, err);
+      tc_fence_after();
+      int qk_next = 0, pv_next = 0;
+      const uint32_t pbase = smem_u32(smem + OFF_P);
+      const uint64_t t_start = global_ns();
+      uint64_t t_last = t_start;
+      while (ok && pv_next < n_tiles) {
+        bool progress = false;
+        if (qk_next < n_tiles) {
+          const int st = qk_next % kStages;
+          if (mbar_try_wait(&full[st], (qk_next / kStages) & 1) &&
+              mbar_try_wait(s_empty, (qk_next & 1) ^ 1)) {
+            tc_fence_after();
+            const uint64_t d0 = desc_sw128(smem_u32(smem + OFF_C + st * kStageBytes) +
+                                           qk_first * kChunkBytes);
+            const int nk = (kChunks - qk_first) * 4;
+            for (int k = 0; k < nk; ++k)
+              mma_bf16_tmem_a(tmem + TM_S, tmem + TM_Q + k * 8,
+                              d0 + (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4),
+                              IDESC_S, k > 0 ? 1u : 0u);
+            mma_commit(s_full);
+            ++qk_next;
+            progress = true;
+          }
+        }
+        if (pv_next < qk_next && mbar_try_wait(p_full, pv_next & 1)) {
+          tc_fence_after();
+          const int st = pv_next % kStages;
+          const uint64_t pd = desc_sw128(pbase);
+          const uint64_t vd = desc_sw128_mn(smem_u32(smem + OFF_C + st * kStageBytes), kChunkBytes);
+#pragma unroll
+          for (int kk = 0; kk < kNp / 16; ++kk)
+            mma_bf16(tmem + TM_O, pd + (uint64_t)((kk * 32) >> 4), vd + (uint64_t)((kk * 2048) >> 4),
+                     IDESC_O, (pv_next > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(p_empty);
+          mma_commit(&empty[st]);
+          ++pv_next;
+          progress = true;
+        }
+        // bounded: give up after kWaitLimitNs without progress
+        if (progress) {
+          t_last = global_ns();
+        } else if (*abort_flag) {
+          ok = false;
+        } else if (global_ns() - t_last > kWaitLimitNs) {
+          *abort_flag = 1;
+          report(err, kErrTimeout);
+          ok = false;
+        }
+      }
+      (void)t_start;
       mma_commit(o_done);
+    } else if (lane == 1) {
+      // ===================== exchange relay ===================================
+      // Turns the softmax threads' local "sent" / "consumed" arrivals into one
+      // cluster-scope arrival on the peer per tile, so that the softmax
+      // threads never wait for a cluster-wide release themselves.
+      const uint32_t xfull_remote = map_to_rank(smem_u32(x_full), peer);
+      const uint32_t xempty_remote = map_to_rank(smem_u32(x_empty), peer);
+      for (int t = 0; t < n_tiles; ++t) {
+        const int bsel = t & 1;
+        const uint32_t par = (t >> 1) & 1;
+        if (!mbar_wait(&sent[bsel], par, abort_flag, err)) break;
+        mbar_arrive_remote(xfull_remote + bsel * 8);
+        if (!mbar_wait(&consumed[bsel], par, abort_flag, err)) break;
+        mbar_arrive_remote(xempty_remote + bsel * 8);
+      }
     }
     __syncwarp();
   } else {
@@ -248,52 +318,64 @@ mla_tc(CacheView c, MlaArgs a, int* err) {
       tc_fence_before();
       mbar_arrive(q_ready);
     }
-    const uint32_t peer = rho ^ 1u;
-    const uint32_t x_remote = map_to_rank(smem_u32(smem + OFF_X), peer);
-    const uint32_t xfull_remote = map_to_rank(smem_u32(x_full), peer);
-    const uint32_t xempty_remote = map_to_rank(smem_u32(x_empty), peer);
-    const float* xrow = reinterpret_cast<const float*>(smem + OFF_X) + h * kNp;
+    // exchange buffer layout [buffer][4-position group][head] x float4: a
+    // warp's stores (and loads) of one group are 512 contiguous bytes
+    const uint32_t x_remote = map_to_rank(smem_u32(smem + OFF_X), peer) + h * 16;
+    const uint8_t* xrow = smem + OFF_X + h * 16;
     uint8_t* prow = smem + OFF_P;
     const float sl2 = a.scale * kLog2e;
     float m_ref = -INFINITY, l_sum = 0.f;
     bool ok = true;
-    for (int t = 0; t < n_tiles; ++t) {
-      if (!(ok = warp_wait(s_full, t & 1, abort_flag, err))) break;
+    float vc[kNp], vn[kNp];   // logits of the current tile and of the next one
+
+    // read this CTA's partial logits of tile tt into v (frees the TMEM S tile)
+    auto load_s = [&](int tt, float* v) -> bool {
+      if (!warp_wait(s_full, tt & 1, abort_flag, err)) return false;
       tc_fence_after();
-      float v[kNp];
       tmem_ld32(tmem + lane_base + TM_S, v);
       tmem_ld32(tmem + lane_base + TM_S + 32, v + 32);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(s_empty);
-      // validity of the tile's 64 positions (two ballots per warp)
-      const int jt = j_begin + t * kNp;
-      const int pa = jt + lane < j_end ? __ldg(irow + jt + lane) : -1;
-      const int pb = jt + 32 + lane < j_end ? __ldg(irow + jt + 32 + lane) : -1;
-      const uint32_t m_lo = __ballot_sync(0xffffffffu, pos_ok(pa, n_vis));
-      const uint32_t m_hi = __ballot_sync(0xffffffffu, pos_ok(pb, n_vis));
-      // swap partial logits with the peer CTA
-      if (!(ok = warp_wait_cluster(x_empty, (t & 1) ^ 1, abort_flag, err))) break;
+      return true;
+    };
+    // store them into the peer's exchange buffer for tile tt
+    auto send = [&](int tt, const float* v) -> bool {
+      const int bsel = tt & 1;
+      if (!warp_wait_cluster(&x_empty[bsel], ((tt >> 1) & 1) ^ 1, abort_flag, err)) return false;
+      const uint32_t dst = x_remote + bsel * (kH * kNp * 4);
 #pragma unroll
       for (int q4 = 0; q4 < kNp / 4; ++q4)
-        st_cluster_v4(x_remote + h * kNp * 4 + ((q4 ^ (h & 15)) << 4),
+        st_cluster_v4(dst + q4 * (kH * 16),
                       make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
-      mbar_arrive_remote(xfull_remote);
-      if (!(ok = warp_wait_cluster(x_full, t & 1, abort_flag, err))) break;
+      mbar_arrive(&sent[bsel]);
+      return true;
+    };
+
+    if (n_tiles > 0) ok = load_s(0, vc) && send(0, vc);
+    for (int t = 0; ok && t < n_tiles; ++t) {
+      // peer's partial logits of tile t
+      const int bsel = t & 1;
+      if (!(ok = warp_wait_cluster(&x_full[bsel], (t >> 1) & 1, abort_flag, err))) break;
 #pragma unroll
       for (int q4 = 0; q4 < kNp / 4; ++q4) {
-        const float4 pv4 = *reinterpret_cast<const float4*>(
-            reinterpret_cast<const uint8_t*>(xrow) + ((q4 ^ (h & 15)) << 4));
-        v[4 * q4] += pv4.x; v[4 * q4 + 1] += pv4.y; v[4 * q4 + 2] += pv4.z; v[4 * q4 + 3] += pv4.w;
+        const float4 pv4 = *reinterpret_cast<const float4*>(xrow + bsel * (kH * kNp * 4) +
+                                                            q4 * (kH * 16));
+        vc[4 * q4] += pv4.x; vc[4 * q4 + 1] += pv4.y; vc[4 * q4 + 2] += pv4.z; vc[4 * q4 + 3] += pv4.w;
       }
-      mbar_arrive_remote(xempty_remote);
+      mbar_arrive(&consumed[bsel]);
+      // start the exchange of tile t+1 before working on tile t
+      if (t + 1 < n_tiles && !(ok = load_s(t + 1, vn) && send(t + 1, vn))) break;
+      // validity of the tile's 64 entries
+      const uint32_t m_lo = __ballot_sync(0xffffffffu, rows_s[t * kNp + lane] >= 0);
+      const uint32_t m_hi = __ballot_sync(0xffffffffu, rows_s[t * kNp + 32 + lane] >= 0);
       // online softmax in log2 units
       float tmax = -INFINITY;
 #pragma unroll
       for (int j = 0; j < kNp; ++j) {
         const bool on = ((j < 32 ? m_lo >> j : m_hi >> (j - 32)) & 1u) != 0;
-        v[j] = on ? v[j] * sl2 : -INFINITY;
-        tmax = fmaxf(tmax, v[j]);
+        vc[j] = on ? vc[j] * sl2 : -INFINITY;
+        tmax = fmaxf(tmax, vc[j]);
       }
       float alpha = 1.f;
       bool rescale = false;
@@ -303,17 +385,6 @@ mla_tc(CacheView c, MlaArgs a, int* err) {
         alpha = exp2f(m_ref - tmax);
         m_ref = tmax;
         rescale = true;
-      }
-      uint32_t pk[kNp / 2];
-      float psum = 0.f;
-#pragma unroll
-      for (int j = 0; j < kNp; j += 2) {
-        const float e0 = (v[j] == -INFINITY) ? 0.f : exp2f(v[j] - m_ref);
-        const float e1 = (v[j + 1] == -INFINITY) ? 0.f : exp2f(v[j + 1] - m_ref);
-        const __nv_bfloat162 p2 = __floats2bfloat162_rn(e0, e1);
-        const float2 pr = __bfloat1622float2(p2);
-        psum += pr.x + pr.y;
-        pk[j / 2] = *reinterpret_cast<const uint32_t*>(&p2);
       }
       // PV(t-1) must be complete before P and the accumulator are touched
       if (!(ok = warp_wait(p_empty, (t & 1) ^ 1, abort_flag, err))) break;
@@ -325,22 +396,38 @@ mla_tc(CacheView c, MlaArgs a, int* err) {
           float o[32];
           tmem_ld32(tmem + lane_base + TM_O + c0, o);
           tmem_ld_wait();
-          uint32_t ob[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ob[i] = __float_as_uint(o[i] * alpha);
-          tmem_st32(tmem + lane_base + TM_O + c0, ob);
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32f(tmem + lane_base + TM_O + c0, o);
         }
         tmem_st_wait();
-        l_sum *= alpha;   // alpha == 1 for heads that did not move their reference
       }
-      l_sum += psum;
+      // P = 2^(logit - reference) in bf16, straight into the swizzled P tile
+      float psum = 0.f;
+      // 2^(-inf) is 0 for skipped entries; a reference of -inf means every
+      // entry so far was skipped (all probabilities 0)
+      const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(prow + sw128_offset(h, u)) =
-            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      for (int u = 0; u < 8; ++u) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = 8 * u + 2 * e;
+          const float e0 = ex2_approx(vc[j] - mr);
+          const float e1 = ex2_approx(vc[j + 1] - mr);
+          const __nv_bfloat162 p2 = __floats2bfloat162_rn(e0, e1);
+          const float2 pr = __bfloat1622float2(p2);
+          psum += pr.x + pr.y;
+          w4[e] = *reinterpret_cast<const uint32_t*>(&p2);
+        }
+        *reinterpret_cast<uint4*>(prow + sw128_offset(h, u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      l_sum = l_sum * alpha + psum;     // alpha == 1 for heads that did not move their reference
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
+#pragma unroll
+      for (int j = 0; j < kNp; ++j) vc[j] = vn[j];
     }
     // ---- epilogue: normalise and store this CTA's 256 output dims ------------
     if (ok && warp_wait(o_done, 0, abort_flag, err)) {
@@ -394,6 +481,13 @@ mla_tc(CacheView c, MlaArgs a, int* err) {
 
 bool tc_mla_supported(int n_heads) { return n_heads == kH; }
 
+// Physical rows must fit the kernel's 32-bit row ids.
+bool tc_mla_cache_ok(const CacheView& c) {
+  const uint64_t rows = c.block_table ? (uint64_t)c.num_pages * c.page_size
+                                      : (uint64_t)c.batch * c.s_max;
+  return rows < (1ull << 31);
+}
+
 int tc_mla_splits(int rows, int K, size_t ws_bytes) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
@@ -426,11 +520,17 @@ cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const int32_
     a.part_o = reinterpret_cast<float*>(ws);
     a.part_ml = reinterpret_cast<float2*>(reinterpret_cast<char*>(ws) + n * DSI_D_LATENT * sizeof(float));
   }
+  // latent rows as a 2D tensor [rows, 576], one-row boxes of 64 dims (gather4)
+  const uint64_t lrows = c.block_table ? (uint64_t)c.num_pages * c.page_size
+                                       : (uint64_t)c.batch * c.s_max;
+  CUtensorMap lmap;
+  if (!tma_map_2d(&lmap, c.latent, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lrows, DSI_D_QK, 64, 1))
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(mla_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
   const long blocks = 2L * rows * a.splits;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
-  mla_tc<<<(unsigned)blocks, kThreads, SMEM, st>>>(c, a, err);
+  mla_tc<<<(unsigned)blocks, kThreads, SMEM, st>>>(lmap, c, a, err);
   note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
