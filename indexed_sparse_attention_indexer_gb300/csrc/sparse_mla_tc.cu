@@ -18,8 +18,9 @@
 // TMEM.  The two partial logit tiles (128 heads x 64 positions, fp32) are
 // swapped through distributed shared memory, so both CTAs hold the same
 // logits and take the same softmax decisions.  Per 64-position tile:
-//   producer (1 thread): TMA gather4 of the tile's rows (four rows per
-//     instruction) into a 128-byte-swizzled stage (ring of 3);
+//   producers (3 warps): the tile's rows into a 128-byte-swizzled stage
+//     (ring of 3), three 64-dim blocks by TMA gather4 (four rows per
+//     instruction) and two by cp.async, so both copy engines work at once;
 //   MMA (1 thread):  S = Qslice . C^T  (A from TMEM, B K-major from the stage)
 //                    O += P . V        (A = P K-major, B = V MN-major, same stage)
 //   softmax (4 warps, one head per thread): read S from TMEM, exchange with
@@ -49,6 +50,11 @@ constexpr int kStageBytes = kChunks * kChunkBytes;
 constexpr int kProducerWarps = 3;
 constexpr int kMmaWarp = kProducerWarps;       // warp 3: lane 0 issues MMAs, lane 1 relays
 constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;   // 256
+// Each tile is gathered by two engines at once: TMA gather4 (warp 0) for the
+// first kTmaChunks 64-dim blocks, cp.async (warps 1-2) for the rest.
+constexpr int kTmaChunks = 3;
+constexpr int kLdgWarps = kProducerWarps - 1;
+constexpr int kLdgThreads = kLdgWarps * 32;
 
 constexpr int kMaxEntries = DSI_MAX_K;         // index entries one split can hold
 
@@ -104,7 +110,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* full = bars;                       // [kStages] gather landed (TMA transactions)
+  uint64_t* full = bars;                       // [kStages] gather landed (TMA bytes + cp.async threads)
   uint64_t* empty = bars + kStages;            // [kStages] stage free (MMA commit)
   uint64_t* s_full = bars + 2 * kStages;       // logits in TMEM (MMA commit)
   uint64_t* s_empty = s_full + 1;              // logits read out (softmax threads)
@@ -138,7 +144,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   const int qk_first = rho ? 1 : 0;                // first stage block used by the logits
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1 + kLdgThreads); mbar_init(&empty[s], 1); }
     mbar_init(s_full, 1);
     mbar_init(s_empty, 128);
     mbar_init(p_full, 128);
@@ -180,13 +186,13 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   const uint32_t tmem = *tmem_slot;
   const int n_tiles = *last_valid < 0 ? 0 : *last_valid / kNp + 1;
 
-  if (warp < kProducerWarps) {
-    // ======================= gather producer ==================================
-    // warp 0, 16 lanes: per tile, lane g gathers rows 4g..4g+3 of the tile, five
-    // 64-dim blocks, each a TMA gather of four 128-byte rows into the swizzled
-    // stage.  Lane 0 first arms the stage's barrier with the tile's byte count.
-    // Skipped entries fetch row 0 (their probability is zero).
-    if (warp == 0 && lane < kNp / 4) {
+  if (warp == 0) {
+    // ======================= gather: TMA part =================================
+    // 16 lanes: lane g gathers rows 4g..4g+3 of the tile for the first
+    // kTmaChunks 64-dim blocks, each a TMA gather of four 128-byte rows into
+    // the swizzled stage.  Lane 0 first arms the stage's barrier.  Skipped
+    // entries fetch row 0 (their probability is zero).
+    if (lane < kNp / 4) {
       if (lane == 0) prefetch_tmap(&lmap);
       int stage = 0;
       uint32_t ph = 0;
@@ -197,7 +203,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
         bool ok = true;
         if (lane == 0) {
           ok = mbar_wait(&empty[stage], ph ^ 1, abort_flag, err);
-          if (ok) mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          if (ok) mbar_arrive_expect_tx(&full[stage], kTmaChunks * kChunkBytes);
         }
         ok = __shfl_sync(gmask, ok, 0);
         if (!ok) break;
@@ -208,7 +214,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
         const int32_t* rw = rows_s + t * kNp + r4;
         const int y0 = max(rw[0], 0), y1 = max(rw[1], 0), y2 = max(rw[2], 0), y3 = max(rw[3], 0);
 #pragma unroll
-        for (int ch = 0; ch < kChunks; ++ch)
+        for (int ch = 0; ch < kTmaChunks; ++ch)
           tma_gather4(st_base + ch * kChunkBytes + r4 * 128, &lmap, (g0 + ch) * 64, y0, y1, y2, y3,
                       &full[stage]);
         if (++stage == kStages) { stage = 0; ph ^= 1; }
@@ -220,6 +226,37 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
           if (issued[s2]) mbar_wait(&full[s2], issued_ph[s2], &no_abort, err, 100000000ull);
       }
     }
+  } else if (warp < kProducerWarps) {
+    // ======================= gather: cp.async part ============================
+    // the remaining 64-dim blocks: half a warp per row (16 lanes x 16 bytes =
+    // two blocks), each piece to its swizzled place; a tile's copies are
+    // signalled (after a proxy fence) once the next tile's are in flight
+    constexpr int kLdgPieces = (kChunks - kTmaChunks) * 8;   // 16-byte pieces per row
+    static_assert(kLdgPieces == 16, "half a warp per row");
+    const int sub = lane >> 4, pi = lane & 15;
+    const int ch = kTmaChunks + (pi >> 3), u = pi & 7;
+    int stage = 0, prev = -1;
+    uint32_t ph = 0;
+    for (int t = 0; t < n_tiles; ++t) {
+      if (!mbar_wait(&empty[stage], ph ^ 1, abort_flag, err)) break;
+      const uint32_t st_addr = smem_u32(smem + OFF_C + stage * kStageBytes);
+      for (int rr = (warp - 1) * 2 + sub; rr < kNp; rr += 2 * kLdgWarps) {
+        const int pr = max(rows_s[t * kNp + rr], 0);
+        cp_async_16(st_addr + ch * kChunkBytes + sw128_offset(rr, u),
+                    c.latent + (int64_t)pr * DSI_D_QK + (g0 + ch) * 64 + u * 8);
+      }
+      cp_async_commit();
+      if (prev >= 0) {
+        cp_async_wait<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(&full[prev]);
+      }
+      prev = stage;
+      if (++stage == kStages) { stage = 0; ph ^= 1; }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    if (prev >= 0) mbar_arrive(&full[prev]);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // ===================== MMA issuer =======================================
@@ -364,8 +401,13 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
         vc[4 * q4] += pv4.x; vc[4 * q4 + 1] += pv4.y; vc[4 * q4 + 2] += pv4.z; vc[4 * q4 + 3] += pv4.w;
       }
       mbar_arrive(&consumed[bsel]);
-      // start the exchange of tile t+1 before working on tile t
-      if (t + 1 < n_tiles && !(ok = load_s(t + 1, vn) && send(t + 1, vn))) break;
+      // start the exchange of tile t+1 before working on tile t when its logits
+      // are already there; otherwise after tile t (never wait on its gather here)
+      bool sent_next = false;
+      if (t + 1 < n_tiles && __all_sync(0xffffffffu, mbar_try_wait(s_full, (t + 1) & 1))) {
+        if (!(ok = load_s(t + 1, vn) && send(t + 1, vn))) break;
+        sent_next = true;
+      }
       // validity of the tile's 64 entries
       const uint32_t m_lo = __ballot_sync(0xffffffffu, rows_s[t * kNp + lane] >= 0);
       const uint32_t m_hi = __ballot_sync(0xffffffffu, rows_s[t * kNp + 32 + lane] >= 0);
@@ -426,6 +468,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
+      if (t + 1 < n_tiles && !sent_next && !(ok = load_s(t + 1, vn) && send(t + 1, vn))) break;
 #pragma unroll
       for (int j = 0; j < kNp; ++j) vc[j] = vn[j];
     }
