@@ -234,12 +234,20 @@ dsi_status dsi_indexed_attention(const void* q_idx, const float* w, const void* 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* err = status_ptr();
   CacheView v = view_of(cache);
-  cudaError_t e = launch_index_score(reinterpret_cast<const bf16*>(q_idx), w, v, rows, n_heads_idx,
-                                     decode, q_offset, scores, p.ld, err, st);
-  if (e != cudaSuccess) return from_cuda(e);
-  e = launch_topk(scores, p.ld, rows, decode ? cache->seq_lens : nullptr, q_offset, K, idx,
-                  count_out, st);
-  if (e != cudaSuccess) return from_cuda(e);
+  cudaError_t e;
+  if (!decode && fused_prefill_topk_supported(v, n_heads_idx, rows, q_offset, K)) {
+    // prefill: scores stay on chip, only the selected indices are written
+    e = launch_index_topk_prefill(reinterpret_cast<const bf16*>(q_idx), w, v, rows, q_offset, K,
+                                  idx, count_out, err, st);
+    if (e != cudaSuccess) return from_cuda(e);
+  } else {
+    e = launch_index_score(reinterpret_cast<const bf16*>(q_idx), w, v, rows, n_heads_idx, decode,
+                           q_offset, scores, p.ld, err, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    e = launch_topk(scores, p.ld, rows, decode ? cache->seq_lens : nullptr, q_offset, K, idx,
+                    count_out, st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
   e = launch_sparse_mla(reinterpret_cast<const bf16*>(q), v, idx, rows, n_heads, K, decode,
                         q_offset, scale, reinterpret_cast<bf16*>(out), lse, ws + p.mla_off,
                         p.total - p.mla_off, err, st);

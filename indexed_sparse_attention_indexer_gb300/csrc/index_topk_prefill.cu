@@ -1,0 +1,471 @@
+// Fused prefill indexer: tcgen05 scoring with ReLU, head weights and a running
+// per-row Top-K in the epilogue; only the selected indices leave the kernel.
+//
+// ("Day 0 Inference Support for New LLM Architectures: Optimization
+// Practices", "Internal Fusion of the Indexer": scoring, head-weight
+// weighting and Top-K in one kernel that writes only the selected indices;
+// "Load Imbalance in Causal Indexing and the Zigzag Layout": later positions
+// have more history, so early and late segments are paired.)
+//
+// Work unit = a group of 2 query tokens (N = 2 x 64 heads).  Each CTA owns
+// whole groups, taken in zigzag pairs (group i with group G-1-i), so every row
+// is selected by one CTA and the causal triangle balances across CTAs.  For a
+// group, the 128-position key tiles stream through TMA stages into
+// tcgen05.mma (as in the scoring kernel); the epilogue computes the fp32
+// scores, and each token keeps a candidate buffer in shared memory of unique
+// 64-bit keys (order-preserving score key << 32 | ~position): larger key =
+// larger score, then lower position, so ties need no special handling.  A
+// candidate is kept when its key beats the current threshold (the K-th best
+// key of the last compaction); when a buffer nears capacity the token's 128
+// threads radix-select the K-th key and compact the buffer to the best K.
+// At the end of the group a final select picks the K best, and their
+// positions are written in ascending order through a bitmap prefix scan.
+#include "kernels.h"
+#include "tc_common.cuh"
+#include "tma_host.h"
+
+namespace dsi {
+using namespace tc;
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kHeads = 64;
+constexpr int kTileM = 128;
+constexpr int kSub = 64;
+constexpr int NT = 2;                        // tokens per group
+constexpr int N = NT * kHeads;               // 128
+constexpr int kStages = 2;
+constexpr int A_BYTES = kTileM * kD * 2;     // 32 KB
+constexpr int B_BYTES = N * kD * 2;          // 32 KB
+constexpr int kCap = 4096;                   // candidates per token
+constexpr int kMaxK = kCap / 2;              // 2048
+constexpr int kMaxRow = kCap * 64 / 2;       // bitmap of a row fits the 32 KB buffer: 131072 positions
+constexpr int EPI_WARPS = 8;                 // 4 per token
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr int THREADS = 64 + EPI_THREADS;    // 320
+constexpr int TMEM_COLS = 2 * N;             // 256
+constexpr uint32_t IDESC = idesc_f32(1, kTileM, N);
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + kStages * A_BYTES;
+constexpr int OFF_BUF = OFF_B + 2 * B_BYTES;                    // NT x kCap x 8 bytes
+constexpr int OFF_W = OFF_BUF + NT * kCap * 8;                  // NT x 64 fp32
+constexpr int OFF_HIST = OFF_W + NT * kHeads * 4;               // NT x 256 int
+constexpr int OFF_TOK = OFF_HIST + NT * 256 * 4;                // per-token state
+constexpr int OFF_BAR = (OFF_TOK + NT * 64 + 7) & ~7;
+constexpr int NBARS = 2 * kStages + 2 + 2 + 2 + 2 + 1;
+constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+constexpr int SMEM = OFF_MISC + 64 + 1024;
+
+struct TokState {
+  unsigned long long theta;   // keys <= theta are rejected
+  int cnt;                    // candidates in the buffer
+  int digit;                  // radix-select scratch
+  int krem;
+  int total;
+  int pad[2];
+};
+static_assert(sizeof(TokState) <= 64, "token state");
+
+struct Args {
+  const bf16* q_idx;
+  const float* w;
+  int32_t* idx;
+  int32_t* count;
+  int64_t q_offset;
+  int rows;
+  int K;
+  int groups;
+  int pairs_per_cta;   // zigzag pairs handled by each CTA (ceil)
+};
+
+__device__ __forceinline__ void bar_epi() {          // all epilogue threads
+  asm volatile("bar.sync 1, %0;\n" ::"n"(EPI_THREADS) : "memory");
+}
+__device__ __forceinline__ void bar_tok(int tk) {    // the 128 threads of one token
+  asm volatile("bar.sync %0, 128;\n" ::"r"(2 + tk) : "memory");
+}
+
+// k-th group (0-based) processed by CTA `cta`: zigzag pairs (i, G-1-i), pairs
+// dealt round-robin over the CTAs.  Returns -1 past the end.
+__device__ __forceinline__ int zigzag_group(int k, int cta, int ncta, int G) {
+  const int pair = cta + (k >> 1) * ncta;
+  const int npairs = (G + 1) / 2;
+  if (pair >= npairs) return -1;
+  const int g = (k & 1) ? G - 1 - pair : pair;
+  if ((k & 1) && g == pair) return -1;             // middle group of an odd count
+  return g;
+}
+
+__device__ __forceinline__ int group_tiles(const Args& a, int g) {
+  const int last = min(a.rows, (g + 1) * NT) - 1;
+  return (int)((a.q_offset + last + 1 + kTileM - 1) / kTileM);
+}
+
+// Radix select over the token's candidate buffer: the k-th largest key (keys
+// are unique).  128 threads of the token (tt = 0..127) take part.
+__device__ unsigned long long select_kth(const unsigned long long* buf, int n, int k, int* hist,
+                                         TokState* ts, int tt, int tk) {
+  unsigned long long prefix = 0, mask = 0;
+  int krem = k;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = tt; i < 256; i += 128) hist[i] = 0;
+    bar_tok(tk);
+    for (int i = tt; i < n; i += 128) {
+      const unsigned long long c = buf[i];
+      if ((c & mask) == prefix) atomicAdd(&hist[(int)((c >> shift) & 255ull)], 1);
+    }
+    bar_tok(tk);
+    if (tt < 32) {
+      int cs[8], tot = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) { cs[e] = hist[255 - (tt * 8 + e)]; tot += cs[e]; }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tt >= o) incl += y;
+      }
+      const int excl = incl - tot;
+      if (excl < krem && incl >= krem) {
+        int run = excl;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (run < krem && run + cs[e] >= krem) { ts->digit = 255 - (tt * 8 + e); ts->krem = krem - run; }
+          run += cs[e];
+        }
+      }
+    }
+    bar_tok(tk);
+    prefix |= (unsigned long long)ts->digit << shift;
+    mask |= 255ull << shift;
+    krem = ts->krem;
+    bar_tok(tk);
+  }
+  return prefix;
+}
+
+// Keep the entries >= t (exactly k of them) at the front of the buffer.
+__device__ void compact_ge(unsigned long long* buf, int n, unsigned long long t, TokState* ts,
+                           int tt, int tk) {
+  constexpr int PER = kCap / 128;
+  unsigned long long keep[PER];
+  int nk = 0;
+  for (int i = tt, e = 0; e < PER; i += 128, ++e) {
+    const unsigned long long c = i < n ? buf[i] : 0ull;
+    keep[e] = c;
+    nk += (i < n && c >= t) ? 1 : 0;
+  }
+  if (tt == 0) ts->total = 0;
+  bar_tok(tk);
+  int base = nk ? atomicAdd(&ts->total, nk) : 0;
+  bar_tok(tk);
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int i = tt + e * 128;
+    if (i < n && keep[e] >= t) buf[base++] = keep[e];
+  }
+  bar_tok(tk);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                   CacheView c, Args a, int* err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* acc_full = bars + 2 * kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* q_full = acc_empty + 2;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* done_bar = q_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], EPI_THREADS);
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nmax = 2 * a.pairs_per_cta;   // groups this CTA may own
+
+  if (warp == 0) {
+    // ======================= TMA producer =====================================
+    if (lane == 0) {
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&qmap);
+      int stage = 0, qcount = 0;
+      uint32_t ph = 0;
+      bool issued[kStages] = {false, false};
+      uint32_t issued_ph[kStages] = {0, 0};
+      bool ok = true;
+      for (int k = 0; ok && k < nmax; ++k) {
+        const int g = zigzag_group(k, blockIdx.x, gridDim.x, a.groups);
+        if (g < 0) continue;
+        const int slot = qcount & 1;
+        if (!(ok = mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1, abort_flag, err))) break;
+        uint8_t* qs = smem + OFF_B + slot * B_BYTES;
+        mbar_arrive_expect_tx(&q_full[slot], B_BYTES);
+        for (int t = 0; t < NT; ++t)
+          for (int cc = 0; cc < 2; ++cc)
+            tma_load_2d(qs + cc * (N * 128) + t * kHeads * 128, &qmap, cc * 64, (g * NT + t) * kHeads,
+                        &q_full[slot]);
+        ++qcount;
+        const int ntile = group_tiles(a, g);
+        for (int j = 0; j < ntile; ++j) {
+          if (!(ok = mbar_wait(&empty[stage], ph ^ 1, abort_flag, err))) break;
+          const int64_t nvis = a.q_offset + min(a.rows, (g + 1) * NT);
+          int nsub = 0;
+          int64_t prow[2];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int64_t p = (int64_t)j * kTileM + i * kSub;
+            prow[i] = -1;
+            if (p < nvis) { prow[i] = phys_row(c, 0, p, err); if (prow[i] >= 0) ++nsub; }
+          }
+          uint8_t* as = smem + OFF_A + stage * A_BYTES;
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(nsub * (A_BYTES / 2)));
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if (prow[i] < 0) continue;
+            tma_load_2d(as + i * (kSub * 128), &kmap, 0, (int)prow[i], &full[stage]);
+            tma_load_2d(as + 16384 + i * (kSub * 128), &kmap, 64, (int)prow[i], &full[stage]);
+          }
+          issued[stage] = true;
+          issued_ph[stage] = ph;
+          if (++stage == kStages) { stage = 0; ph ^= 1; }
+        }
+      }
+      if (*abort_flag) {
+        volatile int no_abort = 0;
+        for (int s = 0; s < kStages; ++s)
+          if (issued[s]) mbar_wait(&full[s], issued_ph[s], &no_abort, err, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ======================= MMA issuer ========================================
+    if (lane == 0) {
+      int stage = 0, abuf = 0, qcount = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true;
+      for (int k = 0; ok && k < nmax; ++k) {
+        const int g = zigzag_group(k, blockIdx.x, gridDim.x, a.groups);
+        if (g < 0) continue;
+        const int slot = qcount & 1;
+        if (!(ok = mbar_wait(&q_full[slot], (qcount >> 1) & 1, abort_flag, err))) break;
+        ++qcount;
+        const int ntile = group_tiles(a, g);
+        for (int j = 0; j < ntile; ++j) {
+          if (!(ok = mbar_wait(&full[stage], ph, abort_flag, err))) break;
+          if (!(ok = mbar_wait(&acc_empty[abuf], aph ^ 1, abort_flag, err))) break;
+          tc_fence_after();
+          const uint64_t ad = desc_sw128(smem_u32(smem + OFF_A + stage * A_BYTES));
+          const uint64_t bd = desc_sw128(smem_u32(smem + OFF_B + slot * B_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16(tmem + abuf * N, ad + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
+                     bd + (uint64_t)(((kk >> 2) * (N * 128) + (kk & 3) * 32) >> 4), IDESC, kk > 0);
+          mma_commit(&empty[stage]);
+          mma_commit(&acc_full[abuf]);
+          if (j == ntile - 1) mma_commit(&q_empty[slot]);
+          if (++stage == kStages) { stage = 0; ph ^= 1; }
+          if (++abuf == 2) { abuf = 0; aph ^= 1; }
+        }
+      }
+      mma_commit(done_bar);
+      mbar_wait(done_bar, 0, abort_flag, err, 100000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ======================= epilogue + running Top-K ===========================
+    const int ew = warp - 2;                  // 0..7
+    const int tk = ew >> 2;                   // token of the group this warp serves
+    const int quarter = warp & 3;             // TMEM lane quarter
+    const int tt = (ew & 3) * 32 + lane;      // thread index within the token's 128
+    const int row = quarter * 32 + lane;      // position within the tile (TMEM lane)
+    unsigned long long* buf = reinterpret_cast<unsigned long long*>(smem + OFF_BUF) + tk * kCap;
+    float* wts = reinterpret_cast<float*>(smem + OFF_W) + tk * kHeads;
+    int* hist = reinterpret_cast<int*>(smem + OFF_HIST) + tk * 256;
+    TokState* ts = reinterpret_cast<TokState*>(smem + OFF_TOK) + tk;
+    int abuf = 0;
+    uint32_t aph = 0;
+    bool ok = true;
+    for (int k = 0; ok && k < nmax; ++k) {
+      const int g = zigzag_group(k, blockIdx.x, gridDim.x, a.groups);
+      if (g < 0) continue;
+      const int r = g * NT + tk;                        // query row this token slot holds
+      const bool live = r < a.rows;
+      const int64_t nvis = live ? a.q_offset + r + 1 : 0;
+      if (tt < kHeads) wts[tt] = live ? __ldg(a.w + (int64_t)r * kHeads + tt) : 0.f;
+      if (tt == 0) { ts->theta = 0ull; ts->cnt = 0; }
+      bar_epi();
+      const int ntile = group_tiles(a, g);
+      for (int j = 0; j < ntile; ++j) {
+        const bool got = warp_wait(&acc_full[abuf], aph, abort_flag, err);
+        bar_epi();
+        if (!got || *abort_flag) { ok = false; break; }
+        tc_fence_after();
+        float v[kHeads];
+        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + abuf * N + tk * kHeads;
+        tmem_ld32(taddr, v);
+        tmem_ld32(taddr + 32, v + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&acc_empty[abuf]);
+        if (++abuf == 2) { abuf = 0; aph ^= 1; }
+        const int64_t p = (int64_t)j * kTileM + row;
+        if (live && p < nvis) {
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int h = 0; h < kHeads; h += 2) {
+            s0 = fmaf(wts[h], fmaxf(v[h], 0.f), s0);
+            s1 = fmaf(wts[h + 1], fmaxf(v[h + 1], 0.f), s1);
+          }
+          const unsigned long long key =
+              ((unsigned long long)score_key(s0 + s1) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)p);
+          if (key > ts->theta) {
+            const int slot = atomicAdd(&ts->cnt, 1);
+            buf[slot] = key;
+          }
+        }
+        bar_epi();
+        // keep room for one more tile: compact a buffer that could overflow
+        if (ts->cnt > kCap - kTileM) {
+          const int n = ts->cnt;
+          const unsigned long long t = select_kth(buf, n, a.K, hist, ts, tt, tk);
+          compact_ge(buf, n, t, ts, tt, tk);
+          if (tt == 0) { ts->cnt = a.K; ts->theta = t - 1ull; }
+        }
+        bar_epi();
+      }
+      if (!ok) break;
+      // ---- final selection of the group's rows -------------------------------
+      if (live) {
+        int n = ts->cnt;
+        if (n > a.K) {
+          const unsigned long long t = select_kth(buf, n, a.K, hist, ts, tt, tk);
+          compact_ge(buf, n, t, ts, tt, tk);
+          n = a.K;
+        }
+        // winners' positions -> registers, then the buffer becomes a bitmap
+        constexpr int PER = kMaxK / 128;
+        int mypos[PER];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+          const int i = tt + e * 128;
+          mypos[e] = i < n ? (int)(0xFFFFFFFFu - (uint32_t)(buf[i] & 0xFFFFFFFFull)) : -1;
+        }
+        bar_tok(tk);
+        uint32_t* bits = reinterpret_cast<uint32_t*>(buf);
+        const int nwords = (int)((nvis + 31) / 32);
+        for (int i = tt; i < nwords; i += 128) bits[i] = 0u;
+        bar_tok(tk);
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+          if (mypos[e] >= 0) atomicOr(&bits[mypos[e] >> 5], 1u << (mypos[e] & 31));
+        bar_tok(tk);
+        // ascending output: each thread owns a contiguous run of words
+        const int per = (nwords + 127) / 128;
+        const int w0 = min(nwords, tt * per), w1 = min(nwords, w0 + per);
+        int mine = 0;
+        for (int i = w0; i < w1; ++i) mine += __popc(bits[i]);
+        // exclusive scan of `mine` over the token's 128 threads (4 warps)
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int* wsum = hist;   // 4 warp totals
+        if (lane == 31) wsum[tt >> 5] = incl;
+        bar_tok(tk);
+        int before = incl - mine;
+        for (int x = 0; x < (tt >> 5); ++x) before += wsum[x];
+        int32_t* out = a.idx + (int64_t)r * a.K;
+        for (int i = w0; i < w1; ++i) {
+          uint32_t m = bits[i];
+          while (m) {
+            const int bpos = __ffs(m) - 1;
+            m &= m - 1;
+            out[before++] = i * 32 + bpos;
+          }
+        }
+        for (int i = n + tt; i < a.K; i += 128) out[i] = -1;
+        if (a.count && tt == 0) a.count[r] = n;
+      }
+      bar_epi();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace
+
+bool fused_prefill_topk_supported(const CacheView& c, int n_heads_idx, int rows, int64_t q_offset,
+                                  int K) {
+  if (n_heads_idx != kHeads || c.d != kD || c.k_dtype != DSI_BF16) return false;
+  if (c.block_table && c.page_size % kSub != 0) return false;
+  if (K < 1 || K > kMaxK) return false;
+  if (q_offset + rows > kMaxRow) return false;
+  const uint64_t krows = c.block_table ? (uint64_t)c.num_pages * c.page_size
+                                       : (uint64_t)c.batch * c.s_max;
+  if (krows >= (1ull << 31) || (int64_t)rows * kHeads >= (1ll << 31)) return false;
+  return tma_encode_fn() != nullptr;
+}
+
+cudaError_t launch_index_topk_prefill(const bf16* q_idx, const float* w, const CacheView& c,
+                                      int rows, int64_t q_offset, int K, int32_t* idx,
+                                      int32_t* count, int* err, cudaStream_t st) {
+  const uint64_t krows = c.block_table ? (uint64_t)c.num_pages * c.page_size
+                                       : (uint64_t)c.batch * c.s_max;
+  CUtensorMap kmap, qmap;
+  if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, krows, kD, 64, kSub))
+    return cudaErrorInvalidValue;
+  if (!tma_map_2d(&qmap, q_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)rows * kHeads, kD, 64,
+                  kHeads))
+    return cudaErrorInvalidValue;
+  Args a;
+  a.q_idx = q_idx;
+  a.w = w;
+  a.idx = idx;
+  a.count = count;
+  a.q_offset = q_offset;
+  a.rows = rows;
+  a.K = K;
+  a.groups = (rows + NT - 1) / NT;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int npairs = (a.groups + 1) / 2;
+  const int grid = npairs < sms ? npairs : sms;
+  a.pairs_per_cta = (npairs + grid - 1) / grid;
+  cudaError_t e = cudaFuncSetAttribute(index_topk_prefill,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  if (e != cudaSuccess) return e;
+  index_topk_prefill<<<grid, THREADS, SMEM, st>>>(kmap, qmap, c, a, err);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace dsi

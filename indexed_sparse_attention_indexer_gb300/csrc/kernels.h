@@ -23,6 +23,14 @@ cudaError_t launch_index_score(const bf16* q_idx, const float* w, const CacheVie
 enum ScoreKernel { kScoreStream = 0, kScoreSimt = 1, kScoreTc = 2 };
 ScoreKernel pick_score_kernel(const CacheView& c, int n_heads_idx);
 
+// Fused prefill indexer: scoring + running per-row Top-K in the epilogue;
+// writes only idx [rows, K] (ascending, -1 padded) and count [rows] (may be null).
+bool fused_prefill_topk_supported(const CacheView& c, int n_heads_idx, int rows, int64_t q_offset,
+                                  int K);
+cudaError_t launch_index_topk_prefill(const bf16* q_idx, const float* w, const CacheView& c,
+                                      int rows, int64_t q_offset, int K, int32_t* idx,
+                                      int32_t* count, int* err, cudaStream_t st);
+
 // ---- Top-K -------------------------------------------------------------------
 cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t* row_len,
                         int64_t q_offset, int K, int32_t* idx, int32_t* count,

@@ -135,6 +135,35 @@ def test_prefill(name):
     assert binding.device_status() == 0
 
 
+FUSED_PREFILL_CASES = [
+    # T, S, q_offset, K: rows longer than the 4096-entry candidate buffer force
+    # compactions; odd T leaves a half-empty last group
+    (300, 6000, 5700, 2048),
+    (257, 5000, 0, 100),
+    (64, 9000, 8936, 1),
+    (33, 4200, 4000, 2048),
+]
+
+
+@pytest.mark.parametrize("case", FUSED_PREFILL_CASES, ids=[str(c) for c in FUSED_PREFILL_CASES])
+def test_fused_prefill_topk_matches_unfused(case):
+    """The fused prefill indexer (scores never leave the chip) selects exactly what
+    scoring + select in two kernels selects, and what the oracle selects."""
+    T, S, off, K = case
+    ws = W.make_prefill(T, S, 64, 128, K, 16, seed=11, q_offset=off)
+    g = ws.to(DEV)
+    out, lse, idx, count = binding.layer(g)
+    scores = binding.index_score(g.q_idx, g.w, binding.Cache.of(g), False, off)
+    idx2, cnt2 = binding.topk(scores, K, q_offset=off)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    assert torch.equal(idx, idx2)
+    assert torch.equal(count, cnt2)
+    for t in (0, T // 2, T - 1):
+        ref = oracle.prefill_row(ws, t)
+        assert np.array_equal(idx[t].cpu().numpy(), ref["idx"]), f"row {t}"
+
+
 def test_prefill_chunk_invariance():
     """A prefill split into query chunks gives the same indices (and outputs) as one call."""
     T, S, Hi, d, K, H = 256, 256, 64, 128, 64, 128
