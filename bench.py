@@ -212,12 +212,20 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """Largest value over the ranks (the slowest rank's time)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tokens_per_s(tokens_per_rank: int, world: int, steps: int, ms_max: float) -> float:
+    """Tokens all ranks processed in the timed region / the slowest rank's time
+    (replicas: every rank runs its own batch, weak scaling)."""
+    return tokens_per_rank * world * steps / (ms_max / 1e3)
 
 
 def run_gpu(args):
@@ -273,8 +281,7 @@ def run_gpu(args):
     clk = clocks.stop()
     ms = max_over_ranks(ms_local, world)
     ms_step = ms / args.steps
-    tokens = ws.T * world
-    value = tokens * args.steps / (ms / 1e3)
+    value = whole_job_tokens_per_s(ws.T, world, args.steps, ms)
 
     # ---- dominant kernel: the indexer scoring launch, timed alone ----------
     scores = torch.empty((ws.T, span), dtype=torch.float32, device=dev)
