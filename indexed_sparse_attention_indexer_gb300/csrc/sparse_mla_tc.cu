@@ -25,8 +25,9 @@
 //                    O += P . V        (A = P K-major, B = V MN-major, same stage)
 //   softmax (4 warps, one head per thread): read S from TMEM, exchange with
 //     the peer (software-pipelined: tile t+1 is sent before tile t is
-//     finished; a relay lane of the MMA warp turns local arrivals into one
-//     cluster-scope arrival per tile), online softmax in log2 units with a
+//     finished; st.async stores count their bytes on the peer's barrier and
+//     a lane of the MMA warp returns buffer credits), online softmax in log2
+//     units with a
 //     lazily moved reference max (the accumulator is rescaled only when the
 //     max grows by more than 2^8), P in bf16 to shared memory.
 // Every wait is bounded; the cluster syncs once after set-up and once before
@@ -63,7 +64,7 @@ constexpr int OFF_P = OFF_C + kStages * kStageBytes;      // P [128 x 64] bf16, 
 constexpr int OFF_X = OFF_P + kH * kNp * 2;               // 2 x peer logits [128 x 64] fp32
 constexpr int OFF_ROWS = OFF_X + 2 * kH * kNp * 4;        // physical row of each entry (or -1)
 constexpr int OFF_BAR = OFF_ROWS + kMaxEntries * 4;
-constexpr int NBARS = 2 * kStages + 6 + 8;
+constexpr int NBARS = 2 * kStages + 6 + 6;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM = OFF_MISC + 64 + 1024;
 
@@ -118,10 +119,9 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   uint64_t* p_empty = s_full + 3;              // P.V done (MMA commit)
   uint64_t* q_ready = s_full + 4;              // query slice in TMEM (softmax threads)
   uint64_t* o_done = s_full + 5;               // last P.V done (MMA commit)
-  uint64_t* x_full = s_full + 6;               // [2] peer's partial logits arrived (peer relay)
-  uint64_t* x_empty = x_full + 2;              // [2] peer has read what we sent (peer relay)
-  uint64_t* sent = x_full + 4;                 // [2] our partial logits stored to the peer
-  uint64_t* consumed = x_full + 6;             // [2] we have read the peer's partial logits
+  uint64_t* x_full = s_full + 6;               // [2] peer's partial logits landed (byte count)
+  uint64_t* x_empty = x_full + 2;              // [2] peer has read what we sent (peer's credit lane)
+  uint64_t* consumed = x_full + 4;             // [2] we have read the peer's partial logits
   int32_t* rows_s = reinterpret_cast<int32_t*>(smem + OFF_ROWS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
@@ -154,7 +154,6 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     for (int i = 0; i < 2; ++i) {
       mbar_init(&x_full[i], 1);
       mbar_init(&x_empty[i], 1);
-      mbar_init(&sent[i], 128);
       mbar_init(&consumed[i], 128);
     }
     *abort_flag = 0;
@@ -182,9 +181,14 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();   // the peer's barriers exist before anyone arrives on them
-  const uint32_t tmem = *tmem_slot;
   const int n_tiles = *last_valid < 0 ? 0 : *last_valid / kNp + 1;
+  constexpr uint32_t kXBytes = kH * kNp * 4;       // one partial logit tile
+  if (tid == 0) {                                  // expect the peer's first two tiles
+    if (n_tiles > 0) mbar_arrive_expect_tx(&x_full[0], kXBytes);
+    if (n_tiles > 1) mbar_arrive_expect_tx(&x_full[1], kXBytes);
+  }
+  cluster_sync();   // the peer's barriers exist (and are armed) before anyone uses them
+  const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
     // ======================= gather: TMA part =================================
@@ -316,19 +320,18 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       (void)t_start;
       mma_commit(o_done);
     } else if (lane == 1) {
-      // ===================== exchange relay ===================================
-      // Turns the softmax threads' local "sent" / "consumed" arrivals into one
-      // cluster-scope arrival on the peer per tile, so that the softmax
-      // threads never wait for a cluster-wide release themselves.
-      const uint32_t xfull_remote = map_to_rank(smem_u32(x_full), peer);
+      // ===================== buffer credits ===================================
+      // Once the softmax threads have read the peer's tile t from exchange
+      // buffer t&1, re-arm that buffer's barrier for tile t+2, then tell the
+      // peer it may write there again.
       const uint32_t xempty_remote = map_to_rank(smem_u32(x_empty), peer);
       for (int t = 0; t < n_tiles; ++t) {
         const int bsel = t & 1;
-        const uint32_t par = (t >> 1) & 1;
-        if (!mbar_wait(&sent[bsel], par, abort_flag, err)) break;
-        mbar_arrive_remote(xfull_remote + bsel * 8);
-        if (!mbar_wait(&consumed[bsel], par, abort_flag, err)) break;
-        mbar_arrive_remote(xempty_remote + bsel * 8);
+        if (!mbar_wait(&consumed[bsel], (t >> 1) & 1, abort_flag, err)) break;
+        if (t + 2 < n_tiles) {
+          mbar_arrive_expect_tx(&x_full[bsel], kXBytes);
+          mbar_arrive_remote(xempty_remote + bsel * 8);
+        }
       }
     }
     __syncwarp();
@@ -376,16 +379,18 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       mbar_arrive(s_empty);
       return true;
     };
-    // store them into the peer's exchange buffer for tile tt
+    // store them into the peer's exchange buffer for tile tt; the bytes are
+    // counted on the peer's x_full barrier as they land
+    const uint32_t xfull_remote = map_to_rank(smem_u32(x_full), peer);
     auto send = [&](int tt, const float* v) -> bool {
       const int bsel = tt & 1;
       if (!warp_wait_cluster(&x_empty[bsel], ((tt >> 1) & 1) ^ 1, abort_flag, err)) return false;
-      const uint32_t dst = x_remote + bsel * (kH * kNp * 4);
+      const uint32_t dst = x_remote + bsel * kXBytes;
 #pragma unroll
       for (int q4 = 0; q4 < kNp / 4; ++q4)
-        st_cluster_v4(dst + q4 * (kH * 16),
-                      make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
-      mbar_arrive(&sent[bsel]);
+        st_async_v4(dst + q4 * (kH * 16),
+                    make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]),
+                    xfull_remote + bsel * 8);
       return true;
     };
 
@@ -396,7 +401,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       if (!(ok = warp_wait_cluster(&x_full[bsel], (t >> 1) & 1, abort_flag, err))) break;
 #pragma unroll
       for (int q4 = 0; q4 < kNp / 4; ++q4) {
-        const float4 pv4 = *reinterpret_cast<const float4*>(xrow + bsel * (kH * kNp * 4) +
+        const float4 pv4 = *reinterpret_cast<const float4*>(xrow + bsel * kXBytes +
                                                             q4 * (kH * 16));
         vc[4 * q4] += pv4.x; vc[4 * q4 + 1] += pv4.y; vc[4 * q4 + 2] += pv4.z; vc[4 * q4 + 3] += pv4.w;
       }
