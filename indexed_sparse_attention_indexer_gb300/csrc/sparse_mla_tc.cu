@@ -264,7 +264,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // ===================== MMA issuer =======================================
-      // Event-driven: a logit tile (QK) is issued when its gather has landed and
+      // Event-driven (non-blocking probes): a logit tile (QK) is issued when its gather has landed and
       // the TMEM logit tile is free; a P.V tile when its P is ready -- whichever
       // comes first, so a slow gather never delays the previous tile's P.V.
       bool ok = mbar_wait(q_ready, 0, abort_flag, err);
@@ -277,8 +277,8 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
         bool progress = false;
         if (qk_next < n_tiles) {
           const int st = qk_next % kStages;
-          if (mbar_try_wait(&full[st], (qk_next / kStages) & 1) &&
-              mbar_try_wait(s_empty, (qk_next & 1) ^ 1)) {
+          if (mbar_test_wait(&full[st], (qk_next / kStages) & 1) &&
+              mbar_test_wait(s_empty, (qk_next & 1) ^ 1)) {
             tc_fence_after();
             const uint64_t d0 = desc_sw128(smem_u32(smem + OFF_C + st * kStageBytes) +
                                            qk_first * kChunkBytes);
@@ -292,7 +292,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
             progress = true;
           }
         }
-        if (pv_next < qk_next && mbar_try_wait(p_full, pv_next & 1)) {
+        if (pv_next < qk_next && mbar_test_wait(p_full, pv_next & 1)) {
           tc_fence_after();
           const int st = pv_next % kStages;
           const uint64_t pd = desc_sw128(pbase);
@@ -409,7 +409,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       // start the exchange of tile t+1 before working on tile t when its logits
       // are already there; otherwise after tile t (never wait on its gather here)
       bool sent_next = false;
-      if (t + 1 < n_tiles && __all_sync(0xffffffffu, mbar_try_wait(s_full, (t + 1) & 1))) {
+      if (t + 1 < n_tiles && __all_sync(0xffffffffu, mbar_test_wait(s_full, (t + 1) & 1))) {
         if (!(ok = load_s(t + 1, vn) && send(t + 1, vn))) break;
         sent_next = true;
       }
