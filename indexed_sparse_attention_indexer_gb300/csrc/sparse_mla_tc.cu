@@ -26,8 +26,8 @@
 //   softmax (4 warps, one head per thread): read S from TMEM, exchange with
 //     the peer (software-pipelined: tile t+1 is sent before tile t is
 //     finished; st.async stores count their bytes on the peer's barrier and
-//     a lane of the MMA warp returns buffer credits), online softmax in log2
-//     units with a
+//     the MMA thread returns buffer credits), online softmax in log2 units
+//     with a
 //     lazily moved reference max (the accumulator is rescaled only when the
 //     max grows by more than 2^8), P in bf16 to shared memory.
 // Every wait is bounded; the cluster syncs once after set-up and once before
@@ -49,7 +49,7 @@ constexpr int kChunkBytes = kNp * 128;         // one 64-dim block of a tile: 8 
 constexpr int kStageBytes = kChunks * kChunkBytes;
 // 8 warps: two per SM sub-partition, so each thread may use up to 255 registers
 constexpr int kProducerWarps = 3;
-constexpr int kMmaWarp = kProducerWarps;       // warp 3: lane 0 issues MMAs, lane 1 relays
+constexpr int kMmaWarp = kProducerWarps;       // warp 3: lane 0 issues MMAs and buffer credits
 constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;   // 256
 // Each tile is gathered by two engines at once: TMA gather4 (warp 0) for the
 // first kTmaChunks 64-dim blocks, cp.async (warps 1-2) for the rest.
@@ -233,13 +233,13 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   } else if (warp < kProducerWarps) {
     // ======================= gather: cp.async part ============================
     // the remaining 64-dim blocks: half a warp per row (16 lanes x 16 bytes =
-    // two blocks), each piece to its swizzled place; a tile's copies are
-    // signalled (after a proxy fence) once the next tile's are in flight
+    // two blocks), each piece to its swizzled place; each tile is signalled
+    // (after a proxy fence) once its copies have landed
     constexpr int kLdgPieces = (kChunks - kTmaChunks) * 8;   // 16-byte pieces per row
     static_assert(kLdgPieces == 16, "half a warp per row");
     const int sub = lane >> 4, pi = lane & 15;
     const int ch = kTmaChunks + (pi >> 3), u = pi & 7;
-    int stage = 0, prev = -1;
+    int stage = 0;
     uint32_t ph = 0;
     for (int t = 0; t < n_tiles; ++t) {
       if (!mbar_wait(&empty[stage], ph ^ 1, abort_flag, err)) break;
@@ -250,31 +250,55 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
                     c.latent + (int64_t)pr * DSI_D_QK + (g0 + ch) * 64 + u * 8);
       }
       cp_async_commit();
-      if (prev >= 0) {
-        cp_async_wait<1>();
-        fence_proxy_async_smem();
-        mbar_arrive(&full[prev]);
-      }
-      prev = stage;
+      // signal this tile as soon as its own copies have landed (not after the
+      // next tile's issue, which would tie it to an older stage's release)
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(&full[stage]);
       if (++stage == kStages) { stage = 0; ph ^= 1; }
     }
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (prev >= 0) mbar_arrive(&full[prev]);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // ===================== MMA issuer =======================================
-      // Event-driven (non-blocking probes): a logit tile (QK) is issued when its gather has landed and
-      // the TMEM logit tile is free; a P.V tile when its P is ready -- whichever
-      // comes first, so a slow gather never delays the previous tile's P.V.
+      // Event-driven with non-blocking probes (nothing in this warp ever
+      // suspends): a logit tile (QK) is issued when its gather has landed and
+      // the TMEM logit tile is free; a P.V tile when its P is ready; an
+      // exchange-buffer credit when the softmax threads have read the buffer.
       bool ok = mbar_wait(q_ready, 0, abort_flag, err);
       tc_fence_after();
-      int qk_next = 0, pv_next = 0;
+      int qk_next = 0, pv_next = 0, cr_next = 0;
+      const uint32_t xempty_remote = map_to_rank(smem_u32(x_empty), peer);
       const uint32_t pbase = smem_u32(smem + OFF_P);
       const uint64_t t_start = global_ns();
       uint64_t t_last = t_start;
-      while (ok && pv_next < n_tiles) {
+      while (ok && (pv_next < n_tiles || cr_next < n_tiles)) {
         bool progress = false;
+        // buffer credit: the softmax threads have read the peer's tile cr_next
+        // from exchange buffer cr_next&1; re-arm it for tile cr_next+2, then let
+        // the peer write there again
+        if (cr_next < n_tiles && mbar_test_wait(&consumed[cr_next & 1], (cr_next >> 1) & 1)) {
+          if (cr_next + 2 < n_tiles) {
+            mbar_arrive_expect_tx(&x_full[cr_next & 1], kXBytes);
+            mbar_arrive_remote(xempty_remote + (cr_next & 1) * 8);
+          }
+          ++cr_next;
+          progress = true;
+        }
+        if (pv_next < qk_next && mbar_test_wait(p_full, pv_next & 1)) {
+          tc_fence_after();
+          const int st = pv_next % kStages;
+          const uint64_t pd = desc_sw128(pbase);
+          const uint64_t vd = desc_sw128_mn(smem_u32(smem + OFF_C + st * kStageBytes), kChunkBytes);
+#pragma unroll
+          for (int kk = 0; kk < kNp / 16; ++kk)
+            mma_bf16(tmem + TM_O, pd + (uint64_t)((kk * 32) >> 4), vd + (uint64_t)((kk * 2048) >> 4),
+                     IDESC_O, (pv_next > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(p_empty);
+          mma_commit(&empty[st]);
+          ++pv_next;
+          progress = true;
+        }
         if (qk_next < n_tiles) {
           const int st = qk_next % kStages;
           if (mbar_test_wait(&full[st], (qk_next / kStages) & 1) &&
@@ -292,20 +316,6 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
             progress = true;
           }
         }
-        if (pv_next < qk_next && mbar_test_wait(p_full, pv_next & 1)) {
-          tc_fence_after();
-          const int st = pv_next % kStages;
-          const uint64_t pd = desc_sw128(pbase);
-          const uint64_t vd = desc_sw128_mn(smem_u32(smem + OFF_C + st * kStageBytes), kChunkBytes);
-#pragma unroll
-          for (int kk = 0; kk < kNp / 16; ++kk)
-            mma_bf16(tmem + TM_O, pd + (uint64_t)((kk * 32) >> 4), vd + (uint64_t)((kk * 2048) >> 4),
-                     IDESC_O, (pv_next > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(p_empty);
-          mma_commit(&empty[st]);
-          ++pv_next;
-          progress = true;
-        }
         // bounded: give up after kWaitLimitNs without progress
         if (progress) {
           t_last = global_ns();
@@ -319,20 +329,6 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       }
       (void)t_start;
       mma_commit(o_done);
-    } else if (lane == 1) {
-      // ===================== buffer credits ===================================
-      // Once the softmax threads have read the peer's tile t from exchange
-      // buffer t&1, re-arm that buffer's barrier for tile t+2, then tell the
-      // peer it may write there again.
-      const uint32_t xempty_remote = map_to_rank(smem_u32(x_empty), peer);
-      for (int t = 0; t < n_tiles; ++t) {
-        const int bsel = t & 1;
-        if (!mbar_wait(&consumed[bsel], (t >> 1) & 1, abort_flag, err)) break;
-        if (t + 2 < n_tiles) {
-          mbar_arrive_expect_tx(&x_full[bsel], kXBytes);
-          mbar_arrive_remote(xempty_remote + bsel * 8);
-        }
-      }
     }
     __syncwarp();
   } else {
