@@ -26,7 +26,7 @@
 //   softmax (4 warps, one head per thread): read S from TMEM, exchange with
 //     the peer (software-pipelined: tile t+1 is sent before tile t is
 //     finished; st.async stores count their bytes on the peer's barrier and
-//     the MMA thread returns buffer credits), online softmax in log2 units
+//     each warp returns a buffer credit), online softmax in log2 units
 //     with a
 //     lazily moved reference max (the accumulator is rescaled only when the
 //     max grows by more than 2^8), P in bf16 to shared memory.
@@ -49,7 +49,7 @@ constexpr int kChunkBytes = kNp * 128;         // one 64-dim block of a tile: 8 
 constexpr int kStageBytes = kChunks * kChunkBytes;
 // 8 warps: two per SM sub-partition, so each thread may use up to 255 registers
 constexpr int kProducerWarps = 3;
-constexpr int kMmaWarp = kProducerWarps;       // warp 3: lane 0 issues MMAs and buffer credits
+constexpr int kMmaWarp = kProducerWarps;       // warp 3: lane 0 issues the MMAs
 constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;   // 256
 // Each tile is gathered by two engines at once: TMA gather4 (warp 0) for the
 // first kTmaChunks 64-dim blocks, cp.async (warps 1-2) for the rest.
@@ -64,7 +64,7 @@ constexpr int OFF_P = OFF_C + kStages * kStageBytes;      // P [128 x 64] bf16, 
 constexpr int OFF_X = OFF_P + kH * kNp * 2;               // 2 x peer logits [128 x 64] fp32
 constexpr int OFF_ROWS = OFF_X + 2 * kH * kNp * 4;        // physical row of each entry (or -1)
 constexpr int OFF_BAR = OFF_ROWS + kMaxEntries * 4;
-constexpr int NBARS = 2 * kStages + 6 + 6;
+constexpr int NBARS = 2 * kStages + 6 + 4;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM = OFF_MISC + 64 + 1024;
 
@@ -120,8 +120,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   uint64_t* q_ready = s_full + 4;              // query slice in TMEM (softmax threads)
   uint64_t* o_done = s_full + 5;               // last P.V done (MMA commit)
   uint64_t* x_full = s_full + 6;               // [2] peer's partial logits landed (byte count)
-  uint64_t* x_empty = x_full + 2;              // [2] peer has read what we sent (peer's credit lane)
-  uint64_t* consumed = x_full + 4;             // [2] we have read the peer's partial logits
+  uint64_t* x_empty = x_full + 2;              // [2] peer has read what we sent (one credit per peer softmax warp)
   int32_t* rows_s = reinterpret_cast<int32_t*>(smem + OFF_ROWS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
@@ -153,8 +152,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     mbar_init(o_done, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&x_full[i], 1);
-      mbar_init(&x_empty[i], 1);
-      mbar_init(&consumed[i], 128);
+      mbar_init(&x_empty[i], 4);
     }
     *abort_flag = 0;
     *last_valid = -1;
@@ -262,29 +260,16 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     if (lane == 0) {
       // ===================== MMA issuer =======================================
       // Event-driven with non-blocking probes (nothing in this warp ever
-      // suspends): a logit tile (QK) is issued when its gather has landed and
-      // the TMEM logit tile is free; a P.V tile when its P is ready; an
-      // exchange-buffer credit when the softmax threads have read the buffer.
+      // suspends): a P.V tile is issued when its P is ready, a logit tile (QK)
+      // when its gather has landed and the TMEM logit tile is free.
       bool ok = mbar_wait(q_ready, 0, abort_flag, err);
       tc_fence_after();
-      int qk_next = 0, pv_next = 0, cr_next = 0;
-      const uint32_t xempty_remote = map_to_rank(smem_u32(x_empty), peer);
+      int qk_next = 0, pv_next = 0;
       const uint32_t pbase = smem_u32(smem + OFF_P);
       const uint64_t t_start = global_ns();
       uint64_t t_last = t_start;
-      while (ok && (pv_next < n_tiles || cr_next < n_tiles)) {
+      while (ok && pv_next < n_tiles) {
         bool progress = false;
-        // buffer credit: the softmax threads have read the peer's tile cr_next
-        // from exchange buffer cr_next&1; re-arm it for tile cr_next+2, then let
-        // the peer write there again
-        if (cr_next < n_tiles && mbar_test_wait(&consumed[cr_next & 1], (cr_next >> 1) & 1)) {
-          if (cr_next + 2 < n_tiles) {
-            mbar_arrive_expect_tx(&x_full[cr_next & 1], kXBytes);
-            mbar_arrive_remote(xempty_remote + (cr_next & 1) * 8);
-          }
-          ++cr_next;
-          progress = true;
-        }
         if (pv_next < qk_next && mbar_test_wait(p_full, pv_next & 1)) {
           tc_fence_after();
           const int st = pv_next % kStages;
@@ -378,6 +363,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     // store them into the peer's exchange buffer for tile tt; the bytes are
     // counted on the peer's x_full barrier as they land
     const uint32_t xfull_remote = map_to_rank(smem_u32(x_full), peer);
+    const uint32_t xempty_remote = map_to_rank(smem_u32(x_empty), peer);
     auto send = [&](int tt, const float* v) -> bool {
       const int bsel = tt & 1;
       if (!warp_wait_cluster(&x_empty[bsel], ((tt >> 1) & 1) ^ 1, abort_flag, err)) return false;
@@ -401,7 +387,16 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
                                                             q4 * (kH * 16));
         vc[4 * q4] += pv4.x; vc[4 * q4 + 1] += pv4.y; vc[4 * q4 + 2] += pv4.z; vc[4 * q4 + 3] += pv4.w;
       }
-      mbar_arrive(&consumed[bsel]);
+      // buffer credit, one per warp: this warp has read the peer's tile t, so
+      // the peer may write tile t+2 there; warp 0 re-arms the byte count.  The
+      // loads above completed (their values are summed) before the warp
+      // barrier, so relaxed arrivals suffice; a cluster-scope release here
+      // measured about 15% slower over the whole kernel.
+      __syncwarp();
+      if (lane == 0 && t + 2 < n_tiles) {
+        if (quarter == 0) mbar_arrive_expect_tx_relaxed(&x_full[bsel], kXBytes);
+        mbar_arrive_remote_relaxed(xempty_remote + bsel * 8);
+      }
       // start the exchange of tile t+1 before working on tile t when its logits
       // are already there; otherwise after tile t (never wait on its gather here)
       bool sent_next = false;

@@ -170,6 +170,18 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t raddr) {
       "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(raddr)
       : "memory");
 }
+// Arrival on a peer CTA's barrier that orders nothing else (no release): for
+// credits whose protected accesses have visibly completed already.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t raddr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(raddr)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_relaxed(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;\n" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
 // Whole-cluster barrier (every thread of every CTA of the cluster).
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n"
