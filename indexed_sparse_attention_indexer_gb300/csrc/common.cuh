@@ -51,7 +51,8 @@ __device__ __forceinline__ int64_t visible_len(const CacheView& c, int r, int de
 // returned (after flagging the status word) when it is out of range.
 __device__ __forceinline__ int64_t phys_row(const CacheView& c, int b, int64_t p, int* err) {
   if (c.block_table == nullptr) return (int64_t)b * c.s_max + p;
-  const int64_t pg = p / c.page_size;
+  // positions come from int32 indices: divide in 32 bits when they fit
+  const int64_t pg = (p >= 0 && p <= 0x7fffffff) ? (int64_t)((int)p / c.page_size) : p / c.page_size;
 #ifdef DSI_CHECKED
   if (pg < 0 || pg >= c.max_pages) { report(err, kErrBounds); return -1; }
 #endif

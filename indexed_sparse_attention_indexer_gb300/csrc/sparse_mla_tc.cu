@@ -58,6 +58,7 @@ constexpr int kLdgWarps = kProducerWarps - 1;
 constexpr int kLdgThreads = kLdgWarps * 32;
 
 constexpr int kMaxEntries = DSI_MAX_K;         // index entries one split can hold
+static_assert(kMaxEntries % kThreads == 0, "entries spread evenly over the threads");
 
 constexpr int OFF_C = 0;
 constexpr int OFF_P = OFF_C + kStages * kStageBytes;      // P [128 x 64] bf16, 16 KB
@@ -141,6 +142,16 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   const int32_t* irow = a.idx + (int64_t)r * a.K;
   const int g0 = rho ? 4 : 0;                      // first gathered 64-dim block
   const int qk_first = rho ? 1 : 0;                // first stage block used by the logits
+  // softmax threads: this CTA's slice of the head's query row is loaded now,
+  // so it lands while the entries are being staged
+  uint4 qv[kChunks * 8];
+  if (warp > kMmaWarp) {
+    const uint4* qsrc = reinterpret_cast<const uint4*>(
+        a.q + ((int64_t)r * kH + (warp & 3) * 32 + lane) * DSI_D_QK + (g0 + qk_first) * 64);
+    const int nq = (kChunks - qk_first) * 8;
+#pragma unroll
+    for (int i = 0; i < kChunks * 8; ++i) qv[i] = i < nq ? __ldg(qsrc + i) : make_uint4(0, 0, 0, 0);
+  }
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1 + kLdgThreads); mbar_init(&empty[s], 1); }
@@ -160,21 +171,32 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   }
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, TMEM_COLS);
   __syncthreads();
-  // the split's entries, translated once to physical cache rows (-1 = skipped)
-  for (int jj = tid; jj < span; jj += kThreads) {
-    const int j = j_begin + jj;
-    int pr = -1;
-    if (j < j_end) {
-      const int pos = __ldg(irow + j);
-#ifdef DSI_CHECKED
-      if (pos >= n_vis) report(err, kErrBounds);
-#endif
-      if (pos_ok(pos, n_vis)) {
-        const int64_t x = phys_row(c, b, pos, err);
-        if (x >= 0) { pr = (int)x; atomicMax(last_valid, jj); }
-      }
+  // the split's entries, translated once to physical cache rows (-1 = skipped);
+  // a thread's index loads are all issued before any translation
+  {
+    constexpr int kPer = kMaxEntries / kThreads;
+    int pos[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int jj = tid + u * kThreads;
+      pos[u] = (jj < span && j_begin + jj < j_end) ? __ldg(irow + j_begin + jj) : -1;
     }
-    rows_s[jj] = pr;
+    int lv = -1;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int jj = tid + u * kThreads;
+      if (jj >= span) break;
+      int pr = -1;
+#ifdef DSI_CHECKED
+      if (pos[u] >= n_vis) report(err, kErrBounds);
+#endif
+      if (pos_ok(pos[u], n_vis)) {
+        const int64_t x = phys_row(c, b, pos[u], err);
+        if (x >= 0) { pr = (int)x; lv = jj; }
+      }
+      rows_s[jj] = pr;
+    }
+    if (lv >= 0) atomicMax(last_valid, lv);
   }
   tc_fence_before();
   __syncthreads();
@@ -323,17 +345,17 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     // this CTA's slice of the query row into TMEM (columns pack bf16 pairs)
     {
-      const int qcols = (kChunks - qk_first) * 32;
-      const uint32_t* qsrc = reinterpret_cast<const uint32_t*>(
-          a.q + ((int64_t)r * kH + h) * DSI_D_QK + (g0 + qk_first) * 64);
-      for (int c0 = 0; c0 < qcols; c0 += 32) {
-        uint32_t w32[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qsrc + c0) + i);
-          w32[4 * i] = v.x; w32[4 * i + 1] = v.y; w32[4 * i + 2] = v.z; w32[4 * i + 3] = v.w;
+      for (int ch = 0; ch < kChunks; ++ch) {
+        if (ch < kChunks - qk_first) {      // CTA-uniform
+          uint32_t w32[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = qv[8 * ch + i];
+            w32[4 * i] = v.x; w32[4 * i + 1] = v.y; w32[4 * i + 2] = v.z; w32[4 * i + 3] = v.w;
+          }
+          tmem_st32(tmem + lane_base + TM_Q + ch * 32, w32);
         }
-        tmem_st32(tmem + lane_base + TM_Q + c0, w32);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -407,14 +429,24 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       // validity of the tile's 64 entries
       const uint32_t m_lo = __ballot_sync(0xffffffffu, rows_s[t * kNp + lane] >= 0);
       const uint32_t m_hi = __ballot_sync(0xffffffffu, rows_s[t * kNp + 32 + lane] >= 0);
-      // online softmax in log2 units
-      float tmax = -INFINITY;
+      if ((m_lo & m_hi) != 0xffffffffu) {   // warp-uniform: the tile has skipped entries
 #pragma unroll
-      for (int j = 0; j < kNp; ++j) {
-        const bool on = ((j < 32 ? m_lo >> j : m_hi >> (j - 32)) & 1u) != 0;
-        vc[j] = on ? vc[j] * sl2 : -INFINITY;
-        tmax = fmaxf(tmax, vc[j]);
+        for (int j = 0; j < kNp; ++j)
+          if ((((j < 32 ? m_lo >> j : m_hi >> (j - 32)) & 1u)) == 0) vc[j] = -INFINITY;
       }
+      // online softmax in log2 units.  The tile max is taken on the raw sums
+      // (scaling by sl2 > 0 keeps the order, and rounding is monotone) in
+      // eight independent chains.
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = vc[i];
+#pragma unroll
+      for (int j = 8; j < kNp; ++j) mx[j & 7] = fmaxf(mx[j & 7], vc[j]);
+#pragma unroll
+      for (int w2 = 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+        for (int i = 0; i < w2; ++i) mx[i] = fmaxf(mx[i], mx[i + w2]);
+      const float tmax = mx[0] * sl2;
       float alpha = 1.f;
       bool rescale = false;
       if (m_ref == -INFINITY) {
@@ -440,26 +472,32 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
         }
         tmem_st_wait();
       }
-      // P = 2^(logit - reference) in bf16, straight into the swizzled P tile
-      float psum = 0.f;
+      // P = 2^(logit * sl2 - reference) in bf16, straight into the swizzled P
+      // tile; the row sum adds the rounded values (what P.V multiplies), in
+      // eight independent chains
+      float ps[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ps[i] = 0.f;
       // 2^(-inf) is 0 for skipped entries; a reference of -inf means every
       // entry so far was skipped (all probabilities 0)
-      const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const float nmr = (m_ref == -INFINITY) ? 0.f : -m_ref;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         uint32_t w4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = 8 * u + 2 * e;
-          const float e0 = ex2_approx(vc[j] - mr);
-          const float e1 = ex2_approx(vc[j + 1] - mr);
+          const float e0 = ex2_approx(fmaf(vc[j], sl2, nmr));
+          const float e1 = ex2_approx(fmaf(vc[j + 1], sl2, nmr));
           const __nv_bfloat162 p2 = __floats2bfloat162_rn(e0, e1);
           const float2 pr = __bfloat1622float2(p2);
-          psum += pr.x + pr.y;
+          ps[2 * e] += pr.x;
+          ps[2 * e + 1] += pr.y;
           w4[e] = *reinterpret_cast<const uint32_t*>(&p2);
         }
         *reinterpret_cast<uint4*>(prow + sw128_offset(h, u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
+      const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l_sum = l_sum * alpha + psum;     // alpha == 1 for heads that did not move their reference
       fence_proxy_async_smem();
       tc_fence_before();
