@@ -5,12 +5,24 @@
 // Practices", "Internal Fusion of the Indexer": Top-K completed on chip, only
 // the selected indices leave the kernel.)
 //
-// One block per row.  Scores become order-preserving 32-bit keys.  Four
-// 8-bit MSB-first histogram passes find the exact K-th largest key T and how
-// many keys equal to T must be kept (the lowest positions among them).  A
-// final pass walks the row in position order with block-wide prefix sums and
-// writes the kept positions ascending.  Rows that fit are staged in shared
-// memory once; longer rows are re-read from global memory (L2) each pass.
+// One block per row.  Scores become order-preserving 32-bit keys; the search
+// finds the exact K-th largest key T and how many keys equal to T must be kept
+// (the lowest positions among them), then the kept positions are written
+// ascending with block-wide prefix sums.
+//
+// Rows of up to 32768 positions (topk_rows_reg): the keys stay in registers,
+// each warp holding 1024 consecutive positions.  The search narrows an interval [lo, hi]
+// that holds T, starting from the row's min and max key: each pass splits the
+// interval into 2048 equal bins (11 bits of the key range per pass, so at most
+// three passes) and keeps the bin where the count from the top reaches K.
+// Bins follow the keys' actual range, so the histogram atomics stay spread
+// out even when most scores share their top bits.  The compaction ranks the
+// warps once (per-warp counts) and then each warp walks its positions in
+// order with ballots, so every store of a round is one contiguous run.
+//
+// Longer rows (topk_rows): four 8-bit MSB-first histogram passes and a
+// compaction walking the row in chunks; rows that fit are staged in shared
+// memory once, longer ones re-read from global memory (L2) each pass.
 #include "kernels.h"
 
 namespace dsi {
@@ -132,11 +144,186 @@ topk_rows(const float* __restrict__ scores, int64_t ld, const int32_t* __restric
   if (count && tid == 0) count[r] = K;
 }
 
+constexpr int kRegPer = 32;                               // keys per thread
+constexpr int kRegKeysMax = kTopkThreads * kRegPer;        // 32768
+constexpr int kBins = 2048;                                // 11-bit digits of the key range
+constexpr int kWarps = kTopkThreads / 32;
+static_assert(kBins == 64 * kWarps, "each warp owns 64 bins in the bin search");
+
+__global__ void __launch_bounds__(kTopkThreads, 1)
+topk_rows_reg(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
+              int64_t q_offset, int K, int32_t* __restrict__ idx, int32_t* __restrict__ count) {
+  __shared__ int hist[2][kBins];          // alternate passes; each is cleared as it is read
+  __shared__ int wsum[2][kWarps];
+  __shared__ int wbase[2][kWarps];
+  __shared__ uint32_t s_sel[2];
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const unsigned kAll = 0xffffffffu;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int64_t n = row_len ? (int64_t)row_len[r] : q_offset + r + 1;
+  if (n < 0) n = 0;
+  if (n > ld) n = ld;
+  int32_t* out = idx + (int64_t)r * K;
+  const float* grow = scores + (int64_t)r * ld;
+  if (n <= K) {  // every candidate is kept
+    for (int64_t j = tid; j < K; j += blockDim.x) out[j] = j < n ? (int32_t)j : -1;
+    if (count && tid == 0) count[r] = (int32_t)n;
+    return;
+  }
+  // ---- keys: warp w holds positions 1024w .. 1024w+1023; in round i lane l
+  // holds position 1024w + 32i + l (every load is one coalesced line per warp).
+  // Valid keys are at least 1 (every non-NaN score maps far above it); slots
+  // past the row end hold 0, so they fall below every interval searched and
+  // below T, and need no separate validity test.
+  const int wpos = wid * (kRegPer * 32);
+  uint32_t key[kRegPer];
+#pragma unroll
+  for (int i = 0; i < kRegPer; ++i) {
+    const int p = wpos + 32 * i + lane;
+    key[i] = p < n ? max(score_key(__ldg(grow + p)), 1u) : 0u;
+  }
+  for (int i = tid; i < 2 * kBins; i += blockDim.x) (&hist[0][0])[i] = 0;
+  // ---- the row's key range ------------------------------------------------
+  {
+    uint32_t kmax = 0u, kmin = 0xffffffffu;
+#pragma unroll
+    for (int i = 0; i < kRegPer; ++i) {
+      kmax = max(kmax, key[i]);
+      kmin = min(kmin, key[i] == 0u ? 0xffffffffu : key[i]);
+    }
+    kmax = __reduce_max_sync(kAll, kmax);
+    kmin = __reduce_min_sync(kAll, kmin);
+    if (lane == 0) { wsum[0][wid] = (int)kmax; wsum[1][wid] = (int)kmin; }
+    __syncthreads();
+    if (wid == 0) {
+      kmax = __reduce_max_sync(kAll, (uint32_t)wsum[0][lane]);
+      kmin = __reduce_min_sync(kAll, (uint32_t)wsum[1][lane]);
+      if (lane == 0) { s_sel[0] = kmin; s_sel[1] = kmax; }
+    }
+    __syncthreads();
+  }
+  uint32_t lo = s_sel[0], hi = s_sel[1];
+  int krem = K;   // keys to take from [lo, hi], counted from the top; T is in [lo, hi]
+  // ---- narrow [lo, hi] to T, 11 bits of the range per pass -------------------
+  int pass = 0;
+#pragma unroll 1
+  while (lo != hi) {
+    const uint32_t span = hi - lo;
+    const int bits = 32 - __clz(span);
+    const int sh = bits > 11 ? bits - 11 : 0;          // bins of 2^sh keys cover [lo, hi]
+    int* h = hist[pass & 1];
+#pragma unroll
+    for (int i = 0; i < kRegPer; ++i) {
+      const uint32_t off = key[i] - lo;                 // wraps for keys below lo
+      if (off <= span) atomicAdd(&h[off >> sh], 1);
+    }
+    __syncthreads();
+    // warp w owns bins 2047-64w down to 1984-64w, lane l the pair starting at
+    // 2047-64w-2l; both are cleared for the pass after next
+    const int b0 = kBins - 1 - 64 * wid - 2 * lane;
+    const int c0 = h[b0], c1 = h[b0 - 1];
+    h[b0] = 0;
+    h[b0 - 1] = 0;
+    int incl = c0 + c1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kAll, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[pass & 1][wid] = incl;
+    __syncthreads();
+    // keys in the bins of the warps above this one
+    const int wt = wsum[pass & 1][lane];
+    int wincl = wt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kAll, wincl, o);
+      if (lane >= o) wincl += y;
+    }
+    const int above_w = __shfl_sync(kAll, wincl - wt, wid);
+    const int above = above_w + incl - (c0 + c1);       // keys in the bins above this pair
+    if (above < krem && above + c0 + c1 >= krem) {
+      if (above + c0 >= krem) { s_sel[0] = (uint32_t)b0; s_sel[1] = (uint32_t)above; }
+      else { s_sel[0] = (uint32_t)(b0 - 1); s_sel[1] = (uint32_t)(above + c0); }
+    }
+    __syncthreads();
+    const uint32_t b = s_sel[0];
+    krem -= (int)s_sel[1];
+    const uint64_t top = (uint64_t)lo + ((uint64_t)(b + 1) << sh) - 1;
+    lo += b << sh;
+    hi = top < (uint64_t)hi ? (uint32_t)top : hi;
+    ++pass;
+    if (sh == 0) break;
+  }
+  const uint32_t T = lo;
+  // ---- ordered compaction -----------------------------------------------------
+  // per-warp counts of keys above T and equal to T; warp 0 turns them into
+  // each warp's rank among equals and output offset
+  int gt = 0, eq = 0;
+#pragma unroll
+  for (int i = 0; i < kRegPer; ++i) { gt += key[i] > T; eq += key[i] == T; }
+  gt = __reduce_add_sync(kAll, gt);
+  eq = __reduce_add_sync(kAll, eq);
+  __syncthreads();                       // s_sel / wsum readers of the last pass are done
+  if (lane == 0) { wsum[0][wid] = gt; wsum[1][wid] = eq; }
+  __syncthreads();
+  if (wid == 0) {
+    const int g = wsum[0][lane], e = wsum[1][lane];
+    int ei = e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kAll, ei, o);
+      if (lane >= o) ei += y;
+    }
+    const int ebase = ei - e;
+    int take = krem - ebase;
+    take = take < 0 ? 0 : (take > e ? e : take);
+    const int sel = g + take;
+    int si = sel;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kAll, si, o);
+      if (lane >= o) si += y;
+    }
+    wbase[0][lane] = ebase;
+    wbase[1][lane] = si - sel;
+  }
+  __syncthreads();
+  int eq_rank = wbase[0][wid], pos = wbase[1][wid];
+  if (eq == 0) {                         // warp-uniform: no ties at T in this warp
+#pragma unroll
+    for (int i = 0; i < kRegPer; ++i) {
+      const bool keep = key[i] > T;
+      const unsigned km = __ballot_sync(kAll, keep);
+      if (keep) out[pos + __popc(km & lt_mask)] = wpos + 32 * i + lane;
+      pos += __popc(km);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kRegPer; ++i) {
+      const bool is_eq = key[i] == T;
+      const unsigned em = __ballot_sync(kAll, is_eq);
+      const bool keep = key[i] > T || (is_eq && eq_rank + __popc(em & lt_mask) < krem);
+      const unsigned km = __ballot_sync(kAll, keep);
+      if (keep) out[pos + __popc(km & lt_mask)] = wpos + 32 * i + lane;
+      pos += __popc(km);
+      eq_rank += __popc(em);
+    }
+  }
+  if (count && tid == 0) count[r] = K;
+}
+
 cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t* row_len,
                         int64_t q_offset, int K, int32_t* idx, int32_t* count, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  // stage rows in shared memory when the longest possible row fits
   const int64_t longest = row_len ? ld : (q_offset + rows < ld ? q_offset + rows : ld);
+  if (longest <= kRegKeysMax) {
+    topk_rows_reg<<<rows, kTopkThreads, 0, st>>>(scores, ld, row_len, q_offset, K, idx, count);
+    note_launch();
+    return cudaGetLastError();
+  }
+  // stage rows in shared memory when the longest possible row fits
   const int stage = longest <= kTopkSmemKeys;
   const size_t smem = stage ? (size_t)longest * sizeof(uint32_t) : 0;
   if (smem > 48 * 1024) {

@@ -189,6 +189,9 @@ TOPK_CASES = [
     (4, 33000, 1, 3, False),
     (3, 600, 600, 5, False),          # K == n
     (2, 70000, 4096, 1 << 20, False),
+    (3, 32768, 2048, 1 << 20, True),  # the register-resident kernel at its largest rows
+    (2, 32767, 2048, 7, False),       # odd row stride (unaligned rows, scalar loads)
+    (2, 32769, 100, 50, False),       # one past the register-resident kernel
 ]
 
 
@@ -207,6 +210,26 @@ def test_topk_ties_and_lengths(case):
     for r in range(rows):
         n = int(lens[r])
         exp, cnt = oracle.topk_select(sc[r, :n].numpy(), K)
+        assert np.array_equal(idx[r].cpu().numpy(), exp), f"row {r}"
+        assert int(count[r]) == cnt
+
+
+def test_topk_wide_key_range_and_constant_rows():
+    """Scores spread over many binades (and signs), plus rows that are constant or
+    hold one distinct value above a constant floor."""
+    rows, ld, K = 4, 32768, 2048
+    gen = torch.Generator().manual_seed(11)
+    mag = torch.exp2(torch.rand((rows, ld), generator=gen) * 120 - 60)
+    sign = torch.where(torch.rand((rows, ld), generator=gen) < 0.3, -1.0, 1.0)
+    sc = mag * sign
+    sc[2] = 1.5
+    sc[3] = -2.0
+    sc[3, 12345] = 7.0
+    g = sc.to(DEV)
+    idx, count = binding.topk(g, K, row_len=torch.full((rows,), ld, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    for r in range(rows):
+        exp, cnt = oracle.topk_select(sc[r].numpy(), K)
         assert np.array_equal(idx[r].cpu().numpy(), exp), f"row {r}"
         assert int(count[r]) == cnt
 
