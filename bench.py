@@ -235,7 +235,9 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     cfg = W.CONFIGS[args.config]
-    ws = W.make_config(args.config, device=dev)  # seeded per config; each rank its own replica
+    # seeded per config; each rank its own replica (--rows: a smaller decode batch
+    # for profiling captures, never a bench line)
+    ws = W.make_config(args.config, device=dev, rows=args.rows)
     torch.cuda.synchronize()
     binding.load()
     stream = torch.cuda.current_stream()
@@ -330,6 +332,8 @@ def run_gpu(args):
             "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
             "gpu_launches_per_step": launches / args.steps, "clocks": clk,
         }
+        if args.rows:
+            result["config"]["profiling_rows"] = args.rows
         if world == 1 and not args.no_cpu:
             result["cpu_baseline"] = cpu_baseline(ws, budget_s=args.cpu_seconds)
     barrier(world)
@@ -460,6 +464,8 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="profiling aid: a smaller decode batch (the printed line is not a bench line)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

@@ -290,10 +290,14 @@ CONFIGS = {
 }
 
 
-def make_config(cfg: int, device="cpu", chunk: int = 0) -> Workload:
+def make_config(cfg: int, device="cpu", chunk: int = 0, rows: int | None = None) -> Workload:
+    """The named workload; ``rows`` shrinks a decode batch (same shapes per
+    sequence, fewer sequences) for profiling captures that must stay small."""
     c = CONFIGS[cfg]
+    if rows is not None and cfg not in (1, 2, 5):
+        raise ValueError("rows applies to the decode workloads only")
     if cfg in (1, 2):
-        return make_decode(c["B"], c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
+        return make_decode(rows or c["B"], c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
                            device=device, name=c["name"])
     if cfg == 3:
         return make_prefill(c["T"], c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
@@ -303,7 +307,7 @@ def make_config(cfg: int, device="cpu", chunk: int = 0) -> Workload:
         return make_chunk(k_idx, latent, chunk, c["T"], c["H_i"], c["K"], c["H"], c["seed"],
                           name=c["name"])
     if cfg == 5:
-        return make_decode(c["B"], 0, c["H_i"], c["d"], c["K"], c["H"], c["seed"],
+        return make_decode(rows or c["B"], 0, c["H_i"], c["d"], c["K"], c["H"], c["seed"],
                            device=device, loguniform=(c["lo"], c["hi"]),
                            page_size=c["page_size"], k_fp8=True, name=c["name"])
     raise ValueError(cfg)
