@@ -45,6 +45,7 @@ constexpr int kH = 128;                        // heads (MMA M)
 constexpr int kNp = 64;                        // positions per tile (MMA N of the logits)
 constexpr int kChunks = 5;                     // 64-dim blocks each CTA gathers per row
 constexpr int kStages = 3;
+constexpr int kXBufs = 2;                      // exchange buffers for the peer's partial logits
 constexpr int kChunkBytes = kNp * 128;         // one 64-dim block of a tile: 8 KB
 constexpr int kStageBytes = kChunks * kChunkBytes;
 // 8 warps: two per SM sub-partition, so each thread may use up to 255 registers
@@ -62,10 +63,10 @@ static_assert(kMaxEntries % kThreads == 0, "entries spread evenly over the threa
 
 constexpr int OFF_C = 0;
 constexpr int OFF_P = OFF_C + kStages * kStageBytes;      // P [128 x 64] bf16, 16 KB
-constexpr int OFF_X = OFF_P + kH * kNp * 2;               // 2 x peer logits [128 x 64] fp32
-constexpr int OFF_ROWS = OFF_X + 2 * kH * kNp * 4;        // physical row of each entry (or -1)
+constexpr int OFF_X = OFF_P + kH * kNp * 2;               // kXBufs x peer logits [128 x 64] fp32
+constexpr int OFF_ROWS = OFF_X + kXBufs * kH * kNp * 4;   // physical row of each entry (or -1)
 constexpr int OFF_BAR = OFF_ROWS + kMaxEntries * 4;
-constexpr int NBARS = 2 * kStages + 6 + 4;
+constexpr int NBARS = 2 * kStages + 6 + 2 * kXBufs;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM = OFF_MISC + 64 + 1024;
 
@@ -120,8 +121,8 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   uint64_t* p_empty = s_full + 3;              // P.V done (MMA commit)
   uint64_t* q_ready = s_full + 4;              // query slice in TMEM (softmax threads)
   uint64_t* o_done = s_full + 5;               // last P.V done (MMA commit)
-  uint64_t* x_full = s_full + 6;               // [2] peer's partial logits landed (byte count)
-  uint64_t* x_empty = x_full + 2;              // [2] peer has read what we sent (one credit per peer softmax warp)
+  uint64_t* x_full = s_full + 6;               // [kXBufs] peer's partial logits landed (byte count)
+  uint64_t* x_empty = x_full + kXBufs;         // [kXBufs] peer has read what we sent (one credit per peer softmax warp)
   int32_t* rows_s = reinterpret_cast<int32_t*>(smem + OFF_ROWS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
@@ -161,7 +162,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     mbar_init(p_empty, 1);
     mbar_init(q_ready, 128);
     mbar_init(o_done, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kXBufs; ++i) {
       mbar_init(&x_full[i], 1);
       mbar_init(&x_empty[i], 4);
     }
@@ -204,8 +205,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   const int n_tiles = *last_valid < 0 ? 0 : *last_valid / kNp + 1;
   constexpr uint32_t kXBytes = kH * kNp * 4;       // one partial logit tile
   if (tid == 0) {                                  // expect the peer's first two tiles
-    if (n_tiles > 0) mbar_arrive_expect_tx(&x_full[0], kXBytes);
-    if (n_tiles > 1) mbar_arrive_expect_tx(&x_full[1], kXBytes);
+    for (int i = 0; i < kXBufs && i < n_tiles; ++i) mbar_arrive_expect_tx(&x_full[i], kXBytes);
   }
   cluster_sync();   // the peer's barriers exist (and are armed) before anyone uses them
   const uint32_t tmem = *tmem_slot;
@@ -220,8 +220,8 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       if (lane == 0) prefetch_tmap(&lmap);
       int stage = 0;
       uint32_t ph = 0;
-      bool issued[kStages] = {false, false, false};
-      uint32_t issued_ph[kStages] = {0, 0, 0};
+      bool issued[kStages] = {};
+      uint32_t issued_ph[kStages] = {};
       const unsigned gmask = 0x0000ffffu;
       for (int t = 0; t < n_tiles; ++t) {
         bool ok = true;
@@ -387,8 +387,8 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     const uint32_t xfull_remote = map_to_rank(smem_u32(x_full), peer);
     const uint32_t xempty_remote = map_to_rank(smem_u32(x_empty), peer);
     auto send = [&](int tt, const float* v) -> bool {
-      const int bsel = tt & 1;
-      if (!warp_wait_cluster(&x_empty[bsel], ((tt >> 1) & 1) ^ 1, abort_flag, err)) return false;
+      const int bsel = tt % kXBufs;
+      if (!warp_wait_cluster(&x_empty[bsel], ((tt / kXBufs) & 1) ^ 1, abort_flag, err)) return false;
       const uint32_t dst = x_remote + bsel * kXBytes;
 #pragma unroll
       for (int q4 = 0; q4 < kNp / 4; ++q4)
@@ -401,8 +401,8 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     if (n_tiles > 0) ok = load_s(0, vc) && send(0, vc);
     for (int t = 0; ok && t < n_tiles; ++t) {
       // peer's partial logits of tile t
-      const int bsel = t & 1;
-      if (!(ok = warp_wait_cluster(&x_full[bsel], (t >> 1) & 1, abort_flag, err))) break;
+      const int bsel = t % kXBufs;
+      if (!(ok = warp_wait_cluster(&x_full[bsel], (t / kXBufs) & 1, abort_flag, err))) break;
 #pragma unroll
       for (int q4 = 0; q4 < kNp / 4; ++q4) {
         const float4 pv4 = *reinterpret_cast<const float4*>(xrow + bsel * kXBytes +
@@ -410,12 +410,12 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
         vc[4 * q4] += pv4.x; vc[4 * q4 + 1] += pv4.y; vc[4 * q4 + 2] += pv4.z; vc[4 * q4 + 3] += pv4.w;
       }
       // buffer credit, one per warp: this warp has read the peer's tile t, so
-      // the peer may write tile t+2 there; warp 0 re-arms the byte count.  The
+      // the peer may write tile t+kXBufs there; warp 0 re-arms the byte count.  The
       // loads above completed (their values are summed) before the warp
       // barrier, so relaxed arrivals suffice; a cluster-scope release here
       // measured about 15% slower over the whole kernel.
       __syncwarp();
-      if (lane == 0 && t + 2 < n_tiles) {
+      if (lane == 0 && t + kXBufs < n_tiles) {
         if (quarter == 0) mbar_arrive_expect_tx_relaxed(&x_full[bsel], kXBytes);
         mbar_arrive_remote_relaxed(xempty_remote + bsel * 8);
       }
