@@ -12,24 +12,26 @@
 // CTA's tensor memory, so the work is split by dimension:
 //   CTA 0: logits over key dims   0..319, output dims   0..255
 //   CTA 1: logits over key dims 320..575, output dims 256..511
-// Each CTA gathers only the 320 dims of every selected row that it needs (no
-// row is fetched twice), keeps its slice of the queries in TMEM as the A
-// operand of the logit MMA, and keeps its half of the output accumulator in
-// TMEM.  The two partial logit tiles (128 heads x 64 positions, fp32) are
-// swapped through distributed shared memory, so both CTAs hold the same
-// logits and take the same softmax decisions.  Per 64-position tile:
-//   producers (3 warps): the tile's rows into a 128-byte-swizzled stage
-//     (ring of 3), three 64-dim blocks by TMA gather4 (four rows per
-//     instruction) and two by cp.async, so both copy engines work at once;
-//   MMA (1 thread):  S = Qslice . C^T  (A from TMEM, B K-major from the stage)
-//                    O += P . V        (A = P K-major, B = V MN-major, same stage)
-//   softmax (4 warps, one head per thread): read S from TMEM, exchange with
-//     the peer (software-pipelined: tile t+1 is sent before tile t is
-//     finished; st.async stores count their bytes on the peer's barrier and
-//     each warp returns a buffer credit), online softmax in log2 units
-//     with a
-//     lazily moved reference max (the accumulator is rescaled only when the
-//     max grows by more than 2^8), P in bf16 to shared memory.
+// Each CTA gathers only the 320 dims of every selected row that it needs,
+// keeps its half of the output accumulator in TMEM (256 columns), two logit
+// tiles (2 x 64 columns) and four 64-dim blocks of its query slice (128
+// columns; CTA 0's fifth block sits in shared memory as an MMA A operand).
+// The two partial logit tiles (128 heads x 64 positions, fp32) are swapped
+// through distributed shared memory, so both CTAs hold the same logits and
+// take the same softmax decisions.  Per 64-position tile, 12 warps:
+//   producers (warps 0-2): the tile's rows into a 128-byte-swizzled stage
+//     (ring of 3), by TMA gather4 (four rows per instruction) and cp.async at
+//     once, so both copy engines work;
+//   MMA (warp 3, one thread): S = Qslice . C^T into the free logit tile,
+//     O += P . V (A = P K-major, B = V MN-major, same stage);
+//   exchange (warps 4-7): partial logits out of TMEM, st.async into the
+//     peer's buffer (bytes counted on the peer's barrier), the peer's partial
+//     added, the sum written back into the TMEM tile; one buffer credit per
+//     warp returns to the peer;
+//   softmax (warps 8-11, one head per thread): online softmax in log2 units
+//     with a lazily moved reference max (the accumulator is rescaled only
+//     when the max grows by more than 2^8), P in bf16 to shared memory, and
+//     the epilogue.
 // Every wait is bounded; the cluster syncs once after set-up and once before
 // exit so no CTA leaves while its peer may still write into it.
 #include "kernels.h"
@@ -45,33 +47,39 @@ constexpr int kH = 128;                        // heads (MMA M)
 constexpr int kNp = 64;                        // positions per tile (MMA N of the logits)
 constexpr int kChunks = 5;                     // 64-dim blocks each CTA gathers per row
 constexpr int kStages = 3;
-constexpr int kXBufs = 2;                      // exchange buffers for the peer's partial logits
+constexpr int kXBufs = 1;                      // exchange buffers for the peer's partial logits
+constexpr int kQkTmem = 4;                     // query blocks held in TMEM (CTA 0's fifth is in shared memory)
 constexpr int kChunkBytes = kNp * 128;         // one 64-dim block of a tile: 8 KB
 constexpr int kStageBytes = kChunks * kChunkBytes;
-// 8 warps: two per SM sub-partition, so each thread may use up to 255 registers
+// 12 warps (three per SM sub-partition): at most 168 registers a thread
 constexpr int kProducerWarps = 3;
 constexpr int kMmaWarp = kProducerWarps;       // warp 3: lane 0 issues the MMAs
-constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;   // 256
+constexpr int kExWarp0 = kMmaWarp + 1;         // warps 4-7: logit exchange with the peer
+constexpr int kSmWarp0 = kExWarp0 + 4;         // warps 8-11: softmax and epilogue
+constexpr int kThreads = (kSmWarp0 + 4) * 32;  // 384
 // Each tile is gathered by two engines at once: TMA gather4 (warp 0) for the
-// first kTmaChunks 64-dim blocks, cp.async (warps 1-2) for the rest.
+// first kTmaChunks 64-dim blocks of the first kTmaRows rows, cp.async (warps
+// 1-2) for the rest.
 constexpr int kTmaChunks = 3;
+constexpr int kTmaRows = 48;                   // rows of those blocks by TMA; cp.async takes the rest
+static_assert(kTmaRows % 4 == 0 && kTmaRows <= kNp, "whole gather4 groups");
 constexpr int kLdgWarps = kProducerWarps - 1;
 constexpr int kLdgThreads = kLdgWarps * 32;
 
 constexpr int kMaxEntries = DSI_MAX_K;         // index entries one split can hold
-static_assert(kMaxEntries % kThreads == 0, "entries spread evenly over the threads");
 
 constexpr int OFF_C = 0;
 constexpr int OFF_P = OFF_C + kStages * kStageBytes;      // P [128 x 64] bf16, 16 KB
 constexpr int OFF_X = OFF_P + kH * kNp * 2;               // kXBufs x peer logits [128 x 64] fp32
-constexpr int OFF_ROWS = OFF_X + kXBufs * kH * kNp * 4;   // physical row of each entry (or -1)
+constexpr int OFF_Q4 = OFF_X + kXBufs * kH * kNp * 4;     // CTA 0's fifth query block [128 x 64] bf16, swizzled
+constexpr int OFF_ROWS = OFF_Q4 + kH * 64 * 2;            // physical row of each entry (or -1)
 constexpr int OFF_BAR = OFF_ROWS + kMaxEntries * 4;
-constexpr int NBARS = 2 * kStages + 6 + 2 * kXBufs;
+constexpr int NBARS = 2 * kStages + 10 + 2 * kXBufs;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM = OFF_MISC + 64 + 1024;
 
-constexpr uint32_t TM_S = 0;      // logits, 64 columns
-constexpr uint32_t TM_Q = 64;     // query slice, 160 (CTA 0) or 128 (CTA 1) columns
+constexpr uint32_t TM_S = 0;      // logits, two buffers of 64 columns
+constexpr uint32_t TM_Q = 128;    // query slice: four 64-dim blocks, 128 columns
 constexpr uint32_t TM_O = 256;    // output half, 256 columns
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_S = idesc_f32(1, kH, kNp);
@@ -115,13 +123,14 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* full = bars;                       // [kStages] gather landed (TMA bytes + cp.async threads)
   uint64_t* empty = bars + kStages;            // [kStages] stage free (MMA commit)
-  uint64_t* s_full = bars + 2 * kStages;       // logits in TMEM (MMA commit)
-  uint64_t* s_empty = s_full + 1;              // logits read out (softmax threads)
-  uint64_t* p_full = s_full + 2;               // P written (softmax threads)
-  uint64_t* p_empty = s_full + 3;              // P.V done (MMA commit)
-  uint64_t* q_ready = s_full + 4;              // query slice in TMEM (softmax threads)
-  uint64_t* o_done = s_full + 5;               // last P.V done (MMA commit)
-  uint64_t* x_full = s_full + 6;               // [kXBufs] peer's partial logits landed (byte count)
+  uint64_t* s_full = bars + 2 * kStages;       // [2] logits in TMEM (MMA commit)
+  uint64_t* s_empty = s_full + 2;              // [2] logits read out (softmax threads)
+  uint64_t* p_full = s_full + 4;               // P written (softmax threads)
+  uint64_t* p_empty = s_full + 5;              // P.V done (MMA commit)
+  uint64_t* q_ready = s_full + 6;              // query slice in place (softmax threads)
+  uint64_t* o_done = s_full + 7;               // last P.V done (MMA commit)
+  uint64_t* s_ready = s_full + 8;              // [2] summed logits back in TMEM (exchange warps)
+  uint64_t* x_full = s_full + 10;              // [kXBufs] peer's partial logits landed (byte count)
   uint64_t* x_empty = x_full + kXBufs;         // [kXBufs] peer has read what we sent (one credit per peer softmax warp)
   int32_t* rows_s = reinterpret_cast<int32_t*>(smem + OFF_ROWS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
@@ -143,24 +152,38 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   const int32_t* irow = a.idx + (int64_t)r * a.K;
   const int g0 = rho ? 4 : 0;                      // first gathered 64-dim block
   const int qk_first = rho ? 1 : 0;                // first stage block used by the logits
-  // softmax threads: this CTA's slice of the head's query row is loaded now,
-  // so it lands while the entries are being staged
-  uint4 qv[kChunks * 8];
-  if (warp > kMmaWarp) {
-    const uint4* qsrc = reinterpret_cast<const uint4*>(
-        a.q + ((int64_t)r * kH + (warp & 3) * 32 + lane) * DSI_D_QK + (g0 + qk_first) * 64);
-    const int nq = (kChunks - qk_first) * 8;
+  // the split's entries: each thread's index loads go out first (they gate the
+  // first gather), then its share of the query slice
+  constexpr int kPer = (kMaxEntries + kThreads - 1) / kThreads;
+  int pos[kPer];
 #pragma unroll
-    for (int i = 0; i < kChunks * 8; ++i) qv[i] = i < nq ? __ldg(qsrc + i) : make_uint4(0, 0, 0, 0);
+  for (int u = 0; u < kPer; ++u) {
+    const int jj = tid + u * kThreads;
+    pos[u] = (jj < span && j_begin + jj < j_end) ? __ldg(irow + j_begin + jj) : -1;
+  }
+  // this CTA's slice of the head's query row is loaded now, so it lands while
+  // the entries are being staged: the exchange warps take its first two 64-dim
+  // blocks, the softmax warps the rest (two, or three on CTA 0)
+  uint4 qv[24];
+  if (warp >= kExWarp0) {
+    const int c_lo = warp < kSmWarp0 ? 0 : 2;
+    const int nq = (warp < kSmWarp0 ? 2 : kChunks - qk_first - 2) * 8;
+    const uint4* qsrc = reinterpret_cast<const uint4*>(
+        a.q + ((int64_t)r * kH + (warp & 3) * 32 + lane) * DSI_D_QK + (g0 + qk_first + c_lo) * 64);
+#pragma unroll
+    for (int i = 0; i < 24; ++i) qv[i] = i < nq ? __ldg(qsrc + i) : make_uint4(0, 0, 0, 0);
   }
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1 + kLdgThreads); mbar_init(&empty[s], 1); }
-    mbar_init(s_full, 1);
-    mbar_init(s_empty, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 128);
+      mbar_init(&s_ready[i], 128);
+    }
     mbar_init(p_full, 128);
     mbar_init(p_empty, 1);
-    mbar_init(q_ready, 128);
+    mbar_init(q_ready, 256);
     mbar_init(o_done, 1);
     for (int i = 0; i < kXBufs; ++i) {
       mbar_init(&x_full[i], 1);
@@ -172,16 +195,8 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   }
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, TMEM_COLS);
   __syncthreads();
-  // the split's entries, translated once to physical cache rows (-1 = skipped);
-  // a thread's index loads are all issued before any translation
+  // the split's entries, translated once to physical cache rows (-1 = skipped)
   {
-    constexpr int kPer = kMaxEntries / kThreads;
-    int pos[kPer];
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int jj = tid + u * kThreads;
-      pos[u] = (jj < span && j_begin + jj < j_end) ? __ldg(irow + j_begin + jj) : -1;
-    }
     int lv = -1;
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
@@ -212,22 +227,22 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
 
   if (warp == 0) {
     // ======================= gather: TMA part =================================
-    // 16 lanes: lane g gathers rows 4g..4g+3 of the tile for the first
-    // kTmaChunks 64-dim blocks, each a TMA gather of four 128-byte rows into
-    // the swizzled stage.  Lane 0 first arms the stage's barrier.  Skipped
-    // entries fetch row 0 (their probability is zero).
-    if (lane < kNp / 4) {
+    // kTmaRows/4 lanes: lane g gathers rows 4g..4g+3 of the tile for the
+    // first kTmaChunks 64-dim blocks, each a TMA gather of four 128-byte rows
+    // into the swizzled stage.  Lane 0 first arms the stage's barrier.
+    // Skipped entries fetch row 0 (their probability is zero).
+    if (lane < kTmaRows / 4) {
       if (lane == 0) prefetch_tmap(&lmap);
       int stage = 0;
       uint32_t ph = 0;
       bool issued[kStages] = {};
       uint32_t issued_ph[kStages] = {};
-      const unsigned gmask = 0x0000ffffu;
+      const unsigned gmask = (1u << (kTmaRows / 4)) - 1u;
       for (int t = 0; t < n_tiles; ++t) {
         bool ok = true;
         if (lane == 0) {
           ok = mbar_wait(&empty[stage], ph ^ 1, abort_flag, err);
-          if (ok) mbar_arrive_expect_tx(&full[stage], kTmaChunks * kChunkBytes);
+          if (ok) mbar_arrive_expect_tx(&full[stage], kTmaChunks * kTmaRows * 128);
         }
         ok = __shfl_sync(gmask, ok, 0);
         if (!ok) break;
@@ -252,9 +267,10 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     }
   } else if (warp < kProducerWarps) {
     // ======================= gather: cp.async part ============================
-    // the remaining 64-dim blocks: half a warp per row (16 lanes x 16 bytes =
-    // two blocks), each piece to its swizzled place; each tile is signalled
-    // (after a proxy fence) once its copies have landed
+    // the remaining 64-dim blocks of every row (half a warp per row: 16 lanes
+    // x 16 bytes = two blocks) and the first blocks of the rows past kTmaRows,
+    // each piece to its swizzled place; each tile is signalled (after a proxy
+    // fence) once its copies have landed.  The split balances the two engines.
     constexpr int kLdgPieces = (kChunks - kTmaChunks) * 8;   // 16-byte pieces per row
     static_assert(kLdgPieces == 16, "half a warp per row");
     const int sub = lane >> 4, pi = lane & 15;
@@ -268,6 +284,13 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
         const int pr = max(rows_s[t * kNp + rr], 0);
         cp_async_16(st_addr + ch * kChunkBytes + sw128_offset(rr, u),
                     c.latent + (int64_t)pr * DSI_D_QK + (g0 + ch) * 64 + u * 8);
+      }
+      constexpr int kTailPieces = (kNp - kTmaRows) * kTmaChunks * 8;
+      for (int q = (warp - 1) * 32 + lane; q < kTailPieces; q += kLdgThreads) {
+        const int rr = kTmaRows + q / (kTmaChunks * 8), w = q % (kTmaChunks * 8);
+        const int pr = max(rows_s[t * kNp + rr], 0);
+        cp_async_16(st_addr + (w >> 3) * kChunkBytes + sw128_offset(rr, w & 7),
+                    c.latent + (int64_t)pr * DSI_D_QK + (g0 + (w >> 3)) * 64 + (w & 7) * 8);
       }
       cp_async_commit();
       // signal this tile as soon as its own copies have landed (not after the
@@ -308,17 +331,26 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
         }
         if (qk_next < n_tiles) {
           const int st = qk_next % kStages;
+          const int sb = qk_next & 1;
           if (mbar_test_wait(&full[st], (qk_next / kStages) & 1) &&
-              mbar_test_wait(s_empty, (qk_next & 1) ^ 1)) {
+              mbar_test_wait(&s_empty[sb], ((qk_next >> 1) & 1) ^ 1)) {
             tc_fence_after();
-            const uint64_t d0 = desc_sw128(smem_u32(smem + OFF_C + st * kStageBytes) +
-                                           qk_first * kChunkBytes);
-            const int nk = (kChunks - qk_first) * 4;
-            for (int k = 0; k < nk; ++k)
-              mma_bf16_tmem_a(tmem + TM_S, tmem + TM_Q + k * 8,
+            const uint32_t t_s = tmem + TM_S + sb * kNp;
+            const uint32_t st_base = smem_u32(smem + OFF_C + st * kStageBytes);
+            const uint64_t d0 = desc_sw128(st_base + qk_first * kChunkBytes);
+            for (int k = 0; k < kQkTmem * 4; ++k)
+              mma_bf16_tmem_a(t_s, tmem + TM_Q + k * 8,
                               d0 + (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4),
                               IDESC_S, k > 0 ? 1u : 0u);
-            mma_commit(s_full);
+            if (rho == 0) {      // fifth block: queries from shared memory
+              const uint64_t qd = desc_sw128(smem_u32(smem + OFF_Q4));
+              const uint64_t cd = desc_sw128(st_base + kQkTmem * kChunkBytes);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_bf16(t_s, qd + (uint64_t)((k * 32) >> 4), cd + (uint64_t)((k * 32) >> 4),
+                         IDESC_S, 1u);
+            }
+            mma_commit(&s_full[sb]);
             ++qk_next;
             progress = true;
           }
@@ -338,80 +370,62 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       mma_commit(o_done);
     }
     __syncwarp();
-  } else {
-    // ======================= softmax + epilogue ================================
+  } else if (warp < kSmWarp0) {
+    // ======================= logit exchange ===================================
+    // Per tile: read this CTA's partial logits from TMEM, store them into the
+    // peer's exchange buffer (st.async, bytes counted on the peer's barrier),
+    // add the peer's partial, and write the summed logits back into the same
+    // TMEM tile for the softmax warps.  This runs a tile ahead of the softmax.
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;               // head = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    // this CTA's slice of the query row into TMEM (columns pack bf16 pairs)
-    {
 #pragma unroll
-      for (int ch = 0; ch < kChunks; ++ch) {
-        if (ch < kChunks - qk_first) {      // CTA-uniform
-          uint32_t w32[32];
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t w32[32];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 v = qv[8 * ch + i];
-            w32[4 * i] = v.x; w32[4 * i + 1] = v.y; w32[4 * i + 2] = v.z; w32[4 * i + 3] = v.w;
-          }
-          tmem_st32(tmem + lane_base + TM_Q + ch * 32, w32);
-        }
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = qv[8 * ch + i];
+        w32[4 * i] = v.x; w32[4 * i + 1] = v.y; w32[4 * i + 2] = v.z; w32[4 * i + 3] = v.w;
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(q_ready);
+      tmem_st32(tmem + lane_base + TM_Q + ch * 32, w32);
     }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(q_ready);
     // exchange buffer layout [buffer][4-position group][head] x float4: a
     // warp's stores (and loads) of one group are 512 contiguous bytes
     const uint32_t x_remote = map_to_rank(smem_u32(smem + OFF_X), peer) + h * 16;
     const uint8_t* xrow = smem + OFF_X + h * 16;
-    uint8_t* prow = smem + OFF_P;
-    const float sl2 = a.scale * kLog2e;
-    float m_ref = -INFINITY, l_sum = 0.f;
-    bool ok = true;
-    float vc[kNp], vn[kNp];   // logits of the current tile and of the next one
-
-    // read this CTA's partial logits of tile tt into v (frees the TMEM S tile)
-    auto load_s = [&](int tt, float* v) -> bool {
-      if (!warp_wait(s_full, tt & 1, abort_flag, err)) return false;
-      tc_fence_after();
-      tmem_ld32(tmem + lane_base + TM_S, v);
-      tmem_ld32(tmem + lane_base + TM_S + 32, v + 32);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(s_empty);
-      return true;
-    };
-    // store them into the peer's exchange buffer for tile tt; the bytes are
-    // counted on the peer's x_full barrier as they land
     const uint32_t xfull_remote = map_to_rank(smem_u32(x_full), peer);
     const uint32_t xempty_remote = map_to_rank(smem_u32(x_empty), peer);
-    auto send = [&](int tt, const float* v) -> bool {
-      const int bsel = tt % kXBufs;
-      if (!warp_wait_cluster(&x_empty[bsel], ((tt / kXBufs) & 1) ^ 1, abort_flag, err)) return false;
+    bool ok = true;
+    for (int t = 0; ok && t < n_tiles; ++t) {
+      const int sb = t & 1, bsel = t % kXBufs;
+      float v[kNp];
+      if (!(ok = warp_wait(&s_full[sb], (t >> 1) & 1, abort_flag, err))) break;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_base + TM_S + sb * kNp, v);
+      tmem_ld32(tmem + lane_base + TM_S + sb * kNp + 32, v + 32);
+      tmem_ld_wait();
+      // this CTA's partial to the peer, once the peer has read the buffer
+      if (!(ok = warp_wait_cluster(&x_empty[bsel], ((t / kXBufs) & 1) ^ 1, abort_flag, err))) break;
       const uint32_t dst = x_remote + bsel * kXBytes;
 #pragma unroll
       for (int q4 = 0; q4 < kNp / 4; ++q4)
         st_async_v4(dst + q4 * (kH * 16),
                     make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]),
                     xfull_remote + bsel * 8);
-      return true;
-    };
-
-    if (n_tiles > 0) ok = load_s(0, vc) && send(0, vc);
-    for (int t = 0; ok && t < n_tiles; ++t) {
-      // peer's partial logits of tile t
-      const int bsel = t % kXBufs;
+      // the peer's partial of the same tile
       if (!(ok = warp_wait_cluster(&x_full[bsel], (t / kXBufs) & 1, abort_flag, err))) break;
 #pragma unroll
       for (int q4 = 0; q4 < kNp / 4; ++q4) {
         const float4 pv4 = *reinterpret_cast<const float4*>(xrow + bsel * kXBytes +
                                                             q4 * (kH * 16));
-        vc[4 * q4] += pv4.x; vc[4 * q4 + 1] += pv4.y; vc[4 * q4 + 2] += pv4.z; vc[4 * q4 + 3] += pv4.w;
+        v[4 * q4] += pv4.x; v[4 * q4 + 1] += pv4.y; v[4 * q4 + 2] += pv4.z; v[4 * q4 + 3] += pv4.w;
       }
       // buffer credit, one per warp: this warp has read the peer's tile t, so
-      // the peer may write tile t+kXBufs there; warp 0 re-arms the byte count.  The
-      // loads above completed (their values are summed) before the warp
+      // the peer may write tile t+kXBufs there; warp 0 re-arms the byte count.
+      // The loads above completed (their values are summed) before the warp
       // barrier, so relaxed arrivals suffice; a cluster-scope release here
       // measured about 15% slower over the whole kernel.
       __syncwarp();
@@ -419,13 +433,56 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
         if (quarter == 0) mbar_arrive_expect_tx_relaxed(&x_full[bsel], kXBytes);
         mbar_arrive_remote_relaxed(xempty_remote + bsel * 8);
       }
-      // start the exchange of tile t+1 before working on tile t when its logits
-      // are already there; otherwise after tile t (never wait on its gather here)
-      bool sent_next = false;
-      if (t + 1 < n_tiles && __all_sync(0xffffffffu, mbar_test_wait(s_full, (t + 1) & 1))) {
-        if (!(ok = load_s(t + 1, vn) && send(t + 1, vn))) break;
-        sent_next = true;
+      // summed logits back into the TMEM tile
+      tmem_st32f(tmem + lane_base + TM_S + sb * kNp, v);
+      tmem_st32f(tmem + lane_base + TM_S + sb * kNp + 32, v + 32);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&s_ready[sb]);
+    }
+  } else {
+    // ======================= softmax + epilogue ================================
+    const int quarter = warp & 3;
+    const int h = quarter * 32 + lane;               // head = TMEM lane
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    // query blocks 2-3 into TMEM; CTA 0's fifth block into shared memory (the
+    // A operand of its last four logit MMAs)
+    {
+#pragma unroll
+      for (int ch = 2; ch < kQkTmem; ++ch) {
+        uint32_t w32[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = qv[8 * (ch - 2) + i];
+          w32[4 * i] = v.x; w32[4 * i + 1] = v.y; w32[4 * i + 2] = v.z; w32[4 * i + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_base + TM_Q + ch * 32, w32);
       }
+      if (rho == 0) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(smem + OFF_Q4 + sw128_offset(h, u)) = qv[8 * (kQkTmem - 2) + u];
+        fence_proxy_async_smem();
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(q_ready);
+    }
+    uint8_t* prow = smem + OFF_P;
+    const float sl2 = a.scale * kLog2e;
+    float m_ref = -INFINITY, l_sum = 0.f;
+    bool ok = true;
+    for (int t = 0; ok && t < n_tiles; ++t) {
+      // summed logits of tile t (frees the TMEM tile for the logits of t+2)
+      const int sb = t & 1;
+      float vc[kNp];
+      if (!(ok = warp_wait(&s_ready[sb], (t >> 1) & 1, abort_flag, err))) break;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_base + TM_S + sb * kNp, vc);
+      tmem_ld32(tmem + lane_base + TM_S + sb * kNp + 32, vc + 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&s_empty[sb]);
       // validity of the tile's 64 entries
       const uint32_t m_lo = __ballot_sync(0xffffffffu, rows_s[t * kNp + lane] >= 0);
       const uint32_t m_hi = __ballot_sync(0xffffffffu, rows_s[t * kNp + 32 + lane] >= 0);
@@ -502,9 +559,6 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
-      if (t + 1 < n_tiles && !sent_next && !(ok = load_s(t + 1, vn) && send(t + 1, vn))) break;
-#pragma unroll
-      for (int j = 0; j < kNp; ++j) vc[j] = vn[j];
     }
     // ---- epilogue: normalise and store this CTA's 256 output dims ------------
     if (ok && warp_wait(o_done, 0, abort_flag, err)) {
