@@ -51,8 +51,11 @@ constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + kStages * A_BYTES;
 constexpr int OFF_BUF = OFF_B + 2 * B_BYTES;                    // NT x kCap x 8 bytes
 constexpr int OFF_W = OFF_BUF + NT * kCap * 8;                  // NT x 64 fp32
-constexpr int OFF_HIST = OFF_W + NT * kHeads * 4;               // NT x 256 int
-constexpr int OFF_TOK = OFF_HIST + NT * 256 * 4;                // per-token state
+constexpr int kSelBits = 11;
+constexpr int kSelBins = 1 << kSelBits;                         // select histogram bins
+constexpr int kHistInts = kSelBins + 32;                        // + reduction scratch
+constexpr int OFF_HIST = OFF_W + NT * kHeads * 4;               // NT x kHistInts int
+constexpr int OFF_TOK = OFF_HIST + NT * kHistInts * 4;          // per-token state
 constexpr int OFF_BAR = (OFF_TOK + NT * 64 + 7) & ~7;
 constexpr int NBARS = 2 * kStages + 2 + 2 + 2 + 2 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
@@ -60,11 +63,11 @@ constexpr int SMEM = OFF_MISC + 64 + 1024;
 
 struct TokState {
   unsigned long long theta;   // keys <= theta are rejected
+  unsigned long long lo, hi;  // select scratch
   int cnt;                    // candidates in the buffer
-  int digit;                  // radix-select scratch
+  int digit;                  // select scratch
   int krem;
   int total;
-  int pad[2];
 };
 static_assert(sizeof(TokState) <= 64, "token state");
 
@@ -103,47 +106,103 @@ __device__ __forceinline__ int group_tiles(const Args& a, int g) {
   return (int)((a.q_offset + last + 1 + kTileM - 1) / kTileM);
 }
 
-// Radix select over the token's candidate buffer: the k-th largest key (keys
-// are unique).  128 threads of the token (tt = 0..127) take part.
+// Select over the token's candidate buffer: the k-th largest key (keys are
+// unique).  128 threads of the token (tt = 0..127) take part.  An interval
+// [lo, hi] holding the answer starts at the candidates' min and max; each pass
+// splits it into kSelBins equal bins and keeps the bin where the count from
+// the top reaches k.  Bins follow the keys' actual spread, so the histogram
+// atomics do not pile onto a few addresses the way fixed top digits of
+// similar scores would; once the chosen bin holds a single key, that key is
+// the answer.
 __device__ unsigned long long select_kth(const unsigned long long* buf, int n, int k, int* hist,
                                          TokState* ts, int tt, int tk) {
-  unsigned long long prefix = 0, mask = 0;
+  const int lane = tt & 31, wq = tt >> 5;
+  const unsigned kAll = 0xffffffffu;
+  unsigned long long mn = ~0ull, mx = 0ull;
+  for (int i = tt; i < n; i += 128) {
+    const unsigned long long c = buf[i];
+    mn = c < mn ? c : mn;
+    mx = c > mx ? c : mx;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const unsigned long long a = __shfl_xor_sync(kAll, mn, o), b = __shfl_xor_sync(kAll, mx, o);
+    mn = a < mn ? a : mn;
+    mx = b > mx ? b : mx;
+  }
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(hist + kSelBins);   // 8 words
+  if (lane == 0) { red[wq] = mn; red[4 + wq] = mx; }
+  bar_tok(tk);
+  if (tt == 0) {
+    unsigned long long l = red[0], h = red[4];
+    for (int x = 1; x < 4; ++x) { l = red[x] < l ? red[x] : l; h = red[4 + x] > h ? red[4 + x] : h; }
+    ts->lo = l;
+    ts->hi = h;
+  }
+  bar_tok(tk);
+  unsigned long long lo = ts->lo, hi = ts->hi;
   int krem = k;
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int i = tt; i < 256; i += 128) hist[i] = 0;
+  bar_tok(tk);
+  while (lo != hi) {
+    const unsigned long long span = hi - lo;
+    const int bits = 64 - __clzll((long long)span);
+    const int sh = bits > kSelBits ? bits - kSelBits : 0;
+    for (int i = tt; i < kSelBins; i += 128) hist[i] = 0;
     bar_tok(tk);
     for (int i = tt; i < n; i += 128) {
-      const unsigned long long c = buf[i];
-      if ((c & mask) == prefix) atomicAdd(&hist[(int)((c >> shift) & 255ull)], 1);
+      const unsigned long long off = buf[i] - lo;         // wraps for keys below lo
+      if (off <= span) atomicAdd(&hist[(int)(off >> sh)], 1);
     }
     bar_tok(tk);
-    if (tt < 32) {
-      int cs[8], tot = 0;
+    // thread tt owns bins kSelBins-1-16tt down to kSelBins-16-16tt
+    constexpr int kPerT = kSelBins / 128;
+    int cs[kPerT], tot = 0;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) { cs[e] = hist[255 - (tt * 8 + e)]; tot += cs[e]; }
-      int incl = tot;
+    for (int e = 0; e < kPerT; ++e) { cs[e] = hist[kSelBins - 1 - kPerT * tt - e]; tot += cs[e]; }
+    int incl = tot;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (tt >= o) incl += y;
-      }
-      const int excl = incl - tot;
-      if (excl < krem && incl >= krem) {
-        int run = excl;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kAll, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int* wsum = hist + kSelBins + 16;
+    if (lane == 31) wsum[wq] = incl;
+    bar_tok(tk);
+    int above = incl - tot;
+    for (int x = 0; x < wq; ++x) above += wsum[x];
+    if (above < krem && above + tot >= krem) {
+      int run = above;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (run < krem && run + cs[e] >= krem) { ts->digit = 255 - (tt * 8 + e); ts->krem = krem - run; }
-          run += cs[e];
+      for (int e = 0; e < kPerT; ++e) {
+        if (run < krem && run + cs[e] >= krem) {
+          ts->digit = kSelBins - 1 - kPerT * tt - e;
+          ts->krem = krem - run;
+          ts->total = cs[e];
         }
+        run += cs[e];
       }
     }
     bar_tok(tk);
-    prefix |= (unsigned long long)ts->digit << shift;
-    mask |= 255ull << shift;
+    const unsigned long long b = (unsigned long long)ts->digit;
+    const int in_bin = ts->total;
     krem = ts->krem;
+    const unsigned long long t1 = (b << sh) + ((1ull << sh) - 1ull);
+    hi = t1 > span ? hi : lo + t1;
+    lo += b << sh;
     bar_tok(tk);
+    if (sh == 0) break;
+    if (in_bin == 1) {           // the bin holds exactly the k-th key: find it
+      for (int i = tt; i < n; i += 128) {
+        const unsigned long long c = buf[i];
+        if (c >= lo && c <= hi) ts->lo = c;
+      }
+      bar_tok(tk);
+      lo = ts->lo;
+      bar_tok(tk);
+      break;
+    }
   }
-  return prefix;
+  return lo;
 }
 
 // Keep the entries >= t (exactly k of them) at the front of the buffer.
@@ -303,7 +362,7 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     const int row = quarter * 32 + lane;      // position within the tile (TMEM lane)
     unsigned long long* buf = reinterpret_cast<unsigned long long*>(smem + OFF_BUF) + tk * kCap;
     float* wts = reinterpret_cast<float*>(smem + OFF_W) + tk * kHeads;
-    int* hist = reinterpret_cast<int*>(smem + OFF_HIST) + tk * 256;
+    int* hist = reinterpret_cast<int*>(smem + OFF_HIST) + tk * kHistInts;
     TokState* ts = reinterpret_cast<TokState*>(smem + OFF_TOK) + tk;
     int abuf = 0;
     uint32_t aph = 0;
@@ -332,6 +391,8 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         mbar_arrive(&acc_empty[abuf]);
         if (++abuf == 2) { abuf = 0; aph ^= 1; }
         const int64_t p = (int64_t)j * kTileM + row;
+        unsigned long long key = 0ull;
+        bool take = false;
         if (live && p < nvis) {
           float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -339,12 +400,17 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             s0 = fmaf(wts[h], fmaxf(v[h], 0.f), s0);
             s1 = fmaf(wts[h + 1], fmaxf(v[h + 1], 0.f), s1);
           }
-          const unsigned long long key =
-              ((unsigned long long)score_key(s0 + s1) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)p);
-          if (key > ts->theta) {
-            const int slot = atomicAdd(&ts->cnt, 1);
-            buf[slot] = key;
-          }
+          key = ((unsigned long long)score_key(s0 + s1) << 32) |
+                (unsigned long long)(0xFFFFFFFFu - (uint32_t)p);
+          take = key > ts->theta;
+        }
+        // append with one atomic per warp
+        const unsigned tm = __ballot_sync(0xffffffffu, take);
+        if (tm) {
+          int slot0 = 0;
+          if (lane == __ffs(tm) - 1) slot0 = atomicAdd(&ts->cnt, __popc(tm));
+          slot0 = __shfl_sync(0xffffffffu, slot0, __ffs(tm) - 1);
+          if (take) buf[slot0 + __popc(tm & ((1u << lane) - 1u))] = key;
         }
         bar_epi();
         // keep room for one more tile: compact a buffer that could overflow
