@@ -167,10 +167,17 @@ class ClockSampler:
                 "samples": len(sm), "samples_in_timed_region": len(inside)}
 
 
-def kernel_source_sha() -> str:
-    """Hash of the scoring kernels' sources (traffic figures go stale when they change)."""
+KERNEL_SOURCES = {
+    "index_score": ("index_score.cu", "index_score_tc.cu", "common.cuh"),
+    "index_topk_prefill": ("index_topk_prefill.cu", "tc_common.cuh", "common.cuh"),
+    "mla_tc": ("sparse_mla_tc.cu", "tc_common.cuh", "common.cuh"),
+}
+
+
+def kernel_source_sha(kernel: str = "index_score") -> str:
+    """Hash of a kernel's sources (traffic figures go stale when they change)."""
     h = hashlib.sha256()
-    for f in ("index_score.cu", "index_score_tc.cu", "common.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(ROOT, "indexed_sparse_attention_indexer_gb300", "csrc", f),
                       "rb").read())
     return h.hexdigest()[:16]
@@ -180,7 +187,7 @@ def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the kernel source as it is now (profiles/traffic.txt: kernel workload bytes sha)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
-    sha = kernel_source_sha()
+    sha = kernel_source_sha(kernel)
     if not os.path.exists(path):
         return None
     for line in open(path):
@@ -193,6 +200,21 @@ def recorded_traffic(kernel: str, workload: str):
 # ----------------------------------------------------------------------------
 # the GPU arm
 # ----------------------------------------------------------------------------
+
+def time_alone(launch, stream, n: int) -> float:
+    """Average ms of one launch, timed with CUDA events on the launching stream
+    over n back-to-back launches after three untimed ones."""
+    for _ in range(3):
+        launch()
+    torch.cuda.synchronize()
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
+    for _ in range(n):
+        launch()
+    k1.record(stream)
+    torch.cuda.synchronize()
+    return k0.elapsed_time(k1) / n
+
 
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -285,29 +307,41 @@ def run_gpu(args):
     ms_step = ms / args.steps
     value = whole_job_tokens_per_s(ws.T, world, args.steps, ms)
 
-    # ---- dominant kernel: the indexer scoring launch, timed alone ----------
-    scores = torch.empty((ws.T, span), dtype=torch.float32, device=dev)
-    for _ in range(3):
-        binding.index_score(ws.q_idx, ws.w, cache, decode, ws.q_offset, scores=scores, ld=span,
-                            stream=stream)
-    torch.cuda.synchronize()
-    nk = max(10, args.steps)
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k0.record(stream)
-    for _ in range(nk):
-        binding.index_score(ws.q_idx, ws.w, cache, decode, ws.q_offset, scores=scores, ld=span,
-                            stream=stream)
-    k1.record(stream)
-    torch.cuda.synchronize()
-    k_ms = k0.elapsed_time(k1) / nk
     hbm, tfl, src = peaks()
-    kbytes = scoring_kernel_bytes(ws)
-    achieved = kbytes / (k_ms / 1e3) / 1e9
-    kname = "index_score"
-    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
-                "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": src,
-                "traffic": recorded_traffic(kname, cfg["name"]),
-                "algorithmic_bytes": kbytes, "kernel_ms": round(k_ms, 5)}
+    extra = {}
+    if decode:
+        # ---- dominant kernel: the indexer scoring launch, timed alone ------
+        scores = torch.empty((ws.T, span), dtype=torch.float32, device=dev)
+        k_ms = time_alone(lambda: binding.index_score(ws.q_idx, ws.w, cache, decode, ws.q_offset,
+                                                      scores=scores, ld=span, stream=stream),
+                          stream, max(10, args.steps))
+        kbytes = scoring_kernel_bytes(ws)
+        achieved = kbytes / (k_ms / 1e3) / 1e9
+        kname = "index_score"
+        roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
+                    "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": src,
+                    "traffic": recorded_traffic(kname, cfg["name"]),
+                    "algorithmic_bytes": kbytes, "kernel_ms": round(k_ms, 5)}
+    else:
+        # ---- prefill: both halves are dense contractions on the tensor cores;
+        # the attention core dominates, the fused indexer is reported beside it
+        fl = algorithmic_flops(ws)
+        nk = max(3, min(10, args.steps))
+        m_ms = time_alone(lambda: binding.sparse_mla_prefill(ws.q, cache, idx, ws.q_offset, ws.scale,
+                                                             out=out, lse=lse, workspace=wsp,
+                                                             stream=stream), stream, nk)
+        i_ms = time_alone(lambda: binding.index_topk_prefill(ws.q_idx, ws.w, cache, ws.K,
+                                                             ws.q_offset, idx=idx, count=cnt,
+                                                             stream=stream), stream, nk)
+
+        def tensor_line(kname, flops, ms):
+            a_tf = flops / (ms / 1e3) / 1e12
+            return {"bound": "tensor", "kernel": kname, "achieved": round(a_tf, 1), "peak": tfl,
+                    "unit": "TFLOP/s", "frac": round(a_tf / tfl, 4), "peak_source": src,
+                    "traffic": recorded_traffic(kname, cfg["name"]),
+                    "algorithmic_flops": flops, "kernel_ms": round(ms, 5)}
+        roofline = tensor_line("mla_tc", fl["mla"], m_ms)
+        extra["indexer_roofline"] = tensor_line("index_topk_prefill", fl["indexer"], i_ms)
     ab = algorithmic_bytes(ws)
     step_gbs = ab["total"] / (ms_step / 1e3) / 1e9
 
@@ -329,7 +363,7 @@ def run_gpu(args):
             "hbm_gbs_step": round(step_gbs, 1),
             "hbm_frac_step": round(step_gbs / hbm, 4),
             "algorithmic_bytes_per_step": ab, "algorithmic_flops_per_step": fl,
-            "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
+            "roofline": roofline, **extra, "e2e": e2e, "gpu_launches": int(launches),
             "gpu_launches_per_step": launches / args.steps, "clocks": clk,
         }
         if args.rows:
@@ -455,6 +489,40 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_gather_ceiling():
+    """Plain-load bandwidth of the attention core's access pattern: 2048 random
+    distinct rows of each of 64 sequences x 32768 rows x 1152 bytes (the decode
+    workload's latent cache), L2 flushed before each timed launch."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from indexed_sparse_attention_indexer_gb300 import binding
+    binding.load()
+    B, S, K, pitch = 64, 32768, 2048, W.D_QK * 2
+    base = torch.ones(B * S * pitch // 2, dtype=torch.bfloat16, device=dev)
+    g = torch.Generator().manual_seed(0)
+    rows = torch.stack([torch.randperm(S, generator=g)[:K] + b * S for b in range(B)])
+    rows = rows.to(torch.int32).reshape(-1).to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    res = []
+    for nbytes in (640, 1152):
+        for blocks in (2 * sms, 4 * sms):
+            best = math.inf
+            for rep_i in range(5):
+                flush.fill_(rep_i & 255)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                binding.probe_random_gather(base, pitch, rows, nbytes, blocks)
+                e1.record()
+                torch.cuda.synchronize()
+                best = min(best, e0.elapsed_time(e1))
+            res.append({"bytes_per_row": nbytes, "blocks": blocks, "us": round(best * 1e3, 1),
+                        "gbs": round(rows.numel() * nbytes / (best / 1e3) / 1e9, 1)})
+    print(json.dumps({"probe": "random_row_gather", "rows": int(rows.numel()),
+                      "cache_bytes": B * S * pitch, "row_pitch": pitch, "results": res,
+                      "best_gbs": max(r["gbs"] for r in res)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -464,9 +532,14 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--gather-ceiling", action="store_true",
+                    help="diagnostic: random-row gather bandwidth of plain loads (not a bench line)")
     ap.add_argument("--rows", type=int, default=None,
                     help="profiling aid: a smaller decode batch (the printed line is not a bench line)")
     args = ap.parse_args()
+    if args.gather_ceiling:
+        run_gather_ceiling()
+        return
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         line = run_reference(args)

@@ -136,6 +136,30 @@ dsi_status dsi_topk(const float* scores, int64_t ld_scores, int32_t rows,
                     int32_t* idx, int32_t* count, void* stream);
 
 /*
+ * dsi_index_topk_prefill — the prefill indexer in one kernel: scores, ReLU
+ * gate, head weights and the running per-row Top-K, writing only indices.
+ * ("Day 0 Inference Support for New LLM Architectures: Optimization
+ * Practices", "Internal Fusion of the Indexer": scoring, weighting and
+ * Top-K fused so the score matrix never leaves the chip; "Load Imbalance in
+ * Causal Indexing and the Zigzag Layout": early and late query tokens paired.)
+ *
+ * Same result as dsi_index_score followed by dsi_topk with the causal rule
+ * (row r sees positions 0 .. q_offset + r): identical indices, order, -1
+ * padding and counts.
+ *   q_idx   bf16 [T, n_heads_idx, d]
+ *   w       fp32 [T, n_heads_idx]
+ *   cache   bf16 index keys, contiguous (batch 1) or paged
+ *   idx     int32 [T, K];  count  int32 [T] or NULL
+ * Errors: DSI_ERR_INVALID_ARG (null, T < 0, K < 1, batch != 1, q_offset + T >
+ * s_max), DSI_ERR_UNSUPPORTED when the fused kernel does not cover the shape
+ * (n_heads_idx != 64, d != 128, FP8 keys, page_size not a multiple of 64,
+ * K > 2048, q_offset + T > 131072): use dsi_index_score + dsi_topk there.
+ */
+dsi_status dsi_index_topk_prefill(const void* q_idx, const float* w, const dsi_cache* cache,
+                                  int32_t T, int32_t n_heads_idx, int64_t q_offset, int32_t K,
+                                  int32_t* idx, int32_t* count, void* stream);
+
+/*
  * dsi_sparse_mla_decode — attention of one query token per sequence over the
  * latent rows at the selected positions.
  * ("Day 0 Inference Support for New LLM Architectures: Optimization
@@ -223,6 +247,21 @@ dsi_status dsi_indexed_attention_static(const void* q_idx, const float* w, const
  * sizing of the dsi_sparse_mla_* calls when n_heads_idx == 0 and s_max == 0). */
 size_t dsi_workspace_size(int32_t rows, int32_t n_heads_idx, int32_t n_heads, int32_t K,
                           int64_t s_max, int32_t decode);
+
+/*
+ * dsi_probe_random_gather — diagnostic, not part of the layer: plain 16-byte
+ * loads of bytes_per_row bytes from each of the rows base + rows[i] *
+ * row_pitch (the attention core's gather pattern), by `blocks` CTAs of 512
+ * threads, nothing written.  Time it on a stream to get the random-row gather
+ * bandwidth the attention core works against.
+ *   base          device array of n_src_rows rows of row_pitch bytes (16-aligned)
+ *   rows          int32 [n_rows] device row ids; ids outside 0..n_src_rows-1 are skipped
+ *   bytes_per_row multiple of 16, <= row_pitch (a multiple of 16)
+ * Errors: DSI_ERR_INVALID_ARG for null pointers, sizes or alignment out of range.
+ */
+dsi_status dsi_probe_random_gather(const void* base, int64_t row_pitch, int64_t n_src_rows,
+                                   const int32_t* rows, int32_t n_rows, int32_t bytes_per_row,
+                                   int32_t blocks, void* stream);
 
 /* Synchronises `stream`, returns and clears the device status word of the
  * current device (DSI_OK, DSI_ERR_BOUNDS or DSI_ERR_TIMEOUT), or DSI_ERR_CUDA

@@ -39,6 +39,9 @@ SIGNATURES = {
                                   c_int32, c_int64, c_void_p, c_int64, c_void_p]),
     "dsi_topk": (c_int32, [c_void_p, c_int64, c_int32, c_void_p, c_int64, c_int32, c_void_p,
                            c_void_p, c_void_p]),
+    "dsi_index_topk_prefill": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(DsiCache), c_int32,
+                                         c_int32, c_int64, c_int32, c_void_p, c_void_p,
+                                         c_void_p]),
     "dsi_sparse_mla_decode": (c_int32, [c_void_p, ctypes.POINTER(DsiCache), c_void_p, c_int32,
                                         c_int32, c_int32, c_float, c_void_p, c_void_p, c_void_p,
                                         c_size_t, c_void_p]),
@@ -53,6 +56,8 @@ SIGNATURES = {
                                                ctypes.POINTER(DsiCache), c_int32, c_int32,
                                                c_int32, c_int32, c_int64, c_float, c_int32,
                                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "dsi_probe_random_gather": (c_int32, [c_void_p, c_int64, c_int64, c_void_p, c_int32, c_int32,
+                                          c_int32, c_void_p]),
     "dsi_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int64, c_int32]),
     "dsi_get_device_status": (c_int32, [c_void_p]),
     "dsi_status_string": (ctypes.c_char_p, [c_int32]),
@@ -161,6 +166,33 @@ def index_score(q_idx, w, cache: Cache, decode: bool, q_offset: int = 0, scores=
                              int(q_offset), _ptr(scores), int(ld), _stream(stream))
     _check(lib, "dsi_index_score", st)
     return scores
+
+
+def index_topk_prefill(q_idx, w, cache: Cache, K: int, q_offset: int = 0, idx=None, count=None,
+                       stream=None, checked: bool = False):
+    """Fused prefill indexer: the causal Top-K indices of every query token,
+    computed without writing the score matrix."""
+    lib = load(checked)
+    T, H_i = int(q_idx.shape[0]), int(q_idx.shape[1])
+    if idx is None:
+        idx = torch.empty((T, K), dtype=torch.int32, device=q_idx.device)
+    if count is None:
+        count = torch.empty((T,), dtype=torch.int32, device=q_idx.device)
+    st = lib.dsi_index_topk_prefill(_ptr(q_idx), _ptr(w), cache.ref(), T, H_i, int(q_offset),
+                                    int(K), _ptr(idx), _ptr(count), _stream(stream))
+    _check(lib, "dsi_index_topk_prefill", st)
+    return idx, count
+
+
+def probe_random_gather(base, row_pitch: int, rows, bytes_per_row: int, blocks: int,
+                        stream=None):
+    """Diagnostic: plain loads of randomly chosen rows of ``base`` (no output)."""
+    lib = load()
+    n_src = base.numel() * base.element_size() // row_pitch
+    st = lib.dsi_probe_random_gather(_ptr(base), int(row_pitch), int(n_src), _ptr(rows),
+                                     int(rows.numel()), int(bytes_per_row), int(blocks),
+                                     _stream(stream))
+    _check(lib, "dsi_probe_random_gather", st)
 
 
 def topk(scores, K: int, row_len=None, q_offset: int = 0, idx=None, count=None, stream=None,

@@ -166,6 +166,22 @@ dsi_status dsi_topk(const float* scores, int64_t ld_scores, int32_t rows, const 
                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dsi_status dsi_index_topk_prefill(const void* q_idx, const float* w, const dsi_cache* cache,
+                                  int32_t T, int32_t n_heads_idx, int64_t q_offset, int32_t K,
+                                  int32_t* idx, int32_t* count, void* stream) {
+  if (!q_idx || !w || !idx || T < 0 || K < 1) return DSI_ERR_INVALID_ARG;
+  if (n_heads_idx < 1 || n_heads_idx > 128 || K > DSI_MAX_K) return DSI_ERR_UNSUPPORTED;
+  dsi_status s = check_cache(cache, T, 0, q_offset, true, false);
+  if (s != DSI_OK) return s;
+  if (!aligned(q_idx, 16)) return DSI_ERR_INVALID_ARG;
+  if (T == 0) return DSI_OK;
+  CacheView v = view_of(cache);
+  if (!fused_prefill_topk_supported(v, n_heads_idx, T, q_offset, K)) return DSI_ERR_UNSUPPORTED;
+  return from_cuda(launch_index_topk_prefill(reinterpret_cast<const bf16*>(q_idx), w, v, T,
+                                             q_offset, K, idx, count, status_ptr(),
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 static dsi_status mla_common(const void* q, const dsi_cache* cache, const int32_t* idx, int rows,
                              int H, int K, int decode, int64_t q_offset, float scale, void* out,
                              float* lse, void* ws, size_t ws_bytes, void* stream) {
@@ -252,6 +268,18 @@ dsi_status dsi_indexed_attention(const void* q_idx, const float* w, const void* 
                         q_offset, scale, reinterpret_cast<bf16*>(out), lse, ws + p.mla_off,
                         p.total - p.mla_off, err, st);
   return from_cuda(e);
+}
+
+dsi_status dsi_probe_random_gather(const void* base, int64_t row_pitch, int64_t n_src_rows,
+                                   const int32_t* rows, int32_t n_rows, int32_t bytes_per_row,
+                                   int32_t blocks, void* stream) {
+  if (!base || !rows || n_rows < 0 || n_src_rows < 1 || blocks < 1) return DSI_ERR_INVALID_ARG;
+  if (row_pitch < 16 || row_pitch % 16 != 0 || bytes_per_row < 16 || bytes_per_row % 16 != 0 ||
+      bytes_per_row > row_pitch || !aligned(base, 16))
+    return DSI_ERR_INVALID_ARG;
+  if (n_rows == 0) return DSI_OK;
+  return from_cuda(launch_probe_gather(base, row_pitch, n_src_rows, rows, n_rows, bytes_per_row,
+                                       blocks, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dsi_status dsi_get_device_status(void* stream) {

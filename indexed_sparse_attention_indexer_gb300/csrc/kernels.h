@@ -48,4 +48,9 @@ cudaError_t launch_sparse_mla(const bf16* q, const CacheView& c, const int32_t* 
                               bf16* out, float* lse, void* ws, size_t ws_bytes, int* err,
                               cudaStream_t st);
 
+// Diagnostic random-row gather (probe_gather.cu).
+cudaError_t launch_probe_gather(const void* base, int64_t row_pitch, int64_t n_src_rows,
+                                const int32_t* rows, int n_rows, int bytes_per_row, int blocks,
+                                cudaStream_t st);
+
 }  // namespace dsi

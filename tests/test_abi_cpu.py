@@ -107,6 +107,43 @@ def test_index_score_validation(L):
     assert _score(L, _cache(batch=0), rows=0) == binding.DSI_OK
 
 
+def _itp(L, c, T=8, heads=64, q_offset=0, K=16, q=FAKE, w=FAKE, idx=FAKE):
+    return L.dsi_index_topk_prefill(q, w, ctypes.byref(c), T, heads, q_offset, K, idx, None, None)
+
+
+def test_index_topk_prefill_validation(L):
+    """Host checks of the fused prefill indexer: errors before any launch."""
+    E, U = binding.DSI_ERR_INVALID_ARG, binding.DSI_ERR_UNSUPPORTED
+    one = dict(batch=1, seq_lens=None)
+    assert _itp(L, _cache(**one), q=None) == E
+    assert _itp(L, _cache(**one), w=None) == E
+    assert _itp(L, _cache(**one), idx=None) == E
+    assert _itp(L, _cache(**one), T=-1) == E
+    assert _itp(L, _cache(**one), K=0) == E
+    assert _itp(L, _cache(**one), K=4097) == U
+    assert _itp(L, _cache(**one), heads=0) == U
+    assert _itp(L, _cache(batch=2, seq_lens=None)) == E       # prefill is one sequence
+    assert _itp(L, _cache(**one), T=8, q_offset=1020) == E    # beyond s_max
+    assert _itp(L, _cache(**one), heads=32) == U              # the fused kernel needs 64 x 128
+    assert _itp(L, _cache(d=64, **one)) == U
+    assert _itp(L, _cache(k_dtype=1, k_scale=FAKE, **one)) == U
+    assert _itp(L, _cache(**one), K=2049) == U
+    assert _itp(L, _cache(**one), T=0) == binding.DSI_OK
+
+
+def test_probe_gather_validation(L):
+    E = binding.DSI_ERR_INVALID_ARG
+    P = L.dsi_probe_random_gather
+    assert P(None, 1152, 10, FAKE, 4, 640, 1, None) == E
+    assert P(FAKE, 1152, 10, None, 4, 640, 1, None) == E
+    assert P(FAKE, 1150, 10, FAKE, 4, 640, 1, None) == E      # pitch not a multiple of 16
+    assert P(FAKE, 1152, 10, FAKE, 4, 650, 1, None) == E      # bytes not a multiple of 16
+    assert P(FAKE, 1152, 10, FAKE, 4, 1168, 1, None) == E     # bytes beyond the row
+    assert P(FAKE + 8, 1152, 10, FAKE, 4, 640, 1, None) == E  # misaligned base
+    assert P(FAKE, 1152, 10, FAKE, 4, 640, 0, None) == E
+    assert P(FAKE, 1152, 10, FAKE, 0, 640, 1, None) == binding.DSI_OK
+
+
 def test_topk_validation(L):
     E, U = binding.DSI_ERR_INVALID_ARG, binding.DSI_ERR_UNSUPPORTED
     assert L.dsi_topk(None, 16, 2, None, 0, 4, FAKE, None, None) == E

@@ -159,6 +159,12 @@ def test_fused_prefill_topk_matches_unfused(case):
     assert binding.device_status() == 0
     assert torch.equal(idx, idx2)
     assert torch.equal(count, cnt2)
+    # the fused indexer through its own entry point
+    idx3, cnt3 = binding.index_topk_prefill(g.q_idx, g.w, binding.Cache.of(g), K, off)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    assert torch.equal(idx3, idx2)
+    assert torch.equal(cnt3, cnt2)
     for t in (0, T // 2, T - 1):
         ref = oracle.prefill_row(ws, t)
         assert np.array_equal(idx[t].cpu().numpy(), ref["idx"]), f"row {t}"
