@@ -44,7 +44,8 @@ constexpr int kMaxRow = kCap * 64 / 2;       // bitmap of a row fits the 32 KB b
 constexpr int EPI_WARPS = 8;                 // 4 per token
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int THREADS = 64 + EPI_THREADS;    // 320
-constexpr int TMEM_COLS = 2 * N;             // 256
+constexpr int kAccBufs = 4;                  // score accumulators in TMEM
+constexpr int TMEM_COLS = kAccBufs * N;      // 512
 constexpr uint32_t IDESC = idesc_f32(1, kTileM, N);
 
 constexpr int OFF_A = 0;
@@ -57,7 +58,7 @@ constexpr int kHistInts = kSelBins + 32;                        // + reduction s
 constexpr int OFF_HIST = OFF_W + NT * kHeads * 4;               // NT x kHistInts int
 constexpr int OFF_TOK = OFF_HIST + NT * kHistInts * 4;          // per-token state
 constexpr int OFF_BAR = (OFF_TOK + NT * 64 + 7) & ~7;
-constexpr int NBARS = 2 * kStages + 2 + 2 + 2 + 2 + 1;
+constexpr int NBARS = 2 * kStages + 2 * kAccBufs + 2 + 2 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM = OFF_MISC + 64 + 1024;
 
@@ -68,6 +69,7 @@ struct TokState {
   int digit;                  // select scratch
   int krem;
   int total;
+  int stop;                   // set (never cleared) when a wait failed: the token's threads leave
 };
 static_assert(sizeof(TokState) <= 64, "token state");
 
@@ -83,9 +85,6 @@ struct Args {
   int pairs_per_cta;   // zigzag pairs handled by each CTA (ceil)
 };
 
-__device__ __forceinline__ void bar_epi() {          // all epilogue threads
-  asm volatile("bar.sync 1, %0;\n" ::"n"(EPI_THREADS) : "memory");
-}
 __device__ __forceinline__ void bar_tok(int tk) {    // the 128 threads of one token
   asm volatile("bar.sync %0, 128;\n" ::"r"(2 + tk) : "memory");
 }
@@ -238,8 +237,8 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* acc_full = bars + 2 * kStages;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* q_full = acc_empty + 2;
+  uint64_t* acc_empty = acc_full + kAccBufs;
+  uint64_t* q_full = acc_empty + kAccBufs;
   uint64_t* q_empty = q_full + 2;
   uint64_t* done_bar = q_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
@@ -248,14 +247,17 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kAccBufs; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], EPI_THREADS);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
+    for (int i = 0; i < NT; ++i) reinterpret_cast<TokState*>(smem + OFF_TOK)[i].stop = 0;
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
@@ -346,7 +348,7 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           mma_commit(&acc_full[abuf]);
           if (j == ntile - 1) mma_commit(&q_empty[slot]);
           if (++stage == kStages) { stage = 0; ph ^= 1; }
-          if (++abuf == 2) { abuf = 0; aph ^= 1; }
+          if (++abuf == kAccBufs) { abuf = 0; aph ^= 1; }
         }
       }
       mma_commit(done_bar);
@@ -375,12 +377,15 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       const int64_t nvis = live ? a.q_offset + r + 1 : 0;
       if (tt < kHeads) wts[tt] = live ? __ldg(a.w + (int64_t)r * kHeads + tt) : 0.f;
       if (tt == 0) { ts->theta = 0ull; ts->cnt = 0; }
-      bar_epi();
+      bar_tok(tk);
       const int ntile = group_tiles(a, g);
       for (int j = 0; j < ntile; ++j) {
+        // the stop decision is published before the token's barrier and read
+        // after it, so its four warps leave together (none is left waiting)
         const bool got = warp_wait(&acc_full[abuf], aph, abort_flag, err);
-        bar_epi();
-        if (!got || *abort_flag) { ok = false; break; }
+        if (lane == 0 && (!got || *abort_flag)) ts->stop = 1;
+        bar_tok(tk);
+        if (ts->stop) { ok = false; break; }
         tc_fence_after();
         float v[kHeads];
         const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + abuf * N + tk * kHeads;
@@ -389,7 +394,7 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&acc_empty[abuf]);
-        if (++abuf == 2) { abuf = 0; aph ^= 1; }
+        if (++abuf == kAccBufs) { abuf = 0; aph ^= 1; }
         const int64_t p = (int64_t)j * kTileM + row;
         unsigned long long key = 0ull;
         bool take = false;
@@ -412,7 +417,7 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           slot0 = __shfl_sync(0xffffffffu, slot0, __ffs(tm) - 1);
           if (take) buf[slot0 + __popc(tm & ((1u << lane) - 1u))] = key;
         }
-        bar_epi();
+        bar_tok(tk);
         // keep room for one more tile: compact a buffer that could overflow
         if (ts->cnt > kCap - kTileM) {
           const int n = ts->cnt;
@@ -420,7 +425,7 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           compact_ge(buf, n, t, ts, tt, tk);
           if (tt == 0) { ts->cnt = a.K; ts->theta = t - 1ull; }
         }
-        bar_epi();
+        bar_tok(tk);
       }
       if (!ok) break;
       // ---- final selection of the group's rows -------------------------------
@@ -477,7 +482,7 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         for (int i = n + tt; i < a.K; i += 128) out[i] = -1;
         if (a.count && tt == 0) a.count[r] = n;
       }
-      bar_epi();
+      bar_tok(tk);
     }
   }
   tc_fence_before();
