@@ -85,6 +85,18 @@ struct Args {
   int pairs_per_cta;   // zigzag pairs handled by each CTA (ceil)
 };
 
+// Two independent fp32 FMAs in one instruction (each rounded as fmaf would).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+
 __device__ __forceinline__ void bar_tok(int tk) {    // the 128 threads of one token
   asm volatile("bar.sync %0, 128;\n" ::"r"(2 + tk) : "memory");
 }
@@ -118,6 +130,7 @@ __device__ unsigned long long select_kth(const unsigned long long* buf, int n, i
   const int lane = tt & 31, wq = tt >> 5;
   const unsigned kAll = 0xffffffffu;
   unsigned long long mn = ~0ull, mx = 0ull;
+#pragma unroll 4
   for (int i = tt; i < n; i += 128) {
     const unsigned long long c = buf[i];
     mn = c < mn ? c : mn;
@@ -148,6 +161,7 @@ __device__ unsigned long long select_kth(const unsigned long long* buf, int n, i
     const int sh = bits > kSelBits ? bits - kSelBits : 0;
     for (int i = tt; i < kSelBins; i += 128) hist[i] = 0;
     bar_tok(tk);
+#pragma unroll 4
     for (int i = tt; i < n; i += 128) {
       const unsigned long long off = buf[i] - lo;         // wraps for keys below lo
       if (off <= span) atomicAdd(&hist[(int)(off >> sh)], 1);
@@ -399,13 +413,18 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         unsigned long long key = 0ull;
         bool take = false;
         if (live && p < nvis) {
-          float s0 = 0.f, s1 = 0.f;
+          // weights four at a time, products two per instruction, two chains
+          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+          const float4* w4 = reinterpret_cast<const float4*>(wts);
 #pragma unroll
-          for (int h = 0; h < kHeads; h += 2) {
-            s0 = fmaf(wts[h], fmaxf(v[h], 0.f), s0);
-            s1 = fmaf(wts[h + 1], fmaxf(v[h + 1], 0.f), s1);
+          for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+            const float4 ww = w4[h4];
+            a0 = ffma2(make_float2(ww.x, ww.y),
+                       make_float2(fmaxf(v[4 * h4], 0.f), fmaxf(v[4 * h4 + 1], 0.f)), a0);
+            a1 = ffma2(make_float2(ww.z, ww.w),
+                       make_float2(fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f)), a1);
           }
-          key = ((unsigned long long)score_key(s0 + s1) << 32) |
+          key = ((unsigned long long)score_key((a0.x + a1.x) + (a0.y + a1.y)) << 32) |
                 (unsigned long long)(0xFFFFFFFFu - (uint32_t)p);
           take = key > ts->theta;
         }
