@@ -12,6 +12,31 @@ namespace dsi {
 // Counts kernel launches made by the library (dsi_launch_count()).
 void note_launch(int n = 1);
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel on the stream finishes (once that kernel has signalled
+// griddepcontrol.launch_dependents, or at its end); the kernel itself executes
+// griddepcontrol.wait before it reads anything the previous kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// Device side of the same: wait for the previous kernel's results / let the
+// next kernel start its set-up.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 // ---- indexer scoring -------------------------------------------------------
 // scores[r, s] for s < visible_len(r); kernels: warp-shuffle streaming (few
 // heads), tcgen05 tensor-core tiles (64 heads x 128 dims), generic SIMT.

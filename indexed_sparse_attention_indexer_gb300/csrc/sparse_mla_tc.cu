@@ -152,18 +152,10 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   const int32_t* irow = a.idx + (int64_t)r * a.K;
   const int g0 = rho ? 4 : 0;                      // first gathered 64-dim block
   const int qk_first = rho ? 1 : 0;                // first stage block used by the logits
-  // the split's entries: each thread's index loads go out first (they gate the
-  // first gather), then its share of the query slice
-  constexpr int kPer = (kMaxEntries + kThreads - 1) / kThreads;
-  int pos[kPer];
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int jj = tid + u * kThreads;
-    pos[u] = (jj < span && j_begin + jj < j_end) ? __ldg(irow + j_begin + jj) : -1;
-  }
-  // this CTA's slice of the head's query row is loaded now, so it lands while
-  // the entries are being staged: the exchange warps take its first two 64-dim
-  // blocks, the softmax warps the rest (two, or three on CTA 0)
+  // this CTA's slice of the head's query row is loaded first, so it lands
+  // while the entries are being staged (and, launched behind the select
+  // kernel, while that kernel finishes): the exchange warps take its first two
+  // 64-dim blocks, the softmax warps the rest (two, or three on CTA 0)
   uint4 qv[24];
   if (warp >= kExWarp0) {
     const int c_lo = warp < kSmWarp0 ? 0 : 2;
@@ -194,6 +186,15 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     fence_barrier_init();
   }
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, TMEM_COLS);
+  // the selected indices come from the previous kernel
+  grid_dep_wait();
+  constexpr int kPer = (kMaxEntries + kThreads - 1) / kThreads;
+  int pos[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int jj = tid + u * kThreads;
+    pos[u] = (jj < span && j_begin + jj < j_end) ? __ldg(irow + j_begin + jj) : -1;
+  }
   __syncthreads();
   // the split's entries, translated once to physical cache rows (-1 = skipped)
   {
@@ -661,9 +662,8 @@ cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const int32_
   if (e != cudaSuccess) return e;
   const long blocks = 2L * rows * a.splits;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
-  mla_tc<<<(unsigned)blocks, kThreads, SMEM, st>>>(lmap, c, a, err);
+  e = launch_overlapped(mla_tc, dim3((unsigned)blocks), dim3(kThreads), SMEM, st, lmap, c, a, err);
   note_launch();
-  e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
   return launch_mla_combine(a.part_o, a.part_ml, rows, H, a.splits, out, lse, st);
 }

@@ -157,6 +157,10 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, const int32_t* __res
   __shared__ int wsum[2][kWarps];
   __shared__ int wbase[2][kWarps];
   __shared__ uint32_t s_sel[2];
+  // the scores come from the previous kernel; the attention kernel after this
+  // one may start its set-up now
+  grid_dep_wait();
+  grid_dep_launch();
   const int r = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const unsigned kAll = 0xffffffffu;
@@ -319,9 +323,10 @@ cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t
   if (rows <= 0) return cudaSuccess;
   const int64_t longest = row_len ? ld : (q_offset + rows < ld ? q_offset + rows : ld);
   if (longest <= kRegKeysMax) {
-    topk_rows_reg<<<rows, kTopkThreads, 0, st>>>(scores, ld, row_len, q_offset, K, idx, count);
+    cudaError_t e = launch_overlapped(topk_rows_reg, dim3(rows), dim3(kTopkThreads), 0, st, scores,
+                                      ld, row_len, q_offset, K, idx, count);
     note_launch();
-    return cudaGetLastError();
+    return e;
   }
   // stage rows in shared memory when the longest possible row fits
   const int stage = longest <= kTopkSmemKeys;
