@@ -129,6 +129,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
          CacheView c, ScoreArgs a, int* err) {
   using C = Cfg<NT, FP8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  grid_dep_wait();   // inputs may come from the kernel launched just before
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   float* wbuf = reinterpret_cast<float*>(smem + C::OFF_W);
@@ -445,9 +446,10 @@ cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, 
   cudaError_t e = cudaFuncSetAttribute(score_tc<NT, FP8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  score_tc<NT, FP8><<<sms, C::THREADS, C::SMEM, st>>>(kmap, qmap, c, a, err);
+  cudaError_t le = launch_overlapped(score_tc<NT, FP8>, dim3(sms), dim3(C::THREADS), C::SMEM,
+                                     st, kmap, qmap, c, a, err);
   note_launch();
-  return cudaGetLastError();
+  return le;
 }
 
 }  // namespace

@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                    CacheView c, Args a, int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  grid_dep_wait();   // inputs may come from the kernel launched just before
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -553,9 +554,10 @@ cudaError_t launch_index_topk_prefill(const bf16* q_idx, const float* w, const C
   cudaError_t e = cudaFuncSetAttribute(index_topk_prefill,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
-  index_topk_prefill<<<grid, THREADS, SMEM, st>>>(kmap, qmap, c, a, err);
+  cudaError_t le = launch_overlapped(index_topk_prefill, dim3(grid), dim3(THREADS), SMEM,
+                                     st, kmap, qmap, c, a, err);
   note_launch();
-  return cudaGetLastError();
+  return le;
 }
 
 }  // namespace dsi

@@ -224,6 +224,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     for (int i = 0; i < kXBufs && i < n_tiles; ++i) mbar_arrive_expect_tx(&x_full[i], kXBytes);
   }
   cluster_sync();   // the peer's barriers exist (and are armed) before anyone uses them
+  grid_dep_launch();   // the next kernel on the stream may start its set-up
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
