@@ -10,8 +10,10 @@
 // (the lowest positions among them), then the kept positions are written
 // ascending with block-wide prefix sums.
 //
-// Rows of up to 32768 positions (topk_rows_reg): the keys stay in registers,
-// each warp holding 1024 consecutive positions.  The search narrows an interval [lo, hi]
+// Rows of up to 131072 positions (topk_rows_reg): 32768-position chunks, each
+// warp holding 1024 consecutive positions of a chunk in registers; a row of
+// one chunk stays in registers, longer rows reload their chunks from L2 for
+// each pass.  The search narrows an interval [lo, hi]
 // that holds T, starting from the row's min and max key: each pass splits the
 // interval into 2048 equal bins (11 bits of the key range per pass, so at most
 // three passes) and keeps the bin where the count from the top reaches K.
@@ -20,7 +22,7 @@
 // warps once (per-warp counts) and then each warp walks its positions in
 // order with ballots, so every store of a round is one contiguous run.
 //
-// Longer rows (topk_rows): four 8-bit MSB-first histogram passes and a
+// Still longer rows (topk_rows): four 8-bit MSB-first histogram passes and a
 // compaction walking the row in chunks; rows that fit are staged in shared
 // memory once, longer ones re-read from global memory (L2) each pass.
 #include "kernels.h"
@@ -145,11 +147,23 @@ topk_rows(const float* __restrict__ scores, int64_t ld, const int32_t* __restric
 }
 
 constexpr int kRegPer = 32;                               // keys per thread
-constexpr int kRegKeysMax = kTopkThreads * kRegPer;        // 32768
+constexpr int kRegKeysMax = kTopkThreads * kRegPer;        // 32768 per chunk
+constexpr int kRegChunks = 4;                              // rows up to 131072 positions
 constexpr int kBins = 2048;                                // 11-bit digits of the key range
 constexpr int kWarps = kTopkThreads / 32;
 static_assert(kBins == 64 * kWarps, "each warp owns 64 bins in the bin search");
 
+// Loads chunk c (32768 positions) of the row into the thread's registers.
+__device__ __forceinline__ void load_chunk(uint32_t* key, const float* grow, int64_t n, int c,
+                                           int wpos, int lane) {
+#pragma unroll
+  for (int i = 0; i < kRegPer; ++i) {
+    const int64_t p = (int64_t)c * kRegKeysMax + wpos + 32 * i + lane;
+    key[i] = p < n ? max(score_key(__ldg(grow + p)), 1u) : 0u;
+  }
+}
+
+template <bool kChunked>
 __global__ void __launch_bounds__(kTopkThreads, 1)
 topk_rows_reg(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
               int64_t q_offset, int K, int32_t* __restrict__ idx, int32_t* __restrict__ count) {
@@ -175,26 +189,29 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, const int32_t* __res
     if (count && tid == 0) count[r] = (int32_t)n;
     return;
   }
-  // ---- keys: warp w holds positions 1024w .. 1024w+1023; in round i lane l
-  // holds position 1024w + 32i + l (every load is one coalesced line per warp).
-  // Valid keys are at least 1 (every non-NaN score maps far above it); slots
-  // past the row end hold 0, so they fall below every interval searched and
-  // below T, and need no separate validity test.
+  // ---- keys: the row in chunks of 32768 positions; within a chunk warp w
+  // holds positions 1024w .. 1024w+1023, in round i lane l position
+  // 1024w + 32i + l (every load is one coalesced line per warp).  A row of one
+  // chunk stays in registers throughout; longer rows reload each chunk per
+  // pass (from L2).  Valid keys are at least 1 (every non-NaN score maps far
+  // above it); slots past the row end hold 0, so they fall below every
+  // interval searched and below T, and need no separate validity test.
+  const int nchunks = kChunked ? (int)((n + kRegKeysMax - 1) / kRegKeysMax) : 1;
+  const bool resident = !kChunked;
   const int wpos = wid * (kRegPer * 32);
   uint32_t key[kRegPer];
-#pragma unroll
-  for (int i = 0; i < kRegPer; ++i) {
-    const int p = wpos + 32 * i + lane;
-    key[i] = p < n ? max(score_key(__ldg(grow + p)), 1u) : 0u;
-  }
+  if (resident) load_chunk(key, grow, n, 0, wpos, lane);
   for (int i = tid; i < 2 * kBins; i += blockDim.x) (&hist[0][0])[i] = 0;
   // ---- the row's key range ------------------------------------------------
   {
     uint32_t kmax = 0u, kmin = 0xffffffffu;
+    for (int c = 0; c < nchunks; ++c) {
+      if (!resident) load_chunk(key, grow, n, c, wpos, lane);
 #pragma unroll
-    for (int i = 0; i < kRegPer; ++i) {
-      kmax = max(kmax, key[i]);
-      kmin = min(kmin, key[i] == 0u ? 0xffffffffu : key[i]);
+      for (int i = 0; i < kRegPer; ++i) {
+        kmax = max(kmax, key[i]);
+        kmin = min(kmin, key[i] == 0u ? 0xffffffffu : key[i]);
+      }
     }
     kmax = __reduce_max_sync(kAll, kmax);
     kmin = __reduce_min_sync(kAll, kmin);
@@ -217,10 +234,13 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, const int32_t* __res
     const int bits = 32 - __clz(span);
     const int sh = bits > 11 ? bits - 11 : 0;          // bins of 2^sh keys cover [lo, hi]
     int* h = hist[pass & 1];
+    for (int c = 0; c < nchunks; ++c) {
+      if (!resident) load_chunk(key, grow, n, c, wpos, lane);
 #pragma unroll
-    for (int i = 0; i < kRegPer; ++i) {
-      const uint32_t off = key[i] - lo;                 // wraps for keys below lo
-      if (off <= span) atomicAdd(&h[off >> sh], 1);
+      for (int i = 0; i < kRegPer; ++i) {
+        const uint32_t off = key[i] - lo;                 // wraps for keys below lo
+        if (off <= span) atomicAdd(&h[off >> sh], 1);
+      }
     }
     __syncthreads();
     // warp w owns bins 2047-64w down to 1984-64w, lane l the pair starting at
@@ -261,59 +281,68 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, const int32_t* __res
     if (sh == 0) break;
   }
   const uint32_t T = lo;
-  // ---- ordered compaction -----------------------------------------------------
+  // ---- ordered compaction, chunk by chunk -------------------------------------
   // per-warp counts of keys above T and equal to T; warp 0 turns them into
-  // each warp's rank among equals and output offset
-  int gt = 0, eq = 0;
-#pragma unroll
-  for (int i = 0; i < kRegPer; ++i) { gt += key[i] > T; eq += key[i] == T; }
-  gt = __reduce_add_sync(kAll, gt);
-  eq = __reduce_add_sync(kAll, eq);
+  // each warp's rank among equals and output offset, carrying both across
+  // chunks (a chunk's positions all follow the previous chunk's)
+  int eq_run = 0, sel_run = 0;           // warp 0: equals and kept keys in earlier chunks
   __syncthreads();                       // s_sel / wsum readers of the last pass are done
-  if (lane == 0) { wsum[0][wid] = gt; wsum[1][wid] = eq; }
-  __syncthreads();
-  if (wid == 0) {
-    const int g = wsum[0][lane], e = wsum[1][lane];
-    int ei = e;
+  for (int c = 0; c < nchunks; ++c) {
+    if (!resident) load_chunk(key, grow, n, c, wpos, lane);
+    int gt = 0, eq = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(kAll, ei, o);
-      if (lane >= o) ei += y;
-    }
-    const int ebase = ei - e;
-    int take = krem - ebase;
-    take = take < 0 ? 0 : (take > e ? e : take);
-    const int sel = g + take;
-    int si = sel;
+    for (int i = 0; i < kRegPer; ++i) { gt += key[i] > T; eq += key[i] == T; }
+    gt = __reduce_add_sync(kAll, gt);
+    eq = __reduce_add_sync(kAll, eq);
+    if (lane == 0) { wsum[0][wid] = gt; wsum[1][wid] = eq; }
+    __syncthreads();
+    if (wid == 0) {
+      const int g = wsum[0][lane], e = wsum[1][lane];
+      int ei = e;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(kAll, si, o);
-      if (lane >= o) si += y;
-    }
-    wbase[0][lane] = ebase;
-    wbase[1][lane] = si - sel;
-  }
-  __syncthreads();
-  int eq_rank = wbase[0][wid], pos = wbase[1][wid];
-  if (eq == 0) {                         // warp-uniform: no ties at T in this warp
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kAll, ei, o);
+        if (lane >= o) ei += y;
+      }
+      const int ebase = eq_run + ei - e;
+      int take = krem - ebase;
+      take = take < 0 ? 0 : (take > e ? e : take);
+      const int sel = g + take;
+      int si = sel;
 #pragma unroll
-    for (int i = 0; i < kRegPer; ++i) {
-      const bool keep = key[i] > T;
-      const unsigned km = __ballot_sync(kAll, keep);
-      if (keep) out[pos + __popc(km & lt_mask)] = wpos + 32 * i + lane;
-      pos += __popc(km);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kAll, si, o);
+        if (lane >= o) si += y;
+      }
+      wbase[0][lane] = ebase;
+      wbase[1][lane] = sel_run + si - sel;
+      eq_run += __shfl_sync(kAll, ei, 31);
+      sel_run += __shfl_sync(kAll, si, 31);
     }
-  } else {
+    __syncthreads();
+    int eq_rank = wbase[0][wid], pos = wbase[1][wid];
+    const int cpos = c * kRegKeysMax + wpos;
+    if (eq == 0) {                       // warp-uniform: no ties at T in this warp
 #pragma unroll
-    for (int i = 0; i < kRegPer; ++i) {
-      const bool is_eq = key[i] == T;
-      const unsigned em = __ballot_sync(kAll, is_eq);
-      const bool keep = key[i] > T || (is_eq && eq_rank + __popc(em & lt_mask) < krem);
-      const unsigned km = __ballot_sync(kAll, keep);
-      if (keep) out[pos + __popc(km & lt_mask)] = wpos + 32 * i + lane;
-      pos += __popc(km);
-      eq_rank += __popc(em);
+      for (int i = 0; i < kRegPer; ++i) {
+        const bool keep = key[i] > T;
+        const unsigned km = __ballot_sync(kAll, keep);
+        if (keep) out[pos + __popc(km & lt_mask)] = cpos + 32 * i + lane;
+        pos += __popc(km);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kRegPer; ++i) {
+        const bool is_eq = key[i] == T;
+        const unsigned em = __ballot_sync(kAll, is_eq);
+        const bool keep = key[i] > T || (is_eq && eq_rank + __popc(em & lt_mask) < krem);
+        const unsigned km = __ballot_sync(kAll, keep);
+        if (keep) out[pos + __popc(km & lt_mask)] = cpos + 32 * i + lane;
+        pos += __popc(km);
+        eq_rank += __popc(em);
+      }
     }
+    __syncthreads();                     // wsum / wbase are rewritten for the next chunk
   }
   if (count && tid == 0) count[r] = K;
 }
@@ -322,9 +351,13 @@ cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t
                         int64_t q_offset, int K, int32_t* idx, int32_t* count, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const int64_t longest = row_len ? ld : (q_offset + rows < ld ? q_offset + rows : ld);
-  if (longest <= kRegKeysMax) {
-    cudaError_t e = launch_overlapped(topk_rows_reg, dim3(rows), dim3(kTopkThreads), 0, st, scores,
-                                      ld, row_len, q_offset, K, idx, count);
+  if (longest <= kRegChunks * kRegKeysMax) {
+    cudaError_t e =
+        longest <= kRegKeysMax
+            ? launch_overlapped(topk_rows_reg<false>, dim3(rows), dim3(kTopkThreads), 0, st, scores,
+                                ld, row_len, q_offset, K, idx, count)
+            : launch_overlapped(topk_rows_reg<true>, dim3(rows), dim3(kTopkThreads), 0, st, scores,
+                                ld, row_len, q_offset, K, idx, count);
     note_launch();
     return e;
   }

@@ -197,7 +197,9 @@ TOPK_CASES = [
     (2, 70000, 4096, 1 << 20, False),
     (3, 32768, 2048, 1 << 20, True),  # the register-resident kernel at its largest rows
     (2, 32767, 2048, 7, False),       # odd row stride (unaligned rows, scalar loads)
-    (2, 32769, 100, 50, False),       # one past the register-resident kernel
+    (2, 32769, 100, 50, False),       # one past the register-resident rows: two chunks
+    (2, 131072, 2048, 1 << 16, True), # four chunks, the longest rows the chunked kernel takes
+    (1, 140000, 512, 100, False),     # beyond: the 8-bit radix kernel, re-reading from L2
 ]
 
 
