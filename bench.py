@@ -54,7 +54,7 @@ def algorithmic_bytes(ws) -> dict:
     B = ws.T
     lens = ws.seq_lens.to(torch.int64).cpu()
     if ws.mode == "decode":
-        vis = lens
+        vis = decode_visible(ws)
     else:
         vis = torch.arange(1, B + 1, dtype=torch.int64) + ws.q_offset
     kel = ws.k_idx.element_size()
@@ -78,9 +78,19 @@ def scoring_kernel_bytes(ws) -> int:
     return a["index_keys"] + ws.q_idx.numel() * 2 + ws.w.numel() * 4 + a["score_rows"] // 2
 
 
-def algorithmic_flops(ws) -> dict:
+def decode_visible(ws) -> torch.Tensor:
+    """Visible history of every decode row: T candidate rows per sequence, row
+    (b, t) sees seq_lens[b] - (T - 1 - t) positions (T = 1: seq_lens)."""
+    T = ws.tokens_per_seq
     lens = ws.seq_lens.to(torch.int64).cpu()
-    vis = lens if ws.mode == "decode" else torch.arange(1, ws.T + 1) + ws.q_offset
+    if T == 1:
+        return lens
+    t = torch.arange(T, dtype=torch.int64)
+    return torch.clamp(lens.view(-1, 1) - (T - 1 - t).view(1, -1), min=0).reshape(-1)
+
+
+def algorithmic_flops(ws) -> dict:
+    vis = decode_visible(ws) if ws.mode == "decode" else torch.arange(1, ws.T + 1) + ws.q_offset
     idx_fl = 2 * int(vis.sum()) * ws.H_i * ws.d
     sel = torch.clamp(vis, max=ws.K)
     mla_fl = 2 * int(sel.sum()) * ws.H * (W.D_QK + W.D_LATENT)
@@ -259,7 +269,8 @@ def run_gpu(args):
     cfg = W.CONFIGS[args.config]
     # seeded per config; each rank its own replica (--rows: a smaller decode batch
     # for profiling captures, never a bench line)
-    ws = W.make_config(args.config, device=dev, rows=args.rows)
+    ws = W.make_config(args.config, device=dev, rows=args.rows, tokens_per_seq=args.tokens_per_seq)
+    tps = ws.tokens_per_seq
     torch.cuda.synchronize()
     binding.load()
     stream = torch.cuda.current_stream()
@@ -274,9 +285,14 @@ def run_gpu(args):
     cnt = torch.empty((ws.T,), dtype=torch.int32, device=dev)
 
     def step():
-        binding.indexed_attention(ws.q_idx, ws.w, ws.q, cache, ws.K, ws.scale, decode,
-                                  ws.q_offset, out=out, lse=lse, idx=idx, count=cnt,
-                                  workspace=wsp, stream=stream)
+        if tps > 1:
+            binding.indexed_attention_multi(ws.q_idx, ws.w, ws.q, cache, tps, ws.K, ws.scale,
+                                            out=out, lse=lse, idx=idx, count=cnt, workspace=wsp,
+                                            stream=stream)
+        else:
+            binding.indexed_attention(ws.q_idx, ws.w, ws.q, cache, ws.K, ws.scale, decode,
+                                      ws.q_offset, out=out, lse=lse, idx=idx, count=cnt,
+                                      workspace=wsp, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -309,7 +325,15 @@ def run_gpu(args):
 
     hbm, tfl, src = peaks()
     extra = {}
-    if decode:
+    if decode and tps > 1:
+        # multi-token step: the scoring entry point takes one row per sequence,
+        # so the step itself stands in for the kernel (HBM-bound like decode)
+        ab_step = algorithmic_bytes(ws)["total"]
+        achieved = ab_step / (ms_step / 1e3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "step", "achieved": round(achieved, 1), "peak": hbm,
+                    "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": src,
+                    "traffic": None, "algorithmic_bytes": ab_step, "kernel_ms": round(ms_step, 5)}
+    elif decode:
         # ---- dominant kernel: the indexer scoring launch, timed alone ------
         scores = torch.empty((ws.T, span), dtype=torch.float32, device=dev)
         k_ms = time_alone(lambda: binding.index_score(ws.q_idx, ws.w, cache, decode, ws.q_offset,
@@ -368,6 +392,8 @@ def run_gpu(args):
         }
         if args.rows:
             result["config"]["profiling_rows"] = args.rows
+        if tps > 1:
+            result["config"]["tokens_per_seq"] = tps
         if world == 1 and not args.no_cpu:
             result["cpu_baseline"] = cpu_baseline(ws, budget_s=args.cpu_seconds)
     barrier(world)
@@ -409,9 +435,14 @@ def run_e2e(ws, cache, wsp, decode, args, stream, dev):
             landed.record(s_in)
         stream.wait_event(landed)
         stream.wait_event(read_back[i])           # step k-2's output was read
-        binding.indexed_attention(d_qidx, d_w, d_q, cache, ws.K, ws.scale, decode, ws.q_offset,
-                                  out=d_out, workspace=wsp, want_lse=False, want_idx=False,
-                                  stream=stream)
+        if ws.tokens_per_seq > 1:
+            binding.indexed_attention_multi(d_qidx, d_w, d_q, cache, ws.tokens_per_seq, ws.K,
+                                            ws.scale, out=d_out, workspace=wsp, want_lse=False,
+                                            want_idx=False, stream=stream)
+        else:
+            binding.indexed_attention(d_qidx, d_w, d_q, cache, ws.K, ws.scale, decode, ws.q_offset,
+                                      out=d_out, workspace=wsp, want_lse=False, want_idx=False,
+                                      stream=stream)
         computed[i].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(computed[i])
@@ -561,6 +592,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--gather-ceiling", action="store_true",
                     help="diagnostic: random-row gather bandwidth of plain loads (not a bench line)")
+    ap.add_argument("--tokens-per-seq", type=int, default=1,
+                    help="decode workloads: candidate tokens verified per sequence in one step "
+                         "(multi-token decode; the default line is 1)")
     ap.add_argument("--rows", type=int, default=None,
                     help="profiling aid: a smaller decode batch (the printed line is not a bench line)")
     args = ap.parse_args()

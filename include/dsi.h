@@ -136,6 +136,32 @@ dsi_status dsi_topk(const float* scores, int64_t ld_scores, int32_t rows,
                     int32_t* idx, int32_t* count, void* stream);
 
 /*
+ * dsi_indexed_attention_multi — the fused layer for a multi-token decode step
+ * (speculative verification: T candidate tokens per sequence checked at once).
+ * ("Day 0 Inference Acceleration for New LLM Architectures: Hybrid Attention
+ * Adaptation and Optimization Practices" §6: the speculative path reuses the
+ * same index selection with a different candidate length.)
+ *
+ * Rows come tokens_per_seq (T) to a sequence: row r is candidate t = r % T of
+ * sequence b = r / T.  The T candidates' keys are the last T cached positions
+ * of sequence b (seq_lens[b] counts them), and candidate t sees positions
+ * 0 .. seq_lens[b] - T + t (itself and everything before it).  Each row then
+ * goes through the same indexer, Top-K and sparse attention as one decode
+ * token (dsi_indexed_attention with decode = 1 is the T = 1 case).
+ *   q_idx  bf16 [batch*T, n_heads_idx, d];  w  fp32 [batch*T, n_heads_idx]
+ *   q      bf16 [batch*T, n_heads, 576];    out bf16 [batch*T, n_heads, 512]
+ *   idx_out / count_out / lse / workspace as for dsi_indexed_attention with
+ *   rows = batch*T (dsi_workspace_size(batch*T, n_heads_idx, n_heads, K, s_max, 1)).
+ * Errors: as dsi_indexed_attention; DSI_ERR_INVALID_ARG for T < 1.
+ */
+dsi_status dsi_indexed_attention_multi(const void* q_idx, const float* w, const void* q,
+                                       const dsi_cache* cache, int32_t tokens_per_seq,
+                                       int32_t n_heads_idx, int32_t n_heads, int32_t K,
+                                       float scale, int32_t* idx_out, int32_t* count_out,
+                                       void* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/*
  * dsi_index_topk_prefill — the prefill indexer in one kernel: scores, ReLU
  * gate, head weights and the running per-row Top-K, writing only indices.
  * ("Day 0 Inference Support for New LLM Architectures: Optimization

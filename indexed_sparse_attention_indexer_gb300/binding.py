@@ -52,6 +52,10 @@ SIGNATURES = {
                                         c_int32, c_int32, c_int32, c_int32, c_int64, c_float,
                                         c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
                                         c_void_p, c_size_t, c_void_p]),
+    "dsi_indexed_attention_multi": (c_int32, [c_void_p, c_void_p, c_void_p, ctypes.POINTER(DsiCache),
+                                              c_int32, c_int32, c_int32, c_int32, c_float, c_void_p,
+                                              c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                              c_void_p]),
     "dsi_indexed_attention_static": (c_int32, [c_void_p, c_void_p, c_void_p,
                                                ctypes.POINTER(DsiCache), c_int32, c_int32,
                                                c_int32, c_int32, c_int64, c_float, c_int32,
@@ -277,6 +281,36 @@ def indexed_attention(q_idx, w, q, cache: Cache, K: int, scale: float, decode: b
                                    _ptr(count), _ptr(out), _ptr(lse), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream))
     _check(lib, "dsi_indexed_attention", st)
+    return out, lse, idx, count
+
+
+def indexed_attention_multi(q_idx, w, q, cache: Cache, tokens_per_seq: int, K: int, scale: float,
+                            out=None, lse=None, idx=None, count=None, workspace=None,
+                            want_lse=True, want_idx=True, stream=None, checked: bool = False):
+    """A multi-token decode step through ``dsi_indexed_attention_multi``: rows
+    come ``tokens_per_seq`` to a sequence (row r is candidate r % T of
+    sequence r // T)."""
+    lib = load(checked)
+    rows, H_i, H = int(q_idx.shape[0]), int(q_idx.shape[1]), int(q.shape[1])
+    dev = q.device
+    if workspace is None:
+        workspace = alloc_workspace(workspace_size(rows, H_i, H, K, cache.struct.s_max, True,
+                                                   checked), dev)
+    if out is None:
+        out = torch.empty((rows, H, D_LATENT), dtype=torch.bfloat16, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((rows, H), dtype=torch.float32, device=dev)
+    if idx is None and want_idx:
+        idx = torch.empty((rows, K), dtype=torch.int32, device=dev)
+    if count is None and want_idx:
+        count = torch.empty((rows,), dtype=torch.int32, device=dev)
+    st = lib.dsi_indexed_attention_multi(_ptr(q_idx), _ptr(w), _ptr(q), cache.ref(),
+                                         int(tokens_per_seq), H_i, H, int(K), float(scale),
+                                         _ptr(idx), _ptr(count), _ptr(out), _ptr(lse),
+                                         _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream(stream))
+    _check(lib, "dsi_indexed_attention_multi", st)
     return out, lse, idx, count
 
 

@@ -27,6 +27,7 @@ struct CacheView {
   int32_t d;
   int32_t k_dtype;
   int32_t batch;
+  int32_t tokens_per_seq;   // decode: query rows per sequence (1; T for a multi-token step)
 };
 
 // Device status word codes (mirrors dsi_status).
@@ -36,12 +37,22 @@ __device__ __forceinline__ void report(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
-// Number of history positions visible to row r (a decode length beyond the
-// cache's rows per sequence is clamped to them).
+// Sequence of query row r: decode rows come tokens_per_seq to a sequence
+// (row r is token r % T of sequence r / T); prefill rows all belong to one.
+__device__ __forceinline__ int seq_of_row(const CacheView& c, int r, int decode) {
+  if (!decode) return 0;
+  return c.tokens_per_seq == 1 ? r : r / c.tokens_per_seq;   // no division in the common case
+}
+
+// Number of history positions visible to row r.  Decode: the T new tokens of
+// a sequence are its last T cached positions, token t sees everything before
+// the later ones (a length beyond the cache's rows per sequence is clamped).
 __device__ __forceinline__ int64_t visible_len(const CacheView& c, int r, int decode,
                                                int64_t q_offset) {
   if (!decode) return q_offset + r + 1;
-  int64_t n = (int64_t)__ldg(c.seq_lens + r);
+  const int T = c.tokens_per_seq;
+  int64_t n = T == 1 ? (int64_t)__ldg(c.seq_lens + r)
+                     : (int64_t)__ldg(c.seq_lens + r / T) - (T - 1 - r % T);
   n = n < 0 ? 0 : n;
   return n > c.s_max ? c.s_max : n;
 }

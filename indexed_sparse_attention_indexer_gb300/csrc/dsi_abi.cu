@@ -41,7 +41,7 @@ dsi_status from_cuda(cudaError_t e) {
 
 // Validate a cache description for rows of a decode batch or of a prefill.
 dsi_status check_cache(const dsi_cache* c, int rows, int decode, int64_t q_offset, bool need_keys,
-                       bool need_latent) {
+                       bool need_latent, int tokens_per_seq = 1) {
   if (!c) return DSI_ERR_INVALID_ARG;
   if (c->batch < 0) return DSI_ERR_INVALID_ARG;
   if (need_keys) {
@@ -62,7 +62,8 @@ dsi_status check_cache(const dsi_cache* c, int rows, int decode, int64_t q_offse
     return DSI_ERR_INVALID_ARG;
   }
   if (decode) {
-    if (rows != c->batch || !c->seq_lens) return DSI_ERR_INVALID_ARG;
+    if ((int64_t)rows != (int64_t)c->batch * tokens_per_seq || !c->seq_lens)
+      return DSI_ERR_INVALID_ARG;
   } else {
     if (c->batch != 1 || q_offset < 0 || q_offset + rows > c->s_max) return DSI_ERR_INVALID_ARG;
   }
@@ -83,6 +84,7 @@ CacheView view_of(const dsi_cache* c) {
   v.d = c->d;
   v.k_dtype = c->k_dtype;
   v.batch = c->batch;
+  v.tokens_per_seq = 1;
   return v;
 }
 
@@ -226,17 +228,19 @@ size_t dsi_workspace_size(int32_t rows, int32_t n_heads_idx, int32_t n_heads, in
   return p.total > 0 ? p.total : 256;
 }
 
-dsi_status dsi_indexed_attention(const void* q_idx, const float* w, const void* q,
-                                 const dsi_cache* cache, int32_t rows, int32_t n_heads_idx,
-                                 int32_t n_heads, int32_t K, int64_t q_offset, float scale,
-                                 int32_t decode, int32_t* idx_out, int32_t* count_out, void* out,
-                                 float* lse, void* workspace, size_t workspace_bytes,
-                                 void* stream) {
+// The fused layer for rows of a decode batch (tokens_per_seq query tokens per
+// sequence) or of a prefill.
+static dsi_status layer_common(const void* q_idx, const float* w, const void* q,
+                               const dsi_cache* cache, int32_t rows, int32_t n_heads_idx,
+                               int32_t n_heads, int32_t K, int64_t q_offset, float scale,
+                               int32_t decode, int32_t tokens_per_seq, int32_t* idx_out,
+                               int32_t* count_out, void* out, float* lse, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   if (!q_idx || !w || !q || !out || rows < 0 || K < 1) return DSI_ERR_INVALID_ARG;
   if (n_heads_idx < 1 || n_heads_idx > 128 || K > DSI_MAX_K) return DSI_ERR_UNSUPPORTED;
   dsi_status s = check_mla_heads(n_heads);
   if (s != DSI_OK) return s;
-  s = check_cache(cache, rows, decode, q_offset, true, true);
+  s = check_cache(cache, rows, decode, q_offset, true, true, tokens_per_seq);
   if (s != DSI_OK) return s;
   if (!aligned(q_idx, 16) || !aligned(q, 16) || !aligned(out, 16)) return DSI_ERR_INVALID_ARG;
   if (!(scale == scale)) return DSI_ERR_INVALID_ARG;
@@ -250,6 +254,7 @@ dsi_status dsi_indexed_attention(const void* q_idx, const float* w, const void* 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* err = status_ptr();
   CacheView v = view_of(cache);
+  v.tokens_per_seq = tokens_per_seq;
   cudaError_t e;
   if (!decode && fused_prefill_topk_supported(v, n_heads_idx, rows, q_offset, K)) {
     // prefill: scores stay on chip, only the selected indices are written
@@ -261,13 +266,37 @@ dsi_status dsi_indexed_attention(const void* q_idx, const float* w, const void* 
                            q_offset, scores, p.ld, err, st);
     if (e != cudaSuccess) return from_cuda(e);
     e = launch_topk(scores, p.ld, rows, decode ? cache->seq_lens : nullptr, q_offset, K, idx,
-                    count_out, st);
+                    count_out, st, tokens_per_seq);
     if (e != cudaSuccess) return from_cuda(e);
   }
   e = launch_sparse_mla(reinterpret_cast<const bf16*>(q), v, idx, rows, n_heads, K, decode,
                         q_offset, scale, reinterpret_cast<bf16*>(out), lse, ws + p.mla_off,
                         p.total - p.mla_off, err, st);
   return from_cuda(e);
+}
+
+dsi_status dsi_indexed_attention(const void* q_idx, const float* w, const void* q,
+                                 const dsi_cache* cache, int32_t rows, int32_t n_heads_idx,
+                                 int32_t n_heads, int32_t K, int64_t q_offset, float scale,
+                                 int32_t decode, int32_t* idx_out, int32_t* count_out, void* out,
+                                 float* lse, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  return layer_common(q_idx, w, q, cache, rows, n_heads_idx, n_heads, K, q_offset, scale, decode,
+                      1, idx_out, count_out, out, lse, workspace, workspace_bytes, stream);
+}
+
+dsi_status dsi_indexed_attention_multi(const void* q_idx, const float* w, const void* q,
+                                       const dsi_cache* cache, int32_t tokens_per_seq,
+                                       int32_t n_heads_idx, int32_t n_heads, int32_t K,
+                                       float scale, int32_t* idx_out, int32_t* count_out,
+                                       void* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  if (!cache || tokens_per_seq < 1 || cache->batch < 0) return DSI_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)cache->batch * tokens_per_seq;
+  if (rows > 0x7fffffff) return DSI_ERR_INVALID_ARG;
+  return layer_common(q_idx, w, q, cache, (int32_t)rows, n_heads_idx, n_heads, K, 0, scale, 1,
+                      tokens_per_seq, idx_out, count_out, out, lse, workspace, workspace_bytes,
+                      stream);
 }
 
 dsi_status dsi_probe_random_gather(const void* base, int64_t row_pitch, int64_t n_src_rows,

@@ -44,7 +44,7 @@ score_stream(const bf16* __restrict__ q_idx, const float* __restrict__ w, CacheV
   const int r = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane % LPP, grp = lane / LPP;
-  const int b = decode ? r : 0;
+  const int b = seq_of_row(c, r, decode);
   const int64_t n = visible_len(c, r, decode, q_offset);
 
   float qr[HI][EPC];
@@ -110,7 +110,7 @@ score_simt(const bf16* __restrict__ q_idx, const float* __restrict__ w, CacheVie
   float* ws = qs + H * c.d;                       // [H]
   const int D = c.d;
   const int r = blockIdx.y;
-  const int b = decode ? r : 0;
+  const int b = seq_of_row(c, r, decode);
   const int64_t n = visible_len(c, r, decode, q_offset);
   for (int i = threadIdx.x; i < H * D; i += blockDim.x)
     qs[i] = KeyTraits<KT>::query(__bfloat162float(q_idx[(int64_t)r * H * D + i]));

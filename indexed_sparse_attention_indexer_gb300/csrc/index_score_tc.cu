@@ -259,7 +259,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if (lane == 0) {
-        const int b = a.decode ? g : 0;
+        const int b = seq_of_row(c, g, a.decode);
         int64_t nvis;
         if (a.decode) nvis = visible_len(c, g, 1, 0);
         else nvis = a.q_offset + min(a.rows, (g + 1) * NT);
@@ -379,7 +379,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&acc_empty[abuf]);
-      const int b = a.decode ? g : 0;
+      const int b = seq_of_row(c, g, a.decode);
       const int64_t p = (int64_t)j * kTileM + row;
 #pragma unroll
       for (int tt = 0; tt < TPT; ++tt) {

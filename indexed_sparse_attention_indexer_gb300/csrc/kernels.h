@@ -57,9 +57,12 @@ cudaError_t launch_index_topk_prefill(const bf16* q_idx, const float* w, const C
                                       int32_t* count, int* err, cudaStream_t st);
 
 // ---- Top-K -------------------------------------------------------------------
+// row_len: candidates per row, or per sequence when tokens_per_seq > 1 (row r
+// is token r % T of sequence r / T and has row_len[r / T] - (T - 1 - r % T));
+// null: the causal prefill rule q_offset + r + 1.
 cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t* row_len,
                         int64_t q_offset, int K, int32_t* idx, int32_t* count,
-                        cudaStream_t st);
+                        cudaStream_t st, int tokens_per_seq = 1);
 
 // ---- sparse MLA ----------------------------------------------------------------
 // part_o / part_ml: split-K partials (may be null when splits == 1).

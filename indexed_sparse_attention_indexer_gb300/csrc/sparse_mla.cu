@@ -51,7 +51,7 @@ mla_simt(const bf16* __restrict__ q, CacheView c, const int32_t* __restrict__ id
   MlaSmem& S = *reinterpret_cast<MlaSmem*>(mla_smem_raw);
   const int g = blockIdx.x, r = blockIdx.y, sp = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = decode ? r : 0;
+  const int b = seq_of_row(c, r, decode);
   const int64_t n_vis = visible_len(c, r, decode, q_offset);
   const int hcount = H - g * kHB < kHB ? H - g * kHB : kHB;  // heads of this block
   const int per = (K + splits - 1) / splits;

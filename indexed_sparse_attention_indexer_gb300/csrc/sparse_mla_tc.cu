@@ -142,7 +142,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   const uint32_t peer = rho ^ 1u;
   const int pair = blockIdx.x >> 1;
   const int r = pair / a.splits, sp = pair % a.splits;
-  const int b = a.decode ? r : 0;
+  const int b = seq_of_row(c, r, a.decode);
   const int64_t n_vis = visible_len(c, r, a.decode, a.q_offset);
   const int tiles_all = (a.K + kNp - 1) / kNp;
   const int tiles_per = (tiles_all + a.splits - 1) / a.splits;

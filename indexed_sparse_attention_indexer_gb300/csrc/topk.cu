@@ -40,7 +40,7 @@ __device__ __forceinline__ uint32_t load_key(const uint32_t* skeys, const float*
 __global__ void __launch_bounds__(kTopkThreads)
 topk_rows(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
           int64_t q_offset, int K, int32_t* __restrict__ idx, int32_t* __restrict__ count,
-          int stage) {
+          int stage, int tps) {
   extern __shared__ uint32_t topk_smem[];
   __shared__ int hist[256];
   __shared__ int scan_ws[40];
@@ -48,7 +48,9 @@ topk_rows(const float* __restrict__ scores, int64_t ld, const int32_t* __restric
   __shared__ int s_krem;
   const int r = blockIdx.x;
   const int tid = threadIdx.x;
-  int64_t n = row_len ? (int64_t)row_len[r] : q_offset + r + 1;
+  int64_t n = !row_len ? q_offset + r + 1
+              : tps == 1 ? (int64_t)row_len[r]
+                         : (int64_t)row_len[r / tps] - (tps - 1 - r % tps);
   if (n < 0) n = 0;
   if (n > ld) n = ld;
   int32_t* out = idx + (int64_t)r * K;
@@ -166,7 +168,8 @@ __device__ __forceinline__ void load_chunk(uint32_t* key, const float* grow, int
 template <bool kChunked>
 __global__ void __launch_bounds__(kTopkThreads, 1)
 topk_rows_reg(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
-              int64_t q_offset, int K, int32_t* __restrict__ idx, int32_t* __restrict__ count) {
+              int64_t q_offset, int K, int32_t* __restrict__ idx, int32_t* __restrict__ count,
+              int tps) {
   __shared__ int hist[2][kBins];          // alternate passes; each is cleared as it is read
   __shared__ int wsum[2][kWarps];
   __shared__ int wbase[2][kWarps];
@@ -179,7 +182,9 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, const int32_t* __res
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const unsigned kAll = 0xffffffffu;
   const unsigned lt_mask = (1u << lane) - 1u;
-  int64_t n = row_len ? (int64_t)row_len[r] : q_offset + r + 1;
+  int64_t n = !row_len ? q_offset + r + 1
+              : tps == 1 ? (int64_t)row_len[r]
+                         : (int64_t)row_len[r / tps] - (tps - 1 - r % tps);
   if (n < 0) n = 0;
   if (n > ld) n = ld;
   int32_t* out = idx + (int64_t)r * K;
@@ -348,16 +353,17 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, const int32_t* __res
 }
 
 cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t* row_len,
-                        int64_t q_offset, int K, int32_t* idx, int32_t* count, cudaStream_t st) {
+                        int64_t q_offset, int K, int32_t* idx, int32_t* count, cudaStream_t st,
+                        int tps) {
   if (rows <= 0) return cudaSuccess;
   const int64_t longest = row_len ? ld : (q_offset + rows < ld ? q_offset + rows : ld);
   if (longest <= kRegChunks * kRegKeysMax) {
     cudaError_t e =
         longest <= kRegKeysMax
             ? launch_overlapped(topk_rows_reg<false>, dim3(rows), dim3(kTopkThreads), 0, st, scores,
-                                ld, row_len, q_offset, K, idx, count)
+                                ld, row_len, q_offset, K, idx, count, tps)
             : launch_overlapped(topk_rows_reg<true>, dim3(rows), dim3(kTopkThreads), 0, st, scores,
-                                ld, row_len, q_offset, K, idx, count);
+                                ld, row_len, q_offset, K, idx, count, tps);
     note_launch();
     return e;
   }
@@ -369,7 +375,8 @@ cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  topk_rows<<<rows, kTopkThreads, smem, st>>>(scores, ld, row_len, q_offset, K, idx, count, stage);
+  topk_rows<<<rows, kTopkThreads, smem, st>>>(scores, ld, row_len, q_offset, K, idx, count, stage,
+                                                tps);
   note_launch();
   return cudaGetLastError();
 }

@@ -83,6 +83,11 @@ class Workload:
         return int(self.seq_lens.shape[0])
 
     @property
+    def tokens_per_seq(self) -> int:
+        """Decode query rows per sequence (1, or T for a multi-token step)."""
+        return int(self.meta.get("tokens_per_seq", 1))
+
+    @property
     def paged(self) -> bool:
         return self.block_table is not None
 
@@ -176,13 +181,17 @@ def make_decode(B: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
                 device="cpu", lengths: Optional[Sequence[int]] = None,
                 loguniform: Optional[tuple] = None, page_size: int = 0,
                 k_fp8: bool = False, scale: Optional[float] = None,
-                q_std: Optional[float] = None, name: str = "decode") -> Workload:
-    """Decode batch: one query token per sequence.
+                q_std: Optional[float] = None, name: str = "decode",
+                tokens_per_seq: int = 1) -> Workload:
+    """Decode batch: one query token per sequence, or ``tokens_per_seq`` (T)
+    candidate tokens per sequence for a multi-token step (query rows come T to
+    a sequence; the candidates' keys are the last T positions of its history).
 
     ``S`` is the history length of every sequence unless ``lengths`` gives them
     or ``loguniform=(lo, hi)`` draws them.  ``page_size > 0`` stores the caches
     as page pools behind a randomly permuted block table.
     """
+    R = B * tokens_per_seq
     g = _gen(seed, device)
     if loguniform is not None:
         L = loguniform_lengths(B, loguniform[0], loguniform[1], g, device).cpu()
@@ -199,12 +208,12 @@ def make_decode(B: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
         s_max = max(1, int(L.max()) if L.numel() else 1)
         rows_shape = (B, s_max)
     kdt = torch.float8_e4m3fn if k_fp8 else torch.bfloat16
-    q_idx = _int_values((B, H_i, d), g, device)
+    q_idx = _int_values((R, H_i, d), g, device)
     k_idx = _int_values(rows_shape + (d,), g, device, kdt)
     k_scale = _pow2_scales(rows_shape, g, device) if k_fp8 else None
-    w = _weights((B, H_i), g, device)
+    w = _weights((R, H_i), g, device)
     std = (1.0 / math.sqrt(D_QK)) if q_std is None else q_std
-    q = _normal_bf16((B, H, D_QK), g, device, std)
+    q = _normal_bf16((R, H, D_QK), g, device, std)
     latent = _normal_bf16(rows_shape + (D_QK,), g, device)
     block_table = None
     if page_size > 0:
@@ -219,7 +228,8 @@ def make_decode(B: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
     return Workload(name=name, mode="decode", H_i=H_i, d=d, K=K, H=H,
                     scale=(1.0 / math.sqrt(D_QK)) if scale is None else scale,
                     q_idx=q_idx, w=w, q=q, k_idx=k_idx, k_scale=k_scale, latent=latent,
-                    seq_lens=L.to(device), block_table=block_table, page_size=page_size)
+                    seq_lens=L.to(device), block_table=block_table, page_size=page_size,
+                    meta={"tokens_per_seq": tokens_per_seq} if tokens_per_seq != 1 else {})
 
 
 def make_prefill(T: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
@@ -290,15 +300,17 @@ CONFIGS = {
 }
 
 
-def make_config(cfg: int, device="cpu", chunk: int = 0, rows: int | None = None) -> Workload:
+def make_config(cfg: int, device="cpu", chunk: int = 0, rows: int | None = None,
+                tokens_per_seq: int = 1) -> Workload:
     """The named workload; ``rows`` shrinks a decode batch (same shapes per
-    sequence, fewer sequences) for profiling captures that must stay small."""
+    sequence, fewer sequences) for profiling captures that must stay small;
+    ``tokens_per_seq`` turns a decode workload into a multi-token step."""
     c = CONFIGS[cfg]
-    if rows is not None and cfg not in (1, 2, 5):
-        raise ValueError("rows applies to the decode workloads only")
+    if (rows is not None or tokens_per_seq != 1) and cfg not in (1, 2, 5):
+        raise ValueError("rows and tokens_per_seq apply to the decode workloads only")
     if cfg in (1, 2):
         return make_decode(rows or c["B"], c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
-                           device=device, name=c["name"])
+                           device=device, name=c["name"], tokens_per_seq=tokens_per_seq)
     if cfg == 3:
         return make_prefill(c["T"], c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
                             device=device, name=c["name"])
@@ -309,5 +321,6 @@ def make_config(cfg: int, device="cpu", chunk: int = 0, rows: int | None = None)
     if cfg == 5:
         return make_decode(rows or c["B"], 0, c["H_i"], c["d"], c["K"], c["H"], c["seed"],
                            device=device, loguniform=(c["lo"], c["hi"]),
-                           page_size=c["page_size"], k_fp8=True, name=c["name"])
+                           page_size=c["page_size"], k_fp8=True, name=c["name"],
+                           tokens_per_seq=tokens_per_seq)
     raise ValueError(cfg)

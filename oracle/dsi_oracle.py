@@ -200,6 +200,28 @@ def decode_row(ws, b: int):
                      lambda p: history_rows(lat, b, p, bt, ws.page_size), L, ws.K, ws.scale)
 
 
+def multi_token_row(ws, r: int, tokens_per_seq: int):
+    """Row r of a multi-token decode step (speculative verification, "Day 0
+    Inference Acceleration for New LLM Architectures: Hybrid Attention Adaptation
+    and Optimization Practices" §6): candidate t = r % T of sequence b = r // T.
+    The T candidates' keys are the last T positions of the sequence's history;
+    candidate t sees its own position and everything before it, i.e. the first
+    seq_lens[b] - (T - 1 - t) positions, and runs the same index selection and
+    attention as a single decode token."""
+    T = int(tokens_per_seq)
+    b, t = divmod(int(r), T)
+    L = max(0, int(ws.seq_lens[b]) - (T - 1 - t))
+    pos = np.arange(L)
+    bt = ws.block_table.cpu() if ws.block_table is not None else None
+    k_hist = history_rows(ws.k_idx.cpu(), b, pos, bt, ws.page_size)
+    ks = None
+    if ws.k_scale is not None:
+        ks = history_rows(ws.k_scale.cpu(), b, pos, bt, ws.page_size)
+    lat = ws.latent.cpu()
+    return layer_row(ws.q_idx[r].cpu(), ws.w[r].cpu(), ws.q[r].cpu(), k_hist, ks,
+                     lambda p: history_rows(lat, b, p, bt, ws.page_size), L, ws.K, ws.scale)
+
+
 def prefill_row(ws, t: int):
     """Query token t (position q_offset+t) of a causal prefill of one sequence."""
     n = ws.q_offset + t + 1

@@ -131,6 +131,28 @@ def test_index_topk_prefill_validation(L):
     assert _itp(L, _cache(**one), T=0) == binding.DSI_OK
 
 
+def test_indexed_attention_multi_validation(L):
+    """Host checks of the multi-token decode entry (rows = batch x T)."""
+    E = binding.DSI_ERR_INVALID_ARG
+    M = L.dsi_indexed_attention_multi
+    c = _cache(batch=4)
+    args = lambda **kw: dict(dict(q_idx=FAKE, w=FAKE, q=FAKE, T=2, Hi=64, H=128, K=16, out=FAKE,
+                                  ws=FAKE, wsb=1 << 30), **kw)
+    def call(cache, **kw):
+        a = args(**kw)
+        return M(a["q_idx"], a["w"], a["q"], ctypes.byref(cache), a["T"], a["Hi"], a["H"], a["K"],
+                 0.04, None, None, a["out"], None, a["ws"], a["wsb"], None)
+    assert M(FAKE, FAKE, FAKE, None, 2, 64, 128, 16, 0.04, None, None, FAKE, None, FAKE, 1 << 30,
+             None) == E
+    assert call(c, T=0) == E
+    assert call(c, q_idx=None) == E
+    assert call(c, out=None) == E
+    assert call(c, K=0) == E
+    assert call(_cache(batch=4, seq_lens=None)) == E
+    assert call(c, ws=None) == binding.DSI_ERR_WORKSPACE
+    assert call(_cache(batch=0)) == binding.DSI_OK     # no rows: nothing to launch
+
+
 def test_probe_gather_validation(L):
     E = binding.DSI_ERR_INVALID_ARG
     P = L.dsi_probe_random_gather

@@ -222,6 +222,38 @@ def test_topk_ties_and_lengths(case):
         assert int(count[r]) == cnt
 
 
+MULTI_CASES = {
+    # name: (lengths, T, H_i, d, K, H, page_size, fp8)
+    "contig_hi64_t2": ([300, 64, 130], 2, 64, 128, 64, 128, 0, False),
+    "paged_fp8_t4": ([1000, 200], 4, 64, 128, 128, 128, 64, True),
+    "small_heads_t3": ([50, 7, 90], 3, 4, 64, 16, 16, 0, False),
+    "shorter_than_t": ([1, 40], 2, 64, 128, 8, 128, 0, False),   # candidate 0 of seq 0 sees nothing
+}
+
+
+@pytest.mark.parametrize("name", sorted(MULTI_CASES))
+def test_multi_token_decode(name):
+    """Speculative verification: T candidate rows per sequence, each causal over the
+    history and the earlier candidates, through dsi_indexed_attention_multi."""
+    lengths, T, Hi, d, K, H, page, fp8 = MULTI_CASES[name]
+    ws = W.make_decode(len(lengths), 0, Hi, d, K, H, seed=23, lengths=lengths, page_size=page,
+                       k_fp8=fp8, tokens_per_seq=T)
+    g = ws.to(DEV)
+    out, lse, idx, count = binding.indexed_attention_multi(g.q_idx, g.w, g.q, binding.Cache.of(g),
+                                                           T, K, ws.scale)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    for r in range(ws.T):
+        ref = oracle.multi_token_row(ws, r, T)
+        assert np.array_equal(idx[r].cpu().numpy(), ref["idx"]), f"row {r}"
+        assert int(count[r]) == ref["count"]
+        if ref["count"] == 0:
+            assert torch.all(out[r] == 0) and torch.all(torch.isinf(lse[r]))
+            continue
+        assert_out_close(out[r].float().cpu().numpy(), ref["out"], f"{name} row {r}")
+        assert_lse_close(lse[r].cpu().numpy(), ref["lse"], f"{name} row {r}")
+
+
 def test_topk_wide_key_range_and_constant_rows():
     """Scores spread over many binades (and signs), plus rows that are constant or
     hold one distinct value above a constant floor."""

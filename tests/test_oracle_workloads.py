@@ -83,3 +83,30 @@ def test_decode_row_short_history_takes_all():
     assert r["count"] == 5 and list(r["idx"][:6]) == [0, 1, 2, 3, 4, -1]
     r = oracle.decode_row(ws, 1)
     assert r["count"] == 32
+
+
+def test_multi_token_rows_reduce_to_decode_rows():
+    """A multi-token step: T = 1 is a decode row; the last candidate sees the whole
+    history (a decode row of the full length); candidate t of a sequence of length L
+    equals a one-token decode of the same query over a history of L - (T-1-t) rows."""
+    T = 3
+    ws = W.make_decode(2, 0, 4, 16, 8, 2, seed=12, lengths=[20, 9], tokens_per_seq=T)
+    assert ws.T == 2 * T and ws.tokens_per_seq == T
+    one = W.make_decode(2, 0, 4, 16, 8, 2, seed=12, lengths=[20, 9])
+    assert np.array_equal(oracle.multi_token_row(one, 1, 1)["out"], oracle.decode_row(one, 1)["out"])
+    for r in range(ws.T):
+        b, t = divmod(r, T)
+        got = oracle.multi_token_row(ws, r, T)
+        # the same query on a workload whose sequence b is cut to L - (T-1-t) rows
+        cut = ws.to("cpu")
+        cut.q_idx, cut.w, cut.q = ws.q_idx[r:r + 1].repeat(2, 1, 1), ws.w[r:r + 1].repeat(2, 1), \
+            ws.q[r:r + 1].repeat(2, 1, 1)
+        lens = ws.seq_lens.clone()
+        lens[b] = int(ws.seq_lens[b]) - (T - 1 - t)
+        cut.seq_lens = lens
+        ref = oracle.decode_row(cut, b)
+        assert np.array_equal(got["idx"], ref["idx"]) and got["count"] == ref["count"]
+        assert np.array_equal(got["out"], ref["out"])
+        # causality: no candidate sees a later candidate's key
+        sel = got["idx"][:got["count"]]
+        assert sel.size == 0 or sel.max() <= int(ws.seq_lens[b]) - (T - t)
