@@ -58,8 +58,12 @@ def algorithmic_bytes(ws) -> dict:
     else:
         vis = torch.arange(1, B + 1, dtype=torch.int64) + ws.q_offset
     kel = ws.k_idx.element_size()
-    key = int(vis.sum()) * ws.d * kel
-    scale = int(vis.sum()) * 4 if ws.k_scale is not None else 0
+    # index keys are read once per sequence: the candidate rows of a
+    # multi-token step see nested prefixes of one history (the longest is the
+    # sequence's length); every other row reads its own
+    kv = torch.clamp(lens, max=ws.s_max) if (ws.mode == "decode" and ws.tokens_per_seq > 1) else vis
+    key = int(kv.sum()) * ws.d * kel
+    scale = int(kv.sum()) * 4 if ws.k_scale is not None else 0
     sel = torch.clamp(vis, max=ws.K)
     gather = int(sel.sum()) * W.D_QK * 2
     q_bytes = ws.q_idx.numel() * 2 + ws.w.numel() * 4 + ws.q.numel() * 2

@@ -159,7 +159,7 @@ cudaError_t launch_index_score_tc(const bf16* q_idx, const float* w, const Cache
                                   int rows, int decode, int64_t q_offset, float* scores,
                                   int64_t ld, int* err, cudaStream_t st);
 bool tc_score_supported(const CacheView& c, int n_heads_idx);
-bool tc_score_shape_ok(int rows, int decode);
+bool tc_score_shape_ok(const CacheView& c, int rows, int decode);
 
 ScoreKernel pick_score_kernel(const CacheView& c, int H) {
   if (tc_score_supported(c, H)) return kScoreTc;
@@ -230,7 +230,7 @@ cudaError_t launch_index_score(const bf16* q_idx, const float* w, const CacheVie
                                int* err, cudaStream_t st) {
   const bool fp8 = c.k_dtype == DSI_FP8_E4M3;
   ScoreKernel k = pick_score_kernel(c, H);
-  if (k == kScoreTc && !tc_score_shape_ok(rows, decode)) k = kScoreSimt;
+  if (k == kScoreTc && !tc_score_shape_ok(c, rows, decode)) k = kScoreSimt;
   switch (k) {
     case kScoreTc:
       return launch_index_score_tc(q_idx, w, c, rows, decode, q_offset, scores, ld, err, st);

@@ -73,17 +73,18 @@ struct ScoreArgs {
   int decode;
 };
 
-// Tiles of group g (decode: sequence g; prefill: tokens g*NT .. g*NT+NT-1).
+// Group g holds query rows g*NT .. g*NT+NT-1: NT tokens of the prefill, or
+// (decode) the NT candidate rows of one sequence, which share its key tiles.
+// The group's last row sees the most history.
+template <int NT>
+__device__ __forceinline__ int64_t group_visible(const CacheView& c, const ScoreArgs& a, int g) {
+  const int last = min(a.rows, (g + 1) * NT) - 1;
+  return a.decode ? visible_len(c, last, 1, 0) : a.q_offset + last + 1;
+}
+
 template <int NT>
 __device__ __forceinline__ int group_tiles(const CacheView& c, const ScoreArgs& a, int g) {
-  int64_t n;
-  if (a.decode) {
-    n = visible_len(c, g, 1, 0);
-  } else {
-    const int last = min(a.rows, (g + 1) * NT) - 1;
-    n = a.q_offset + last + 1;
-  }
-  return (int)((n + kTileM - 1) / kTileM);
+  return (int)((group_visible<NT>(c, a, g) + kTileM - 1) / kTileM);
 }
 
 // Walks the CTA's contiguous range of (group, tile) items.
@@ -211,7 +212,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
           for (int i = lane; i < C::N * 8; i += 32) {
             const int n = i >> 3, u = i & 7;
             const int t = n / kHeads, h = n % kHeads;
-            const int r = a.decode ? g : g * NT + t;
+            const int r = g * NT + t;
             uint4 outv = make_uint4(0, 0, 0, 0);
             if (r < a.rows) {
               const bf16* src = a.q_idx + ((int64_t)r * kHeads + h) * kD + u * 16;
@@ -242,7 +243,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
           mbar_arrive_expect_tx(&q_full[slot], C::B_BYTES);
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            const int r = a.decode ? g : g * NT + t;   // rows past the end read as zeros
+            const int r = g * NT + t;   // rows past the end read as zeros
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc)
               tma_load_2d(qs + cc * (C::N * 128) + t * kHeads * 128, &qmap, cc * 64, r * kHeads,
@@ -259,10 +260,8 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if (lane == 0) {
-        const int b = seq_of_row(c, g, a.decode);
-        int64_t nvis;
-        if (a.decode) nvis = visible_len(c, g, 1, 0);
-        else nvis = a.q_offset + min(a.rows, (g + 1) * NT);
+        const int b = seq_of_row(c, g * NT, a.decode);
+        const int64_t nvis = group_visible<NT>(c, a, g);
         const int64_t p0 = (int64_t)j * kTileM;
         int64_t prow[2];
         int nsub = 0;
@@ -359,7 +358,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         __syncwarp();
         for (int i = lane; i < TPT * kHeads; i += 32) {
           const int t = half * TPT + i / kHeads, h = i % kHeads;
-          const int r = a.decode ? g : g * NT + t;
+          const int r = g * NT + t;
           wg[i] = r < a.rows ? __ldg(a.w + (int64_t)r * kHeads + h) : 0.f;
         }
         __syncwarp();
@@ -379,14 +378,14 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&acc_empty[abuf]);
-      const int b = seq_of_row(c, g, a.decode);
+      const int b = seq_of_row(c, g * NT, a.decode);
       const int64_t p = (int64_t)j * kTileM + row;
 #pragma unroll
       for (int tt = 0; tt < TPT; ++tt) {
         const int t = half * TPT + tt;
-        const int r = a.decode ? g : g * NT + t;
+        const int r = g * NT + t;
         if (r >= a.rows) continue;
-        const int64_t nvis = a.decode ? visible_len(c, g, 1, 0) : a.q_offset + r + 1;
+        const int64_t nvis = a.decode ? visible_len(c, r, 1, 0) : a.q_offset + r + 1;
         if (p >= nvis) continue;
         const float* wt = wg + tt * kHeads;
         float s0 = 0.f, s1 = 0.f;
@@ -439,7 +438,7 @@ cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, 
   a.q_offset = q_offset;
   a.rows = rows;
   a.decode = decode;
-  a.groups = decode ? rows : (rows + NT - 1) / NT;
+  a.groups = (rows + NT - 1) / NT;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -464,8 +463,17 @@ bool tc_score_supported(const CacheView& c, int H) {
   return tma_encode_fn() != nullptr;
 }
 
-bool tc_score_shape_ok(int rows, int decode) {
-  const int groups = decode ? rows : (rows + 3) / 4;
+// Query rows per group: prefill 4 tokens; decode one row, or the 2 or 4
+// candidate rows of a sequence in a multi-token step (they share its keys,
+// which are then read once for all of them).
+static int tokens_per_group(const CacheView& c, int decode) {
+  if (!decode) return 4;
+  return (c.tokens_per_seq == 2 || c.tokens_per_seq == 4) ? c.tokens_per_seq : 1;
+}
+
+bool tc_score_shape_ok(const CacheView& c, int rows, int decode) {
+  const int nt = tokens_per_group(c, decode);
+  const int groups = (rows + nt - 1) / nt;
   return groups <= kMaxGroups && (int64_t)rows * kHeads < (1ll << 31);
 }
 
@@ -474,8 +482,17 @@ cudaError_t launch_index_score_tc(const bf16* q_idx, const float* w, const Cache
                                   int* err, cudaStream_t st) {
   const bool fp8 = c.k_dtype == DSI_FP8_E4M3;
   if (decode) {
-    return fp8 ? go<1, true>(q_idx, w, c, rows, 1, 0, scores, ld, err, st)
-               : go<1, false>(q_idx, w, c, rows, 1, 0, scores, ld, err, st);
+    switch (tokens_per_group(c, decode)) {
+      case 4:
+        return fp8 ? go<4, true>(q_idx, w, c, rows, 1, 0, scores, ld, err, st)
+                   : go<4, false>(q_idx, w, c, rows, 1, 0, scores, ld, err, st);
+      case 2:
+        return fp8 ? go<2, true>(q_idx, w, c, rows, 1, 0, scores, ld, err, st)
+                   : go<2, false>(q_idx, w, c, rows, 1, 0, scores, ld, err, st);
+      default:
+        return fp8 ? go<1, true>(q_idx, w, c, rows, 1, 0, scores, ld, err, st)
+                   : go<1, false>(q_idx, w, c, rows, 1, 0, scores, ld, err, st);
+    }
   }
   return fp8 ? go<4, true>(q_idx, w, c, rows, 0, q_offset, scores, ld, err, st)
              : go<4, false>(q_idx, w, c, rows, 0, q_offset, scores, ld, err, st);
