@@ -551,6 +551,42 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_crossover():
+    """Dense versus sparse attention for a decode batch as the history grows:
+    the sparse layer (indexer + Top-K 2048 + attention over 2048 rows) against
+    attention over every history row (the same attention kernel given all
+    positions, K = S, up to the library's 4096-entry limit).  64 sequences,
+    64x128 indexer heads, 128 MLA heads, inputs resident."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from indexed_sparse_attention_indexer_gb300 import binding
+    binding.load()
+    stream = torch.cuda.current_stream()
+    B, K = 64, 2048
+    res = []
+    for S in (1024, 2048, 2560, 3072, 3584, 4096):
+        ws = W.make_decode(B, S, 64, 128, K, 128, seed=0, device=dev, name="crossover")
+        cache = binding.Cache.of(ws)
+        wsp = binding.alloc_workspace(binding.workspace_size(B, 64, 128, K, S, True), dev)
+        out = torch.empty((B, 128, W.D_LATENT), dtype=torch.bfloat16, device=dev)
+        sparse_ms = time_alone(lambda: binding.indexed_attention(
+            ws.q_idx, ws.w, ws.q, cache, K, ws.scale, True, 0, out=out, workspace=wsp,
+            want_lse=False, want_idx=False, stream=stream), stream, 20)
+        every = torch.arange(S, dtype=torch.int32, device=dev).repeat(B, 1)
+        wsd = binding.alloc_workspace(binding.workspace_size(B, 0, 128, S, 0, True), dev)
+        dense_ms = time_alone(lambda: binding.sparse_mla_decode(
+            ws.q, cache, every, ws.scale, out=out, want_lse=False, workspace=wsd,
+            stream=stream), stream, 20)
+        res.append({"history": S, "sparse_ms": round(sparse_ms, 4), "dense_ms": round(dense_ms, 4),
+                    "sparse_over_dense": round(sparse_ms / dense_ms, 3)})
+        del ws, cache, wsp, wsd, every
+        torch.cuda.empty_cache()
+    cross = next((r["history"] for r in res if r["sparse_ms"] < r["dense_ms"]), None)
+    print(json.dumps({"probe": "dense_vs_sparse_decode", "batch": B, "topk": K,
+                      "indexer": "64x128", "mla_heads": 128, "results": res,
+                      "first_history_where_sparse_wins": cross}))
+
+
 def run_gather_ceiling():
     """Plain-load bandwidth of the attention core's access pattern: 2048 random
     distinct rows of each of 64 sequences x 32768 rows x 1152 bytes (the decode
@@ -594,6 +630,8 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--crossover", action="store_true",
+                    help="measurement: dense vs sparse attention as the history grows (not a bench line)")
     ap.add_argument("--gather-ceiling", action="store_true",
                     help="diagnostic: random-row gather bandwidth of plain loads (not a bench line)")
     ap.add_argument("--tokens-per-seq", type=int, default=1,
@@ -604,6 +642,9 @@ def main():
     args = ap.parse_args()
     if args.gather_ceiling:
         run_gather_ceiling()
+        return
+    if args.crossover:
+        run_crossover()
         return
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
