@@ -197,7 +197,8 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
 #pragma unroll
     for (int s = 0; s < C::STAGES; ++s) { issued[s] = false; issued_phase[s] = 0; }
     if (lane == 0) { prefetch_tmap(&kmap); if (!FP8) prefetch_tmap(&qmap); }
-    while (it.valid() && !*abort_flag) {
+    // lane 0's reading of the flag decides for the warp, so all lanes leave together
+    while (it.valid() && !__shfl_sync(0xffffffffu, (int)*abort_flag, 0)) {
       const int g = it.g, j = it.j;
       if (g != gprev) {
         const int slot = qcount & 1;
