@@ -14,6 +14,16 @@ measured on):
   integers exactly, with one positive power-of-two scale 2^e, e in {-4..0}, per
   token).  Every dot product of two such vectors is an exact small integer, so
   fp32 scores are exact in any summation order.
+* MXFP8 index keys (the microscaled variant): E4M3 codes holding integers
+  from {-3..3} plus one E8M0 scale byte per group of G (32 unless stated)
+  elements, drawn uniformly from {125, 126, 127} (scales 1/4, 1/2, 1).  With
+  integer index queries (whose MXFP8 quantisation is exact) every dot product
+  is a multiple of 1/4 below 2^11 and the weighted head sums stay far below
+  the 2^15 where fp32 would start to round them.
+* inputs of the MXFP8 quantiser: bf16 normal rows with a per-row magnitude
+  exp(U(-8, 8)), four outlier channels x32, and special rows (all zero, bf16
+  subnormals, magnitudes near 2^120, exact powers of two, group maxima with
+  mantissa 1.875 that saturate at 448).
 * head weights ``w``: uniform [0,1) rounded down to a multiple of 2^-7, so that
   every partial sum of ``w_h * relu(u_h)`` is a multiple of 2^-7 below 2^24
   and hence exact in fp32 whatever the order.
@@ -167,6 +177,10 @@ def _pow2_scales(shape, g, device) -> torch.Tensor:
     return torch.pow(torch.tensor(2.0, device=device), -e.to(torch.float32))
 
 
+def _e8m0_bytes(shape, g, device, lo: int = 125, hi: int = 127) -> torch.Tensor:
+    return torch.randint(lo, hi + 1, shape, generator=g, device=device).to(torch.uint8)
+
+
 def loguniform_lengths(B: int, lo: int, hi: int, g, device) -> torch.Tensor:
     u = torch.rand(B, generator=g, device=device, dtype=torch.float64)
     L = torch.floor(torch.exp(math.log(lo) + u * (math.log(hi) - math.log(lo))))
@@ -182,14 +196,16 @@ def make_decode(B: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
                 loguniform: Optional[tuple] = None, page_size: int = 0,
                 k_fp8: bool = False, scale: Optional[float] = None,
                 q_std: Optional[float] = None, name: str = "decode",
-                tokens_per_seq: int = 1) -> Workload:
+                tokens_per_seq: int = 1, k_mx_group: int = 0) -> Workload:
     """Decode batch: one query token per sequence, or ``tokens_per_seq`` (T)
     candidate tokens per sequence for a multi-token step (query rows come T to
     a sequence; the candidates' keys are the last T positions of its history).
 
     ``S`` is the history length of every sequence unless ``lengths`` gives them
     or ``loguniform=(lo, hi)`` draws them.  ``page_size > 0`` stores the caches
-    as page pools behind a randomly permuted block table.
+    as page pools behind a randomly permuted block table.  ``k_mx_group > 0``
+    stores the index keys as MXFP8 (E4M3 codes, one E8M0 byte per group of
+    that many elements in ``k_scale``).
     """
     R = B * tokens_per_seq
     g = _gen(seed, device)
@@ -207,10 +223,14 @@ def make_decode(B: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
     else:
         s_max = max(1, int(L.max()) if L.numel() else 1)
         rows_shape = (B, s_max)
-    kdt = torch.float8_e4m3fn if k_fp8 else torch.bfloat16
+    kdt = torch.float8_e4m3fn if (k_fp8 or k_mx_group) else torch.bfloat16
     q_idx = _int_values((R, H_i, d), g, device)
     k_idx = _int_values(rows_shape + (d,), g, device, kdt)
-    k_scale = _pow2_scales(rows_shape, g, device) if k_fp8 else None
+    if k_mx_group:
+        assert d % k_mx_group == 0
+        k_scale = _e8m0_bytes(rows_shape + (d // k_mx_group,), g, device)
+    else:
+        k_scale = _pow2_scales(rows_shape, g, device) if k_fp8 else None
     w = _weights((R, H_i), g, device)
     std = (1.0 / math.sqrt(D_QK)) if q_std is None else q_std
     q = _normal_bf16((R, H, D_QK), g, device, std)
@@ -234,22 +254,63 @@ def make_decode(B: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
 
 def make_prefill(T: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
                  device="cpu", q_offset: int = 0, scale: Optional[float] = None,
-                 q_std: Optional[float] = None, name: str = "prefill") -> Workload:
+                 q_std: Optional[float] = None, name: str = "prefill",
+                 k_mx_group: int = 0) -> Workload:
     """Causal prefill of one sequence: query tokens q_offset .. q_offset+T-1
-    against a cache of S >= q_offset+T rows, all from one generator."""
+    against a cache of S >= q_offset+T rows, all from one generator
+    (``k_mx_group``: MXFP8 index keys as in ``make_decode``)."""
     assert S >= q_offset + T
     g = _gen(seed, device)
     q_idx = _int_values((T, H_i, d), g, device)
-    k_idx = _int_values((1, S, d), g, device)
+    k_idx = _int_values((1, S, d), g, device,
+                        torch.float8_e4m3fn if k_mx_group else torch.bfloat16)
+    k_scale = _e8m0_bytes((1, S, d // k_mx_group), g, device) if k_mx_group else None
     w = _weights((T, H_i), g, device)
     std = (1.0 / math.sqrt(D_QK)) if q_std is None else q_std
     q = _normal_bf16((T, H, D_QK), g, device, std)
     latent = _normal_bf16((1, S, D_QK), g, device)
     return Workload(name=name, mode="prefill", H_i=H_i, d=d, K=K, H=H,
                     scale=(1.0 / math.sqrt(D_QK)) if scale is None else scale,
-                    q_idx=q_idx, w=w, q=q, k_idx=k_idx, k_scale=None, latent=latent,
+                    q_idx=q_idx, w=w, q=q, k_idx=k_idx, k_scale=k_scale, latent=latent,
                     seq_lens=torch.tensor([S], dtype=torch.int32, device=device),
                     q_offset=q_offset)
+
+
+def make_mx_input(n: int, d: int, seed: int = 0, device="cpu", special: bool = True,
+                  row_spread: float = 8.0) -> torch.Tensor:
+    """bf16 rows [n, d] for the MXFP8 quantiser: normal values with a per-row
+    magnitude exp(U(-row_spread, row_spread)) and four outlier channels x32;
+    with ``special`` and n >= 8 the first rows are special: all zero, bf16
+    subnormals, magnitudes near 2^120, exact powers of two, and groups whose
+    largest magnitude has mantissa 1.875 (they saturate at 448 after scaling)."""
+    g = _gen(seed, device)
+    x = torch.empty((n, d), device=device, dtype=torch.bfloat16)
+    mag = torch.exp(torch.empty((n, 1), device=device).uniform_(-row_spread, row_spread,
+                                                                 generator=g))
+    ch = torch.randperm(d, generator=g, device=device)[:4]
+    boost = torch.ones(d, device=device)
+    boost[ch] = 32.0
+    step = max(1, _CHUNK // max(1, d))
+    for s in range(0, n, step):
+        e = min(n, s + step)
+        x[s:e] = (torch.randn((e - s, d), generator=g, device=device) * mag[s:e] * boost).to(
+            torch.bfloat16)
+    if not special or n < 8:
+        return x
+    x = x.float()
+    if n >= 8:
+        x[0] = 0.0
+        x[1] = torch.randn(d, generator=g, device=device) * 2.0 ** -130
+        x[2] = torch.randn(d, generator=g, device=device) * 2.0 ** 118
+        e = torch.randint(-20, 20, (d,), generator=g, device=device).to(torch.float32)
+        x[3] = torch.pow(2.0, e) * torch.where(torch.rand(d, generator=g, device=device) < 0.5,
+                                               -1.0, 1.0)
+        x[4] = torch.randn(d, generator=g, device=device)
+        m = x[4, ::16].numel()
+        x[4, ::16] = 1.875 * torch.pow(2.0, torch.randint(-5, 5, (m,), generator=g,
+                                                           device=device).to(torch.float32))
+        x[5] = -x[4]
+    return x.to(torch.bfloat16)
 
 
 CHUNK_STREAM = 1_000_003
@@ -301,16 +362,20 @@ CONFIGS = {
 
 
 def make_config(cfg: int, device="cpu", chunk: int = 0, rows: int | None = None,
-                tokens_per_seq: int = 1) -> Workload:
+                tokens_per_seq: int = 1, k_mx_group: int = 0) -> Workload:
     """The named workload; ``rows`` shrinks a decode batch (same shapes per
     sequence, fewer sequences) for profiling captures that must stay small;
-    ``tokens_per_seq`` turns a decode workload into a multi-token step."""
+    ``tokens_per_seq`` turns a decode workload into a multi-token step;
+    ``k_mx_group`` stores the 64x128-head decode workload's index keys as MXFP8."""
     c = CONFIGS[cfg]
     if (rows is not None or tokens_per_seq != 1) and cfg not in (1, 2, 5):
         raise ValueError("rows and tokens_per_seq apply to the decode workloads only")
+    if k_mx_group and cfg != 2:
+        raise ValueError("MXFP8 keys apply to the 64x128-head contiguous decode workload only")
     if cfg in (1, 2):
         return make_decode(rows or c["B"], c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
-                           device=device, name=c["name"], tokens_per_seq=tokens_per_seq)
+                           device=device, name=c["name"] + ("-mxfp8" if k_mx_group else ""),
+                           tokens_per_seq=tokens_per_seq, k_mx_group=k_mx_group)
     if cfg == 3:
         return make_prefill(c["T"], c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
                             device=device, name=c["name"])

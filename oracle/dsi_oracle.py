@@ -28,6 +28,9 @@ Readings where the pages are silent (each also listed in the design notes):
   element (key * scale) before the dot product, and the index query takes
   part rounded to E4M3 (the index path quantises both index Q and K, "Day 0
   Inference Support...", "A Layered Strategy").
+* MXFP8 index keys carry one E8M0 scale per group of 32 (or G) elements; the
+  group exponent is floor(log2(amax)) - 8 (the microscaling rule for E4M3),
+  and the index query is quantised the same way before the dot product.
 * Attention core = absorbed MLA: the key of a position is its whole 576-wide
   latent row (512 latent + 64 rope), the value is the first 512 dims; logits
   are ``scale * q . c``, softmax over the selected positions, ``lse`` is the
@@ -41,6 +44,8 @@ selection, torch's scaled_dot_product_attention in fp64).  The pages print no
 worked example, so nothing is pinned to values printed on the pages.
 """
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -69,18 +74,73 @@ def e4m3_round(x) -> np.ndarray:
     return t.to(torch.float8_e4m3fn).to(torch.float64).numpy()
 
 
+# MXFP8 ("Day 0 Inference Support for New LLM Architectures: Optimization
+# Practices", "A Layered Strategy"; "Day 0 Inference Acceleration ...: Hybrid
+# Attention Adaptation and Optimization Practices", quantisation of the index
+# Q/K): every group of G consecutive elements (G = 32 on the pages) shares one
+# power-of-two scale, chosen dynamically from the group's largest magnitude.
+# The reading taken here is the usual microscaling rule: the shared exponent is
+# X = floor(log2(amax)) - emax, emax = 8 being the exponent of E4M3's largest
+# normal (448 = 1.75 * 2**8); X is stored as an E8M0 byte X + 127 and held in
+# [-127, 127]; an all-zero group takes X = -127.  Elements are x / 2**X rounded
+# to the nearest E4M3 value (ties to even), saturating at +-448.
+
+E4M3_EMAX = 8
+E8M0_BIAS = 127
+
+
+def mx_exponent(amax) -> int:
+    """Shared exponent X of one group from its largest magnitude."""
+    a = abs(float(amax))
+    if a == 0.0:
+        return -E8M0_BIAS
+    m, e = math.frexp(a)              # a = m * 2**e with 0.5 <= m < 1: floor(log2 a) = e - 1
+    return int(min(E8M0_BIAS, max(-E8M0_BIAS, e - 1 - E4M3_EMAX)))
+
+
+def mxfp8_quantize(x, group: int = 32):
+    """x [..., d] -> (codes [..., d] as E4M3 values in fp64, X [..., d/group] int64)."""
+    a = _f64(x)
+    d = a.shape[-1]
+    assert d % group == 0
+    blocks = a.reshape(a.shape[:-1] + (d // group, group))
+    amax = np.abs(blocks).max(axis=-1)
+    X = np.vectorize(mx_exponent, otypes=[np.int64])(amax) if amax.size else \
+        np.zeros(amax.shape, dtype=np.int64)
+    codes = e4m3_round(blocks / np.ldexp(1.0, X)[..., None])
+    return codes.reshape(a.shape), X
+
+
+def mxfp8_dequantize(codes, X, group: int = 32) -> np.ndarray:
+    """codes [..., d] (E4M3 values) and X [..., d/group] -> values codes * 2**X."""
+    c = _f64(codes)
+    d = c.shape[-1]
+    blocks = c.reshape(c.shape[:-1] + (d // group, group))
+    return (blocks * np.ldexp(1.0, np.asarray(X, dtype=np.int64))[..., None]).reshape(c.shape)
+
+
 def index_scores(q_idx, w, k_rows, k_scale=None) -> np.ndarray:
     """Indexer score of each given history row for one query token.
 
-    q_idx [H_i, d], w [H_i], k_rows [n, d], k_scale [n] or None -> I [n] fp64:
-        I[s] = sum_h w[h] * max(0, sum_j q_idx[h, j] * k[s, j]),
-    with k = k_rows * k_scale[s] when the keys are quantised (dequantise first).
-    With quantised (FP8) keys the index query takes part in E4M3 as well: the
-    index path quantises both index Q and K.
+    q_idx [H_i, d], w [H_i], k_rows [n, d] -> I [n] fp64:
+        I[s] = sum_h w[h] * max(0, sum_j q[h, j] * k[s, j]),
+    where the keys are dequantised first when they are quantised:
+    * k_scale [n] (FP8, one scale per token): k = k_rows * k_scale[s] and the
+      index query takes part rounded to E4M3 (the index path quantises both
+      index Q and K);
+    * k_scale [n, d/G] of E8M0 bytes (MXFP8, one scale per group of G = d /
+      k_scale.shape[1] elements): k = k_rows * 2**(byte - 127) group by group,
+      and the index query is MXFP8-quantised with the same G and dequantised.
     """
     q = _f64(q_idx)
     k = _f64(k_rows)
-    if k_scale is not None:
+    if k_scale is not None and np.ndim(_f64(k_scale)) == 2:
+        byt = _f64(k_scale)
+        group = k.shape[-1] // byt.shape[-1]
+        qc, qX = mxfp8_quantize(q, group)
+        q = mxfp8_dequantize(qc, qX, group)
+        k = mxfp8_dequantize(k, byt.astype(np.int64) - E8M0_BIAS, group)
+    elif k_scale is not None:
         q = e4m3_round(q)
         k = k * _f64(k_scale)[:, None]
     u = k @ q.T                       # relevance of row s for indexer head h: [n, H_i]
@@ -222,12 +282,22 @@ def multi_token_row(ws, r: int, tokens_per_seq: int):
                      lambda p: history_rows(lat, b, p, bt, ws.page_size), L, ws.K, ws.scale)
 
 
+def _rows_prefix(k_idx, n: int):
+    """The first n key rows of the single prefill sequence (FP8 keys are
+    sliced as raw bytes: not every torch build slices float8 tensors)."""
+    k = k_idx.cpu()
+    if "float8" in str(k.dtype):
+        return k.view(__import__("torch").uint8)[0, :n].view(k.dtype)
+    return k[0, :n]
+
+
 def prefill_row(ws, t: int):
     """Query token t (position q_offset+t) of a causal prefill of one sequence."""
     n = ws.q_offset + t + 1
-    k_hist = ws.k_idx[0, :n].cpu()
+    k_hist = _rows_prefix(ws.k_idx, n)
+    ks = None if ws.k_scale is None else ws.k_scale[0, :n].cpu()
     lat = ws.latent[0].cpu()
-    return layer_row(ws.q_idx[t].cpu(), ws.w[t].cpu(), ws.q[t].cpu(), k_hist, None,
+    return layer_row(ws.q_idx[t].cpu(), ws.w[t].cpu(), ws.q[t].cpu(), k_hist, ks,
                      lambda p: lat[np.asarray(p, dtype=np.int64)] if len(p) else lat[:0],
                      n, ws.K, ws.scale)
 
@@ -243,7 +313,8 @@ def row_scores(ws, r: int) -> np.ndarray:
                                                            ws.page_size)
         return index_scores(ws.q_idx[r].cpu(), ws.w[r].cpu(), k_hist, ks)
     n = ws.q_offset + r + 1
-    return index_scores(ws.q_idx[r].cpu(), ws.w[r].cpu(), ws.k_idx[0, :n].cpu(), None)
+    ks = None if ws.k_scale is None else ws.k_scale[0, :n].cpu()
+    return index_scores(ws.q_idx[r].cpu(), ws.w[r].cpu(), _rows_prefix(ws.k_idx, n), ks)
 
 
 def layer(ws, rows=None):

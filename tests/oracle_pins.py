@@ -125,6 +125,166 @@ def check_scores_fp8_query_rounding(o):
     assert o.index_scores(np.array([[0.1]]), np.array([1.0]), k)[0] == 0.1
 
 
+# ----------------------------------------------------------------------------
+# MXFP8 quantisation (E4M3 elements, one E8M0 power-of-two scale per group)
+# ----------------------------------------------------------------------------
+
+def _e4m3_table():
+    """Every finite E4M3 value, from the bit layout: sign, 4 exponent bits with
+    bias 7, 3 mantissa bits, subnormals at exponent 0, S.1111.111 = NaN.
+    Returns (value as Fraction, mantissa-lsb) pairs, NaN codes left out."""
+    out = []
+    for b in range(256):
+        s, e, m = b >> 7, (b >> 3) & 15, b & 7
+        if e == 15 and m == 7:
+            continue
+        mag = Fraction(m, 8) * Fraction(2) ** -6 if e == 0 else \
+            (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+        out.append((-mag if s else mag, m & 1))
+    return out
+
+
+def _nearest_e4m3(v: Fraction) -> Fraction:
+    """Nearest finite E4M3 value, ties to the even mantissa, saturating at 448."""
+    best = None
+    for val, lsb in _e4m3_table():
+        dist = abs(val - v)
+        key = (dist, lsb)
+        if best is None or key < best[0]:
+            best = (key, val)
+    return best[1]
+
+
+def _floor_log2(a: Fraction) -> int:
+    e = 0
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    while Fraction(2) ** e > a:
+        e -= 1
+    return e
+
+
+def _mx_group_exact(vals, emax=8):
+    """One group by exact rational arithmetic: (X, element values as Fractions)."""
+    fr = [Fraction(float(v)) for v in vals]
+    amax = max(abs(v) for v in fr)
+    X = -127 if amax == 0 else max(-127, min(127, _floor_log2(amax) - emax))
+    return X, [_nearest_e4m3(v / Fraction(2) ** X) for v in fr]
+
+
+def check_mx_e4m3_rounding_table(o):
+    """E4M3 rounding against the code table built from the bit layout: every code,
+    every midpoint between neighbours (ties to even), values past 448 saturate."""
+    vals = sorted({v for v, _ in _e4m3_table()})
+    probes = list(vals)
+    probes += [(a + b) / 2 for a, b in zip(vals, vals[1:])]          # exact midpoints
+    probes += [(3 * a + b) / 4 for a, b in zip(vals, vals[1:])]      # off-midpoint
+    probes += [Fraction(449), Fraction(500), Fraction(-1000), Fraction(1, 2048), Fraction(3, 2048)]
+    # groups of two: the probe beside 256, which pins the group exponent at 0
+    # (|probe| < 512), so the probe itself is rounded on the whole code table
+    x = np.array([[float(p), 256.0] for p in probes])
+    c, X = o.mxfp8_quantize(x, 2)
+    for p, row, xr in zip(probes, c, X):
+        Xe, ce = _mx_group_exact([float(p), 256.0])
+        assert xr[0] == Xe and Fraction(float(row[0])) == ce[0], (p, row, xr)
+
+
+def check_mx_exponent_closed_forms(o):
+    """Shared exponent: amax = 2^k -> k - 8 (largest element codes to 256);
+    amax = 1.75 * 2^k -> 448 exactly; 1.875 * 2^k saturates to 448; all-zero
+    group -> -127 with zero codes; tiny groups clamp at -127."""
+    for k in (-20, -3, 0, 5, 30):
+        g = np.zeros(32); g[3] = 2.0 ** k; g[7] = -(2.0 ** (k - 1))
+        c, X = o.mxfp8_quantize(g.reshape(1, 32), 32)
+        assert X[0, 0] == k - 8 and c[0, 3] == 256 and c[0, 7] == -128, (k, X, c[0, :8])
+        g[3] = 1.75 * 2.0 ** k
+        c, X = o.mxfp8_quantize(g.reshape(1, 32), 32)
+        assert X[0, 0] == k - 8 and c[0, 3] == 448
+        g[3] = 1.875 * 2.0 ** k
+        c, X = o.mxfp8_quantize(g.reshape(1, 32), 32)
+        assert X[0, 0] == k - 8 and c[0, 3] == 448
+    c, X = o.mxfp8_quantize(np.zeros((1, 64)), 32)
+    assert (X == -127).all() and (c == 0).all()
+    c, X = o.mxfp8_quantize(np.full((1, 32), 2.0 ** -140), 32)
+    assert X[0, 0] == -127
+    assert o.mx_exponent(0.0) == -127 and o.mx_exponent(448.0) == 0 and o.mx_exponent(511.9) == 0
+
+
+def check_mx_groups_exact(o):
+    """Random groups (normal data with outliers, several group sizes) against exact
+    rational quantisation of each group: exponents and element values."""
+    rng = _rng(21)
+    for group in (32, 64, 128):
+        x = rng.standard_normal((3, 128)) * np.exp(rng.uniform(-6, 6, size=(3, 1)))
+        x[0, 5] *= 40.0                                  # an outlier channel
+        x[2, :group] = 0.0                               # an all-zero group
+        x = x.astype(np.float32).astype(np.float64)
+        c, X = o.mxfp8_quantize(x, group)
+        for r in range(3):
+            for gi in range(128 // group):
+                seg = x[r, gi * group:(gi + 1) * group]
+                Xe, ce = _mx_group_exact(seg)
+                assert X[r, gi] == Xe, (group, r, gi, X[r, gi], Xe)
+                assert all(Fraction(float(a)) == b for a, b in zip(c[r, gi * group:(gi + 1) * group], ce))
+
+
+def check_mx_roundtrip_and_shift(o):
+    """Groups that are already E4M3 values times 2^X (largest code in [256, 448])
+    quantise to themselves; scaling the input by 2^j shifts every exponent by j
+    and leaves the codes alone; groups do not see each other."""
+    rng = _rng(22)
+    vals = np.array(sorted({float(v) for v, _ in _e4m3_table()}))
+    codes = rng.choice(vals, size=(4, 64))
+    codes[:, 0] = 384.0; codes[:, 32] = -288.0           # group maxima inside [256, 448]
+    X = rng.integers(-20, 20, size=(4, 2))
+    x = o.mxfp8_dequantize(codes, X, 32)
+    c2, X2 = o.mxfp8_quantize(x, 32)
+    assert np.array_equal(c2, codes) and np.array_equal(X2, X)
+    c3, X3 = o.mxfp8_quantize(x * 2.0 ** 7, 32)
+    assert np.array_equal(c3, codes) and np.array_equal(X3, X + 7)
+    y = x.copy(); y[:, 32:] *= 1e6                       # second group only
+    c4, X4 = o.mxfp8_quantize(y, 32)
+    assert np.array_equal(c4[:, :32], codes[:, :32]) and np.array_equal(X4[:, 0], X[:, 0])
+
+
+def check_mx_scores_exact(o):
+    """MXFP8 scores on a tiny case by exact rational arithmetic: the query is
+    quantised group by group, the keys are E4M3 codes times their group scales."""
+    rng = _rng(23)
+    Hi, d, n, group = 2, 64, 5, 32
+    q = (rng.standard_normal((Hi, d)) * 3).astype(np.float32).astype(np.float64)
+    vals = np.array(sorted({float(v) for v, _ in _e4m3_table()}))
+    kc = rng.choice(vals[(vals > -40) & (vals < 40)], size=(n, d))
+    kb = rng.integers(120, 131, size=(n, d // group)).astype(np.uint8)
+    w = _grid_w(rng, Hi)
+    got = o.index_scores(q, w, kc, kb)
+    for s in range(n):
+        tot = Fraction(0)
+        for h in range(Hi):
+            dot = Fraction(0)
+            for gi in range(d // group):
+                Xq, qv = _mx_group_exact(q[h, gi * group:(gi + 1) * group])
+                ks = Fraction(2) ** (int(kb[s, gi]) - 127)
+                for j in range(group):
+                    dot += qv[j] * Fraction(2) ** Xq * Fraction(float(kc[s, gi * group + j])) * ks
+            if dot > 0:
+                tot += Fraction(w[h]) * dot
+        assert abs(Fraction(got[s]) - tot) <= abs(tot) * Fraction(1, 2 ** 50), (s, got[s], float(tot))
+
+
+def check_mx_scores_unit_scales(o):
+    """Integer queries and keys with every group scale 2^0: the MXFP8 score
+    equals the unquantised score (the quantisation is exact there)."""
+    rng = _rng(24)
+    q = _int_mat(rng, (4, 64)); k = _int_mat(rng, (30, 64)); w = _grid_w(rng, 4)
+    kb = np.full((30, 2), 127, dtype=np.uint8)
+    assert np.array_equal(o.index_scores(q, w, k, kb), o.index_scores(q, w, k))
+    # one group's scale doubled -> that group's part of every dot product doubles
+    kb2 = kb.copy(); kb2[:, 1] = 128
+    k2 = k.copy(); k2[:, 32:] *= 2
+    assert np.array_equal(o.index_scores(q, w, k, kb2), o.index_scores(q, w, k2))
+
+
 def _load_golden_indexer():
     cases = []
     path = os.path.join(GOLDEN, "indexer_tiny.txt")

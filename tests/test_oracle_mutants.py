@@ -97,6 +97,56 @@ def _mla_unnormalised(q, rows, scale, d_v=512):
     return e @ c[:, :d_v], l.max(1)
 
 
+def _mx_quantize_with(exponent, rounding=None):
+    """An MXFP8 quantiser with a planted change in the exponent rule or rounding."""
+    def quantize(x, group=32):
+        a = real._f64(x); d = a.shape[-1]
+        blocks = a.reshape(a.shape[:-1] + (d // group, group))
+        amax = np.abs(blocks).max(axis=-1)
+        X = np.vectorize(exponent, otypes=[np.int64])(amax)
+        y = blocks / np.ldexp(1.0, X)[..., None]
+        c = real.e4m3_round(y) if rounding is None else rounding(y)
+        return c.reshape(a.shape), X
+    return quantize
+
+
+def _exp_rounded_log2(amax):
+    return -127 if amax == 0 else max(-127, int(round(math.log2(amax))) - 8)
+
+
+def _exp_emax7(amax):
+    return -127 if amax == 0 else max(-127, math.frexp(amax)[1] - 1 - 7)
+
+
+def _exp_zero_group_0(amax):
+    return 0 if amax == 0 else real.mx_exponent(amax)
+
+
+def _e4m3_truncate(y):
+    """Toward-zero rounding onto the E4M3 grid (saturating at 448)."""
+    import torch
+    codes = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn)
+    mags = np.sort(codes.to(torch.float64).numpy())      # 0 .. 448
+    a = np.minimum(np.abs(y), 448.0)
+    return np.sign(y) * mags[np.searchsorted(mags, a, side="right") - 1]
+
+
+def _mx_scores(q_quant=True, per_row_scale=False):
+    def scores(q_idx, w, k_rows, k_scale=None):
+        if k_scale is None or np.ndim(real._f64(k_scale)) != 2:
+            return real.index_scores(q_idx, w, k_rows, k_scale)
+        byt = real._f64(k_scale).astype(np.int64)
+        k = real._f64(k_rows); group = k.shape[-1] // byt.shape[-1]
+        if per_row_scale:
+            byt = np.repeat(byt[:, :1], byt.shape[1], axis=1)
+        q = real._f64(q_idx)
+        if q_quant:
+            q = real.mxfp8_dequantize(*real.mxfp8_quantize(q, group), group)
+        kk = real.mxfp8_dequantize(k, byt - 127, group)
+        return np.maximum(kk @ q.T, 0.0) @ real._f64(w)
+    return scores
+
+
 MUTANTS = {
     "no_relu": dict(index_scores=_scores_no_relu),
     "relu_after_head_sum": dict(index_scores=_scores_relu_after_sum),
@@ -111,6 +161,13 @@ MUTANTS = {
     "softmax_scale_dropped": dict(sparse_mla=_mla_no_scale, dense_mla=_mla_no_scale),
     "lse_base_2": dict(sparse_mla=_mla_lse_log2, dense_mla=_mla_lse_log2),
     "softmax_not_normalised": dict(sparse_mla=_mla_unnormalised, dense_mla=_mla_unnormalised),
+    "mx_exponent_rounded": dict(mxfp8_quantize=_mx_quantize_with(_exp_rounded_log2)),
+    "mx_emax_7": dict(mxfp8_quantize=_mx_quantize_with(_exp_emax7)),
+    "mx_zero_group_exponent_0": dict(mxfp8_quantize=_mx_quantize_with(_exp_zero_group_0)),
+    "mx_round_toward_zero": dict(mxfp8_quantize=_mx_quantize_with(real.mx_exponent,
+                                                                   _e4m3_truncate)),
+    "mx_query_not_quantised": dict(index_scores=_mx_scores(q_quant=False)),
+    "mx_one_scale_per_row": dict(index_scores=_mx_scores(per_row_scale=True)),
 }
 
 
