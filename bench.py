@@ -63,7 +63,14 @@ def algorithmic_bytes(ws) -> dict:
     # sequence's length); every other row reads its own
     kv = torch.clamp(lens, max=ws.s_max) if (ws.mode == "decode" and ws.tokens_per_seq > 1) else vis
     key = int(kv.sum()) * ws.d * kel
-    scale = int(kv.sum()) * 4 if ws.k_scale is not None else 0
+    # scale bytes per key: one fp32 (FP8) or d/G E8M0 bytes (MXFP8)
+    if ws.k_scale is None:
+        per_key_scale = 0
+    elif ws.k_scale.dim() == ws.k_idx.dim():
+        per_key_scale = ws.k_scale.shape[-1] * ws.k_scale.element_size()
+    else:
+        per_key_scale = ws.k_scale.element_size()
+    scale = int(kv.sum()) * per_key_scale
     sel = torch.clamp(vis, max=ws.K)
     gather = int(sel.sum()) * W.D_QK * 2
     q_bytes = ws.q_idx.numel() * 2 + ws.w.numel() * 4 + ws.q.numel() * 2
@@ -273,8 +280,10 @@ def run_gpu(args):
     cfg = W.CONFIGS[args.config]
     # seeded per config; each rank its own replica (--rows: a smaller decode batch
     # for profiling captures, never a bench line)
-    ws = W.make_config(args.config, device=dev, rows=args.rows, tokens_per_seq=args.tokens_per_seq)
+    ws = W.make_config(args.config, device=dev, rows=args.rows, tokens_per_seq=args.tokens_per_seq,
+                       k_mx_group=getattr(args, "k_mx_group", 0))
     tps = ws.tokens_per_seq
+    wname = ws.name   # the config's workload, or its MXFP8-key variant
     torch.cuda.synchronize()
     binding.load()
     stream = torch.cuda.current_stream()
@@ -348,7 +357,7 @@ def run_gpu(args):
         kname = "index_score"
         roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": src,
-                    "traffic": recorded_traffic(kname, cfg["name"]),
+                    "traffic": recorded_traffic(kname, wname),
                     "algorithmic_bytes": kbytes, "kernel_ms": round(k_ms, 5)}
     else:
         # ---- prefill: both halves are dense contractions on the tensor cores;
@@ -384,7 +393,7 @@ def run_gpu(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded generators; integer-valued indexer inputs, N(0,1) latent)",
-            "config": {"workload": cfg["name"], "batch": ws.T, "history": int(ws.s_max),
+            "config": {"workload": wname, "batch": ws.T, "history": int(ws.s_max),
                        "indexer": f"{ws.H_i}x{ws.d}", "topk": ws.K, "mla_heads": ws.H,
                        "parallelism": f"replicas x{world} (batch shards, no collective)",
                        "l2": "inputs larger than L2 (537 MB of index keys streamed per step)"},
@@ -398,6 +407,10 @@ def run_gpu(args):
             result["config"]["profiling_rows"] = args.rows
         if tps > 1:
             result["config"]["tokens_per_seq"] = tps
+        mxg = getattr(args, "k_mx_group", 0)
+        if mxg:
+            result["config"]["index_keys"] = f"mxfp8 (E4M3 + E8M0 per {mxg})"
+            result["config"]["l2"] = "inputs larger than L2 (MXFP8 index keys streamed per step)"
         if world == 1 and not args.no_cpu:
             result["cpu_baseline"] = cpu_baseline(ws, budget_s=args.cpu_seconds)
     barrier(world)
@@ -523,7 +536,7 @@ def run_reference(args):
         return None
     cfg = W.CONFIGS[args.config]
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
-    ws = W.make_config(args.config, device=dev)
+    ws = W.make_config(args.config, device=dev, k_mx_group=getattr(args, "k_mx_group", 0))
     per_step = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
     start = 0
     for _ in range(args.warmup):
@@ -543,7 +556,7 @@ def run_reference(args):
             "ms_per_step": round(1e3 * tot_s / max(1, args.steps), 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (same seeded generators as the GPU arm)",
-            "config": {"workload": cfg["name"], "batch": ws.T, "history": int(ws.s_max),
+            "config": {"workload": ws.name, "batch": ws.T, "history": int(ws.s_max),
                        "indexer": f"{ws.H_i}x{ws.d}", "topk": ws.K, "mla_heads": ws.H},
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
@@ -585,6 +598,68 @@ def run_crossover():
     print(json.dumps({"probe": "dense_vs_sparse_decode", "batch": B, "topk": K,
                       "indexer": "64x128", "mla_heads": 128, "results": res,
                       "first_history_where_sparse_wins": cross}))
+
+
+def run_mx_scan():
+    """MXFP8 group-size scan on the decode workload's shapes (64 sequences x
+    32768 positions, 64x128 indexer heads, Top-2048): bf16 keys with outlier
+    channels and N(0,1) index queries; for G = 32, 64, 128 the keys go through
+    the quantiser, are scored on the MXFP8 path (the query quantised in the
+    kernel with the same G) and selected, and the selection is compared with
+    the one made from bf16 scores of the unquantised keys.  Reports the Top-K
+    recall, the score error, the scoring time and the quantiser's bandwidth.
+    G = 128 with 128-wide keys is one power-of-two scale per key."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from indexed_sparse_attention_indexer_gb300 import binding
+    binding.load()
+    stream = torch.cuda.current_stream()
+    B, S, Hi, d, K = 64, 32768, 64, 128, 2048
+    hbm, _, src = peaks()
+    keys = W.make_mx_input(B * S, d, seed=5, device=dev, special=False, row_spread=1.0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(6)
+    q_idx = torch.randn((B, Hi, d), generator=g, device=dev).to(torch.bfloat16)
+    w = torch.rand((B, Hi), generator=g, device=dev)
+    lens = torch.full((B,), S, dtype=torch.int32, device=dev)
+    latent = torch.empty((1, 1, W.D_QK), dtype=torch.bfloat16, device=dev)   # not read here
+    scores = torch.empty((B, S), dtype=torch.float32, device=dev)
+    c_bf = binding.Cache(keys.view(B, S, d), latent, lens)
+    ms_bf = time_alone(lambda: binding.index_score(q_idx, w, c_bf, True, scores=scores, ld=S,
+                                                   stream=stream), stream, 20)
+    ref = scores.clone()
+    ref_idx, _ = binding.topk(ref, K, row_len=lens)
+    mask = torch.zeros((B, S), dtype=torch.bool, device=dev)
+    mask.scatter_(1, ref_idx.to(torch.int64), True)
+    ref_mag = ref.abs().mean(dim=1, keepdim=True)
+    res = [{"group": None, "keys": "bf16", "key_bytes_per_position": 2 * d,
+            "score_ms": round(ms_bf, 4)}]
+    for G in (32, 64, 128):
+        codes = torch.empty((B * S, d), dtype=torch.float8_e4m3fn, device=dev)
+        sc = torch.empty((B * S, d // G), dtype=torch.uint8, device=dev)
+        q_ms = time_alone(lambda: binding.mxfp8_quantize(keys, G, codes=codes, scales=sc,
+                                                         stream=stream), stream, 20)
+        qbytes = B * S * (2 * d + d + d // G)
+        c_mx = binding.Cache(codes.view(B, S, d), latent, lens, k_scale=sc.view(B, S, d // G))
+        ms = time_alone(lambda: binding.index_score(q_idx, w, c_mx, True, scores=scores, ld=S,
+                                                    stream=stream), stream, 20)
+        idx, _ = binding.topk(scores, K, row_len=lens)
+        hits = mask.gather(1, idx.to(torch.int64)).sum(dim=1).float() / K
+        err = ((scores - ref).abs() / ref_mag).flatten()
+        res.append({"group": G, "keys": "mxfp8", "key_bytes_per_position": d + d // G,
+                    "topk_recall_vs_bf16": round(float(hits.mean()), 5),
+                    "topk_recall_min_row": round(float(hits.min()), 5),
+                    "score_err_rel_mean_abs_median": float(err.median()),
+                    "score_err_rel_mean_abs_max": float(err.max()),
+                    "score_ms": round(ms, 4),
+                    "quantize_ms": round(q_ms, 4),
+                    "quantize_gbs": round(qbytes / (q_ms / 1e3) / 1e9, 1),
+                    "quantize_hbm_frac": round(qbytes / (q_ms / 1e3) / 1e9 / hbm, 4)})
+        del codes, sc, c_mx
+    print(json.dumps({"probe": "mxfp8_group_scan", "batch": B, "history": S,
+                      "indexer": f"{Hi}x{d}", "topk": K, "peak_source": src,
+                      "keys": "bf16 N(0,1) x exp(U(-1,1)) per row, 4 outlier channels x32",
+                      "results": res}))
 
 
 def run_gather_ceiling():
@@ -637,6 +712,11 @@ def main():
     ap.add_argument("--tokens-per-seq", type=int, default=1,
                     help="decode workloads: candidate tokens verified per sequence in one step "
                          "(multi-token decode; the default line is 1)")
+    ap.add_argument("--k-mx-group", type=int, default=0, choices=[0, 32, 64, 128],
+                    help="contiguous decode workloads: index keys stored as MXFP8 with this "
+                         "many elements per scale (0: the workload's own key format)")
+    ap.add_argument("--mx-scan", action="store_true",
+                    help="measurement: MXFP8 group-size scan, precision and speed (not a bench line)")
     ap.add_argument("--rows", type=int, default=None,
                     help="profiling aid: a smaller decode batch (the printed line is not a bench line)")
     args = ap.parse_args()
@@ -645,6 +725,9 @@ def main():
         return
     if args.crossover:
         run_crossover()
+        return
+    if args.mx_scan:
+        run_mx_scan()
         return
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

@@ -70,13 +70,20 @@ typedef enum {
   DSI_ERR_WORKSPACE = 6      /* workspace NULL or smaller than dsi_workspace_size() */
 } dsi_status;
 
-typedef enum { DSI_BF16 = 0, DSI_FP8_E4M3 = 1 } dsi_dtype;
+/* Index key formats.  DSI_MXFP8_E4M3: microscaled FP8 ("Day 0 Inference
+ * Support for New LLM Architectures: Optimization Practices", "A Layered
+ * Strategy": index Q/K in MXFP8, one scale per 32 elements, quantised
+ * dynamically) -- E4M3 codes plus one E8M0 byte (scale 2^(byte-127)) per
+ * group of k_group consecutive elements of a key. */
+typedef enum { DSI_BF16 = 0, DSI_FP8_E4M3 = 1, DSI_MXFP8_E4M3 = 2 } dsi_dtype;
 
 typedef struct dsi_cache {
   const void*    k_idx;        /* index keys, k_dtype elements */
   int32_t        k_dtype;      /* dsi_dtype of k_idx */
   int32_t        d;            /* index key width (64 or 128; any multiple of 8 on the generic kernel) */
-  const float*   k_scale;      /* FP8 only: one fp32 scale per position; NULL for bf16 */
+  const void*    k_scale;      /* FP8: fp32 [positions], one scale per position;
+                                  MXFP8: uint8 E8M0 [positions, d / k_group];
+                                  NULL for bf16 (laid out like k_idx, minus d) */
   const void*    latent;       /* bf16 latent rows, 576 per position */
   const int32_t* block_table;  /* [batch, max_pages] page ids, or NULL for contiguous */
   int32_t        page_size;    /* positions per page (paged only; multiple of 8) */
@@ -85,6 +92,7 @@ typedef struct dsi_cache {
   int32_t        batch;        /* number of sequences */
   int64_t        s_max;        /* contiguous: rows per sequence; paged: max_pages * page_size */
   int64_t        num_pages;    /* paged: pages in the pools (bounds checks); contiguous: 0 */
+  int32_t        k_group;      /* MXFP8: elements per scale, 32, 64 or 128 (0 = 32); else unused */
 } dsi_cache;
 
 /*
@@ -97,7 +105,14 @@ typedef struct dsi_cache {
  *   scores[r, s] = k_scale_s * sum_h w[r, h] * max(0, q_idx[r, h, :] . k[s, :])
  *
  * with k_scale_s = 1 for bf16 keys.  The ReLU gate is this library's stated
- * choice (the pages leave the activation open).
+ * choice (the pages leave the activation open).  With FP8 keys the index
+ * query takes part rounded to E4M3.  With MXFP8 keys k[s, :] is the
+ * dequantised key (code * 2^(byte-127) group by group, k_scale_s = 1) and
+ * the index query is MXFP8-quantised on the fly with the same group size (see
+ * dsi_mxfp8_quantize) and dequantised; MXFP8 keys need n_heads_idx == 64,
+ * d == 128, a paged page_size that is a multiple of 64 or a contiguous s_max
+ * that is a multiple of 4, and a 16-byte aligned k_scale (else
+ * DSI_ERR_UNSUPPORTED / DSI_ERR_INVALID_ARG).
  *   q_idx   bf16 [rows, n_heads_idx, d]
  *   w       fp32 [rows, n_heads_idx] head weights per query token
  *   cache   see above; decode: rows == batch
@@ -273,6 +288,40 @@ dsi_status dsi_indexed_attention_static(const void* q_idx, const float* w, const
  * sizing of the dsi_sparse_mla_* calls when n_heads_idx == 0 and s_max == 0). */
 size_t dsi_workspace_size(int32_t rows, int32_t n_heads_idx, int32_t n_heads, int32_t K,
                           int64_t s_max, int32_t decode);
+
+/*
+ * dsi_mxfp8_quantize — dynamic MXFP8 quantisation of bf16 rows: index keys on
+ * their way into the cache (an append: dst_rows are the cache rows of the new
+ * positions) or any index vectors.
+ * ("Day 0 Inference Support for New LLM Architectures: Optimization
+ * Practices", "A Layered Strategy": MXFP8 index Q/K, dynamic per-group
+ * quantisation, 32 elements per scale; "Day 0 Inference Acceleration for New
+ * LLM Architectures: Hybrid Attention Adaptation and Optimization Practices",
+ * quantisation of the index Q/K, and its advice to scan the group size.)
+ *
+ * For row i and group g (elements g*group .. g*group+group-1):
+ *   X = floor(log2(max |x|)) - 8 over the group, held in [-127, 127]
+ *       (8 = exponent of E4M3's largest normal, 448); an all-zero group has X = -127
+ *   codes[dst(i), j]  = E4M3 of x[i, j] / 2^X, nearest (ties to even),
+ *                       saturating at +-448
+ *   scales[dst(i), g] = X + 127 (E8M0)
+ * with dst(i) = dst_rows[i], or i when dst_rows is NULL; a negative dst_rows
+ * entry skips the row.  This library's reading of the scale rule is the usual
+ * microscaling one; the pages fix only the group size and the dynamic choice.
+ *   x         bf16 [n_rows, ld_x] (16-byte aligned, ld_x a multiple of 8, >= d);
+ *             the first d elements of each row are quantised
+ *   group     32, 64 or 128; d a multiple of group
+ *   dst_rows  int64 [n_rows] device array, or NULL
+ *   codes     uint8 E4M3 [*, d] (16-byte aligned), rows addressed by dst(i)
+ *   scales    uint8 E8M0 [*, d / group], rows addressed by dst(i)
+ * The caller guarantees every dst(i) lies inside codes and scales.
+ * Errors: DSI_ERR_INVALID_ARG (null pointer, n_rows < 0, ld_x < d, ld_x not a
+ * multiple of 8, misaligned x or codes), DSI_ERR_UNSUPPORTED (group not 32,
+ * 64 or 128; d < 1 or not a multiple of group).
+ */
+dsi_status dsi_mxfp8_quantize(const void* x, int64_t n_rows, int32_t d, int64_t ld_x,
+                              int32_t group, const int64_t* dst_rows, void* codes, void* scales,
+                              void* stream);
 
 /*
  * dsi_probe_random_gather — diagnostic, not part of the layer: plain 16-byte

@@ -18,7 +18,7 @@ _LIBS = {}
 
 DSI_OK, DSI_ERR_INVALID_ARG, DSI_ERR_UNSUPPORTED, DSI_ERR_CUDA = 0, 1, 2, 3
 DSI_ERR_TIMEOUT, DSI_ERR_BOUNDS, DSI_ERR_WORKSPACE = 4, 5, 6
-DSI_BF16, DSI_FP8_E4M3 = 0, 1
+DSI_BF16, DSI_FP8_E4M3, DSI_MXFP8_E4M3 = 0, 1, 2
 D_QK, D_LATENT = 576, 512
 
 c_void_p, c_int32, c_int64, c_float, c_size_t = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
@@ -30,7 +30,7 @@ class DsiCache(ctypes.Structure):
     _fields_ = [("k_idx", c_void_p), ("k_dtype", c_int32), ("d", c_int32), ("k_scale", c_void_p),
                 ("latent", c_void_p), ("block_table", c_void_p), ("page_size", c_int32),
                 ("max_pages", c_int32), ("seq_lens", c_void_p), ("batch", c_int32),
-                ("s_max", c_int64), ("num_pages", c_int64)]
+                ("s_max", c_int64), ("num_pages", c_int64), ("k_group", c_int32)]
 
 
 # name -> (restype, argtypes); the exported surface of include/dsi.h
@@ -60,6 +60,8 @@ SIGNATURES = {
                                                ctypes.POINTER(DsiCache), c_int32, c_int32,
                                                c_int32, c_int32, c_int64, c_float, c_int32,
                                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "dsi_mxfp8_quantize": (c_int32, [c_void_p, c_int64, c_int32, c_int64, c_int32, c_void_p,
+                                     c_void_p, c_void_p, c_void_p]),
     "dsi_probe_random_gather": (c_int32, [c_void_p, c_int64, c_int64, c_void_p, c_int32, c_int32,
                                           c_int32, c_void_p]),
     "dsi_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int64, c_int32]),
@@ -126,8 +128,16 @@ class Cache:
         ref = k_idx if k_idx is not None else latent
         s = DsiCache()
         s.k_idx = k_idx.data_ptr() if k_idx is not None else None
-        s.k_dtype = DSI_FP8_E4M3 if (k_idx is not None and k_idx.dtype == torch.float8_e4m3fn) else DSI_BF16
         s.d = int(k_idx.shape[-1]) if k_idx is not None else 0
+        s.k_dtype = DSI_BF16
+        s.k_group = 0
+        if k_idx is not None and k_idx.dtype == torch.float8_e4m3fn:
+            # uint8 scales [.., d/G] are MXFP8 group scales; fp32 [..] per-position scales
+            if k_scale is not None and k_scale.dtype == torch.uint8:
+                s.k_dtype = DSI_MXFP8_E4M3
+                s.k_group = s.d // int(k_scale.shape[-1])
+            else:
+                s.k_dtype = DSI_FP8_E4M3
         s.k_scale = k_scale.data_ptr() if k_scale is not None else None
         s.latent = latent.data_ptr() if latent is not None else None
         if block_table is not None:
@@ -186,6 +196,23 @@ def index_topk_prefill(q_idx, w, cache: Cache, K: int, q_offset: int = 0, idx=No
                                     int(K), _ptr(idx), _ptr(count), _stream(stream))
     _check(lib, "dsi_index_topk_prefill", st)
     return idx, count
+
+
+def mxfp8_quantize(x, group: int = 32, dst_rows=None, codes=None, scales=None, stream=None,
+                   checked: bool = False):
+    """MXFP8 codes (float8_e4m3fn) and E8M0 scale bytes (uint8) of bf16 rows
+    ``x [n, d]``; with ``dst_rows`` (int64 [n]) row i goes to row dst_rows[i]
+    of the given ``codes``/``scales`` (an append into a cache)."""
+    lib = load(checked)
+    n, d = int(x.shape[0]), int(x.shape[1])
+    if codes is None:
+        codes = torch.empty((n, d), dtype=torch.float8_e4m3fn, device=x.device)
+    if scales is None:
+        scales = torch.empty((n, d // group), dtype=torch.uint8, device=x.device)
+    st = lib.dsi_mxfp8_quantize(_ptr(x), n, d, int(x.stride(0)), int(group), _ptr(dst_rows),
+                                _ptr(codes), _ptr(scales), _stream(stream))
+    _check(lib, "dsi_mxfp8_quantize", st)
+    return codes, scales
 
 
 def probe_random_gather(base, row_pitch: int, rows, bytes_per_row: int, blocks: int,

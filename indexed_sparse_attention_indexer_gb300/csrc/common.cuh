@@ -16,7 +16,8 @@ typedef __nv_bfloat16 bf16;
 // Kernel-side copy of dsi_cache (passed by value).
 struct CacheView {
   const void* k_idx;
-  const float* k_scale;
+  const float* k_scale;      // FP8 keys: one scale per position (null otherwise)
+  const uint8_t* k_mx_scale; // MXFP8 keys: E8M0 bytes [positions, d / k_group] (null otherwise)
   const bf16* latent;
   const int32_t* block_table;
   const int32_t* seq_lens;
@@ -28,6 +29,7 @@ struct CacheView {
   int32_t k_dtype;
   int32_t batch;
   int32_t tokens_per_seq;   // decode: query rows per sequence (1; T for a multi-token step)
+  int32_t k_group;          // MXFP8 keys: elements per scale (32, 64 or 128)
 };
 
 // Device status word codes (mirrors dsi_status).
@@ -93,6 +95,70 @@ __device__ __forceinline__ void fp8x16_to_f32(const uint4& v, float* f) {
     f[2 * i] = t.x;
     f[2 * i + 1] = t.y;
   }
+}
+
+// ---- MXFP8 (E4M3 codes with one power-of-two scale per group) -------------
+// Shared exponent of a group from its largest magnitude (a non-negative
+// float): floor(log2(amax)) - 8, held in [-127, 127].  floor(log2) is the
+// biased exponent field minus 127 for normal numbers; zero and subnormal
+// maxima lie below the E8M0 range and clamp to -127.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const int e = (int)(__float_as_uint(amax) >> 23);   // sign bit is clear
+  if (e == 0) return -127;
+  const int x = e - 127 - 8;
+  return x < -127 ? -127 : x;                          // e <= 254 keeps x <= 119
+}
+
+// 16 floats scaled by 2^-X (exact: a power of two) and rounded to E4M3,
+// nearest-even, saturating at +-448; byte i of the result is element i.
+__device__ __forceinline__ uint4 mx_encode16(const float* f, int X) {
+  const float inv = __uint_as_float((uint32_t)(127 - X) << 23);   // 2^-X, -X in [-119, 127]
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(f[4 * k] * inv, f[4 * k + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(f[4 * k + 2] * inv, f[4 * k + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+    w[k] = (uint32_t)lo | ((uint32_t)hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// 16 E4M3 codes -> the 16 bf16 values code * 2^X (exact down to bf16's
+// subnormal range).  Each code's sign, exponent and mantissa bits are moved
+// into a bf16 bit pattern whose exponent field is the E4M3 field itself (so
+// a subnormal code lands on a bf16 subnormal with the same mantissa); that
+// pattern is the code's value times 2^-120, and one bf16 multiply by
+// 2^(120 + X) rebiases and scales it (X > 7 takes a second multiply, since
+// 2^(120 + X) would leave bf16's range).  lo = elements 0..7, hi = 8..15.
+__device__ __forceinline__ void mx_decode16(const uint4& v, int X, uint4& lo, uint4& hi) {
+  const uint32_t e1 = (uint32_t)(X <= 7 ? X + 247 : 247);
+  const uint32_t m1 = (e1 << 7) | (e1 << 23);
+  const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    // codes 0,1 (then 2,3) of the word into the high bytes of two halves
+    const uint32_t a = __byte_perm(in[k], 0u, 0x1404);
+    const uint32_t b = __byte_perm(in[k], 0u, 0x3424);
+    out[2 * k] = bf16x2_mul((a & 0x80008000u) | ((a >> 4) & 0x07F007F0u), m1);
+    out[2 * k + 1] = bf16x2_mul((b & 0x80008000u) | ((b >> 4) & 0x07F007F0u), m1);
+  }
+  if (X > 7) {
+    const uint32_t e2 = (uint32_t)(X + 127);
+    const uint32_t m2 = (e2 << 7) | (e2 << 23);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = bf16x2_mul(out[i], m2);
+  }
+  lo = make_uint4(out[0], out[1], out[2], out[3]);
+  hi = make_uint4(out[4], out[5], out[6], out[7]);
 }
 
 // Exclusive block-wide prefix sum of one int per thread.  `ws` holds >= 33

@@ -46,12 +46,19 @@ dsi_status check_cache(const dsi_cache* c, int rows, int decode, int64_t q_offse
   if (c->batch < 0) return DSI_ERR_INVALID_ARG;
   if (need_keys) {
     if (!c->k_idx) return DSI_ERR_INVALID_ARG;
-    if (c->k_dtype != DSI_BF16 && c->k_dtype != DSI_FP8_E4M3) return DSI_ERR_UNSUPPORTED;
+    if (c->k_dtype != DSI_BF16 && c->k_dtype != DSI_FP8_E4M3 && c->k_dtype != DSI_MXFP8_E4M3)
+      return DSI_ERR_UNSUPPORTED;
     if (c->d <= 0) return DSI_ERR_INVALID_ARG;
-    const int chunk = c->k_dtype == DSI_FP8_E4M3 ? 16 : 8;  // elements per 16-byte load
+    const int chunk = c->k_dtype == DSI_BF16 ? 8 : 16;  // elements per 16-byte load
     if (c->d % chunk != 0 || c->d > 256) return DSI_ERR_UNSUPPORTED;
     if (!aligned(c->k_idx, 16)) return DSI_ERR_INVALID_ARG;
-    if (c->k_dtype == DSI_FP8_E4M3 && !c->k_scale) return DSI_ERR_INVALID_ARG;
+    if (c->k_dtype != DSI_BF16 && !c->k_scale) return DSI_ERR_INVALID_ARG;
+    if (c->k_dtype == DSI_MXFP8_E4M3) {
+      const int g = c->k_group ? c->k_group : 32;
+      if (g != 32 && g != 64 && g != 128) return DSI_ERR_UNSUPPORTED;
+      if (c->d % g != 0) return DSI_ERR_UNSUPPORTED;
+      if (!aligned(c->k_scale, 16)) return DSI_ERR_INVALID_ARG;
+    }
   }
   if (need_latent && (!c->latent || !aligned(c->latent, 16))) return DSI_ERR_INVALID_ARG;
   if (c->block_table) {
@@ -73,7 +80,10 @@ dsi_status check_cache(const dsi_cache* c, int rows, int decode, int64_t q_offse
 CacheView view_of(const dsi_cache* c) {
   CacheView v;
   v.k_idx = c->k_idx;
-  v.k_scale = c->k_scale;
+  v.k_scale = c->k_dtype == DSI_FP8_E4M3 ? static_cast<const float*>(c->k_scale) : nullptr;
+  v.k_mx_scale =
+      c->k_dtype == DSI_MXFP8_E4M3 ? static_cast<const uint8_t*>(c->k_scale) : nullptr;
+  v.k_group = c->k_group ? c->k_group : 32;
   v.latent = reinterpret_cast<const bf16*>(c->latent);
   v.block_table = c->block_table;
   v.seq_lens = c->seq_lens;
@@ -153,6 +163,7 @@ dsi_status dsi_index_score(const void* q_idx, const float* w, const dsi_cache* c
   if (ld_scores < (decode ? cache->s_max : q_offset + rows)) return DSI_ERR_INVALID_ARG;
   if (rows == 0) return DSI_OK;
   CacheView v = view_of(cache);
+  if (!index_score_supported(v, n_heads_idx, rows, decode)) return DSI_ERR_UNSUPPORTED;
   return from_cuda(launch_index_score(reinterpret_cast<const bf16*>(q_idx), w, v, rows,
                                       n_heads_idx, decode, q_offset, scores, ld_scores,
                                       status_ptr(), reinterpret_cast<cudaStream_t>(stream)));
@@ -255,8 +266,12 @@ static dsi_status layer_common(const void* q_idx, const float* w, const void* q,
   int* err = status_ptr();
   CacheView v = view_of(cache);
   v.tokens_per_seq = tokens_per_seq;
+  const bool fused_prefill = !decode && fused_prefill_topk_supported(v, n_heads_idx, rows,
+                                                                     q_offset, K);
+  if (!fused_prefill && !index_score_supported(v, n_heads_idx, rows, decode))
+    return DSI_ERR_UNSUPPORTED;
   cudaError_t e;
-  if (!decode && fused_prefill_topk_supported(v, n_heads_idx, rows, q_offset, K)) {
+  if (fused_prefill) {
     // prefill: scores stay on chip, only the selected indices are written
     e = launch_index_topk_prefill(reinterpret_cast<const bf16*>(q_idx), w, v, rows, q_offset, K,
                                   idx, count_out, err, st);
@@ -297,6 +312,21 @@ dsi_status dsi_indexed_attention_multi(const void* q_idx, const float* w, const 
   return layer_common(q_idx, w, q, cache, (int32_t)rows, n_heads_idx, n_heads, K, 0, scale, 1,
                       tokens_per_seq, idx_out, count_out, out, lse, workspace, workspace_bytes,
                       stream);
+}
+
+dsi_status dsi_mxfp8_quantize(const void* x, int64_t n_rows, int32_t d, int64_t ld_x,
+                              int32_t group, const int64_t* dst_rows, void* codes, void* scales,
+                              void* stream) {
+  if (!x || !codes || !scales || n_rows < 0) return DSI_ERR_INVALID_ARG;
+  if (group != 32 && group != 64 && group != 128) return DSI_ERR_UNSUPPORTED;
+  if (d < 1 || d % group != 0) return DSI_ERR_UNSUPPORTED;
+  if (ld_x < d || ld_x % 8 != 0 || !aligned(x, 16) || !aligned(codes, 16))
+    return DSI_ERR_INVALID_ARG;
+  if (n_rows == 0) return DSI_OK;
+  return from_cuda(launch_mxfp8_quantize(reinterpret_cast<const bf16*>(x), n_rows, d, ld_x, group,
+                                         dst_rows, static_cast<uint8_t*>(codes),
+                                         static_cast<uint8_t*>(scales),
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dsi_status dsi_probe_random_gather(const void* base, int64_t row_pitch, int64_t n_src_rows,

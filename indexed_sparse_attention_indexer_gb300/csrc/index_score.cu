@@ -225,10 +225,16 @@ static cudaError_t dispatch_simt(const bf16* q, const float* w, const CacheView&
   return cudaErrorInvalidValue;
 }
 
+bool index_score_supported(const CacheView& c, int H, int rows, int decode) {
+  if (c.k_dtype != DSI_MXFP8_E4M3) return true;
+  return tc_score_supported(c, H) && tc_score_shape_ok(c, rows, decode);
+}
+
 cudaError_t launch_index_score(const bf16* q_idx, const float* w, const CacheView& c, int rows,
                                int H, int decode, int64_t q_offset, float* scores, int64_t ld,
                                int* err, cudaStream_t st) {
   const bool fp8 = c.k_dtype == DSI_FP8_E4M3;
+  if (!index_score_supported(c, H, rows, decode)) return cudaErrorInvalidValue;
   ScoreKernel k = pick_score_kernel(c, H);
   if (k == kScoreTc && !tc_score_shape_ok(c, rows, decode)) k = kScoreSimt;
   switch (k) {

@@ -22,6 +22,16 @@
 // contiguous ranges over one CTA per SM, so causal prefill rows balance
 // without a special order.  FP8 keys use kind::f8f6f4 with the queries
 // rounded to E4M3 (exact for the integer-valued index queries).
+//
+// MXFP8 keys (E4M3 codes, one E8M0 scale per group of 32, 64 or 128
+// elements; "Day 0 Inference Support...", "A Layered Strategy"): the producer
+// lands the codes by TMA and each tile's group scales by cp.async, extra
+// dequantising warps turn them into the exact bf16 values code * 2^X in a
+// swizzled A tile, and the bf16 MMA runs on that; the index queries are
+// MXFP8-quantised group by group on the fly and stored dequantised the same
+// way.  The tensor core thus sums exactly the products of the dequantised
+// operands (what a block-scaled MMA computes) while HBM carries one byte per
+// key element plus a byte per group.
 #include "kernels.h"
 #include "tc_common.cuh"
 #include "tma_host.h"
@@ -37,29 +47,43 @@ constexpr int kTileM = 128;      // positions per tile
 constexpr int kSub = 64;         // positions per TMA sub-tile
 constexpr int kMaxGroups = 2048;
 
-template <int NT, bool FP8>
+enum : int { kKeyBf16 = 0, kKeyFp8 = 1, kKeyMx = 2 };
+
+template <int NT, int KK>
 struct Cfg {
+  static constexpr bool FP8 = KK == kKeyFp8;
+  static constexpr bool MX = KK == kKeyMx;
+  static constexpr bool K8 = FP8 || MX;                   // one byte per key element in HBM
   static constexpr int N = NT * kHeads;
-  static constexpr int EB = FP8 ? 1 : 2;                  // key/query element bytes
-  static constexpr int A_BYTES = kTileM * kD * EB;        // 16 or 32 KB
+  static constexpr int EB = FP8 ? 1 : 2;                  // MMA operand element bytes
+  static constexpr int A_BYTES = kTileM * kD * EB;        // one MMA A tile: 16 or 32 KB
+  static constexpr int ST_BYTES = K8 ? kTileM * kD : A_BYTES;   // one TMA stage of keys
   static constexpr int B_BYTES = N * kD * EB;
-  static constexpr int STAGES = FP8 ? 8 : (NT == 1 ? 4 : 2);
+  static constexpr int STAGES = FP8 ? 8 : MX ? (NT == 1 ? 6 : NT == 2 ? 4 : 2) : (NT == 1 ? 4 : 2);
+  static constexpr int ABUFS = MX ? (NT == 4 ? 1 : 2) : 0;      // dequantised bf16 A tiles
+  static constexpr int DQ_WARPS = MX ? (NT == 1 ? 4 : 2) : 0;   // dequantising warps
+  static constexpr int DQ_THREADS = DQ_WARPS * 32;
+  static constexpr int DQ_ROWS = MX ? kTileM / DQ_THREADS : 0;  // tile rows per such thread
+  static constexpr int SC_BYTES = kTileM * 4;             // one stage's group scales (<= 4 per key)
   static constexpr int EPI_WARPS = NT == 1 ? 4 : 8;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
-  static constexpr int THREADS = 64 + EPI_THREADS;
+  static constexpr int THREADS = 64 + EPI_THREADS + DQ_THREADS;
   static constexpr int TMEM_COLS = 2 * N <= 128 ? 128 : (2 * N <= 256 ? 256 : 512);
   static constexpr int KSTEPS = FP8 ? 4 : 8;              // 32 bytes of K per MMA
   static constexpr uint32_t IDESC = idesc_f32(FP8 ? 0u : 1u, kTileM, N);
   static constexpr int TOK_PER_THREAD = NT == 1 ? 1 : NT / 2;   // epilogue column split
   // shared memory carve (offsets from a 1024-aligned base)
-  static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_W = OFF_B + 2 * B_BYTES;                 // per epilogue warp: its tokens' weights
+  static constexpr int OFF_A = 0;                                   // TMA stages
+  static constexpr int OFF_ABF = OFF_A + STAGES * ST_BYTES;         // MXFP8: bf16 A tiles
+  static constexpr int OFF_B = OFF_ABF + ABUFS * A_BYTES;
+  static constexpr int OFF_SC = OFF_B + 2 * B_BYTES;                // MXFP8: group scales
+  static constexpr int OFF_W = OFF_SC + (MX ? STAGES * SC_BYTES : 0);   // per epilogue warp: weights
   static constexpr int OFF_PREFIX = OFF_W + EPI_WARPS * TOK_PER_THREAD * kHeads * 4;
   static constexpr int OFF_BAR = (OFF_PREFIX + (kMaxGroups + 1) * 4 + 7) & ~7;
-  static constexpr int NBARS = 2 * STAGES + 2 + 2 + 2 + 2 + 1;
+  static constexpr int NBARS = 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 2 * ABUFS;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8 + 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;                 // + alignment slack
+  static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 struct ScoreArgs {
@@ -71,6 +95,7 @@ struct ScoreArgs {
   int rows;      // query rows (decode: sequences)
   int groups;
   int decode;
+  int lg_group;  // MXFP8: log2 of the elements per scale (5, 6 or 7)
 };
 
 // Group g holds query rows g*NT .. g*NT+NT-1: NT tokens of the prefill, or
@@ -124,11 +149,12 @@ struct ItemIter {
   }
 };
 
-template <int NT, bool FP8>
-__global__ void __launch_bounds__(Cfg<NT, FP8>::THREADS, 1)
+template <int NT, int KK>
+__global__ void __launch_bounds__(Cfg<NT, KK>::THREADS, 1)
 score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
          CacheView c, ScoreArgs a, int* err) {
-  using C = Cfg<NT, FP8>;
+  using C = Cfg<NT, KK>;
+  constexpr bool FP8 = C::FP8;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   grid_dep_wait();   // inputs may come from the kernel launched just before
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -143,6 +169,8 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
   uint64_t* q_full = acc_empty + 2;
   uint64_t* q_empty = q_full + 2;
   uint64_t* done_bar = q_empty + 2;
+  uint64_t* a_full = done_bar + 1;          // MXFP8: dequantised A tile ready
+  uint64_t* a_empty = a_full + C::ABUFS;    // MXFP8: its MMAs are done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   __shared__ int scan_tmp[40];
@@ -165,7 +193,13 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     if (tid == 0) prefix[G] = total;
   }
   if (tid == 0) {
-    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    // MXFP8: a stage is full after the producer's byte count and one cp.async
+    // arrival per producer lane, and empty after every dequantising warp
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], C::MX ? 1 + 32 : 1);
+      mbar_init(&empty[s], C::MX ? C::DQ_WARPS : 1);
+    }
+    for (int i = 0; i < C::ABUFS; ++i) { mbar_init(&a_full[i], C::DQ_WARPS); mbar_init(&a_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], C::EPI_THREADS);
@@ -196,7 +230,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     bool issued[C::STAGES];
 #pragma unroll
     for (int s = 0; s < C::STAGES; ++s) { issued[s] = false; issued_phase[s] = 0; }
-    if (lane == 0) { prefetch_tmap(&kmap); if (!FP8) prefetch_tmap(&qmap); }
+    if (lane == 0) { prefetch_tmap(&kmap); if (!C::K8) prefetch_tmap(&qmap); }
     // lane 0's reading of the flag decides for the warp, so all lanes leave together
     while (it.valid() && !__shfl_sync(0xffffffffu, (int)*abort_flag, 0)) {
       const int g = it.g, j = it.j;
@@ -208,7 +242,40 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         uint8_t* qs = smem + C::OFF_B + slot * C::B_BYTES;
-        if (FP8) {
+        if (C::MX) {
+          // MXFP8-quantise the index queries group by group and store them
+          // dequantised (exact in bf16) in the swizzled B slot; the lanes of
+          // one group are adjacent, so the group maximum is a butterfly
+          const int upg = 1 << (a.lg_group - 4);     // 16-element units per group
+          for (int i = lane; i < C::N * 8; i += 32) {
+            const int n = i >> 3, u = i & 7;
+            const int t = n / kHeads, h = n % kHeads;
+            const int r = g * NT + t;
+            float f[16];
+            float amax = 0.f;
+            if (r < a.rows) {
+              const bf16* src = a.q_idx + ((int64_t)r * kHeads + h) * kD + u * 16;
+              bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(src)), f);
+              bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(src + 8)), f + 8);
+#pragma unroll
+              for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(f[k]));
+            } else {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) f[k] = 0.f;
+            }
+            for (int m = 1; m < upg; m <<= 1)
+              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+            const int X = mx_exponent(amax);
+            uint4 lo, hi;
+            mx_decode16(mx_encode16(f, X), X, lo, hi);
+            uint8_t* blk = qs + (u >> 2) * (C::N * 128);
+            *reinterpret_cast<uint4*>(blk + sw128_offset(n, (2 * u) & 7)) = lo;
+            *reinterpret_cast<uint4*>(blk + sw128_offset(n, (2 * u + 1) & 7)) = hi;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&q_full[slot]);
+        } else if (FP8) {
           // round the bf16 index queries to E4M3 into the swizzled B slot
           for (int i = lane; i < C::N * 8; i += 32) {
             const int n = i >> 3, u = i & 7;
@@ -257,27 +324,31 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       }
       // ---- one key tile -----------------------------------------------------
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, err);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (C::MX) {
+        ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, err);   // every lane copies
+      } else {
+        if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, err);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
       if (!ok) break;
+      const int64_t p0 = (int64_t)j * kTileM;
+      int64_t prow[2] = {-1, -1};
+      int64_t nvis = 0;
       if (lane == 0) {
         const int b = seq_of_row(c, g * NT, a.decode);
-        const int64_t nvis = group_visible<NT>(c, a, g);
-        const int64_t p0 = (int64_t)j * kTileM;
-        int64_t prow[2];
+        nvis = group_visible<NT>(c, a, g);
         int nsub = 0;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const int64_t p = p0 + i * kSub;
-          prow[i] = -1;
           if (p < nvis) { prow[i] = phys_row(c, b, p, err); if (prow[i] >= 0) ++nsub; }
         }
-        uint8_t* as = smem + C::OFF_A + stage * C::A_BYTES;
-        mbar_arrive_expect_tx(&full[stage], (uint32_t)(nsub * (C::A_BYTES / 2)));
+        uint8_t* as = smem + C::OFF_A + stage * C::ST_BYTES;
+        mbar_arrive_expect_tx(&full[stage], (uint32_t)(nsub * (C::ST_BYTES / 2)));
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (prow[i] < 0) continue;
-          if (FP8) {
+          if (C::K8) {
             tma_load_2d(as + i * (kSub * 128), &kmap, 0, (int)prow[i], &full[stage]);
           } else {
             tma_load_2d(as + i * (kSub * 128), &kmap, 0, (int)prow[i], &full[stage]);
@@ -286,6 +357,27 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         }
         issued[stage] = true;
         issued_phase[stage] = phase;
+      }
+      if (C::MX) {
+        // the tile's group scales: lane l copies those of rows 4l .. 4l+3
+        // (4 * 128/G contiguous bytes of one sub-tile's rows); its arrival
+        // on full[stage] fires once the copy has landed.  Only pieces that
+        // start at a visible position are read, and those end inside the
+        // page (paged) or inside the sequence's rows (s_max % 4 == 0).
+        const int64_t pr0 = __shfl_sync(0xffffffffu, prow[0], 0);
+        const int64_t pr1 = __shfl_sync(0xffffffffu, prow[1], 0);
+        nvis = __shfl_sync(0xffffffffu, nvis, 0);
+        const int t = lane * 4;
+        const int64_t pr = t < kSub ? pr0 : pr1;
+        if (pr >= 0 && p0 + t < nvis) {
+          const int spr = kD >> a.lg_group;          // scale bytes per key: 4, 2 or 1
+          const uint8_t* src = c.k_mx_scale + (pr + (t & (kSub - 1))) * spr;
+          const uint32_t dst = smem_u32(smem + C::OFF_SC + stage * C::SC_BYTES + t * spr);
+          if (spr == 4) cp_async_16(dst, src);
+          else if (spr == 2) cp_async_8(dst, src);
+          else cp_async_4(dst, src);
+        }
+        cp_async_mbar_arrive_noinc(&full[stage]);
       }
       if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
       it.next();
@@ -301,8 +393,8 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     if (lane == 0) {
       ItemIter it;
       it.init(prefix, a.groups, it_begin, it_end);
-      int gprev = -1, qcount = 0, stage = 0, abuf = 0, slot = 0;
-      uint32_t phase = 0, aph = 0;
+      int gprev = -1, qcount = 0, stage = 0, abuf = 0, slot = 0, xb = 0;
+      uint32_t phase = 0, aph = 0, xph = 0;
       while (it.valid()) {
         const int g = it.g;
         if (g != gprev) {
@@ -311,10 +403,15 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
           ++qcount;
           gprev = g;
         }
-        if (!mbar_wait(&full[stage], phase, abort_flag, err)) break;
+        if (C::MX) {
+          if (!mbar_wait(&a_full[xb], xph, abort_flag, err)) break;
+        } else {
+          if (!mbar_wait(&full[stage], phase, abort_flag, err)) break;
+        }
         if (!mbar_wait(&acc_empty[abuf], aph ^ 1, abort_flag, err)) break;
         tc_fence_after();
-        const uint32_t a_base = smem_u32(smem + C::OFF_A + stage * C::A_BYTES);
+        const uint32_t a_base = C::MX ? smem_u32(smem + C::OFF_ABF + xb * C::A_BYTES)
+                                      : smem_u32(smem + C::OFF_A + stage * C::A_BYTES);
         const uint32_t b_base = smem_u32(smem + C::OFF_B + slot * C::B_BYTES);
         const uint32_t d_tmem = tmem + abuf * C::N;
 #pragma unroll
@@ -327,10 +424,16 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
           if (FP8) mma_fp8(d_tmem, ad, bd, C::IDESC, k > 0);
           else mma_bf16(d_tmem, ad, bd, C::IDESC, k > 0);
         }
-        mma_commit(&empty[stage]);
+        if (C::MX) mma_commit(&a_empty[xb]);
+        else mma_commit(&empty[stage]);
         mma_commit(&acc_full[abuf]);
         if (it.next_group() != g) mma_commit(&q_empty[slot]);
-        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        if (C::MX) {
+          if (++xb == C::ABUFS) { xb = 0; xph ^= 1; }
+        } else if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
         if (++abuf == 2) { abuf = 0; aph ^= 1; }
         it.next();
       }
@@ -339,6 +442,47 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       mbar_wait(done_bar, 0, abort_flag, err, 100000000ull);
     }
     __syncwarp();
+  } else if (C::MX && warp >= 2 + C::EPI_WARPS) {
+    // ======================= dequantisation (MXFP8 keys) ======================
+    // E4M3 codes of a landed stage -> bf16 code * 2^X in a swizzled A tile,
+    // one tile row (128 codes, 128/G scales) per thread and pass
+    const int dt = tid - (64 + C::EPI_THREADS);
+    ItemIter it;
+    it.init(prefix, a.groups, it_begin, it_end);
+    int stage = 0, xb = 0;
+    uint32_t phase = 0, xph = 0;
+    const int lg = a.lg_group;
+    const int spr = kD >> lg;
+    while (it.valid()) {
+      if (!warp_wait(&full[stage], phase, abort_flag, err)) break;
+      if (!warp_wait(&a_empty[xb], xph ^ 1, abort_flag, err)) break;
+      const uint8_t* src = smem + C::OFF_A + stage * C::ST_BYTES;
+      const uint8_t* sc = smem + C::OFF_SC + stage * C::SC_BYTES;
+      uint8_t* dst = smem + C::OFF_ABF + xb * C::A_BYTES;
+#pragma unroll
+      for (int rr = 0; rr < C::DQ_ROWS; ++rr) {
+        const int t = dt + rr * C::DQ_THREADS;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + sw128_offset(t, u));
+          const int X = (int)sc[t * spr + ((u * 16) >> lg)] - 127;
+          uint4 lo, hi;
+          mx_decode16(v, X, lo, hi);
+          uint8_t* blk = dst + (u >> 2) * 16384;
+          *reinterpret_cast<uint4*>(blk + sw128_offset(t, (2 * u) & 7)) = lo;
+          *reinterpret_cast<uint4*>(blk + sw128_offset(t, (2 * u + 1) & 7)) = hi;
+        }
+      }
+      fence_proxy_async_smem();   // the tensor core reads the tile through the async proxy
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&a_full[xb]);
+        mbar_arrive(&empty[stage]);
+      }
+      if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+      if (++xb == C::ABUFS) { xb = 0; xph ^= 1; }
+      it.next();
+    }
   } else {
     // ======================= epilogue =========================================
     const int ew = warp - 2;                 // 0 .. EPI_WARPS-1
@@ -413,15 +557,15 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
 }
 
 // ---------------------------------------------------------------- host side
-template <int NT, bool FP8>
+template <int NT, int KK>
 cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, int decode,
                int64_t q_offset, float* scores, int64_t ld, int* err, cudaStream_t st) {
-  using C = Cfg<NT, FP8>;
+  using C = Cfg<NT, KK>;
   const uint64_t krows = c.block_table ? (uint64_t)c.num_pages * c.page_size
                                        : (uint64_t)c.batch * c.s_max;
   CUtensorMap kmap, qmap;
   memset(&qmap, 0, sizeof(qmap));
-  if (FP8) {
+  if (C::K8) {
     if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, krows, kD, 128, kSub))
       return cudaErrorInvalidValue;
   } else {
@@ -440,16 +584,30 @@ cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, 
   a.rows = rows;
   a.decode = decode;
   a.groups = (rows + NT - 1) / NT;
+  a.lg_group = c.k_group == 128 ? 7 : c.k_group == 64 ? 6 : 5;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaError_t e = cudaFuncSetAttribute(score_tc<NT, FP8>,
+  cudaError_t e = cudaFuncSetAttribute(score_tc<NT, KK>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  cudaError_t le = launch_overlapped(score_tc<NT, FP8>, dim3(sms), dim3(C::THREADS), C::SMEM,
+  cudaError_t le = launch_overlapped(score_tc<NT, KK>, dim3(sms), dim3(C::THREADS), C::SMEM,
                                      st, kmap, qmap, c, a, err);
   note_launch();
   return le;
+}
+
+template <int NT>
+cudaError_t go_kind(const bf16* q_idx, const float* w, const CacheView& c, int rows, int decode,
+                    int64_t q_offset, float* scores, int64_t ld, int* err, cudaStream_t st) {
+  switch (c.k_dtype) {
+    case DSI_FP8_E4M3:
+      return go<NT, kKeyFp8>(q_idx, w, c, rows, decode, q_offset, scores, ld, err, st);
+    case DSI_MXFP8_E4M3:
+      return go<NT, kKeyMx>(q_idx, w, c, rows, decode, q_offset, scores, ld, err, st);
+    default:
+      return go<NT, kKeyBf16>(q_idx, w, c, rows, decode, q_offset, scores, ld, err, st);
+  }
 }
 
 }  // namespace
@@ -461,6 +619,12 @@ bool tc_score_supported(const CacheView& c, int H) {
                                        : (uint64_t)c.batch * c.s_max;
   if (krows >= (1ull << 31)) return false;
   if ((reinterpret_cast<uintptr_t>(c.k_idx) & 15) != 0) return false;
+  if (c.k_dtype == DSI_MXFP8_E4M3) {
+    // the scale copies move 4-key pieces that must stay inside a sequence's rows
+    if (!c.k_mx_scale || (reinterpret_cast<uintptr_t>(c.k_mx_scale) & 15) != 0) return false;
+    if (c.k_group != 32 && c.k_group != 64 && c.k_group != 128) return false;
+    if (!c.block_table && c.s_max % 4 != 0) return false;
+  }
   return tma_encode_fn() != nullptr;
 }
 
@@ -481,22 +645,14 @@ bool tc_score_shape_ok(const CacheView& c, int rows, int decode) {
 cudaError_t launch_index_score_tc(const bf16* q_idx, const float* w, const CacheView& c, int rows,
                                   int decode, int64_t q_offset, float* scores, int64_t ld,
                                   int* err, cudaStream_t st) {
-  const bool fp8 = c.k_dtype == DSI_FP8_E4M3;
   if (decode) {
     switch (tokens_per_group(c, decode)) {
-      case 4:
-        return fp8 ? go<4, true>(q_idx, w, c, rows, 1, 0, scores, ld, err, st)
-                   : go<4, false>(q_idx, w, c, rows, 1, 0, scores, ld, err, st);
-      case 2:
-        return fp8 ? go<2, true>(q_idx, w, c, rows, 1, 0, scores, ld, err, st)
-                   : go<2, false>(q_idx, w, c, rows, 1, 0, scores, ld, err, st);
-      default:
-        return fp8 ? go<1, true>(q_idx, w, c, rows, 1, 0, scores, ld, err, st)
-                   : go<1, false>(q_idx, w, c, rows, 1, 0, scores, ld, err, st);
+      case 4: return go_kind<4>(q_idx, w, c, rows, 1, 0, scores, ld, err, st);
+      case 2: return go_kind<2>(q_idx, w, c, rows, 1, 0, scores, ld, err, st);
+      default: return go_kind<1>(q_idx, w, c, rows, 1, 0, scores, ld, err, st);
     }
   }
-  return fp8 ? go<4, true>(q_idx, w, c, rows, 0, q_offset, scores, ld, err, st)
-             : go<4, false>(q_idx, w, c, rows, 0, q_offset, scores, ld, err, st);
+  return go_kind<4>(q_idx, w, c, rows, 0, q_offset, scores, ld, err, st);
 }
 
 }  // namespace dsi

@@ -44,6 +44,10 @@ cudaError_t launch_index_score(const bf16* q_idx, const float* w, const CacheVie
                                int n_heads_idx, int decode, int64_t q_offset, float* scores,
                                int64_t ld, int* err, cudaStream_t st);
 
+// Whether a scoring kernel exists for the shape (MXFP8 keys: the tensor-core
+// kernel only).
+bool index_score_supported(const CacheView& c, int n_heads_idx, int rows, int decode);
+
 // Which scoring kernel a shape takes (for tests and the bench's accounting).
 enum ScoreKernel { kScoreStream = 0, kScoreSimt = 1, kScoreTc = 2 };
 ScoreKernel pick_score_kernel(const CacheView& c, int n_heads_idx);
@@ -75,6 +79,12 @@ cudaError_t launch_sparse_mla(const bf16* q, const CacheView& c, const int32_t* 
                               int n_heads, int K, int decode, int64_t q_offset, float scale,
                               bf16* out, float* lse, void* ws, size_t ws_bytes, int* err,
                               cudaStream_t st);
+
+// ---- MXFP8 quantisation ------------------------------------------------------
+// codes[dst(i), :d] / scales[dst(i), :d/group] of bf16 rows x[i, :d] (row pitch ld_x).
+cudaError_t launch_mxfp8_quantize(const bf16* x, int64_t n_rows, int d, int64_t ld_x, int group,
+                                  const int64_t* dst_rows, uint8_t* codes, uint8_t* scales,
+                                  cudaStream_t st);
 
 // Diagnostic random-row gather (probe_gather.cu).
 cudaError_t launch_probe_gather(const void* base, int64_t row_pitch, int64_t n_src_rows,

@@ -166,6 +166,34 @@ def test_probe_gather_validation(L):
     assert P(FAKE, 1152, 10, FAKE, 0, 640, 1, None) == binding.DSI_OK
 
 
+def test_mxfp8_validation(L):
+    """Host checks of the MXFP8 quantiser and of MXFP8 key caches."""
+    E, U = binding.DSI_ERR_INVALID_ARG, binding.DSI_ERR_UNSUPPORTED
+    Q = L.dsi_mxfp8_quantize
+    assert Q(None, 4, 128, 128, 32, None, FAKE, FAKE, None) == E
+    assert Q(FAKE, 4, 128, 128, 32, None, None, FAKE, None) == E
+    assert Q(FAKE, 4, 128, 128, 32, None, FAKE, None, None) == E
+    assert Q(FAKE, -1, 128, 128, 32, None, FAKE, FAKE, None) == E
+    assert Q(FAKE, 4, 128, 128, 16, None, FAKE, FAKE, None) == U     # group size
+    assert Q(FAKE, 4, 96, 96, 64, None, FAKE, FAKE, None) == U       # d not a multiple of group
+    assert Q(FAKE, 4, 128, 120, 32, None, FAKE, FAKE, None) == E     # ld_x < d
+    assert Q(FAKE, 4, 128, 132, 32, None, FAKE, FAKE, None) == E     # ld_x not a multiple of 8
+    assert Q(FAKE + 8, 4, 128, 128, 32, None, FAKE, FAKE, None) == E
+    assert Q(FAKE, 4, 128, 128, 32, None, FAKE + 4, FAKE, None) == E
+    assert Q(FAKE, 0, 128, 128, 32, None, FAKE, FAKE, None) == binding.DSI_OK
+    mx = dict(k_dtype=binding.DSI_MXFP8_E4M3, k_scale=FAKE)
+    assert _score(L, _cache(k_dtype=binding.DSI_MXFP8_E4M3)) == E          # no scales
+    assert _score(L, _cache(**mx, k_group=48)) == U
+    assert _score(L, _cache(**dict(mx, k_scale=FAKE + 4))) == E            # misaligned scales
+    assert _score(L, _cache(**mx, d=96, k_group=64)) == U
+    # MXFP8 keys only on the tensor-core shape (64 heads x 128 dims)
+    assert _score(L, _cache(**mx), heads=32) == U
+    c = _cache(**mx)
+    args = [FAKE, FAKE, FAKE, ctypes.byref(c), 4, 32, 128, 2048, 0, 0.04, 1, None, None, FAKE,
+            None]
+    assert L.dsi_indexed_attention(*args, FAKE, 1 << 40, None) == U
+
+
 def test_topk_validation(L):
     E, U = binding.DSI_ERR_INVALID_ARG, binding.DSI_ERR_UNSUPPORTED
     assert L.dsi_topk(None, 16, 2, None, 0, 4, FAKE, None, None) == E
