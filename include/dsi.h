@@ -110,9 +110,10 @@ typedef struct dsi_cache {
  * dequantised key (code * 2^(byte-127) group by group, k_scale_s = 1) and
  * the index query is MXFP8-quantised on the fly with the same group size (see
  * dsi_mxfp8_quantize) and dequantised; MXFP8 keys need n_heads_idx == 64,
- * d == 128, a paged page_size that is a multiple of 64 or a contiguous s_max
- * that is a multiple of 4, and a 16-byte aligned k_scale (else
- * DSI_ERR_UNSUPPORTED / DSI_ERR_INVALID_ARG).
+ * d == 128, a 16-byte aligned k_scale, and either a paged page_size that is a
+ * multiple of 64 or a contiguous s_max (and batch * s_max) that is a multiple
+ * of 4, 8 or 16 for k_group 32, 64 or 128 (else DSI_ERR_UNSUPPORTED /
+ * DSI_ERR_INVALID_ARG).
  *   q_idx   bf16 [rows, n_heads_idx, d]
  *   w       fp32 [rows, n_heads_idx] head weights per query token
  *   cache   see above; decode: rows == batch

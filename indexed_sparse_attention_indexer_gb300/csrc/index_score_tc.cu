@@ -25,9 +25,9 @@
 //
 // MXFP8 keys (E4M3 codes, one E8M0 scale per group of 32, 64 or 128
 // elements; "Day 0 Inference Support...", "A Layered Strategy"): the producer
-// lands the codes by TMA and each tile's group scales by cp.async, extra
-// dequantising warps turn them into the exact bf16 values code * 2^X in a
-// swizzled A tile, and the bf16 MMA runs on that; the index queries are
+// lands the codes and each tile's group scales by TMA, extra dequantising
+// warps turn them into the exact bf16 values code * 2^X in a swizzled A tile
+// (three tiles in flight), and the bf16 MMA runs on that; the index queries are
 // MXFP8-quantised group by group on the fly and stored dequantised the same
 // way.  The tensor core thus sums exactly the products of the dequantised
 // operands (what a block-scaled MMA computes) while HBM carries one byte per
@@ -59,12 +59,18 @@ struct Cfg {
   static constexpr int A_BYTES = kTileM * kD * EB;        // one MMA A tile: 16 or 32 KB
   static constexpr int ST_BYTES = K8 ? kTileM * kD : A_BYTES;   // one TMA stage of keys
   static constexpr int B_BYTES = N * kD * EB;
-  static constexpr int STAGES = FP8 ? 8 : MX ? (NT == 1 ? 6 : NT == 2 ? 4 : 2) : (NT == 1 ? 4 : 2);
-  static constexpr int ABUFS = MX ? (NT == 4 ? 1 : 2) : 0;      // dequantised bf16 A tiles
-  static constexpr int DQ_WARPS = MX ? (NT == 1 ? 4 : 2) : 0;   // dequantising warps
+  static constexpr int STAGES = FP8 ? 8 : MX ? (NT == 1 ? 5 : NT == 2 ? 4 : 2) : (NT == 1 ? 4 : 2);
+  static constexpr int ABUFS = MX ? (NT == 1 ? 3 : NT == 2 ? 2 : 1) : 0;   // dequantised bf16 A tiles
+  static constexpr int DQ_WARPS = MX ? (NT == 1 ? 8 : 2) : 0;   // dequantising warps
   static constexpr int DQ_THREADS = DQ_WARPS * 32;
-  static constexpr int DQ_ROWS = MX ? kTileM / DQ_THREADS : 0;  // tile rows per such thread
-  static constexpr int SC_BYTES = kTileM * 4;             // one stage's group scales (<= 4 per key)
+  // a dequantising thread converts DQ_UPP 16-code units of each of DQ_PASSES
+  // tile rows per tile (the 32 rows of one warp are consecutive)
+  static constexpr int DQ_PASSES = MX ? (DQ_THREADS >= kTileM ? 1 : kTileM / DQ_THREADS) : 0;
+  static constexpr int DQ_UPP = MX ? (DQ_THREADS >= kTileM ? 8 * kTileM / DQ_THREADS : 8) : 0;
+  // one stage's group scales: two 64-key sub-tiles of <= 256 bytes, each at a
+  // 256-byte slot (TMA destinations are 128-byte aligned)
+  static constexpr int SC_SUB = 256;
+  static constexpr int SC_BYTES = 2 * SC_SUB;
   static constexpr int EPI_WARPS = NT == 1 ? 4 : 8;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int THREADS = 64 + EPI_THREADS + DQ_THREADS;
@@ -152,7 +158,7 @@ struct ItemIter {
 template <int NT, int KK>
 __global__ void __launch_bounds__(Cfg<NT, KK>::THREADS, 1)
 score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-         CacheView c, ScoreArgs a, int* err) {
+         const __grid_constant__ CUtensorMap smap, CacheView c, ScoreArgs a, int* err) {
   using C = Cfg<NT, KK>;
   constexpr bool FP8 = C::FP8;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -193,10 +199,9 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     if (tid == 0) prefix[G] = total;
   }
   if (tid == 0) {
-    // MXFP8: a stage is full after the producer's byte count and one cp.async
-    // arrival per producer lane, and empty after every dequantising warp
+    // MXFP8: a stage is empty once every dequantising warp has read it
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], C::MX ? 1 + 32 : 1);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], C::MX ? C::DQ_WARPS : 1);
     }
     for (int i = 0; i < C::ABUFS; ++i) { mbar_init(&a_full[i], C::DQ_WARPS); mbar_init(&a_empty[i], 1); }
@@ -230,7 +235,11 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     bool issued[C::STAGES];
 #pragma unroll
     for (int s = 0; s < C::STAGES; ++s) { issued[s] = false; issued_phase[s] = 0; }
-    if (lane == 0) { prefetch_tmap(&kmap); if (!C::K8) prefetch_tmap(&qmap); }
+    if (lane == 0) {
+      prefetch_tmap(&kmap);
+      if (!C::K8) prefetch_tmap(&qmap);
+      if (C::MX) prefetch_tmap(&smap);
+    }
     // lane 0's reading of the flag decides for the warp, so all lanes leave together
     while (it.valid() && !__shfl_sync(0xffffffffu, (int)*abort_flag, 0)) {
       const int g = it.g, j = it.j;
@@ -324,27 +333,27 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       }
       // ---- one key tile -----------------------------------------------------
       bool ok = true;
-      if (C::MX) {
-        ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, err);   // every lane copies
-      } else {
-        if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, err);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-      }
+      if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      const int64_t p0 = (int64_t)j * kTileM;
-      int64_t prow[2] = {-1, -1};
-      int64_t nvis = 0;
       if (lane == 0) {
         const int b = seq_of_row(c, g * NT, a.decode);
-        nvis = group_visible<NT>(c, a, g);
+        const int64_t nvis = group_visible<NT>(c, a, g);
+        const int64_t p0 = (int64_t)j * kTileM;
+        int64_t prow[2];
         int nsub = 0;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const int64_t p = p0 + i * kSub;
+          prow[i] = -1;
           if (p < nvis) { prow[i] = phys_row(c, b, p, err); if (prow[i] >= 0) ++nsub; }
         }
+        // MXFP8: the sub-tile's 64 keys' group scales (64 * 128/G bytes) ride
+        // along, from a map that views the scale array as rows of 16 bytes
+        const int spr = kD >> a.lg_group;
         uint8_t* as = smem + C::OFF_A + stage * C::ST_BYTES;
-        mbar_arrive_expect_tx(&full[stage], (uint32_t)(nsub * (C::ST_BYTES / 2)));
+        mbar_arrive_expect_tx(&full[stage], (uint32_t)(nsub * (C::ST_BYTES / 2 +
+                                                                (C::MX ? kSub * spr : 0))));
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (prow[i] < 0) continue;
@@ -354,30 +363,12 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
             tma_load_2d(as + i * (kSub * 128), &kmap, 0, (int)prow[i], &full[stage]);
             tma_load_2d(as + 16384 + i * (kSub * 128), &kmap, 64, (int)prow[i], &full[stage]);
           }
+          if (C::MX)
+            tma_load_2d(smem + C::OFF_SC + stage * C::SC_BYTES + i * C::SC_SUB, &smap, 0,
+                        (int)(prow[i] * spr / 16), &full[stage]);
         }
         issued[stage] = true;
         issued_phase[stage] = phase;
-      }
-      if (C::MX) {
-        // the tile's group scales: lane l copies those of rows 4l .. 4l+3
-        // (4 * 128/G contiguous bytes of one sub-tile's rows); its arrival
-        // on full[stage] fires once the copy has landed.  Only pieces that
-        // start at a visible position are read, and those end inside the
-        // page (paged) or inside the sequence's rows (s_max % 4 == 0).
-        const int64_t pr0 = __shfl_sync(0xffffffffu, prow[0], 0);
-        const int64_t pr1 = __shfl_sync(0xffffffffu, prow[1], 0);
-        nvis = __shfl_sync(0xffffffffu, nvis, 0);
-        const int t = lane * 4;
-        const int64_t pr = t < kSub ? pr0 : pr1;
-        if (pr >= 0 && p0 + t < nvis) {
-          const int spr = kD >> a.lg_group;          // scale bytes per key: 4, 2 or 1
-          const uint8_t* src = c.k_mx_scale + (pr + (t & (kSub - 1))) * spr;
-          const uint32_t dst = smem_u32(smem + C::OFF_SC + stage * C::SC_BYTES + t * spr);
-          if (spr == 4) cp_async_16(dst, src);
-          else if (spr == 2) cp_async_8(dst, src);
-          else cp_async_4(dst, src);
-        }
-        cp_async_mbar_arrive_noinc(&full[stage]);
       }
       if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
       it.next();
@@ -444,8 +435,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     __syncwarp();
   } else if (C::MX && warp >= 2 + C::EPI_WARPS) {
     // ======================= dequantisation (MXFP8 keys) ======================
-    // E4M3 codes of a landed stage -> bf16 code * 2^X in a swizzled A tile,
-    // one tile row (128 codes, 128/G scales) per thread and pass
+    // E4M3 codes of a landed stage -> bf16 code * 2^X in a swizzled A tile
     const int dt = tid - (64 + C::EPI_THREADS);
     ItemIter it;
     it.init(prefix, a.groups, it_begin, it_end);
@@ -460,12 +450,19 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       const uint8_t* sc = smem + C::OFF_SC + stage * C::SC_BYTES;
       uint8_t* dst = smem + C::OFF_ABF + xb * C::A_BYTES;
 #pragma unroll
-      for (int rr = 0; rr < C::DQ_ROWS; ++rr) {
-        const int t = dt + rr * C::DQ_THREADS;
+      for (int rp = 0; rp < C::DQ_PASSES; ++rp) {
+        const int t = (dt & (kTileM - 1)) + rp * C::DQ_THREADS;
+        const int u0 = C::DQ_THREADS >= kTileM ? (dt >> 7) * C::DQ_UPP : 0;
+        // the row's scale bytes (spr of them, little-endian in one word)
+        const uint8_t* srow = sc + (t >> 6) * C::SC_SUB + (t & (kSub - 1)) * spr;
+        const uint32_t sw = spr == 4   ? *reinterpret_cast<const uint32_t*>(srow)
+                            : spr == 2 ? *reinterpret_cast<const uint16_t*>(srow)
+                                       : *srow;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int k = 0; k < C::DQ_UPP; ++k) {
+          const int u = u0 + k;
           const uint4 v = *reinterpret_cast<const uint4*>(src + sw128_offset(t, u));
-          const int X = (int)sc[t * spr + ((u * 16) >> lg)] - 127;
+          const int X = (int)((sw >> (8 * ((u * 16) >> lg))) & 255u) - 127;
           uint4 lo, hi;
           mx_decode16(v, X, lo, hi);
           uint8_t* blk = dst + (u >> 2) * 16384;
@@ -563,8 +560,16 @@ cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, 
   using C = Cfg<NT, KK>;
   const uint64_t krows = c.block_table ? (uint64_t)c.num_pages * c.page_size
                                        : (uint64_t)c.batch * c.s_max;
-  CUtensorMap kmap, qmap;
+  CUtensorMap kmap, qmap, smap;
   memset(&qmap, 0, sizeof(qmap));
+  memset(&smap, 0, sizeof(smap));
+  const int spr = c.k_group == 128 ? 1 : c.k_group == 64 ? 2 : 4;   // MXFP8 scale bytes per key
+  if (C::MX) {
+    // the scale array as rows of 16 bytes; one box = one 64-key sub-tile
+    if (!tma_map_2d(&smap, c.k_mx_scale, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, krows * spr / 16, 16,
+                    16, kSub * spr / 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  }
   if (C::K8) {
     if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, krows, kD, 128, kSub))
       return cudaErrorInvalidValue;
@@ -592,7 +597,7 @@ cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, 
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   cudaError_t le = launch_overlapped(score_tc<NT, KK>, dim3(sms), dim3(C::THREADS), C::SMEM,
-                                     st, kmap, qmap, c, a, err);
+                                     st, kmap, qmap, smap, c, a, err);
   note_launch();
   return le;
 }
@@ -620,10 +625,13 @@ bool tc_score_supported(const CacheView& c, int H) {
   if (krows >= (1ull << 31)) return false;
   if ((reinterpret_cast<uintptr_t>(c.k_idx) & 15) != 0) return false;
   if (c.k_dtype == DSI_MXFP8_E4M3) {
-    // the scale copies move 4-key pieces that must stay inside a sequence's rows
+    // the scales are copied as rows of 16 bytes, 64 keys at a time: a
+    // sequence's (contiguous) or page's first key must start such a row
     if (!c.k_mx_scale || (reinterpret_cast<uintptr_t>(c.k_mx_scale) & 15) != 0) return false;
     if (c.k_group != 32 && c.k_group != 64 && c.k_group != 128) return false;
-    if (!c.block_table && c.s_max % 4 != 0) return false;
+    const int per16 = 16 / (kD / c.k_group);             // keys per 16 bytes of scales
+    if (!c.block_table && c.s_max % per16 != 0) return false;
+    if (krows % per16 != 0) return false;
   }
   return tma_encode_fn() != nullptr;
 }

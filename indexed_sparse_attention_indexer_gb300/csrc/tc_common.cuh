@@ -192,18 +192,6 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void cp_async_16(uint32_t saddr, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(saddr), "l"(gmem) : "memory");
 }
-__device__ __forceinline__ void cp_async_8(uint32_t saddr, const void* gmem) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(saddr), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_4(uint32_t saddr, const void* gmem) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(saddr), "l"(gmem) : "memory");
-}
-// Arrive on `bar` once this thread's earlier cp.async copies have landed; the
-// arrival counts against the barrier's expected count (no pending increment).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar))
-               : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }

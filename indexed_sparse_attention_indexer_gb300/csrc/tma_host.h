@@ -22,9 +22,11 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tma_encode_fn() {
   return fn;
 }
 
-// 2D map over a row-major [rows, cols] array, box [box_rows, box_cols], 128-byte swizzle.
+// 2D map over a row-major [rows, cols] array, box [box_rows, box_cols],
+// 128-byte swizzle unless stated otherwise.
 inline bool tma_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
-                       uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
+                       uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
+                       CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tma_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -32,7 +34,7 @@ inline bool tma_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt,
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

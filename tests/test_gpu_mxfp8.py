@@ -74,7 +74,7 @@ def test_quantize_appends_into_cache_rows():
 MX_CASES = {
     # name: (lengths, tokens per sequence, K, H, page size, group)
     "contig_g32": ([700, 132, 64, 1000], 1, 64, 128, 0, 32),
-    "contig_ragged_tiles_g64": ([4100, 128, 2052], 1, 256, 128, 0, 64),
+    "contig_ragged_tiles_g64": ([4104, 128, 2052], 1, 256, 128, 0, 64),
     "paged_g32": ([1100, 300, 65, 2], 1, 128, 128, 64, 32),
     "paged_g128_page128": ([1000, 128, 301], 1, 200, 128, 128, 128),
     "zero_length_g32": ([100, 0, 8], 1, 16, 128, 0, 32),
@@ -126,7 +126,7 @@ def test_mx_decode_layer(name):
 def test_mx_prefill_scores_and_layer(group):
     """Causal prefill with MXFP8 keys (groups of 4 query tokens per tile pass),
     with an offset so that rows start mid-cache."""
-    ws = W.make_prefill(70, 600, 64, 128, 64, 16, seed=group, q_offset=500, k_mx_group=group)
+    ws = W.make_prefill(70, 608, 64, 128, 64, 16, seed=group, q_offset=500, k_mx_group=group)
     g = ws.to(DEV)
     cache = binding.Cache.of(g)
     scores = binding.index_score(g.q_idx, g.w, cache, False, ws.q_offset)
@@ -196,9 +196,10 @@ def test_mx_append_then_score_matches_oracle_quantisation():
         assert np.allclose(got, ref, rtol=1e-5, atol=1e-5 * np.abs(ref).max()), b
 
 
-def test_mx_contiguous_needs_s_max_multiple_of_4():
-    """A contiguous MXFP8 cache whose rows per sequence are not a multiple of 4
-    is refused on the host (nothing launched)."""
+def test_mx_contiguous_needs_aligned_s_max():
+    """A contiguous MXFP8 cache whose rows per sequence do not start a 16-byte
+    row of scales (s_max a multiple of 4 for groups of 32) is refused on the
+    host (nothing launched)."""
     ws = W.make_decode(2, 0, 64, 128, 16, 16, seed=3, lengths=[10, 9], k_mx_group=32)
     g = ws.to(DEV)
     with pytest.raises(binding.DsiError) as e:
