@@ -188,10 +188,11 @@ class ClockSampler:
                 "samples": len(sm), "samples_in_timed_region": len(inside)}
 
 
+_HEADERS = ("common.cuh", "tc_common.cuh", "tma_host.h", "kernels.h")
 KERNEL_SOURCES = {
-    "index_score": ("index_score.cu", "index_score_tc.cu", "common.cuh"),
-    "index_topk_prefill": ("index_topk_prefill.cu", "tc_common.cuh", "common.cuh"),
-    "mla_tc": ("sparse_mla_tc.cu", "tc_common.cuh", "common.cuh"),
+    "index_score": ("index_score.cu", "index_score_tc.cu") + _HEADERS,
+    "index_topk_prefill": ("index_topk_prefill.cu",) + _HEADERS,
+    "mla_tc": ("sparse_mla_tc.cu",) + _HEADERS,
 }
 
 
