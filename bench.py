@@ -609,7 +609,10 @@ def run_mx_scan():
     kernel with the same G) and selected, and the selection is compared with
     the one made from bf16 scores of the unquantised keys.  Reports the Top-K
     recall, the score error, the scoring time and the quantiser's bandwidth.
-    G = 128 with 128-wide keys is one power-of-two scale per key."""
+    G = 128 with 128-wide keys is one power-of-two scale per key.  Two key
+    distributions: outlier channels (x32 on four channels), and channels whose
+    magnitudes spread over exp(U(-5, 5)) (about 2^14 between the extremes),
+    where a key's small channels fall below E4M3's range under one coarse scale."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     from indexed_sparse_attention_indexer_gb300 import binding
@@ -617,7 +620,6 @@ def run_mx_scan():
     stream = torch.cuda.current_stream()
     B, S, Hi, d, K = 64, 32768, 64, 128, 2048
     hbm, _, src = peaks()
-    keys = W.make_mx_input(B * S, d, seed=5, device=dev, special=False, row_spread=1.0)
     g = torch.Generator(device=dev)
     g.manual_seed(6)
     q_idx = torch.randn((B, Hi, d), generator=g, device=dev).to(torch.bfloat16)
@@ -625,42 +627,49 @@ def run_mx_scan():
     lens = torch.full((B,), S, dtype=torch.int32, device=dev)
     latent = torch.empty((1, 1, W.D_QK), dtype=torch.bfloat16, device=dev)   # not read here
     scores = torch.empty((B, S), dtype=torch.float32, device=dev)
-    c_bf = binding.Cache(keys.view(B, S, d), latent, lens)
-    ms_bf = time_alone(lambda: binding.index_score(q_idx, w, c_bf, True, scores=scores, ld=S,
-                                                   stream=stream), stream, 20)
-    ref = scores.clone()
-    ref_idx, _ = binding.topk(ref, K, row_len=lens)
-    mask = torch.zeros((B, S), dtype=torch.bool, device=dev)
-    mask.scatter_(1, ref_idx.to(torch.int64), True)
-    ref_mag = ref.abs().mean(dim=1, keepdim=True)
-    res = [{"group": None, "keys": "bf16", "key_bytes_per_position": 2 * d,
-            "score_ms": round(ms_bf, 4)}]
-    for G in (32, 64, 128):
-        codes = torch.empty((B * S, d), dtype=torch.float8_e4m3fn, device=dev)
-        sc = torch.empty((B * S, d // G), dtype=torch.uint8, device=dev)
-        q_ms = time_alone(lambda: binding.mxfp8_quantize(keys, G, codes=codes, scales=sc,
-                                                         stream=stream), stream, 20)
-        qbytes = B * S * (2 * d + d + d // G)
-        c_mx = binding.Cache(codes.view(B, S, d), latent, lens, k_scale=sc.view(B, S, d // G))
-        ms = time_alone(lambda: binding.index_score(q_idx, w, c_mx, True, scores=scores, ld=S,
-                                                    stream=stream), stream, 20)
-        idx, _ = binding.topk(scores, K, row_len=lens)
-        hits = mask.gather(1, idx.to(torch.int64)).sum(dim=1).float() / K
-        err = ((scores - ref).abs() / ref_mag).flatten()
-        res.append({"group": G, "keys": "mxfp8", "key_bytes_per_position": d + d // G,
-                    "topk_recall_vs_bf16": round(float(hits.mean()), 5),
-                    "topk_recall_min_row": round(float(hits.min()), 5),
-                    "score_err_rel_mean_abs_median": float(err.median()),
-                    "score_err_rel_mean_abs_max": float(err.max()),
-                    "score_ms": round(ms, 4),
-                    "quantize_ms": round(q_ms, 4),
-                    "quantize_gbs": round(qbytes / (q_ms / 1e3) / 1e9, 1),
-                    "quantize_hbm_frac": round(qbytes / (q_ms / 1e3) / 1e9 / hbm, 4)})
-        del codes, sc, c_mx
+    res = []
+    for dist_name, spread in (("outlier channels x32", 0.0), ("channel magnitudes exp(U(-5,5))", 5.0)):
+        keys = W.make_mx_input(B * S, d, seed=5, device=dev, special=False, row_spread=1.0,
+                               channel_spread=spread)
+        c_bf = binding.Cache(keys.view(B, S, d), latent, lens)
+        ms_bf = time_alone(lambda: binding.index_score(q_idx, w, c_bf, True, scores=scores, ld=S,
+                                                       stream=stream), stream, 20)
+        ref = scores.clone()
+        ref_idx, _ = binding.topk(ref, K, row_len=lens)
+        mask = torch.zeros((B, S), dtype=torch.bool, device=dev)
+        mask.scatter_(1, ref_idx.to(torch.int64), True)
+        ref_mag = ref.abs().mean(dim=1, keepdim=True)
+        res.append({"keys_dist": dist_name, "group": None, "keys": "bf16",
+                    "key_bytes_per_position": 2 * d, "score_ms": round(ms_bf, 4)})
+        for G in (32, 64, 128):
+            codes = torch.empty((B * S, d), dtype=torch.float8_e4m3fn, device=dev)
+            sc = torch.empty((B * S, d // G), dtype=torch.uint8, device=dev)
+            q_ms = time_alone(lambda: binding.mxfp8_quantize(keys, G, codes=codes, scales=sc,
+                                                             stream=stream), stream, 20)
+            qbytes = B * S * (2 * d + d + d // G)
+            c_mx = binding.Cache(codes.view(B, S, d), latent, lens, k_scale=sc.view(B, S, d // G))
+            ms = time_alone(lambda: binding.index_score(q_idx, w, c_mx, True, scores=scores, ld=S,
+                                                        stream=stream), stream, 20)
+            idx, _ = binding.topk(scores, K, row_len=lens)
+            hits = mask.gather(1, idx.to(torch.int64)).sum(dim=1).float() / K
+            err = ((scores - ref).abs() / ref_mag).flatten()
+            res.append({"keys_dist": dist_name, "group": G, "keys": "mxfp8",
+                        "key_bytes_per_position": d + d // G,
+                        "topk_recall_vs_bf16": round(float(hits.mean()), 5),
+                        "topk_recall_min_row": round(float(hits.min()), 5),
+                        "score_err_rel_mean_abs_median": float(err.median()),
+                        "score_err_rel_mean_abs_max": float(err.max()),
+                        "score_ms": round(ms, 4),
+                        "quantize_ms": round(q_ms, 4),
+                        "quantize_gbs": round(qbytes / (q_ms / 1e3) / 1e9, 1),
+                        "quantize_hbm_frac": round(qbytes / (q_ms / 1e3) / 1e9 / hbm, 4)})
+            del codes, sc, c_mx
+        del keys, c_bf
+        torch.cuda.empty_cache()
     print(json.dumps({"probe": "mxfp8_group_scan", "batch": B, "history": S,
                       "indexer": f"{Hi}x{d}", "topk": K, "peak_source": src,
-                      "keys": "bf16 N(0,1) x exp(U(-1,1)) per row, 4 outlier channels x32",
-                      "results": res}))
+                      "keys": "bf16 N(0,1) x exp(U(-1,1)) per row, then per-channel scaling",
+                      "queries": "N(0,1) bf16", "results": res}))
 
 
 def run_gather_ceiling():

@@ -23,7 +23,8 @@ measured on):
 * inputs of the MXFP8 quantiser: bf16 normal rows with a per-row magnitude
   exp(U(-8, 8)), four outlier channels x32, and special rows (all zero, bf16
   subnormals, magnitudes near 2^120, exact powers of two, group maxima with
-  mantissa 1.875 that saturate at 448).
+  mantissa 1.875 that saturate at 448); the group-size scan also uses rows
+  whose channels carry their own magnitudes exp(U(-5, 5)).
 * head weights ``w``: uniform [0,1) rounded down to a multiple of 2^-7, so that
   every partial sum of ``w_h * relu(u_h)`` is a multiple of 2^-7 below 2^24
   and hence exact in fp32 whatever the order.
@@ -277,9 +278,11 @@ def make_prefill(T: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0
 
 
 def make_mx_input(n: int, d: int, seed: int = 0, device="cpu", special: bool = True,
-                  row_spread: float = 8.0) -> torch.Tensor:
+                  row_spread: float = 8.0, channel_spread: float = 0.0) -> torch.Tensor:
     """bf16 rows [n, d] for the MXFP8 quantiser: normal values with a per-row
-    magnitude exp(U(-row_spread, row_spread)) and four outlier channels x32;
+    magnitude exp(U(-row_spread, row_spread)) and four outlier channels x32
+    (with ``channel_spread`` > 0 every channel is scaled instead by its own
+    exp(U(-channel_spread, channel_spread)), drawn after the outlier channels);
     with ``special`` and n >= 8 the first rows are special: all zero, bf16
     subnormals, magnitudes near 2^120, exact powers of two, and groups whose
     largest magnitude has mantissa 1.875 (they saturate at 448 after scaling)."""
@@ -290,6 +293,9 @@ def make_mx_input(n: int, d: int, seed: int = 0, device="cpu", special: bool = T
     ch = torch.randperm(d, generator=g, device=device)[:4]
     boost = torch.ones(d, device=device)
     boost[ch] = 32.0
+    if channel_spread > 0:
+        boost = torch.exp(torch.empty(d, device=device).uniform_(-channel_spread, channel_spread,
+                                                                  generator=g))
     step = max(1, _CHUNK // max(1, d))
     for s in range(0, n, step):
         e = min(n, s + step)
