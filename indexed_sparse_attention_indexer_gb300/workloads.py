@@ -25,6 +25,11 @@ measured on):
   subnormals, magnitudes near 2^120, exact powers of two, group maxima with
   mantissa 1.875 that saturate at 448); the group-size scan also uses rows
   whose channels carry their own magnitudes exp(U(-5, 5)).
+* FP8 latent cache (the quantised KV cache variant): E4M3 codes drawn as
+  bytes with a random sign, exponent field uniform in {4..10} and mantissa
+  uniform in {0..7} (magnitudes 1/8 .. 15), and one fp32 scale per position
+  and tile of 128 dims (5 tiles: the rope dims are the fifth) uniform in
+  [0.02, 0.2); drawn where the bf16 latent would be, codes then scales.
 * head weights ``w``: uniform [0,1) rounded down to a multiple of 2^-7, so that
   every partial sum of ``w_h * relu(u_h)`` is a multiple of 2^-7 below 2^24
   and hence exact in fp32 whatever the order.
@@ -84,6 +89,7 @@ class Workload:
     page_size: int = 0
     q_offset: int = 0
     meta: dict = field(default_factory=dict)
+    latent_scale: Optional[torch.Tensor] = None   # FP8 latent: fp32 [..., 5] tile scales
 
     @property
     def T(self) -> int:
@@ -115,12 +121,12 @@ class Workload:
         return Workload(self.name, self.mode, self.H_i, self.d, self.K, self.H, self.scale,
                         mv(self.q_idx), mv(self.w), mv(self.q), mv(self.k_idx), mv(self.k_scale),
                         mv(self.latent), mv(self.seq_lens), mv(self.block_table),
-                        self.page_size, self.q_offset, dict(self.meta))
+                        self.page_size, self.q_offset, dict(self.meta), mv(self.latent_scale))
 
     def input_bytes(self) -> int:
         n = 0
         for x in (self.q_idx, self.w, self.q, self.k_idx, self.k_scale, self.latent,
-                  self.seq_lens, self.block_table):
+                  self.latent_scale, self.seq_lens, self.block_table):
             if x is not None:
                 n += x.numel() * x.element_size()
         return n
@@ -182,6 +188,28 @@ def _e8m0_bytes(shape, g, device, lo: int = 125, hi: int = 127) -> torch.Tensor:
     return torch.randint(lo, hi + 1, shape, generator=g, device=device).to(torch.uint8)
 
 
+LATENT_TILES = 5   # tiles of 128 dims per latent row; the 64 rope dims are the fifth
+
+
+def _latent_fp8(shape, g, device):
+    """E4M3 latent codes [*shape, 576] (as bytes, viewed as float8) and fp32
+    tile scales [*shape, 5]."""
+    n = 1
+    for v in shape:
+        n *= v
+    out = torch.empty((n * D_QK,), dtype=torch.uint8, device=device)
+    for s in range(0, n * D_QK, _CHUNK):
+        e = min(n * D_QK, s + _CHUNK)
+        sign = torch.randint(0, 2, (e - s,), generator=g, device=device)
+        expo = torch.randint(4, 11, (e - s,), generator=g, device=device)
+        mant = torch.randint(0, 8, (e - s,), generator=g, device=device)
+        out[s:e] = (sign * 128 + expo * 8 + mant).to(torch.uint8)
+    codes = out.view(tuple(shape) + (D_QK,)).view(torch.float8_e4m3fn)
+    scales = torch.empty(tuple(shape) + (LATENT_TILES,), dtype=torch.float32,
+                         device=device).uniform_(0.02, 0.2, generator=g)
+    return codes, scales
+
+
 def loguniform_lengths(B: int, lo: int, hi: int, g, device) -> torch.Tensor:
     u = torch.rand(B, generator=g, device=device, dtype=torch.float64)
     L = torch.floor(torch.exp(math.log(lo) + u * (math.log(hi) - math.log(lo))))
@@ -197,7 +225,8 @@ def make_decode(B: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
                 loguniform: Optional[tuple] = None, page_size: int = 0,
                 k_fp8: bool = False, scale: Optional[float] = None,
                 q_std: Optional[float] = None, name: str = "decode",
-                tokens_per_seq: int = 1, k_mx_group: int = 0) -> Workload:
+                tokens_per_seq: int = 1, k_mx_group: int = 0,
+                latent_fp8: bool = False) -> Workload:
     """Decode batch: one query token per sequence, or ``tokens_per_seq`` (T)
     candidate tokens per sequence for a multi-token step (query rows come T to
     a sequence; the candidates' keys are the last T positions of its history).
@@ -206,7 +235,8 @@ def make_decode(B: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
     or ``loguniform=(lo, hi)`` draws them.  ``page_size > 0`` stores the caches
     as page pools behind a randomly permuted block table.  ``k_mx_group > 0``
     stores the index keys as MXFP8 (E4M3 codes, one E8M0 byte per group of
-    that many elements in ``k_scale``).
+    that many elements in ``k_scale``); ``latent_fp8`` stores the latent cache
+    as E4M3 codes with per-tile fp32 scales (``latent_scale``).
     """
     R = B * tokens_per_seq
     g = _gen(seed, device)
@@ -235,7 +265,11 @@ def make_decode(B: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
     w = _weights((R, H_i), g, device)
     std = (1.0 / math.sqrt(D_QK)) if q_std is None else q_std
     q = _normal_bf16((R, H, D_QK), g, device, std)
-    latent = _normal_bf16(rows_shape + (D_QK,), g, device)
+    latent_scale = None
+    if latent_fp8:
+        latent, latent_scale = _latent_fp8(rows_shape, g, device)
+    else:
+        latent = _normal_bf16(rows_shape + (D_QK,), g, device)
     block_table = None
     if page_size > 0:
         perm = torch.randperm(n_pages, generator=g, device=device).to(torch.int32).cpu()
@@ -250,13 +284,14 @@ def make_decode(B: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
                     scale=(1.0 / math.sqrt(D_QK)) if scale is None else scale,
                     q_idx=q_idx, w=w, q=q, k_idx=k_idx, k_scale=k_scale, latent=latent,
                     seq_lens=L.to(device), block_table=block_table, page_size=page_size,
-                    meta={"tokens_per_seq": tokens_per_seq} if tokens_per_seq != 1 else {})
+                    meta={"tokens_per_seq": tokens_per_seq} if tokens_per_seq != 1 else {},
+                    latent_scale=latent_scale)
 
 
 def make_prefill(T: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0,
                  device="cpu", q_offset: int = 0, scale: Optional[float] = None,
                  q_std: Optional[float] = None, name: str = "prefill",
-                 k_mx_group: int = 0) -> Workload:
+                 k_mx_group: int = 0, latent_fp8: bool = False) -> Workload:
     """Causal prefill of one sequence: query tokens q_offset .. q_offset+T-1
     against a cache of S >= q_offset+T rows, all from one generator
     (``k_mx_group``: MXFP8 index keys as in ``make_decode``)."""
@@ -269,12 +304,16 @@ def make_prefill(T: int, S: int, H_i: int, d: int, K: int, H: int, seed: int = 0
     w = _weights((T, H_i), g, device)
     std = (1.0 / math.sqrt(D_QK)) if q_std is None else q_std
     q = _normal_bf16((T, H, D_QK), g, device, std)
-    latent = _normal_bf16((1, S, D_QK), g, device)
+    latent_scale = None
+    if latent_fp8:
+        latent, latent_scale = _latent_fp8((1, S), g, device)
+    else:
+        latent = _normal_bf16((1, S, D_QK), g, device)
     return Workload(name=name, mode="prefill", H_i=H_i, d=d, K=K, H=H,
                     scale=(1.0 / math.sqrt(D_QK)) if scale is None else scale,
                     q_idx=q_idx, w=w, q=q, k_idx=k_idx, k_scale=k_scale, latent=latent,
                     seq_lens=torch.tensor([S], dtype=torch.int32, device=device),
-                    q_offset=q_offset)
+                    q_offset=q_offset, latent_scale=latent_scale)
 
 
 def make_mx_input(n: int, d: int, seed: int = 0, device="cpu", special: bool = True,
@@ -368,20 +407,26 @@ CONFIGS = {
 
 
 def make_config(cfg: int, device="cpu", chunk: int = 0, rows: int | None = None,
-                tokens_per_seq: int = 1, k_mx_group: int = 0) -> Workload:
+                tokens_per_seq: int = 1, k_mx_group: int = 0,
+                latent_fp8: bool = False) -> Workload:
     """The named workload; ``rows`` shrinks a decode batch (same shapes per
     sequence, fewer sequences) for profiling captures that must stay small;
     ``tokens_per_seq`` turns a decode workload into a multi-token step;
-    ``k_mx_group`` stores the 64x128-head decode workload's index keys as MXFP8."""
+    ``k_mx_group`` stores the 64x128-head decode workload's index keys as MXFP8;
+    ``latent_fp8`` stores its latent cache as FP8 with per-tile scales."""
     c = CONFIGS[cfg]
     if (rows is not None or tokens_per_seq != 1) and cfg not in (1, 2, 5):
         raise ValueError("rows and tokens_per_seq apply to the decode workloads only")
-    if k_mx_group and cfg != 2:
-        raise ValueError("MXFP8 keys apply to the 64x128-head contiguous decode workload only")
+    if (k_mx_group or latent_fp8) and cfg != 2:
+        raise ValueError("MXFP8 keys and the FP8 latent cache apply to the 64x128-head "
+                         "contiguous decode workload only")
     if cfg in (1, 2):
         return make_decode(rows or c["B"], c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
-                           device=device, name=c["name"] + ("-mxfp8" if k_mx_group else ""),
-                           tokens_per_seq=tokens_per_seq, k_mx_group=k_mx_group)
+                           device=device,
+                           name=c["name"] + ("-mxfp8" if k_mx_group else "")
+                           + ("-fp8latent" if latent_fp8 else ""),
+                           tokens_per_seq=tokens_per_seq, k_mx_group=k_mx_group,
+                           latent_fp8=latent_fp8)
     if cfg == 3:
         return make_prefill(c["T"], c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
                             device=device, name=c["name"])

@@ -37,6 +37,9 @@ Readings where the pages are silent (each also listed in the design notes):
   natural-log log-sum-exp of the scaled logits.
 * Decode row b sees positions 0..seq_lens[b]-1 (the new token's key is already
   in the cache); prefill token t at position q_offset+t sees 0..q_offset+t.
+* FP8 latent cache: E4M3 codes with one fp32 scale per token and tile of 128
+  dims (the 64 rope dims form a fifth tile); scale = tile max / 448 in fp32,
+  code = nearest E4M3 of x / scale in fp32; the oracle attends over code * scale.
 
 Every function is pinned by the CPU tests to closed forms, brute force and
 textbook routines (exact rational arithmetic, a rank-count definition of the
@@ -202,6 +205,46 @@ def dense_mla(q, rows, scale: float, d_v: int = D_V):
 
 
 # ----------------------------------------------------------------------------
+# FP8 latent cache ("Day 0 Inference Support for New LLM Architectures:
+# Optimization Practices", "A Layered Strategy": the KV cache in FP8 with one
+# scale per token and head tile of 128 elements).  The latent row (one MLA
+# "head") splits into tiles of 128: dims 0-127, 128-255, 256-383, 384-511, and
+# the 64 rope dims 512-575 as a fifth tile.  Reading: the scale of a tile is
+# its largest magnitude over 448 (E4M3's largest normal), computed in fp32;
+# each element is x / scale computed in fp32, rounded to the nearest E4M3
+# value (ties to even); an all-zero tile has scale 0 and zero codes.
+# ----------------------------------------------------------------------------
+
+LATENT_TILES = ((0, 128), (128, 256), (256, 384), (384, 512), (512, 576))
+
+
+def latent_fp8_quantize(rows):
+    """rows [n, 576] -> (codes [n, 576] as E4M3 values in fp64, scales [n, 5]
+    holding fp32 values)."""
+    x = _f64(rows).astype(np.float32)
+    codes = np.zeros(x.shape, dtype=np.float64)
+    scales = np.zeros(x.shape[:-1] + (len(LATENT_TILES),), dtype=np.float32)
+    for t, (a, b) in enumerate(LATENT_TILES):
+        seg = x[..., a:b]
+        amax = np.abs(seg).max(axis=-1)
+        sc = (amax / np.float32(448.0)).astype(np.float32)
+        safe = np.where(sc > 0, sc, np.float32(1.0)).astype(np.float32)
+        y = np.where((sc > 0)[..., None], seg / safe[..., None], np.float32(0.0))
+        codes[..., a:b] = e4m3_round(y.astype(np.float64))
+        scales[..., t] = sc
+    return codes, scales.astype(np.float64)
+
+
+def latent_fp8_dequantize(codes, scales) -> np.ndarray:
+    """codes [n, 576] (E4M3 values) and scales [n, 5] -> code * scale, tile by tile."""
+    c = _f64(codes).copy()
+    sc = _f64(scales)
+    for t, (a, b) in enumerate(LATENT_TILES):
+        c[..., a:b] *= sc[..., t:t + 1]
+    return c
+
+
+# ----------------------------------------------------------------------------
 # cache addressing (contiguous or paged through a block table)
 # ----------------------------------------------------------------------------
 
@@ -230,6 +273,21 @@ def history_rows(cache, b: int, positions, block_table=None, page_size: int = 0)
 # one row of the whole layer
 # ----------------------------------------------------------------------------
 
+def _latent_reader(ws, b: int, bt):
+    """latent_of(positions) for sequence b: bf16 rows, or FP8 codes dequantised
+    with their tile scales."""
+    lat = ws.latent.cpu()
+    lsc = getattr(ws, "latent_scale", None)
+    lsc = None if lsc is None else lsc.cpu()
+
+    def latent_of(p):
+        rows = history_rows(lat, b, p, bt, ws.page_size)
+        if lsc is None:
+            return rows
+        return latent_fp8_dequantize(rows, history_rows(lsc, b, p, bt, ws.page_size))
+    return latent_of
+
+
 def layer_row(q_idx_t, w_t, q_t, k_hist, k_scale_hist, latent_of, n_hist: int, K: int,
               scale: float):
     """Indexer -> Top-K -> sparse MLA for one query token with n_hist visible rows.
@@ -255,9 +313,8 @@ def decode_row(ws, b: int):
     ks = None
     if ws.k_scale is not None:
         ks = history_rows(ws.k_scale.cpu(), b, pos, bt, ws.page_size)
-    lat = ws.latent.cpu()
     return layer_row(ws.q_idx[b].cpu(), ws.w[b].cpu(), ws.q[b].cpu(), k_hist, ks,
-                     lambda p: history_rows(lat, b, p, bt, ws.page_size), L, ws.K, ws.scale)
+                     _latent_reader(ws, b, bt), L, ws.K, ws.scale)
 
 
 def multi_token_row(ws, r: int, tokens_per_seq: int):
@@ -277,9 +334,8 @@ def multi_token_row(ws, r: int, tokens_per_seq: int):
     ks = None
     if ws.k_scale is not None:
         ks = history_rows(ws.k_scale.cpu(), b, pos, bt, ws.page_size)
-    lat = ws.latent.cpu()
     return layer_row(ws.q_idx[r].cpu(), ws.w[r].cpu(), ws.q[r].cpu(), k_hist, ks,
-                     lambda p: history_rows(lat, b, p, bt, ws.page_size), L, ws.K, ws.scale)
+                     _latent_reader(ws, b, bt), L, ws.K, ws.scale)
 
 
 def _rows_prefix(k_idx, n: int):
@@ -296,10 +352,8 @@ def prefill_row(ws, t: int):
     n = ws.q_offset + t + 1
     k_hist = _rows_prefix(ws.k_idx, n)
     ks = None if ws.k_scale is None else ws.k_scale[0, :n].cpu()
-    lat = ws.latent[0].cpu()
     return layer_row(ws.q_idx[t].cpu(), ws.w[t].cpu(), ws.q[t].cpu(), k_hist, ks,
-                     lambda p: lat[np.asarray(p, dtype=np.int64)] if len(p) else lat[:0],
-                     n, ws.K, ws.scale)
+                     _latent_reader(ws, 0, None), n, ws.K, ws.scale)
 
 
 def row_scores(ws, r: int) -> np.ndarray:

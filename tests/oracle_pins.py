@@ -285,6 +285,87 @@ def check_mx_scores_unit_scales(o):
     assert np.array_equal(o.index_scores(q, w, k, kb2), o.index_scores(q, w, k2))
 
 
+# ----------------------------------------------------------------------------
+# FP8 latent cache (E4M3 codes, one fp32 scale per tile of 128 dims, the rope
+# dims as a fifth tile of 64)
+# ----------------------------------------------------------------------------
+
+_TILES = ((0, 128), (128, 256), (256, 384), (384, 512), (512, 576))
+
+
+def _round_f32(v: Fraction) -> Fraction:
+    """Exact round-to-nearest-even of a rational onto the fp32 grid (no overflow)."""
+    if v == 0:
+        return Fraction(0)
+    sign = -1 if v < 0 else 1
+    a = abs(v)
+    e = max(_floor_log2(a), -126)
+    ulp = Fraction(2) ** (e - 23)
+    return sign * round(a / ulp) * ulp
+
+
+def check_latent_fp8_exact_rational(o):
+    """Tile scales and codes against exact rational arithmetic with fp32 rounding
+    of the scale and of every quotient, then nearest-E4M3 from the code table."""
+    rng = _rng(31)
+    x = (rng.standard_normal((2, 576)) * np.exp(rng.uniform(-3, 3, size=(2, 576)))).astype(np.float32)
+    x[1, 128:256] = 0.0                                    # an all-zero tile
+    codes, scales = o.latent_fp8_quantize(x)
+    for r in range(2):
+        for t, (a, b) in enumerate(_TILES):
+            seg = [Fraction(float(v)) for v in x[r, a:b]]
+            amax = max(abs(v) for v in seg)
+            sc = _round_f32(amax / 448)
+            assert Fraction(float(scales[r, t])) == sc, (r, t, scales[r, t], float(sc))
+            for j, v in enumerate(seg):
+                exp = Fraction(0) if sc == 0 else _nearest_e4m3(_round_f32(v / sc))
+                assert Fraction(float(codes[r, a + j])) == exp, (r, t, j)
+
+
+def check_latent_fp8_closed_forms(o):
+    """A tile whose largest magnitude is 448 * 2^k has scale 2^k and codes equal to
+    values already on the E4M3 grid; every tile's largest element codes to +-448;
+    tiles are the 128-dim blocks and the 64 rope dims; dequantisation error within
+    half an E4M3 step."""
+    rng = _rng(32)
+    vals = np.array(sorted({float(v) for v, _ in _e4m3_table()}))
+    grid = rng.choice(vals, size=(1, 576))
+    for t, (a, b) in enumerate(_TILES):
+        grid[0, a] = 448.0 if t % 2 == 0 else -448.0
+    k = np.array([-3, 0, 2, -7, 5], dtype=np.float64)
+    x = grid.copy()
+    for t, (a, b) in enumerate(_TILES):
+        x[0, a:b] *= 2.0 ** k[t]
+    codes, scales = o.latent_fp8_quantize(x.astype(np.float32))
+    assert np.array_equal(scales[0], 2.0 ** k)
+    assert np.array_equal(codes, grid)
+    assert np.array_equal(o.latent_fp8_dequantize(codes, scales), x)
+    # tile boundaries: dims 511 and 512 belong to different tiles
+    y = rng.standard_normal((1, 576)).astype(np.float32)
+    c0, s0 = o.latent_fp8_quantize(y)
+    y2 = y.copy(); y2[0, 511] = 1000.0
+    c1, s1 = o.latent_fp8_quantize(y2)
+    assert np.array_equal(s1[0, [0, 1, 2, 4]], s0[0, [0, 1, 2, 4]]) and s1[0, 3] != s0[0, 3]
+    y3 = y.copy(); y3[0, 512] = -1000.0
+    c2, s2 = o.latent_fp8_quantize(y3)
+    assert np.array_equal(s2[0, :4], s0[0, :4]) and s2[0, 4] != s0[0, 4]
+    assert np.array_equal(c2[0, :512], c0[0, :512])
+    for t, (a, b) in enumerate(_TILES):
+        assert np.abs(c0[0, a:b]).max() == 448.0
+    # error bound: normal codes within 2^-4 relative, the rest within s * 2^-10
+    z = (rng.standard_normal((4, 576)) * 10).astype(np.float32)
+    c, sc = o.latent_fp8_quantize(z)
+    d = o.latent_fp8_dequantize(c, sc)
+    for t, (a, b) in enumerate(_TILES):
+        s_t = sc[:, t:t + 1]
+        err = np.abs(d[:, a:b] - z[:, a:b])
+        normal = np.abs(z[:, a:b]) >= s_t * 2.0 ** -6
+        assert np.all(err[normal] <= np.abs(z[:, a:b])[normal] * 2.0 ** -4 * (1 + 1e-6))
+        assert np.all(err[~normal] <= np.broadcast_to(s_t, err.shape)[~normal] * 2.0 ** -10 * (1 + 1e-6))
+    zc, zs = o.latent_fp8_quantize(np.zeros((1, 576), dtype=np.float32))
+    assert (zs == 0).all() and (zc == 0).all()
+
+
 def _load_golden_indexer():
     cases = []
     path = os.path.join(GOLDEN, "indexer_tiny.txt")

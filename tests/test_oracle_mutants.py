@@ -147,6 +147,23 @@ def _mx_scores(q_quant=True, per_row_scale=False):
     return scores
 
 
+def _latent_quantize_with(tiles=None, qmax=448.0):
+    """An FP8 latent quantiser with a planted change in the tiling or the scale."""
+    tl = tiles or real.LATENT_TILES
+    def quantize(rows):
+        x = real._f64(rows).astype(np.float32)
+        codes = np.zeros(x.shape)
+        scales = np.zeros(x.shape[:-1] + (len(real.LATENT_TILES),))
+        for t, (a, b) in enumerate(tl):
+            seg = x[..., a:b]
+            sc = (np.abs(seg).max(axis=-1) / np.float32(qmax)).astype(np.float32)
+            safe = np.where(sc > 0, sc, np.float32(1.0)).astype(np.float32)
+            codes[..., a:b] = real.e4m3_round((seg / safe[..., None]).astype(np.float64))
+            scales[..., min(t, len(real.LATENT_TILES) - 1)] = sc
+        return codes, scales
+    return quantize
+
+
 MUTANTS = {
     "no_relu": dict(index_scores=_scores_no_relu),
     "relu_after_head_sum": dict(index_scores=_scores_relu_after_sum),
@@ -168,6 +185,11 @@ MUTANTS = {
                                                                    _e4m3_truncate)),
     "mx_query_not_quantised": dict(index_scores=_mx_scores(q_quant=False)),
     "mx_one_scale_per_row": dict(index_scores=_mx_scores(per_row_scale=True)),
+    "latent_scale_over_240": dict(latent_fp8_quantize=_latent_quantize_with(qmax=240.0)),
+    "latent_rope_in_last_tile": dict(latent_fp8_quantize=_latent_quantize_with(
+        tiles=((0, 128), (128, 256), (256, 384), (384, 576)))),
+    "latent_tiles_of_64": dict(latent_fp8_quantize=_latent_quantize_with(
+        tiles=tuple((a, a + 64) for a in range(0, 576, 64))[:5])),
 }
 
 
