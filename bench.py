@@ -72,7 +72,11 @@ def algorithmic_bytes(ws) -> dict:
         per_key_scale = ws.k_scale.element_size()
     scale = int(kv.sum()) * per_key_scale
     sel = torch.clamp(vis, max=ws.K)
-    gather = int(sel.sum()) * W.D_QK * 2
+    # one latent row: 576 bf16, or 576 E4M3 codes + 5 fp32 tile scales
+    row_bytes = W.D_QK * ws.latent.element_size()
+    if getattr(ws, "latent_scale", None) is not None:
+        row_bytes += ws.latent_scale.shape[-1] * ws.latent_scale.element_size()
+    gather = int(sel.sum()) * row_bytes
     q_bytes = ws.q_idx.numel() * 2 + ws.w.numel() * 4 + ws.q.numel() * 2
     out = B * ws.H * W.D_LATENT * 2 + B * ws.H * 4
     idx = B * ws.K * 4
@@ -282,7 +286,8 @@ def run_gpu(args):
     # seeded per config; each rank its own replica (--rows: a smaller decode batch
     # for profiling captures, never a bench line)
     ws = W.make_config(args.config, device=dev, rows=args.rows, tokens_per_seq=args.tokens_per_seq,
-                       k_mx_group=getattr(args, "k_mx_group", 0))
+                       k_mx_group=getattr(args, "k_mx_group", 0),
+                       latent_fp8=getattr(args, "latent_fp8", False))
     tps = ws.tokens_per_seq
     wname = ws.name   # the config's workload, or its MXFP8-key variant
     torch.cuda.synchronize()
@@ -339,9 +344,10 @@ def run_gpu(args):
 
     hbm, tfl, src = peaks()
     extra = {}
-    if decode and tps > 1:
-        # multi-token step: the scoring entry point takes one row per sequence,
-        # so the step itself stands in for the kernel (HBM-bound like decode)
+    if decode and (tps > 1 or ws.latent_scale is not None):
+        # multi-token step (the scoring entry point takes one row per sequence)
+        # or FP8 latent cache (the attention core is the changed kernel): the
+        # step itself stands in for the kernel (HBM-bound like decode)
         ab_step = algorithmic_bytes(ws)["total"]
         achieved = ab_step / (ms_step / 1e3) / 1e9
         roofline = {"bound": "hbm", "kernel": "step", "achieved": round(achieved, 1), "peak": hbm,
@@ -408,6 +414,8 @@ def run_gpu(args):
             result["config"]["profiling_rows"] = args.rows
         if tps > 1:
             result["config"]["tokens_per_seq"] = tps
+        if ws.latent_scale is not None:
+            result["config"]["latent_cache"] = "fp8 (E4M3 + fp32 scale per 128-dim tile)"
         mxg = getattr(args, "k_mx_group", 0)
         if mxg:
             result["config"]["index_keys"] = f"mxfp8 (E4M3 + E8M0 per {mxg})"
@@ -537,7 +545,8 @@ def run_reference(args):
         return None
     cfg = W.CONFIGS[args.config]
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
-    ws = W.make_config(args.config, device=dev, k_mx_group=getattr(args, "k_mx_group", 0))
+    ws = W.make_config(args.config, device=dev, k_mx_group=getattr(args, "k_mx_group", 0),
+                       latent_fp8=getattr(args, "latent_fp8", False))
     per_step = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
     start = 0
     for _ in range(args.warmup):
@@ -725,6 +734,8 @@ def main():
     ap.add_argument("--k-mx-group", type=int, default=0, choices=[0, 32, 64, 128],
                     help="contiguous decode workloads: index keys stored as MXFP8 with this "
                          "many elements per scale (0: the workload's own key format)")
+    ap.add_argument("--latent-fp8", action="store_true",
+                    help="the 64x128-head decode workload with an FP8 latent cache (own bench line)")
     ap.add_argument("--mx-scan", action="store_true",
                     help="measurement: MXFP8 group-size scan, precision and speed (not a bench line)")
     ap.add_argument("--rows", type=int, default=None,

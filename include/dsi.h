@@ -38,6 +38,13 @@
  *   k_scale [num_pages, page_size], latent [num_pages, page_size, 576];
  *   logical position p of sequence b lives in page block_table[b, p/page_size]
  *   at slot p % page_size.
+ * - FP8 latent cache (latent_dtype == DSI_FP8_E4M3; "Day 0 Inference Support
+ *   for New LLM Architectures: Optimization Practices", "A Layered Strategy":
+ *   the KV cache in FP8 with one scale per token and head tile of 128
+ *   elements): latent holds E4M3 codes [positions, 576] and latent_scale fp32
+ *   [positions, 5], one scale per tile of dims 0-127, 128-255, 256-383,
+ *   384-511 and 512-575 (the rope dims); the row's value is code * scale of
+ *   its tile (see dsi_latent_fp8_append).
  * Row semantics:
  * - decode != 0: one query token per sequence; row b sees positions
  *   0 .. seq_lens[b]-1 (the new token's own key is already in the cache).
@@ -84,7 +91,7 @@ typedef struct dsi_cache {
   const void*    k_scale;      /* FP8: fp32 [positions], one scale per position;
                                   MXFP8: uint8 E8M0 [positions, d / k_group];
                                   NULL for bf16 (laid out like k_idx, minus d) */
-  const void*    latent;       /* bf16 latent rows, 576 per position */
+  const void*    latent;       /* latent rows, 576 per position (bf16, or E4M3 codes) */
   const int32_t* block_table;  /* [batch, max_pages] page ids, or NULL for contiguous */
   int32_t        page_size;    /* positions per page (paged only; multiple of 8) */
   int32_t        max_pages;    /* columns of block_table (paged only) */
@@ -93,6 +100,8 @@ typedef struct dsi_cache {
   int64_t        s_max;        /* contiguous: rows per sequence; paged: max_pages * page_size */
   int64_t        num_pages;    /* paged: pages in the pools (bounds checks); contiguous: 0 */
   int32_t        k_group;      /* MXFP8: elements per scale, 32, 64 or 128 (0 = 32); else unused */
+  int32_t        latent_dtype; /* dsi_dtype of latent: DSI_BF16 (0) or DSI_FP8_E4M3 */
+  const float*   latent_scale; /* FP8 latent: fp32 [positions, 5] tile scales; else NULL */
 } dsi_cache;
 
 /*
@@ -212,7 +221,9 @@ dsi_status dsi_index_topk_prefill(const void* q_idx, const float* w, const dsi_c
  * Absorbed-MLA reading (the pages give no formula): for head h,
  *   l_s = scale * q[b, h, :] . c_s  (c_s = latent row of position s, 576 wide)
  *   out[b, h, :] = sum_s softmax(l)_s * c_s[0:512];  lse[b, h] = ln sum_s exp(l_s)
- * over the positions s = idx[b, j] >= 0.
+ * over the positions s = idx[b, j] >= 0.  With an FP8 latent cache c_s is the
+ * dequantised row (code * tile scale); the 128-head tensor-core kernel reads
+ * bf16 rows only, so FP8 latent caches take the CUDA-core kernel.
  *   q       bf16 [batch, n_heads, 576]
  *   idx     int32 [batch, K] logical positions (< seq_lens[b]); entries < 0 skipped
  *   out     bf16 [batch, n_heads, 512]
@@ -323,6 +334,32 @@ size_t dsi_workspace_size(int32_t rows, int32_t n_heads_idx, int32_t n_heads, in
 dsi_status dsi_mxfp8_quantize(const void* x, int64_t n_rows, int32_t d, int64_t ld_x,
                               int32_t group, const int64_t* dst_rows, void* codes, void* scales,
                               void* stream);
+
+/*
+ * dsi_latent_fp8_append — quantise bf16 latent rows into an FP8 latent cache
+ * (the on-the-fly cache write of new positions; "Day 0 Inference Adaptation
+ * and Sparse Attention Optimization for New Large Model Architectures": cache
+ * writes compressed to FP8 as they happen).
+ *
+ * For row i and tile t (dims 0-127, 128-255, 256-383, 384-511, 512-575):
+ *   scale = (largest |x| of the tile) / 448 in fp32 (0 for an all-zero tile)
+ *   codes[dst(i), j] = E4M3 of x[i, j] / scale computed in fp32, nearest
+ *                      (ties to even), saturating at +-448 (0 when scale is 0)
+ *   scales[dst(i), t] = scale
+ * with dst(i) = dst_rows[i], or i when dst_rows is NULL; a negative entry
+ * skips the row.  The scale rule is this library's reading; the pages fix the
+ * tile of 128 per token and the FP8 format only.
+ *   x         bf16 [n_rows, ld_x] (16-byte aligned, ld_x a multiple of 8, >= 576)
+ *   dst_rows  int64 [n_rows] device array, or NULL
+ *   codes     uint8 E4M3 [*, 576] (16-byte aligned)
+ *   scales    fp32 [*, 5]
+ * The caller guarantees every dst(i) lies inside codes and scales.
+ * Errors: DSI_ERR_INVALID_ARG (null pointer, n_rows < 0, ld_x < 576, ld_x not
+ * a multiple of 8, misaligned x, codes or scales).
+ */
+dsi_status dsi_latent_fp8_append(const void* x, int64_t n_rows, int64_t ld_x,
+                                 const int64_t* dst_rows, void* codes, float* scales,
+                                 void* stream);
 
 /*
  * dsi_probe_random_gather — diagnostic, not part of the layer: plain 16-byte

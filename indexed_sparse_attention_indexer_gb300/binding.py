@@ -30,7 +30,8 @@ class DsiCache(ctypes.Structure):
     _fields_ = [("k_idx", c_void_p), ("k_dtype", c_int32), ("d", c_int32), ("k_scale", c_void_p),
                 ("latent", c_void_p), ("block_table", c_void_p), ("page_size", c_int32),
                 ("max_pages", c_int32), ("seq_lens", c_void_p), ("batch", c_int32),
-                ("s_max", c_int64), ("num_pages", c_int64), ("k_group", c_int32)]
+                ("s_max", c_int64), ("num_pages", c_int64), ("k_group", c_int32),
+                ("latent_dtype", c_int32), ("latent_scale", c_void_p)]
 
 
 # name -> (restype, argtypes); the exported surface of include/dsi.h
@@ -62,6 +63,8 @@ SIGNATURES = {
                                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dsi_mxfp8_quantize": (c_int32, [c_void_p, c_int64, c_int32, c_int64, c_int32, c_void_p,
                                      c_void_p, c_void_p, c_void_p]),
+    "dsi_latent_fp8_append": (c_int32, [c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
+                                        c_void_p]),
     "dsi_probe_random_gather": (c_int32, [c_void_p, c_int64, c_int64, c_void_p, c_int32, c_int32,
                                           c_int32, c_void_p]),
     "dsi_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int64, c_int32]),
@@ -122,9 +125,11 @@ class Cache:
 
     def __init__(self, k_idx: Optional[torch.Tensor], latent: Optional[torch.Tensor],
                  seq_lens: Optional[torch.Tensor] = None, k_scale: Optional[torch.Tensor] = None,
-                 block_table: Optional[torch.Tensor] = None, page_size: int = 0):
+                 block_table: Optional[torch.Tensor] = None, page_size: int = 0,
+                 latent_scale: Optional[torch.Tensor] = None):
         self.k_idx, self.latent, self.seq_lens = k_idx, latent, seq_lens
         self.k_scale, self.block_table, self.page_size = k_scale, block_table, page_size
+        self.latent_scale = latent_scale
         ref = k_idx if k_idx is not None else latent
         s = DsiCache()
         s.k_idx = k_idx.data_ptr() if k_idx is not None else None
@@ -140,6 +145,9 @@ class Cache:
                 s.k_dtype = DSI_FP8_E4M3
         s.k_scale = k_scale.data_ptr() if k_scale is not None else None
         s.latent = latent.data_ptr() if latent is not None else None
+        # an E4M3 latent cache is FP8 with per-tile scales
+        s.latent_dtype = DSI_FP8_E4M3 if (latent is not None and latent.dtype == torch.float8_e4m3fn) else DSI_BF16
+        s.latent_scale = latent_scale.data_ptr() if latent_scale is not None else None
         if block_table is not None:
             s.block_table = block_table.data_ptr()
             s.page_size = int(page_size)
@@ -158,7 +166,8 @@ class Cache:
     @classmethod
     def of(cls, ws) -> "Cache":
         """Cache of a workload whose tensors are on the device."""
-        return cls(ws.k_idx, ws.latent, ws.seq_lens, ws.k_scale, ws.block_table, ws.page_size)
+        return cls(ws.k_idx, ws.latent, ws.seq_lens, ws.k_scale, ws.block_table, ws.page_size,
+                   getattr(ws, "latent_scale", None))
 
     def ref(self):
         return ctypes.byref(self.struct)
@@ -212,6 +221,23 @@ def mxfp8_quantize(x, group: int = 32, dst_rows=None, codes=None, scales=None, s
     st = lib.dsi_mxfp8_quantize(_ptr(x), n, d, int(x.stride(0)), int(group), _ptr(dst_rows),
                                 _ptr(codes), _ptr(scales), _stream(stream))
     _check(lib, "dsi_mxfp8_quantize", st)
+    return codes, scales
+
+
+def latent_fp8_append(x, dst_rows=None, codes=None, scales=None, stream=None,
+                      checked: bool = False):
+    """FP8 latent codes (float8_e4m3fn [*, 576]) and fp32 tile scales ([*, 5]) of
+    bf16 latent rows ``x [n, 576]``; with ``dst_rows`` (int64 [n]) row i goes to
+    row dst_rows[i] of the given ``codes``/``scales`` (an append into a cache)."""
+    lib = load(checked)
+    n = int(x.shape[0])
+    if codes is None:
+        codes = torch.empty((n, D_QK), dtype=torch.float8_e4m3fn, device=x.device)
+    if scales is None:
+        scales = torch.empty((n, 5), dtype=torch.float32, device=x.device)
+    st = lib.dsi_latent_fp8_append(_ptr(x), n, int(x.stride(0)), _ptr(dst_rows), _ptr(codes),
+                                   _ptr(scales), _stream(stream))
+    _check(lib, "dsi_latent_fp8_append", st)
     return codes, scales
 
 

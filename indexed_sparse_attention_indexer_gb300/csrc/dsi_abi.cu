@@ -6,6 +6,7 @@
 #include <atomic>
 
 #include "kernels.h"
+#include "latent_fp8.h"
 
 using namespace dsi;
 
@@ -60,7 +61,12 @@ dsi_status check_cache(const dsi_cache* c, int rows, int decode, int64_t q_offse
       if (!aligned(c->k_scale, 16)) return DSI_ERR_INVALID_ARG;
     }
   }
-  if (need_latent && (!c->latent || !aligned(c->latent, 16))) return DSI_ERR_INVALID_ARG;
+  if (need_latent) {
+    if (!c->latent || !aligned(c->latent, 16)) return DSI_ERR_INVALID_ARG;
+    if (c->latent_dtype != DSI_BF16 && c->latent_dtype != DSI_FP8_E4M3) return DSI_ERR_UNSUPPORTED;
+    if (c->latent_dtype == DSI_FP8_E4M3 && (!c->latent_scale || !aligned(c->latent_scale, 4)))
+      return DSI_ERR_INVALID_ARG;
+  }
   if (c->block_table) {
     if (c->page_size <= 0 || c->max_pages <= 0 || c->num_pages <= 0) return DSI_ERR_INVALID_ARG;
     if (c->page_size % 8 != 0) return DSI_ERR_UNSUPPORTED;
@@ -96,6 +102,18 @@ CacheView view_of(const dsi_cache* c) {
   v.batch = c->batch;
   v.tokens_per_seq = 1;
   return v;
+}
+
+// The attention core over the cache's latent rows: bf16 rows, or FP8 codes
+// with their tile scales.
+cudaError_t attend(const bf16* q, const CacheView& v, const dsi_cache* c, const int32_t* idx,
+                   int rows, int H, int K, int decode, int64_t q_offset, float scale, bf16* out,
+                   float* lse, void* ws, size_t ws_bytes, int* err, cudaStream_t st) {
+  if (c->latent_dtype == DSI_FP8_E4M3)
+    return launch_sparse_mla_fp8(q, v, c->latent_scale, idx, rows, H, K, decode, q_offset, scale,
+                                 out, lse, ws, ws_bytes, err, st);
+  return launch_sparse_mla(q, v, idx, rows, H, K, decode, q_offset, scale, out, lse, ws, ws_bytes,
+                           err, st);
 }
 
 dsi_status check_mla_heads(int H) {
@@ -208,10 +226,9 @@ static dsi_status mla_common(const void* q, const dsi_cache* cache, const int32_
   if (!(scale == scale)) return DSI_ERR_INVALID_ARG;
   if (rows == 0) return DSI_OK;
   CacheView v = view_of(cache);
-  return from_cuda(launch_sparse_mla(reinterpret_cast<const bf16*>(q), v, idx, rows, H, K, decode,
-                                     q_offset, scale, reinterpret_cast<bf16*>(out), lse, ws,
-                                     ws ? ws_bytes : 0, status_ptr(),
-                                     reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(attend(reinterpret_cast<const bf16*>(q), v, cache, idx, rows, H, K, decode,
+                          q_offset, scale, reinterpret_cast<bf16*>(out), lse, ws,
+                          ws ? ws_bytes : 0, status_ptr(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dsi_status dsi_sparse_mla_decode(const void* q, const dsi_cache* cache, const int32_t* idx,
@@ -284,9 +301,9 @@ static dsi_status layer_common(const void* q_idx, const float* w, const void* q,
                     count_out, st, tokens_per_seq);
     if (e != cudaSuccess) return from_cuda(e);
   }
-  e = launch_sparse_mla(reinterpret_cast<const bf16*>(q), v, idx, rows, n_heads, K, decode,
-                        q_offset, scale, reinterpret_cast<bf16*>(out), lse, ws + p.mla_off,
-                        p.total - p.mla_off, err, st);
+  e = attend(reinterpret_cast<const bf16*>(q), v, cache, idx, rows, n_heads, K, decode, q_offset,
+             scale, reinterpret_cast<bf16*>(out), lse, ws + p.mla_off, p.total - p.mla_off, err,
+             st);
   return from_cuda(e);
 }
 
@@ -327,6 +344,19 @@ dsi_status dsi_mxfp8_quantize(const void* x, int64_t n_rows, int32_t d, int64_t 
                                          dst_rows, static_cast<uint8_t*>(codes),
                                          static_cast<uint8_t*>(scales),
                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dsi_status dsi_latent_fp8_append(const void* x, int64_t n_rows, int64_t ld_x,
+                                 const int64_t* dst_rows, void* codes, float* scales,
+                                 void* stream) {
+  if (!x || !codes || !scales || n_rows < 0) return DSI_ERR_INVALID_ARG;
+  if (ld_x < DSI_D_QK || ld_x % 8 != 0 || !aligned(x, 16) || !aligned(codes, 16) ||
+      !aligned(scales, 4))
+    return DSI_ERR_INVALID_ARG;
+  if (n_rows == 0) return DSI_OK;
+  return from_cuda(launch_latent_fp8_append(reinterpret_cast<const bf16*>(x), n_rows, ld_x,
+                                            dst_rows, static_cast<uint8_t*>(codes), scales,
+                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dsi_status dsi_probe_random_gather(const void* base, int64_t row_pitch, int64_t n_src_rows,

@@ -16,21 +16,39 @@
 // max and sum per head) and P.V accumulates in registers.  With several
 // splits, each block writes an unnormalised partial (o, m, l) and a combine
 // kernel merges them with their log-sum-exp weights.
+//
+// FP8 latent cache ("Day 0 Inference Support...", "A Layered Strategy": the
+// KV cache in FP8 with one scale per token and tile of 128 elements): the same
+// kernel gathers the E4M3 codes (576 bytes per row) and the row's five tile
+// scales; a logit sums code * q tile by tile and multiplies each tile's sum by
+// its scale, and P.V scales each row's probability by the scale of the tile
+// that holds the thread's output dims.
 #include <math.h>
 
 #include "kernels.h"
+#include "latent_fp8.h"
 
 namespace dsi {
 
 constexpr int kHB = 16;        // heads per block
 constexpr int kNT = 32;        // gathered rows per tile
 constexpr int kRS = 584;       // shared row stride (bf16), 1168 bytes
+constexpr int kRS8 = 656;      // FP8 rows: shared row stride in bytes (164 words: 16-byte reads of
+                               // 8 consecutive rows fall in different banks)
 constexpr int kMlaThreads = 256;
+static_assert(sizeof(uint8_t[2][kNT][kRS8]) + sizeof(float[2][kNT][8]) <=
+                  sizeof(bf16[2][kNT][kRS]), "FP8 tile fits the bf16 tile's space");
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct MlaSmem {
   float q[kHB][DSI_D_QK];          // 36864 B
-  bf16 c[2][kNT][kRS];             // 74752 B
+  union {
+    bf16 c[2][kNT][kRS];           // 74752 B
+    struct {
+      uint8_t c8[2][kNT][kRS8];    // FP8 latent codes: 41984 B
+      float sc[2][kNT][8];         // and the rows' tile scales (5 used)
+    };
+  };
   float p[kHB][kNT];               // 2048 B
   float m[kHB], l[kHB], alpha[kHB];
   int valid[2][kNT];
@@ -40,13 +58,30 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
 }
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem));
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+
+// 8 E4M3 codes (byte i = element i) -> floats
+__device__ __forceinline__ void fp8x8_to_f32(const uint2& v, float* f) {
+  const __nv_fp8x2_e4m3* h = reinterpret_cast<const __nv_fp8x2_e4m3*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = static_cast<float2>(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n"); }
 
+template <bool F8>
 __global__ void __launch_bounds__(kMlaThreads)
-mla_simt(const bf16* __restrict__ q, CacheView c, const int32_t* __restrict__ idx, int H, int K,
-         int decode, int64_t q_offset, float scale, bf16* __restrict__ out, float* __restrict__ lse,
-         float* __restrict__ part_o, float2* __restrict__ part_ml, int splits, int* err) {
+mla_simt(const bf16* __restrict__ q, CacheView c, const float* __restrict__ lscale,
+         const int32_t* __restrict__ idx, int H, int K, int decode, int64_t q_offset, float scale,
+         bf16* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
+         float2* __restrict__ part_ml, int splits, int* err) {
   extern __shared__ float4 mla_smem_raw[];
   MlaSmem& S = *reinterpret_cast<MlaSmem*>(mla_smem_raw);
   const int g = blockIdx.x, r = blockIdx.y, sp = blockIdx.z;
@@ -68,9 +103,10 @@ mla_simt(const bf16* __restrict__ q, CacheView c, const int32_t* __restrict__ id
   if (tid < kHB) { S.m[tid] = -INFINITY; S.l[tid] = 0.f; }
 
   auto gather = [&](int buf, int j0) {
-    // 32 rows x 72 chunks of 16 bytes
-    for (int i = tid; i < kNT * 72; i += kMlaThreads) {
-      const int rr = i / 72, ch = i - rr * 72;
+    // bf16: 32 rows x 72 chunks of 16 bytes; FP8: 36 chunks of codes + 5 scales
+    constexpr int kPer = F8 ? 41 : 72;
+    for (int i = tid; i < kNT * kPer; i += kMlaThreads) {
+      const int rr = i / kPer, ch = i - rr * kPer;
       const int j = j0 + rr;
       int pos = (j < j_end) ? __ldg(irow + j) : -1;
 #ifdef DSI_CHECKED
@@ -79,7 +115,14 @@ mla_simt(const bf16* __restrict__ q, CacheView c, const int32_t* __restrict__ id
       (void)n_vis;
       int64_t row = pos >= 0 ? phys_row(c, b, pos, err) : -1;
       if (ch == 0) S.valid[buf][rr] = row >= 0;
-      if (row >= 0) cp_async16(&S.c[buf][rr][ch * 8], c.latent + row * DSI_D_QK + ch * 8);
+      if (row < 0) continue;
+      if (F8) {
+        const uint8_t* codes = reinterpret_cast<const uint8_t*>(c.latent);
+        if (ch < 36) cp_async16(&S.c8[buf][rr][ch * 16], codes + row * DSI_D_QK + ch * 16);
+        else cp_async4(&S.sc[buf][rr][ch - 36], lscale + row * kLatentTiles + (ch - 36));
+      } else {
+        cp_async16(&S.c[buf][rr][ch * 8], c.latent + row * DSI_D_QK + ch * 8);
+      }
     }
     cp_async_commit();
   };
@@ -103,7 +146,33 @@ mla_simt(const bf16* __restrict__ q, CacheView c, const int32_t* __restrict__ id
     {
       const int pr = lane, h0 = warp * 2;
       float a0 = 0.f, a1 = 0.f;
-      if (S.valid[buf][pr]) {
+      if (F8 && S.valid[buf][pr]) {
+        // tile by tile: sum code * q over the tile, then times the tile's scale
+        const uint8_t* crow = &S.c8[buf][pr][0];
+#pragma unroll 1
+        for (int t = 0; t < kLatentTiles; ++t) {
+          const int ch0 = t * 8, ch1 = t < 4 ? ch0 + 8 : 36;   // 16-code chunks of the tile
+          float b0 = 0.f, b1 = 0.f;
+#pragma unroll 2
+          for (int ch = ch0; ch < ch1; ++ch) {
+            float cf[16];
+            fp8x16_to_f32(*reinterpret_cast<const uint4*>(crow + ch * 16), cf);
+            const float4* q0 = reinterpret_cast<const float4*>(&S.q[h0][ch * 16]);
+            const float4* q1 = reinterpret_cast<const float4*>(&S.q[h0 + 1][ch * 16]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float4 x = q0[k], y = q1[k];
+              b0 = fmaf(x.x, cf[4 * k], b0); b0 = fmaf(x.y, cf[4 * k + 1], b0);
+              b0 = fmaf(x.z, cf[4 * k + 2], b0); b0 = fmaf(x.w, cf[4 * k + 3], b0);
+              b1 = fmaf(y.x, cf[4 * k], b1); b1 = fmaf(y.y, cf[4 * k + 1], b1);
+              b1 = fmaf(y.z, cf[4 * k + 2], b1); b1 = fmaf(y.w, cf[4 * k + 3], b1);
+            }
+          }
+          const float st = S.sc[buf][pr][t];
+          a0 = fmaf(st, b0, a0);
+          a1 = fmaf(st, b1, a1);
+        }
+      } else if (!F8 && S.valid[buf][pr]) {
         const bf16* crow = &S.c[buf][pr][0];
 #pragma unroll 4
         for (int ch = 0; ch < 72; ++ch) {
@@ -158,10 +227,16 @@ mla_simt(const bf16* __restrict__ q, CacheView c, const int32_t* __restrict__ id
       for (int j = 0; j < kNT; ++j) {
         if (!S.valid[buf][j]) continue;
         float cf[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(&S.c[buf][j][dc * 8]), cf);
+        float sj = 1.f;   // FP8: the scale of the tile holding dims dc*8 .. dc*8+7
+        if (F8) {
+          fp8x8_to_f32(*reinterpret_cast<const uint2*>(&S.c8[buf][j][dc * 8]), cf);
+          sj = S.sc[buf][j][dc >> 4];
+        } else {
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(&S.c[buf][j][dc * 8]), cf);
+        }
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const float pj = S.p[hq + h][j];
+          const float pj = F8 ? S.p[hq + h][j] * sj : S.p[hq + h][j];
 #pragma unroll
           for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(pj, cf[e], acc[h][e]);
         }
@@ -259,16 +334,14 @@ cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const int32_
 bool tc_mla_supported(int n_heads);
 bool tc_mla_cache_ok(const CacheView& c);
 
-cudaError_t launch_sparse_mla(const bf16* q, const CacheView& c, const int32_t* idx, int rows,
-                              int H, int K, int decode, int64_t q_offset, float scale, bf16* out,
-                              float* lse, void* ws, size_t ws_bytes, int* err, cudaStream_t st) {
-  if (rows <= 0) return cudaSuccess;
-  if (tc_mla_supported(H) && tc_mla_cache_ok(c))
-    return launch_sparse_mla_tc(q, c, idx, rows, H, K, decode, q_offset, scale, out, lse, ws,
-                                ws_bytes, err, st);
+template <bool F8>
+static cudaError_t launch_simt(const bf16* q, const CacheView& c, const float* lscale,
+                               const int32_t* idx, int rows, int H, int K, int decode,
+                               int64_t q_offset, float scale, bf16* out, float* lse, void* ws,
+                               size_t ws_bytes, int* err, cudaStream_t st) {
   const int splits = mla_pick_splits(rows, H, K, ws ? ws_bytes : 0);
   const size_t smem = sizeof(MlaSmem);
-  cudaError_t e = cudaFuncSetAttribute(mla_simt, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(mla_simt<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   float* part_o = nullptr;
@@ -279,14 +352,34 @@ cudaError_t launch_sparse_mla(const bf16* q, const CacheView& c, const int32_t* 
     part_ml = reinterpret_cast<float2*>(reinterpret_cast<char*>(ws) + n * DSI_D_LATENT * sizeof(float));
   }
   dim3 grid((H + kHB - 1) / kHB, rows, splits);
-  mla_simt<<<grid, kMlaThreads, smem, st>>>(q, c, idx, H, K, decode, q_offset, scale, out, lse,
-                                            part_o, part_ml, splits, err);
+  mla_simt<F8><<<grid, kMlaThreads, smem, st>>>(q, c, lscale, idx, H, K, decode, q_offset, scale,
+                                                out, lse, part_o, part_ml, splits, err);
   note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess || splits == 1) return e;
   mla_combine<<<dim3(H, rows), 128, 0, st>>>(part_o, part_ml, H, splits, out, lse);
   note_launch();
   return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_mla(const bf16* q, const CacheView& c, const int32_t* idx, int rows,
+                              int H, int K, int decode, int64_t q_offset, float scale, bf16* out,
+                              float* lse, void* ws, size_t ws_bytes, int* err, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  if (tc_mla_supported(H) && tc_mla_cache_ok(c))
+    return launch_sparse_mla_tc(q, c, idx, rows, H, K, decode, q_offset, scale, out, lse, ws,
+                                ws_bytes, err, st);
+  return launch_simt<false>(q, c, nullptr, idx, rows, H, K, decode, q_offset, scale, out, lse, ws,
+                            ws_bytes, err, st);
+}
+
+cudaError_t launch_sparse_mla_fp8(const bf16* q, const CacheView& c, const float* latent_scale,
+                                  const int32_t* idx, int rows, int H, int K, int decode,
+                                  int64_t q_offset, float scale, bf16* out, float* lse, void* ws,
+                                  size_t ws_bytes, int* err, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  return launch_simt<true>(q, c, latent_scale, idx, rows, H, K, decode, q_offset, scale, out,
+                           lse, ws, ws_bytes, err, st);
 }
 
 }  // namespace dsi

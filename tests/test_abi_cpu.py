@@ -194,6 +194,29 @@ def test_mxfp8_validation(L):
     assert L.dsi_indexed_attention(*args, FAKE, 1 << 40, None) == U
 
 
+def test_latent_fp8_validation(L):
+    """Host checks of the FP8 latent append and of FP8 latent caches."""
+    E, U = binding.DSI_ERR_INVALID_ARG, binding.DSI_ERR_UNSUPPORTED
+    A = L.dsi_latent_fp8_append
+    assert A(None, 4, 576, None, FAKE, FAKE, None) == E
+    assert A(FAKE, 4, 576, None, None, FAKE, None) == E
+    assert A(FAKE, 4, 576, None, FAKE, None, None) == E
+    assert A(FAKE, -1, 576, None, FAKE, FAKE, None) == E
+    assert A(FAKE, 4, 512, None, FAKE, FAKE, None) == E      # ld_x < 576
+    assert A(FAKE, 4, 580, None, FAKE, FAKE, None) == E      # ld_x not a multiple of 8
+    assert A(FAKE + 8, 4, 576, None, FAKE, FAKE, None) == E
+    assert A(FAKE, 4, 576, None, FAKE + 8, FAKE, None) == E
+    assert A(FAKE, 4, 576, None, FAKE, FAKE + 2, None) == E
+    assert A(FAKE, 0, 576, None, FAKE, FAKE, None) == binding.DSI_OK
+    f = L.dsi_sparse_mla_decode
+    c = _cache(latent_dtype=binding.DSI_FP8_E4M3)             # FP8 latent without scales
+    assert f(FAKE, ctypes.byref(c), FAKE, 4, 16, 64, 0.1, FAKE, None, None, 0, None) == E
+    c = _cache(latent_dtype=7)
+    assert f(FAKE, ctypes.byref(c), FAKE, 4, 16, 64, 0.1, FAKE, None, None, 0, None) == U
+    c = _cache(latent_dtype=binding.DSI_FP8_E4M3, latent_scale=FAKE + 2)
+    assert f(FAKE, ctypes.byref(c), FAKE, 4, 16, 64, 0.1, FAKE, None, None, 0, None) == E
+
+
 def test_topk_validation(L):
     E, U = binding.DSI_ERR_INVALID_ARG, binding.DSI_ERR_UNSUPPORTED
     assert L.dsi_topk(None, 16, 2, None, 0, 4, FAKE, None, None) == E
