@@ -65,7 +65,7 @@ extern "C" {
 #define DSI_D_ROPE 64
 #define DSI_D_QK 576
 #define DSI_MAX_K 4096          /* largest supported top-k */
-#define DSI_VERSION 1
+#define DSI_VERSION 2          /* 2: MXFP8 keys and FP8 latent caches in dsi_cache */
 
 typedef enum {
   DSI_OK = 0,

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.dsi_version() == 1
+    assert L.dsi_version() == 2
     for code in range(7):
         s = L.dsi_status_string(code)
         assert s and s != b"unknown status"
