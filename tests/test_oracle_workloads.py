@@ -110,3 +110,25 @@ def test_multi_token_rows_reduce_to_decode_rows():
         # causality: no candidate sees a later candidate's key
         sel = got["idx"][:got["count"]]
         assert sel.size == 0 or sel.max() <= int(ws.seq_lens[b]) - (T - t)
+
+
+def test_mxfp8_and_fp8_latent_recipes():
+    """MXFP8 keys: integer codes, E8M0 bytes in {125, 126, 127}, one per group;
+    FP8 latent: exponent fields 4..10 (no NaN codes), tile scales in [0.02, 0.2)."""
+    ws = W.make_decode(2, 0, 8, 64, 8, 16, seed=4, lengths=[40, 9], k_mx_group=32,
+                       latent_fp8=True)
+    k = ws.k_idx.float()
+    assert torch.equal(k, k.round()) and k.abs().max() <= 3
+    assert ws.k_scale.dtype == torch.uint8 and ws.k_scale.shape[-1] == 2
+    assert int(ws.k_scale.min()) >= 125 and int(ws.k_scale.max()) <= 127
+    raw = ws.latent.view(torch.uint8)
+    ex = (raw >> 3) & 15
+    assert int(ex.min()) >= 4 and int(ex.max()) <= 10
+    assert ws.latent_scale.shape == ws.latent.shape[:-1] + (5,)
+    assert float(ws.latent_scale.min()) >= 0.02 and float(ws.latent_scale.max()) < 0.2
+    # the MXFP8 key scores of a row equal the unquantised scores of its dequantised keys
+    b = 0
+    kb = ws.k_idx[b, :40].float().numpy() * np.repeat(
+        2.0 ** (ws.k_scale[b, :40].numpy().astype(np.int64) - 127), 32, axis=1)
+    qd = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(ws.q_idx[b].float(), 32), 32)
+    assert np.array_equal(oracle.row_scores(ws, b), oracle.index_scores(qd, ws.w[b], kb))
