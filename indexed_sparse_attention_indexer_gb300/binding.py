@@ -109,6 +109,12 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _rows_contiguous(t: torch.Tensor, name: str):
+    """The C ABI takes a row pitch: elements within a row must be contiguous."""
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with contiguous rows")
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -214,6 +220,7 @@ def mxfp8_quantize(x, group: int = 32, dst_rows=None, codes=None, scales=None, s
     of the given ``codes``/``scales`` (an append into a cache)."""
     lib = load(checked)
     n, d = int(x.shape[0]), int(x.shape[1])
+    _rows_contiguous(x, "x")
     if codes is None:
         codes = torch.empty((n, d), dtype=torch.float8_e4m3fn, device=x.device)
     if scales is None:
@@ -231,6 +238,9 @@ def latent_fp8_append(x, dst_rows=None, codes=None, scales=None, stream=None,
     row dst_rows[i] of the given ``codes``/``scales`` (an append into a cache)."""
     lib = load(checked)
     n = int(x.shape[0])
+    _rows_contiguous(x, "x")
+    if int(x.shape[1]) != D_QK:
+        raise ValueError(f"latent rows are {D_QK} wide, got {int(x.shape[1])}")
     if codes is None:
         codes = torch.empty((n, D_QK), dtype=torch.float8_e4m3fn, device=x.device)
     if scales is None:

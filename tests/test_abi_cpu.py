@@ -264,3 +264,14 @@ def test_workspace_size(L):
     assert a >= 64 * 32768 * 4 + 64 * 2048 * 4
     assert L.dsi_workspace_size(64, 64, 128, 2048, 65536, 1) > a
     assert L.dsi_workspace_size(0, 64, 128, 2048, 32768, 1) == 256
+
+
+def test_binding_rejects_strided_rows():
+    """The quantiser bindings pass a row pitch: rows must be contiguous (checked
+    before anything reaches the library)."""
+    import torch
+    x = torch.zeros((128, 4), dtype=torch.bfloat16).t()      # 4 rows with stride 1 between rows
+    with pytest.raises(ValueError):
+        binding.mxfp8_quantize(x)
+    with pytest.raises(ValueError):
+        binding.latent_fp8_append(torch.zeros((2, 512), dtype=torch.bfloat16))
