@@ -308,8 +308,10 @@ size_t dsi_workspace_size(int32_t rows, int32_t n_heads_idx, int32_t n_heads, in
  * ("Day 0 Inference Support for New LLM Architectures: Optimization
  * Practices", "A Layered Strategy": MXFP8 index Q/K, dynamic per-group
  * quantisation, 32 elements per scale; "Day 0 Inference Acceleration for New
- * LLM Architectures: Hybrid Attention Adaptation and Optimization Practices",
- * quantisation of the index Q/K, and its advice to scan the group size.)
+ * LLM Architectures: Hybrid Attention Adaptation and Optimization Practices"
+ * §4, per-group dynamic quantisation of the index Q/K; "Day 0 Inference
+ * Adaptation and Performance Optimization for New Models" §4 and §7: the group
+ * size as a configurable parameter to scan.)
  *
  * For row i and group g (elements g*group .. g*group+group-1):
  *   X = floor(log2(max |x|)) - 8 over the group, held in [-127, 127]
