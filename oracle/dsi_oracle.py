@@ -79,7 +79,7 @@ def e4m3_round(x) -> np.ndarray:
 
 # MXFP8 ("Day 0 Inference Support for New LLM Architectures: Optimization
 # Practices", "A Layered Strategy"; "Day 0 Inference Acceleration ...: Hybrid
-# Attention Adaptation and Optimization Practices", quantisation of the index
+# Attention Adaptation and Optimization Practices" §4, quantisation of the index
 # Q/K): every group of G consecutive elements (G = 32 on the pages) shares one
 # power-of-two scale, chosen dynamically from the group's largest magnitude.
 # The reading taken here is the usual microscaling rule: the shared exponent is
