@@ -60,3 +60,21 @@ def test_reference_arm_line_on_cpu(monkeypatch):
     assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_algorithmic_bytes_of_the_quantised_variants():
+    """Per-step byte accounting: MXFP8 keys move d code bytes plus d/G scale bytes
+    per visible position; an FP8 latent row moves 576 code bytes plus five fp32
+    tile scales; the bf16 forms 2 bytes per element."""
+    import bench
+    from indexed_sparse_attention_indexer_gb300 import workloads as W
+    lens = [100, 37]
+    base = W.make_decode(2, 0, 4, 64, 16, 16, seed=1, lengths=lens)
+    mx = W.make_decode(2, 0, 4, 64, 16, 16, seed=1, lengths=lens, k_mx_group=32)
+    l8 = W.make_decode(2, 0, 4, 64, 16, 16, seed=1, lengths=lens, latent_fp8=True)
+    n = sum(lens)
+    sel = sum(min(16, x) for x in lens)
+    assert bench.algorithmic_bytes(base)["index_keys"] == n * 64 * 2
+    assert bench.algorithmic_bytes(mx)["index_keys"] == n * (64 + 2)
+    assert bench.algorithmic_bytes(base)["gather"] == sel * 576 * 2
+    assert bench.algorithmic_bytes(l8)["gather"] == sel * (576 + 5 * 4)
