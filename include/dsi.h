@@ -48,6 +48,8 @@
  * Row semantics:
  * - decode != 0: one query token per sequence; row b sees positions
  *   0 .. seq_lens[b]-1 (the new token's own key is already in the cache).
+ *   A length above s_max counts as s_max (a negative one as 0) in every
+ *   kernel: scoring, Top-K and attention agree on the clamped history.
  * - decode == 0 (prefill): one sequence (batch == 1); query token t sits at
  *   position q_offset + t and sees positions 0 .. q_offset + t.
  */
@@ -283,11 +285,16 @@ dsi_status dsi_indexed_attention(const void* q_idx, const float* w, const void* 
  * array of DSI_STATIC_SCRATCH_BYTES inside the library, which every GPU that
  * loads the library keeps until the process exits.  The caller still owns
  * inputs and outputs.  Returns DSI_ERR_WORKSPACE, before launching anything,
- * when dsi_workspace_size() for the call exceeds DSI_STATIC_SCRATCH_BYTES.
- * The first call on a device (with that device current) looks up the
- * array's device address; make that first call before any stream capture.
- * All calls share the array: calls whose kernels overlap on the GPU race.
- * Nothing in the array needs to start at zero.  Allocates nothing.
+ * when dsi_layer_workspace_size() for the call exceeds
+ * DSI_STATIC_SCRATCH_BYTES (a prefill on the fused indexer needs no score
+ * rows, so e.g. 8192 tokens with K = 2048 fit where their score matrix
+ * would not).  The first call on a device (with that device current) looks
+ * up the array's device address and caches it; make that first call before
+ * any stream capture.  The cached address belongs to the device's primary
+ * context: after cudaDeviceReset() on that device the library must not be
+ * called again in the process.  All calls share the array: calls whose
+ * kernels overlap on the GPU race.  Nothing in the array needs to start at
+ * zero.  Allocates nothing.
  */
 #define DSI_STATIC_SCRATCH_BYTES (16u << 20)
 dsi_status dsi_indexed_attention_static(const void* q_idx, const float* w, const void* q,
@@ -296,10 +303,24 @@ dsi_status dsi_indexed_attention_static(const void* q_idx, const float* w, const
                                         int32_t decode, int32_t* idx_out, int32_t* count_out,
                                         void* out, float* lse, void* stream);
 
-/* Bytes of workspace dsi_indexed_attention needs (and the larger, split-K
- * sizing of the dsi_sparse_mla_* calls when n_heads_idx == 0 and s_max == 0). */
+/* Bytes of workspace dsi_indexed_attention needs for any cache of these
+ * sizes (and the larger, split-K sizing of the dsi_sparse_mla_* calls when
+ * n_heads_idx == 0 and s_max == 0).  It counts the fp32 score rows of the
+ * unfused scoring + Top-K pair, rows x round_up(s_max, 64) x 4 bytes, which a
+ * prefill that takes the fused indexer does not use: dsi_layer_workspace_size
+ * gives the exact figure for one call. */
 size_t dsi_workspace_size(int32_t rows, int32_t n_heads_idx, int32_t n_heads, int32_t K,
                           int64_t s_max, int32_t decode);
+
+/* Exact bytes of workspace one dsi_indexed_attention call with these
+ * arguments needs (a multi-token step: rows = batch * tokens_per_seq,
+ * decode = 1): the score rows only when the call runs the unfused scoring +
+ * Top-K pair (every decode call; a prefill whose shape the fused indexer
+ * does not cover), the indices, and the split-K partials.  Never more than
+ * dsi_workspace_size(rows, n_heads_idx, n_heads, K, s_max or q_offset + rows,
+ * decode).  Host only; returns 256 for non-positive sizes or a NULL cache. */
+size_t dsi_layer_workspace_size(const dsi_cache* cache, int32_t rows, int32_t n_heads_idx,
+                                int32_t n_heads, int32_t K, int64_t q_offset, int32_t decode);
 
 /*
  * dsi_mxfp8_quantize — dynamic MXFP8 quantisation of bf16 rows: index keys on
@@ -364,19 +385,18 @@ dsi_status dsi_latent_fp8_append(const void* x, int64_t n_rows, int64_t ld_x,
                                  void* stream);
 
 /*
- * dsi_probe_random_gather — diagnostic, not part of the layer: plain 16-byte
- * loads of bytes_per_row bytes from each of the rows base + rows[i] *
- * row_pitch (the attention core's gather pattern), by `blocks` CTAs of 512
- * threads, nothing written.  Time it on a stream to get the random-row gather
- * bandwidth the attention core works against.
- *   base          device array of n_src_rows rows of row_pitch bytes (16-aligned)
- *   rows          int32 [n_rows] device row ids; ids outside 0..n_src_rows-1 are skipped
- *   bytes_per_row multiple of 16, <= row_pitch (a multiple of 16)
- * Errors: DSI_ERR_INVALID_ARG for null pointers, sizes or alignment out of range.
+ * dsi_selftest_wait_timeout — exercises the failure-detection path.  The
+ * pages have no counterpart: every wait inside the library's kernels is
+ * bounded, and a wait that runs out sets the device status word to
+ * DSI_ERR_TIMEOUT, drains its CTA and returns instead of hanging.  This call
+ * launches one warp that waits, with the given limit, on a barrier nothing
+ * ever completes, so that path can be tested: afterwards
+ * dsi_get_device_status() returns DSI_ERR_TIMEOUT once, and the device stays
+ * usable.  No memory is touched but the status word.
+ *   limit_ns  1000 .. 1e9 (1 us .. 1 s); the kernel ends after about that long
+ * Errors: DSI_ERR_INVALID_ARG for a limit outside the range.
  */
-dsi_status dsi_probe_random_gather(const void* base, int64_t row_pitch, int64_t n_src_rows,
-                                   const int32_t* rows, int32_t n_rows, int32_t bytes_per_row,
-                                   int32_t blocks, void* stream);
+dsi_status dsi_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 
 /* Synchronises `stream`, returns and clears the device status word of the
  * current device (DSI_OK, DSI_ERR_BOUNDS or DSI_ERR_TIMEOUT), or DSI_ERR_CUDA

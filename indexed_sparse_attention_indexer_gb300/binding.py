@@ -65,10 +65,11 @@ SIGNATURES = {
                                      c_void_p, c_void_p, c_void_p]),
     "dsi_latent_fp8_append": (c_int32, [c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
                                         c_void_p]),
-    "dsi_probe_random_gather": (c_int32, [c_void_p, c_int64, c_int64, c_void_p, c_int32, c_int32,
-                                          c_int32, c_void_p]),
     "dsi_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int64, c_int32]),
+    "dsi_layer_workspace_size": (c_size_t, [ctypes.POINTER(DsiCache), c_int32, c_int32, c_int32,
+                                            c_int32, c_int64, c_int32]),
     "dsi_get_device_status": (c_int32, [c_void_p]),
+    "dsi_selftest_wait_timeout": (c_int32, [ctypes.c_uint64, c_void_p]),
     "dsi_status_string": (ctypes.c_char_p, [c_int32]),
     "dsi_version": (c_int32, []),
     "dsi_launch_count": (ctypes.c_uint64, []),
@@ -251,17 +252,6 @@ def latent_fp8_append(x, dst_rows=None, codes=None, scales=None, stream=None,
     return codes, scales
 
 
-def probe_random_gather(base, row_pitch: int, rows, bytes_per_row: int, blocks: int,
-                        stream=None):
-    """Diagnostic: plain loads of randomly chosen rows of ``base`` (no output)."""
-    lib = load()
-    n_src = base.numel() * base.element_size() // row_pitch
-    st = lib.dsi_probe_random_gather(_ptr(base), int(row_pitch), int(n_src), _ptr(rows),
-                                     int(rows.numel()), int(bytes_per_row), int(blocks),
-                                     _stream(stream))
-    _check(lib, "dsi_probe_random_gather", st)
-
-
 def topk(scores, K: int, row_len=None, q_offset: int = 0, idx=None, count=None, stream=None,
          checked: bool = False):
     lib = load(checked)
@@ -315,6 +305,14 @@ def workspace_size(rows: int, n_heads_idx: int, n_heads: int, K: int, s_max: int
                                                  int(bool(decode))))
 
 
+def layer_workspace_size(cache: "Cache", rows: int, n_heads_idx: int, n_heads: int, K: int,
+                         q_offset: int, decode: bool, checked: bool = False) -> int:
+    """Exact workspace bytes of one fused-layer call (no score rows when a
+    prefill takes the fused indexer)."""
+    return int(load(checked).dsi_layer_workspace_size(cache.ref(), rows, n_heads_idx, n_heads, K,
+                                                       int(q_offset), int(bool(decode))))
+
+
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:
     # torch's caching allocator returns 512-byte aligned blocks
     return torch.empty((max(256, nbytes),), dtype=torch.uint8, device=device)
@@ -328,9 +326,9 @@ def indexed_attention(q_idx, w, q, cache: Cache, K: int, scale: float, decode: b
     lib = load(checked)
     rows, H_i, H = int(q_idx.shape[0]), int(q_idx.shape[1]), int(q.shape[1])
     dev = q.device
-    span = cache.struct.s_max if decode else q_offset + rows
     if workspace is None:
-        workspace = alloc_workspace(workspace_size(rows, H_i, H, K, span, decode, checked), dev)
+        workspace = alloc_workspace(
+            layer_workspace_size(cache, rows, H_i, H, K, q_offset, decode, checked), dev)
     if out is None:
         out = torch.empty((rows, H, D_LATENT), dtype=torch.bfloat16, device=dev)
     if lse is None and want_lse:
@@ -381,6 +379,14 @@ def device_status(stream=None, checked: bool = False) -> int:
     """Synchronise the stream and read/clear the device status word."""
     lib = load(checked)
     return int(lib.dsi_get_device_status(_stream(stream)))
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None, checked: bool = False) -> None:
+    """Launch the bounded-wait self-test (one warp waits on a barrier nothing
+    completes, for ``limit_ns``); ``device_status()`` then reports the timeout."""
+    lib = load(checked)
+    _check(lib, "dsi_selftest_wait_timeout", lib.dsi_selftest_wait_timeout(int(limit_ns),
+                                                                          _stream(stream)))
 
 
 def launch_count(checked: bool = False) -> int:

@@ -15,8 +15,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 
 SOURCES = ["dsi_abi.cu", "index_score.cu", "index_score_tc.cu", "topk.cu", "sparse_mla.cu",
-           "sparse_mla_tc.cu", "index_topk_prefill.cu", "dsi_static.cu", "probe_gather.cu",
-           "mxfp8_quant.cu", "latent_fp8.cu"]
+           "sparse_mla_tc.cu", "index_topk_prefill.cu", "dsi_static.cu",
+           "mxfp8_quant.cu", "latent_fp8.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

@@ -17,18 +17,23 @@ std::atomic<unsigned long long> g_launches{0};
 __device__ int g_status_word;  // device status (DSI_ERR_BOUNDS / DSI_ERR_TIMEOUT), 0 = ok
 
 constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices];  // per-device address of g_status_word
+// per-device address of g_status_word; atomics, so host threads that look it
+// up at once store the same value without a data race
+std::atomic<int*> g_status_ptr[kMaxDevices];
 
-// Device address of the status word on the current device (looked up once).
+// Device address of the status word on the current device (looked up once;
+// valid while the device's primary context lives).
 int* status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_status_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = static_cast<int*>(p);
+  int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_status_word) != cudaSuccess) return nullptr;
+    p = static_cast<int*>(a);
+    g_status_ptr[dev].store(p, std::memory_order_release);
   }
-  return g_status_ptr[dev];
+  return p;
 }
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -146,6 +151,20 @@ WsPlan plan_workspace(int rows, int Hi, int H, int K, int64_t s_max, size_t mla_
   return p;
 }
 
+// Whether a call of the fused layer takes the fused prefill indexer (scores
+// stay on chip) rather than the scoring kernel + Top-K pair.
+bool uses_fused_prefill(const CacheView& v, int n_heads_idx, int rows, int64_t q_offset, int K,
+                        int decode) {
+  return !decode && fused_prefill_topk_supported(v, n_heads_idx, rows, q_offset, K);
+}
+
+// Workspace of one fused-layer call: score rows only for the unfused pair.
+WsPlan layer_plan(const dsi_cache* c, int rows, int Hi, int H, int K, int64_t q_offset, int decode,
+                  bool fused_prefill) {
+  const int64_t span = decode ? c->s_max : q_offset + rows;
+  return plan_workspace(rows, Hi, H, K, span, (size_t)-1, !fused_prefill, true);
+}
+
 }  // namespace
 
 void dsi::note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
@@ -256,6 +275,16 @@ size_t dsi_workspace_size(int32_t rows, int32_t n_heads_idx, int32_t n_heads, in
   return p.total > 0 ? p.total : 256;
 }
 
+size_t dsi_layer_workspace_size(const dsi_cache* cache, int32_t rows, int32_t n_heads_idx,
+                                int32_t n_heads, int32_t K, int64_t q_offset, int32_t decode) {
+  if (!cache || rows <= 0 || K <= 0 || n_heads <= 0) return 256;
+  if (!decode && q_offset < 0) return 256;
+  const CacheView v = view_of(cache);
+  const bool fused = uses_fused_prefill(v, n_heads_idx, rows, q_offset, K, decode);
+  const WsPlan p = layer_plan(cache, rows, n_heads_idx, n_heads, K, q_offset, decode, fused);
+  return p.total > 0 ? p.total : 256;
+}
+
 // The fused layer for rows of a decode batch (tokens_per_seq query tokens per
 // sequence) or of a prefill.
 static dsi_status layer_common(const void* q_idx, const float* w, const void* q,
@@ -273,20 +302,19 @@ static dsi_status layer_common(const void* q_idx, const float* w, const void* q,
   if (!aligned(q_idx, 16) || !aligned(q, 16) || !aligned(out, 16)) return DSI_ERR_INVALID_ARG;
   if (!(scale == scale)) return DSI_ERR_INVALID_ARG;
   if (rows == 0) return DSI_OK;
-  const int64_t span = decode ? cache->s_max : q_offset + rows;
-  WsPlan p = plan_workspace(rows, n_heads_idx, n_heads, K, span, (size_t)-1, true, true);
+  CacheView v = view_of(cache);
+  v.tokens_per_seq = tokens_per_seq;
+  const bool fused_prefill = uses_fused_prefill(v, n_heads_idx, rows, q_offset, K, decode);
+  if (!fused_prefill && !index_score_supported(v, n_heads_idx, rows, decode))
+    return DSI_ERR_UNSUPPORTED;
+  // the score rows only exist when the unfused scoring/select pair runs
+  const WsPlan p = layer_plan(cache, rows, n_heads_idx, n_heads, K, q_offset, decode, fused_prefill);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < p.total) return DSI_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   float* scores = reinterpret_cast<float*>(ws + p.scores_off);
   int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + p.idx_off);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* err = status_ptr();
-  CacheView v = view_of(cache);
-  v.tokens_per_seq = tokens_per_seq;
-  const bool fused_prefill = !decode && fused_prefill_topk_supported(v, n_heads_idx, rows,
-                                                                     q_offset, K);
-  if (!fused_prefill && !index_score_supported(v, n_heads_idx, rows, decode))
-    return DSI_ERR_UNSUPPORTED;
   cudaError_t e;
   if (fused_prefill) {
     // prefill: scores stay on chip, only the selected indices are written
@@ -297,8 +325,10 @@ static dsi_status layer_common(const void* q_idx, const float* w, const void* q,
     e = launch_index_score(reinterpret_cast<const bf16*>(q_idx), w, v, rows, n_heads_idx, decode,
                            q_offset, scores, p.ld, err, st);
     if (e != cudaSuccess) return from_cuda(e);
+    // rows are clamped to what the scorer wrote: a decode length above s_max
+    // counts as s_max, as in visible_len()
     e = launch_topk(scores, p.ld, rows, decode ? cache->seq_lens : nullptr, q_offset, K, idx,
-                    count_out, st, tokens_per_seq);
+                    count_out, st, tokens_per_seq, decode ? cache->s_max : q_offset + rows);
     if (e != cudaSuccess) return from_cuda(e);
   }
   e = attend(reinterpret_cast<const bf16*>(q), v, cache, idx, rows, n_heads, K, decode, q_offset,
@@ -359,16 +389,12 @@ dsi_status dsi_latent_fp8_append(const void* x, int64_t n_rows, int64_t ld_x,
                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
-dsi_status dsi_probe_random_gather(const void* base, int64_t row_pitch, int64_t n_src_rows,
-                                   const int32_t* rows, int32_t n_rows, int32_t bytes_per_row,
-                                   int32_t blocks, void* stream) {
-  if (!base || !rows || n_rows < 0 || n_src_rows < 1 || blocks < 1) return DSI_ERR_INVALID_ARG;
-  if (row_pitch < 16 || row_pitch % 16 != 0 || bytes_per_row < 16 || bytes_per_row % 16 != 0 ||
-      bytes_per_row > row_pitch || !aligned(base, 16))
-    return DSI_ERR_INVALID_ARG;
-  if (n_rows == 0) return DSI_OK;
-  return from_cuda(launch_probe_gather(base, row_pitch, n_src_rows, rows, n_rows, bytes_per_row,
-                                       blocks, reinterpret_cast<cudaStream_t>(stream)));
+dsi_status dsi_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000ull) return DSI_ERR_INVALID_ARG;
+  int* err = status_ptr();
+  if (!err) return DSI_ERR_CUDA;
+  return from_cuda(launch_selftest_wait_timeout(limit_ns, err,
+                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dsi_status dsi_get_device_status(void* stream) {

@@ -13,8 +13,11 @@
 // only a stand-in symbol, not a device address).  The first call on each
 // device, with that device current, looks up the array's device address with
 // cudaGetSymbolAddress and caches it; that first call should therefore come
-// before any stream capture.  Nothing here calls cudaMalloc, cudaFree or an
-// allocating library routine.
+// before any stream capture.  The cache is an atomic per device, so host
+// threads that make their first calls at once both store the same address.
+// The address belongs to the device's primary context: after
+// cudaDeviceReset() the library must not be called again in the process.
+// Nothing here calls cudaMalloc, cudaFree or an allocating library routine.
 //
 // Every call shares the one array and leaves its contents behind: calls whose
 // kernels overlap on the GPU (different streams, or different host threads on
@@ -24,12 +27,14 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 namespace {
 
 __device__ __align__(256) unsigned char g_static_scratch[DSI_STATIC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];  // device address of g_static_scratch, per device
+std::atomic<void*> g_scratch_addr[kMaxDevices];  // device address of g_static_scratch, per device
 
 // Device address of the scratch array on the current device (looked up once).
 void* scratch_address(dsi_status* st) {
@@ -38,16 +43,16 @@ void* scratch_address(dsi_status* st) {
     *st = DSI_ERR_CUDA;
     return nullptr;
   }
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
+  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
       *st = DSI_ERR_CUDA;
       return nullptr;
     }
-    g_scratch_addr[dev] = p;
+    g_scratch_addr[dev].store(p, std::memory_order_release);
   }
   *st = DSI_OK;
-  return g_scratch_addr[dev];
+  return p;
 }
 
 }  // namespace
@@ -60,8 +65,8 @@ extern "C" dsi_status dsi_indexed_attention_static(const void* q_idx, const floa
                                                    float* lse, void* stream) {
   if (!cache) return DSI_ERR_INVALID_ARG;
   if (rows > 0 && K > 0 && n_heads > 0) {
-    const int64_t span = decode ? cache->s_max : q_offset + rows;
-    const size_t need = dsi_workspace_size(rows, n_heads_idx, n_heads, K, span, decode);
+    const size_t need =
+        dsi_layer_workspace_size(cache, rows, n_heads_idx, n_heads, K, q_offset, decode);
     if (need > (size_t)DSI_STATIC_SCRATCH_BYTES) return DSI_ERR_WORKSPACE;
   }
   dsi_status st;

@@ -63,10 +63,12 @@ cudaError_t launch_index_topk_prefill(const bf16* q_idx, const float* w, const C
 // ---- Top-K -------------------------------------------------------------------
 // row_len: candidates per row, or per sequence when tokens_per_seq > 1 (row r
 // is token r % T of sequence r / T and has row_len[r / T] - (T - 1 - r % T));
-// null: the causal prefill rule q_offset + r + 1.
+// null: the causal prefill rule q_offset + r + 1.  Row lengths are clamped
+// to n_cap (negative: ld), the longest row the scorer wrote (s_max for a
+// decode batch: its visible lengths never exceed the cache's rows).
 cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t* row_len,
                         int64_t q_offset, int K, int32_t* idx, int32_t* count,
-                        cudaStream_t st, int tokens_per_seq = 1);
+                        cudaStream_t st, int tokens_per_seq = 1, int64_t n_cap = -1);
 
 // ---- sparse MLA ----------------------------------------------------------------
 // part_o / part_ml: split-K partials (may be null when splits == 1).
@@ -86,9 +88,9 @@ cudaError_t launch_mxfp8_quantize(const bf16* x, int64_t n_rows, int d, int64_t 
                                   const int64_t* dst_rows, uint8_t* codes, uint8_t* scales,
                                   cudaStream_t st);
 
-// Diagnostic random-row gather (probe_gather.cu).
-cudaError_t launch_probe_gather(const void* base, int64_t row_pitch, int64_t n_src_rows,
-                                const int32_t* rows, int n_rows, int bytes_per_row, int blocks,
-                                cudaStream_t st);
+// ---- failure detection self-test (selftest.cu) ------------------------------
+// One warp waits, with the given limit, on an mbarrier nothing arrives at:
+// the timeout path of every bounded wait, run on purpose.
+cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, int* err, cudaStream_t st);
 
 }  // namespace dsi

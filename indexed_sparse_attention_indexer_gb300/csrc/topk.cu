@@ -38,9 +38,9 @@ __device__ __forceinline__ uint32_t load_key(const uint32_t* skeys, const float*
 }
 
 __global__ void __launch_bounds__(kTopkThreads)
-topk_rows(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
-          int64_t q_offset, int K, int32_t* __restrict__ idx, int32_t* __restrict__ count,
-          int stage, int tps) {
+topk_rows(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
+          const int32_t* __restrict__ row_len, int64_t q_offset, int K, int32_t* __restrict__ idx,
+          int32_t* __restrict__ count, int stage, int tps) {
   extern __shared__ uint32_t topk_smem[];
   __shared__ int hist[256];
   __shared__ int scan_ws[40];
@@ -52,7 +52,7 @@ topk_rows(const float* __restrict__ scores, int64_t ld, const int32_t* __restric
               : tps == 1 ? (int64_t)row_len[r]
                          : (int64_t)row_len[r / tps] - (tps - 1 - r % tps);
   if (n < 0) n = 0;
-  if (n > ld) n = ld;
+  if (n > n_cap) n = n_cap;   // the scorer's visible length never exceeds it
   int32_t* out = idx + (int64_t)r * K;
   const float* grow = scores + (int64_t)r * ld;
 
@@ -167,9 +167,9 @@ __device__ __forceinline__ void load_chunk(uint32_t* key, const float* grow, int
 
 template <bool kChunked>
 __global__ void __launch_bounds__(kTopkThreads, 1)
-topk_rows_reg(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
-              int64_t q_offset, int K, int32_t* __restrict__ idx, int32_t* __restrict__ count,
-              int tps) {
+topk_rows_reg(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
+              const int32_t* __restrict__ row_len, int64_t q_offset, int K,
+              int32_t* __restrict__ idx, int32_t* __restrict__ count, int tps) {
   __shared__ int hist[2][kBins];          // alternate passes; each is cleared as it is read
   __shared__ int wsum[2][kWarps];
   __shared__ int wbase[2][kWarps];
@@ -186,7 +186,7 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, const int32_t* __res
               : tps == 1 ? (int64_t)row_len[r]
                          : (int64_t)row_len[r / tps] - (tps - 1 - r % tps);
   if (n < 0) n = 0;
-  if (n > ld) n = ld;
+  if (n > n_cap) n = n_cap;   // the scorer's visible length never exceeds it
   int32_t* out = idx + (int64_t)r * K;
   const float* grow = scores + (int64_t)r * ld;
   if (n <= K) {  // every candidate is kept
@@ -354,16 +354,17 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, const int32_t* __res
 
 cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t* row_len,
                         int64_t q_offset, int K, int32_t* idx, int32_t* count, cudaStream_t st,
-                        int tps) {
+                        int tps, int64_t n_cap) {
   if (rows <= 0) return cudaSuccess;
-  const int64_t longest = row_len ? ld : (q_offset + rows < ld ? q_offset + rows : ld);
+  n_cap = (n_cap < 0 || n_cap > ld) ? ld : n_cap;
+  const int64_t longest = row_len ? n_cap : (q_offset + rows < n_cap ? q_offset + rows : n_cap);
   if (longest <= kRegChunks * kRegKeysMax) {
     cudaError_t e =
         longest <= kRegKeysMax
             ? launch_overlapped(topk_rows_reg<false>, dim3(rows), dim3(kTopkThreads), 0, st, scores,
-                                ld, row_len, q_offset, K, idx, count, tps)
+                                ld, n_cap, row_len, q_offset, K, idx, count, tps)
             : launch_overlapped(topk_rows_reg<true>, dim3(rows), dim3(kTopkThreads), 0, st, scores,
-                                ld, row_len, q_offset, K, idx, count, tps);
+                                ld, n_cap, row_len, q_offset, K, idx, count, tps);
     note_launch();
     return e;
   }
@@ -375,8 +376,8 @@ cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  topk_rows<<<rows, kTopkThreads, smem, st>>>(scores, ld, row_len, q_offset, K, idx, count, stage,
-                                                tps);
+  topk_rows<<<rows, kTopkThreads, smem, st>>>(scores, ld, n_cap, row_len, q_offset, K, idx, count,
+                                                stage, tps);
   note_launch();
   return cudaGetLastError();
 }

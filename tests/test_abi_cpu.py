@@ -153,19 +153,6 @@ def test_indexed_attention_multi_validation(L):
     assert call(_cache(batch=0)) == binding.DSI_OK     # no rows: nothing to launch
 
 
-def test_probe_gather_validation(L):
-    E = binding.DSI_ERR_INVALID_ARG
-    P = L.dsi_probe_random_gather
-    assert P(None, 1152, 10, FAKE, 4, 640, 1, None) == E
-    assert P(FAKE, 1152, 10, None, 4, 640, 1, None) == E
-    assert P(FAKE, 1150, 10, FAKE, 4, 640, 1, None) == E      # pitch not a multiple of 16
-    assert P(FAKE, 1152, 10, FAKE, 4, 650, 1, None) == E      # bytes not a multiple of 16
-    assert P(FAKE, 1152, 10, FAKE, 4, 1168, 1, None) == E     # bytes beyond the row
-    assert P(FAKE + 8, 1152, 10, FAKE, 4, 640, 1, None) == E  # misaligned base
-    assert P(FAKE, 1152, 10, FAKE, 4, 640, 0, None) == E
-    assert P(FAKE, 1152, 10, FAKE, 0, 640, 1, None) == binding.DSI_OK
-
-
 def test_mxfp8_validation(L):
     """Host checks of the MXFP8 quantiser and of MXFP8 key caches."""
     E, U = binding.DSI_ERR_INVALID_ARG, binding.DSI_ERR_UNSUPPORTED
@@ -217,6 +204,12 @@ def test_latent_fp8_validation(L):
     assert f(FAKE, ctypes.byref(c), FAKE, 4, 16, 64, 0.1, FAKE, None, None, 0, None) == E
 
 
+def test_selftest_wait_timeout_validation(L):
+    E = binding.DSI_ERR_INVALID_ARG
+    assert L.dsi_selftest_wait_timeout(999, None) == E            # below 1 us
+    assert L.dsi_selftest_wait_timeout(1000000001, None) == E     # above 1 s
+
+
 def test_topk_validation(L):
     E, U = binding.DSI_ERR_INVALID_ARG, binding.DSI_ERR_UNSUPPORTED
     assert L.dsi_topk(None, 16, 2, None, 0, 4, FAKE, None, None) == E
@@ -264,6 +257,23 @@ def test_workspace_size(L):
     assert a >= 64 * 32768 * 4 + 64 * 2048 * 4
     assert L.dsi_workspace_size(64, 64, 128, 2048, 65536, 1) > a
     assert L.dsi_workspace_size(0, 64, 128, 2048, 32768, 1) == 256
+
+
+def test_layer_workspace_size(L):
+    """The exact size of one call: a decode call needs what the upper bound
+    gives; no call needs more than it; degenerate sizes give 256."""
+    c = _cache(batch=64, s_max=32768)
+    ws = L.dsi_layer_workspace_size
+    assert ws(ctypes.byref(c), 64, 64, 128, 2048, 0, 1) == L.dsi_workspace_size(64, 64, 128, 2048,
+                                                                                32768, 1)
+    p = _cache(batch=1, s_max=8192, seq_lens=None)
+    for T, off in ((8192, 0), (4096, 4096), (100, 7)):
+        assert ws(ctypes.byref(p), T, 64, 128, 2048, off, 0) <= L.dsi_workspace_size(
+            T, 64, 128, 2048, off + T, 0)
+        # an index row per token at least
+        assert ws(ctypes.byref(p), T, 64, 128, 2048, off, 0) >= T * 2048 * 4
+    assert ws(None, 64, 64, 128, 2048, 0, 1) == 256
+    assert ws(ctypes.byref(c), 0, 64, 128, 2048, 0, 1) == 256
 
 
 def test_binding_rejects_strided_rows():

@@ -324,3 +324,27 @@ def test_checked_build_flags_out_of_range_index():
     binding.sparse_mla_decode(g.q, binding.Cache.of(g), idx, ws.scale, checked=True)
     assert binding.device_status(checked=True) == binding.DSI_ERR_BOUNDS
     assert binding.device_status(checked=True) == 0   # read clears it
+
+
+@pytest.mark.parametrize("Hi,d,H", [(64, 128, 128), (4, 64, 16)])
+def test_decode_length_above_s_max_is_clamped(Hi, d, H):
+    """A seq_lens entry above a contiguous cache's s_max (here 100, not a
+    multiple of 64) counts as s_max in every kernel: scoring, Top-K (whose
+    score rows are 128 wide) and attention see the same clamped history, and
+    the result equals the oracle on that history."""
+    ws = W.make_decode(3, 100, Hi, d, 32, H, seed=31, lengths=[100, 77, 100])
+    g = ws.to(DEV)
+    g.seq_lens = torch.tensor([130, 77, 5000], dtype=torch.int32, device=DEV)
+    cache = binding.Cache.of(g)
+    for _ in range(2):     # the second call runs over the first call's workspace
+        out, lse, idx, count = binding.indexed_attention(g.q_idx, g.w, g.q, cache, ws.K, ws.scale,
+                                                         True)
+        torch.cuda.synchronize()
+        ref = oracle.layer(ws)     # ws keeps the clamped lengths [100, 77, 100]
+        for b in range(ws.B):
+            assert np.array_equal(idx[b].cpu().numpy(), ref[b]["idx"]), f"row {b}"
+            assert int(count[b]) == ref[b]["count"]
+            assert int(idx[b].max()) < 100
+        assert_out_close(out.float().cpu().numpy(), np.stack([ref[b]["out"] for b in range(ws.B)]),
+                         "clamped")
+    assert binding.device_status() == 0

@@ -46,6 +46,10 @@ CASES = {
                                                    lengths=[3000, 700, 64, 1500], page_size=64,
                                                    k_fp8=True),
     "prefill_hi64": lambda: W.make_prefill(96, 400, 64, 128, 128, 128, seed=23, q_offset=304),
+    # 2304 x 2304 fp32 scores alone would be 21 MB: the fused indexer writes
+    # none, so the call fits the 16 MiB scratch
+    "prefill_scores_beyond_scratch": lambda: W.make_prefill(2304, 2304, 64, 128, 256, 128,
+                                                            seed=25),
 }
 
 
@@ -67,6 +71,16 @@ def test_static_matches_workspace_entry_point(name):
         fin = torch.isfinite(ref_lse)
         assert torch.equal(torch.isfinite(lse), fin)
         assert float((lse[fin] - ref_lse[fin]).abs().max()) <= 1e-3
+
+
+def test_static_sizes_prefill_without_score_rows():
+    lib = binding.load()
+    g = CASES["prefill_scores_beyond_scratch"]().to(DEV)
+    cache = binding.Cache.of(g)
+    upper = binding.workspace_size(g.T, g.H_i, g.H, g.K, g.T, False)
+    exact = binding.layer_workspace_size(cache, g.T, g.H_i, g.H, g.K, 0, False)
+    assert upper > (16 << 20) >= exact
+    assert exact < g.T * g.T * 4
 
 
 def test_static_rejects_sizes_beyond_the_scratch():
