@@ -21,17 +21,18 @@
 // take the same softmax decisions.  Per 64-position tile, 12 warps:
 //   producers (warps 0-2): the tile's rows into a 128-byte-swizzled stage
 //     (ring of 3), by TMA gather4 (four rows per instruction) and cp.async at
-//     once, so both copy engines work;
+//     once, so both copy engines work; the cp.async threads arrive on the
+//     stage's barrier when their copies land, without waiting for them;
 //   MMA (warp 3, one thread): S = Qslice . C^T into the free logit tile,
 //     O += P . V (A = P K-major, B = V MN-major, same stage);
-//   exchange (warps 4-7): partial logits out of TMEM, st.async into the
-//     peer's buffer (bytes counted on the peer's barrier), the peer's partial
-//     added, the sum written back into the TMEM tile; one buffer credit per
-//     warp returns to the peer;
-//   softmax (warps 8-11, one head per thread): online softmax in log2 units
-//     with a lazily moved reference max (the accumulator is rescaled only
-//     when the max grows by more than 2^8), P in bf16 to shared memory, and
-//     the epilogue.
+//   exchange (warps 4-7): this CTA's partial logits out of TMEM and into the
+//     peer's buffer (st.async, bytes counted on the peer's barrier);
+//   softmax (warps 8-11, one head per thread): own partial from TMEM plus the
+//     peer's from the buffer (one buffer credit per warp returns to the
+//     peer), online softmax in log2 units with a lazily moved reference max
+//     (the accumulator is rescaled only when the max grows by more than 2^8),
+//     P in bf16 to one of two shared-memory tiles (so P of tile t is written
+//     while P.V of tile t-1 runs), and the epilogue.
 // Every wait is bounded; the cluster syncs once after set-up and once before
 // exit so no CTA leaves while its peer may still write into it.
 #include "kernels.h"
@@ -69,12 +70,12 @@ constexpr int kLdgThreads = kLdgWarps * 32;
 constexpr int kMaxEntries = DSI_MAX_K;         // index entries one split can hold
 
 constexpr int OFF_C = 0;
-constexpr int OFF_P = OFF_C + kStages * kStageBytes;      // P [128 x 64] bf16, 16 KB
-constexpr int OFF_X = OFF_P + kH * kNp * 2;               // kXBufs x peer logits [128 x 64] fp32
+constexpr int OFF_P = OFF_C + kStages * kStageBytes;      // two P tiles [128 x 64] bf16, 16 KB each
+constexpr int OFF_X = OFF_P + 2 * kH * kNp * 2;           // kXBufs x peer logits [128 x 64] fp32
 constexpr int OFF_Q4 = OFF_X + kXBufs * kH * kNp * 4;     // CTA 0's fifth query block [128 x 64] bf16, swizzled
 constexpr int OFF_ROWS = OFF_Q4 + kH * 64 * 2;            // physical row of each entry (or -1)
 constexpr int OFF_BAR = OFF_ROWS + kMaxEntries * 4;
-constexpr int NBARS = 2 * kStages + 10 + 2 * kXBufs;
+constexpr int NBARS = 2 * kStages + 12 + 2 * kXBufs;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM = OFF_MISC + 64 + 1024;
 
@@ -125,11 +126,10 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   uint64_t* empty = bars + kStages;            // [kStages] stage free (MMA commit)
   uint64_t* s_full = bars + 2 * kStages;       // [2] logits in TMEM (MMA commit)
   uint64_t* s_empty = s_full + 2;              // [2] logits read out (softmax threads)
-  uint64_t* p_full = s_full + 4;               // P written (softmax threads)
-  uint64_t* p_empty = s_full + 5;              // P.V done (MMA commit)
-  uint64_t* q_ready = s_full + 6;              // query slice in place (softmax threads)
-  uint64_t* o_done = s_full + 7;               // last P.V done (MMA commit)
-  uint64_t* s_ready = s_full + 8;              // [2] summed logits back in TMEM (exchange warps)
+  uint64_t* p_full = s_full + 4;               // [2] P written (softmax threads)
+  uint64_t* p_empty = s_full + 6;              // [2] P.V done (MMA commit)
+  uint64_t* q_ready = s_full + 8;              // query slice in place (softmax threads)
+  uint64_t* o_done = s_full + 9;               // last P.V done (MMA commit)
   uint64_t* x_full = s_full + 10;              // [kXBufs] peer's partial logits landed (byte count)
   uint64_t* x_empty = x_full + kXBufs;         // [kXBufs] peer has read what we sent (one credit per peer softmax warp)
   int32_t* rows_s = reinterpret_cast<int32_t*>(smem + OFF_ROWS);
@@ -170,11 +170,10 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1 + kLdgThreads); mbar_init(&empty[s], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 128);
-      mbar_init(&s_ready[i], 128);
+      mbar_init(&s_empty[i], 256);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&p_empty[i], 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(p_empty, 1);
     mbar_init(q_ready, 256);
     mbar_init(o_done, 1);
     for (int i = 0; i < kXBufs; ++i) {
@@ -294,12 +293,9 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
         cp_async_16(st_addr + (w >> 3) * kChunkBytes + sw128_offset(rr, w & 7),
                     c.latent + (int64_t)pr * DSI_D_QK + (g0 + (w >> 3)) * 64 + (w & 7) * 8);
       }
-      cp_async_commit();
-      // signal this tile as soon as its own copies have landed (not after the
-      // next tile's issue, which would tie it to an older stage's release)
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(&full[stage]);
+      // the stage's barrier counts this thread once its copies have landed;
+      // the thread goes on to the next stage without waiting for them
+      cp_async_mbar_arrive_noinc(&full[stage]);
       if (++stage == kStages) { stage = 0; ph ^= 1; }
     }
     cp_async_wait<0>();
@@ -313,20 +309,20 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       tc_fence_after();
       int qk_next = 0, pv_next = 0;
       const uint32_t pbase = smem_u32(smem + OFF_P);
-      const uint64_t t_start = global_ns();
-      uint64_t t_last = t_start;
+      uint64_t t_last = global_ns();
+      uint32_t idle = 0;
       while (ok && pv_next < n_tiles) {
         bool progress = false;
-        if (pv_next < qk_next && mbar_test_wait(p_full, pv_next & 1)) {
+        if (pv_next < qk_next && mbar_test_wait(&p_full[pv_next & 1], (pv_next >> 1) & 1)) {
           tc_fence_after();
           const int st = pv_next % kStages;
-          const uint64_t pd = desc_sw128(pbase);
+          const uint64_t pd = desc_sw128(pbase + (pv_next & 1) * (kH * kNp * 2));
           const uint64_t vd = desc_sw128_mn(smem_u32(smem + OFF_C + st * kStageBytes), kChunkBytes);
 #pragma unroll
           for (int kk = 0; kk < kNp / 16; ++kk)
             mma_bf16(tmem + TM_O, pd + (uint64_t)((kk * 32) >> 4), vd + (uint64_t)((kk * 2048) >> 4),
                      IDESC_O, (pv_next > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(p_empty);
+          mma_commit(&p_empty[pv_next & 1]);
           mma_commit(&empty[st]);
           ++pv_next;
           progress = true;
@@ -337,6 +333,8 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
           if (mbar_test_wait(&full[st], (qk_next / kStages) & 1) &&
               mbar_test_wait(&s_empty[sb], ((qk_next >> 1) & 1) ^ 1)) {
             tc_fence_after();
+            // the stage's cp.async part was written through the generic proxy
+            fence_proxy_async_smem();
             const uint32_t t_s = tmem + TM_S + sb * kNp;
             const uint32_t st_base = smem_u32(smem + OFF_C + st * kStageBytes);
             const uint64_t d0 = desc_sw128(st_base + qk_first * kChunkBytes);
@@ -357,27 +355,28 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
             progress = true;
           }
         }
-        // bounded: give up after kWaitLimitNs without progress
+        // bounded: give up after kWaitLimitNs without progress (the clock is
+        // read once per 256 idle probes)
         if (progress) {
+          idle = 0;
           t_last = global_ns();
         } else if (*abort_flag) {
           ok = false;
-        } else if (global_ns() - t_last > kWaitLimitNs) {
+        } else if ((++idle & 255u) == 0 && global_ns() - t_last > kWaitLimitNs) {
           *abort_flag = 1;
           report(err, kErrTimeout);
           ok = false;
         }
       }
-      (void)t_start;
       mma_commit(o_done);
     }
     __syncwarp();
   } else if (warp < kSmWarp0) {
     // ======================= logit exchange ===================================
-    // Per tile: read this CTA's partial logits from TMEM, store them into the
-    // peer's exchange buffer (st.async, bytes counted on the peer's barrier),
-    // add the peer's partial, and write the summed logits back into the same
-    // TMEM tile for the softmax warps.  This runs a tile ahead of the softmax.
+    // Per tile: read this CTA's partial logits from TMEM and store them into
+    // the peer's exchange buffer (st.async, bytes counted on the peer's
+    // barrier) once the peer has read the previous tile out of it.  The
+    // softmax warps read the same TMEM tile and add the peer's partial.
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;               // head = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -397,9 +396,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
     // exchange buffer layout [buffer][4-position group][head] x float4: a
     // warp's stores (and loads) of one group are 512 contiguous bytes
     const uint32_t x_remote = map_to_rank(smem_u32(smem + OFF_X), peer) + h * 16;
-    const uint8_t* xrow = smem + OFF_X + h * 16;
     const uint32_t xfull_remote = map_to_rank(smem_u32(x_full), peer);
-    const uint32_t xempty_remote = map_to_rank(smem_u32(x_empty), peer);
     bool ok = true;
     for (int t = 0; ok && t < n_tiles; ++t) {
       const int sb = t & 1, bsel = t % kXBufs;
@@ -409,6 +406,8 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       tmem_ld32(tmem + lane_base + TM_S + sb * kNp, v);
       tmem_ld32(tmem + lane_base + TM_S + sb * kNp + 32, v + 32);
       tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&s_empty[sb]);
       // this CTA's partial to the peer, once the peer has read the buffer
       if (!(ok = warp_wait_cluster(&x_empty[bsel], ((t / kXBufs) & 1) ^ 1, abort_flag, err))) break;
       const uint32_t dst = x_remote + bsel * kXBytes;
@@ -417,30 +416,6 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
         st_async_v4(dst + q4 * (kH * 16),
                     make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]),
                     xfull_remote + bsel * 8);
-      // the peer's partial of the same tile
-      if (!(ok = warp_wait_cluster(&x_full[bsel], (t / kXBufs) & 1, abort_flag, err))) break;
-#pragma unroll
-      for (int q4 = 0; q4 < kNp / 4; ++q4) {
-        const float4 pv4 = *reinterpret_cast<const float4*>(xrow + bsel * kXBytes +
-                                                            q4 * (kH * 16));
-        v[4 * q4] += pv4.x; v[4 * q4 + 1] += pv4.y; v[4 * q4 + 2] += pv4.z; v[4 * q4 + 3] += pv4.w;
-      }
-      // buffer credit, one per warp: this warp has read the peer's tile t, so
-      // the peer may write tile t+kXBufs there; warp 0 re-arms the byte count.
-      // The loads above completed (their values are summed) before the warp
-      // barrier, so relaxed arrivals suffice; a cluster-scope release here
-      // measured about 15% slower over the whole kernel.
-      __syncwarp();
-      if (lane == 0 && t + kXBufs < n_tiles) {
-        if (quarter == 0) mbar_arrive_expect_tx_relaxed(&x_full[bsel], kXBytes);
-        mbar_arrive_remote_relaxed(xempty_remote + bsel * 8);
-      }
-      // summed logits back into the TMEM tile
-      tmem_st32f(tmem + lane_base + TM_S + sb * kNp, v);
-      tmem_st32f(tmem + lane_base + TM_S + sb * kNp + 32, v + 32);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&s_ready[sb]);
     }
   } else {
     // ======================= softmax + epilogue ================================
@@ -470,7 +445,9 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       tc_fence_before();
       mbar_arrive(q_ready);
     }
-    uint8_t* prow = smem + OFF_P;
+    uint8_t* const pbuf = smem + OFF_P;
+    const uint8_t* xrow = smem + OFF_X + h * 16;
+    const uint32_t xempty_remote = map_to_rank(smem_u32(x_empty), peer);
     const float sl2 = a.scale * kLog2e;
     float m_ref = -INFINITY, l_sum = 0.f;
     bool ok = true;
@@ -478,13 +455,28 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       // summed logits of tile t (frees the TMEM tile for the logits of t+2)
       const int sb = t & 1;
       float vc[kNp];
-      if (!(ok = warp_wait(&s_ready[sb], (t >> 1) & 1, abort_flag, err))) break;
+      const int bsel = t % kXBufs;
+      if (!(ok = warp_wait(&s_full[sb], (t >> 1) & 1, abort_flag, err))) break;
       tc_fence_after();
       tmem_ld32(tmem + lane_base + TM_S + sb * kNp, vc);
       tmem_ld32(tmem + lane_base + TM_S + sb * kNp + 32, vc + 32);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&s_empty[sb]);
+      // the peer's partial logits of the same tile, summed here
+      if (!(ok = warp_wait_cluster(&x_full[bsel], (t / kXBufs) & 1, abort_flag, err))) break;
+#pragma unroll
+      for (int q4 = 0; q4 < kNp / 4; ++q4) {
+        const float4 pv4 = *reinterpret_cast<const float4*>(xrow + bsel * kXBytes +
+                                                            q4 * (kH * 16));
+        vc[4 * q4] += pv4.x; vc[4 * q4 + 1] += pv4.y; vc[4 * q4 + 2] += pv4.z; vc[4 * q4 + 3] += pv4.w;
+      }
+      // buffer credit, one per warp; warp 0 re-arms the byte count first
+      __syncwarp();
+      if (lane == 0 && t + kXBufs < n_tiles) {
+        if (quarter == 0) mbar_arrive_expect_tx_relaxed(&x_full[bsel], kXBytes);
+        mbar_arrive_remote_relaxed(xempty_remote + bsel * 8);
+      }
       // validity of the tile's 64 entries
       const uint32_t m_lo = __ballot_sync(0xffffffffu, rows_s[t * kNp + lane] >= 0);
       const uint32_t m_hi = __ballot_sync(0xffffffffu, rows_s[t * kNp + 32 + lane] >= 0);
@@ -515,12 +507,17 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
         m_ref = tmax;
         rescale = true;
       }
-      // PV(t-1) must be complete before P and the accumulator are touched
-      if (!(ok = warp_wait(p_empty, (t & 1) ^ 1, abort_flag, err))) break;
+      // P tile t&1 is free once PV(t-2) is done
+      if (!(ok = warp_wait(&p_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag, err))) break;
       tc_fence_after();
+      uint8_t* prow = pbuf + (t & 1) * (kH * kNp * 2);
       // TMEM loads/stores are warp-collective: rescale when any head of the
-      // warp needs it (the others multiply by 1)
+      // warp needs it (the others multiply by 1), once PV(t-1) has landed in
+      // the accumulator
       if (__any_sync(0xffffffffu, rescale)) {
+        if (t > 0 && !(ok = warp_wait(&p_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, err)))
+          break;
+        tc_fence_after();
         for (int c0 = 0; c0 < 256; c0 += 32) {
           float o[32];
           tmem_ld32(tmem + lane_base + TM_O + c0, o);
@@ -560,7 +557,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
       l_sum = l_sum * alpha + psum;     // alpha == 1 for heads that did not move their reference
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[t & 1]);
     }
     // ---- epilogue: normalise and store this CTA's 256 output dims ------------
     if (ok && warp_wait(o_done, 0, abort_flag, err)) {

@@ -130,8 +130,8 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 // (.sync.aligned) TMEM instructions so that a timeout in one lane can never
 // leave the warp divergent at such an instruction.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* err) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err));
+                                          int* err, uint64_t limit_ns = kWaitLimitNs) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err, limit_ns));
 }
 __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, int* err) {
@@ -192,12 +192,25 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void cp_async_16(uint32_t saddr, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(saddr), "l"(gmem) : "memory");
 }
+// 4-byte copy (through L1): for small scattered values such as per-row scales.
+__device__ __forceinline__ void cp_async_4(uint32_t saddr, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(saddr), "l"(gmem) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread has issued so far has
+// landed, without waiting here.  The arrival is not added to the barrier's
+// pending count: its expected count must include one per such thread.  The
+// copies are generic-proxy writes: a thread that hands the stage to the
+// tensor core issues fence.proxy.async after it observes the phase.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar))
+               : "memory");
 }
 
 // 2^x on the special-function unit (approximate, flushes denormals; 2^-inf = 0).
