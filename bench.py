@@ -276,13 +276,219 @@ def whole_job_tokens_per_s(tokens_per_rank: int, world: int, steps: int, ms_max:
     return tokens_per_rank * world * steps / (ms_max / 1e3)
 
 
+def _outputs(ws, dev):
+    out = torch.empty((ws.T, ws.H, W.D_LATENT), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((ws.T, ws.H), dtype=torch.float32, device=dev)
+    idx = torch.empty((ws.T, ws.K), dtype=torch.int32, device=dev)
+    cnt = torch.empty((ws.T,), dtype=torch.int32, device=dev)
+    return out, lse, idx, cnt
+
+
+def _layer_step(ws, cache, wsp, bufs, stream):
+    """One call of the fused layer over the workload (the bench's step)."""
+    from indexed_sparse_attention_indexer_gb300 import binding
+    out, lse, idx, cnt = bufs
+    decode = ws.mode == "decode"
+    tps = ws.tokens_per_seq
+    if tps > 1:
+        return lambda: binding.indexed_attention_multi(
+            ws.q_idx, ws.w, ws.q, cache, tps, ws.K, ws.scale, out=out, lse=lse, idx=idx,
+            count=cnt, workspace=wsp, stream=stream)
+    return lambda: binding.indexed_attention(
+        ws.q_idx, ws.w, ws.q, cache, ws.K, ws.scale, decode, ws.q_offset, out=out, lse=lse,
+        idx=idx, count=cnt, workspace=wsp, stream=stream)
+
+
+def _workspace(ws, cache, dev):
+    from indexed_sparse_attention_indexer_gb300 import binding
+    return binding.alloc_workspace(binding.layer_workspace_size(
+        cache, ws.T, ws.H_i, ws.H, ws.K, ws.q_offset, ws.mode == "decode"), dev)
+
+
+def time_steps(step, stream, steps: int, warmup: int, local: int, world: int = 1,
+               flush=None) -> dict:
+    """Warm-up, then exactly ``steps`` steps timed with CUDA events on the
+    launching stream between barriers, nvidia-smi clocks sampled meanwhile.
+    With ``flush`` (a callable writing a buffer larger than L2) every step is
+    timed on its own after a flush, for workloads that would sit in L2."""
+    from indexed_sparse_attention_indexer_gb300 import binding
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_end = time.time() + 0.3        # keep the GPU busy while the sampler starts
+    while time.time() < t_end:
+        step()
+        torch.cuda.synchronize()
+    l0 = binding.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark(True)
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_local = e0.elapsed_time(e1)
+    else:
+        evs = []
+        for _ in range(steps):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        ms_local = sum(a.elapsed_time(b) for a, b in evs)
+    clocks.mark(False)
+    barrier(world)
+    launches = binding.launch_count() - l0
+    return {"ms_local": ms_local, "clocks": clocks.stop(), "launches": launches}
+
+
+def _tensor_line(kname, flops, ms, tfl, src, workload):
+    a_tf = flops / (ms / 1e3) / 1e12
+    return {"bound": "tensor", "kernel": kname, "achieved": round(a_tf, 1), "peak": tfl,
+            "unit": "TFLOP/s", "frac": round(a_tf / tfl, 4), "peak_source": src,
+            "traffic": recorded_traffic(kname, workload), "algorithmic_flops": flops,
+            "kernel_ms": round(ms, 5)}
+
+
+def _score_roofline(ws, cache, span, stream, dev, n, hbm, src):
+    """The indexer scoring launch timed alone (decode: the dominant kernel)."""
+    from indexed_sparse_attention_indexer_gb300 import binding
+    scores = torch.empty((ws.T, span), dtype=torch.float32, device=dev)
+    k_ms = time_alone(lambda: binding.index_score(ws.q_idx, ws.w, cache, True, 0, scores=scores,
+                                                  ld=span, stream=stream), stream, n)
+    kbytes = scoring_kernel_bytes(ws)
+    achieved = kbytes / (k_ms / 1e3) / 1e9
+    return {"bound": "hbm", "kernel": "index_score", "achieved": round(achieved, 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": src,
+            "traffic": recorded_traffic("index_score", ws.name), "algorithmic_bytes": kbytes,
+            "kernel_ms": round(k_ms, 5)}
+
+
+def _prefill_rooflines(parts, cache, part_bufs, wsp, stream, n, tfl, src):
+    """Both prefill kernels timed alone over the step's calls (one workload,
+    or a rank's zigzag segments), against their algorithmic flops."""
+    from indexed_sparse_attention_indexer_gb300 import binding
+    if not isinstance(parts, (list, tuple)):
+        parts, part_bufs = [parts], [part_bufs]
+    fl_m = sum(algorithmic_flops(p)["mla"] for p in parts)
+    fl_i = sum(algorithmic_flops(p)["indexer"] for p in parts)
+
+    def mla():
+        for p, (out, lse, idx, _) in zip(parts, part_bufs):
+            binding.sparse_mla_prefill(p.q, cache, idx, p.q_offset, p.scale, out=out, lse=lse,
+                                       workspace=wsp, stream=stream)
+
+    def indexer():
+        for p, (_, _, idx, cnt) in zip(parts, part_bufs):
+            binding.index_topk_prefill(p.q_idx, p.w, cache, p.K, p.q_offset, idx=idx, count=cnt,
+                                       stream=stream)
+    # the indexer first: the attention core reads the indices it writes
+    i_ms = time_alone(indexer, stream, n)
+    m_ms = time_alone(mla, stream, n)
+    name = parts[0].name
+    return (_tensor_line("mla_tc", fl_m, m_ms, tfl, src, name),
+            _tensor_line("index_topk_prefill", fl_i, i_ms, tfl, src, name))
+
+
+def prefill_parts(ws, world: int, rank: int):
+    """This rank's zigzag segments of a prefill, each a workload of its own
+    (query rows sliced, query offset at the segment's start, cache shared)."""
+    from indexed_sparse_attention_indexer_gb300 import partition
+    out = []
+    for a, b in partition.zigzag_segments(ws.T, world)[rank]:
+        out.append(W.Workload(ws.name, "prefill", ws.H_i, ws.d, ws.K, ws.H, ws.scale,
+                              ws.q_idx[a:b], ws.w[a:b], ws.q[a:b], ws.k_idx, ws.k_scale,
+                              ws.latent, ws.seq_lens, ws.block_table, ws.page_size,
+                              ws.q_offset + a, dict(ws.meta), ws.latent_scale))
+    return out
+
+
+def _l2_flusher(dev):
+    buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    state = {"i": 0}
+
+    def flush():
+        state["i"] += 1
+        buf.fill_(state["i"] & 255)
+    return flush
+
+
+def measure_config(cfg: int, args, stream, dev, local: int) -> dict:
+    """One entry of the per-config table (1 GPU, same invocation as the
+    headline): step time, tokens/s, rooflines and clocks."""
+    from indexed_sparse_attention_indexer_gb300 import binding
+    hbm, tfl, src = peaks()
+    steps = max(3, min(args.steps, 20))
+    n = max(3, min(args.steps, 10))
+    entry = {"workload": W.CONFIGS[cfg]["name"]}
+    if cfg == 4:
+        c = W.CONFIGS[4]
+        k_idx, latent = W.make_long_cache(c["S"], c["d"], c["seed"], dev)
+        chunks = []
+        n_chunks = c["S"] // c["T"]
+        for ch in sorted({0, 7, 15, 23, n_chunks - 1}):
+            ws = W.make_chunk(k_idx, latent, ch, c["T"], c["H_i"], c["K"], c["H"], c["seed"],
+                              name=c["name"])
+            cache = binding.Cache.of(ws)
+            wsp = _workspace(ws, cache, dev)
+            bufs = _outputs(ws, dev)
+            tm = time_steps(_layer_step(ws, cache, wsp, bufs, stream), stream, max(3, steps // 4),
+                            args.warmup, local)
+            ms = tm["ms_local"] / max(3, steps // 4)
+            mla, idxr = _prefill_rooflines(ws, cache, bufs, wsp, stream, 3, tfl, src)
+            chunks.append({"chunk": ch, "history_end": (ch + 1) * c["T"], "ms_per_step": round(ms, 4),
+                           "tokens_per_s": round(ws.T / (ms / 1e3), 1),
+                           "roofline": mla, "indexer_roofline": idxr, "clocks": tm["clocks"]})
+            del ws, cache, wsp, bufs
+            torch.cuda.empty_cache()
+        entry.update({"unit": UNIT, "chunk_tokens": c["T"], "chunks": chunks,
+                      "note": "chunks sampled across the 32 of the sequence; tokens/s per chunk "
+                              "falls as its causal history (indexer work) grows"})
+        return entry
+    ws = W.make_config(cfg, device=dev)
+    cache = binding.Cache.of(ws)
+    wsp = _workspace(ws, cache, dev)
+    bufs = _outputs(ws, dev)
+    decode = ws.mode == "decode"
+    flush = _l2_flusher(dev) if cfg == 1 else None   # its 0.4 MB would otherwise sit in L2
+    tm = time_steps(_layer_step(ws, cache, wsp, bufs, stream), stream, steps, args.warmup, local,
+                    flush=flush)
+    ms = tm["ms_local"] / steps
+    ab = algorithmic_bytes(ws)
+    gbs = ab["total"] / (ms / 1e3) / 1e9
+    entry.update({"ms_per_step": round(ms, 5), "tokens_per_s": round(ws.T / (ms / 1e3), 1),
+                  "unit": UNIT, "hbm_gbs_step": round(gbs, 1), "hbm_frac_step": round(gbs / hbm, 4),
+                  "algorithmic_bytes_per_step": ab["total"], "clocks": tm["clocks"],
+                  "gpu_launches_per_step": tm["launches"] / steps})
+    if cfg == 1:
+        entry["us_per_call"] = round(ms * 1e3, 2)
+        entry["l2"] = "256 MB written before every timed call (the workload fits in L2)"
+        entry["note"] = "latency-bound: 0.4 MB per call"
+    if decode:
+        span = cache.struct.s_max
+        entry["roofline"] = _score_roofline(ws, cache, span, stream, dev, n, hbm, src)
+    else:
+        entry["roofline"], entry["indexer_roofline"] = _prefill_rooflines(
+            ws, cache, bufs, wsp, stream, n, tfl, src)
+    del ws, cache, wsp, bufs
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_gpu(args):
     from indexed_sparse_attention_indexer_gb300 import binding
 
     world, rank, local = dist_setup()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    cfg = W.CONFIGS[args.config]
     # seeded per config; each rank its own replica (--rows: a smaller decode batch
     # for profiling captures, never a bench line)
     ws = W.make_config(args.config, device=dev, rows=args.rows, tokens_per_seq=args.tokens_per_seq,
@@ -296,51 +502,21 @@ def run_gpu(args):
     cache = binding.Cache.of(ws)
     decode = ws.mode == "decode"
     span = cache.struct.s_max if decode else ws.q_offset + ws.T
-    wsp = binding.alloc_workspace(
-        binding.workspace_size(ws.T, ws.H_i, ws.H, ws.K, span, decode), dev)
-    out = torch.empty((ws.T, ws.H, W.D_LATENT), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((ws.T, ws.H), dtype=torch.float32, device=dev)
-    idx = torch.empty((ws.T, ws.K), dtype=torch.int32, device=dev)
-    cnt = torch.empty((ws.T,), dtype=torch.int32, device=dev)
-
-    def step():
-        if tps > 1:
-            binding.indexed_attention_multi(ws.q_idx, ws.w, ws.q, cache, tps, ws.K, ws.scale,
-                                            out=out, lse=lse, idx=idx, count=cnt, workspace=wsp,
-                                            stream=stream)
-        else:
-            binding.indexed_attention(ws.q_idx, ws.w, ws.q, cache, ws.K, ws.scale, decode,
-                                      ws.q_offset, out=out, lse=lse, idx=idx, count=cnt,
-                                      workspace=wsp, stream=stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    clocks.start()
-    # keep the GPU busy while the sampler starts, then time exactly K steps
-    t_end = time.time() + 0.3
-    while time.time() < t_end:
-        step()
-        torch.cuda.synchronize()
-    l0 = binding.launch_count()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks.mark(True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    clocks.mark(False)
-    barrier(world)
-    launches = binding.launch_count() - l0
-    ms_local = e0.elapsed_time(e1)
-    clk = clocks.stop()
-    ms = max_over_ranks(ms_local, world)
+    # decode: every rank runs its own batch (replicas); prefill: the ranks
+    # share the query rows of one sequence in zigzag segment pairs, each over
+    # the whole (replicated) causal history
+    parts = [ws] if (decode or world == 1) else prefill_parts(ws, world, rank)
+    wsp = _workspace(max(parts, key=lambda p: p.T), cache, dev)
+    part_bufs = [_outputs(p, dev) for p in parts]
+    bufs = part_bufs[0]
+    steps_of = [_layer_step(p, cache, wsp, b, stream) for p, b in zip(parts, part_bufs)]
+    tm = time_steps(lambda: [f() for f in steps_of], stream, args.steps, args.warmup, local,
+                    world)
+    launches, clk = tm["launches"], tm["clocks"]
+    ms = max_over_ranks(tm["ms_local"], world)
     ms_step = ms / args.steps
-    value = whole_job_tokens_per_s(ws.T, world, args.steps, ms)
+    rows_job = ws.T * (world if decode else 1)      # query tokens all ranks processed per step
+    value = rows_job * args.steps / (ms / 1e3)
 
     hbm, tfl, src = peaks()
     extra = {}
@@ -355,42 +531,21 @@ def run_gpu(args):
                     "traffic": None, "algorithmic_bytes": ab_step, "kernel_ms": round(ms_step, 5)}
     elif decode:
         # ---- dominant kernel: the indexer scoring launch, timed alone ------
-        scores = torch.empty((ws.T, span), dtype=torch.float32, device=dev)
-        k_ms = time_alone(lambda: binding.index_score(ws.q_idx, ws.w, cache, decode, ws.q_offset,
-                                                      scores=scores, ld=span, stream=stream),
-                          stream, max(10, args.steps))
-        kbytes = scoring_kernel_bytes(ws)
-        achieved = kbytes / (k_ms / 1e3) / 1e9
-        kname = "index_score"
-        roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
-                    "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": src,
-                    "traffic": recorded_traffic(kname, wname),
-                    "algorithmic_bytes": kbytes, "kernel_ms": round(k_ms, 5)}
+        roofline = _score_roofline(ws, cache, span, stream, dev, max(10, args.steps), hbm, src)
     else:
         # ---- prefill: both halves are dense contractions on the tensor cores;
         # the attention core dominates, the fused indexer is reported beside it
-        fl = algorithmic_flops(ws)
         nk = max(3, min(10, args.steps))
-        m_ms = time_alone(lambda: binding.sparse_mla_prefill(ws.q, cache, idx, ws.q_offset, ws.scale,
-                                                             out=out, lse=lse, workspace=wsp,
-                                                             stream=stream), stream, nk)
-        i_ms = time_alone(lambda: binding.index_topk_prefill(ws.q_idx, ws.w, cache, ws.K,
-                                                             ws.q_offset, idx=idx, count=cnt,
-                                                             stream=stream), stream, nk)
-
-        def tensor_line(kname, flops, ms):
-            a_tf = flops / (ms / 1e3) / 1e12
-            return {"bound": "tensor", "kernel": kname, "achieved": round(a_tf, 1), "peak": tfl,
-                    "unit": "TFLOP/s", "frac": round(a_tf / tfl, 4), "peak_source": src,
-                    "traffic": recorded_traffic(kname, cfg["name"]),
-                    "algorithmic_flops": flops, "kernel_ms": round(ms, 5)}
-        roofline = tensor_line("mla_tc", fl["mla"], m_ms)
-        extra["indexer_roofline"] = tensor_line("index_topk_prefill", fl["indexer"], i_ms)
+        roofline, extra["indexer_roofline"] = _prefill_rooflines(parts, cache, part_bufs, wsp,
+                                                                 stream, nk, tfl, src)
     ab = algorithmic_bytes(ws)
     step_gbs = ab["total"] / (ms_step / 1e3) / 1e9
 
     # ---- end to end through the public API with host buffers ---------------
-    e2e = run_e2e(ws, cache, wsp, decode, args, stream, dev)
+    e2e = run_e2e(parts, cache, wsp, decode, args, stream, dev)
+    if world > 1:
+        e2e["value"] = round(rows_job * args.steps / (max_over_ranks(e2e["ms_per_step"], world)
+                                                      * args.steps / 1e3), 1)
 
     result = None
     if rank == 0:
@@ -398,12 +553,10 @@ def run_gpu(args):
         result = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak" if decode else "strong",
+            "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded generators; integer-valued indexer inputs, N(0,1) latent)",
-            "config": {"workload": wname, "batch": ws.T, "history": int(ws.s_max),
-                       "indexer": f"{ws.H_i}x{ws.d}", "topk": ws.K, "mla_heads": ws.H,
-                       "parallelism": f"replicas x{world} (batch shards, no collective)",
-                       "l2": "inputs larger than L2 (537 MB of index keys streamed per step)"},
+            "config": config_dict(ws, world),
             "hbm_gbs_step": round(step_gbs, 1),
             "hbm_frac_step": round(step_gbs / hbm, 4),
             "algorithmic_bytes_per_step": ab, "algorithmic_flops_per_step": fl,
@@ -420,28 +573,53 @@ def run_gpu(args):
         if mxg:
             result["config"]["index_keys"] = f"mxfp8 (E4M3 + E8M0 per {mxg})"
             result["config"]["l2"] = "inputs larger than L2 (MXFP8 index keys streamed per step)"
-        if world == 1 and not args.no_cpu:
-            result["cpu_baseline"] = cpu_baseline(ws, budget_s=args.cpu_seconds)
+    del wsp, bufs, part_bufs
+    torch.cuda.empty_cache()
+    plain = (args.config == 2 and not args.rows and tps == 1 and ws.latent_scale is None
+             and not getattr(args, "k_mx_group", 0))
+    if world == 1 and plain and not args.no_configs:
+        # every workload of the table, measured in this same invocation
+        table = {}
+        for c in sorted(W.CONFIGS):
+            if c == args.config:
+                table[str(c)] = {"workload": wname, "ms_per_step": round(ms_step, 5),
+                                 "tokens_per_s": round(value, 1), "unit": UNIT,
+                                 "hbm_gbs_step": round(step_gbs, 1),
+                                 "hbm_frac_step": round(step_gbs / hbm, 4),
+                                 "roofline": roofline, "clocks": clk, "headline": True}
+            else:
+                table[str(c)] = measure_config(c, args, stream, dev, local)
+        result["configs"] = table
+    if rank == 0 and world == 1 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(ws, budget_s=args.cpu_seconds)
     barrier(world)
     return result
 
 
-def run_e2e(ws, cache, wsp, decode, args, stream, dev):
+def config_dict(ws, world: int = 1) -> dict:
+    """The ``config`` object of a line (shared by the GPU and reference arms)."""
+    return {"workload": ws.name, "batch": ws.T, "history": int(ws.s_max),
+            "indexer": f"{ws.H_i}x{ws.d}", "topk": ws.K, "mla_heads": ws.H,
+            "parallelism": (f"replicas x{world} (batch shards, no collective)" if ws.mode == "decode"
+                            else f"query-row shards x{world} (zigzag segment pairs, replicated cache, no collective)"),
+            "l2": "inputs larger than L2 (index keys and latent rows streamed per step)"}
+
+
+def run_e2e(parts, cache, wsp, decode, args, stream, dev):
     """Same metric through binding.indexed_attention with the per-step inputs
     (q_idx, w, q) copied from pinned host memory and the output read back every
     step; the caches stay resident as they would in serving.  As a server
     would, the copies of one step overlap the computation of its neighbour:
     two device input/output sets alternate, host-to-device copies run on one
-    side stream and device-to-host reads on another, ordered by events."""
+    side stream and device-to-host reads on another, ordered by events.
+    ``parts``: the step's calls (one workload, or a rank's prefill segments)."""
     from indexed_sparse_attention_indexer_gb300 import binding
-    h_qidx = ws.q_idx.cpu().pin_memory()
-    h_w = ws.w.cpu().pin_memory()
-    h_q = ws.q.cpu().pin_memory()
-    h_out = [torch.empty((ws.T, ws.H, W.D_LATENT), dtype=torch.bfloat16).pin_memory()
-             for _ in range(2)]
-    sets = [(torch.empty_like(ws.q_idx), torch.empty_like(ws.w), torch.empty_like(ws.q),
-             torch.empty((ws.T, ws.H, W.D_LATENT), dtype=torch.bfloat16, device=dev))
-            for _ in range(2)]
+    host = [(p.q_idx.cpu().pin_memory(), p.w.cpu().pin_memory(), p.q.cpu().pin_memory(),
+             [torch.empty((p.T, p.H, W.D_LATENT), dtype=torch.bfloat16).pin_memory()
+              for _ in range(2)]) for p in parts]
+    sets = [[(torch.empty_like(p.q_idx), torch.empty_like(p.w), torch.empty_like(p.q),
+              torch.empty((p.T, p.H, W.D_LATENT), dtype=torch.bfloat16, device=dev))
+             for p in parts] for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()
     computed = [ev(), ev()]     # step on set i finished computing
@@ -451,28 +629,30 @@ def run_e2e(ws, cache, wsp, decode, args, stream, dev):
 
     def step(k):
         i = k & 1
-        d_qidx, d_w, d_q, d_out = sets[i]
         landed = ev()
         with torch.cuda.stream(s_in):
             s_in.wait_event(computed[i])          # step k-2 no longer reads set i
-            d_qidx.copy_(h_qidx, non_blocking=True)
-            d_w.copy_(h_w, non_blocking=True)
-            d_q.copy_(h_q, non_blocking=True)
+            for (h_qidx, h_w, h_q, _), (d_qidx, d_w, d_q, _) in zip(host, sets[i]):
+                d_qidx.copy_(h_qidx, non_blocking=True)
+                d_w.copy_(h_w, non_blocking=True)
+                d_q.copy_(h_q, non_blocking=True)
             landed.record(s_in)
         stream.wait_event(landed)
         stream.wait_event(read_back[i])           # step k-2's output was read
-        if ws.tokens_per_seq > 1:
-            binding.indexed_attention_multi(d_qidx, d_w, d_q, cache, ws.tokens_per_seq, ws.K,
-                                            ws.scale, out=d_out, workspace=wsp, want_lse=False,
-                                            want_idx=False, stream=stream)
-        else:
-            binding.indexed_attention(d_qidx, d_w, d_q, cache, ws.K, ws.scale, decode, ws.q_offset,
-                                      out=d_out, workspace=wsp, want_lse=False, want_idx=False,
-                                      stream=stream)
+        for p, (d_qidx, d_w, d_q, d_out) in zip(parts, sets[i]):
+            if p.tokens_per_seq > 1:
+                binding.indexed_attention_multi(d_qidx, d_w, d_q, cache, p.tokens_per_seq, p.K,
+                                                p.scale, out=d_out, workspace=wsp, want_lse=False,
+                                                want_idx=False, stream=stream)
+            else:
+                binding.indexed_attention(d_qidx, d_w, d_q, cache, p.K, p.scale, decode,
+                                          p.q_offset, out=d_out, workspace=wsp, want_lse=False,
+                                          want_idx=False, stream=stream)
         computed[i].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(computed[i])
-            h_out[i].copy_(d_out, non_blocking=True)
+            for (_, _, _, h_out), (_, _, _, d_out) in zip(host, sets[i]):
+                h_out[i].copy_(d_out, non_blocking=True)
             read_back[i].record(s_out)
 
     for k in range(max(3, args.warmup)):
@@ -488,9 +668,10 @@ def run_e2e(ws, cache, wsp, decode, args, stream, dev):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    bi = h_qidx.numel() * 2 + h_w.numel() * 4 + h_q.numel() * 2
-    bo = h_out[0].numel() * 2
-    return {"value": round(ws.T * args.steps / (ms / 1e3), 1), "unit": UNIT,
+    bi = sum(h[0].numel() * 2 + h[1].numel() * 4 + h[2].numel() * 2 for h in host)
+    bo = sum(h[3][0].numel() * 2 for h in host)
+    rows = sum(p.T for p in parts)
+    return {"value": round(rows * args.steps / (ms / 1e3), 1), "unit": UNIT,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "ms_per_step": round(ms / args.steps, 5),
             "note": "caches resident; per-step queries in, attention output out; copies of a "
@@ -501,40 +682,133 @@ def run_e2e(ws, cache, wsp, decode, args, stream, dev):
 # the oracle (CPU baseline / reference arm)
 # ----------------------------------------------------------------------------
 
-def _cpu_rows(ws_dev, rows):
-    """CPU copy of the sampled decode rows (the oracle's inputs)."""
-    sub = ws_dev.to(ws_dev.q.device)
-    sub.q_idx, sub.w, sub.q = ws_dev.q_idx[rows], ws_dev.w[rows], ws_dev.q[rows]
-    sub.seq_lens = ws_dev.seq_lens[rows]
-    sub.k_idx, sub.latent = ws_dev.k_idx[rows], ws_dev.latent[rows]
-    sub.k_scale = None if ws_dev.k_scale is None else ws_dev.k_scale[rows]
-    return sub.to("cpu")
+def _row_bundle(ws, r: int):
+    """A CPU workload with only what row r of ``ws`` reads: its sequence (its
+    pages gathered in order, for a paged cache; the oracle's paged and
+    contiguous results are pinned equal) or, for prefill, the causal prefix."""
+    d = ws.q.device
+    if ws.mode == "decode":
+        T = ws.tokens_per_seq
+        b = r // T
+        rows = slice(b * T, b * T + T)
+        L = int(ws.seq_lens[b])
+        if ws.block_table is not None:
+            npg = max(1, -(-L // ws.page_size))
+            pages = ws.block_table[b, :npg].to(torch.int64)
 
-
-def _oracle_rows(ws, budget_s: float, start: int = 0):
-    """Run the oracle row by row (starting at ``start``) until ``budget_s`` has
-    passed (at least one row).  Returns (rows done, seconds)."""
-    import oracle
-    rows_done = 0
-    cpu_ws = None if ws.mode == "decode" else ws.to("cpu")
-    t0 = time.perf_counter()
-    while True:
-        r = (start + rows_done) % ws.T
-        if cpu_ws is None:
-            oracle.decode_row(_cpu_rows(ws, [r]), 0)
+            def seq(x):
+                if x is None:
+                    return None
+                raw = x.view(torch.uint8) if x.element_size() == 1 else x   # float8 as bytes
+                y = raw[pages].reshape((1, -1) + tuple(x.shape[2:]))
+                return y.view(x.dtype) if raw is not x else y
         else:
-            oracle.prefill_row(cpu_ws, r)
-        rows_done += 1
-        if time.perf_counter() - t0 >= budget_s or rows_done >= ws.T:
+            def seq(x):
+                return None if x is None else x[b:b + 1]
+        sub = W.Workload(ws.name, "decode", ws.H_i, ws.d, ws.K, ws.H, ws.scale, ws.q_idx[rows],
+                         ws.w[rows], ws.q[rows], seq(ws.k_idx), seq(ws.k_scale), seq(ws.latent),
+                         torch.tensor([L], dtype=torch.int32, device=d), None, 0, 0,
+                         dict(ws.meta), seq(ws.latent_scale))
+        return sub.to("cpu"), ("multi", r % T, T) if T > 1 else ("decode", 0, 1)
+    n = ws.q_offset + r + 1
+    sub = W.Workload(ws.name, "prefill", ws.H_i, ws.d, ws.K, ws.H, ws.scale, ws.q_idx[r:r + 1],
+                     ws.w[r:r + 1], ws.q[r:r + 1], ws.k_idx[:, :n],
+                     None if ws.k_scale is None else ws.k_scale[:, :n], ws.latent[:, :n],
+                     torch.tensor([n], dtype=torch.int32, device=d), None, 0, n - 1, {},
+                     None if ws.latent_scale is None else ws.latent_scale[:, :n])
+    return sub.to("cpu"), ("prefill", 0, 1)
+
+
+def _oracle_one(bundle) -> None:
+    import oracle
+    sub, (kind, t, T) = bundle
+    if kind == "decode":
+        oracle.decode_row(sub, 0)
+    elif kind == "multi":
+        oracle.multi_token_row(sub, t, T)
+    else:
+        oracle.prefill_row(sub, 0)
+
+
+_POOL_BUNDLES = None
+
+
+def _pool_init(bundles):
+    global _POOL_BUNDLES
+    _POOL_BUNDLES = bundles
+
+
+def _pool_task(i: int) -> int:
+    _oracle_one(_POOL_BUNDLES[i % len(_POOL_BUNDLES)])
+    return 1
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _sample_rows(ws, n: int):
+    """Rows spread evenly over the batch (decode) or the prefill's tokens."""
+    n = max(1, min(n, ws.T))
+    return sorted({int(i * ws.T // n) for i in range(n)})
+
+
+def oracle_throughput(ws, budget_s: float, cores: int) -> dict:
+    """Oracle rows per second over a bounded sample of the workload's rows:
+    first one core, then ``cores`` worker processes (spawned: no GPU state is
+    inherited) sharing the sample through shared memory.  The sample's host
+    copies are made before either timed region."""
+    rows = _sample_rows(ws, 2 * cores)
+    bundles = [_row_bundle(ws, r) for r in rows]
+    for sub, _ in bundles:
+        for f in ("q_idx", "w", "q", "k_idx", "k_scale", "latent", "latent_scale", "seq_lens"):
+            x = getattr(sub, f)
+            if x is not None:
+                x.share_memory_()
+    # one core
+    t_one = 0.3 * budget_s
+    done, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_one(bundles[done % len(bundles)])
+        done += 1
+        if time.perf_counter() - t0 >= t_one:
             break
-    return rows_done, time.perf_counter() - t0
+    el1 = time.perf_counter() - t0
+    rate1 = done / el1
+    res = {"single_core": {"value": round(rate1, 3), "rows": done, "seconds": round(el1, 2)}}
+    if cores > 1:
+        # spawned workers (never forked from a process that has touched the
+        # GPU); a worker that dies breaks the pool with an error, it never
+        # hangs the run
+        import concurrent.futures as cf
+        import torch.multiprocessing as tmp
+        with cf.ProcessPoolExecutor(cores, mp_context=tmp.get_context("spawn"),
+                                    initializer=_pool_init, initargs=(bundles,)) as pool:
+            list(pool.map(_pool_task, range(cores), timeout=600))      # warm: imports, first touch
+            n_tasks = max(cores, int(rate1 * cores * 0.7 * budget_s * 0.8))
+            t0 = time.perf_counter()
+            done = sum(pool.map(_pool_task, range(n_tasks), timeout=600))
+            el = time.perf_counter() - t0
+        res["all_cores"] = {"value": round(done / el, 3), "rows": done, "seconds": round(el, 2)}
+    res["sample_rows"] = len(rows)
+    return res
 
 
 def cpu_baseline(ws, budget_s: float = 10.0) -> dict:
-    rows, el = _oracle_rows(ws, budget_s)
-    return {"value": round(rows / el, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{rows} of {ws.T} query rows of the same workload (fp64 numpy oracle, "
-                      f"single-threaded BLAS, inputs copied to the host per row), {el:.1f} s"}
+    cores = host_cores()
+    r = oracle_throughput(ws, budget_s, cores)
+    best = r.get("all_cores", r["single_core"])
+    used = cores if "all_cores" in r else 1
+    return {"value": best["value"], "unit": UNIT, "cores": used, "kind": "oracle",
+            "single_core_value": r["single_core"]["value"], "nproc": cores,
+            "sample": f"{r['sample_rows']} of {ws.T} query rows of the same workload, spread "
+                      f"evenly, cycled: {best['rows']} rows in {best['seconds']} s on {used} "
+                      f"worker processes (fp64 numpy oracle, single-threaded BLAS each); "
+                      f"one core: {r['single_core']['rows']} rows in "
+                      f"{r['single_core']['seconds']} s; host copies made before timing"}
 
 
 def run_reference(args):
@@ -543,33 +817,31 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and rank != 0:
         return None
-    cfg = W.CONFIGS[args.config]
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    if args.config == 4:
+        raise SystemExit("--impl reference takes the single-batch configs (1, 2, 3, 5)")
     ws = W.make_config(args.config, device=dev, k_mx_group=getattr(args, "k_mx_group", 0),
-                       latent_fp8=getattr(args, "latent_fp8", False))
+                       latent_fp8=getattr(args, "latent_fp8", False),
+                       tokens_per_seq=args.tokens_per_seq)
+    cores = host_cores()
+    # each step is a bounded sample: the whole run stays within --cpu-seconds
     per_step = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
-    start = 0
-    for _ in range(args.warmup):
-        n, _ = _oracle_rows(ws, per_step, start)
-        start += n
-    tot_rows, tot_s = 0, 0.0
-    for _ in range(args.steps):
-        n, el = _oracle_rows(ws, per_step, start)
-        start += n
-        tot_rows += n
-        tot_s += el
-    value = tot_rows / tot_s
-    sample = (f"{tot_rows} query rows over {args.steps} timed steps (each a bounded sample of the "
-              f"{ws.T}-row batch, ~{per_step:.1f} s), fp64 numpy oracle, single-threaded BLAS")
+    r = oracle_throughput(ws, per_step * (args.steps + args.warmup), cores)
+    best = r.get("all_cores", r["single_core"])
+    used = cores if "all_cores" in r else 1
+    value = best["value"]
+    sample = (f"{r['sample_rows']} of {ws.T} query rows spread evenly, cycled: {best['rows']} rows "
+              f"in {best['seconds']} s on {used} worker processes (fp64 numpy oracle, "
+              f"single-threaded BLAS each); one core {r['single_core']['value']} rows/s")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 * tot_s / max(1, args.steps), 3),
+            "ms_per_step": round(1e3 * ws.T / value, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (same seeded generators as the GPU arm)",
-            "config": {"workload": ws.name, "batch": ws.T, "history": int(ws.s_max),
-                       "indexer": f"{ws.H_i}x{ws.d}", "topk": ws.K, "mla_heads": ws.H},
-            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "config": config_dict(ws, world),
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": used,
+                             "kind": "oracle", "sample": sample,
+                             "single_core_value": r["single_core"]["value"], "nproc": cores},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -681,38 +953,21 @@ def run_mx_scan():
                       "queries": "N(0,1) bf16", "results": res}))
 
 
-def run_gather_ceiling():
-    """Plain-load bandwidth of the attention core's access pattern: 2048 random
-    distinct rows of each of 64 sequences x 32768 rows x 1152 bytes (the decode
-    workload's latent cache), L2 flushed before each timed launch."""
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    from indexed_sparse_attention_indexer_gb300 import binding
-    binding.load()
-    B, S, K, pitch = 64, 32768, 2048, W.D_QK * 2
-    base = torch.ones(B * S * pitch // 2, dtype=torch.bfloat16, device=dev)
-    g = torch.Generator().manual_seed(0)
-    rows = torch.stack([torch.randperm(S, generator=g)[:K] + b * S for b in range(B)])
-    rows = rows.to(torch.int32).reshape(-1).to(dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    res = []
-    for nbytes in (640, 1152):
-        for blocks in (2 * sms, 4 * sms):
-            best = math.inf
-            for rep_i in range(5):
-                flush.fill_(rep_i & 255)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                binding.probe_random_gather(base, pitch, rows, nbytes, blocks)
-                e1.record()
-                torch.cuda.synchronize()
-                best = min(best, e0.elapsed_time(e1))
-            res.append({"bytes_per_row": nbytes, "blocks": blocks, "us": round(best * 1e3, 1),
-                        "gbs": round(rows.numel() * nbytes / (best / 1e3) / 1e9, 1)})
-    print(json.dumps({"probe": "random_row_gather", "rows": int(rows.numel()),
-                      "cache_bytes": B * S * pitch, "row_pitch": pitch, "results": res,
-                      "best_gbs": max(r["gbs"] for r in res)}))
+def relaunch_ranks(n: int) -> int:
+    """``--gpus N`` without an outside launcher: start N ranks of this script
+    (one per local GPU, NCCL for the timing barrier) through torch's launcher
+    and return its exit status; rank 0 prints the line."""
+    import socket
+    if torch.cuda.device_count() < n:
+        print(json.dumps({"error": f"--gpus {n}: only {torch.cuda.device_count()} GPUs visible"}))
+        return 2
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__),
+           *sys.argv[1:]]
+    return subprocess.run(cmd).returncode
 
 
 def main():
@@ -724,10 +979,10 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="headline line only (skip the per-config table)")
     ap.add_argument("--crossover", action="store_true",
                     help="measurement: dense vs sparse attention as the history grows (not a bench line)")
-    ap.add_argument("--gather-ceiling", action="store_true",
-                    help="diagnostic: random-row gather bandwidth of plain loads (not a bench line)")
     ap.add_argument("--tokens-per-seq", type=int, default=1,
                     help="decode workloads: candidate tokens verified per sequence in one step "
                          "(multi-token decode; the default line is 1)")
@@ -741,9 +996,6 @@ def main():
     ap.add_argument("--rows", type=int, default=None,
                     help="profiling aid: a smaller decode batch (the printed line is not a bench line)")
     args = ap.parse_args()
-    if args.gather_ceiling:
-        run_gather_ceiling()
-        return
     if args.crossover:
         run_crossover()
         return
@@ -751,6 +1003,8 @@ def main():
         run_mx_scan()
         return
     args.warmup = max(3, args.warmup)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(relaunch_ranks(args.gpus))
     if args.impl == "reference":
         line = run_reference(args)
     else:

@@ -44,7 +44,7 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     import bench
     monkeypatch.setenv("WORLD_SIZE", "2")
     monkeypatch.setenv("RANK", "1")
-    args = argparse.Namespace(config=1, steps=1, warmup=0, cpu_seconds=0.1)
+    args = argparse.Namespace(config=1, steps=1, warmup=0, cpu_seconds=0.1, tokens_per_seq=1)
     assert bench.run_reference(args) is None
 
 
@@ -55,10 +55,15 @@ def test_reference_arm_line_on_cpu(monkeypatch):
     import bench
     monkeypatch.delenv("WORLD_SIZE", raising=False)
     monkeypatch.delenv("RANK", raising=False)
-    args = argparse.Namespace(config=1, steps=2, warmup=1, cpu_seconds=0.5)
+    args = argparse.Namespace(config=1, steps=2, warmup=1, cpu_seconds=0.5, tokens_per_seq=1)
     line = bench.run_reference(args)
     assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == bench.host_cores() and cb["nproc"] >= 1
+    assert cb["single_core_value"] > 0
+    # the GPU arm's config keys, so both arms describe the same workload
+    assert set(line["config"]) == {"workload", "batch", "history", "indexer", "topk", "mla_heads",
+                                   "parallelism", "l2"}
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
 
 
@@ -78,3 +83,53 @@ def test_algorithmic_bytes_of_the_quantised_variants():
     assert bench.algorithmic_bytes(mx)["index_keys"] == n * (64 + 2)
     assert bench.algorithmic_bytes(base)["gather"] == sel * 576 * 2
     assert bench.algorithmic_bytes(l8)["gather"] == sel * (576 + 5 * 4)
+
+
+def test_zigzag_partition_covers_and_balances():
+    from indexed_sparse_attention_indexer_gb300 import partition as P
+    for T, world in ((8192, 2), (8192, 8), (4096, 4), (130, 3), (7, 4), (1, 2)):
+        segs = P.zigzag_segments(T, world)
+        rows = sorted(t for r in range(world) for t in P.rank_rows(T, world, r))
+        assert rows == list(range(T)), (T, world)
+        if T >= 64 * world:
+            work = [P.causal_pairs(s, q_offset=0) for s in segs]
+            assert max(work) / min(work) < 1.01, (T, world, work)
+            cont = [P.causal_pairs(s) for s in P.contiguous_segments(T, world)]
+            assert max(cont) / min(cont) > 2.0          # what the zigzag avoids
+    # the pair count is the sum of the visible lengths
+    assert P.causal_pairs([(0, 3)], q_offset=5) == 6 + 7 + 8
+
+
+def _zigzag_rank(rank, world, port, out):
+    """Each rank runs its zigzag rows of a tiny prefill through the oracle (the
+    CPU stand-in for its GPU) and the rows are reassembled on rank 0."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import oracle
+    from indexed_sparse_attention_indexer_gb300 import partition as P
+    from indexed_sparse_attention_indexer_gb300 import workloads as W
+    ws = W.make_prefill(40, 70, 4, 64, 8, 16, seed=9, q_offset=30)   # same seeded cache on every rank
+    mine = {t: oracle.prefill_row(ws, t) for t in P.rank_rows(ws.T, world, rank)}
+    got = [None] * world
+    dist.all_gather_object(got, {t: (r["idx"], r["out"]) for t, r in mine.items()})
+    if rank == 0:
+        merged = {}
+        for part in got:
+            assert not (set(part) & set(merged))
+            merged.update(part)
+        out["rows"] = sorted(merged)
+        ref = oracle.layer(ws)
+        out["same"] = all(
+            (merged[t][0] == ref[t]["idx"]).all() and (merged[t][1] == ref[t]["out"]).all()
+            for t in range(ws.T))
+    dist.destroy_process_group()
+
+
+def test_zigzag_rows_reassemble_to_the_one_rank_result():
+    world = 2
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_zigzag_rank, args=(world, _free_port(), out), nprocs=world, join=True)
+    assert out["rows"] == list(range(40))
+    assert out["same"]
