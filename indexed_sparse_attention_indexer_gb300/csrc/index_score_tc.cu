@@ -83,7 +83,8 @@ struct Cfg {
   static constexpr int OFF_ABF = OFF_A + STAGES * ST_BYTES;         // MXFP8: bf16 A tiles
   static constexpr int OFF_B = OFF_ABF + ABUFS * A_BYTES;
   static constexpr int OFF_SC = OFF_B + 2 * B_BYTES;                // MXFP8: group scales
-  static constexpr int OFF_W = OFF_SC + (MX ? STAGES * SC_BYTES : 0);   // per epilogue warp: weights
+  static constexpr int OFF_KS = OFF_SC + (MX ? STAGES * SC_BYTES : 0);  // FP8: per-stage key scales
+  static constexpr int OFF_W = OFF_KS + (FP8 ? STAGES * kTileM * 4 : 0); // per epilogue warp: weights
   static constexpr int OFF_PREFIX = OFF_W + EPI_WARPS * TOK_PER_THREAD * kHeads * 4;
   static constexpr int OFF_BAR = (OFF_PREFIX + (kMaxGroups + 1) * 4 + 7) & ~7;
   static constexpr int NBARS = 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 2 * ABUFS;
@@ -200,9 +201,12 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
   }
   if (tid == 0) {
     // MXFP8: a stage is empty once every dequantising warp has read it
+    // FP8: the producer warp's 32 lanes also arrive on full (their key-scale
+    // copies), and a stage is empty once the MMAs and every epilogue warp
+    // (which reads its scales) are done with it
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::MX ? C::DQ_WARPS : 1);
+      mbar_init(&full[s], FP8 ? 33 : 1);
+      mbar_init(&empty[s], C::MX ? C::DQ_WARPS : FP8 ? 1 + C::EPI_WARPS : 1);
     }
     for (int i = 0; i < C::ABUFS; ++i) { mbar_init(&a_full[i], C::DQ_WARPS); mbar_init(&a_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
@@ -230,6 +234,8 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     ItemIter it;
     it.init(prefix, a.groups, it_begin, it_end);
     int gprev = -1, qcount = 0, stage = 0;
+    int gvis = -1, gb = 0, win = -1;     // group whose visible length / block-table window is held
+    int64_t gnvis = 0, win0 = -1;
     uint32_t phase = 0;
     uint32_t issued_phase[C::STAGES];
     bool issued[C::STAGES];
@@ -256,62 +262,86 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
           // dequantised (exact in bf16) in the swizzled B slot; the lanes of
           // one group are adjacent, so the group maximum is a butterfly
           const int upg = 1 << (a.lg_group - 4);     // 16-element units per group
-          for (int i = lane; i < C::N * 8; i += 32) {
-            const int n = i >> 3, u = i & 7;
-            const int t = n / kHeads, h = n % kHeads;
-            const int r = g * NT + t;
-            float f[16];
-            float amax = 0.f;
-            if (r < a.rows) {
-              const bf16* src = a.q_idx + ((int64_t)r * kHeads + h) * kD + u * 16;
-              bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(src)), f);
-              bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(src + 8)), f + 8);
+          constexpr int kIters = C::N * 8 / 32, kBatch = 4;
+          static_assert(kIters % kBatch == 0, "whole batches");
+          for (int i0 = 0; i0 < kIters; i0 += kBatch) {
+            // the loads of a batch of units first, then their quantisation
+            uint4 v[kBatch][2];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(f[k]));
-            } else {
-#pragma unroll
-              for (int k = 0; k < 16; ++k) f[k] = 0.f;
+            for (int k = 0; k < kBatch; ++k) {
+              const int i = lane + (i0 + k) * 32;
+              const int n = i >> 3, u = i & 7;
+              const int r = g * NT + n / kHeads;
+              v[k][0] = v[k][1] = make_uint4(0, 0, 0, 0);
+              if (r < a.rows) {
+                const bf16* src = a.q_idx + ((int64_t)r * kHeads + n % kHeads) * kD + u * 16;
+                v[k][0] = __ldg(reinterpret_cast<const uint4*>(src));
+                v[k][1] = __ldg(reinterpret_cast<const uint4*>(src + 8));
+              }
             }
-            for (int m = 1; m < upg; m <<= 1)
-              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-            const int X = mx_exponent(amax);
-            uint4 lo, hi;
-            mx_decode16(mx_encode16(f, X), X, lo, hi);
-            uint8_t* blk = qs + (u >> 2) * (C::N * 128);
-            *reinterpret_cast<uint4*>(blk + sw128_offset(n, (2 * u) & 7)) = lo;
-            *reinterpret_cast<uint4*>(blk + sw128_offset(n, (2 * u + 1) & 7)) = hi;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+              const int i = lane + (i0 + k) * 32;
+              const int n = i >> 3, u = i & 7;
+              float f[16];
+              bf16x8_to_f32(v[k][0], f);
+              bf16x8_to_f32(v[k][1], f + 8);
+              float amax = 0.f;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(f[e]));
+              for (int m = 1; m < upg; m <<= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+              const int X = mx_exponent(amax);
+              uint4 lo, hi;
+              mx_decode16(mx_encode16(f, X), X, lo, hi);
+              uint8_t* blk = qs + (u >> 2) * (C::N * 128);
+              *reinterpret_cast<uint4*>(blk + sw128_offset(n, (2 * u) & 7)) = lo;
+              *reinterpret_cast<uint4*>(blk + sw128_offset(n, (2 * u + 1) & 7)) = hi;
+            }
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&q_full[slot]);
         } else if (FP8) {
-          // round the bf16 index queries to E4M3 into the swizzled B slot
-          for (int i = lane; i < C::N * 8; i += 32) {
-            const int n = i >> 3, u = i & 7;
-            const int t = n / kHeads, h = n % kHeads;
-            const int r = g * NT + t;
-            uint4 outv = make_uint4(0, 0, 0, 0);
-            if (r < a.rows) {
-              const bf16* src = a.q_idx + ((int64_t)r * kHeads + h) * kD + u * 16;
-              const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(src));
-              const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(src + 8));
+          // round the bf16 index queries to E4M3 into the swizzled B slot; the
+          // loads of eight units are issued before any of them is converted
+          constexpr int kIters = C::N * 8 / 32, kBatch = 8;
+          static_assert(kIters % kBatch == 0, "whole batches");
+          for (int i0 = 0; i0 < kIters; i0 += kBatch) {
+            uint4 v[kBatch][2];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+              const int i = lane + (i0 + k) * 32;
+              const int n = i >> 3, u = i & 7;
+              const int r = g * NT + n / kHeads;
+              v[k][0] = v[k][1] = make_uint4(0, 0, 0, 0);
+              if (r < a.rows) {
+                const bf16* src = a.q_idx + ((int64_t)r * kHeads + n % kHeads) * kD + u * 16;
+                v[k][0] = __ldg(reinterpret_cast<const uint4*>(src));
+                v[k][1] = __ldg(reinterpret_cast<const uint4*>(src + 8));
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+              const int i = lane + (i0 + k) * 32;
+              const int n = i >> 3, u = i & 7;
               float f[16];
-              bf16x8_to_f32(v0, f);
-              bf16x8_to_f32(v1, f + 8);
+              bf16x8_to_f32(v[k][0], f);
+              bf16x8_to_f32(v[k][1], f + 8);
               uint32_t wds[4];
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
+              for (int e = 0; e < 4; ++e) {
                 const __nv_fp8x2_storage_t lo =
-                    __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k], f[4 * k + 1]), __NV_SATFINITE,
+                    __nv_cvt_float2_to_fp8x2(make_float2(f[4 * e], f[4 * e + 1]), __NV_SATFINITE,
                                              __NV_E4M3);
                 const __nv_fp8x2_storage_t hi =
-                    __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k + 2], f[4 * k + 3]),
+                    __nv_cvt_float2_to_fp8x2(make_float2(f[4 * e + 2], f[4 * e + 3]),
                                              __NV_SATFINITE, __NV_E4M3);
-                wds[k] = (uint32_t)lo | ((uint32_t)hi << 16);
+                wds[e] = (uint32_t)lo | ((uint32_t)hi << 16);
               }
-              outv = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+              *reinterpret_cast<uint4*>(qs + sw128_offset(n, u)) =
+                  make_uint4(wds[0], wds[1], wds[2], wds[3]);
             }
-            *reinterpret_cast<uint4*>(qs + sw128_offset(n, u)) = outv;
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -336,18 +366,60 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      if (lane == 0) {
-        const int b = seq_of_row(c, g * NT, a.decode);
-        const int64_t nvis = group_visible<NT>(c, a, g);
-        const int64_t p0 = (int64_t)j * kTileM;
-        int64_t prow[2];
-        int nsub = 0;
+      if (g != gvis) {               // the group's sequence and visible length, once
+        gb = seq_of_row(c, g * NT, a.decode);
+        gnvis = group_visible<NT>(c, a, g);
+        gvis = g;
+        win0 = -1;
+      }
+      const int64_t p0 = (int64_t)j * kTileM;
+      // physical row of each 64-position sub-tile (-1: past the visible
+      // history).  Paged caches: the page ids come from a window of 32
+      // block-table entries that the warp loads at once (one load per lane),
+      // so no lane waits on a dependent page-table read per tile.
+      int64_t prow[2];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int64_t p = p0 + i * kSub;
-          prow[i] = -1;
-          if (p < nvis) { prow[i] = phys_row(c, b, p, err); if (prow[i] >= 0) ++nsub; }
+      for (int i = 0; i < 2; ++i) {
+        const int64_t pp = p0 + i * kSub;
+        prow[i] = -1;
+        if (pp >= gnvis) continue;
+        if (c.block_table == nullptr) {
+          prow[i] = (int64_t)gb * c.s_max + pp;
+          continue;
         }
+        const int64_t pg = pp / c.page_size;
+        if (win0 < 0 || pg < win0 || pg >= win0 + 32) {
+          win0 = pg;
+          const int64_t e = win0 + lane;
+          win = e < c.max_pages ? __ldg(c.block_table + (int64_t)gb * c.max_pages + e) : -1;
+        }
+        const int page = __shfl_sync(0xffffffffu, win, (int)(pg - win0));
+#ifdef DSI_CHECKED
+        if (page < 0 || page >= c.num_pages) {
+          if (lane == 0) report(err, kErrBounds);
+          continue;
+        }
+#endif
+        prow[i] = (int64_t)page * c.page_size + (pp - pg * c.page_size);
+      }
+      int nsub = 0;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) nsub += prow[i] >= 0;
+      if (FP8) {
+        // the tile's per-position key scales into the stage's scale slot, four
+        // positions a lane (only visible positions are copied or read); the
+        // lanes' barrier arrivals land with their copies
+        float* ks = reinterpret_cast<float*>(smem + C::OFF_KS) + stage * kTileM;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int q = lane * 4 + k;
+          const int64_t pr = prow[q / kSub];
+          if (pr >= 0 && p0 + q < gnvis)
+            cp_async_4(smem_u32(ks + q), c.k_scale + pr + (q % kSub));
+        }
+        cp_async_mbar_arrive_noinc(&full[stage]);
+      }
+      if (lane == 0) {
         // MXFP8: the sub-tile's 64 keys' group scales (64 * 128/G bytes) ride
         // along, from a map that views the scale array as rows of 16 bytes
         const int spr = kD >> a.lg_group;
@@ -370,10 +442,12 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         issued[stage] = true;
         issued_phase[stage] = phase;
       }
+      __syncwarp();
       if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
       it.next();
     }
-    // never leave the CTA with a TMA copy still landing in shared memory
+    // never leave the CTA with a copy still landing in shared memory
+    if (FP8) cp_async_wait<0>();
     if (lane == 0 && *abort_flag) {
       volatile int no_abort = 0;   // the drain is bounded by time only
       for (int s = 0; s < C::STAGES; ++s)
@@ -488,12 +562,13 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     const int row = quarter * 32 + lane;     // position within the tile
     ItemIter it;
     it.init(prefix, a.groups, it_begin, it_end);
-    int gprev = -1, abuf = 0;
-    uint32_t aph = 0;
+    int gprev = -1, abuf = 0, kst = 0;
+    uint32_t aph = 0, kph = 0;
     constexpr int TPT = C::TOK_PER_THREAD;
     // this warp's private copy of the head weights of its tokens (no
     // cross-warp barrier: a warp that leaves early can never block the others)
     float* wg = wbuf + ew * TPT * kHeads;
+    int64_t nv[TPT];                         // visible length of each of the thread's tokens
     while (it.valid()) {
       const int g = it.g, j = it.j;
       if (g != gprev) {
@@ -502,6 +577,11 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
           const int t = half * TPT + i / kHeads, h = i % kHeads;
           const int r = g * NT + t;
           wg[i] = r < a.rows ? __ldg(a.w + (int64_t)r * kHeads + h) : 0.f;
+        }
+#pragma unroll
+        for (int tt = 0; tt < TPT; ++tt) {
+          const int r = g * NT + half * TPT + tt;
+          nv[tt] = r >= a.rows ? 0 : a.decode ? visible_len(c, r, 1, 0) : a.q_offset + r + 1;
         }
         __syncwarp();
         gprev = g;
@@ -520,15 +600,24 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&acc_empty[abuf]);
-      const int b = seq_of_row(c, g * NT, a.decode);
       const int64_t p = (int64_t)j * kTileM + row;
+      // FP8 keys: this position's scale from the stage the producer filled
+      // (acquire its copies through the stage's barrier), then release the
+      // stage's scale slot
+      float ksc = 1.f;
+      if (FP8) {
+        if (!warp_wait(&full[kst], kph, abort_flag, err)) break;
+        ksc = reinterpret_cast<const float*>(smem + C::OFF_KS)[kst * kTileM + row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[kst]);
+        if (++kst == C::STAGES) { kst = 0; kph ^= 1; }
+      }
 #pragma unroll
       for (int tt = 0; tt < TPT; ++tt) {
         const int t = half * TPT + tt;
         const int r = g * NT + t;
         if (r >= a.rows) continue;
-        const int64_t nvis = a.decode ? visible_len(c, r, 1, 0) : a.q_offset + r + 1;
-        if (p >= nvis) continue;
+        if (p >= nv[tt]) continue;
         const float* wt = wg + tt * kHeads;
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -537,10 +626,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
           s1 = fmaf(wt[h + 1], fmaxf(v[tt][h + 1], 0.f), s1);
         }
         float s = s0 + s1;
-        if (FP8) {
-          const int64_t pr = phys_row(c, b, p, err);
-          if (pr >= 0) s *= __ldg(c.k_scale + pr);
-        }
+        if (FP8) s *= ksc;
         a.scores[(int64_t)r * a.ld + p] = s;
       }
       if (++abuf == 2) { abuf = 0; aph ^= 1; }

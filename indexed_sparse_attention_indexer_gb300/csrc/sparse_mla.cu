@@ -327,12 +327,13 @@ int mla_pick_splits(int rows, int n_heads, int K, size_t ws_bytes) {
   return splits;
 }
 
-cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const int32_t* idx, int rows,
-                                 int n_heads, int K, int decode, int64_t q_offset, float scale,
-                                 bf16* out, float* lse, void* ws, size_t ws_bytes, int* err,
-                                 cudaStream_t st);
+cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const float* latent_scale,
+                                 const int32_t* idx, int rows, int n_heads, int K, int decode,
+                                 int64_t q_offset, float scale, bf16* out, float* lse, void* ws,
+                                 size_t ws_bytes, int* err, cudaStream_t st);
 bool tc_mla_supported(int n_heads);
 bool tc_mla_cache_ok(const CacheView& c);
+bool tc_mla_fp8_ok(const CacheView& c, const float* latent_scale);
 
 template <bool F8>
 static cudaError_t launch_simt(const bf16* q, const CacheView& c, const float* lscale,
@@ -367,8 +368,8 @@ cudaError_t launch_sparse_mla(const bf16* q, const CacheView& c, const int32_t* 
                               float* lse, void* ws, size_t ws_bytes, int* err, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   if (tc_mla_supported(H) && tc_mla_cache_ok(c))
-    return launch_sparse_mla_tc(q, c, idx, rows, H, K, decode, q_offset, scale, out, lse, ws,
-                                ws_bytes, err, st);
+    return launch_sparse_mla_tc(q, c, nullptr, idx, rows, H, K, decode, q_offset, scale, out, lse,
+                                ws, ws_bytes, err, st);
   return launch_simt<false>(q, c, nullptr, idx, rows, H, K, decode, q_offset, scale, out, lse, ws,
                             ws_bytes, err, st);
 }
@@ -378,6 +379,10 @@ cudaError_t launch_sparse_mla_fp8(const bf16* q, const CacheView& c, const float
                                   int64_t q_offset, float scale, bf16* out, float* lse, void* ws,
                                   size_t ws_bytes, int* err, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
+  // 128 heads: the tensor-core kernel, rows converted to bf16 as they land
+  if (tc_mla_supported(H) && tc_mla_cache_ok(c) && tc_mla_fp8_ok(c, latent_scale))
+    return launch_sparse_mla_tc(q, c, latent_scale, idx, rows, H, K, decode, q_offset, scale, out,
+                                lse, ws, ws_bytes, err, st);
   return launch_simt<true>(q, c, latent_scale, idx, rows, H, K, decode, q_offset, scale, out,
                            lse, ws, ws_bytes, err, st);
 }

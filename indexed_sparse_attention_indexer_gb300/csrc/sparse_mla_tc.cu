@@ -116,8 +116,34 @@ __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float* v) {
   tmem_st32(taddr, r);
 }
 
+// FP8 latent rows: 16 codes a piece, 20 pieces of this CTA's 320 dims per
+// row, 1280 pieces a tile over the three producer warps.
+constexpr int kF8Pieces = kNp * kChunks * 64 / 16;
+constexpr int kF8PerThread = (kF8Pieces + kProducerWarps * 32 - 1) / (kProducerWarps * 32);
+
+// 16 E4M3 codes times their tile scale, rounded to bf16 (lo = codes 0..7).
+__device__ __forceinline__ void fp8x16_scaled_bf16(const uint4& v, float sc, uint4& lo, uint4& hi) {
+  const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((in[k] >> (16 * hh)) & 0xFFFFu);
+      const __half2 h2 = __half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3));
+      const float2 f = __half22float2(h2);
+      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+      out[2 * k + hh] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+  }
+  lo = make_uint4(out[0], out[1], out[2], out[3]);
+  hi = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+template <bool F8L>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* err) {
+mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscale, MlaArgs a,
+       int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -167,7 +193,12 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   }
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1 + kLdgThreads); mbar_init(&empty[s], 1); }
+    // bf16 rows: the TMA lane's byte count plus the cp.async threads; FP8
+    // rows: every producer thread once its converted pieces are stored
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], F8L ? kProducerWarps * 32 : 1 + kLdgThreads);
+      mbar_init(&empty[s], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 256);
@@ -226,7 +257,59 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
   grid_dep_launch();   // the next kernel on the stream may start its set-up
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (F8L && warp < kProducerWarps) {
+    // ======================= gather: FP8 rows ===================================
+    // Each thread owns kF8PerThread pieces of every tile (16 codes of one row)
+    // and keeps one tile of them in registers: piece k of tile t is converted
+    // (code * tile scale, rounded to bf16) into the swizzled stage, and its
+    // registers at once take piece k of tile t+1, so a tile's loads are in
+    // flight while the previous tile is converted and processed.  The stage
+    // is occupied from conversion to its P.V only.
+    const uint8_t* codes = reinterpret_cast<const uint8_t*>(c.latent);
+    uint4 cv[kF8PerThread];
+    float sc[kF8PerThread];
+    auto load_tile = [&](int t) {
+#pragma unroll
+      for (int k = 0; k < kF8PerThread; ++k) {
+        const int q = tid + k * kProducerWarps * 32;
+        if (q < kF8Pieces) {
+          const int rr = q / 20, u = q % 20;
+          const int64_t pr = max(rows_s[t * kNp + rr], 0);
+          const int d0 = g0 * 64 + u * 16;             // first dim of the piece
+          cv[k] = __ldg(reinterpret_cast<const uint4*>(codes + pr * DSI_D_QK + d0));
+          sc[k] = __ldg(lscale + pr * 5 + (d0 >> 7));
+        }
+      }
+    };
+    if (n_tiles > 0) load_tile(0);
+    int stage = 0;
+    uint32_t ph = 0;
+    for (int t = 0; t < n_tiles; ++t) {
+      if (!mbar_wait(&empty[stage], ph ^ 1, abort_flag, err)) break;
+      uint8_t* st_base = smem + OFF_C + stage * kStageBytes;
+#pragma unroll
+      for (int k = 0; k < kF8PerThread; ++k) {
+        const int q = tid + k * kProducerWarps * 32;
+        if (q < kF8Pieces) {
+          const int rr = q / 20, u = q % 20;
+          uint4 lo, hi;
+          fp8x16_scaled_bf16(cv[k], sc[k], lo, hi);
+          uint8_t* blk = st_base + (u >> 2) * kChunkBytes;
+          *reinterpret_cast<uint4*>(blk + sw128_offset(rr, (u & 3) * 2)) = lo;
+          *reinterpret_cast<uint4*>(blk + sw128_offset(rr, (u & 3) * 2 + 1)) = hi;
+          if (t + 1 < n_tiles) {
+            const int64_t pr = max(rows_s[(t + 1) * kNp + rr], 0);
+            const int d0 = g0 * 64 + u * 16;
+            cv[k] = __ldg(reinterpret_cast<const uint4*>(codes + pr * DSI_D_QK + d0));
+            sc[k] = __ldg(lscale + pr * 5 + (d0 >> 7));
+          }
+        }
+      }
+      fence_proxy_async_smem();   // the tensor core reads the stage through the async proxy
+      mbar_arrive(&full[stage]);
+      if (++stage == kStages) { stage = 0; ph ^= 1; }
+    }
+  } else if (warp == 0) {
     // ======================= gather: TMA part =================================
     // kTmaRows/4 lanes: lane g gathers rows 4g..4g+3 of the tile for the
     // first kTmaChunks 64-dim blocks, each a TMA gather of four 128-byte rows
@@ -266,7 +349,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
           if (issued[s2]) mbar_wait(&full[s2], issued_ph[s2], &no_abort, err, 100000000ull);
       }
     }
-  } else if (warp < kProducerWarps) {
+  } else if (!F8L && warp < kProducerWarps) {
     // ======================= gather: cp.async part ============================
     // the remaining 64-dim blocks of every row (half a warp per row: 16 lanes
     // x 16 bytes = two blocks) and the first blocks of the rows past kTmaRows,
@@ -611,6 +694,11 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* er
 
 bool tc_mla_supported(int n_heads) { return n_heads == kH; }
 
+// FP8 latent rows are read as 16-byte pieces at row offsets of 576 bytes.
+bool tc_mla_fp8_ok(const CacheView& c, const float* latent_scale) {
+  return latent_scale != nullptr && (reinterpret_cast<uintptr_t>(c.latent) & 15) == 0;
+}
+
 // Physical rows must fit the kernel's 32-bit row ids.
 bool tc_mla_cache_ok(const CacheView& c) {
   const uint64_t rows = c.block_table ? (uint64_t)c.num_pages * c.page_size
@@ -629,9 +717,10 @@ int tc_mla_splits(int rows, int K, size_t ws_bytes) {
   return splits;
 }
 
-cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const int32_t* idx, int rows,
-                                 int H, int K, int decode, int64_t q_offset, float scale, bf16* out,
-                                 float* lse, void* ws, size_t ws_bytes, int* err, cudaStream_t st) {
+cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const float* latent_scale,
+                                 const int32_t* idx, int rows, int H, int K, int decode,
+                                 int64_t q_offset, float scale, bf16* out, float* lse, void* ws,
+                                 size_t ws_bytes, int* err, cudaStream_t st) {
   MlaArgs a;
   a.q = q;
   a.idx = idx;
@@ -650,17 +739,23 @@ cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const int32_
     a.part_o = reinterpret_cast<float*>(ws);
     a.part_ml = reinterpret_cast<float2*>(reinterpret_cast<char*>(ws) + n * DSI_D_LATENT * sizeof(float));
   }
-  // latent rows as a 2D tensor [rows, 576], one-row boxes of 64 dims (gather4)
+  // bf16 latent rows as a 2D tensor [rows, 576], one-row boxes of 64 dims
+  // (gather4); FP8 rows are read with plain loads (no tensor map)
+  const bool f8 = latent_scale != nullptr;
   const uint64_t lrows = c.block_table ? (uint64_t)c.num_pages * c.page_size
                                        : (uint64_t)c.batch * c.s_max;
   CUtensorMap lmap;
-  if (!tma_map_2d(&lmap, c.latent, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lrows, DSI_D_QK, 64, 1))
+  memset(&lmap, 0, sizeof(lmap));
+  if (!f8 &&
+      !tma_map_2d(&lmap, c.latent, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lrows, DSI_D_QK, 64, 1))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(mla_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  auto kern = f8 ? mla_tc<true> : mla_tc<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
   const long blocks = 2L * rows * a.splits;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
-  e = launch_overlapped(mla_tc, dim3((unsigned)blocks), dim3(kThreads), SMEM, st, lmap, c, a, err);
+  e = launch_overlapped(kern, dim3((unsigned)blocks), dim3(kThreads), SMEM, st, lmap, c,
+                        latent_scale, a, err);
   note_launch();
   if (e != cudaSuccess || a.splits == 1) return e;
   return launch_mla_combine(a.part_o, a.part_ml, rows, H, a.splits, out, lse, st);

@@ -76,6 +76,10 @@ CASES = {
     "zero_length_h16": ([100, 0, 5], 4, 64, 16, 16, 0),
     "k_ge_history_h48": ([200, 31], 16, 64, 512, 48, 0),
     "single_seq_splitk_h128": ([5000], 64, 128, 2048, 128, 0),
+    # 128 heads run on the tensor-core kernel (rows converted to bf16 as they land)
+    "contig_h128_ragged": ([3000, 129, 64, 1, 700], 64, 128, 256, 128, 0),
+    "zero_length_h128": ([0, 300, 2], 64, 128, 64, 128, 0),
+    "paged128_h128": ([1000, 128, 300], 64, 128, 200, 128, 128),
 }
 
 
@@ -109,6 +113,47 @@ def test_prefill_fp8_latent():
         assert np.array_equal(idx[t].cpu().numpy(), ref["idx"]), f"row {t}"
         assert_out_close(out[t].float().cpu().numpy(), ref["out"], f"prefill row {t}")
         assert_lse_close(lse[t].cpu().numpy(), ref["lse"], f"prefill row {t}")
+
+
+def test_prefill_fp8_latent_h128():
+    """Causal prefill with 128 heads over an FP8 latent cache: the fused
+    prefill indexer, then the tensor-core attention kernel on FP8 rows."""
+    ws = W.make_prefill(130, 333, 64, 128, 100, 128, seed=13, q_offset=203, latent_fp8=True)
+    g = ws.to(DEV)
+    out, lse, idx, count = binding.layer(g)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    for t in (0, 1, 64, 100, 129):
+        ref = oracle.prefill_row(ws, t)
+        assert np.array_equal(idx[t].cpu().numpy(), ref["idx"]), f"row {t}"
+        assert_out_close(out[t].float().cpu().numpy(), ref["out"], f"prefill row {t}")
+        assert_lse_close(lse[t].cpu().numpy(), ref["lse"], f"prefill row {t}")
+
+
+@pytest.mark.parametrize("H,page", [(16, 64), (128, 64), (128, 0)])
+def test_append_then_attend_matches_oracle_quantisation_heads(H, page):
+    """bf16 rows quantised by the append kernel, attended by the CUDA-core (16
+    heads) or tensor-core (128 heads) kernel; the oracle quantises the same
+    rows itself."""
+    Hi, d = (4, 64) if H == 16 else (64, 128)
+    ws = W.make_decode(3, 0, Hi, d, 64, H, seed=19, lengths=[900, 70, 130], page_size=page)
+    pool = ws.latent.reshape(-1, 576)
+    g = ws.to(DEV)
+    codes, scales = binding.latent_fp8_append(pool.to(DEV))
+    g.latent = codes.view(ws.latent.shape)
+    g.latent_scale = scales.view(ws.latent.shape[:-1] + (5,))
+    out, lse, idx, count = binding.layer(g)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    rc, rs = oracle.latent_fp8_quantize(pool.float())
+    wq = ws.to("cpu")
+    wq.latent = torch.tensor(rc).to(torch.float8_e4m3fn).view(ws.latent.shape)
+    wq.latent_scale = torch.tensor(rs, dtype=torch.float32).view(ws.latent.shape[:-1] + (5,))
+    for b in range(ws.B):
+        ref = oracle.decode_row(wq, b)
+        assert np.array_equal(idx[b].cpu().numpy(), ref["idx"])
+        assert_out_close(out[b].float().cpu().numpy(), ref["out"], f"row {b}")
+        assert_lse_close(lse[b].cpu().numpy(), ref["lse"], f"row {b}")
 
 
 def test_append_then_attend_matches_oracle_quantisation():
