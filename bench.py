@@ -412,7 +412,10 @@ def prefill_parts(ws, world: int, rank: int):
 
 
 def _l2_flusher(dev):
-    buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # 1 GB: far larger than L2, and long enough on the device (~0.15 ms) for
+    # the host to enqueue the timed call behind it, so the call's time is
+    # device time, not launch latency
+    buf = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
     state = {"i": 0}
 
     def flush():
@@ -470,7 +473,7 @@ def measure_config(cfg: int, args, stream, dev, local: int) -> dict:
                   "gpu_launches_per_step": tm["launches"] / steps})
     if cfg == 1:
         entry["us_per_call"] = round(ms * 1e3, 2)
-        entry["l2"] = "256 MB written before every timed call (the workload fits in L2)"
+        entry["l2"] = "1 GB written before every timed call (the workload fits in L2)"
         entry["note"] = "latency-bound: 0.4 MB per call"
     if decode:
         span = cache.struct.s_max
@@ -970,6 +973,40 @@ def relaunch_ranks(n: int) -> int:
     return subprocess.run(cmd).returncode
 
 
+def run_appends():
+    """The two cache-append kernels at cache scale, HBM-bound: MXFP8
+    quantisation of the 64x32768 decode batch's index keys (bf16 in, E4M3 +
+    E8M0 out) and the FP8 append of its latent rows (bf16 in, E4M3 + five
+    fp32 tile scales out).  Bytes counted once each way; CUDA events, best of
+    five after warm-up (not a bench line)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from indexed_sparse_attention_indexer_gb300 import binding
+    binding.load()
+    stream = torch.cuda.current_stream()
+    hbm, _, src = peaks()
+    rows, d, G = 64 * 32768, 128, 32
+    keys = W.make_mx_input(rows, d, seed=5, device=dev, special=False)
+    codes = torch.empty((rows, d), dtype=torch.float8_e4m3fn, device=dev)
+    sc = torch.empty((rows, d // G), dtype=torch.uint8, device=dev)
+    q_ms = time_alone(lambda: binding.mxfp8_quantize(keys, G, codes=codes, scales=sc,
+                                                     stream=stream), stream, 10)
+    q_bytes = rows * (2 * d + d + d // G)
+    del keys, codes, sc
+    lat = torch.randn((rows, W.D_QK), device=dev).to(torch.bfloat16)
+    lc = torch.empty((rows, W.D_QK), dtype=torch.float8_e4m3fn, device=dev)
+    ls = torch.empty((rows, 5), dtype=torch.float32, device=dev)
+    a_ms = time_alone(lambda: binding.latent_fp8_append(lat, codes=lc, scales=ls, stream=stream),
+                      stream, 10)
+    a_bytes = rows * (2 * W.D_QK + W.D_QK + 5 * 4)
+    out = []
+    for name, ms, b in (("mxfp8_quantize", q_ms, q_bytes), ("latent_fp8_append", a_ms, a_bytes)):
+        gbs = b / (ms / 1e3) / 1e9
+        out.append({"kernel": name, "rows": rows, "bytes": b, "ms": round(ms, 4),
+                    "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4), "peak_source": src})
+    print(json.dumps({"probe": "cache_appends", "results": out}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -993,6 +1030,8 @@ def main():
                     help="the 64x128-head decode workload with an FP8 latent cache (own bench line)")
     ap.add_argument("--mx-scan", action="store_true",
                     help="measurement: MXFP8 group-size scan, precision and speed (not a bench line)")
+    ap.add_argument("--appends", action="store_true",
+                    help="measurement: the two cache-append kernels at cache scale (not a bench line)")
     ap.add_argument("--rows", type=int, default=None,
                     help="profiling aid: a smaller decode batch (the printed line is not a bench line)")
     args = ap.parse_args()
@@ -1001,6 +1040,9 @@ def main():
         return
     if args.mx_scan:
         run_mx_scan()
+        return
+    if args.appends:
+        run_appends()
         return
     args.warmup = max(3, args.warmup)
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
