@@ -321,8 +321,12 @@ int mla_pick_splits(int rows, int n_heads, int K, size_t ws_bytes) {
   const int groups = (n_heads + kHB - 1) / kHB;
   const long blocks = (long)rows * groups;
   int splits = 1;
-  // aim for >= 2 blocks per SM, each split keeping >= 4 tiles of work
-  while (blocks * splits < 2L * sms && (K / (splits * 2)) >= 4 * kNT && splits < 16) splits *= 2;
+  // aim for >= 2 blocks per SM, each split keeping >= 4 tiles of work; a
+  // batch that fills under a quarter of the SMs (a single decode row) is
+  // latency-bound and splits down to one tile per block
+  const int min_tiles = blocks < sms / 4 ? 1 : 4;
+  while (blocks * splits < 2L * sms && (K / (splits * 2)) >= min_tiles * kNT && splits < 16)
+    splits *= 2;
   while (splits > 1 && mla_partials_bytes(rows, n_heads, splits) > ws_bytes) splits /= 2;
   return splits;
 }
