@@ -54,6 +54,7 @@ constexpr int OFF_BUF = OFF_B + 2 * B_BYTES;                    // NT x kCap x 8
 constexpr int OFF_W = OFF_BUF + NT * kCap * 8;                  // NT x 64 fp32
 constexpr int kSelBits = 11;
 constexpr int kSelBins = 1 << kSelBits;                         // select histogram bins
+constexpr int kRankMax = 128;                                   // bin size ranked directly
 constexpr int kHistInts = kSelBins + 32;                        // + reduction scratch
 constexpr int OFF_HIST = OFF_W + NT * kHeads * 4;               // NT x kHistInts int
 constexpr int OFF_TOK = OFF_HIST + NT * kHistInts * 4;          // per-token state
@@ -70,6 +71,7 @@ struct TokState {
   int krem;
   int total;
   int stop;                   // set (never cleared) when a wait failed: the token's threads leave
+  int cnt2;                   // select scratch: keys collected from the final bin
 };
 static_assert(sizeof(TokState) <= 64, "token state");
 
@@ -123,8 +125,9 @@ __device__ __forceinline__ int group_tiles(const Args& a, int g) {
 // splits it into kSelBins equal bins and keeps the bin where the count from
 // the top reaches k.  Bins follow the keys' actual spread, so the histogram
 // atomics do not pile onto a few addresses the way fixed top digits of
-// similar scores would; once the chosen bin holds a single key, that key is
-// the answer.
+// similar scores would.  Once the chosen bin holds at most kRankMax keys, they
+// are collected and ranked against each other directly (each thread counts
+// the keys above its own), which ends the search without further passes.
 __device__ unsigned long long select_kth(const unsigned long long* buf, int n, int k, int* hist,
                                          TokState* ts, int tt, int tk) {
   const int lane = tt & 31, wq = tt >> 5;
@@ -204,10 +207,23 @@ __device__ unsigned long long select_kth(const unsigned long long* buf, int n, i
     lo += b << sh;
     bar_tok(tk);
     if (sh == 0) break;
-    if (in_bin == 1) {           // the bin holds exactly the k-th key: find it
+    if (in_bin <= kRankMax) {
+      // collect the bin's keys (unique) and rank them: the key with exactly
+      // krem-1 larger keys in the bin is the k-th of the buffer
+      unsigned long long* small = reinterpret_cast<unsigned long long*>(hist);
+      if (tt == 0) ts->cnt2 = 0;
+      bar_tok(tk);
       for (int i = tt; i < n; i += 128) {
         const unsigned long long c = buf[i];
-        if (c >= lo && c <= hi) ts->lo = c;
+        if (c >= lo && c <= hi) small[atomicAdd(&ts->cnt2, 1)] = c;
+      }
+      bar_tok(tk);
+      const int m = ts->cnt2;
+      if (tt < m) {
+        const unsigned long long mine = small[tt];
+        int above = 0;
+        for (int x = 0; x < m; ++x) above += small[x] > mine ? 1 : 0;
+        if (above == krem - 1) ts->lo = mine;
       }
       bar_tok(tk);
       lo = ts->lo;
@@ -396,39 +412,39 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       const int ntile = group_tiles(a, g);
       for (int j = 0; j < ntile; ++j) {
         // the stop decision is published before the token's barrier and read
-        // after it, so its four warps leave together (none is left waiting)
+        // after it, so its four warps leave together (none is left waiting);
+        // a warp whose wait failed appends nothing
         const bool got = warp_wait(&acc_full[abuf], aph, abort_flag, err);
-        if (lane == 0 && (!got || *abort_flag)) ts->stop = 1;
-        bar_tok(tk);
-        if (ts->stop) { ok = false; break; }
-        tc_fence_after();
-        float v[kHeads];
-        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + abuf * N + tk * kHeads;
-        tmem_ld32(taddr, v);
-        tmem_ld32(taddr + 32, v + 32);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&acc_empty[abuf]);
-        if (++abuf == kAccBufs) { abuf = 0; aph ^= 1; }
-        const int64_t p = (int64_t)j * kTileM + row;
         unsigned long long key = 0ull;
         bool take = false;
-        if (live && p < nvis) {
-          // weights four at a time, products two per instruction, two chains
-          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-          const float4* w4 = reinterpret_cast<const float4*>(wts);
+        if (got) {
+          tc_fence_after();
+          float v[kHeads];
+          const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + abuf * N + tk * kHeads;
+          tmem_ld32(taddr, v);
+          tmem_ld32(taddr + 32, v + 32);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&acc_empty[abuf]);
+          const int64_t p = (int64_t)j * kTileM + row;
+          if (live && p < nvis) {
+            // weights four at a time, products two per instruction, two chains
+            float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+            const float4* w4 = reinterpret_cast<const float4*>(wts);
 #pragma unroll
-          for (int h4 = 0; h4 < kHeads / 4; ++h4) {
-            const float4 ww = w4[h4];
-            a0 = ffma2(make_float2(ww.x, ww.y),
-                       make_float2(fmaxf(v[4 * h4], 0.f), fmaxf(v[4 * h4 + 1], 0.f)), a0);
-            a1 = ffma2(make_float2(ww.z, ww.w),
-                       make_float2(fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f)), a1);
+            for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+              const float4 ww = w4[h4];
+              a0 = ffma2(make_float2(ww.x, ww.y),
+                         make_float2(fmaxf(v[4 * h4], 0.f), fmaxf(v[4 * h4 + 1], 0.f)), a0);
+              a1 = ffma2(make_float2(ww.z, ww.w),
+                         make_float2(fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f)), a1);
+            }
+            key = ((unsigned long long)score_key((a0.x + a1.x) + (a0.y + a1.y)) << 32) |
+                  (unsigned long long)(0xFFFFFFFFu - (uint32_t)p);
+            take = key > ts->theta;
           }
-          key = ((unsigned long long)score_key((a0.x + a1.x) + (a0.y + a1.y)) << 32) |
-                (unsigned long long)(0xFFFFFFFFu - (uint32_t)p);
-          take = key > ts->theta;
         }
+        if (++abuf == kAccBufs) { abuf = 0; aph ^= 1; }
         // append with one atomic per warp
         const unsigned tm = __ballot_sync(0xffffffffu, take);
         if (tm) {
@@ -437,7 +453,9 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           slot0 = __shfl_sync(0xffffffffu, slot0, __ffs(tm) - 1);
           if (take) buf[slot0 + __popc(tm & ((1u << lane) - 1u))] = key;
         }
+        if (lane == 0 && (!got || *abort_flag)) ts->stop = 1;
         bar_tok(tk);
+        if (ts->stop) { ok = false; break; }
         // keep room for one more tile: compact a buffer that could overflow
         if (ts->cnt > kCap - kTileM) {
           const int n = ts->cnt;
