@@ -493,7 +493,7 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     # seeded per config; each rank its own replica (--rows: a smaller decode batch
-    # for profiling captures, never a bench line)
+    # or a shorter prefill for profiling captures, never a bench line)
     ws = W.make_config(args.config, device=dev, rows=args.rows, tokens_per_seq=args.tokens_per_seq,
                        k_mx_group=getattr(args, "k_mx_group", 0),
                        latent_fp8=getattr(args, "latent_fp8", False))
@@ -1033,7 +1033,8 @@ def main():
     ap.add_argument("--appends", action="store_true",
                     help="measurement: the two cache-append kernels at cache scale (not a bench line)")
     ap.add_argument("--rows", type=int, default=None,
-                    help="profiling aid: a smaller decode batch (the printed line is not a bench line)")
+                    help="profiling aid: a smaller decode batch or a shorter prefill (the printed "
+                         "line is not a bench line)")
     args = ap.parse_args()
     if args.crossover:
         run_crossover()

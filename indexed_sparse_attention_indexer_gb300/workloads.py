@@ -410,13 +410,16 @@ def make_config(cfg: int, device="cpu", chunk: int = 0, rows: int | None = None,
                 tokens_per_seq: int = 1, k_mx_group: int = 0,
                 latent_fp8: bool = False) -> Workload:
     """The named workload; ``rows`` shrinks a decode batch (same shapes per
-    sequence, fewer sequences) for profiling captures that must stay small;
+    sequence, fewer sequences) or a prefill (fewer tokens) for profiling
+    captures that must stay small;
     ``tokens_per_seq`` turns a decode workload into a multi-token step;
     ``k_mx_group`` stores the 64x128-head decode workload's index keys as MXFP8;
     ``latent_fp8`` stores its latent cache as FP8 with per-tile scales."""
     c = CONFIGS[cfg]
-    if (rows is not None or tokens_per_seq != 1) and cfg not in (1, 2, 5):
-        raise ValueError("rows and tokens_per_seq apply to the decode workloads only")
+    if tokens_per_seq != 1 and cfg not in (1, 2, 5):
+        raise ValueError("tokens_per_seq applies to the decode workloads only")
+    if rows is not None and cfg not in (1, 2, 3, 5):
+        raise ValueError("rows applies to the decode workloads and the prefill")
     if (k_mx_group or latent_fp8) and cfg != 2:
         raise ValueError("MXFP8 keys and the FP8 latent cache apply to the 64x128-head "
                          "contiguous decode workload only")
@@ -427,8 +430,9 @@ def make_config(cfg: int, device="cpu", chunk: int = 0, rows: int | None = None,
                            + ("-fp8latent" if latent_fp8 else ""),
                            tokens_per_seq=tokens_per_seq, k_mx_group=k_mx_group,
                            latent_fp8=latent_fp8)
-    if cfg == 3:
-        return make_prefill(c["T"], c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
+    if cfg == 3:     # rows: a shorter prefill (T = S = rows) for small profiling captures
+        T = rows or c["T"]
+        return make_prefill(T, rows or c["S"], c["H_i"], c["d"], c["K"], c["H"], c["seed"],
                             device=device, name=c["name"])
     if cfg == 4:
         k_idx, latent = make_long_cache(c["S"], c["d"], c["seed"], device)
