@@ -35,22 +35,24 @@ constexpr int kTileM = 128;
 constexpr int kSub = 64;
 constexpr int NT = 2;                        // tokens per group
 constexpr int N = NT * kHeads;               // 128
-constexpr int kStages = 2;
+constexpr int kStages = 3;                   // key tiles in flight (L2 latency per tile)
+constexpr int kQSlots = 1;                   // the next group's queries load while the epilogue selects
 constexpr int A_BYTES = kTileM * kD * 2;     // 32 KB
 constexpr int B_BYTES = N * kD * 2;          // 32 KB
 constexpr int kCap = 4096;                   // candidates per token
 constexpr int kMaxK = kCap / 2;              // 2048
 constexpr int kMaxRow = kCap * 64 / 2;       // bitmap of a row fits the 32 KB buffer: 131072 positions
-constexpr int EPI_WARPS = 8;                 // 4 per token
+constexpr int EPI_WARPS = 16;                // 8 per token: two sets of 4 taking alternate tiles
+constexpr int TOKT = 256;                    // threads per token (both sets)
 constexpr int EPI_THREADS = EPI_WARPS * 32;
-constexpr int THREADS = 64 + EPI_THREADS;    // 320
+constexpr int THREADS = 64 + EPI_THREADS;    // 576
 constexpr int kAccBufs = 4;                  // score accumulators in TMEM
 constexpr int TMEM_COLS = kAccBufs * N;      // 512
 constexpr uint32_t IDESC = idesc_f32(1, kTileM, N);
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + kStages * A_BYTES;
-constexpr int OFF_BUF = OFF_B + 2 * B_BYTES;                    // NT x kCap x 8 bytes
+constexpr int OFF_BUF = OFF_B + kQSlots * B_BYTES;              // NT x kCap x 8 bytes
 constexpr int OFF_W = OFF_BUF + NT * kCap * 8;                  // NT x 64 fp32
 constexpr int kSelBits = 11;
 constexpr int kSelBins = 1 << kSelBits;                         // select histogram bins
@@ -59,9 +61,10 @@ constexpr int kHistInts = kSelBins + 32;                        // + reduction s
 constexpr int OFF_HIST = OFF_W + NT * kHeads * 4;               // NT x kHistInts int
 constexpr int OFF_TOK = OFF_HIST + NT * kHistInts * 4;          // per-token state
 constexpr int OFF_BAR = (OFF_TOK + NT * 64 + 7) & ~7;
-constexpr int NBARS = 2 * kStages + 2 * kAccBufs + 2 + 2 + 1;
+constexpr int NBARS = 2 * kStages + 2 * kAccBufs + 2 * kQSlots + 1;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM = OFF_MISC + 64 + 1024;
+static_assert(SMEM <= 227 * 1024, "shared memory");
 
 struct TokState {
   unsigned long long theta;   // keys <= theta are rejected
@@ -99,8 +102,8 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return d;
 }
 
-__device__ __forceinline__ void bar_tok(int tk) {    // the 128 threads of one token
-  asm volatile("bar.sync %0, 128;\n" ::"r"(2 + tk) : "memory");
+__device__ __forceinline__ void bar_tok(int tk) {    // the TOKT threads of one token
+  asm volatile("bar.sync %0, %1;\n" ::"r"(2 + tk), "n"(TOKT) : "memory");
 }
 
 // k-th group (0-based) processed by CTA `cta`: zigzag pairs (i, G-1-i), pairs
@@ -134,7 +137,7 @@ __device__ unsigned long long select_kth(const unsigned long long* buf, int n, i
   const unsigned kAll = 0xffffffffu;
   unsigned long long mn = ~0ull, mx = 0ull;
 #pragma unroll 4
-  for (int i = tt; i < n; i += 128) {
+  for (int i = tt; i < n; i += TOKT) {
     const unsigned long long c = buf[i];
     mn = c < mn ? c : mn;
     mx = c > mx ? c : mx;
@@ -145,12 +148,13 @@ __device__ unsigned long long select_kth(const unsigned long long* buf, int n, i
     mn = a < mn ? a : mn;
     mx = b > mx ? b : mx;
   }
-  unsigned long long* red = reinterpret_cast<unsigned long long*>(hist + kSelBins);   // 8 words
-  if (lane == 0) { red[wq] = mn; red[4 + wq] = mx; }
+  constexpr int kW = TOKT / 32;                  // warps of the token
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(hist + kSelBins);   // 2 kW words
+  if (lane == 0) { red[wq] = mn; red[kW + wq] = mx; }
   bar_tok(tk);
   if (tt == 0) {
-    unsigned long long l = red[0], h = red[4];
-    for (int x = 1; x < 4; ++x) { l = red[x] < l ? red[x] : l; h = red[4 + x] > h ? red[4 + x] : h; }
+    unsigned long long l = red[0], h = red[kW];
+    for (int x = 1; x < kW; ++x) { l = red[x] < l ? red[x] : l; h = red[kW + x] > h ? red[kW + x] : h; }
     ts->lo = l;
     ts->hi = h;
   }
@@ -162,16 +166,16 @@ __device__ unsigned long long select_kth(const unsigned long long* buf, int n, i
     const unsigned long long span = hi - lo;
     const int bits = 64 - __clzll((long long)span);
     const int sh = bits > kSelBits ? bits - kSelBits : 0;
-    for (int i = tt; i < kSelBins; i += 128) hist[i] = 0;
+    for (int i = tt; i < kSelBins; i += TOKT) hist[i] = 0;
     bar_tok(tk);
 #pragma unroll 4
-    for (int i = tt; i < n; i += 128) {
+    for (int i = tt; i < n; i += TOKT) {
       const unsigned long long off = buf[i] - lo;         // wraps for keys below lo
       if (off <= span) atomicAdd(&hist[(int)(off >> sh)], 1);
     }
     bar_tok(tk);
-    // thread tt owns bins kSelBins-1-16tt down to kSelBins-16-16tt
-    constexpr int kPerT = kSelBins / 128;
+    // thread tt owns bins kSelBins-1-kPerT*tt down to kSelBins-kPerT-kPerT*tt
+    constexpr int kPerT = kSelBins / TOKT;
     int cs[kPerT], tot = 0;
 #pragma unroll
     for (int e = 0; e < kPerT; ++e) { cs[e] = hist[kSelBins - 1 - kPerT * tt - e]; tot += cs[e]; }
@@ -213,7 +217,7 @@ __device__ unsigned long long select_kth(const unsigned long long* buf, int n, i
       unsigned long long* small = reinterpret_cast<unsigned long long*>(hist);
       if (tt == 0) ts->cnt2 = 0;
       bar_tok(tk);
-      for (int i = tt; i < n; i += 128) {
+      for (int i = tt; i < n; i += TOKT) {
         const unsigned long long c = buf[i];
         if (c >= lo && c <= hi) small[atomicAdd(&ts->cnt2, 1)] = c;
       }
@@ -237,10 +241,10 @@ __device__ unsigned long long select_kth(const unsigned long long* buf, int n, i
 // Keep the entries >= t (exactly k of them) at the front of the buffer.
 __device__ void compact_ge(unsigned long long* buf, int n, unsigned long long t, TokState* ts,
                            int tt, int tk) {
-  constexpr int PER = kCap / 128;
+  constexpr int PER = kCap / TOKT;
   unsigned long long keep[PER];
   int nk = 0;
-  for (int i = tt, e = 0; e < PER; i += 128, ++e) {
+  for (int i = tt, e = 0; e < PER; i += TOKT, ++e) {
     const unsigned long long c = i < n ? buf[i] : 0ull;
     keep[e] = c;
     nk += (i < n && c >= t) ? 1 : 0;
@@ -251,7 +255,7 @@ __device__ void compact_ge(unsigned long long* buf, int n, unsigned long long t,
   bar_tok(tk);
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
-    const int i = tt + e * 128;
+    const int i = tt + e * TOKT;
     if (i < n && keep[e] >= t) buf[base++] = keep[e];
   }
   bar_tok(tk);
@@ -270,8 +274,8 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   uint64_t* acc_full = bars + 2 * kStages;
   uint64_t* acc_empty = acc_full + kAccBufs;
   uint64_t* q_full = acc_empty + kAccBufs;
-  uint64_t* q_empty = q_full + 2;
-  uint64_t* done_bar = q_empty + 2;
+  uint64_t* q_empty = q_full + kQSlots;
+  uint64_t* done_bar = q_empty + kQSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -280,9 +284,9 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int i = 0; i < kAccBufs; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], EPI_THREADS);
+      mbar_init(&acc_empty[i], NT * 128);   // one warp set (4 warps) of each token reads a tile
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kQSlots; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
     }
@@ -305,14 +309,14 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       prefetch_tmap(&qmap);
       int stage = 0, qcount = 0;
       uint32_t ph = 0;
-      bool issued[kStages] = {false, false};
-      uint32_t issued_ph[kStages] = {0, 0};
+      bool issued[kStages] = {};
+      uint32_t issued_ph[kStages] = {};
       bool ok = true;
       for (int k = 0; ok && k < nmax; ++k) {
         const int g = zigzag_group(k, blockIdx.x, gridDim.x, a.groups);
         if (g < 0) continue;
-        const int slot = qcount & 1;
-        if (!(ok = mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1, abort_flag, err))) break;
+        const int slot = qcount % kQSlots;
+        if (!(ok = mbar_wait(&q_empty[slot], ((qcount / kQSlots) & 1) ^ 1, abort_flag, err))) break;
         uint8_t* qs = smem + OFF_B + slot * B_BYTES;
         mbar_arrive_expect_tx(&q_full[slot], B_BYTES);
         for (int t = 0; t < NT; ++t)
@@ -361,8 +365,8 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       for (int k = 0; ok && k < nmax; ++k) {
         const int g = zigzag_group(k, blockIdx.x, gridDim.x, a.groups);
         if (g < 0) continue;
-        const int slot = qcount & 1;
-        if (!(ok = mbar_wait(&q_full[slot], (qcount >> 1) & 1, abort_flag, err))) break;
+        const int slot = qcount % kQSlots;
+        if (!(ok = mbar_wait(&q_full[slot], (qcount / kQSlots) & 1, abort_flag, err))) break;
         ++qcount;
         const int ntile = group_tiles(a, g);
         for (int j = 0; j < ntile; ++j) {
@@ -388,17 +392,17 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     __syncwarp();
   } else {
     // ======================= epilogue + running Top-K ===========================
-    const int ew = warp - 2;                  // 0..7
-    const int tk = ew >> 2;                   // token of the group this warp serves
+    const int ew = warp - 2;                  // 0..15
+    const int tk = ew >> 3;                   // token of the group this warp serves
+    const int set = (ew >> 2) & 1;            // tiles of this parity (each set covers 4 lane quarters)
     const int quarter = warp & 3;             // TMEM lane quarter
-    const int tt = (ew & 3) * 32 + lane;      // thread index within the token's 128
+    const int tt = (ew & 7) * 32 + lane;      // thread index within the token's TOKT
     const int row = quarter * 32 + lane;      // position within the tile (TMEM lane)
     unsigned long long* buf = reinterpret_cast<unsigned long long*>(smem + OFF_BUF) + tk * kCap;
     float* wts = reinterpret_cast<float*>(smem + OFF_W) + tk * kHeads;
     int* hist = reinterpret_cast<int*>(smem + OFF_HIST) + tk * kHistInts;
     TokState* ts = reinterpret_cast<TokState*>(smem + OFF_TOK) + tk;
-    int abuf = 0;
-    uint32_t aph = 0;
+    int gbase = 0;                            // the CTA's tile count before this group
     bool ok = true;
     for (int k = 0; ok && k < nmax; ++k) {
       const int g = zigzag_group(k, blockIdx.x, gridDim.x, a.groups);
@@ -410,41 +414,52 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       if (tt == 0) { ts->theta = 0ull; ts->cnt = 0; }
       bar_tok(tk);
       const int ntile = group_tiles(a, g);
-      for (int j = 0; j < ntile; ++j) {
+      // the two sets take tiles j0 and j0 + 1 at once; the token's barrier
+      // then publishes both tiles' appends
+      for (int j0 = 0; j0 < ntile; j0 += 2) {
+        const int j = j0 + set;
         // the stop decision is published before the token's barrier and read
-        // after it, so its four warps leave together (none is left waiting);
-        // a warp whose wait failed appends nothing
-        const bool got = warp_wait(&acc_full[abuf], aph, abort_flag, err);
+        // after it, so its warps leave together (none is left waiting); a
+        // warp whose wait failed appends nothing
+        bool got = true;
         unsigned long long key = 0ull;
         bool take = false;
-        if (got) {
-          tc_fence_after();
-          float v[kHeads];
-          const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + abuf * N + tk * kHeads;
-          tmem_ld32(taddr, v);
-          tmem_ld32(taddr + 32, v + 32);
-          tmem_ld_wait();
-          tc_fence_before();
-          mbar_arrive(&acc_empty[abuf]);
-          const int64_t p = (int64_t)j * kTileM + row;
-          if (live && p < nvis) {
-            // weights four at a time, products two per instruction, two chains
+        if (j < ntile) {
+          const int gi = gbase + j;                       // the CTA's tile index
+          const int abuf = gi & (kAccBufs - 1);
+          const uint32_t aph = (uint32_t)(gi / kAccBufs) & 1u;
+          got = warp_wait(&acc_full[abuf], aph, abort_flag, err);
+          if (got) {
+            tc_fence_after();
+            // the token's 64 head scores in two halves of 32 (fewer live
+            // registers); weights four at a time, products two per instruction
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + abuf * N + tk * kHeads;
+            const int64_t p = (int64_t)j * kTileM + row;
             float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
             const float4* w4 = reinterpret_cast<const float4*>(wts);
 #pragma unroll
-            for (int h4 = 0; h4 < kHeads / 4; ++h4) {
-              const float4 ww = w4[h4];
-              a0 = ffma2(make_float2(ww.x, ww.y),
-                         make_float2(fmaxf(v[4 * h4], 0.f), fmaxf(v[4 * h4 + 1], 0.f)), a0);
-              a1 = ffma2(make_float2(ww.z, ww.w),
-                         make_float2(fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f)), a1);
+            for (int hh = 0; hh < 2; ++hh) {
+              float v[32];
+              tmem_ld32(taddr + hh * 32, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int h4 = 0; h4 < 8; ++h4) {
+                const float4 ww = w4[hh * 8 + h4];
+                a0 = ffma2(make_float2(ww.x, ww.y),
+                           make_float2(fmaxf(v[4 * h4], 0.f), fmaxf(v[4 * h4 + 1], 0.f)), a0);
+                a1 = ffma2(make_float2(ww.z, ww.w),
+                           make_float2(fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f)), a1);
+              }
             }
-            key = ((unsigned long long)score_key((a0.x + a1.x) + (a0.y + a1.y)) << 32) |
-                  (unsigned long long)(0xFFFFFFFFu - (uint32_t)p);
-            take = key > ts->theta;
+            tc_fence_before();
+            mbar_arrive(&acc_empty[abuf]);
+            if (live && p < nvis) {
+              key = ((unsigned long long)score_key((a0.x + a1.x) + (a0.y + a1.y)) << 32) |
+                    (unsigned long long)(0xFFFFFFFFu - (uint32_t)p);
+              take = key > ts->theta;
+            }
           }
         }
-        if (++abuf == kAccBufs) { abuf = 0; aph ^= 1; }
         // append with one atomic per warp
         const unsigned tm = __ballot_sync(0xffffffffu, take);
         if (tm) {
@@ -456,8 +471,8 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         if (lane == 0 && (!got || *abort_flag)) ts->stop = 1;
         bar_tok(tk);
         if (ts->stop) { ok = false; break; }
-        // keep room for one more tile: compact a buffer that could overflow
-        if (ts->cnt > kCap - kTileM) {
+        // keep room for two more tiles: compact a buffer that could overflow
+        if (ts->cnt > kCap - 2 * kTileM) {
           const int n = ts->cnt;
           const unsigned long long t = select_kth(buf, n, a.K, hist, ts, tt, tk);
           compact_ge(buf, n, t, ts, tt, tk);
@@ -465,6 +480,7 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         }
         bar_tok(tk);
       }
+      gbase += ntile;
       if (!ok) break;
       // ---- final selection of the group's rows -------------------------------
       if (live) {
@@ -475,35 +491,35 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           n = a.K;
         }
         // winners' positions -> registers, then the buffer becomes a bitmap
-        constexpr int PER = kMaxK / 128;
+        constexpr int PER = kMaxK / TOKT;
         int mypos[PER];
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
-          const int i = tt + e * 128;
+          const int i = tt + e * TOKT;
           mypos[e] = i < n ? (int)(0xFFFFFFFFu - (uint32_t)(buf[i] & 0xFFFFFFFFull)) : -1;
         }
         bar_tok(tk);
         uint32_t* bits = reinterpret_cast<uint32_t*>(buf);
         const int nwords = (int)((nvis + 31) / 32);
-        for (int i = tt; i < nwords; i += 128) bits[i] = 0u;
+        for (int i = tt; i < nwords; i += TOKT) bits[i] = 0u;
         bar_tok(tk);
 #pragma unroll
         for (int e = 0; e < PER; ++e)
           if (mypos[e] >= 0) atomicOr(&bits[mypos[e] >> 5], 1u << (mypos[e] & 31));
         bar_tok(tk);
         // ascending output: each thread owns a contiguous run of words
-        const int per = (nwords + 127) / 128;
+        const int per = (nwords + TOKT - 1) / TOKT;
         const int w0 = min(nwords, tt * per), w1 = min(nwords, w0 + per);
         int mine = 0;
         for (int i = w0; i < w1; ++i) mine += __popc(bits[i]);
-        // exclusive scan of `mine` over the token's 128 threads (4 warps)
+        // exclusive scan of `mine` over the token's TOKT threads
         int incl = mine;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int y = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += y;
         }
-        int* wsum = hist;   // 4 warp totals
+        int* wsum = hist;   // the token's warp totals
         if (lane == 31) wsum[tt >> 5] = incl;
         bar_tok(tk);
         int before = incl - mine;
@@ -517,7 +533,7 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             out[before++] = i * 32 + bpos;
           }
         }
-        for (int i = n + tt; i < a.K; i += 128) out[i] = -1;
+        for (int i = n + tt; i < a.K; i += TOKT) out[i] = -1;
         if (a.count && tt == 0) a.count[r] = n;
       }
       bar_tok(tk);

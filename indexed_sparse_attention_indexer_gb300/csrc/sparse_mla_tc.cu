@@ -100,13 +100,11 @@ struct MlaArgs {
   int rows, K, decode, splits;
 };
 
+// An entry takes part when it names a visible position.  Checked in every
+// build (the checked build also reports entries past the history), so indices
+// left unwritten by a failed earlier kernel never address rows outside the cache.
 __device__ __forceinline__ bool pos_ok(int pos, int64_t n_vis) {
-#ifdef DSI_CHECKED
   return pos >= 0 && pos < n_vis;
-#else
-  (void)n_vis;
-  return pos >= 0;
-#endif
 }
 
 __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float* v) {

@@ -326,6 +326,30 @@ def test_checked_build_flags_out_of_range_index():
     assert binding.device_status(checked=True) == 0   # read clears it
 
 
+@pytest.mark.parametrize("H,paged", [(16, 0), (128, 0), (128, 64)])
+def test_indices_past_the_history_are_skipped_in_every_build(H, paged):
+    """Entries beyond a row's visible history (here up to 2^30, far outside the
+    cache) take no part in the attention in the release build either: the
+    result equals the same call with those entries set to -1, and no row
+    outside the cache is read."""
+    Hi, d = (4, 64) if H == 16 else (64, 128)
+    ws = W.make_decode(3, 0, Hi, d, 64, H, seed=37, lengths=[300, 90, 200], page_size=paged)
+    g = ws.to(DEV)
+    cache = binding.Cache.of(g)
+    gen = torch.Generator().manual_seed(3)
+    good = torch.stack([torch.randperm(int(L), generator=gen)[:64].sort().values
+                        for L in ws.seq_lens]).to(torch.int32)
+    bad = good.clone()
+    bad[0, 5], bad[1, 0], bad[2, 63] = 300, 1 << 30, 5000     # past each row's history
+    clean = good.clone()
+    clean[0, 5], clean[1, 0], clean[2, 63] = -1, -1, -1
+    ref, ref_lse = binding.sparse_mla_decode(g.q, cache, clean.to(DEV), ws.scale)
+    out, lse = binding.sparse_mla_decode(g.q, cache, bad.to(DEV), ws.scale)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
+
+
 @pytest.mark.parametrize("Hi,d,H", [(64, 128, 128), (4, 64, 16)])
 def test_decode_length_above_s_max_is_clamped(Hi, d, H):
     """A seq_lens entry above a contiguous cache's s_max (here 100, not a
