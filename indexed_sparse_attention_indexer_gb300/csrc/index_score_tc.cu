@@ -74,7 +74,10 @@ struct Cfg {
   static constexpr int EPI_WARPS = NT == 1 ? 4 : 8;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int THREADS = 64 + EPI_THREADS + DQ_THREADS;
-  static constexpr int TMEM_COLS = 2 * N <= 128 ? 128 : (2 * N <= 256 ? 256 : 512);
+  // TMEM accumulators: four where they fit (the epilogue of tile i then
+  // releases its accumulator four tiles ahead of the MMA that reuses it)
+  static constexpr int ACCS = 4 * N <= 512 ? 4 : 2;
+  static constexpr int TMEM_COLS = ACCS * N <= 128 ? 128 : (ACCS * N <= 256 ? 256 : 512);
   static constexpr int KSTEPS = FP8 ? 4 : 8;              // 32 bytes of K per MMA
   static constexpr uint32_t IDESC = idesc_f32(FP8 ? 0u : 1u, kTileM, N);
   static constexpr int TOK_PER_THREAD = NT == 1 ? 1 : NT / 2;   // epilogue column split
@@ -87,7 +90,7 @@ struct Cfg {
   static constexpr int OFF_W = OFF_KS + (FP8 ? STAGES * kTileM * 4 : 0); // per epilogue warp: weights
   static constexpr int OFF_PREFIX = OFF_W + EPI_WARPS * TOK_PER_THREAD * kHeads * 4;
   static constexpr int OFF_BAR = (OFF_PREFIX + (kMaxGroups + 1) * 4 + 7) & ~7;
-  static constexpr int NBARS = 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 2 * ABUFS;
+  static constexpr int NBARS = 2 * STAGES + 2 * ACCS + 2 + 2 + 1 + 2 * ABUFS;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8 + 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;                 // + alignment slack
   static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -172,8 +175,8 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
   uint64_t* acc_full = bars + 2 * C::STAGES;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* q_full = acc_empty + 2;
+  uint64_t* acc_empty = acc_full + C::ACCS;
+  uint64_t* q_full = acc_empty + C::ACCS;
   uint64_t* q_empty = q_full + 2;
   uint64_t* done_bar = q_empty + 2;
   uint64_t* a_full = done_bar + 1;          // MXFP8: dequantised A tile ready
@@ -209,9 +212,11 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       mbar_init(&empty[s], C::MX ? C::DQ_WARPS : FP8 ? 1 + C::EPI_WARPS : 1);
     }
     for (int i = 0; i < C::ABUFS; ++i) { mbar_init(&a_full[i], C::DQ_WARPS); mbar_init(&a_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::ACCS; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], C::EPI_THREADS);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
     }
@@ -236,6 +241,10 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     int gprev = -1, qcount = 0, stage = 0;
     int gvis = -1, gb = 0, win = -1;     // group whose visible length / block-table window is held
     int64_t gnvis = 0, win0 = -1;
+    // log2 of a power-of-two page size (the common case: shifts instead of
+    // 64-bit divisions per sub-tile), else -1
+    const int pshift = (c.block_table && (c.page_size & (c.page_size - 1)) == 0)
+                           ? __ffs(c.page_size) - 1 : -1;
     uint32_t phase = 0;
     uint32_t issued_phase[C::STAGES];
     bool issued[C::STAGES];
@@ -387,7 +396,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
           prow[i] = (int64_t)gb * c.s_max + pp;
           continue;
         }
-        const int64_t pg = pp / c.page_size;
+        const int64_t pg = pshift >= 0 ? (pp >> pshift) : pp / c.page_size;
         if (win0 < 0 || pg < win0 || pg >= win0 + 32) {
           win0 = pg;
           const int64_t e = win0 + lane;
@@ -499,7 +508,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
           stage = 0;
           phase ^= 1;
         }
-        if (++abuf == 2) { abuf = 0; aph ^= 1; }
+        if (++abuf == C::ACCS) { abuf = 0; aph ^= 1; }
         it.next();
       }
       // all MMAs of this CTA complete before TMEM is released
@@ -629,7 +638,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         if (FP8) s *= ksc;
         a.scores[(int64_t)r * a.ld + p] = s;
       }
-      if (++abuf == 2) { abuf = 0; aph ^= 1; }
+      if (++abuf == C::ACCS) { abuf = 0; aph ^= 1; }
       it.next();
     }
   }
