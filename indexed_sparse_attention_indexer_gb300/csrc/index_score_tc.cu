@@ -73,7 +73,12 @@ struct Cfg {
   static constexpr int SC_BYTES = 2 * SC_SUB;
   static constexpr int EPI_WARPS = NT == 1 ? 4 : 8;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
-  static constexpr int THREADS = 64 + EPI_THREADS + DQ_THREADS;
+  // producer warps: tile k is issued by producer k % PRODUCERS (one warp's
+  // serial per-tile path cannot keep up with single-token decode over
+  // one-byte keys, whose 16 KB tiles arrive twice as often as bf16 tiles)
+  static constexpr int PRODUCERS = NT == 1 && K8 ? 2 : 1;
+  static constexpr int PROD_WARP1 = 2 + EPI_WARPS + DQ_WARPS;   // first extra producer warp
+  static constexpr int THREADS = 64 + EPI_THREADS + DQ_THREADS + 32 * (PRODUCERS - 1);
   // TMEM accumulators: four where they fit (the epilogue of tile i then
   // releases its accumulator four tiles ahead of the MMA that reuses it)
   static constexpr int ACCS = 4 * N <= 512 ? 4 : 2;
@@ -106,6 +111,7 @@ struct ScoreArgs {
   int groups;
   int decode;
   int lg_group;  // MXFP8: log2 of the elements per scale (5, 6 or 7)
+  int sc_bulk;   // FP8: key scales by one bulk copy per box (aligned) instead of per lane
 };
 
 // Group g holds query rows g*NT .. g*NT+NT-1: NT tokens of the prefill, or
@@ -204,11 +210,11 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
   }
   if (tid == 0) {
     // MXFP8: a stage is empty once every dequantising warp has read it
-    // FP8: the producer warp's 32 lanes also arrive on full (their key-scale
-    // copies), and a stage is empty once the MMAs and every epilogue warp
-    // (which reads its scales) are done with it
+    // FP8: the producer warp's 32 lanes also arrive on full when they copy the
+    // key scales themselves, and a stage is empty once the MMAs and every
+    // epilogue warp (which reads its scales) are done with it
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], FP8 ? 33 : 1);
+      mbar_init(&full[s], FP8 && !a.sc_bulk ? 33 : 1);
       mbar_init(&empty[s], C::MX ? C::DQ_WARPS : FP8 ? 1 + C::EPI_WARPS : 1);
     }
     for (int i = 0; i < C::ABUFS; ++i) { mbar_init(&a_full[i], C::DQ_WARPS); mbar_init(&a_empty[i], 1); }
@@ -234,31 +240,38 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
   const int64_t it_begin = total_items * blockIdx.x / gridDim.x;
   const int64_t it_end = total_items * (blockIdx.x + 1) / gridDim.x;
 
-  if (warp == 0) {
-    // ======================= TMA producer ====================================
+  if (warp == 0 || warp >= C::PROD_WARP1) {
+    // ======================= TMA producers ===================================
+    // Producer pw issues the tiles k = pw, pw + PRODUCERS, ... of the CTA's
+    // range; producer 0 also loads each group's queries.
+    const int pw = warp == 0 ? 0 : warp - C::PROD_WARP1 + 1;
     ItemIter it;
     it.init(prefix, a.groups, it_begin, it_end);
     int gprev = -1, qcount = 0, stage = 0;
     int gvis = -1, gb = 0, win = -1;     // group whose visible length / block-table window is held
-    int64_t gnvis = 0, win0 = -1;
+    int64_t gnvis = 0, win0 = -1, rbase = 0;
     // log2 of a power-of-two page size (the common case: shifts instead of
     // 64-bit divisions per sub-tile), else -1
     const int pshift = (c.block_table && (c.page_size & (c.page_size - 1)) == 0)
                            ? __ffs(c.page_size) - 1 : -1;
     uint32_t phase = 0;
-    uint32_t issued_phase[C::STAGES];
-    bool issued[C::STAGES];
-#pragma unroll
-    for (int s = 0; s < C::STAGES; ++s) { issued[s] = false; issued_phase[s] = 0; }
+    int k = 0, last_k = -1;              // item index; last tile this warp issued (stage k % STAGES)
+    // contiguous bf16 / FP8 keys: one 128-row box per tile (the map's box is
+    // 128 rows); paged caches and MXFP8 keys: two 64-row boxes
+    const bool whole = !C::MX && c.block_table == nullptr;
     if (lane == 0) {
       prefetch_tmap(&kmap);
       if (!C::K8) prefetch_tmap(&qmap);
       if (C::MX) prefetch_tmap(&smap);
     }
-    // lane 0's reading of the flag decides for the warp, so all lanes leave together
-    while (it.valid() && !__shfl_sync(0xffffffffu, (int)*abort_flag, 0)) {
+    // The per-tile path is short: a warp's own instruction latency bounds its
+    // tile rate.  Page ids and rows are worked out before the stage wait;
+    // lane 0's wait result (false on abort or timeout) is the one value the
+    // warp shares per tile.
+    for (; it.valid(); ++k, it.next()) {
+      if (k != 0 && ++stage == C::STAGES) { stage = 0; phase ^= 1; }
       const int g = it.g, j = it.j;
-      if (g != gprev) {
+      if (pw == 0 && g != gprev) {
         const int slot = qcount & 1;
         const uint32_t qph = (qcount >> 1) & 1;
         bool ok = true;
@@ -370,14 +383,12 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         ++qcount;
         gprev = g;
       }
+      if (k % C::PRODUCERS != pw) continue;
       // ---- one key tile -----------------------------------------------------
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, err);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
       if (g != gvis) {               // the group's sequence and visible length, once
         gb = seq_of_row(c, g * NT, a.decode);
         gnvis = group_visible<NT>(c, a, g);
+        rbase = (int64_t)gb * c.s_max;
         gvis = g;
         win0 = -1;
       }
@@ -393,7 +404,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         prow[i] = -1;
         if (pp >= gnvis) continue;
         if (c.block_table == nullptr) {
-          prow[i] = (int64_t)gb * c.s_max + pp;
+          prow[i] = rbase + pp;
           continue;
         }
         const int64_t pg = pshift >= 0 ? (pp >> pshift) : pp / c.page_size;
@@ -414,7 +425,50 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       int nsub = 0;
 #pragma unroll
       for (int i = 0; i < 2; ++i) nsub += prow[i] >= 0;
-      if (FP8) {
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, err);
+        if (ok) {
+          uint8_t* as = smem + C::OFF_A + stage * C::ST_BYTES;
+          float* ks = reinterpret_cast<float*>(smem + C::OFF_KS) + stage * kTileM;
+          if (whole) {
+            // contiguous keys: the tile is one 128-row box (rows past the
+            // history are read and ignored; past the array, zero-filled)
+            const uint32_t sc_bytes =
+                FP8 && a.sc_bulk ? (uint32_t)(c.s_max - p0 < kTileM ? c.s_max - p0 : kTileM) * 4u : 0u;
+            mbar_arrive_expect_tx(&full[stage], (uint32_t)C::ST_BYTES + sc_bytes);
+            tma_load_2d(as, &kmap, 0, (int)prow[0], &full[stage]);
+            if (!C::K8) tma_load_2d(as + 16384, &kmap, 64, (int)prow[0], &full[stage]);
+            if (sc_bytes) bulk_load(ks, c.k_scale + prow[0], sc_bytes, &full[stage]);
+          } else {
+            // 64-row boxes (paged: one page's run each).  MXFP8: the sub-tile's
+            // 64 keys' group scales (64 * 128/G bytes) ride along, from a map
+            // that views the scale array as rows of 16 bytes
+            const int spr = kD >> a.lg_group;
+            mbar_arrive_expect_tx(
+                &full[stage],
+                (uint32_t)(nsub * (C::ST_BYTES / 2 + (C::MX ? kSub * spr : 0) +
+                                   (FP8 && a.sc_bulk ? kSub * 4 : 0))));
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              if (prow[i] < 0) continue;
+              if (C::K8) {
+                tma_load_2d(as + i * (kSub * 128), &kmap, 0, (int)prow[i], &full[stage]);
+              } else {
+                tma_load_2d(as + i * (kSub * 128), &kmap, 0, (int)prow[i], &full[stage]);
+                tma_load_2d(as + 16384 + i * (kSub * 128), &kmap, 64, (int)prow[i], &full[stage]);
+              }
+              if (C::MX)
+                tma_load_2d(smem + C::OFF_SC + stage * C::SC_BYTES + i * C::SC_SUB, &smap, 0,
+                            (int)(prow[i] * spr / 16), &full[stage]);
+              if (FP8 && a.sc_bulk)
+                bulk_load(ks + i * kSub, c.k_scale + prow[i], kSub * 4, &full[stage]);
+            }
+          }
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (FP8 && !a.sc_bulk) {
         // the tile's per-position key scales into the stage's scale slot, four
         // positions a lane (only visible positions are copied or read); the
         // lanes' barrier arrivals land with their copies
@@ -428,39 +482,17 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         }
         cp_async_mbar_arrive_noinc(&full[stage]);
       }
-      if (lane == 0) {
-        // MXFP8: the sub-tile's 64 keys' group scales (64 * 128/G bytes) ride
-        // along, from a map that views the scale array as rows of 16 bytes
-        const int spr = kD >> a.lg_group;
-        uint8_t* as = smem + C::OFF_A + stage * C::ST_BYTES;
-        mbar_arrive_expect_tx(&full[stage], (uint32_t)(nsub * (C::ST_BYTES / 2 +
-                                                                (C::MX ? kSub * spr : 0))));
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (prow[i] < 0) continue;
-          if (C::K8) {
-            tma_load_2d(as + i * (kSub * 128), &kmap, 0, (int)prow[i], &full[stage]);
-          } else {
-            tma_load_2d(as + i * (kSub * 128), &kmap, 0, (int)prow[i], &full[stage]);
-            tma_load_2d(as + 16384 + i * (kSub * 128), &kmap, 64, (int)prow[i], &full[stage]);
-          }
-          if (C::MX)
-            tma_load_2d(smem + C::OFF_SC + stage * C::SC_BYTES + i * C::SC_SUB, &smap, 0,
-                        (int)(prow[i] * spr / 16), &full[stage]);
-        }
-        issued[stage] = true;
-        issued_phase[stage] = phase;
-      }
-      __syncwarp();
-      if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
-      it.next();
+      last_k = k;
     }
-    // never leave the CTA with a copy still landing in shared memory
+    // never leave the CTA with a copy still landing in shared memory: after
+    // an abort, wait (bounded by time) for the stages of this warp's last
+    // tiles (any tile still in flight is one of the last STAGES issued)
     if (FP8) cp_async_wait<0>();
     if (lane == 0 && *abort_flag) {
-      volatile int no_abort = 0;   // the drain is bounded by time only
-      for (int s = 0; s < C::STAGES; ++s)
-        if (issued[s]) mbar_wait(&full[s], issued_phase[s], &no_abort, err, 100000000ull);
+      volatile int no_abort = 0;
+      for (int t = last_k; t >= 0 && t > last_k - C::STAGES; t -= C::PRODUCERS)
+        mbar_wait(&full[t % C::STAGES], (uint32_t)((t / C::STAGES) & 1), &no_abort, err,
+                  100000000ull);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================================
@@ -665,11 +697,13 @@ cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, 
                     16, kSub * spr / 16, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
+  // contiguous bf16 / FP8 keys are copied a whole 128-position tile per box
+  const uint32_t box_rows = (C::MX || c.block_table) ? kSub : kTileM;
   if (C::K8) {
-    if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, krows, kD, 128, kSub))
+    if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, krows, kD, 128, box_rows))
       return cudaErrorInvalidValue;
   } else {
-    if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, krows, kD, 64, kSub))
+    if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, krows, kD, 64, box_rows))
       return cudaErrorInvalidValue;
     if (!tma_map_2d(&qmap, q_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)rows * kHeads, kD,
                   64, kHeads))
@@ -685,6 +719,10 @@ cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, 
   a.decode = decode;
   a.groups = (rows + NT - 1) / NT;
   a.lg_group = c.k_group == 128 ? 7 : c.k_group == 64 ? 6 : 5;
+  // FP8 key scales by bulk copy: 16-byte aligned runs (a page's rows start at
+  // multiples of 64 positions; a sequence's at multiples of s_max)
+  a.sc_bulk = C::FP8 && (reinterpret_cast<uintptr_t>(c.k_scale) & 15) == 0 &&
+              (c.block_table != nullptr || c.s_max % 4 == 0);
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

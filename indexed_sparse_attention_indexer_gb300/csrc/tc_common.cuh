@@ -240,6 +240,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+// Plain bulk copy of `bytes` contiguous bytes (both addresses 16-byte
+// aligned, size a multiple of 16), counted on `bar` when they land.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 // Four rows (any row indices) x one box of columns, landing as four
 // consecutive box rows at dst; the tensor map's box is one row high.
 __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int x, int y0,

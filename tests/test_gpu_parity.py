@@ -31,6 +31,8 @@ DECODE_CASES = {
     "heads_48_hi16": (2, [300, 90], 16, 64, 50, 48, 0, False, {}),
     "softmax_stress": (2, [400, 150], 4, 64, 64, 16, 0, False, {"q_std": 1.0, "scale": 1.0}),
     "hi64_fp8_contiguous": (3, [900, 129, 2], 64, 128, 100, 128, 0, True, {}),
+    # s_max not a multiple of 4: the key scales are copied lane by lane
+    "hi64_fp8_contiguous_odd_s_max": (2, [901, 37], 64, 128, 64, 128, 0, True, {}),
     "hi64_paged_page128": (3, [1000, 128, 300], 64, 128, 200, 128, 128, False, {}),
     "hi64_paged_page16_generic": (2, [333, 40], 64, 128, 64, 128, 16, False, {}),
     "zero_length_sequence": (3, [100, 0, 5], 64, 128, 16, 128, 0, False, {}),
