@@ -26,6 +26,7 @@
 // compaction walking the row in chunks; rows that fit are staged in shared
 // memory once, longer ones re-read from global memory (L2) each pass.
 #include "kernels.h"
+#include "tc_common.cuh"
 
 namespace dsi {
 
@@ -352,6 +353,251 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
   if (count && tid == 0) count[r] = K;
 }
 
+// ---------------------------------------------------------------------------
+// Cluster form: the CL CTAs of a cluster share one row.  The row is cut into
+// CL equal runs of kpt * 1024 positions (kpt <= KPT keys a thread, chosen per
+// row from its length), CTA q holding run q in registers with the same
+// warp-major layout as above.  Each pass every CTA histograms its own keys,
+// and after a cluster barrier every CTA sums the CL histograms through
+// distributed shared memory, so all of them take the same bin and the same
+// number of passes.  The compaction offsets of run q are the kept counts of
+// runs 0 .. q-1, read the same way.  A row that fits one CTA's registers
+// (KPT keys a thread) is taken by CTA 0 alone, the others leave at once, so
+// short rows cost one CTA.  Used when the rows are too few (or too long) to
+// fill the GPU with one CTA each.
+__device__ __forceinline__ int ld_peer_s32(const void* local, uint32_t rank) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];\n"
+               : "=r"(v)
+               : "r"(tc::map_to_rank(tc::smem_u32(local), rank))
+               : "memory");
+  return v;
+}
+// Two adjacent counters (8-byte aligned) of the same CTA of the cluster.
+__device__ __forceinline__ int2 ld_peer_v2(const void* local, uint32_t rank) {
+  int2 v;
+  asm volatile("ld.shared::cluster.v2.s32 {%0, %1}, [%2];\n"
+               : "=r"(v.x), "=r"(v.y)
+               : "r"(tc::map_to_rank(tc::smem_u32(local), rank))
+               : "memory");
+  return v;
+}
+
+template <int CL, int KPT>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kTopkThreads, 1)
+topk_rows_cl(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
+             const int32_t* __restrict__ row_len, int64_t q_offset, int K,
+             int32_t* __restrict__ idx, int32_t* __restrict__ count, int tps) {
+  __shared__ __align__(16) int hist[2][kBins];   // alternate passes (the peers read both)
+  __shared__ int wsum[2][kWarps];
+  __shared__ int wbase[2][kWarps];
+  __shared__ uint32_t s_sel[2];
+  __shared__ uint32_t s_range[2];         // this CTA's smallest and largest key (peers read them)
+  __shared__ int s_cnt[2];                // this CTA's keys above T and equal to T (peers read them)
+  grid_dep_wait();
+  grid_dep_launch();
+  const int q = (int)tc::cluster_ctarank();
+  const int r = blockIdx.x / CL;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const unsigned kAll = 0xffffffffu;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int64_t n = !row_len ? q_offset + r + 1
+              : tps == 1 ? (int64_t)row_len[r]
+                         : (int64_t)row_len[r / tps] - (tps - 1 - r % tps);
+  if (n < 0) n = 0;
+  if (n > n_cap) n = n_cap;
+  int32_t* out = idx + (int64_t)r * K;
+  const float* grow = scores + (int64_t)r * ld;
+  if (n <= K) {  // every candidate is kept (the same decision in every CTA of the cluster)
+    for (int64_t j = q * kTopkThreads + tid; j < K; j += CL * kTopkThreads)
+      out[j] = j < n ? (int32_t)j : -1;
+    if (count && q == 0 && tid == 0) count[r] = (int32_t)n;
+    return;
+  }
+  // ---- this CTA's run of the row: kpt keys a thread --------------------------
+  // coop: the CL CTAs share the row; otherwise CTA 0 takes it alone (a
+  // decision every CTA of the cluster makes the same way)
+  const bool coop = n > (int64_t)KPT * kTopkThreads;
+  if (!coop && q != 0) return;
+  const int parts = coop ? CL : 1;
+  const int kpt = (int)((n + parts * kTopkThreads - 1) / (parts * kTopkThreads));   // <= KPT
+  const int64_t run0 = (int64_t)q * kpt * kTopkThreads;
+  const int64_t wpos = run0 + (int64_t)wid * kpt * 32;
+  uint32_t key[KPT];
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    const int64_t p = wpos + 32 * i + lane;
+    key[i] = (i < kpt && p < n) ? max(score_key(__ldg(grow + p)), 1u) : 0u;
+  }
+  for (int i = tid; i < 2 * kBins; i += blockDim.x) (&hist[0][0])[i] = 0;
+  {
+    uint32_t kmax = 0u, kmin = 0xffffffffu;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      kmax = max(kmax, key[i]);
+      kmin = min(kmin, key[i] == 0u ? 0xffffffffu : key[i]);
+    }
+    kmax = __reduce_max_sync(kAll, kmax);
+    kmin = __reduce_min_sync(kAll, kmin);
+    if (lane == 0) { wsum[0][wid] = (int)kmax; wsum[1][wid] = (int)kmin; }
+    __syncthreads();
+    if (wid == 0) {
+      kmax = __reduce_max_sync(kAll, (uint32_t)wsum[0][lane]);
+      kmin = __reduce_min_sync(kAll, (uint32_t)wsum[1][lane]);
+      if (lane == 0) { s_range[0] = kmin; s_range[1] = kmax; }
+    }
+  }
+  // every CTA's range (and cleared histograms) in place
+  if (coop) tc::cluster_sync(); else __syncthreads();
+  if (wid == 0) {
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    if (lane < parts) {
+      kmin = (uint32_t)ld_peer_s32(&s_range[0], lane);
+      kmax = (uint32_t)ld_peer_s32(&s_range[1], lane);
+    }
+    kmin = __reduce_min_sync(kAll, kmin);
+    kmax = __reduce_max_sync(kAll, kmax);
+    if (lane == 0) { s_sel[0] = kmin; s_sel[1] = kmax; }
+  }
+  __syncthreads();
+  uint32_t lo = s_sel[0], hi = s_sel[1];
+  int krem = K;
+  // ---- narrow [lo, hi] to T over the cluster's summed histograms --------------
+  int pass = 0;
+#pragma unroll 1
+  while (lo != hi) {
+    const uint32_t span = hi - lo;
+    const int bits = 32 - __clz(span);
+    const int sh = bits > 11 ? bits - 11 : 0;
+    int* h = hist[pass & 1];
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      const uint32_t off = key[i] - lo;
+      if (off <= span) atomicAdd(&h[off >> sh], 1);
+    }
+    // every CTA's histogram of this pass is complete, and every CTA is done
+    // reading the previous pass's buffer, which is cleared for the next pass
+    if (coop) tc::cluster_sync(); else __syncthreads();
+    {
+      int* hp = hist[(pass + 1) & 1];
+      hp[tid] = 0;
+      hp[tid + kTopkThreads] = 0;
+    }
+    const int b0 = kBins - 1 - 64 * wid - 2 * lane;
+    int c0 = 0, c1 = 0;
+    if (coop) {
+#pragma unroll
+      for (int rk = 0; rk < CL; ++rk) {
+        const int2 v = ld_peer_v2(&h[b0 - 1], rk);
+        c0 += v.y;
+        c1 += v.x;
+      }
+    } else {
+      c0 = h[b0];
+      c1 = h[b0 - 1];
+    }
+    int incl = c0 + c1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kAll, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[pass & 1][wid] = incl;
+    __syncthreads();
+    const int wt = wsum[pass & 1][lane];
+    int wincl = wt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kAll, wincl, o);
+      if (lane >= o) wincl += y;
+    }
+    const int above_w = __shfl_sync(kAll, wincl - wt, wid);
+    const int above = above_w + incl - (c0 + c1);
+    if (above < krem && above + c0 + c1 >= krem) {
+      if (above + c0 >= krem) { s_sel[0] = (uint32_t)b0; s_sel[1] = (uint32_t)above; }
+      else { s_sel[0] = (uint32_t)(b0 - 1); s_sel[1] = (uint32_t)(above + c0); }
+    }
+    __syncthreads();
+    const uint32_t b = s_sel[0];
+    krem -= (int)s_sel[1];
+    const uint64_t top = (uint64_t)lo + ((uint64_t)(b + 1) << sh) - 1;
+    lo += b << sh;
+    hi = top < (uint64_t)hi ? (uint32_t)top : hi;
+    ++pass;
+    if (sh == 0) break;
+  }
+  const uint32_t T = lo;
+  // ---- ordered compaction: this run's offsets follow runs 0 .. q-1 -----------
+  int gt = 0, eq = 0;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) { gt += key[i] > T; eq += key[i] == T; }
+  gt = __reduce_add_sync(kAll, gt);
+  eq = __reduce_add_sync(kAll, eq);
+  __syncthreads();                       // s_sel / wsum readers of the last pass are done
+  if (lane == 0) { wsum[0][wid] = gt; wsum[1][wid] = eq; }
+  __syncthreads();
+  if (wid == 0) {
+    const int gs = __reduce_add_sync(kAll, wsum[0][lane]);
+    const int es = __reduce_add_sync(kAll, wsum[1][lane]);
+    if (lane == 0) { s_cnt[0] = gs; s_cnt[1] = es; }
+  }
+  if (coop) tc::cluster_sync();          // every run's counts in place
+  else __syncthreads();
+  if (wid == 0) {
+    int eq_run = 0, sel_run = 0;         // equals and kept keys of the runs before this one
+    for (int rk = 0; rk < q; ++rk) {
+      const int g = ld_peer_s32(&s_cnt[0], rk), e = ld_peer_s32(&s_cnt[1], rk);
+      int take = krem - eq_run;
+      take = take < 0 ? 0 : (take > e ? e : take);
+      sel_run += g + take;
+      eq_run += e;
+    }
+    const int g = wsum[0][lane], e = wsum[1][lane];
+    int ei = e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kAll, ei, o);
+      if (lane >= o) ei += y;
+    }
+    const int ebase = eq_run + ei - e;
+    int take = krem - ebase;
+    take = take < 0 ? 0 : (take > e ? e : take);
+    const int sel = g + take;
+    int si = sel;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kAll, si, o);
+      if (lane >= o) si += y;
+    }
+    wbase[0][lane] = ebase;
+    wbase[1][lane] = sel_run + si - sel;
+  }
+  if (coop) tc::cluster_sync();          // no peer reads this CTA's shared memory past here
+  else __syncthreads();
+  int eq_rank = wbase[0][wid], pos = wbase[1][wid];
+  if (eq == 0) {                         // warp-uniform: no ties at T in this warp
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      const bool keep = key[i] > T;
+      const unsigned km = __ballot_sync(kAll, keep);
+      if (keep) out[pos + __popc(km & lt_mask)] = (int32_t)(wpos + 32 * i + lane);
+      pos += __popc(km);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      const bool is_eq = key[i] == T;
+      const unsigned em = __ballot_sync(kAll, is_eq);
+      const bool keep = key[i] > T || (is_eq && eq_rank + __popc(em & lt_mask) < krem);
+      const unsigned km = __ballot_sync(kAll, keep);
+      if (keep) out[pos + __popc(km & lt_mask)] = (int32_t)(wpos + 32 * i + lane);
+      pos += __popc(km);
+      eq_rank += __popc(em);
+    }
+  }
+  if (count && q == 0 && tid == 0) count[r] = K;
+}
+
 cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t* row_len,
                         int64_t q_offset, int K, int32_t* idx, int32_t* count, cudaStream_t st,
                         int tps, int64_t n_cap) {
@@ -359,12 +605,25 @@ cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t
   n_cap = (n_cap < 0 || n_cap > ld) ? ld : n_cap;
   const int64_t longest = row_len ? n_cap : (q_offset + rows < n_cap ? q_offset + rows : n_cap);
   if (longest <= kRegChunks * kRegKeysMax) {
-    cudaError_t e =
-        longest <= kRegKeysMax
-            ? launch_overlapped(topk_rows_reg<false>, dim3(rows), dim3(kTopkThreads), 0, st, scores,
-                                ld, n_cap, row_len, q_offset, K, idx, count, tps)
-            : launch_overlapped(topk_rows_reg<true>, dim3(rows), dim3(kTopkThreads), 0, st, scores,
-                                ld, n_cap, row_len, q_offset, K, idx, count, tps);
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e;
+    if (longest <= kRegKeysMax) {
+      // rows of one chunk: two CTAs a row while that still fits in one wave
+      e = 2L * rows <= sms
+              ? launch_overlapped(topk_rows_cl<2, kRegPer / 2>, dim3(2 * rows), dim3(kTopkThreads),
+                                  0, st, scores, ld, n_cap, row_len, q_offset, K, idx, count, tps)
+              : launch_overlapped(topk_rows_reg<false>, dim3(rows), dim3(kTopkThreads), 0, st,
+                                  scores, ld, n_cap, row_len, q_offset, K, idx, count, tps);
+    } else {
+      // longer rows: four CTAs a row hold up to 131072 keys in registers
+      e = (long)rows <= 2L * sms
+              ? launch_overlapped(topk_rows_cl<4, kRegPer>, dim3(4 * rows), dim3(kTopkThreads), 0,
+                                  st, scores, ld, n_cap, row_len, q_offset, K, idx, count, tps)
+              : launch_overlapped(topk_rows_reg<true>, dim3(rows), dim3(kTopkThreads), 0, st,
+                                  scores, ld, n_cap, row_len, q_offset, K, idx, count, tps);
+    }
     note_launch();
     return e;
   }

@@ -202,6 +202,8 @@ TOPK_CASES = [
     (2, 32769, 100, 50, False),       # one past the register-resident rows: two chunks
     (2, 131072, 2048, 1 << 16, True), # four chunks, the longest rows the chunked kernel takes
     (1, 140000, 512, 100, False),     # beyond: the 8-bit radix kernel, re-reading from L2
+    (160, 4000, 256, 9, True),        # enough rows for one CTA each (no cluster)
+    (320, 40000, 512, 1 << 12, False),  # enough long rows for one CTA each: chunked reloads
 ]
 
 
