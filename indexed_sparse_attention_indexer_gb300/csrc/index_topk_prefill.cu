@@ -307,11 +307,15 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     if (lane == 0) {
       prefetch_tmap(&kmap);
       prefetch_tmap(&qmap);
-      int stage = 0, qcount = 0;
+      int stage = 0, qcount = 0, n_issued = 0;
       uint32_t ph = 0;
-      bool issued[kStages] = {};
-      uint32_t issued_ph[kStages] = {};
       bool ok = true;
+      // contiguous keys: a tile is one 128-row box per 64-dim block (rows past
+      // the group's history are read and masked by the epilogue); paged:
+      // 64-row boxes through the block table.  The rows are worked out before
+      // the stage wait: one thread issues every tile, so its instruction
+      // latency bounds the tile rate.
+      const bool whole = c.block_table == nullptr;
       for (int k = 0; ok && k < nmax; ++k) {
         const int g = zigzag_group(k, blockIdx.x, gridDim.x, a.groups);
         if (g < 0) continue;
@@ -325,34 +329,44 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                         &q_full[slot]);
         ++qcount;
         const int ntile = group_tiles(a, g);
+        const int64_t nvis = a.q_offset + min(a.rows, (g + 1) * NT);
         for (int j = 0; j < ntile; ++j) {
-          if (!(ok = mbar_wait(&empty[stage], ph ^ 1, abort_flag, err))) break;
-          const int64_t nvis = a.q_offset + min(a.rows, (g + 1) * NT);
-          int nsub = 0;
+          int nsub = 2;
           int64_t prow[2];
+          prow[0] = (int64_t)j * kTileM;
+          prow[1] = prow[0] + kSub;
+          if (!whole) {
+            nsub = 0;
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int64_t p = (int64_t)j * kTileM + i * kSub;
-            prow[i] = -1;
-            if (p < nvis) { prow[i] = phys_row(c, 0, p, err); if (prow[i] >= 0) ++nsub; }
+            for (int i = 0; i < 2; ++i) {
+              const int64_t p = (int64_t)j * kTileM + i * kSub;
+              prow[i] = -1;
+              if (p < nvis) { prow[i] = phys_row(c, 0, p, err); if (prow[i] >= 0) ++nsub; }
+            }
           }
+          if (!(ok = mbar_wait(&empty[stage], ph ^ 1, abort_flag, err))) break;
           uint8_t* as = smem + OFF_A + stage * A_BYTES;
           mbar_arrive_expect_tx(&full[stage], (uint32_t)(nsub * (A_BYTES / 2)));
+          if (whole) {
+            tma_load_2d(as, &kmap, 0, (int)prow[0], &full[stage]);
+            tma_load_2d(as + 16384, &kmap, 64, (int)prow[0], &full[stage]);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            if (prow[i] < 0) continue;
-            tma_load_2d(as + i * (kSub * 128), &kmap, 0, (int)prow[i], &full[stage]);
-            tma_load_2d(as + 16384 + i * (kSub * 128), &kmap, 64, (int)prow[i], &full[stage]);
+            for (int i = 0; i < 2; ++i) {
+              if (prow[i] < 0) continue;
+              tma_load_2d(as + i * (kSub * 128), &kmap, 0, (int)prow[i], &full[stage]);
+              tma_load_2d(as + 16384 + i * (kSub * 128), &kmap, 64, (int)prow[i], &full[stage]);
+            }
           }
-          issued[stage] = true;
-          issued_ph[stage] = ph;
+          ++n_issued;
           if (++stage == kStages) { stage = 0; ph ^= 1; }
         }
       }
+      // after an abort, wait (bounded by time) for the last tiles' copies
       if (*abort_flag) {
         volatile int no_abort = 0;
-        for (int s = 0; s < kStages; ++s)
-          if (issued[s]) mbar_wait(&full[s], issued_ph[s], &no_abort, err, 100000000ull);
+        for (int t = max(0, n_issued - kStages); t < n_issued; ++t)
+          mbar_wait(&full[t % kStages], (uint32_t)((t / kStages) & 1), &no_abort, err, 100000000ull);
       }
     }
     __syncwarp();
@@ -565,7 +579,9 @@ cudaError_t launch_index_topk_prefill(const bf16* q_idx, const float* w, const C
   const uint64_t krows = c.block_table ? (uint64_t)c.num_pages * c.page_size
                                        : (uint64_t)c.batch * c.s_max;
   CUtensorMap kmap, qmap;
-  if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, krows, kD, 64, kSub))
+  // contiguous keys: one 128-row box per 64-dim block of a tile; paged: 64-row boxes
+  if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, krows, kD, 64,
+                  c.block_table ? kSub : kTileM))
     return cudaErrorInvalidValue;
   if (!tma_map_2d(&qmap, q_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)rows * kHeads, kD, 64,
                   kHeads))
