@@ -95,11 +95,37 @@ mla_simt(const bf16* __restrict__ q, CacheView c, const float* __restrict__ lsca
   const int32_t* irow = idx + (int64_t)r * K;
   const float sl2 = scale * kLog2e;  // logits in log2 units
 
-  for (int i = tid; i < kHB * DSI_D_QK; i += kMlaThreads) {
-    const int h = i / DSI_D_QK, e = i - h * DSI_D_QK;
-    S.q[h][e] = h < hcount ? __bfloat162float(q[((int64_t)r * H + g * kHB + h) * DSI_D_QK + e]) * sl2
-                           : 0.f;
+  // the block's query rows in fp32 (pre-scaled): every 16-byte load is issued
+  // before any is converted, so their latencies overlap
+  {
+    constexpr int kQv = kHB * DSI_D_QK / 8;                     // 8-element pieces
+    constexpr int kQPer = (kQv + kMlaThreads - 1) / kMlaThreads;
+    uint4 qr[kQPer];
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = tid + k * kMlaThreads;
+      const int h = i / (DSI_D_QK / 8), pc = i - h * (DSI_D_QK / 8);
+      qr[k] = (i < kQv && h < hcount)
+                  ? __ldg(reinterpret_cast<const uint4*>(
+                        q + ((int64_t)r * H + g * kHB + h) * DSI_D_QK + pc * 8))
+                  : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = tid + k * kMlaThreads;
+      if (i < kQv) {
+        const int h = i / (DSI_D_QK / 8), pc = i - h * (DSI_D_QK / 8);
+        float f[8];
+        bf16x8_to_f32(qr[k], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) S.q[h][pc * 8 + e] = f[e] * sl2;
+      }
+    }
   }
+  // the indices come from the kernel launched before this one (the query rows
+  // do not); the kernel after this one may start its set-up
+  grid_dep_wait();
+  grid_dep_launch();
   if (tid < kHB) { S.m[tid] = -INFINITY; S.l[tid] = 0.f; }
 
   auto gather = [&](int buf, int j0) {
@@ -178,7 +204,10 @@ mla_simt(const bf16* __restrict__ q, CacheView c, const float* __restrict__ lsca
           a1 = fmaf(st, b1, a1);
         }
       } else if (!F8 && S.valid[buf][pr]) {
+        // four partial sums per head (dims 8ch + {0,4}, {1,5}, ...), so the
+        // multiply-adds form four short chains instead of one long one
         const bf16* crow = &S.c[buf][pr][0];
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
         for (int ch = 0; ch < 72; ++ch) {
           float cf[8];
@@ -186,13 +215,17 @@ mla_simt(const bf16* __restrict__ q, CacheView c, const float* __restrict__ lsca
           const float4* q0 = reinterpret_cast<const float4*>(&S.q[h0][ch * 8]);
           const float4* q1 = reinterpret_cast<const float4*>(&S.q[h0 + 1][ch * 8]);
           float4 x0 = q0[0], x1 = q0[1], y0 = q1[0], y1 = q1[1];
-          a0 = fmaf(x0.x, cf[0], a0); a0 = fmaf(x0.y, cf[1], a0); a0 = fmaf(x0.z, cf[2], a0);
-          a0 = fmaf(x0.w, cf[3], a0); a0 = fmaf(x1.x, cf[4], a0); a0 = fmaf(x1.y, cf[5], a0);
-          a0 = fmaf(x1.z, cf[6], a0); a0 = fmaf(x1.w, cf[7], a0);
-          a1 = fmaf(y0.x, cf[0], a1); a1 = fmaf(y0.y, cf[1], a1); a1 = fmaf(y0.z, cf[2], a1);
-          a1 = fmaf(y0.w, cf[3], a1); a1 = fmaf(y1.x, cf[4], a1); a1 = fmaf(y1.y, cf[5], a1);
-          a1 = fmaf(y1.z, cf[6], a1); a1 = fmaf(y1.w, cf[7], a1);
+          s0[0] = fmaf(x0.x, cf[0], s0[0]); s0[1] = fmaf(x0.y, cf[1], s0[1]);
+          s0[2] = fmaf(x0.z, cf[2], s0[2]); s0[3] = fmaf(x0.w, cf[3], s0[3]);
+          s0[0] = fmaf(x1.x, cf[4], s0[0]); s0[1] = fmaf(x1.y, cf[5], s0[1]);
+          s0[2] = fmaf(x1.z, cf[6], s0[2]); s0[3] = fmaf(x1.w, cf[7], s0[3]);
+          s1[0] = fmaf(y0.x, cf[0], s1[0]); s1[1] = fmaf(y0.y, cf[1], s1[1]);
+          s1[2] = fmaf(y0.z, cf[2], s1[2]); s1[3] = fmaf(y0.w, cf[3], s1[3]);
+          s1[0] = fmaf(y1.x, cf[4], s1[0]); s1[1] = fmaf(y1.y, cf[5], s1[1]);
+          s1[2] = fmaf(y1.z, cf[6], s1[2]); s1[3] = fmaf(y1.w, cf[7], s1[3]);
         }
+        a0 = (s0[0] + s0[1]) + (s0[2] + s0[3]);
+        a1 = (s1[0] + s1[1]) + (s1[2] + s1[3]);
       } else {
         a0 = -INFINITY; a1 = -INFINITY;
       }
@@ -284,6 +317,7 @@ __global__ void __launch_bounds__(128)
 mla_combine(const float* __restrict__ part_o, const float2* __restrict__ part_ml, int H,
             int splits, bf16* __restrict__ out, float* __restrict__ lse) {
   const int r = blockIdx.y, h = blockIdx.x, tid = threadIdx.x;
+  grid_dep_wait();   // the partials come from the attention kernel launched just before
   float M = -INFINITY;
   for (int s = 0; s < splits; ++s) M = fmaxf(M, part_ml[((int64_t)r * splits + s) * H + h].x);
   float L = 0.f;
@@ -308,9 +342,10 @@ mla_combine(const float* __restrict__ part_o, const float2* __restrict__ part_ml
 
 cudaError_t launch_mla_combine(const float* part_o, const float2* part_ml, int rows, int H,
                                int splits, bf16* out, float* lse, cudaStream_t st) {
-  mla_combine<<<dim3(H, rows), 128, 0, st>>>(part_o, part_ml, H, splits, out, lse);
+  const cudaError_t e = launch_overlapped(mla_combine, dim3(H, rows), dim3(128), 0, st, part_o,
+                                          part_ml, H, splits, out, lse);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 size_t mla_partials_bytes(int rows, int n_heads, int splits) {
@@ -362,14 +397,11 @@ static cudaError_t launch_simt(const bf16* q, const CacheView& c, const float* l
     part_ml = reinterpret_cast<float2*>(reinterpret_cast<char*>(ws) + n * DSI_D_LATENT * sizeof(float));
   }
   dim3 grid((H + kHB - 1) / kHB, rows, splits);
-  mla_simt<F8><<<grid, kMlaThreads, smem, st>>>(q, c, lscale, idx, H, K, decode, q_offset, scale,
-                                                out, lse, part_o, part_ml, splits, err);
+  e = launch_overlapped(mla_simt<F8>, grid, dim3(kMlaThreads), smem, st, q, c, lscale, idx, H, K,
+                        decode, q_offset, scale, out, lse, part_o, part_ml, splits, err);
   note_launch();
-  e = cudaGetLastError();
   if (e != cudaSuccess || splits == 1) return e;
-  mla_combine<<<dim3(H, rows), 128, 0, st>>>(part_o, part_ml, H, splits, out, lse);
-  note_launch();
-  return cudaGetLastError();
+  return launch_mla_combine(part_o, part_ml, rows, H, splits, out, lse, st);
 }
 
 cudaError_t launch_sparse_mla(const bf16* q, const CacheView& c, const int32_t* idx, int rows,

@@ -204,6 +204,9 @@ TOPK_CASES = [
     (1, 140000, 512, 100, False),     # beyond: the 8-bit radix kernel, re-reading from L2
     (160, 4000, 256, 9, True),        # enough rows for one CTA each (no cluster)
     (320, 40000, 512, 1 << 12, False),  # enough long rows for one CTA each: chunked reloads
+    (9, 2048, 128, 3, True),          # short rows, heavy ties
+    (7, 1999, 1, 1 << 20, False),     # short rows, K = 1, odd row stride
+    (6, 2048, 2000, 50, True),        # short rows, K near n
 ]
 
 
