@@ -207,6 +207,8 @@ TOPK_CASES = [
     (9, 2048, 128, 3, True),          # short rows, heavy ties
     (7, 1999, 1, 1 << 20, False),     # short rows, K = 1, odd row stride
     (6, 2048, 2000, 50, True),        # short rows, K near n
+    (3, 16384, 2048, 50, True),       # the largest row one CTA of a two-CTA cluster takes alone
+    (3, 16385, 2048, 50, False),      # one past it: both CTAs share the row (9 keys a thread)
 ]
 
 
