@@ -24,14 +24,16 @@
 // rounded to E4M3 (exact for the integer-valued index queries).
 //
 // MXFP8 keys (E4M3 codes, one E8M0 scale per group of 32, 64 or 128
-// elements; "Day 0 Inference Support...", "A Layered Strategy"): the producer
-// lands the codes and each tile's group scales by TMA, extra dequantising
-// warps turn them into the exact bf16 values code * 2^X in a swizzled A tile
-// (three tiles in flight), and the bf16 MMA runs on that; the index queries are
-// MXFP8-quantised group by group on the fly and stored dequantised the same
-// way.  The tensor core thus sums exactly the products of the dequantised
-// operands (what a block-scaled MMA computes) while HBM carries one byte per
-// key element plus a byte per group.
+// elements; "Day 0 Inference Support...", "A Layered Strategy"): the codes
+// land by TMA as FP8 keys do and the tile's group scales by one bulk copy; the
+// index queries are MXFP8-quantised group by group on the fly (codes in the
+// B slot, scale bytes beside it).  Four scale warps, one per TMEM lane
+// quarter, copy each tile's key scales and each query group's scales into
+// TMEM, and the block-scaled MMA (kind::mxf8f6f4, one scale per 32 elements
+// of K on both operands) applies them inside the tensor core: the
+// dequantisation is fused into the contraction and nothing else in the
+// kernel touches a code.  HBM carries one byte per key element plus a byte
+// per group.
 #include "kernels.h"
 #include "tc_common.cuh"
 #include "tma_host.h"
@@ -55,47 +57,58 @@ struct Cfg {
   static constexpr bool MX = KK == kKeyMx;
   static constexpr bool K8 = FP8 || MX;                   // one byte per key element in HBM
   static constexpr int N = NT * kHeads;
-  static constexpr int EB = FP8 ? 1 : 2;                  // MMA operand element bytes
-  static constexpr int A_BYTES = kTileM * kD * EB;        // one MMA A tile: 16 or 32 KB
-  static constexpr int ST_BYTES = K8 ? kTileM * kD : A_BYTES;   // one TMA stage of keys
+  static constexpr int EB = K8 ? 1 : 2;                   // MMA operand element bytes
+  static constexpr int ST_BYTES = kTileM * kD * EB;       // one stage = one MMA A tile: 16 or 32 KB
   static constexpr int B_BYTES = N * kD * EB;
-  static constexpr int STAGES = FP8 ? 8 : MX ? (NT == 1 ? 5 : NT == 2 ? 4 : 2) : (NT == 1 ? 4 : 2);
-  static constexpr int ABUFS = MX ? (NT == 1 ? 3 : NT == 2 ? 2 : 1) : 0;   // dequantised bf16 A tiles
-  static constexpr int DQ_WARPS = MX ? (NT == 1 ? 8 : 2) : 0;   // dequantising warps
-  static constexpr int DQ_THREADS = DQ_WARPS * 32;
-  // a dequantising thread converts DQ_UPP 16-code units of each of DQ_PASSES
-  // tile rows per tile (the 32 rows of one warp are consecutive)
-  static constexpr int DQ_PASSES = MX ? (DQ_THREADS >= kTileM ? 1 : kTileM / DQ_THREADS) : 0;
-  static constexpr int DQ_UPP = MX ? (DQ_THREADS >= kTileM ? 8 * kTileM / DQ_THREADS : 8) : 0;
-  // one stage's group scales: two 64-key sub-tiles of <= 256 bytes, each at a
-  // 256-byte slot (TMA destinations are 128-byte aligned)
-  static constexpr int SC_SUB = 256;
-  static constexpr int SC_BYTES = 2 * SC_SUB;
+  static constexpr int STAGES = K8 ? 8 : (NT == 1 ? 4 : 2);
+  // MXFP8: one stage's key scales (128 keys x up to 4 bytes) and one query
+  // slot's scale words (a 32-bit word per query row: the E8M0 bytes of its
+  // four 32-element blocks of K)
+  static constexpr int SC_BYTES = MX ? kTileM * 4 : 0;
+  static constexpr int SQ_BYTES = MX ? N * 4 : 0;
+  static constexpr int SF_WARPS = MX ? 4 : 0;             // scale warps, one per TMEM lane quarter
   static constexpr int EPI_WARPS = NT == 1 ? 4 : 8;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   // producer warps: tile k is issued by producer k % PRODUCERS (one warp's
   // serial per-tile path cannot keep up with single-token decode over
   // one-byte keys, whose 16 KB tiles arrive twice as often as bf16 tiles)
   static constexpr int PRODUCERS = NT == 1 && K8 ? 2 : 1;
-  static constexpr int PROD_WARP1 = 2 + EPI_WARPS + DQ_WARPS;   // first extra producer warp
-  static constexpr int THREADS = 64 + EPI_THREADS + DQ_THREADS + 32 * (PRODUCERS - 1);
+  static constexpr int PROD_WARP1 = 2 + EPI_WARPS + SF_WARPS;   // the extra producer warp
+  // MMA issuers: tile k is issued by issuer k % MMA_WARPS.  One thread's
+  // serial chain per tile (three barrier waits, four or eight MMAs, two or
+  // three commits, the work-list step) takes ~0.7 us, longer than a
+  // single-token decode tile takes to arrive.
+  static constexpr int MMA_WARPS = NT == 1 ? 2 : 1;
+  static constexpr int MMA_WARP1 = PROD_WARP1 + PRODUCERS - 1;   // the extra MMA warp
+  static constexpr int THREADS =
+      64 + EPI_THREADS + 32 * SF_WARPS + 32 * (PRODUCERS - 1) + 32 * (MMA_WARPS - 1);
+  // MXFP8 scale columns in TMEM: per stage four (key row m's word in column
+  // m / 32 of lane m), per query slot N / 32 (at least four)
+  static constexpr int SFB_STRIDE = N / 32 < 4 ? 4 : N / 32;
+  static constexpr int SF_COLS = MX ? STAGES * 4 + 2 * SFB_STRIDE : 0;
   // TMEM accumulators: four where they fit (the epilogue of tile i then
   // releases its accumulator four tiles ahead of the MMA that reuses it)
-  static constexpr int ACCS = 4 * N <= 512 ? 4 : 2;
-  static constexpr int TMEM_COLS = ACCS * N <= 128 ? 128 : (ACCS * N <= 256 ? 256 : 512);
-  static constexpr int KSTEPS = FP8 ? 4 : 8;              // 32 bytes of K per MMA
-  static constexpr uint32_t IDESC = idesc_f32(FP8 ? 0u : 1u, kTileM, N);
+  static constexpr int ACCS =
+      4 * N + SF_COLS <= 512 ? 4 : (2 * N + SF_COLS <= 512 ? 2 : 1);
+  static constexpr int SFA_COL = ACCS * N;
+  static constexpr int SFB_COL = SFA_COL + STAGES * 4;
+  static constexpr int TMEM_USED = ACCS * N + SF_COLS;
+  static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : (TMEM_USED <= 256 ? 256 : 512);
+  static_assert(TMEM_USED <= 512, "TMEM columns");
+  static constexpr int KSTEPS = K8 ? 4 : 8;               // 32 bytes of K per MMA
+  static constexpr uint32_t IDESC =
+      MX ? idesc_mxf8(kTileM, N, 0, 0) : idesc_f32(FP8 ? 0u : 1u, kTileM, N);
   static constexpr int TOK_PER_THREAD = NT == 1 ? 1 : NT / 2;   // epilogue column split
   // shared memory carve (offsets from a 1024-aligned base)
   static constexpr int OFF_A = 0;                                   // TMA stages
-  static constexpr int OFF_ABF = OFF_A + STAGES * ST_BYTES;         // MXFP8: bf16 A tiles
-  static constexpr int OFF_B = OFF_ABF + ABUFS * A_BYTES;
-  static constexpr int OFF_SC = OFF_B + 2 * B_BYTES;                // MXFP8: group scales
-  static constexpr int OFF_KS = OFF_SC + (MX ? STAGES * SC_BYTES : 0);  // FP8: per-stage key scales
+  static constexpr int OFF_B = OFF_A + STAGES * ST_BYTES;
+  static constexpr int OFF_SC = OFF_B + 2 * B_BYTES;                // MXFP8: key scales
+  static constexpr int OFF_SQ = OFF_SC + STAGES * SC_BYTES;         // MXFP8: query scale words
+  static constexpr int OFF_KS = OFF_SQ + 2 * SQ_BYTES;              // FP8: per-stage key scales
   static constexpr int OFF_W = OFF_KS + (FP8 ? STAGES * kTileM * 4 : 0); // per epilogue warp: weights
   static constexpr int OFF_PREFIX = OFF_W + EPI_WARPS * TOK_PER_THREAD * kHeads * 4;
   static constexpr int OFF_BAR = (OFF_PREFIX + (kMaxGroups + 1) * 4 + 7) & ~7;
-  static constexpr int NBARS = 2 * STAGES + 2 * ACCS + 2 + 2 + 1 + 2 * ABUFS;
+  static constexpr int NBARS = 2 * STAGES + 2 * ACCS + 2 + 2 + 1 + (MX ? STAGES : 0);
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8 + 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;                 // + alignment slack
   static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -168,7 +181,7 @@ struct ItemIter {
 template <int NT, int KK>
 __global__ void __launch_bounds__(Cfg<NT, KK>::THREADS, 1)
 score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-         const __grid_constant__ CUtensorMap smap, CacheView c, ScoreArgs a, int* err) {
+         CacheView c, ScoreArgs a, int* err) {
   using C = Cfg<NT, KK>;
   constexpr bool FP8 = C::FP8;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -185,8 +198,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
   uint64_t* q_full = acc_empty + C::ACCS;
   uint64_t* q_empty = q_full + 2;
   uint64_t* done_bar = q_empty + 2;
-  uint64_t* a_full = done_bar + 1;          // MXFP8: dequantised A tile ready
-  uint64_t* a_empty = a_full + C::ABUFS;    // MXFP8: its MMAs are done
+  uint64_t* sf_full = done_bar + 1;         // MXFP8: the stage's scales are in TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   __shared__ int scan_tmp[40];
@@ -209,24 +221,25 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     if (tid == 0) prefix[G] = total;
   }
   if (tid == 0) {
-    // MXFP8: a stage is empty once every dequantising warp has read it
     // FP8: the producer warp's 32 lanes also arrive on full when they copy the
     // key scales themselves, and a stage is empty once the MMAs and every
-    // epilogue warp (which reads its scales) are done with it
+    // epilogue warp (which reads its scales) are done with it.  MXFP8: the
+    // scale warps read the stage's scales before the MMAs are issued, so
+    // the MMAs' commit empties it.
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], FP8 && !a.sc_bulk ? 33 : 1);
-      mbar_init(&empty[s], C::MX ? C::DQ_WARPS : FP8 ? 1 + C::EPI_WARPS : 1);
+      mbar_init(&empty[s], FP8 ? 1 + C::EPI_WARPS : 1);
+      if (C::MX) mbar_init(&sf_full[s], C::SF_WARPS);
     }
-    for (int i = 0; i < C::ABUFS; ++i) { mbar_init(&a_full[i], C::DQ_WARPS); mbar_init(&a_empty[i], 1); }
     for (int i = 0; i < C::ACCS; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], C::EPI_THREADS);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
+      mbar_init(&q_empty[i], C::MMA_WARPS);
     }
-    mbar_init(done_bar, 1);
+    mbar_init(done_bar, C::MMA_WARPS);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -240,11 +253,13 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
   const int64_t it_begin = total_items * blockIdx.x / gridDim.x;
   const int64_t it_end = total_items * (blockIdx.x + 1) / gridDim.x;
 
-  if (warp == 0 || warp >= C::PROD_WARP1) {
+  const bool producer = warp == 0 || (C::PRODUCERS > 1 && warp == C::PROD_WARP1);
+  const bool issuer = warp == 1 || (C::MMA_WARPS > 1 && warp == C::MMA_WARP1);
+  if (producer) {
     // ======================= TMA producers ===================================
     // Producer pw issues the tiles k = pw, pw + PRODUCERS, ... of the CTA's
     // range; producer 0 also loads each group's queries.
-    const int pw = warp == 0 ? 0 : warp - C::PROD_WARP1 + 1;
+    const int pw = warp == 0 ? 0 : 1;
     ItemIter it;
     it.init(prefix, a.groups, it_begin, it_end);
     int gprev = -1, qcount = 0, stage = 0;
@@ -256,13 +271,13 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
                            ? __ffs(c.page_size) - 1 : -1;
     uint32_t phase = 0;
     int k = 0, last_k = -1;              // item index; last tile this warp issued (stage k % STAGES)
-    // contiguous bf16 / FP8 keys: one 128-row box per tile (the map's box is
-    // 128 rows); paged caches and MXFP8 keys: two 64-row boxes
-    const bool whole = !C::MX && c.block_table == nullptr;
+    // contiguous keys: one 128-row box per tile (the map's box is 128 rows);
+    // paged caches: two 64-row boxes
+    const bool whole = c.block_table == nullptr;
+    const int spr = kD >> a.lg_group;    // MXFP8: scale bytes per key
     if (lane == 0) {
       prefetch_tmap(&kmap);
       if (!C::K8) prefetch_tmap(&qmap);
-      if (C::MX) prefetch_tmap(&smap);
     }
     // The per-tile path is short: a warp's own instruction latency bounds its
     // tile rate.  Page ids and rows are worked out before the stage wait;
@@ -280,10 +295,12 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         if (!ok) break;
         uint8_t* qs = smem + C::OFF_B + slot * C::B_BYTES;
         if (C::MX) {
-          // MXFP8-quantise the index queries group by group and store them
-          // dequantised (exact in bf16) in the swizzled B slot; the lanes of
-          // one group are adjacent, so the group maximum is a butterfly
+          // MXFP8-quantise the index queries group by group: E4M3 codes into
+          // the swizzled B slot, the group's E8M0 byte into the row's scale
+          // word (once per 32-element block it covers); the lanes of one
+          // group are adjacent, so the group maximum is a butterfly
           const int upg = 1 << (a.lg_group - 4);     // 16-element units per group
+          uint8_t* sq = smem + C::OFF_SQ + slot * C::SQ_BYTES;
           constexpr int kIters = C::N * 8 / 32, kBatch = 4;
           static_assert(kIters % kBatch == 0, "whole batches");
           for (int i0 = 0; i0 < kIters; i0 += kBatch) {
@@ -314,11 +331,11 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
               for (int m = 1; m < upg; m <<= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
               const int X = mx_exponent(amax);
-              uint4 lo, hi;
-              mx_decode16(mx_encode16(f, X), X, lo, hi);
-              uint8_t* blk = qs + (u >> 2) * (C::N * 128);
-              *reinterpret_cast<uint4*>(blk + sw128_offset(n, (2 * u) & 7)) = lo;
-              *reinterpret_cast<uint4*>(blk + sw128_offset(n, (2 * u + 1) & 7)) = hi;
+              *reinterpret_cast<uint4*>(qs + sw128_offset(n, u)) = mx_encode16(f, X);
+              if ((u & (upg - 1)) == 0) {
+                const int kb0 = u >> 1, nkb = upg >> 1;
+                for (int t = 0; t < nkb; ++t) sq[n * 4 + kb0 + t] = (uint8_t)(X + 127);
+              }
             }
           }
           fence_proxy_async_smem();
@@ -431,20 +448,22 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         if (ok) {
           uint8_t* as = smem + C::OFF_A + stage * C::ST_BYTES;
           float* ks = reinterpret_cast<float*>(smem + C::OFF_KS) + stage * kTileM;
+          uint8_t* ms = smem + C::OFF_SC + stage * C::SC_BYTES;
           if (whole) {
             // contiguous keys: the tile is one 128-row box (rows past the
-            // history are read and ignored; past the array, zero-filled)
-            const uint32_t sc_bytes =
-                FP8 && a.sc_bulk ? (uint32_t)(c.s_max - p0 < kTileM ? c.s_max - p0 : kTileM) * 4u : 0u;
+            // history are read and ignored; past the array, zero-filled); the
+            // key scales of the sequence's rows in the tile follow by one bulk
+            // copy (16-byte aligned: sequences start at multiples of s_max)
+            const uint32_t kr = (uint32_t)(c.s_max - p0 < kTileM ? c.s_max - p0 : kTileM);
+            const uint32_t sc_bytes = FP8 && a.sc_bulk ? kr * 4u : C::MX ? kr * (uint32_t)spr : 0u;
             mbar_arrive_expect_tx(&full[stage], (uint32_t)C::ST_BYTES + sc_bytes);
             tma_load_2d(as, &kmap, 0, (int)prow[0], &full[stage]);
             if (!C::K8) tma_load_2d(as + 16384, &kmap, 64, (int)prow[0], &full[stage]);
-            if (sc_bytes) bulk_load(ks, c.k_scale + prow[0], sc_bytes, &full[stage]);
+            if (FP8 && sc_bytes) bulk_load(ks, c.k_scale + prow[0], sc_bytes, &full[stage]);
+            if (C::MX) bulk_load(ms, c.k_mx_scale + prow[0] * spr, sc_bytes, &full[stage]);
           } else {
-            // 64-row boxes (paged: one page's run each).  MXFP8: the sub-tile's
-            // 64 keys' group scales (64 * 128/G bytes) ride along, from a map
-            // that views the scale array as rows of 16 bytes
-            const int spr = kD >> a.lg_group;
+            // 64-row boxes (paged: one page's run each), each with its 64
+            // keys' scales by one bulk copy
             mbar_arrive_expect_tx(
                 &full[stage],
                 (uint32_t)(nsub * (C::ST_BYTES / 2 + (C::MX ? kSub * spr : 0) +
@@ -459,8 +478,8 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
                 tma_load_2d(as + 16384 + i * (kSub * 128), &kmap, 64, (int)prow[i], &full[stage]);
               }
               if (C::MX)
-                tma_load_2d(smem + C::OFF_SC + stage * C::SC_BYTES + i * C::SC_SUB, &smap, 0,
-                            (int)(prow[i] * spr / 16), &full[stage]);
+                bulk_load(ms + i * kSub * spr, c.k_mx_scale + prow[i] * spr, kSub * spr,
+                          &full[stage]);
               if (FP8 && a.sc_bulk)
                 bulk_load(ks + i * kSub, c.k_scale + prow[i], kSub * 4, &full[stage]);
             }
@@ -494,49 +513,70 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         mbar_wait(&full[t % C::STAGES], (uint32_t)((t / C::STAGES) & 1), &no_abort, err,
                   100000000ull);
     }
-  } else if (warp == 1) {
-    // ======================= MMA issuer =======================================
+  } else if (issuer) {
+    // ======================= MMA issuers ======================================
+    // Issuer mw takes the tiles k = mw, mw + MMA_WARPS, ... (disjoint stages
+    // and accumulators); a group's query slot is released once every issuer
+    // has passed the group's last tile (a commit after its own MMAs on it,
+    // else a plain arrival).
+    const int mw = warp == 1 ? 0 : 1;
     if (lane == 0) {
       ItemIter it;
       it.init(prefix, a.groups, it_begin, it_end);
-      int gprev = -1, qcount = 0, stage = 0, abuf = 0, slot = 0, xb = 0;
-      uint32_t phase = 0, aph = 0, xph = 0;
-      while (it.valid()) {
+      int gprev = -1, qcount = 0, stage = 0, abuf = 0, slot = 0;
+      uint32_t phase = 0, aph = 0, qph = 0;
+      bool qwait = false, used = false, any = false;
+      for (int kt = 0; it.valid(); ++kt) {
         const int g = it.g;
         if (g != gprev) {
           slot = qcount & 1;
-          if (!mbar_wait(&q_full[slot], (qcount >> 1) & 1, abort_flag, err)) break;
+          qph = (qcount >> 1) & 1;
           ++qcount;
           gprev = g;
+          qwait = true;
+          used = false;
         }
-        if (C::MX) {
-          if (!mbar_wait(&a_full[xb], xph, abort_flag, err)) break;
-        } else {
-          if (!mbar_wait(&full[stage], phase, abort_flag, err)) break;
+        const bool last_of_group = it.next_group() != g;
+        if (kt % C::MMA_WARPS != mw) {
+          if (last_of_group) {
+            if (used) mma_commit(&q_empty[slot]); else mbar_arrive(&q_empty[slot]);
+          }
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+          if (++abuf == C::ACCS) { abuf = 0; aph ^= 1; }
+          it.next();
+          continue;
         }
+        if (qwait) {
+          if (!mbar_wait(&q_full[slot], qph, abort_flag, err)) break;
+          qwait = false;
+        }
+        if (!mbar_wait(&full[stage], phase, abort_flag, err)) break;
+        // MXFP8: the tile's key scales (and the group's query scales) in TMEM
+        if (C::MX && !mbar_wait(&sf_full[stage], phase, abort_flag, err)) break;
         if (!mbar_wait(&acc_empty[abuf], aph ^ 1, abort_flag, err)) break;
         tc_fence_after();
-        const uint32_t a_base = C::MX ? smem_u32(smem + C::OFF_ABF + xb * C::A_BYTES)
-                                      : smem_u32(smem + C::OFF_A + stage * C::A_BYTES);
+        const uint32_t a_base = smem_u32(smem + C::OFF_A + stage * C::ST_BYTES);
         const uint32_t b_base = smem_u32(smem + C::OFF_B + slot * C::B_BYTES);
         const uint32_t d_tmem = tmem + abuf * C::N;
 #pragma unroll
         for (int k = 0; k < C::KSTEPS; ++k) {
           uint32_t ao, bo;
-          if (FP8) { ao = k * 32; bo = k * 32; }
+          if (C::K8) { ao = k * 32; bo = k * 32; }
           else { ao = (k >> 2) * 16384 + (k & 3) * 32; bo = (k >> 2) * (C::N * 128) + (k & 3) * 32; }
           const uint64_t ad = desc_sw128(a_base + ao);
           const uint64_t bd = desc_sw128(b_base + bo);
-          if (FP8) mma_fp8(d_tmem, ad, bd, C::IDESC, k > 0);
+          if (C::MX)   // K step k = 32-element block k: byte k of every scale word
+            mma_mxf8(d_tmem, ad, bd, C::IDESC | ((uint32_t)k << 4) | ((uint32_t)k << 29),
+                     tmem + C::SFA_COL + stage * 4, tmem + C::SFB_COL + slot * C::SFB_STRIDE,
+                     k > 0);
+          else if (FP8) mma_fp8(d_tmem, ad, bd, C::IDESC, k > 0);
           else mma_bf16(d_tmem, ad, bd, C::IDESC, k > 0);
         }
-        if (C::MX) mma_commit(&a_empty[xb]);
-        else mma_commit(&empty[stage]);
+        mma_commit(&empty[stage]);
         mma_commit(&acc_full[abuf]);
-        if (it.next_group() != g) mma_commit(&q_empty[slot]);
-        if (C::MX) {
-          if (++xb == C::ABUFS) { xb = 0; xph ^= 1; }
-        } else if (++stage == C::STAGES) {
+        used = any = true;
+        if (last_of_group) mma_commit(&q_empty[slot]);
+        if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1;
         }
@@ -544,55 +584,51 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         it.next();
       }
       // all MMAs of this CTA complete before TMEM is released
-      mma_commit(done_bar);
+      if (any) mma_commit(done_bar); else mbar_arrive(done_bar);
       mbar_wait(done_bar, 0, abort_flag, err, 100000000ull);
     }
     __syncwarp();
-  } else if (C::MX && warp >= 2 + C::EPI_WARPS) {
-    // ======================= dequantisation (MXFP8 keys) ======================
-    // E4M3 codes of a landed stage -> bf16 code * 2^X in a swizzled A tile
-    const int dt = tid - (64 + C::EPI_THREADS);
+  } else if (C::MX && warp >= 2 + C::EPI_WARPS) {   // (the warps before PROD_WARP1)
+    // ======================= scale warps (MXFP8 keys) =========================
+    // Warp q of the four (q = its TMEM lane quarter) copies into its lanes,
+    // per query group, the scale words of query rows lane + 32c into column c
+    // of the slot's (every lane quarter holds them all) and, per tile, the
+    // scale word of key row 32q + lane into column q of the stage's four.
+    const int quarter = warp & 3;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int spr = kD >> a.lg_group;
+    constexpr int NBC = C::N / 32;
     ItemIter it;
     it.init(prefix, a.groups, it_begin, it_end);
-    int stage = 0, xb = 0;
-    uint32_t phase = 0, xph = 0;
-    const int lg = a.lg_group;
-    const int spr = kD >> lg;
+    int gprev = -1, qcount = 0, stage = 0;
+    uint32_t phase = 0;
     while (it.valid()) {
+      const int g = it.g;
+      if (g != gprev) {
+        const int slot = qcount & 1;
+        if (!warp_wait(&q_full[slot], (qcount >> 1) & 1, abort_flag, err)) break;
+        const uint32_t* sq = reinterpret_cast<const uint32_t*>(smem + C::OFF_SQ + slot * C::SQ_BYTES);
+        uint32_t r[NBC];
+#pragma unroll
+        for (int cc = 0; cc < NBC; ++cc) r[cc] = sq[lane + 32 * cc];
+        tmem_st_words<NBC>(tmem + lane_base + C::SFB_COL + slot * C::SFB_STRIDE, r);
+        ++qcount;
+        gprev = g;
+      }
       if (!warp_wait(&full[stage], phase, abort_flag, err)) break;
-      if (!warp_wait(&a_empty[xb], xph ^ 1, abort_flag, err)) break;
-      const uint8_t* src = smem + C::OFF_A + stage * C::ST_BYTES;
-      const uint8_t* sc = smem + C::OFF_SC + stage * C::SC_BYTES;
-      uint8_t* dst = smem + C::OFF_ABF + xb * C::A_BYTES;
-#pragma unroll
-      for (int rp = 0; rp < C::DQ_PASSES; ++rp) {
-        const int t = (dt & (kTileM - 1)) + rp * C::DQ_THREADS;
-        const int u0 = C::DQ_THREADS >= kTileM ? (dt >> 7) * C::DQ_UPP : 0;
-        // the row's scale bytes (spr of them, little-endian in one word)
-        const uint8_t* srow = sc + (t >> 6) * C::SC_SUB + (t & (kSub - 1)) * spr;
-        const uint32_t sw = spr == 4   ? *reinterpret_cast<const uint32_t*>(srow)
-                            : spr == 2 ? *reinterpret_cast<const uint16_t*>(srow)
-                                       : *srow;
-#pragma unroll
-        for (int k = 0; k < C::DQ_UPP; ++k) {
-          const int u = u0 + k;
-          const uint4 v = *reinterpret_cast<const uint4*>(src + sw128_offset(t, u));
-          const int X = (int)((sw >> (8 * ((u * 16) >> lg))) & 255u) - 127;
-          uint4 lo, hi;
-          mx_decode16(v, X, lo, hi);
-          uint8_t* blk = dst + (u >> 2) * 16384;
-          *reinterpret_cast<uint4*>(blk + sw128_offset(t, (2 * u) & 7)) = lo;
-          *reinterpret_cast<uint4*>(blk + sw128_offset(t, (2 * u + 1) & 7)) = hi;
-        }
-      }
-      fence_proxy_async_smem();   // the tensor core reads the tile through the async proxy
+      // the key's spr scale bytes, each repeated over the 32-element blocks
+      // of its group
+      const uint8_t* ks = smem + C::OFF_SC + stage * C::SC_BYTES + (quarter * 32 + lane) * spr;
+      uint32_t wd;
+      if (spr == 4) wd = *reinterpret_cast<const uint32_t*>(ks);
+      else if (spr == 2) wd = __byte_perm(*reinterpret_cast<const uint16_t*>(ks), 0u, 0x1100);
+      else wd = *ks * 0x01010101u;
+      tmem_st_words<1>(tmem + lane_base + C::SFA_COL + stage * 4 + quarter, &wd);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&a_full[xb]);
-        mbar_arrive(&empty[stage]);
-      }
+      if (lane == 0) mbar_arrive(&sf_full[stage]);
       if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
-      if (++xb == C::ABUFS) { xb = 0; xph ^= 1; }
       it.next();
     }
   } else {
@@ -687,18 +723,10 @@ cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, 
   using C = Cfg<NT, KK>;
   const uint64_t krows = c.block_table ? (uint64_t)c.num_pages * c.page_size
                                        : (uint64_t)c.batch * c.s_max;
-  CUtensorMap kmap, qmap, smap;
+  CUtensorMap kmap, qmap;
   memset(&qmap, 0, sizeof(qmap));
-  memset(&smap, 0, sizeof(smap));
-  const int spr = c.k_group == 128 ? 1 : c.k_group == 64 ? 2 : 4;   // MXFP8 scale bytes per key
-  if (C::MX) {
-    // the scale array as rows of 16 bytes; one box = one 64-key sub-tile
-    if (!tma_map_2d(&smap, c.k_mx_scale, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, krows * spr / 16, 16,
-                    16, kSub * spr / 16, CU_TENSOR_MAP_SWIZZLE_NONE))
-      return cudaErrorInvalidValue;
-  }
-  // contiguous bf16 / FP8 keys are copied a whole 128-position tile per box
-  const uint32_t box_rows = (C::MX || c.block_table) ? kSub : kTileM;
+  // contiguous keys are copied a whole 128-position tile per box
+  const uint32_t box_rows = c.block_table ? kSub : kTileM;
   if (C::K8) {
     if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, krows, kD, 128, box_rows))
       return cudaErrorInvalidValue;
@@ -730,7 +758,7 @@ cudaError_t go(const bf16* q_idx, const float* w, const CacheView& c, int rows, 
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   cudaError_t le = launch_overlapped(score_tc<NT, KK>, dim3(sms), dim3(C::THREADS), C::SMEM,
-                                     st, kmap, qmap, smap, c, a, err);
+                                     st, kmap, qmap, c, a, err);
   note_launch();
   return le;
 }

@@ -311,6 +311,30 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// Each thread writes NW (1, 2, 4 or 8) consecutive 32-bit columns of its own
+// TMEM lane.
+template <int NW>
+__device__ __forceinline__ void tmem_st_words(uint32_t taddr, const uint32_t* r) {
+  static_assert(NW == 1 || NW == 2 || NW == 4 || NW == 8, "word count");
+  if constexpr (NW == 1) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n" ::"r"(taddr), "r"(r[0])
+                 : "memory");
+  } else if constexpr (NW == 2) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};\n" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1])
+                 : "memory");
+  } else if constexpr (NW == 4) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+  } else {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(
+                     taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                 "r"(r[7])
+                 : "memory");
+  }
+}
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
@@ -331,6 +355,23 @@ __device__ __forceinline__ void mma_fp8(uint32_t d_tmem, uint64_t a_desc, uint64
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Block-scaled E4M3 x E4M3 MMA (MX formats: one E8M0 scale per 32 elements
+// of K for every row of A and of B; one instruction covers K = 32).  The
+// scales are read from TMEM: A row m from lane m, column sfa + m / 32; B row
+// n from column sfb + n / 32 of the lane (n % 32) in the lane quarter of the
+// D row being computed (so B's scales are stored once per lane quarter);
+// byte `id` of each 32-bit word, the ids sitting in the instruction
+// descriptor (bits 4-5 for B, 29-30 for A).
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
 // Same with the A operand in TMEM (M lanes x K/2 columns; column c of lane m
@@ -380,6 +421,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 // ab_format: 1 = bf16 (kind::f16), 0 = e4m3 (kind::f8f6f4).
 __host__ __device__ constexpr uint32_t idesc_f32(uint32_t ab_format, uint32_t M, uint32_t N) {
   return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+// Instruction descriptor of the block-scaled E4M3 MMA (fp32 accumulate, A/B
+// K-major, E8M0 scales: bit 23) with scale byte ids a_id / b_id.
+__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32_t a_id,
+                                                  uint32_t b_id) {
+  return (b_id << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (a_id << 29);
 }
 // Same with B MN-major (bit 16).
 __host__ __device__ constexpr uint32_t idesc_f32_bmn(uint32_t ab_format, uint32_t M, uint32_t N) {
