@@ -74,12 +74,14 @@ struct Cfg {
   // one-byte keys, whose 16 KB tiles arrive twice as often as bf16 tiles)
   static constexpr int PRODUCERS = NT == 1 && K8 ? 2 : 1;
   static constexpr int PROD_WARP1 = 2 + EPI_WARPS + SF_WARPS;   // the extra producer warp
-  // MMA issuers: tile k is issued by issuer k % MMA_WARPS.  One thread's
-  // serial chain per tile (three barrier waits, four or eight MMAs, two or
-  // three commits, the work-list step) takes ~0.7 us, longer than a
-  // single-token decode tile takes to arrive.
+  // MMA issuers: tile k is issued by issuer k % MMA_WARPS.  A thread issuing
+  // tcgen05.mma back to back waits ~120 cycles per instruction whatever N
+  // (64 or 128) and kind (bf16 or E4M3), while two threads issuing at once
+  // reach ~60 cycles per M = 128, N = 64 instruction (measured); a
+  // single-token tile (N = 64) would otherwise be bound by its issuer's chain
+  // of waits, four or eight MMAs and commits.
   static constexpr int MMA_WARPS = NT == 1 ? 2 : 1;
-  static constexpr int MMA_WARP1 = PROD_WARP1 + PRODUCERS - 1;   // the extra MMA warp
+  static constexpr int MMA_WARP1 = PROD_WARP1 + PRODUCERS - 1;   // the extra MMA warps
   static constexpr int THREADS =
       64 + EPI_THREADS + 32 * SF_WARPS + 32 * (PRODUCERS - 1) + 32 * (MMA_WARPS - 1);
   // MXFP8 scale columns in TMEM: per stage four (key row m's word in column
@@ -141,9 +143,11 @@ __device__ __forceinline__ int group_tiles(const CacheView& c, const ScoreArgs& 
   return (int)((group_visible<NT>(c, a, g) + kTileM - 1) / kTileM);
 }
 
-// Walks the CTA's contiguous range of (group, tile) items.
+// Walks the CTA's contiguous range of (group, tile) items.  The current
+// group's tile count is kept in a register, so a step within a group reads
+// no shared memory.
 struct ItemIter {
-  int g, j, left;
+  int g, j, left, gtiles;
   const int* prefix;
   int groups;
   __device__ void init(const int* pre, int G, int64_t begin, int64_t end) {
@@ -161,19 +165,24 @@ struct ItemIter {
     skip_empty();
   }
   __device__ void skip_empty() {
-    while (g < groups && prefix[g] + j >= prefix[g + 1]) { ++g; j = 0; }
+    gtiles = g < groups ? prefix[g + 1] - prefix[g] : 0;
+    while (g < groups && j >= gtiles) {
+      ++g;
+      j = 0;
+      gtiles = g < groups ? prefix[g + 1] - prefix[g] : 0;
+    }
   }
   __device__ bool valid() const { return left > 0; }
   __device__ void next() {
     --left;
-    ++j;
-    skip_empty();
+    if (++j >= gtiles) skip_empty();
   }
   // group of the item after the current one (or -1 when none)
   __device__ int next_group() const {
     if (left <= 1) return -1;
-    int gg = g, jj = j + 1;
-    while (gg < groups && prefix[gg] + jj >= prefix[gg + 1]) { ++gg; jj = 0; }
+    if (j + 1 < gtiles) return g;
+    int gg = g + 1;
+    while (gg < groups && prefix[gg + 1] == prefix[gg]) ++gg;
     return gg;
   }
 };
@@ -254,7 +263,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
   const int64_t it_end = total_items * (blockIdx.x + 1) / gridDim.x;
 
   const bool producer = warp == 0 || (C::PRODUCERS > 1 && warp == C::PROD_WARP1);
-  const bool issuer = warp == 1 || (C::MMA_WARPS > 1 && warp == C::MMA_WARP1);
+  const bool issuer = warp == 1 || (warp >= C::MMA_WARP1 && warp < C::MMA_WARP1 + C::MMA_WARPS - 1);
   if (producer) {
     // ======================= TMA producers ===================================
     // Producer pw issues the tiles k = pw, pw + PRODUCERS, ... of the CTA's
@@ -519,7 +528,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
     // and accumulators); a group's query slot is released once every issuer
     // has passed the group's last tile (a commit after its own MMAs on it,
     // else a plain arrival).
-    const int mw = warp == 1 ? 0 : 1;
+    const int mw = warp == 1 ? 0 : warp - C::MMA_WARP1 + 1;
     if (lane == 0) {
       ItemIter it;
       it.init(prefix, a.groups, it_begin, it_end);
