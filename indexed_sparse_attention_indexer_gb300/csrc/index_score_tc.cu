@@ -548,6 +548,11 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         const bool last_of_group = it.next_group() != g;
         if (kt % C::MMA_WARPS != mw) {
           if (last_of_group) {
+            // an issuer with no tile of the group still waits for its queries
+            // before it arrives, so it cannot run a whole slot cycle ahead
+            // and complete the slot's next phase for the group after
+            if (qwait && !mbar_wait(&q_full[slot], qph, abort_flag, err)) break;
+            qwait = false;
             if (used) mma_commit(&q_empty[slot]); else mbar_arrive(&q_empty[slot]);
           }
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }

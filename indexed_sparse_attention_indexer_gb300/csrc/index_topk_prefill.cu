@@ -45,7 +45,12 @@ constexpr int kMaxRow = kCap * 64 / 2;       // bitmap of a row fits the 32 KB b
 constexpr int EPI_WARPS = 16;                // 8 per token: two sets of 4 taking alternate tiles
 constexpr int TOKT = 256;                    // threads per token (both sets)
 constexpr int EPI_THREADS = EPI_WARPS * 32;
-constexpr int THREADS = 64 + EPI_THREADS;    // 576
+// MMA issuers: warp 1 and the last warp take alternate tiles (a thread
+// issuing tcgen05.mma back to back waits ~120 cycles per instruction; two
+// issuing at once halve the eight-MMA tile's issue time)
+constexpr int kMmaWarps = 2;
+constexpr int kMmaWarp1 = 2 + EPI_WARPS;     // the second issuer
+constexpr int THREADS = 64 + EPI_THREADS + 32 * (kMmaWarps - 1);   // 608
 constexpr int kAccBufs = 4;                  // score accumulators in TMEM
 constexpr int TMEM_COLS = kAccBufs * N;      // 512
 constexpr uint32_t IDESC = idesc_f32(1, kTileM, N);
@@ -288,9 +293,9 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     }
     for (int i = 0; i < kQSlots; ++i) {
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
+      mbar_init(&q_empty[i], kMmaWarps);
     }
-    mbar_init(done_bar, 1);
+    mbar_init(done_bar, kMmaWarps);
     *abort_flag = 0;
     for (int i = 0; i < NT; ++i) reinterpret_cast<TokState*>(smem + OFF_TOK)[i].stop = 0;
     fence_barrier_init();
@@ -370,12 +375,16 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kMmaWarp1) {
     // ======================= MMA issuer ========================================
+    // Issuer mw takes the CTA's tiles kt = mw, mw + 2, ...; both wait for a
+    // group's queries and both release them (a commit after its own MMAs on
+    // them, else a plain arrival).
+    const int mw = warp == 1 ? 0 : 1;
     if (lane == 0) {
-      int stage = 0, abuf = 0, qcount = 0;
+      int stage = 0, abuf = 0, qcount = 0, kt = 0;
       uint32_t ph = 0, aph = 0;
-      bool ok = true;
+      bool ok = true, any = false;
       for (int k = 0; ok && k < nmax; ++k) {
         const int g = zigzag_group(k, blockIdx.x, gridDim.x, a.groups);
         if (g < 0) continue;
@@ -383,7 +392,13 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         if (!(ok = mbar_wait(&q_full[slot], (qcount / kQSlots) & 1, abort_flag, err))) break;
         ++qcount;
         const int ntile = group_tiles(a, g);
-        for (int j = 0; j < ntile; ++j) {
+        bool used = false;
+        for (int j = 0; j < ntile; ++j, ++kt) {
+          if (kt % kMmaWarps != mw) {
+            if (++stage == kStages) { stage = 0; ph ^= 1; }
+            if (++abuf == kAccBufs) { abuf = 0; aph ^= 1; }
+            continue;
+          }
           if (!(ok = mbar_wait(&full[stage], ph, abort_flag, err))) break;
           if (!(ok = mbar_wait(&acc_empty[abuf], aph ^ 1, abort_flag, err))) break;
           tc_fence_after();
@@ -395,12 +410,14 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                      bd + (uint64_t)(((kk >> 2) * (N * 128) + (kk & 3) * 32) >> 4), IDESC, kk > 0);
           mma_commit(&empty[stage]);
           mma_commit(&acc_full[abuf]);
-          if (j == ntile - 1) mma_commit(&q_empty[slot]);
+          used = any = true;
           if (++stage == kStages) { stage = 0; ph ^= 1; }
           if (++abuf == kAccBufs) { abuf = 0; aph ^= 1; }
         }
+        if (!ok) break;
+        if (used) mma_commit(&q_empty[slot]); else mbar_arrive(&q_empty[slot]);
       }
-      mma_commit(done_bar);
+      if (any) mma_commit(done_bar); else mbar_arrive(done_bar);
       mbar_wait(done_bar, 0, abort_flag, err, 100000000ull);
     }
     __syncwarp();

@@ -80,6 +80,11 @@ MX_CASES = {
     "zero_length_g32": ([100, 0, 8], 1, 16, 128, 0, 32),
     "multi_t2_g32": ([300, 64, 132], 2, 64, 128, 0, 32),
     "multi_t4_paged_g64": ([1000, 200], 4, 128, 128, 64, 64),
+    # sequences of one key tile: query slots turn over every tile
+    "one_tile_seqs_g32": ([128, 1, 64, 127, 128, 30, 128, 128, 9, 100, 128, 64, 2, 128, 128, 77],
+                          1, 16, 128, 0, 32),
+    "one_tile_seqs_paged_g64": ([64, 128, 1, 128, 128, 30, 100, 128, 128, 5, 128, 64], 1, 16,
+                                128, 64, 64),
 }
 
 

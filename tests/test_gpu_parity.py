@@ -41,6 +41,14 @@ DECODE_CASES = {
                             {"q_std": 1.0, "scale": 1.0}),
     "k100_h128": (3, [900, 50, 101], 4, 64, 100, 128, 0, False, {}),
     "single_seq_h128_splitk": (1, [5000], 64, 128, 2048, 128, 0, False, {}),
+    # runs of sequences of one key tile (groups of a single tile): the query
+    # slots turn over as fast as the tiles arrive
+    "hi64_many_one_tile_seqs": (24, [1, 128, 77, 64, 3, 128, 90, 129, 100, 5, 128, 60,
+                                     33, 128, 2, 127, 128, 700, 41, 128, 9, 64, 128, 16],
+                                64, 128, 16, 128, 0, False, {}),
+    "hi64_many_one_tile_seqs_paged_fp8": (20, [64, 128, 7, 100, 128, 1, 65, 128, 30, 128,
+                                               300, 12, 128, 128, 99, 2, 128, 64, 50, 128],
+                                          64, 128, 16, 128, 64, True, {}),
 }
 
 
