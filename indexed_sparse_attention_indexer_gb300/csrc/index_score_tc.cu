@@ -80,7 +80,7 @@ struct Cfg {
   // reach ~60 cycles per M = 128, N = 64 instruction (measured); a
   // single-token tile (N = 64) would otherwise be bound by its issuer's chain
   // of waits, four or eight MMAs and commits.
-  static constexpr int MMA_WARPS = NT == 1 ? 2 : 1;
+  static constexpr int MMA_WARPS = NT == 1 || (MX && NT == 2) ? 2 : 1;
   static constexpr int MMA_WARP1 = PROD_WARP1 + PRODUCERS - 1;   // the extra MMA warps
   static constexpr int THREADS =
       64 + EPI_THREADS + 32 * SF_WARPS + 32 * (PRODUCERS - 1) + 32 * (MMA_WARPS - 1);
@@ -90,8 +90,15 @@ struct Cfg {
   static constexpr int SF_COLS = MX ? STAGES * 4 + 2 * SFB_STRIDE : 0;
   // TMEM accumulators: four where they fit (the epilogue of tile i then
   // releases its accumulator four tiles ahead of the MMA that reuses it)
-  static constexpr int ACCS =
-      4 * N + SF_COLS <= 512 ? 4 : (2 * N + SF_COLS <= 512 ? 2 : 1);
+  static constexpr int ACCS_FIT = 4 * N + SF_COLS <= 512   ? 4
+                                 : 3 * N + SF_COLS <= 512 ? 3
+                                 : 2 * N + SF_COLS <= 512 ? 2
+                                                          : 1;
+  // Each issuer must be the one that used a stage or an accumulator last
+  // before it waits on its barrier again (a parity wait cannot tell a phase
+  // from the one two later), so both counts are multiples of the issuers.
+  static constexpr int ACCS = MMA_WARPS == 2 ? ACCS_FIT & ~1 : ACCS_FIT;
+  static_assert(ACCS >= 1 && ACCS % MMA_WARPS == 0 && STAGES % MMA_WARPS == 0, "issuer phases");
   static constexpr int SFA_COL = ACCS * N;
   static constexpr int SFB_COL = SFA_COL + STAGES * 4;
   static constexpr int TMEM_USED = ACCS * N + SF_COLS;
@@ -101,6 +108,7 @@ struct Cfg {
   static constexpr uint32_t IDESC =
       MX ? idesc_mxf8(kTileM, N, 0, 0) : idesc_f32(FP8 ? 0u : 1u, kTileM, N);
   static constexpr int TOK_PER_THREAD = NT == 1 ? 1 : NT / 2;   // epilogue column split
+  static constexpr bool SEQ_TOK = MX && TOK_PER_THREAD > 1;      // epilogue loads a token at a time
   // shared memory carve (offsets from a 1024-aligned base)
   static constexpr int OFF_A = 0;                                   // TMA stages
   static constexpr int OFF_B = OFF_A + STAGES * ST_BYTES;
@@ -679,6 +687,45 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       }
       if (!warp_wait(&acc_full[abuf], aph, abort_flag, err)) break;
       tc_fence_after();
+      const int64_t p = (int64_t)j * kTileM + row;
+      // the weighted ReLU head sum of token tt of this thread's tokens
+      auto store = [&](int tt, const float* vt, float ksc) {
+        const int t = half * TPT + tt;
+        const int r = g * NT + t;
+        if (r >= a.rows || p >= nv[tt]) return;
+        const float* wt = wg + tt * kHeads;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < kHeads; h += 2) {
+          s0 = fmaf(wt[h], fmaxf(vt[h], 0.f), s0);
+          s1 = fmaf(wt[h + 1], fmaxf(vt[h + 1], 0.f), s1);
+        }
+        float sc = s0 + s1;
+        if (FP8) sc *= ksc;
+        a.scores[(int64_t)r * a.ld + p] = sc;
+      };
+      if constexpr (C::SEQ_TOK) {
+        // one token's 64 columns at a time (the scale warps leave 128
+        // registers a thread); the accumulator is released after the last
+        // token's loads
+#pragma unroll
+        for (int tt = 0; tt < TPT; ++tt) {
+          float v[kHeads];
+          const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + abuf * C::N +
+                                 (half * TPT + tt) * kHeads;
+          tmem_ld32(taddr, v);
+          tmem_ld32(taddr + 32, v + 32);
+          tmem_ld_wait();
+          if (tt == TPT - 1) {
+            tc_fence_before();
+            mbar_arrive(&acc_empty[abuf]);
+          }
+          store(tt, v, 1.f);
+        }
+        if (++abuf == C::ACCS) { abuf = 0; aph ^= 1; }
+        it.next();
+        continue;
+      }
       float v[TPT][kHeads];
 #pragma unroll
       for (int tt = 0; tt < TPT; ++tt) {
@@ -691,7 +738,6 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&acc_empty[abuf]);
-      const int64_t p = (int64_t)j * kTileM + row;
       // FP8 keys: this position's scale from the stage the producer filled
       // (acquire its copies through the stage's barrier), then release the
       // stage's scale slot
@@ -704,22 +750,7 @@ score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUten
         if (++kst == C::STAGES) { kst = 0; kph ^= 1; }
       }
 #pragma unroll
-      for (int tt = 0; tt < TPT; ++tt) {
-        const int t = half * TPT + tt;
-        const int r = g * NT + t;
-        if (r >= a.rows) continue;
-        if (p >= nv[tt]) continue;
-        const float* wt = wg + tt * kHeads;
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-        for (int h = 0; h < kHeads; h += 2) {
-          s0 = fmaf(wt[h], fmaxf(v[tt][h], 0.f), s0);
-          s1 = fmaf(wt[h + 1], fmaxf(v[tt][h + 1], 0.f), s1);
-        }
-        float s = s0 + s1;
-        if (FP8) s *= ksc;
-        a.scores[(int64_t)r * a.ld + p] = s;
-      }
+      for (int tt = 0; tt < TPT; ++tt) store(tt, v[tt], ksc);
       if (++abuf == C::ACCS) { abuf = 0; aph ^= 1; }
       it.next();
     }

@@ -49,10 +49,13 @@ constexpr int EPI_THREADS = EPI_WARPS * 32;
 // issuing tcgen05.mma back to back waits ~120 cycles per instruction; two
 // issuing at once halve the eight-MMA tile's issue time)
 constexpr int kMmaWarps = 2;
+
 constexpr int kMmaWarp1 = 2 + EPI_WARPS;     // the second issuer
 constexpr int THREADS = 64 + EPI_THREADS + 32 * (kMmaWarps - 1);   // 608
 constexpr int kAccBufs = 4;                  // score accumulators in TMEM
 constexpr int TMEM_COLS = kAccBufs * N;      // 512
+// an issuer reuses only accumulators it used last (parity waits)
+static_assert(kAccBufs % kMmaWarps == 0, "issuer phases");
 constexpr uint32_t IDESC = idesc_f32(1, kTileM, N);
 
 constexpr int OFF_A = 0;
@@ -395,6 +398,12 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         bool used = false;
         for (int j = 0; j < ntile; ++j, ++kt) {
           if (kt % kMmaWarps != mw) {
+            // the other issuer's tile: wait for its keys all the same.  With
+            // an odd stage count the stages alternate between the issuers, and
+            // a parity wait on a stage cannot tell its next phase from the one
+            // after; having seen every phase in order, an issuer is never two
+            // phases ahead of a stage.
+            if (!(ok = mbar_wait(&full[stage], ph, abort_flag, err))) break;
             if (++stage == kStages) { stage = 0; ph ^= 1; }
             if (++abuf == kAccBufs) { abuf = 0; aph ^= 1; }
             continue;
