@@ -13,14 +13,14 @@
 //   CTA 0: logits over key dims   0..319, output dims   0..255
 //   CTA 1: logits over key dims 320..575, output dims 256..511
 // Each CTA gathers only the 320 dims of every selected row that it needs,
-// keeps its half of the output accumulator in TMEM (256 columns), two logit
-// tiles (2 x 64 columns) and four 64-dim blocks of its query slice (128
-// columns; CTA 0's fifth block sits in shared memory as an MMA A operand).
+// keeps its half of the output accumulator in TMEM (256 columns), one logit
+// tile (64 columns) and its query slice (four 64-dim blocks, 128 columns; CTA
+// 0's fifth block in 32 more).
 // The two partial logit tiles (128 heads x 64 positions, fp32) are swapped
 // through distributed shared memory, so both CTAs hold the same logits and
 // take the same softmax decisions.  Per 64-position tile, 12 warps:
 //   producers (warps 0-2): the tile's rows into a 128-byte-swizzled stage
-//     (ring of 3), by TMA gather4 (four rows per instruction) and cp.async at
+//     (ring of 4), by TMA gather4 (four rows per instruction) and cp.async at
 //     once, so both copy engines work; the cp.async threads arrive on the
 //     stage's barrier when their copies land, without waiting for them;
 //   MMA (warp 3, one thread): S = Qslice . C^T into the free logit tile,
@@ -47,9 +47,13 @@ namespace {
 constexpr int kH = 128;                        // heads (MMA M)
 constexpr int kNp = 64;                        // positions per tile (MMA N of the logits)
 constexpr int kChunks = 5;                     // 64-dim blocks each CTA gathers per row
-constexpr int kStages = 3;
+// Four stages: the logit tile and the P tile are single (their next use waits
+// only for the readers of the previous one), and CTA 0's fifth query block
+// sits in the TMEM columns the second logit tile would take, which leaves the
+// shared memory for a fourth 40 KB stage of gathered rows.
+constexpr int kStages = 4;
 constexpr int kXBufs = 1;                      // exchange buffers for the peer's partial logits
-constexpr int kQkTmem = 4;                     // query blocks held in TMEM (CTA 0's fifth is in shared memory)
+constexpr int kQkTmem = 4;                     // query blocks of the main logit MMAs (CTA 0's fifth apart)
 constexpr int kChunkBytes = kNp * 128;         // one 64-dim block of a tile: 8 KB
 constexpr int kStageBytes = kChunks * kChunkBytes;
 // 12 warps (three per SM sub-partition): at most 168 registers a thread
@@ -70,16 +74,17 @@ constexpr int kLdgThreads = kLdgWarps * 32;
 constexpr int kMaxEntries = DSI_MAX_K;         // index entries one split can hold
 
 constexpr int OFF_C = 0;
-constexpr int OFF_P = OFF_C + kStages * kStageBytes;      // two P tiles [128 x 64] bf16, 16 KB each
-constexpr int OFF_X = OFF_P + 2 * kH * kNp * 2;           // kXBufs x peer logits [128 x 64] fp32
-constexpr int OFF_Q4 = OFF_X + kXBufs * kH * kNp * 4;     // CTA 0's fifth query block [128 x 64] bf16, swizzled
-constexpr int OFF_ROWS = OFF_Q4 + kH * 64 * 2;            // physical row of each entry (or -1)
+constexpr int OFF_P = OFF_C + kStages * kStageBytes;      // the P tile [128 x 64] bf16, 16 KB
+constexpr int OFF_X = OFF_P + kH * kNp * 2;               // kXBufs x peer logits [128 x 64] fp32
+constexpr int OFF_ROWS = OFF_X + kXBufs * kH * kNp * 4;   // physical row of each entry (or -1)
 constexpr int OFF_BAR = OFF_ROWS + kMaxEntries * 4;
 constexpr int NBARS = 2 * kStages + 12 + 2 * kXBufs;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM = OFF_MISC + 64 + 1024;
+static_assert(SMEM <= 227 * 1024, "shared memory");
 
-constexpr uint32_t TM_S = 0;      // logits, two buffers of 64 columns
+constexpr uint32_t TM_S = 0;      // logits, 64 columns
+constexpr uint32_t TM_Q4 = 64;    // CTA 0's fifth query block, 32 columns
 constexpr uint32_t TM_Q = 128;    // query slice: four 64-dim blocks, 128 columns
 constexpr uint32_t TM_O = 256;    // output half, 256 columns
 constexpr uint32_t TMEM_COLS = 512;
@@ -394,44 +399,42 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
       uint32_t idle = 0;
       while (ok && pv_next < n_tiles) {
         bool progress = false;
-        if (pv_next < qk_next && mbar_test_wait(&p_full[pv_next & 1], (pv_next >> 1) & 1)) {
+        if (pv_next < qk_next && mbar_test_wait(&p_full[0], pv_next & 1)) {
           tc_fence_after();
           const int st = pv_next % kStages;
-          const uint64_t pd = desc_sw128(pbase + (pv_next & 1) * (kH * kNp * 2));
+          const uint64_t pd = desc_sw128(pbase);
           const uint64_t vd = desc_sw128_mn(smem_u32(smem + OFF_C + st * kStageBytes), kChunkBytes);
 #pragma unroll
           for (int kk = 0; kk < kNp / 16; ++kk)
             mma_bf16(tmem + TM_O, pd + (uint64_t)((kk * 32) >> 4), vd + (uint64_t)((kk * 2048) >> 4),
                      IDESC_O, (pv_next > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&p_empty[pv_next & 1]);
+          mma_commit(&p_empty[0]);
           mma_commit(&empty[st]);
           ++pv_next;
           progress = true;
         }
         if (qk_next < n_tiles) {
           const int st = qk_next % kStages;
-          const int sb = qk_next & 1;
           if (mbar_test_wait(&full[st], (qk_next / kStages) & 1) &&
-              mbar_test_wait(&s_empty[sb], ((qk_next >> 1) & 1) ^ 1)) {
+              mbar_test_wait(&s_empty[0], (qk_next & 1) ^ 1)) {
             tc_fence_after();
             // the stage's cp.async part was written through the generic proxy
             fence_proxy_async_smem();
-            const uint32_t t_s = tmem + TM_S + sb * kNp;
+            const uint32_t t_s = tmem + TM_S;
             const uint32_t st_base = smem_u32(smem + OFF_C + st * kStageBytes);
             const uint64_t d0 = desc_sw128(st_base + qk_first * kChunkBytes);
             for (int k = 0; k < kQkTmem * 4; ++k)
               mma_bf16_tmem_a(t_s, tmem + TM_Q + k * 8,
                               d0 + (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4),
                               IDESC_S, k > 0 ? 1u : 0u);
-            if (rho == 0) {      // fifth block: queries from shared memory
-              const uint64_t qd = desc_sw128(smem_u32(smem + OFF_Q4));
+            if (rho == 0) {      // fifth block, its queries in TMEM too
               const uint64_t cd = desc_sw128(st_base + kQkTmem * kChunkBytes);
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_bf16(t_s, qd + (uint64_t)((k * 32) >> 4), cd + (uint64_t)((k * 32) >> 4),
-                         IDESC_S, 1u);
+                mma_bf16_tmem_a(t_s, tmem + TM_Q4 + k * 8, cd + (uint64_t)((k * 32) >> 4),
+                                IDESC_S, 1u);
             }
-            mma_commit(&s_full[sb]);
+            mma_commit(&s_full[0]);
             ++qk_next;
             progress = true;
           }
@@ -480,15 +483,15 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
     const uint32_t xfull_remote = map_to_rank(smem_u32(x_full), peer);
     bool ok = true;
     for (int t = 0; ok && t < n_tiles; ++t) {
-      const int sb = t & 1, bsel = t % kXBufs;
+      const int bsel = t % kXBufs;
       float v[kNp];
-      if (!(ok = warp_wait(&s_full[sb], (t >> 1) & 1, abort_flag, err))) break;
+      if (!(ok = warp_wait(&s_full[0], t & 1, abort_flag, err))) break;
       tc_fence_after();
-      tmem_ld32(tmem + lane_base + TM_S + sb * kNp, v);
-      tmem_ld32(tmem + lane_base + TM_S + sb * kNp + 32, v + 32);
+      tmem_ld32(tmem + lane_base + TM_S, v);
+      tmem_ld32(tmem + lane_base + TM_S + 32, v + 32);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&s_empty[sb]);
+      mbar_arrive(&s_empty[0]);
       // this CTA's partial to the peer, once the peer has read the buffer
       if (!(ok = warp_wait_cluster(&x_empty[bsel], ((t / kXBufs) & 1) ^ 1, abort_flag, err))) break;
       const uint32_t dst = x_remote + bsel * kXBytes;
@@ -503,8 +506,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;               // head = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    // query blocks 2-3 into TMEM; CTA 0's fifth block into shared memory (the
-    // A operand of its last four logit MMAs)
+    // query blocks 2-3 into TMEM, and CTA 0's fifth block
     {
 #pragma unroll
       for (int ch = 2; ch < kQkTmem; ++ch) {
@@ -517,10 +519,13 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
         tmem_st32(tmem + lane_base + TM_Q + ch * 32, w32);
       }
       if (rho == 0) {
+        uint32_t w32[32];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(smem + OFF_Q4 + sw128_offset(h, u)) = qv[8 * (kQkTmem - 2) + u];
-        fence_proxy_async_smem();
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = qv[8 * (kQkTmem - 2) + i];
+          w32[4 * i] = v.x; w32[4 * i + 1] = v.y; w32[4 * i + 2] = v.z; w32[4 * i + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_base + TM_Q4, w32);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -533,17 +538,16 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
     float m_ref = -INFINITY, l_sum = 0.f;
     bool ok = true;
     for (int t = 0; ok && t < n_tiles; ++t) {
-      // summed logits of tile t (frees the TMEM tile for the logits of t+2)
-      const int sb = t & 1;
+      // summed logits of tile t (frees the TMEM tile for the logits of t+1)
       float vc[kNp];
       const int bsel = t % kXBufs;
-      if (!(ok = warp_wait(&s_full[sb], (t >> 1) & 1, abort_flag, err))) break;
+      if (!(ok = warp_wait(&s_full[0], t & 1, abort_flag, err))) break;
       tc_fence_after();
-      tmem_ld32(tmem + lane_base + TM_S + sb * kNp, vc);
-      tmem_ld32(tmem + lane_base + TM_S + sb * kNp + 32, vc + 32);
+      tmem_ld32(tmem + lane_base + TM_S, vc);
+      tmem_ld32(tmem + lane_base + TM_S + 32, vc + 32);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&s_empty[sb]);
+      mbar_arrive(&s_empty[0]);
       // the peer's partial logits of the same tile, summed here
       if (!(ok = warp_wait_cluster(&x_full[bsel], (t / kXBufs) & 1, abort_flag, err))) break;
 #pragma unroll
@@ -588,17 +592,14 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
         m_ref = tmax;
         rescale = true;
       }
-      // P tile t&1 is free once PV(t-2) is done
-      if (!(ok = warp_wait(&p_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag, err))) break;
+      // the P tile is free, and PV(t-1) has landed in the accumulator, once
+      // PV(t-1) is done
+      if (!(ok = warp_wait(&p_empty[0], (t & 1) ^ 1, abort_flag, err))) break;
       tc_fence_after();
-      uint8_t* prow = pbuf + (t & 1) * (kH * kNp * 2);
+      uint8_t* prow = pbuf;
       // TMEM loads/stores are warp-collective: rescale when any head of the
-      // warp needs it (the others multiply by 1), once PV(t-1) has landed in
-      // the accumulator
+      // warp needs it (the others multiply by 1)
       if (__any_sync(0xffffffffu, rescale)) {
-        if (t > 0 && !(ok = warp_wait(&p_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, err)))
-          break;
-        tc_fence_after();
         for (int c0 = 0; c0 < 256; c0 += 32) {
           float o[32];
           tmem_ld32(tmem + lane_base + TM_O + c0, o);
@@ -638,7 +639,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
       l_sum = l_sum * alpha + psum;     // alpha == 1 for heads that did not move their reference
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[t & 1]);
+      mbar_arrive(&p_full[0]);
     }
     // ---- epilogue: normalise and store this CTA's 256 output dims ------------
     if (ok && warp_wait(o_done, 0, abort_flag, err)) {
