@@ -10,12 +10,13 @@
 // One (query row, K split) is a cluster of two CTAs.  With all 128 heads as
 // the MMA M dimension, the fp32 output of one row (128 x 512) alone fills a
 // CTA's tensor memory, so the work is split by dimension:
-//   CTA 0: logits over key dims   0..319, output dims   0..255
-//   CTA 1: logits over key dims 320..575, output dims 256..511
+//   CTA 0: logits over key dims   0..287, output dims   0..255, gathers dims   0..319
+//   CTA 1: logits over key dims 288..575, output dims 256..511, gathers dims 256..575
 // Each CTA gathers only the 320 dims of every selected row that it needs,
 // keeps its half of the output accumulator in TMEM (256 columns), one logit
-// tile (64 columns) and its query slice (four 64-dim blocks, 128 columns; CTA
-// 0's fifth block in 32 more).
+// tile (64 columns) and its query slice (four 64-dim blocks, 128 columns,
+// and the block of dims 256..319, which the CTAs split, in 32 more): 18
+// logit MMAs a tile on each CTA.
 // The two partial logit tiles (128 heads x 64 positions, fp32) are swapped
 // through distributed shared memory, so both CTAs hold the same logits and
 // take the same softmax decisions.  Per 64-position tile, 12 warps:
@@ -48,12 +49,12 @@ constexpr int kH = 128;                        // heads (MMA M)
 constexpr int kNp = 64;                        // positions per tile (MMA N of the logits)
 constexpr int kChunks = 5;                     // 64-dim blocks each CTA gathers per row
 // Four stages: the logit tile and the P tile are single (their next use waits
-// only for the readers of the previous one), and CTA 0's fifth query block
-// sits in the TMEM columns the second logit tile would take, which leaves the
-// shared memory for a fourth 40 KB stage of gathered rows.
+// only for the readers of the previous one), and the query block of dims
+// 256..319 sits in the TMEM columns the second logit tile would take, which
+// leaves the shared memory for a fourth 40 KB stage of gathered rows.
 constexpr int kStages = 4;
 constexpr int kXBufs = 1;                      // exchange buffers for the peer's partial logits
-constexpr int kQkTmem = 4;                     // query blocks of the main logit MMAs (CTA 0's fifth apart)
+constexpr int kQkTmem = 4;                     // query blocks of the main logit MMAs (dims 256..319 apart)
 constexpr int kChunkBytes = kNp * 128;         // one 64-dim block of a tile: 8 KB
 constexpr int kStageBytes = kChunks * kChunkBytes;
 // 12 warps (three per SM sub-partition): at most 168 registers a thread
@@ -84,7 +85,7 @@ constexpr int SMEM = OFF_MISC + 64 + 1024;
 static_assert(SMEM <= 227 * 1024, "shared memory");
 
 constexpr uint32_t TM_S = 0;      // logits, 64 columns
-constexpr uint32_t TM_Q4 = 64;    // CTA 0's fifth query block, 32 columns
+constexpr uint32_t TM_Q4 = 64;    // query dims 256..319, 32 columns
 constexpr uint32_t TM_Q = 128;    // query slice: four 64-dim blocks, 128 columns
 constexpr uint32_t TM_O = 256;    // output half, 256 columns
 constexpr uint32_t TMEM_COLS = 512;
@@ -183,16 +184,18 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
   const int qk_first = rho ? 1 : 0;                // first stage block used by the logits
   // this CTA's slice of the head's query row is loaded first, so it lands
   // while the entries are being staged (and, launched behind the select
-  // kernel, while that kernel finishes): the exchange warps take its first two
-  // 64-dim blocks, the softmax warps the rest (two, or three on CTA 0)
+  // kernel, while that kernel finishes): the exchange warps take the first two
+  // of its four main blocks, the softmax warps the other two and the block of
+  // dims 256..319 (eight 16-byte pieces a block)
   uint4 qv[24];
   if (warp >= kExWarp0) {
-    const int c_lo = warp < kSmWarp0 ? 0 : 2;
-    const int nq = (warp < kSmWarp0 ? 2 : kChunks - qk_first - 2) * 8;
-    const uint4* qsrc = reinterpret_cast<const uint4*>(
-        a.q + ((int64_t)r * kH + (warp & 3) * 32 + lane) * DSI_D_QK + (g0 + qk_first + c_lo) * 64);
+    const int b0 = g0 + qk_first + (warp < kSmWarp0 ? 0 : 2);
+    const int nq = (warp < kSmWarp0 ? 2 : 3) * 8;
+    const uint4* qrow = reinterpret_cast<const uint4*>(
+        a.q + ((int64_t)r * kH + (warp & 3) * 32 + lane) * DSI_D_QK);
 #pragma unroll
-    for (int i = 0; i < 24; ++i) qv[i] = i < nq ? __ldg(qsrc + i) : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 24; ++i)
+      qv[i] = i < nq ? __ldg(qrow + (i < 16 ? b0 * 8 + i : 4 * 8 + (i - 16))) : make_uint4(0, 0, 0, 0);
   }
 
   if (tid == 0) {
@@ -427,12 +430,15 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
               mma_bf16_tmem_a(t_s, tmem + TM_Q + k * 8,
                               d0 + (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4),
                               IDESC_S, k > 0 ? 1u : 0u);
-            if (rho == 0) {      // fifth block, its queries in TMEM too
-              const uint64_t cd = desc_sw128(st_base + kQkTmem * kChunkBytes);
+            {   // dims 256..319: CTA 0 takes the first half (its stage block
+                // 4), CTA 1 the second (its block 0)
+              const uint64_t cd = desc_sw128(st_base + (rho ? 0 : kQkTmem) * kChunkBytes);
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_bf16_tmem_a(t_s, tmem + TM_Q4 + k * 8, cd + (uint64_t)((k * 32) >> 4),
+              for (int k = 0; k < 2; ++k) {
+                const int kk = (int)rho * 2 + k;
+                mma_bf16_tmem_a(t_s, tmem + TM_Q4 + kk * 8, cd + (uint64_t)((kk * 32) >> 4),
                                 IDESC_S, 1u);
+              }
             }
             mma_commit(&s_full[0]);
             ++qk_next;
@@ -506,7 +512,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;               // head = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    // query blocks 2-3 into TMEM, and CTA 0's fifth block
+    // query blocks 2-3 and dims 256..319 into TMEM
     {
 #pragma unroll
       for (int ch = 2; ch < kQkTmem; ++ch) {
@@ -518,7 +524,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
         }
         tmem_st32(tmem + lane_base + TM_Q + ch * 32, w32);
       }
-      if (rho == 0) {
+      {
         uint32_t w32[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
