@@ -85,6 +85,9 @@ MX_CASES = {
                           1, 16, 128, 0, 32),
     "one_tile_seqs_paged_g64": ([64, 128, 1, 128, 128, 30, 100, 128, 128, 5, 128, 64], 1, 16,
                                 128, 64, 64),
+    # candidate pairs (two issuers on alternate tiles, two accumulators) over
+    # paged keys, with sequences of one tile among longer ones
+    "multi_t2_paged_g32_one_tile_seqs": ([700, 128, 64, 129, 3, 128, 1000, 66], 2, 64, 128, 64, 32),
 }
 
 

@@ -245,6 +245,10 @@ MULTI_CASES = {
     "paged_fp8_t4": ([1000, 200], 4, 64, 128, 128, 128, 64, True),
     "small_heads_t3": ([50, 7, 90], 3, 4, 64, 16, 16, 0, False),
     "shorter_than_t": ([1, 40], 2, 64, 128, 8, 128, 0, False),   # candidate 0 of seq 0 sees nothing
+    # sequences of one key tile among longer ones: the query slots turn over
+    # at every tile for the groups of four candidates
+    "one_tile_seqs_t4_paged_fp8": ([128, 64, 700, 2, 128, 129, 30, 128], 4, 64, 128, 32, 128, 64,
+                                   True),
 }
 
 
