@@ -166,6 +166,37 @@ __device__ __forceinline__ void load_chunk(uint32_t* key, const float* grow, int
   }
 }
 
+// The chosen bin [lo, hi] holds at most kRankMax of the CTA's keys: they are
+// collected and ranked against each other (each lane counts the keys above
+// and equal to its own), which gives T and the number of keys equal to T to
+// take, without the passes that would narrow the bin to one value.  On return
+// lo == hi == T and krem counts the keys equal to T to keep.
+constexpr int kRankMax = 32;
+template <int N>
+__device__ __forceinline__ void rank_bin(const uint32_t (&key)[N], uint32_t& lo, uint32_t& hi,
+                                         int& krem, uint32_t* cand, int* nc, uint32_t* sel,
+                                         int tid, int lane, int wid) {
+  const uint32_t span = hi - lo;
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (key[i] - lo <= span) cand[atomicAdd(nc, 1)] = key[i];
+  __syncthreads();
+  if (wid == 0) {
+    const int m = *nc;
+    const uint32_t kv = lane < m ? cand[lane] : 0u;
+    int g = 0, e = 0;
+    for (int j = 0; j < m; ++j) {
+      const uint32_t c = cand[j];
+      g += c > kv;
+      e += c == kv;
+    }
+    if (lane < m && g < krem && krem <= g + e) { sel[0] = kv; sel[1] = (uint32_t)g; }
+  }
+  __syncthreads();
+  lo = hi = sel[0];
+  krem -= (int)sel[1];
+}
+
 template <bool kChunked>
 __global__ void __launch_bounds__(kTopkThreads, 1)
 topk_rows_reg(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
@@ -174,7 +205,9 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
   __shared__ int hist[2][kBins];          // alternate passes; each is cleared as it is read
   __shared__ int wsum[2][kWarps];
   __shared__ int wbase[2][kWarps];
-  __shared__ uint32_t s_sel[2];
+  __shared__ uint32_t s_sel[3];
+  __shared__ uint32_t s_cand[kRankMax];
+  __shared__ int s_nc;
   // the scores come from the previous kernel; the attention kernel after this
   // one may start its set-up now
   grid_dep_wait();
@@ -208,6 +241,7 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
   uint32_t key[kRegPer];
   if (resident) load_chunk(key, grow, n, 0, wpos, lane);
   for (int i = tid; i < 2 * kBins; i += blockDim.x) (&hist[0][0])[i] = 0;
+  if (tid == 0) s_nc = 0;
   // ---- the row's key range ------------------------------------------------
   {
     uint32_t kmax = 0u, kmin = 0xffffffffu;
@@ -274,8 +308,11 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
     const int above_w = __shfl_sync(kAll, wincl - wt, wid);
     const int above = above_w + incl - (c0 + c1);       // keys in the bins above this pair
     if (above < krem && above + c0 + c1 >= krem) {
-      if (above + c0 >= krem) { s_sel[0] = (uint32_t)b0; s_sel[1] = (uint32_t)above; }
-      else { s_sel[0] = (uint32_t)(b0 - 1); s_sel[1] = (uint32_t)(above + c0); }
+      if (above + c0 >= krem) {
+        s_sel[0] = (uint32_t)b0; s_sel[1] = (uint32_t)above; s_sel[2] = (uint32_t)c0;
+      } else {
+        s_sel[0] = (uint32_t)(b0 - 1); s_sel[1] = (uint32_t)(above + c0); s_sel[2] = (uint32_t)c1;
+      }
     }
     __syncthreads();
     const uint32_t b = s_sel[0];
@@ -285,6 +322,10 @@ topk_rows_reg(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
     hi = top < (uint64_t)hi ? (uint32_t)top : hi;
     ++pass;
     if (sh == 0) break;
+    if (resident && s_sel[2] <= (uint32_t)kRankMax) {
+      rank_bin(key, lo, hi, krem, s_cand, &s_nc, s_sel, tid, lane, wid);
+      break;
+    }
   }
   const uint32_t T = lo;
   // ---- ordered compaction, chunk by chunk -------------------------------------
@@ -391,8 +432,10 @@ topk_rows_cl(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
   __shared__ __align__(16) int hist[2][kBins];   // alternate passes (the peers read both)
   __shared__ int wsum[2][kWarps];
   __shared__ int wbase[2][kWarps];
-  __shared__ uint32_t s_sel[2];
+  __shared__ uint32_t s_sel[3];
   __shared__ uint32_t s_range[2];         // this CTA's smallest and largest key (peers read them)
+  __shared__ uint32_t s_cand[kRankMax];
+  __shared__ int s_nc;
   __shared__ int s_cnt[2];                // this CTA's keys above T and equal to T (peers read them)
   grid_dep_wait();
   grid_dep_launch();
@@ -430,6 +473,7 @@ topk_rows_cl(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
     key[i] = (i < kpt && p < n) ? max(score_key(__ldg(grow + p)), 1u) : 0u;
   }
   for (int i = tid; i < 2 * kBins; i += blockDim.x) (&hist[0][0])[i] = 0;
+  if (tid == 0) s_nc = 0;
   {
     uint32_t kmax = 0u, kmin = 0xffffffffu;
 #pragma unroll
@@ -514,8 +558,11 @@ topk_rows_cl(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
     const int above_w = __shfl_sync(kAll, wincl - wt, wid);
     const int above = above_w + incl - (c0 + c1);
     if (above < krem && above + c0 + c1 >= krem) {
-      if (above + c0 >= krem) { s_sel[0] = (uint32_t)b0; s_sel[1] = (uint32_t)above; }
-      else { s_sel[0] = (uint32_t)(b0 - 1); s_sel[1] = (uint32_t)(above + c0); }
+      if (above + c0 >= krem) {
+        s_sel[0] = (uint32_t)b0; s_sel[1] = (uint32_t)above; s_sel[2] = (uint32_t)c0;
+      } else {
+        s_sel[0] = (uint32_t)(b0 - 1); s_sel[1] = (uint32_t)(above + c0); s_sel[2] = (uint32_t)c1;
+      }
     }
     __syncthreads();
     const uint32_t b = s_sel[0];
@@ -525,6 +572,11 @@ topk_rows_cl(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
     hi = top < (uint64_t)hi ? (uint32_t)top : hi;
     ++pass;
     if (sh == 0) break;
+    // a row on one CTA whose chosen bin holds few keys: rank them directly
+    if (!coop && s_sel[2] <= (uint32_t)kRankMax) {
+      rank_bin(key, lo, hi, krem, s_cand, &s_nc, s_sel, tid, lane, wid);
+      break;
+    }
   }
   const uint32_t T = lo;
   // ---- ordered compaction: this run's offsets follow runs 0 .. q-1 -----------
