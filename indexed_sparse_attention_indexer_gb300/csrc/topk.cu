@@ -172,6 +172,7 @@ __device__ __forceinline__ void load_chunk(uint32_t* key, const float* grow, int
 // take, without the passes that would narrow the bin to one value.  On return
 // lo == hi == T and krem counts the keys equal to T to keep.
 constexpr int kRankMax = 32;
+constexpr int kPackRows = kTopkThreads;   // rows a packed cluster launch can order
 template <int N>
 __device__ __forceinline__ void rank_bin(const uint32_t (&key)[N], uint32_t& lo, uint32_t& hi,
                                          int& krem, uint32_t* cand, int* nc, uint32_t* sel,
@@ -458,11 +459,11 @@ __device__ __forceinline__ void rank_bin_cluster(const uint32_t (&key)[N], uint3
   krem -= (int)sel[1];
 }
 
-template <int CL, int KPT>
+template <int CL, int KPT, bool PACK>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kTopkThreads, 1)
 topk_rows_cl(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
              const int32_t* __restrict__ row_len, int64_t q_offset, int K,
-             int32_t* __restrict__ idx, int32_t* __restrict__ count, int tps) {
+             int32_t* __restrict__ idx, int32_t* __restrict__ count, int tps, int rows) {
   __shared__ __align__(16) int hist[2][kBins];   // alternate passes (the peers read both)
   __shared__ int wsum[2][kWarps];
   __shared__ int wbase[2][kWarps];
@@ -471,31 +472,68 @@ topk_rows_cl(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
   __shared__ uint32_t s_cand[kRankMax];
   __shared__ int s_nc;
   __shared__ int s_cnt[2];                // this CTA's keys above T and equal to T (peers read them)
+  __shared__ int s_rows[PACK ? kPackRows : 1];   // PACK: the long rows in row order, then the others
+  __shared__ int s_wl[kWarps];
   grid_dep_wait();
   grid_dep_launch();
-  const int q = (int)tc::cluster_ctarank();
-  const int r = blockIdx.x / CL;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const unsigned kAll = 0xffffffffu;
   const unsigned lt_mask = (1u << lane) - 1u;
-  int64_t n = !row_len ? q_offset + r + 1
-              : tps == 1 ? (int64_t)row_len[r]
-                         : (int64_t)row_len[r / tps] - (tps - 1 - r % tps);
-  if (n < 0) n = 0;
-  if (n > n_cap) n = n_cap;
+  const int qc = (int)tc::cluster_ctarank();
+  auto row_n = [&](int rr) {
+    int64_t v = !row_len ? q_offset + rr + 1
+                : tps == 1 ? (int64_t)row_len[rr]
+                           : (int64_t)row_len[rr / tps] - (tps - 1 - rr % tps);
+    if (v < 0) v = 0;
+    return v > n_cap ? n_cap : v;   // the scorer's visible length never exceeds it
+  };
+  // row of this cluster.  PACK: rows longer than one CTA's registers take a
+  // cluster each (first, in row order), the others one CTA each, CL to a
+  // cluster, so short rows do not hold the SMs of a whole cluster (every CTA
+  // derives the same order from the row lengths)
+  int r = blockIdx.x / CL;
+  bool solo = false;                      // this CTA takes a row of its own
+  if constexpr (PACK) {
+    const bool lng = tid < rows && row_n(tid) > (int64_t)KPT * kTopkThreads;
+    const unsigned bl = __ballot_sync(kAll, lng);
+    if (lane == 0) s_wl[wid] = __popc(bl);
+    __syncthreads();
+    int lb = 0, nlong = 0;
+    for (int w2 = 0; w2 < kWarps; ++w2) {
+      lb += w2 < wid ? s_wl[w2] : 0;
+      nlong += s_wl[w2];
+    }
+    if (tid < rows) {
+      const int lp = lb + __popc(bl & lt_mask);
+      s_rows[lng ? lp : nlong + tid - lp] = tid;
+    }
+    __syncthreads();
+    const int cl = blockIdx.x / CL;
+    if (cl >= nlong) {
+      const int si = nlong + (cl - nlong) * CL + qc;
+      if (si >= rows) return;
+      r = s_rows[si];
+      solo = true;
+    } else {
+      r = s_rows[cl];
+    }
+  }
+  const int q = solo ? 0 : qc;            // this CTA's run of the row
+  const int64_t n = row_n(r);
   int32_t* out = idx + (int64_t)r * K;
   const float* grow = scores + (int64_t)r * ld;
   if (n <= K) {  // every candidate is kept (the same decision in every CTA of the cluster)
-    for (int64_t j = q * kTopkThreads + tid; j < K; j += CL * kTopkThreads)
+    const int ncta = solo ? 1 : CL;
+    for (int64_t j = q * kTopkThreads + tid; j < K; j += ncta * kTopkThreads)
       out[j] = j < n ? (int32_t)j : -1;
     if (count && q == 0 && tid == 0) count[r] = (int32_t)n;
     return;
   }
   // ---- this CTA's run of the row: kpt keys a thread --------------------------
-  // coop: the CL CTAs share the row; otherwise CTA 0 takes it alone (a
+  // coop: the CL CTAs share the row; otherwise one CTA takes it alone (a
   // decision every CTA of the cluster makes the same way)
-  const bool coop = n > (int64_t)KPT * kTopkThreads;
-  if (!coop && q != 0) return;
+  const bool coop = !solo && n > (int64_t)KPT * kTopkThreads;
+  if (!coop && !solo && q != 0) return;
   const int parts = coop ? CL : 1;
   const int kpt = (int)((n + parts * kTopkThreads - 1) / (parts * kTopkThreads));   // <= KPT
   const int64_t run0 = (int64_t)q * kpt * kTopkThreads;
@@ -530,8 +568,12 @@ topk_rows_cl(const float* __restrict__ scores, int64_t ld, int64_t n_cap,
   if (wid == 0) {
     uint32_t kmin = 0xffffffffu, kmax = 0u;
     if (lane < parts) {
-      kmin = (uint32_t)ld_peer_s32(&s_range[0], lane);
-      kmax = (uint32_t)ld_peer_s32(&s_range[1], lane);
+      // the cluster's runs, or (a CTA alone on its row) this CTA's own range:
+      // a CTA alone never reads another CTA's shared memory, which may belong
+      // to another row or be gone
+      const uint32_t rk = coop ? (uint32_t)lane : (uint32_t)qc;
+      kmin = (uint32_t)ld_peer_s32(&s_range[0], rk);
+      kmax = (uint32_t)ld_peer_s32(&s_range[1], rk);
     }
     kmin = __reduce_min_sync(kAll, kmin);
     kmax = __reduce_max_sync(kAll, kmax);
@@ -701,15 +743,17 @@ cudaError_t launch_topk(const float* scores, int64_t ld, int rows, const int32_t
     if (longest <= kRegKeysMax) {
       // rows of one chunk: two CTAs a row while that still fits in one wave
       e = 2L * rows <= sms
-              ? launch_overlapped(topk_rows_cl<2, kRegPer / 2>, dim3(2 * rows), dim3(kTopkThreads),
-                                  0, st, scores, ld, n_cap, row_len, q_offset, K, idx, count, tps)
+              ? launch_overlapped(topk_rows_cl<2, kRegPer / 2, false>, dim3(2 * rows),
+                                  dim3(kTopkThreads), 0, st, scores, ld, n_cap, row_len, q_offset,
+                                  K, idx, count, tps, rows)
               : launch_overlapped(topk_rows_reg<false>, dim3(rows), dim3(kTopkThreads), 0, st,
                                   scores, ld, n_cap, row_len, q_offset, K, idx, count, tps);
     } else {
       // longer rows: four CTAs a row hold up to 131072 keys in registers
-      e = (long)rows <= 2L * sms
-              ? launch_overlapped(topk_rows_cl<4, kRegPer>, dim3(4 * rows), dim3(kTopkThreads), 0,
-                                  st, scores, ld, n_cap, row_len, q_offset, K, idx, count, tps)
+      e = (long)rows <= 2L * sms && rows <= kPackRows
+              ? launch_overlapped(topk_rows_cl<4, kRegPer, true>, dim3(4 * rows),
+                                  dim3(kTopkThreads), 0, st, scores, ld, n_cap, row_len, q_offset,
+                                  K, idx, count, tps, rows)
               : launch_overlapped(topk_rows_reg<true>, dim3(rows), dim3(kTopkThreads), 0, st,
                                   scores, ld, n_cap, row_len, q_offset, K, idx, count, tps);
     }
