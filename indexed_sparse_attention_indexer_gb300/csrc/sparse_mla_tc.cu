@@ -24,16 +24,17 @@
 //     (ring of 4), by TMA gather4 (four rows per instruction) and cp.async at
 //     once, so both copy engines work; the cp.async threads arrive on the
 //     stage's barrier when their copies land, without waiting for them;
-//   MMA (warp 3, one thread): S = Qslice . C^T into the free logit tile,
-//     O += P . V (A = P K-major, B = V MN-major, same stage);
+//   MMA (warp 3, one thread): S = Qslice . C^T into the logit tile once both
+//     readers of the previous tile have loaded it, O += P . V (A = P K-major,
+//     B = V MN-major, same stage);
 //   exchange (warps 4-7): this CTA's partial logits out of TMEM and into the
 //     peer's buffer (st.async, bytes counted on the peer's barrier);
 //   softmax (warps 8-11, one head per thread): own partial from TMEM plus the
 //     peer's from the buffer (one buffer credit per warp returns to the
 //     peer), online softmax in log2 units with a lazily moved reference max
 //     (the accumulator is rescaled only when the max grows by more than 2^8),
-//     P in bf16 to one of two shared-memory tiles (so P of tile t is written
-//     while P.V of tile t-1 runs), and the epilogue.
+//     P in bf16 to the shared-memory P tile once P.V of the previous tile is
+//     done, and the epilogue.
 // Every wait is bounded; the cluster syncs once after set-up and once before
 // exit so no CTA leaves while its peer may still write into it.
 #include "kernels.h"
