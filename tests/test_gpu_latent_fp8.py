@@ -75,6 +75,7 @@ CASES = {
     "paged_h128": ([650, 64, 129], 64, 128, 128, 128, 64),
     "zero_length_h16": ([100, 0, 5], 4, 64, 16, 16, 0),
     "k_ge_history_h48": ([200, 31], 16, 64, 512, 48, 0),
+    "single_seq_h16_cluster_merge8": ([900], 4, 64, 256, 16, 0),
     "single_seq_splitk_h128": ([5000], 64, 128, 2048, 128, 0),
     # 128 heads run on the tensor-core kernel (rows converted to bf16 as they land)
     "contig_h128_ragged": ([3000, 129, 64, 1, 700], 64, 128, 256, 128, 0),

@@ -27,6 +27,10 @@ DECODE_CASES = {
     "paged_fp8": (4, [1100, 300, 65, 2], 64, 128, 128, 128, 64, True, {}),
     "paged_fp8_small_heads": (2, [333, 90], 4, 64, 40, 16, 16, True, {}),
     "k_ge_history": (2, [200, 31], 4, 64, 512, 16, 0, False, {}),
+    # a single row splits its selection eight ways, merged inside one cluster
+    "single_seq_h16_cluster_merge8": (1, [900], 4, 64, 256, 16, 0, False, {}),
+    # four-way clusters per head group; the short row's later splits hold no index
+    "h48_cluster_merge4": (2, [400, 60], 4, 64, 128, 48, 0, False, {}),
     "heads_8": (2, [100, 257], 4, 64, 16, 8, 0, False, {}),
     "heads_48_hi16": (2, [300, 90], 16, 64, 50, 48, 0, False, {}),
     "softmax_stress": (2, [400, 150], 4, 64, 64, 16, 0, False, {"q_std": 1.0, "scale": 1.0}),
