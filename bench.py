@@ -106,7 +106,10 @@ def decode_visible(ws) -> torch.Tensor:
 
 def algorithmic_flops(ws) -> dict:
     vis = decode_visible(ws) if ws.mode == "decode" else torch.arange(1, ws.T + 1) + ws.q_offset
-    idx_fl = 2 * int(vis.sum()) * ws.H_i * ws.d
+    # a prefill row with at most K positions of history takes all of them: its
+    # scores decide nothing, and the fused indexer does not compute them
+    scored = vis if ws.mode == "decode" else vis[vis > ws.K]
+    idx_fl = 2 * int(scored.sum()) * ws.H_i * ws.d
     sel = torch.clamp(vis, max=ws.K)
     mla_fl = 2 * int(sel.sum()) * ws.H * (W.D_QK + W.D_LATENT)
     return {"indexer": idx_fl, "mla": mla_fl}

@@ -20,6 +20,12 @@
 // threads radix-select the K-th key and compact the buffer to the best K.
 // At the end of the group a final select picks the K best, and their
 // positions are written in ascending order through a bitmap prefix scan.
+// A row whose history holds at most K positions selects all of them whatever
+// the scores, so the leading rows of a prefill (up to K - q_offset of them)
+// are not scored: a small kernel launched just before writes their positions
+// in order, and the groups cover the remaining rows only.
+#include <algorithm>
+
 #include "kernels.h"
 #include "tc_common.cuh"
 #include "tma_host.h"
@@ -585,6 +591,21 @@ index_topk_prefill(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// Leading rows whose history holds at most K positions: 0, 1, .., n - 1, then
+// -1 (the selection of every position, whatever the scores).
+__global__ void __launch_bounds__(256)
+prefill_take_all(int32_t* __restrict__ idx, int32_t* __restrict__ count, int rows, int K,
+                 int64_t q_offset) {
+  grid_dep_wait();     // the kernel launched before may still read these outputs
+  grid_dep_launch();   // the fused indexer may start its set-up
+  for (int t = blockIdx.x; t < rows; t += gridDim.x) {
+    const int64_t n = q_offset + t + 1;
+    int32_t* o = idx + (int64_t)t * K;
+    for (int j = threadIdx.x; j < K; j += blockDim.x) o[j] = j < n ? j : -1;
+    if (count && threadIdx.x == 0) count[t] = (int)n;
+  }
+}
+
 }  // namespace
 
 bool fused_prefill_topk_supported(const CacheView& c, int n_heads_idx, int rows, int64_t q_offset,
@@ -604,26 +625,37 @@ cudaError_t launch_index_topk_prefill(const bf16* q_idx, const float* w, const C
                                       int32_t* count, int* err, cudaStream_t st) {
   const uint64_t krows = c.block_table ? (uint64_t)c.num_pages * c.page_size
                                        : (uint64_t)c.batch * c.s_max;
+  // rows r < K - q_offset see at most K positions and take them all
+  const int r0 = (int)std::max<int64_t>(0, std::min<int64_t>(rows, (int64_t)K - q_offset));
+  const int fr = rows - r0;                        // rows scored and selected
+  const bf16* fq = q_idx + (int64_t)r0 * kHeads * kD;
   CUtensorMap kmap, qmap;
   // contiguous keys: one 128-row box per 64-dim block of a tile; paged: 64-row boxes
   if (!tma_map_2d(&kmap, c.k_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, krows, kD, 64,
                   c.block_table ? kSub : kTileM))
     return cudaErrorInvalidValue;
-  if (!tma_map_2d(&qmap, q_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)rows * kHeads, kD, 64,
-                  kHeads))
+  // (with no row to score the map is never used)
+  if (!tma_map_2d(&qmap, fr > 0 ? fq : q_idx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  (uint64_t)(fr > 0 ? fr : rows) * kHeads, kD, 64, kHeads))
     return cudaErrorInvalidValue;
   Args a;
-  a.q_idx = q_idx;
-  a.w = w;
-  a.idx = idx;
-  a.count = count;
-  a.q_offset = q_offset;
-  a.rows = rows;
+  a.q_idx = fq;
+  a.w = w + (int64_t)r0 * kHeads;
+  a.idx = idx + (int64_t)r0 * K;
+  a.count = count ? count + r0 : nullptr;
+  a.q_offset = q_offset + r0;
+  a.rows = fr;
   a.K = K;
-  a.groups = (rows + NT - 1) / NT;
+  a.groups = (fr + NT - 1) / NT;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (r0 > 0) {
+    const cudaError_t te = launch_overlapped(prefill_take_all, dim3(std::min(r0, sms)), dim3(256),
+                                             0, st, idx, count, r0, K, q_offset);
+    note_launch();
+    if (te != cudaSuccess || fr == 0) return te;
+  }
   const int npairs = (a.groups + 1) / 2;
   const int grid = npairs < sms ? npairs : sms;
   a.pairs_per_cta = (npairs + grid - 1) / grid;

@@ -156,6 +156,11 @@ FUSED_PREFILL_CASES = [
     (257, 5000, 0, 100),
     (64, 9000, 8936, 1),
     (33, 4200, 4000, 2048),
+    # rows with at most K positions of history take all of them unscored:
+    # every row, from the start and after an offset, and the first 98 of 200
+    (40, 40, 0, 64),
+    (64, 1000, 900, 2048),
+    (200, 2150, 1950, 2048),
 ]
 
 
