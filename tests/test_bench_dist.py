@@ -85,6 +85,24 @@ def test_algorithmic_bytes_of_the_quantised_variants():
     assert bench.algorithmic_bytes(l8)["gather"] == sel * (576 + 5 * 4)
 
 
+def test_algorithmic_flops_count_the_scored_prefill_rows():
+    """Indexer flops: every visible position of a decode row; for a prefill,
+    only the rows with more than K positions of history (a row seeing at most
+    K takes them all, whatever the scores).  Attention flops: min(K, visible)
+    rows per query, either way."""
+    import bench
+    from indexed_sparse_attention_indexer_gb300 import workloads as W
+    K = 16
+    pf = W.make_prefill(40, 50, 4, 64, K, 16, seed=2, q_offset=10)
+    vis = [10 + t + 1 for t in range(40)]                 # 11 .. 50
+    scored = sum(v for v in vis if v > K)
+    fl = bench.algorithmic_flops(pf)
+    assert fl["indexer"] == 2 * scored * 4 * 64
+    assert fl["mla"] == 2 * sum(min(K, v) for v in vis) * 16 * (576 + 512)
+    dec = W.make_decode(2, 0, 4, 64, K, 16, seed=1, lengths=[100, 9])
+    assert bench.algorithmic_flops(dec)["indexer"] == 2 * (100 + 9) * 4 * 64
+
+
 def test_zigzag_partition_covers_and_balances():
     from indexed_sparse_attention_indexer_gb300 import partition as P
     for T, world in ((8192, 2), (8192, 8), (4096, 4), (130, 3), (7, 4), (1, 2)):
