@@ -696,6 +696,573 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
   cluster_sync();   // the peer may still arrive on / write into this CTA until here
 }
 
+// ---------------------------------------------------------------------------
+// Persistent form for prefills of at least two rows per cluster slot (bf16
+// rows, no split, K <= 2048): each cluster takes rows pair, pair + nclu, ... in turn,
+// so a row's set-up, first gathers and first logits overlap the end of the
+// previous row instead of a new cluster's launch and pipeline fill.
+//   - The exchange warps prepare the next row while the current one runs
+//     (its entries translated into the other half of the entries' space, and
+//     its tile count), after sending the current row's third partial tile;
+//     `rows_ready[b]` publishes a row's entries, `rows_free[b]` returns them
+//     (producers, softmax warps and the MMA thread).  At a row's start the
+//     same warps write its query slice into TMEM (the previous row's logit
+//     MMAs are complete by then: they have seen every one of its logit tiles)
+//     and arrive on `q_ready`.
+//   - Stages, logit/P tiles and exchange buffers run on the cluster's tile
+//     count across rows, as if the rows were one long row; the accumulator
+//     starts afresh at each row's first P.V, which follows the previous row's
+//     epilogue (the softmax warps write the row's first P only after it).
+//   - `q_ready` and `o_done` complete one phase per row with tiles, and rows
+//     without tiles skip them, so no phase can complete twice before it is
+//     waited for.
+constexpr int kPerEntries = kMaxEntries / 2;   // each of the two row buffers
+constexpr int NBARS_R = NBARS + 5;             // + rows_ready[2], rows_free[2], setup_bar
+constexpr int OFF_MISC_R = OFF_BAR + NBARS_R * 8;
+constexpr int SMEM_R = OFF_MISC_R + 64 + 1024;
+static_assert(SMEM_R <= 227 * 1024, "shared memory (persistent form)");
+constexpr int kSetupThreads = 128;             // the exchange warps
+constexpr int kFreeArrivals = kProducerWarps + 4 + 1;   // producer warps, softmax warps, MMA thread
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+mla_tc_rows(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, int* err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* s_full = bars + 2 * kStages;
+  uint64_t* s_empty = s_full + 2;
+  uint64_t* p_full = s_full + 4;
+  uint64_t* p_empty = s_full + 6;
+  uint64_t* q_ready = s_full + 8;
+  uint64_t* o_done = s_full + 9;
+  uint64_t* x_full = s_full + 10;
+  uint64_t* x_empty = x_full + kXBufs;
+  uint64_t* rows_ready = bars + NBARS;           // [2] a row's entries and tile count in place
+  uint64_t* rows_free = rows_ready + 2;          // [2] every reader is done with them
+  uint64_t* setup_bar = rows_ready + 4;          // the preparing warps' entries written
+  int32_t* rows_s = reinterpret_cast<int32_t*>(smem + OFF_ROWS);   // [2][kPerEntries]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC_R);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC_R + 4);
+  int* ntiles_s = reinterpret_cast<int*>(smem + OFF_MISC_R + 8);   // [2]
+  int* lastv_s = reinterpret_cast<int*>(smem + OFF_MISC_R + 16);   // [2]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rho = cluster_ctarank();
+  const uint32_t peer = rho ^ 1u;
+  const int pair = blockIdx.x >> 1, nclu = gridDim.x >> 1;
+  const int items = pair < a.rows ? (a.rows - pair + nclu - 1) / nclu : 0;   // rows of this cluster
+  const int tiles_all = (a.K + kNp - 1) / kNp;
+  const int span = tiles_all * kNp;                // entries of a row (<= kPerEntries)
+  const int g0 = rho ? 4 : 0;
+  const int qk_first = rho ? 1 : 0;
+  constexpr uint32_t kXBytes = kH * kNp * 4;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1 + kLdgThreads);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 256);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&p_empty[i], 1);
+      mbar_init(&rows_ready[i], kSetupThreads);
+      mbar_init(&rows_free[i], kFreeArrivals);
+      lastv_s[i] = -1;
+    }
+    mbar_init(q_ready, kSetupThreads);
+    mbar_init(o_done, 1);
+    mbar_init(setup_bar, kSetupThreads);
+    for (int i = 0; i < kXBufs; ++i) {
+      mbar_init(&x_full[i], 1);
+      mbar_init(&x_empty[i], 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, TMEM_COLS);
+  grid_dep_wait();   // the indices (and queries) come from the kernels launched before
+  __syncthreads();
+  // the peer's first partial tile (every later one is expected as the
+  // previous is consumed)
+  if (tid == 0) mbar_arrive_expect_tx(&x_full[0], kXBytes);
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  grid_dep_launch();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ======================= gather: TMA part =================================
+    if (lane < kTmaRows / 4) {
+      if (lane == 0) prefetch_tmap(&lmap);
+      int stage = 0;
+      uint32_t ph = 0;
+      bool issued[kStages] = {};
+      uint32_t issued_ph[kStages] = {};
+      const unsigned gmask = (1u << (kTmaRows / 4)) - 1u;
+      bool ok = true;
+      for (int i = 0; ok && i < items; ++i) {
+        const int bsel = i & 1;
+        ok = mbar_wait(&rows_ready[bsel], (uint32_t)(i >> 1) & 1u, abort_flag, err);
+        ok = __all_sync(gmask, ok);
+        if (!ok) break;
+        const int n = ntiles_s[bsel];
+        const int32_t* rs = rows_s + bsel * kPerEntries;
+        for (int t = 0; t < n; ++t) {
+          if (lane == 0) {
+            ok = mbar_wait(&empty[stage], ph ^ 1, abort_flag, err);
+            if (ok) mbar_arrive_expect_tx(&full[stage], kTmaChunks * kTmaRows * 128);
+          }
+          ok = __shfl_sync(gmask, ok, 0);
+          if (!ok) break;
+          issued[stage] = true;
+          issued_ph[stage] = ph;
+          uint8_t* st_base = smem + OFF_C + stage * kStageBytes;
+          const int r4 = lane * 4;
+          const int32_t* rw = rs + t * kNp + r4;
+          const int y0 = max(rw[0], 0), y1 = max(rw[1], 0), y2 = max(rw[2], 0), y3 = max(rw[3], 0);
+#pragma unroll
+          for (int ch = 0; ch < kTmaChunks; ++ch)
+            tma_gather4(st_base + ch * kChunkBytes + r4 * 128, &lmap, (g0 + ch) * 64, y0, y1, y2, y3,
+                        &full[stage]);
+          if (++stage == kStages) { stage = 0; ph ^= 1; }
+        }
+        __syncwarp(gmask);
+        if (ok && lane == 0) mbar_arrive(&rows_free[bsel]);
+      }
+      if (lane == 0 && *abort_flag) {
+        volatile int no_abort = 0;
+        for (int s2 = 0; s2 < kStages; ++s2)
+          if (issued[s2]) mbar_wait(&full[s2], issued_ph[s2], &no_abort, err, 100000000ull);
+      }
+    }
+  } else if (warp < kProducerWarps) {
+    // ======================= gather: cp.async part ============================
+    constexpr int kLdgPieces = (kChunks - kTmaChunks) * 8;
+    static_assert(kLdgPieces == 16, "half a warp per row");
+    const int sub = lane >> 4, pi = lane & 15;
+    const int ch = kTmaChunks + (pi >> 3), u = pi & 7;
+    int stage = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int i = 0; ok && i < items; ++i) {
+      const int bsel = i & 1;
+      if (!(ok = warp_wait(&rows_ready[bsel], (uint32_t)(i >> 1) & 1u, abort_flag, err))) break;
+      const int n = ntiles_s[bsel];
+      const int32_t* rs = rows_s + bsel * kPerEntries;
+      for (int t = 0; t < n; ++t) {
+        if (!(ok = mbar_wait(&empty[stage], ph ^ 1, abort_flag, err))) break;
+        const uint32_t st_addr = smem_u32(smem + OFF_C + stage * kStageBytes);
+        for (int rr = (warp - 1) * 2 + sub; rr < kNp; rr += 2 * kLdgWarps) {
+          const int pr = max(rs[t * kNp + rr], 0);
+          cp_async_16(st_addr + ch * kChunkBytes + sw128_offset(rr, u),
+                      c.latent + (int64_t)pr * DSI_D_QK + (g0 + ch) * 64 + u * 8);
+        }
+        constexpr int kTailPieces = (kNp - kTmaRows) * kTmaChunks * 8;
+        for (int q = (warp - 1) * 32 + lane; q < kTailPieces; q += kLdgThreads) {
+          const int rr = kTmaRows + q / (kTmaChunks * 8), w = q % (kTmaChunks * 8);
+          const int pr = max(rs[t * kNp + rr], 0);
+          cp_async_16(st_addr + (w >> 3) * kChunkBytes + sw128_offset(rr, w & 7),
+                      c.latent + (int64_t)pr * DSI_D_QK + (g0 + (w >> 3)) * 64 + (w & 7) * 8);
+        }
+        cp_async_mbar_arrive_noinc(&full[stage]);
+        if (++stage == kStages) { stage = 0; ph ^= 1; }
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok && lane == 0) mbar_arrive(&rows_free[bsel]);
+    }
+    cp_async_wait<0>();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      // ===================== MMA issuer =======================================
+      // Two cursors over the cluster's tiles: the logits (QK) and P.V, each
+      // with its row and tile within the row; the QK cursor learns each row's
+      // tile count (returning its entries' buffer at once) and stays at most
+      // three rows ahead of P.V.
+      int n0 = 0, n1 = 0, n2 = 0;                // tile counts of rows pi, pi + 1, pi + 2
+      int qi = 0, qt = 0, qg = 0, nq = 0;        // QK: row, tile, tile count so far, rows with tiles
+      bool qin = false;                          // the QK cursor has entered row qi
+      bool qq = false;                           // ... and its queries are in TMEM
+      int pi = 0, pt = 0, pg = 0;                // P.V: row, tile, tile count so far
+      const uint32_t pbase = smem_u32(smem + OFF_P);
+      uint64_t t_last = global_ns();
+      uint32_t idle = 0;
+      bool ok = true;
+      while (ok && pi < items) {
+        bool progress = false;
+        // ---- P.V ----
+        if (pi < qi || (pi == qi && qin)) {
+          const int pn = n0;
+          if (pt >= pn) {            // a row without tiles, or one just finished
+            ++pi;
+            pt = 0;
+            n0 = n1;
+            n1 = n2;
+            progress = true;
+          } else if (pg < qg && mbar_test_wait(&p_full[0], pg & 1)) {
+            tc_fence_after();
+            const int st = pg % kStages;
+            const uint64_t pd = desc_sw128(pbase);
+            const uint64_t vd = desc_sw128_mn(smem_u32(smem + OFF_C + st * kStageBytes), kChunkBytes);
+#pragma unroll
+            for (int kk = 0; kk < kNp / 16; ++kk)
+              mma_bf16(tmem + TM_O, pd + (uint64_t)((kk * 32) >> 4), vd + (uint64_t)((kk * 2048) >> 4),
+                       IDESC_O, (pt > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&p_empty[0]);
+            mma_commit(&empty[st]);
+            ++pg;
+            if (++pt == pn) mma_commit(o_done);   // the row's output is complete
+            progress = true;
+          }
+        }
+        // ---- QK ----
+        if (qi < items) {
+          if (!qin) {
+            if (qi - pi < 3 && mbar_test_wait(&rows_ready[qi & 1], (uint32_t)(qi >> 1) & 1u)) {
+              const int nn = ntiles_s[qi & 1];
+              if (qi == pi) n0 = nn; else if (qi == pi + 1) n1 = nn; else n2 = nn;
+              mbar_arrive(&rows_free[qi & 1]);
+              qin = true;
+              qq = false;
+              qt = 0;
+              progress = true;
+            }
+          } else if (qt >= (qi == pi ? n0 : qi == pi + 1 ? n1 : n2)) {
+            ++qi;
+            qin = false;
+            progress = true;
+          } else if (!qq) {
+            if (mbar_test_wait(q_ready, (uint32_t)nq & 1u)) {
+              tc_fence_after();
+              ++nq;
+              qq = true;
+              progress = true;
+            }
+          } else {
+            const int st = qg % kStages;
+            if (mbar_test_wait(&full[st], (qg / kStages) & 1) &&
+                mbar_test_wait(&s_empty[0], (qg & 1) ^ 1)) {
+              tc_fence_after();
+              fence_proxy_async_smem();
+              const uint32_t t_s = tmem + TM_S;
+              const uint32_t st_base = smem_u32(smem + OFF_C + st * kStageBytes);
+              const uint64_t d0 = desc_sw128(st_base + qk_first * kChunkBytes);
+              for (int k = 0; k < kQkTmem * 4; ++k)
+                mma_bf16_tmem_a(t_s, tmem + TM_Q + k * 8,
+                                d0 + (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4),
+                                IDESC_S, k > 0 ? 1u : 0u);
+              {
+                const uint64_t cd = desc_sw128(st_base + (rho ? 0 : kQkTmem) * kChunkBytes);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  const int kk = (int)rho * 2 + k;
+                  mma_bf16_tmem_a(t_s, tmem + TM_Q4 + kk * 8, cd + (uint64_t)((kk * 32) >> 4),
+                                  IDESC_S, 1u);
+                }
+              }
+              mma_commit(&s_full[0]);
+              ++qg;
+              ++qt;
+              progress = true;
+            }
+          }
+        }
+        if (progress) {
+          idle = 0;
+          t_last = global_ns();
+        } else if (*abort_flag) {
+          ok = false;
+        } else if ((++idle & 255u) == 0 && global_ns() - t_last > kWaitLimitNs) {
+          *abort_flag = 1;
+          report(err, kErrTimeout);
+          ok = false;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < kSmWarp0) {
+    // ======================= row preparation + logit exchange =================
+    const int quarter = warp & 3;
+    const int h = quarter * 32 + lane;
+    const int et = tid - kExWarp0 * 32;              // 0..127
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    int setups = 0;
+    // entries of row item i, translated into buffer i & 1, and its tile count
+    auto prepare = [&](int i) -> bool {
+      const int bsel = i & 1, use = i >> 1;
+      if (use > 0 && !warp_wait(&rows_free[bsel], (uint32_t)(use - 1) & 1u, abort_flag, err))
+        return false;
+      const int r = pair + i * nclu;
+      const int64_t n_vis = visible_len(c, r, a.decode, a.q_offset);
+      const int b = seq_of_row(c, r, a.decode);
+      const int32_t* irow = a.idx + (int64_t)r * a.K;
+      int32_t* rs = rows_s + bsel * kPerEntries;
+      // every index load is issued before any is used
+      constexpr int kPP = kPerEntries / kSetupThreads;
+      int pos[kPP];
+#pragma unroll
+      for (int u = 0; u < kPP; ++u) {
+        const int jj = et + u * kSetupThreads;
+        pos[u] = (jj < span && jj < a.K) ? __ldg(irow + jj) : -1;
+      }
+      int lv = -1;
+#pragma unroll
+      for (int u = 0; u < kPP; ++u) {
+        const int jj = et + u * kSetupThreads;
+        if (jj >= span) break;
+        int pr = -1;
+#ifdef DSI_CHECKED
+        if (pos[u] >= n_vis) report(err, kErrBounds);
+#endif
+        if (pos_ok(pos[u], n_vis)) {
+          const int64_t x = phys_row(c, b, pos[u], err);
+          if (x >= 0) { pr = (int)x; lv = jj; }
+        }
+        rs[jj] = pr;
+      }
+      lv = __reduce_max_sync(0xffffffffu, lv);
+      if (lane == 0 && lv >= 0) atomicMax(&lastv_s[bsel], lv);
+      // the next row's query slice toward L2 (it is read at the row's start)
+      if (i + 1 < items) {
+        const bf16* qn = a.q + ((int64_t)(r + nclu) * kH + h) * DSI_D_QK;
+#pragma unroll
+        for (int k = 0; k < kQkTmem; ++k)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + (g0 + qk_first + k) * 64));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + 4 * 64));
+      }
+      mbar_arrive(setup_bar);
+      if (et == 0) {
+        if (!mbar_wait(setup_bar, (uint32_t)setups & 1u, abort_flag, err)) return false;
+        const int l = lastv_s[bsel];
+        ntiles_s[bsel] = l < 0 ? 0 : l / kNp + 1;
+        lastv_s[bsel] = -1;
+      }
+      ++setups;
+      mbar_arrive(&rows_ready[bsel]);
+      return true;
+    };
+    // this row's query slice (four 64-dim blocks and the block of dims
+    // 256..319) into TMEM, eight 16-byte pieces a block
+    auto load_q = [&](int r) {
+      const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)r * kH + h) * DSI_D_QK);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint4 qv[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) qv[k] = __ldg(qrow + (g0 + qk_first + half * 2) * 8 + k);
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {
+          uint32_t w32[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint4 v = qv[cb * 8 + k];
+            w32[4 * k] = v.x; w32[4 * k + 1] = v.y; w32[4 * k + 2] = v.z; w32[4 * k + 3] = v.w;
+          }
+          tmem_st32(tmem + lane_base + TM_Q + (half * 2 + cb) * 32, w32);
+        }
+      }
+      {
+        uint32_t w32[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = __ldg(qrow + 4 * 8 + k);
+          w32[4 * k] = v.x; w32[4 * k + 1] = v.y; w32[4 * k + 2] = v.z; w32[4 * k + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_base + TM_Q4, w32);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(q_ready);
+    };
+    const uint32_t x_remote = map_to_rank(smem_u32(smem + OFF_X), peer) + h * 16;
+    const uint32_t xfull_remote = map_to_rank(smem_u32(x_full), peer);
+    bool ok = items > 0 ? prepare(0) : true;
+    int tg = 0;
+    for (int i = 0; ok && i < items; ++i) {
+      const int bsel = i & 1;
+      if (!(ok = warp_wait(&rows_ready[bsel], (uint32_t)(i >> 1) & 1u, abort_flag, err))) break;
+      const int n = ntiles_s[bsel];
+      const bool more = i + 1 < items;
+      if (n == 0) {
+        if (more) ok = prepare(i + 1);
+        continue;
+      }
+      // every logit tile of the previous rows has been seen complete, so no
+      // MMA reads the query slice any more
+      load_q(pair + i * nclu);
+      const int prep_at = n > 2 ? 2 : n - 1;
+      for (int t = 0; ok && t < n; ++t, ++tg) {
+        float v[kNp];
+        if (!(ok = warp_wait(&s_full[0], tg & 1, abort_flag, err))) break;
+        tc_fence_after();
+        tmem_ld32(tmem + lane_base + TM_S, v);
+        tmem_ld32(tmem + lane_base + TM_S + 32, v + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&s_empty[0]);
+        if (!(ok = warp_wait_cluster(&x_empty[0], (tg & 1) ^ 1, abort_flag, err))) break;
+#pragma unroll
+        for (int q4 = 0; q4 < kNp / 4; ++q4)
+          st_async_v4(x_remote + q4 * (kH * 16),
+                      make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]),
+                      xfull_remote);
+        if (t == prep_at && more) ok = prepare(i + 1);
+      }
+    }
+  } else {
+    // ======================= softmax + epilogue ================================
+    const int quarter = warp & 3;
+    const int h = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    uint8_t* const pbuf = smem + OFF_P;
+    const uint8_t* xrow = smem + OFF_X + h * 16;
+    const uint32_t xempty_remote = map_to_rank(smem_u32(x_empty), peer);
+    const float sl2 = a.scale * kLog2e;
+    bool ok = true;
+    int tg = 0, nrows = 0;                          // tiles so far; rows with tiles so far
+    for (int i = 0; ok && i < items; ++i) {
+      const int bsel = i & 1;
+      const int r = pair + i * nclu;
+      if (!(ok = warp_wait(&rows_ready[bsel], (uint32_t)(i >> 1) & 1u, abort_flag, err))) break;
+      const int n = ntiles_s[bsel];
+      const int32_t* rs = rows_s + bsel * kPerEntries;
+      float m_ref = -INFINITY, l_sum = 0.f;
+      for (int t = 0; ok && t < n; ++t, ++tg) {
+        float vc[kNp];
+        if (!(ok = warp_wait(&s_full[0], tg & 1, abort_flag, err))) break;
+        tc_fence_after();
+        tmem_ld32(tmem + lane_base + TM_S, vc);
+        tmem_ld32(tmem + lane_base + TM_S + 32, vc + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&s_empty[0]);
+        if (!(ok = warp_wait_cluster(&x_full[0], tg & 1, abort_flag, err))) break;
+#pragma unroll
+        for (int q4 = 0; q4 < kNp / 4; ++q4) {
+          const float4 pv4 = *reinterpret_cast<const float4*>(xrow + q4 * (kH * 16));
+          vc[4 * q4] += pv4.x; vc[4 * q4 + 1] += pv4.y; vc[4 * q4 + 2] += pv4.z; vc[4 * q4 + 3] += pv4.w;
+        }
+        // buffer credit (the next tile may be in a later row; none after the
+        // cluster's last row)
+        __syncwarp();
+        if (lane == 0 && !(i + 1 == items && t + 1 == n)) {
+          if (quarter == 0) mbar_arrive_expect_tx_relaxed(&x_full[0], kXBytes);
+          mbar_arrive_remote_relaxed(xempty_remote);
+        }
+        const uint32_t m_lo = __ballot_sync(0xffffffffu, rs[t * kNp + lane] >= 0);
+        const uint32_t m_hi = __ballot_sync(0xffffffffu, rs[t * kNp + 32 + lane] >= 0);
+        if ((m_lo & m_hi) != 0xffffffffu) {
+#pragma unroll
+          for (int j = 0; j < kNp; ++j)
+            if ((((j < 32 ? m_lo >> j : m_hi >> (j - 32)) & 1u)) == 0) vc[j] = -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = vc[k];
+#pragma unroll
+        for (int j = 8; j < kNp; ++j) mx[j & 7] = fmaxf(mx[j & 7], vc[j]);
+#pragma unroll
+        for (int w2 = 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+          for (int k = 0; k < w2; ++k) mx[k] = fmaxf(mx[k], mx[k + w2]);
+        const float tmax = mx[0] * sl2;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m_ref == -INFINITY) {
+          m_ref = tmax;
+        } else if (tmax > m_ref + kRescaleLog2) {
+          alpha = exp2f(m_ref - tmax);
+          m_ref = tmax;
+          rescale = true;
+        }
+        if (!(ok = warp_wait(&p_empty[0], (tg & 1) ^ 1, abort_flag, err))) break;
+        tc_fence_after();
+        float ps[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+        const float nmr = (m_ref == -INFINITY) ? 0.f : -m_ref;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 8 * u + 2 * e;
+            const float e0 = ex2_approx(fmaf(vc[j], sl2, nmr));
+            const float e1 = ex2_approx(fmaf(vc[j + 1], sl2, nmr));
+            const __nv_bfloat162 p2 = __floats2bfloat162_rn(e0, e1);
+            const float2 pr = __bfloat1622float2(p2);
+            ps[2 * e] += pr.x;
+            ps[2 * e + 1] += pr.y;
+            w4[e] = *reinterpret_cast<const uint32_t*>(&p2);
+          }
+          *reinterpret_cast<uint4*>(pbuf + sw128_offset(h, u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        l_sum = l_sum * alpha + psum;
+        // the accumulator rescaled once this tile's P is written (the logits
+        // are no longer live): P.V of the previous tile has landed in it, and
+        // this tile's P.V waits for the arrival below
+        if (__any_sync(0xffffffffu, rescale)) {
+          for (int c0 = 0; c0 < 256; c0 += 32) {
+            float o[32];
+            tmem_ld32(tmem + lane_base + TM_O + c0, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] *= alpha;
+            tmem_st32f(tmem + lane_base + TM_O + c0, o);
+          }
+          tmem_st_wait();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[0]);
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rows_free[bsel]);
+      // ---- this row's output: normalise and store this CTA's 256 dims ---------
+      const bool have = n > 0 && l_sum > 0.f;
+      if (n > 0) {
+        if (!(ok = warp_wait(o_done, (uint32_t)nrows & 1u, abort_flag, err))) break;
+        tc_fence_after();
+        ++nrows;
+      }
+      const int col0 = (int)rho * 256;
+      const float inv = have ? 1.f / l_sum : 0.f;
+      bf16* dst0 = a.out + ((int64_t)r * kH + h) * DSI_D_LATENT + col0;
+      for (int c0 = 0; c0 < 256; c0 += 32) {
+        float o[32];
+        if (n > 0) {
+          tmem_ld32(tmem + lane_base + TM_O + c0, o);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 32; k += 8) {
+          __align__(16) bf16 o8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o8[e] = __float2bfloat16(o[k + e] * inv);
+          *reinterpret_cast<uint4*>(dst0 + c0 + k) = *reinterpret_cast<const uint4*>(o8);
+        }
+      }
+      if (rho == 0 && a.lse)
+        a.lse[(int64_t)r * kH + h] = have ? (m_ref + log2f(l_sum)) / kLog2e : -INFINITY;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, TMEM_COLS);
+  cluster_sync();
+}
+
 }  // namespace
 
 bool tc_mla_supported(int n_heads) { return n_heads == kH; }
@@ -755,6 +1322,38 @@ cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const float*
   if (!f8 &&
       !tma_map_2d(&lmap, c.latent, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lrows, DSI_D_QK, 64, 1))
     return cudaErrorInvalidValue;
+  // a prefill of at least two rows per cluster slot (bf16 rows, no split,
+  // K <= 2048): the persistent form, one cluster per slot taking rows in turn
+  // (rows of a prefill are dealt round-robin, so every slot gets a like mix;
+  // decode batches, whose rows differ in length at random, keep one cluster a
+  // row, which the hardware places as slots free up)
+  if (!decode && !f8 && a.splits == 1 && (K + kNp - 1) / kNp * kNp <= kPerEntries) {
+    cudaError_t e = cudaFuncSetAttribute(mla_tc_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_R);
+    if (e != cudaSuccess) return e;
+    int slots = 0;
+    cudaLaunchConfig_t qc = {};
+    qc.gridDim = dim3(2);
+    qc.blockDim = dim3(kThreads);
+    qc.dynamicSmemBytes = SMEM_R;
+    cudaLaunchAttribute ca;
+    ca.id = cudaLaunchAttributeClusterDimension;
+    ca.val.clusterDim.x = 2;
+    ca.val.clusterDim.y = 1;
+    ca.val.clusterDim.z = 1;
+    qc.attrs = &ca;
+    qc.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&slots, mla_tc_rows, &qc) != cudaSuccess) {
+      cudaGetLastError();
+      slots = 0;
+    }
+    if (slots > 0 && rows >= 2 * slots) {
+      e = launch_overlapped(mla_tc_rows, dim3(2u * (unsigned)slots), dim3(kThreads), SMEM_R, st,
+                            lmap, c, a, err);
+      note_launch();
+      return e;
+    }
+  }
   auto kern = f8 ? mla_tc<true> : mla_tc<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;

@@ -50,6 +50,17 @@ DECODE_CASES = {
     "hi64_many_one_tile_seqs": (24, [1, 128, 77, 64, 3, 128, 90, 129, 100, 5, 128, 60,
                                      33, 128, 2, 127, 128, 700, 41, 128, 9, 64, 128, 16],
                                 64, 128, 16, 128, 0, False, {}),
+    # more rows than the attention core's cluster slots (a second wave of
+    # clusters), with zero-length and one-tile sequences
+    "hi64_many_rows_paged": (96, [90, 1179, 952, 64, 1193, 0, 1297, 502, 1452, 478, 537, 585,
+                                  490, 1202, 281, 137, 1366, 0, 316, 1187, 1094, 1138, 1108, 906,
+                                  1456, 196, 1158, 540, 1012, 1306, 64, 1467, 307, 1061, 214,
+                                  242, 62, 1317, 276, 243, 0, 0, 389, 530, 498, 582, 957, 174,
+                                  823, 279, 825, 1132, 511, 114, 1446, 589, 687, 5, 1495, 692,
+                                  64, 131, 558, 52, 1035, 1218, 504, 310, 80, 1216, 1406, 403,
+                                  652, 1200, 622, 663, 1245, 1006, 1079, 1461, 1215, 311, 962,
+                                  947, 161, 125, 1114, 698, 0, 242, 991, 1149, 26, 161, 468, 667],
+                             64, 128, 192, 128, 64, False, {}),
     "hi64_many_one_tile_seqs_paged_fp8": (20, [64, 128, 7, 100, 128, 1, 65, 128, 30, 128,
                                                300, 12, 128, 128, 99, 2, 128, 64, 50, 128],
                                           64, 128, 16, 128, 64, True, {}),
@@ -147,6 +158,46 @@ def test_prefill(name):
     assert_out_close(out2.float().cpu().numpy(), ref_out, name + " fused")
     assert_lse_close(lse2.cpu().numpy(), np.stack([ref[t]["lse"] for t in range(T)]), name)
     assert binding.device_status() == 0
+
+
+def test_prefill_attention_on_given_indices():
+    """The attention core over index sets it is handed, with several rows per
+    cluster slot (each cluster takes rows in turn): rows with no valid entry,
+    a first tile of skipped entries, a single entry in the last tile, and
+    entries past the row's history (skipped), against the oracle's attention
+    over the valid rows."""
+    T, S, off, K, H = 400, 820, 400, 192, 128
+    ws = W.make_prefill(T, S, 4, 64, K, H, seed=31, q_offset=off)
+    rng = np.random.default_rng(31)
+    idx = np.full((T, K), -1, dtype=np.int32)
+    for t in range(T):
+        n_vis = off + t + 1
+        kind = t % 5
+        if kind == 1:
+            idx[t] = rng.choice(n_vis, K, replace=False)
+        elif kind == 2:
+            idx[t, 64:] = rng.choice(n_vis, K - 64, replace=False)
+        elif kind == 3:
+            idx[t, K - 1] = rng.integers(0, n_vis)
+        elif kind == 4:
+            idx[t] = rng.choice(n_vis, K, replace=False)
+            bad = rng.choice(K, 20, replace=False)
+            idx[t, bad] = rng.integers(n_vis, S + 50, 20)   # past the history
+    g = ws.to(DEV)
+    cache = binding.Cache.of(g)
+    out, lse = binding.sparse_mla_prefill(g.q, cache, torch.tensor(idx, device=DEV), off,
+                                          ws.scale)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    lat = ws.latent[0].float().numpy()
+    q = ws.q.float().numpy()
+    ref_o = np.zeros((T, H, W.D_LATENT))
+    ref_l = np.zeros((T, H))
+    for t in range(T):
+        v = idx[t][(idx[t] >= 0) & (idx[t] < off + t + 1)]
+        ref_o[t], ref_l[t] = oracle.sparse_mla(q[t], lat[v], ws.scale)
+    assert_out_close(out.float().cpu().numpy(), ref_o, "given indices")
+    assert_lse_close(lse.cpu().numpy(), ref_l, "given indices")
 
 
 FUSED_PREFILL_CASES = [
@@ -258,6 +309,11 @@ MULTI_CASES = {
     # at every tile for the groups of four candidates
     "one_tile_seqs_t4_paged_fp8": ([128, 64, 700, 2, 128, 129, 30, 128], 4, 64, 128, 32, 128, 64,
                                    True),
+    # 90 candidate rows: more than the attention core's cluster slots
+    "many_rows_t2": ([242, 63, 330, 424, 223, 798, 890, 692, 144, 426, 705, 829, 207, 440, 4,
+                       232, 172, 127, 451, 735, 542, 135, 707, 583, 801, 776, 874, 233, 460, 676,
+                       562, 105, 619, 33, 832, 608, 333, 388, 897, 856, 480, 842, 42, 681, 736],
+                     2, 64, 128, 128, 128, 0, False),
 }
 
 
