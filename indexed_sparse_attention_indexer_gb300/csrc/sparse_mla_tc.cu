@@ -604,19 +604,6 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
       if (!(ok = warp_wait(&p_empty[0], (t & 1) ^ 1, abort_flag, err))) break;
       tc_fence_after();
       uint8_t* prow = pbuf;
-      // TMEM loads/stores are warp-collective: rescale when any head of the
-      // warp needs it (the others multiply by 1)
-      if (__any_sync(0xffffffffu, rescale)) {
-        for (int c0 = 0; c0 < 256; c0 += 32) {
-          float o[32];
-          tmem_ld32(tmem + lane_base + TM_O + c0, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32f(tmem + lane_base + TM_O + c0, o);
-        }
-        tmem_st_wait();
-      }
       // P = 2^(logit * sl2 - reference) in bf16, straight into the swizzled P
       // tile; the row sum adds the rounded values (what P.V multiplies), in
       // eight independent chains
@@ -644,6 +631,20 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
       }
       const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l_sum = l_sum * alpha + psum;     // alpha == 1 for heads that did not move their reference
+      // the accumulator rescaled once P is written (the logits are no longer
+      // live); TMEM loads/stores are warp-collective: rescale when any head of
+      // the warp needs it (the others multiply by 1)
+      if (__any_sync(0xffffffffu, rescale)) {
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+          float o[32];
+          tmem_ld32(tmem + lane_base + TM_O + c0, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32f(tmem + lane_base + TM_O + c0, o);
+        }
+        tmem_st_wait();
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[0]);
