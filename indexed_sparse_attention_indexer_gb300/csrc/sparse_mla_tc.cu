@@ -37,6 +37,8 @@
 //     done, and the epilogue.
 // Every wait is bounded; the cluster syncs once after set-up and once before
 // exit so no CTA leaves while its peer may still write into it.
+#include <atomic>
+
 #include "kernels.h"
 #include "tc_common.cuh"
 #include "tma_host.h"
@@ -1291,6 +1293,34 @@ int tc_mla_splits(int rows, int K, size_t ws_bytes) {
   return splits;
 }
 
+// Two-CTA clusters of the persistent form that fit on the device at once
+// (queried once per device; 0 when the query fails).
+static int rows_slots() {
+  static std::atomic<int> cached[16];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) return 0;
+  const int v = cached[dev].load(std::memory_order_relaxed);
+  if (v != 0) return v > 0 ? v : 0;
+  int slots = 0;
+  cudaLaunchConfig_t qc = {};
+  qc.gridDim = dim3(2);
+  qc.blockDim = dim3(kThreads);
+  qc.dynamicSmemBytes = SMEM_R;
+  cudaLaunchAttribute ca;
+  ca.id = cudaLaunchAttributeClusterDimension;
+  ca.val.clusterDim.x = 2;
+  ca.val.clusterDim.y = 1;
+  ca.val.clusterDim.z = 1;
+  qc.attrs = &ca;
+  qc.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&slots, mla_tc_rows, &qc) != cudaSuccess) {
+    cudaGetLastError();
+    slots = 0;
+  }
+  cached[dev].store(slots > 0 ? slots : -1, std::memory_order_relaxed);
+  return slots;
+}
+
 cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const float* latent_scale,
                                  const int32_t* idx, int rows, int H, int K, int decode,
                                  int64_t q_offset, float scale, bf16* out, float* lse, void* ws,
@@ -1332,22 +1362,7 @@ cudaError_t launch_sparse_mla_tc(const bf16* q, const CacheView& c, const float*
     cudaError_t e = cudaFuncSetAttribute(mla_tc_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_R);
     if (e != cudaSuccess) return e;
-    int slots = 0;
-    cudaLaunchConfig_t qc = {};
-    qc.gridDim = dim3(2);
-    qc.blockDim = dim3(kThreads);
-    qc.dynamicSmemBytes = SMEM_R;
-    cudaLaunchAttribute ca;
-    ca.id = cudaLaunchAttributeClusterDimension;
-    ca.val.clusterDim.x = 2;
-    ca.val.clusterDim.y = 1;
-    ca.val.clusterDim.z = 1;
-    qc.attrs = &ca;
-    qc.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&slots, mla_tc_rows, &qc) != cudaSuccess) {
-      cudaGetLastError();
-      slots = 0;
-    }
+    const int slots = rows_slots();
     if (slots > 0 && rows >= 2 * slots) {
       e = launch_overlapped(mla_tc_rows, dim3(2u * (unsigned)slots), dim3(kThreads), SMEM_R, st,
                             lmap, c, a, err);
