@@ -10,13 +10,14 @@
 // One (query row, K split) is a cluster of two CTAs.  With all 128 heads as
 // the MMA M dimension, the fp32 output of one row (128 x 512) alone fills a
 // CTA's tensor memory, so the work is split by dimension:
-//   CTA 0: logits over key dims   0..287, output dims   0..255, gathers dims   0..319
-//   CTA 1: logits over key dims 288..575, output dims 256..511, gathers dims 256..575
-// Each CTA gathers only the 320 dims of every selected row that it needs,
-// keeps its half of the output accumulator in TMEM (256 columns), one logit
-// tile (64 columns) and its query slice (four 64-dim blocks, 128 columns,
-// and the block of dims 256..319, which the CTAs split, in 32 more): 18
-// logit MMAs a tile on each CTA.
+//   CTA 0: logits over key dims   0..255 and 512..543, output dims   0..255
+//   CTA 1: logits over key dims 256..511 and 544..575, output dims 256..511
+// Each CTA gathers only the 288 dims of every selected row that it uses
+// (no dim is gathered twice), keeps its half of the output accumulator in
+// TMEM (256 columns), one logit tile (64 columns) and its query slice (four
+// 64-dim blocks, 128 columns, and its half of the rope dims in 16 more): 18
+// logit MMAs a tile on each CTA.  Stage block 4 holds the rope half in the
+// first 64 bytes of each 128-byte row.
 // The two partial logit tiles (128 heads x 64 positions, fp32) are swapped
 // through distributed shared memory, so both CTAs hold the same logits and
 // take the same softmax decisions.  Per 64-position tile, 12 warps:
@@ -57,7 +58,8 @@ constexpr int kChunks = 5;                     // 64-dim blocks each CTA gathers
 // leaves the shared memory for a fourth 40 KB stage of gathered rows.
 constexpr int kStages = 4;
 constexpr int kXBufs = 1;                      // exchange buffers for the peer's partial logits
-constexpr int kQkTmem = 4;                     // query blocks of the main logit MMAs (dims 256..319 apart)
+constexpr int kQkTmem = 4;                     // query blocks of the main logit MMAs (the rope half apart)
+constexpr int kRopeHalf = 32;                  // rope dims each CTA takes (512.. or 544..)
 constexpr int kChunkBytes = kNp * 128;         // one 64-dim block of a tile: 8 KB
 constexpr int kStageBytes = kChunks * kChunkBytes;
 // 12 warps (three per SM sub-partition): at most 168 registers a thread
@@ -116,6 +118,40 @@ __device__ __forceinline__ bool pos_ok(int pos, int64_t n_vis) {
   return pos >= 0 && pos < n_vis;
 }
 
+// A tile's cp.async part, thread lt of kLdgThreads: the fourth 64-dim block
+// of every row (8 pieces a row), the rope half (4 pieces, into the first half
+// of block 4) and the first kTmaChunks blocks of the rows past kTmaRows, each
+// 16-byte piece to its swizzled place (consecutive threads take consecutive
+// pieces of a row).  `rows` holds the tile's physical rows (-1: row 0).
+__device__ __forceinline__ void ldg_tile(uint32_t st_addr, const bf16* latent, const int32_t* rows,
+                                         int lt, uint32_t rho, int g0) {
+#pragma unroll
+  for (int k = 0; k < kNp * 8 / kLdgThreads; ++k) {
+    const int q = lt + k * kLdgThreads, rr = q >> 3, u = q & 7;
+    const int pr = max(rows[rr], 0);
+    cp_async_16(st_addr + 3 * kChunkBytes + sw128_offset(rr, u),
+                latent + (int64_t)pr * DSI_D_QK + (g0 + 3) * 64 + u * 8);
+  }
+#pragma unroll
+  for (int k = 0; k < kNp * 4 / kLdgThreads; ++k) {
+    const int q = lt + k * kLdgThreads, rr = q >> 2, u = q & 3;
+    const int pr = max(rows[rr], 0);
+    cp_async_16(st_addr + kQkTmem * kChunkBytes + sw128_offset(rr, u),
+                latent + (int64_t)pr * DSI_D_QK + DSI_D_LATENT + (int)rho * kRopeHalf + u * 8);
+  }
+  constexpr int kTail = (kNp - kTmaRows) * kTmaChunks * 8;
+#pragma unroll
+  for (int k = 0; k < kTail / kLdgThreads; ++k) {
+    const int q = lt + k * kLdgThreads;
+    const int rr = kTmaRows + q / (kTmaChunks * 8), w = q % (kTmaChunks * 8);
+    const int pr = max(rows[rr], 0);
+    cp_async_16(st_addr + (w >> 3) * kChunkBytes + sw128_offset(rr, w & 7),
+                latent + (int64_t)pr * DSI_D_QK + (g0 + (w >> 3)) * 64 + (w & 7) * 8);
+  }
+}
+static_assert(kNp * 8 % kLdgThreads == 0 && kNp * 4 % kLdgThreads == 0 &&
+              (kNp - kTmaRows) * kTmaChunks * 8 % kLdgThreads == 0, "whole rounds of pieces");
+
 __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float* v) {
   uint32_t r[32];
 #pragma unroll
@@ -125,8 +161,14 @@ __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float* v) {
 
 // FP8 latent rows: 16 codes a piece, 20 pieces of this CTA's 320 dims per
 // row, 1280 pieces a tile over the three producer warps.
-constexpr int kF8Pieces = kNp * kChunks * 64 / 16;
+constexpr int kF8RowPieces = (kQkTmem * 64 + kRopeHalf) / 16;   // 18 pieces of 16 codes a row
+constexpr int kF8Pieces = kNp * kF8RowPieces;
 constexpr int kF8PerThread = (kF8Pieces + kProducerWarps * 32 - 1) / (kProducerWarps * 32);
+// first latent dim of piece u of a row: the four 64-dim blocks, then the rope half
+__device__ __forceinline__ int f8_piece_dim(int u, uint32_t rho, int g0) {
+  return u < kQkTmem * 4 ? g0 * 64 + u * 16
+                         : DSI_D_LATENT + (int)rho * kRopeHalf + (u - kQkTmem * 4) * 16;
+}
 
 // 16 E4M3 codes times their tile scale, rounded to bf16 (lo = codes 0..7).
 __device__ __forceinline__ void fp8x16_scaled_bf16(const uint4& v, float sc, uint4& lo, uint4& hi) {
@@ -184,7 +226,6 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
   const int span = tiles_per * kNp;                // entries this split owns (<= kMaxEntries)
   const int32_t* irow = a.idx + (int64_t)r * a.K;
   const int g0 = rho ? 4 : 0;                      // first gathered 64-dim block
-  const int qk_first = rho ? 1 : 0;                // first stage block used by the logits
   // this CTA's slice of the head's query row is loaded first, so it lands
   // while the entries are being staged (and, launched behind the select
   // kernel, while that kernel finishes): the exchange warps take the first two
@@ -192,13 +233,15 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
   // dims 256..319 (eight 16-byte pieces a block)
   uint4 qv[24];
   if (warp >= kExWarp0) {
-    const int b0 = g0 + qk_first + (warp < kSmWarp0 ? 0 : 2);
-    const int nq = (warp < kSmWarp0 ? 2 : 3) * 8;
+    const int b0 = g0 + (warp < kSmWarp0 ? 0 : 2);
+    const int nq = warp < kSmWarp0 ? 16 : 16 + kRopeHalf / 8;
     const uint4* qrow = reinterpret_cast<const uint4*>(
         a.q + ((int64_t)r * kH + (warp & 3) * 32 + lane) * DSI_D_QK);
 #pragma unroll
     for (int i = 0; i < 24; ++i)
-      qv[i] = i < nq ? __ldg(qrow + (i < 16 ? b0 * 8 + i : 4 * 8 + (i - 16))) : make_uint4(0, 0, 0, 0);
+      qv[i] = i < nq ? __ldg(qrow + (i < 16 ? b0 * 8 + i
+                                            : (DSI_D_LATENT + (int)rho * kRopeHalf) / 8 + (i - 16)))
+                     : make_uint4(0, 0, 0, 0);
   }
 
   if (tid == 0) {
@@ -282,9 +325,9 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
       for (int k = 0; k < kF8PerThread; ++k) {
         const int q = tid + k * kProducerWarps * 32;
         if (q < kF8Pieces) {
-          const int rr = q / 20, u = q % 20;
+          const int rr = q / kF8RowPieces, u = q % kF8RowPieces;
           const int64_t pr = max(rows_s[t * kNp + rr], 0);
-          const int d0 = g0 * 64 + u * 16;             // first dim of the piece
+          const int d0 = f8_piece_dim(u, rho, g0);     // first dim of the piece
           cv[k] = __ldg(reinterpret_cast<const uint4*>(codes + pr * DSI_D_QK + d0));
           sc[k] = __ldg(lscale + pr * 5 + (d0 >> 7));
         }
@@ -300,7 +343,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
       for (int k = 0; k < kF8PerThread; ++k) {
         const int q = tid + k * kProducerWarps * 32;
         if (q < kF8Pieces) {
-          const int rr = q / 20, u = q % 20;
+          const int rr = q / kF8RowPieces, u = q % kF8RowPieces;
           uint4 lo, hi;
           fp8x16_scaled_bf16(cv[k], sc[k], lo, hi);
           uint8_t* blk = st_base + (u >> 2) * kChunkBytes;
@@ -308,7 +351,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
           *reinterpret_cast<uint4*>(blk + sw128_offset(rr, (u & 3) * 2 + 1)) = hi;
           if (t + 1 < n_tiles) {
             const int64_t pr = max(rows_s[(t + 1) * kNp + rr], 0);
-            const int d0 = g0 * 64 + u * 16;
+            const int d0 = f8_piece_dim(u, rho, g0);
             cv[k] = __ldg(reinterpret_cast<const uint4*>(codes + pr * DSI_D_QK + d0));
             sc[k] = __ldg(lscale + pr * 5 + (d0 >> 7));
           }
@@ -360,31 +403,17 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
     }
   } else if (!F8L && warp < kProducerWarps) {
     // ======================= gather: cp.async part ============================
-    // the remaining 64-dim blocks of every row (half a warp per row: 16 lanes
-    // x 16 bytes = two blocks) and the first blocks of the rows past kTmaRows,
-    // each piece to its swizzled place; each tile is signalled (after a proxy
-    // fence) once its copies have landed.  The split balances the two engines.
-    constexpr int kLdgPieces = (kChunks - kTmaChunks) * 8;   // 16-byte pieces per row
-    static_assert(kLdgPieces == 16, "half a warp per row");
-    const int sub = lane >> 4, pi = lane & 15;
-    const int ch = kTmaChunks + (pi >> 3), u = pi & 7;
+    // the fourth 64-dim block and the rope half of every row, and the first
+    // blocks of the rows past kTmaRows, each 16-byte piece to its swizzled
+    // place (consecutive lanes take consecutive pieces of a row); each tile is
+    // signalled (after a proxy fence) once its copies have landed.  The split
+    // balances the two engines.
     int stage = 0;
     uint32_t ph = 0;
     for (int t = 0; t < n_tiles; ++t) {
       if (!mbar_wait(&empty[stage], ph ^ 1, abort_flag, err)) break;
       const uint32_t st_addr = smem_u32(smem + OFF_C + stage * kStageBytes);
-      for (int rr = (warp - 1) * 2 + sub; rr < kNp; rr += 2 * kLdgWarps) {
-        const int pr = max(rows_s[t * kNp + rr], 0);
-        cp_async_16(st_addr + ch * kChunkBytes + sw128_offset(rr, u),
-                    c.latent + (int64_t)pr * DSI_D_QK + (g0 + ch) * 64 + u * 8);
-      }
-      constexpr int kTailPieces = (kNp - kTmaRows) * kTmaChunks * 8;
-      for (int q = (warp - 1) * 32 + lane; q < kTailPieces; q += kLdgThreads) {
-        const int rr = kTmaRows + q / (kTmaChunks * 8), w = q % (kTmaChunks * 8);
-        const int pr = max(rows_s[t * kNp + rr], 0);
-        cp_async_16(st_addr + (w >> 3) * kChunkBytes + sw128_offset(rr, w & 7),
-                    c.latent + (int64_t)pr * DSI_D_QK + (g0 + (w >> 3)) * 64 + (w & 7) * 8);
-      }
+      ldg_tile(st_addr, c.latent, rows_s + t * kNp, (warp - 1) * 32 + lane, rho, g0);
       // the stage's barrier counts this thread once its copies have landed;
       // the thread goes on to the next stage without waiting for them
       cp_async_mbar_arrive_noinc(&full[stage]);
@@ -428,20 +457,17 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
             fence_proxy_async_smem();
             const uint32_t t_s = tmem + TM_S;
             const uint32_t st_base = smem_u32(smem + OFF_C + st * kStageBytes);
-            const uint64_t d0 = desc_sw128(st_base + qk_first * kChunkBytes);
+            const uint64_t d0 = desc_sw128(st_base);
             for (int k = 0; k < kQkTmem * 4; ++k)
               mma_bf16_tmem_a(t_s, tmem + TM_Q + k * 8,
                               d0 + (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4),
                               IDESC_S, k > 0 ? 1u : 0u);
-            {   // dims 256..319: CTA 0 takes the first half (its stage block
-                // 4), CTA 1 the second (its block 0)
-              const uint64_t cd = desc_sw128(st_base + (rho ? 0 : kQkTmem) * kChunkBytes);
+            {   // this CTA's half of the rope dims, in the first half of stage block 4
+              const uint64_t cd = desc_sw128(st_base + kQkTmem * kChunkBytes);
 #pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const int kk = (int)rho * 2 + k;
+              for (int kk = 0; kk < kRopeHalf / 16; ++kk)
                 mma_bf16_tmem_a(t_s, tmem + TM_Q4 + kk * 8, cd + (uint64_t)((kk * 32) >> 4),
                                 IDESC_S, 1u);
-              }
             }
             mma_commit(&s_full[0]);
             ++qk_next;
@@ -760,7 +786,6 @@ mla_tc_rows(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, in
   const int tiles_all = (a.K + kNp - 1) / kNp;
   const int span = tiles_all * kNp;                // entries of a row (<= kPerEntries)
   const int g0 = rho ? 4 : 0;
-  const int qk_first = rho ? 1 : 0;
   constexpr uint32_t kXBytes = kH * kNp * 4;
 
   if (tid == 0) {
@@ -846,10 +871,6 @@ mla_tc_rows(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, in
     }
   } else if (warp < kProducerWarps) {
     // ======================= gather: cp.async part ============================
-    constexpr int kLdgPieces = (kChunks - kTmaChunks) * 8;
-    static_assert(kLdgPieces == 16, "half a warp per row");
-    const int sub = lane >> 4, pi = lane & 15;
-    const int ch = kTmaChunks + (pi >> 3), u = pi & 7;
     int stage = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -861,18 +882,7 @@ mla_tc_rows(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, in
       for (int t = 0; t < n; ++t) {
         if (!(ok = mbar_wait(&empty[stage], ph ^ 1, abort_flag, err))) break;
         const uint32_t st_addr = smem_u32(smem + OFF_C + stage * kStageBytes);
-        for (int rr = (warp - 1) * 2 + sub; rr < kNp; rr += 2 * kLdgWarps) {
-          const int pr = max(rs[t * kNp + rr], 0);
-          cp_async_16(st_addr + ch * kChunkBytes + sw128_offset(rr, u),
-                      c.latent + (int64_t)pr * DSI_D_QK + (g0 + ch) * 64 + u * 8);
-        }
-        constexpr int kTailPieces = (kNp - kTmaRows) * kTmaChunks * 8;
-        for (int q = (warp - 1) * 32 + lane; q < kTailPieces; q += kLdgThreads) {
-          const int rr = kTmaRows + q / (kTmaChunks * 8), w = q % (kTmaChunks * 8);
-          const int pr = max(rs[t * kNp + rr], 0);
-          cp_async_16(st_addr + (w >> 3) * kChunkBytes + sw128_offset(rr, w & 7),
-                      c.latent + (int64_t)pr * DSI_D_QK + (g0 + (w >> 3)) * 64 + (w & 7) * 8);
-        }
+        ldg_tile(st_addr, c.latent, rs + t * kNp, (warp - 1) * 32 + lane, rho, g0);
         cp_async_mbar_arrive_noinc(&full[stage]);
         if (++stage == kStages) { stage = 0; ph ^= 1; }
       }
@@ -954,19 +964,17 @@ mla_tc_rows(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, in
               fence_proxy_async_smem();
               const uint32_t t_s = tmem + TM_S;
               const uint32_t st_base = smem_u32(smem + OFF_C + st * kStageBytes);
-              const uint64_t d0 = desc_sw128(st_base + qk_first * kChunkBytes);
+              const uint64_t d0 = desc_sw128(st_base);
               for (int k = 0; k < kQkTmem * 4; ++k)
                 mma_bf16_tmem_a(t_s, tmem + TM_Q + k * 8,
                                 d0 + (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4),
                                 IDESC_S, k > 0 ? 1u : 0u);
               {
-                const uint64_t cd = desc_sw128(st_base + (rho ? 0 : kQkTmem) * kChunkBytes);
+                const uint64_t cd = desc_sw128(st_base + kQkTmem * kChunkBytes);
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                  const int kk = (int)rho * 2 + k;
+                for (int kk = 0; kk < kRopeHalf / 16; ++kk)
                   mma_bf16_tmem_a(t_s, tmem + TM_Q4 + kk * 8, cd + (uint64_t)((kk * 32) >> 4),
                                   IDESC_S, 1u);
-                }
               }
               mma_commit(&s_full[0]);
               ++qg;
@@ -1035,8 +1043,8 @@ mla_tc_rows(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, in
         const bf16* qn = a.q + ((int64_t)(r + nclu) * kH + h) * DSI_D_QK;
 #pragma unroll
         for (int k = 0; k < kQkTmem; ++k)
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + (g0 + qk_first + k) * 64));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + 4 * 64));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + (g0 + k) * 64));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + DSI_D_LATENT + (int)rho * kRopeHalf));
       }
       mbar_arrive(setup_bar);
       if (et == 0) {
@@ -1057,7 +1065,7 @@ mla_tc_rows(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, in
       for (int half = 0; half < 2; ++half) {
         uint4 qv[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) qv[k] = __ldg(qrow + (g0 + qk_first + half * 2) * 8 + k);
+        for (int k = 0; k < 16; ++k) qv[k] = __ldg(qrow + (g0 + half * 2) * 8 + k);
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) {
           uint32_t w32[32];
@@ -1073,7 +1081,9 @@ mla_tc_rows(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, in
         uint32_t w32[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint4 v = __ldg(qrow + 4 * 8 + k);
+          const uint4 v = k < kRopeHalf / 8
+                              ? __ldg(qrow + (DSI_D_LATENT + (int)rho * kRopeHalf) / 8 + k)
+                              : make_uint4(0, 0, 0, 0);
           w32[4 * k] = v.x; w32[4 * k + 1] = v.y; w32[4 * k + 2] = v.z; w32[4 * k + 3] = v.w;
         }
         tmem_st32(tmem + lane_base + TM_Q4, w32);
