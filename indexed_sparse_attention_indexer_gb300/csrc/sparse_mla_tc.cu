@@ -72,8 +72,13 @@ constexpr int kThreads = (kSmWarp0 + 4) * 32;  // 384
 // first kTmaChunks 64-dim blocks of the first kTmaRows rows, cp.async (warps
 // 1-2) for the rest.
 constexpr int kTmaChunks = 3;
-constexpr int kTmaRows = 48;                   // rows of those blocks by TMA; cp.async takes the rest
-static_assert(kTmaRows % 4 == 0 && kTmaRows <= kNp, "whole gather4 groups");
+// rows of those blocks by TMA (cp.async takes the rest): rows from HBM (one
+// cluster a row, the decode batches) gather faster with more of them on
+// cp.async, rows from L2 (the persistent prefill form) with more on TMA
+constexpr int kTmaRows = 40;
+constexpr int kTmaRowsP = 48;
+static_assert(kTmaRows % 4 == 0 && kTmaRows <= kNp && kTmaRowsP % 4 == 0 && kTmaRowsP <= kNp,
+              "whole gather4 groups");
 constexpr int kLdgWarps = kProducerWarps - 1;
 constexpr int kLdgThreads = kLdgWarps * 32;
 
@@ -123,8 +128,10 @@ __device__ __forceinline__ bool pos_ok(int pos, int64_t n_vis) {
 // of block 4) and the first kTmaChunks blocks of the rows past kTmaRows, each
 // 16-byte piece to its swizzled place (consecutive threads take consecutive
 // pieces of a row).  `rows` holds the tile's physical rows (-1: row 0).
+template <int TR>
 __device__ __forceinline__ void ldg_tile(uint32_t st_addr, const bf16* latent, const int32_t* rows,
                                          int lt, uint32_t rho, int g0) {
+  static_assert((kNp - TR) * kTmaChunks * 8 % kLdgThreads == 0, "whole rounds of pieces");
 #pragma unroll
   for (int k = 0; k < kNp * 8 / kLdgThreads; ++k) {
     const int q = lt + k * kLdgThreads, rr = q >> 3, u = q & 7;
@@ -139,18 +146,17 @@ __device__ __forceinline__ void ldg_tile(uint32_t st_addr, const bf16* latent, c
     cp_async_16(st_addr + kQkTmem * kChunkBytes + sw128_offset(rr, u),
                 latent + (int64_t)pr * DSI_D_QK + DSI_D_LATENT + (int)rho * kRopeHalf + u * 8);
   }
-  constexpr int kTail = (kNp - kTmaRows) * kTmaChunks * 8;
+  constexpr int kTail = (kNp - TR) * kTmaChunks * 8;
 #pragma unroll
   for (int k = 0; k < kTail / kLdgThreads; ++k) {
     const int q = lt + k * kLdgThreads;
-    const int rr = kTmaRows + q / (kTmaChunks * 8), w = q % (kTmaChunks * 8);
+    const int rr = TR + q / (kTmaChunks * 8), w = q % (kTmaChunks * 8);
     const int pr = max(rows[rr], 0);
     cp_async_16(st_addr + (w >> 3) * kChunkBytes + sw128_offset(rr, w & 7),
                 latent + (int64_t)pr * DSI_D_QK + (g0 + (w >> 3)) * 64 + (w & 7) * 8);
   }
 }
-static_assert(kNp * 8 % kLdgThreads == 0 && kNp * 4 % kLdgThreads == 0 &&
-              (kNp - kTmaRows) * kTmaChunks * 8 % kLdgThreads == 0, "whole rounds of pieces");
+static_assert(kNp * 8 % kLdgThreads == 0 && kNp * 4 % kLdgThreads == 0, "whole rounds of pieces");
 
 __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float* v) {
   uint32_t r[32];
@@ -413,7 +419,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
     for (int t = 0; t < n_tiles; ++t) {
       if (!mbar_wait(&empty[stage], ph ^ 1, abort_flag, err)) break;
       const uint32_t st_addr = smem_u32(smem + OFF_C + stage * kStageBytes);
-      ldg_tile(st_addr, c.latent, rows_s + t * kNp, (warp - 1) * 32 + lane, rho, g0);
+      ldg_tile<kTmaRows>(st_addr, c.latent, rows_s + t * kNp, (warp - 1) * 32 + lane, rho, g0);
       // the stage's barrier counts this thread once its copies have landed;
       // the thread goes on to the next stage without waiting for them
       cp_async_mbar_arrive_noinc(&full[stage]);
@@ -826,13 +832,13 @@ mla_tc_rows(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, in
 
   if (warp == 0) {
     // ======================= gather: TMA part =================================
-    if (lane < kTmaRows / 4) {
+    if (lane < kTmaRowsP / 4) {
       if (lane == 0) prefetch_tmap(&lmap);
       int stage = 0;
       uint32_t ph = 0;
       bool issued[kStages] = {};
       uint32_t issued_ph[kStages] = {};
-      const unsigned gmask = (1u << (kTmaRows / 4)) - 1u;
+      const unsigned gmask = (1u << (kTmaRowsP / 4)) - 1u;
       bool ok = true;
       for (int i = 0; ok && i < items; ++i) {
         const int bsel = i & 1;
@@ -844,7 +850,7 @@ mla_tc_rows(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, in
         for (int t = 0; t < n; ++t) {
           if (lane == 0) {
             ok = mbar_wait(&empty[stage], ph ^ 1, abort_flag, err);
-            if (ok) mbar_arrive_expect_tx(&full[stage], kTmaChunks * kTmaRows * 128);
+            if (ok) mbar_arrive_expect_tx(&full[stage], kTmaChunks * kTmaRowsP * 128);
           }
           ok = __shfl_sync(gmask, ok, 0);
           if (!ok) break;
@@ -882,7 +888,7 @@ mla_tc_rows(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, in
       for (int t = 0; t < n; ++t) {
         if (!(ok = mbar_wait(&empty[stage], ph ^ 1, abort_flag, err))) break;
         const uint32_t st_addr = smem_u32(smem + OFF_C + stage * kStageBytes);
-        ldg_tile(st_addr, c.latent, rs + t * kNp, (warp - 1) * 32 + lane, rho, g0);
+        ldg_tile<kTmaRowsP>(st_addr, c.latent, rs + t * kNp, (warp - 1) * 32 + lane, rho, g0);
         cp_async_mbar_arrive_noinc(&full[stage]);
         if (++stage == kStages) { stage = 0; ph ^= 1; }
       }
