@@ -51,11 +51,11 @@ namespace {
 
 constexpr int kH = 128;                        // heads (MMA M)
 constexpr int kNp = 64;                        // positions per tile (MMA N of the logits)
-constexpr int kChunks = 5;                     // 64-dim blocks each CTA gathers per row
+constexpr int kChunks = 5;                     // stage blocks per row: four 64-dim blocks and the rope half
 // Four stages: the logit tile and the P tile are single (their next use waits
-// only for the readers of the previous one), and the query block of dims
-// 256..319 sits in the TMEM columns the second logit tile would take, which
-// leaves the shared memory for a fourth 40 KB stage of gathered rows.
+// only for the readers of the previous one), and the query's rope half sits
+// in the TMEM columns the second logit tile would take, which leaves the
+// shared memory for a fourth 40 KB stage of gathered rows.
 constexpr int kStages = 4;
 constexpr int kXBufs = 1;                      // exchange buffers for the peer's partial logits
 constexpr int kQkTmem = 4;                     // query blocks of the main logit MMAs (the rope half apart)
@@ -95,7 +95,7 @@ constexpr int SMEM = OFF_MISC + 64 + 1024;
 static_assert(SMEM <= 227 * 1024, "shared memory");
 
 constexpr uint32_t TM_S = 0;      // logits, 64 columns
-constexpr uint32_t TM_Q4 = 64;    // query dims 256..319, 32 columns
+constexpr uint32_t TM_Q4 = 64;    // the query's rope half (16 of 32 columns used)
 constexpr uint32_t TM_Q = 128;    // query slice: four 64-dim blocks, 128 columns
 constexpr uint32_t TM_O = 256;    // output half, 256 columns
 constexpr uint32_t TMEM_COLS = 512;
@@ -165,8 +165,8 @@ __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float* v) {
   tmem_st32(taddr, r);
 }
 
-// FP8 latent rows: 16 codes a piece, 20 pieces of this CTA's 320 dims per
-// row, 1280 pieces a tile over the three producer warps.
+// FP8 latent rows: 16 codes a piece, 18 pieces of this CTA's 288 dims per
+// row, 1152 pieces a tile over the three producer warps.
 constexpr int kF8RowPieces = (kQkTmem * 64 + kRopeHalf) / 16;   // 18 pieces of 16 codes a row
 constexpr int kF8Pieces = kNp * kF8RowPieces;
 constexpr int kF8PerThread = (kF8Pieces + kProducerWarps * 32 - 1) / (kProducerWarps * 32);
@@ -235,8 +235,8 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
   // this CTA's slice of the head's query row is loaded first, so it lands
   // while the entries are being staged (and, launched behind the select
   // kernel, while that kernel finishes): the exchange warps take the first two
-  // of its four main blocks, the softmax warps the other two and the block of
-  // dims 256..319 (eight 16-byte pieces a block)
+  // of its four main blocks, the softmax warps the other two and the rope half
+  // (eight 16-byte pieces a block, four for the rope half)
   uint4 qv[24];
   if (warp >= kExWarp0) {
     const int b0 = g0 + (warp < kSmWarp0 ? 0 : 2);
@@ -547,7 +547,7 @@ mla_tc(const __grid_constant__ CUtensorMap lmap, CacheView c, const float* lscal
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;               // head = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    // query blocks 2-3 and dims 256..319 into TMEM
+    // query blocks 2-3 and the rope half into TMEM
     {
 #pragma unroll
       for (int ch = 2; ch < kQkTmem; ++ch) {
@@ -1063,8 +1063,8 @@ mla_tc_rows(const __grid_constant__ CUtensorMap lmap, CacheView c, MlaArgs a, in
       mbar_arrive(&rows_ready[bsel]);
       return true;
     };
-    // this row's query slice (four 64-dim blocks and the block of dims
-    // 256..319) into TMEM, eight 16-byte pieces a block
+    // this row's query slice (four 64-dim blocks and the rope half) into
+    // TMEM, eight 16-byte pieces a block
     auto load_q = [&](int r) {
       const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)r * kH + h) * DSI_D_QK);
 #pragma unroll
